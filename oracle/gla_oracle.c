@@ -1,0 +1,208 @@
+/*
+ * fp64 CPU oracle for the forward pass of causal gated linear attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path links, loads or calls
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do. It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes is the plain definition, the gated recurrence
+ *     S_t = Diag(alpha_t) S_{t-1} + k_t^T v_t,      o_t = q_t S_t,
+ * ("Gated Linear Attention Transformers with Hardware-Efficient Training",
+ * §4.1 Eq. 3; the ungated case alpha = 1 is §2.1 Eq. 1; the fixed per-head
+ * decay alpha = lambda_h is the recurrence "Lightning Attention-2" §3.2.1
+ * starts from). S_0 is zero or a caller-given state carried from a previous
+ * segment (same GLA paper, §2.2, below Eq. 2). The chunkwise method of
+ * §4.2-4.3 reaches exactly this result (up to rounding order), so the
+ * oracle is the token-by-token recurrence itself, one token at a time, with
+ * no chunking, blocking or reordering.
+ *
+ * Gate modes (alpha_t in (0,1]^dk is given as log alpha_t):
+ *   0  alpha_t = 1                         (log_g unused)
+ *   1  alpha_t = exp(log_g[h]) for all t,k (log_g is [H])
+ *   2  alpha_t = exp(log_g[b,h,t,:])       (log_g is [B,H,T,dk])
+ *
+ * Layouts (row-major, contiguous): q [B,H,T,dk], k [B,H,T,dk], v [B,H,T,dv],
+ * O [B,H,T,dv], S0 and ST [B,H,dk,dv]. S0 may be NULL (zero state); ST may be
+ * NULL (not written).
+ *
+ * Parallelism: the columns j of S evolve independently (the gate scales the
+ * rows i of S only), so work is split over (b, h, column block) with POSIX
+ * threads. The arithmetic per column is unchanged by the split.
+ *
+ * "mutant" plants one deliberate mistake so that the tests can show the
+ * pins catch it. It is 0 everywhere except in those tests:
+ *   1  decay applied after the update:  S_t = Diag(a_t)(S_{t-1} + k^T v)
+ *   2  output read before the update:    o_t = q_t S_{t-1}
+ *   3  gate applied to the columns j instead of the rows i (needs dk == dv)
+ *   4  gate taken one step late:          alpha_{t-1} used at step t
+ *   5  S_0 ignored
+ *   6  q and k exchanged
+ *   7  diagonal (current-token) term dropped from the output
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    const double *q, *k, *v, *log_g, *S0;
+    double *O, *ST;
+    long B, H, T, dk, dv;
+    int gate, mutant;
+    long j0, j1; /* column block [j0, j1) */
+    long bh;     /* flattened (b, h) */
+    int status;
+} job_t;
+
+static double gate_alpha(const job_t* J, long t, long i)
+{
+    if (J->gate == 0) return 1.0;
+    if (J->gate == 1) return exp(J->log_g[J->bh % J->H]);
+    return exp(J->log_g[(J->bh * J->T + t) * J->dk + i]);
+}
+
+static void run_job(job_t* J)
+{
+    const long dk = J->dk, dv = J->dv, T = J->T, w = J->j1 - J->j0;
+    double* S = (double*)calloc((size_t)(dk * w), sizeof(double));
+    double* Sprev = (J->mutant == 2 || J->mutant == 7) ? (double*)calloc((size_t)(dk * w), sizeof(double)) : NULL;
+    double* alpha = (double*)malloc((size_t)dk * sizeof(double));
+    if (!S || !alpha || ((J->mutant == 2 || J->mutant == 7) && !Sprev)) {
+        J->status = 1;
+        free(S); free(Sprev); free(alpha);
+        return;
+    }
+    const double* q = J->q + J->bh * T * dk;
+    const double* k = J->k + J->bh * T * dk;
+    const double* v = J->v + J->bh * T * dv;
+    double* O = J->O + J->bh * T * dv;
+    if (J->mutant == 6) { const double* tmp = q; q = k; k = tmp; }
+
+    /* S <- S_0 (or zero) */
+    if (J->S0 && J->mutant != 5) {
+        const double* s0 = J->S0 + J->bh * dk * dv;
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < w; ++j) S[i * w + j] = s0[i * dv + J->j0 + j];
+    }
+
+    for (long t = 0; t < T; ++t) {
+        /* alpha_t (one value per row i of S) */
+        long tg = (J->mutant == 4) ? (t > 0 ? t - 1 : 0) : t;
+        for (long i = 0; i < dk; ++i) alpha[i] = gate_alpha(J, tg, i);
+        if (J->mutant == 4 && t == 0)
+            for (long i = 0; i < dk; ++i) alpha[i] = 1.0;
+        if (Sprev) memcpy(Sprev, S, (size_t)(dk * w) * sizeof(double));
+
+        const double* kt = k + t * dk;
+        const double* vt = v + t * dv + J->j0;
+        const double* qt = q + t * dk;
+        double* ot = O + t * dv + J->j0;
+        for (long j = 0; j < w; ++j) ot[j] = 0.0;
+
+        for (long i = 0; i < dk; ++i) {
+            double* Si = S + i * w;
+            const double a = alpha[i], ki = kt[i], qi = qt[i];
+            if (J->mutant == 1) {
+                for (long j = 0; j < w; ++j) Si[j] = a * (Si[j] + ki * vt[j]);
+            } else if (J->mutant == 3) {
+                /* gate indexed by the column instead of the row */
+                for (long j = 0; j < w; ++j) Si[j] = alpha[J->j0 + j] * Si[j] + ki * vt[j];
+            } else {
+                /* Eq. 3: S_t[i][j] = alpha_t[i] * S_{t-1}[i][j] + k_t[i] * v_t[j] */
+                for (long j = 0; j < w; ++j) Si[j] = a * Si[j] + ki * vt[j];
+            }
+            if (J->mutant == 2) {
+                const double* Pi = Sprev + i * w;
+                for (long j = 0; j < w; ++j) ot[j] += qi * Pi[j];
+            } else if (J->mutant == 7) {
+                /* q_t (Diag(alpha_t) S_{t-1}): the k_t^T v_t term left out */
+                const double* Pi = Sprev + i * w;
+                for (long j = 0; j < w; ++j) ot[j] += qi * a * Pi[j];
+            } else {
+                /* o_t[j] = sum_i q_t[i] * S_t[i][j] */
+                for (long j = 0; j < w; ++j) ot[j] += qi * Si[j];
+            }
+        }
+    }
+
+    if (J->ST) {
+        double* st = J->ST + J->bh * dk * dv;
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < w; ++j) st[i * dv + J->j0 + j] = S[i * w + j];
+    }
+    free(S); free(Sprev); free(alpha);
+}
+
+typedef struct {
+    job_t* jobs;
+    long njobs;
+    long next;
+    pthread_mutex_t mu;
+} pool_t;
+
+static void* worker(void* arg)
+{
+    pool_t* P = (pool_t*)arg;
+    for (;;) {
+        pthread_mutex_lock(&P->mu);
+        long idx = P->next++;
+        pthread_mutex_unlock(&P->mu);
+        if (idx >= P->njobs) break;
+        run_job(&P->jobs[idx]);
+    }
+    return NULL;
+}
+
+/* Returns 0 on success, 1 on bad arguments, 2 on allocation failure. */
+int gla_oracle_fwd(const double* q, const double* k, const double* v,
+                   const double* log_g, int gate, const double* S0,
+                   double* O, double* ST,
+                   long B, long H, long T, long dk, long dv,
+                   int nthreads, int mutant)
+{
+    if (!q || !k || !v || !O || B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
+    if (gate < 0 || gate > 2 || (gate != 0 && !log_g)) return 1;
+    if (mutant == 3 && dk != dv) return 1;
+    if (T == 0) {
+        if (ST) {
+            for (long i = 0; i < B * H * dk * dv; ++i) ST[i] = (S0 && mutant != 5) ? S0[i] : 0.0;
+        }
+        return 0;
+    }
+    /* Column blocks: small enough to spread over threads, large enough to
+       keep the inner loops long. Mutant 3 reads alpha by absolute column, so
+       it uses one block. */
+    long jb = (mutant == 3) ? dv : (dv >= 64 ? 64 : dv);
+    long nblk = (dv + jb - 1) / jb;
+    long njobs = B * H * nblk;
+    job_t* jobs = (job_t*)calloc((size_t)njobs, sizeof(job_t));
+    if (!jobs) return 2;
+    for (long bh = 0; bh < B * H; ++bh)
+        for (long c = 0; c < nblk; ++c) {
+            job_t* J = &jobs[bh * nblk + c];
+            J->q = q; J->k = k; J->v = v; J->log_g = log_g; J->S0 = S0;
+            J->O = O; J->ST = ST;
+            J->B = B; J->H = H; J->T = T; J->dk = dk; J->dv = dv;
+            J->gate = gate; J->mutant = mutant;
+            J->bh = bh; J->j0 = c * jb; J->j1 = (c + 1) * jb < dv ? (c + 1) * jb : dv;
+        }
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > njobs) nthreads = (int)njobs;
+    pool_t P;
+    P.jobs = jobs; P.njobs = njobs; P.next = 0;
+    pthread_mutex_init(&P.mu, NULL);
+    pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
+    int started = 0;
+    if (th) {
+        for (int i = 0; i + 1 < nthreads; ++i)
+            if (pthread_create(&th[started], NULL, worker, &P) == 0) ++started;
+    }
+    worker(&P); /* the calling thread works too */
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&P.mu);
+    int st = 0;
+    for (long i = 0; i < njobs; ++i) if (jobs[i].status) st = 2;
+    free(jobs);
+    return st;
+}

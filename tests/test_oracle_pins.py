@@ -1,0 +1,336 @@
+"""Pins for the fp64 oracle: it is checked against forms and facts the pages
+and the mathematics fix, none of which is the recurrence retyped.
+
+Sources (page title, section):
+  [GLA]   "Gated Linear Attention Transformers with Hardware-Efficient Training"
+          (arXiv 2312.06635): §2.1 Eq. 1 and the masked parallel form,
+          §2.2 Eq. 2 (chunkwise form, "C = L recovers the parallel form and
+          C = 1 the recurrent form"), §4.1 Eq. 3 / parallel form / Eq. 4
+          (log-space pairwise form), §4.2 (chunkwise GLA: Lambda, Gamma, gamma).
+  [LA2]   "Lightning Attention-2: A Free Lunch for Handling Unlimited Sequence
+          Lengths in Large Language Models", §3.2.1 Alg. 1 (decay mask
+          M_ij = lambda^(i-j) for i >= j).
+All of these run on the CPU.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunkwise_gated_linear_gla_gb300 import inputs as gi
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _case(B=1, H=2, T=37, dk=8, dv=6, gate=gi.GATE_PER_KEY, dist="logsigmoid16",
+          s0=0.5, seed=1, dtype=torch.float32):
+    w = gi.Workload("pin", B=B, H=H, T=T, dk=dk, dv=dv, dtype=dtype, gate=gate,
+                    s0_std=s0, gate_dist=dist)
+    x = gi.make_inputs(w, seed=seed)
+    f = lambda t: None if t is None else t.to(torch.float64).numpy()
+    return f(x["q"]), f(x["k"]), f(x["v"]), f(x["log_g"]), x["gate"], f(x["S0"])
+
+
+def _logb(log_g, gate, B, H, T, dk):
+    """Inclusive cumulative log-decay log b_t = sum_{j<=t} log alpha_j, [B,H,T,dk]."""
+    if gate == gi.GATE_NONE:
+        return np.zeros((B, H, T, dk))
+    if gate == gi.GATE_HEAD_SCALAR:
+        steps = np.arange(1, T + 1, dtype=np.float64)
+        return np.broadcast_to(log_g[None, :, None, None] * steps[None, None, :, None], (B, H, T, dk)).copy()
+    return np.cumsum(log_g, axis=2)
+
+
+def _gate_log(log_g, gate, B, H, T, dk):
+    if gate == gi.GATE_NONE:
+        return np.zeros((B, H, T, dk))
+    if gate == gi.GATE_HEAD_SCALAR:
+        return np.broadcast_to(log_g[None, :, None, None], (B, H, T, dk)).copy()
+    return log_g
+
+
+# ---------------------------------------------------------------- golden
+
+def _read_golden(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(None, 1)
+            rows[key] = np.array([[float(x) for x in part.split()] for part in rest.split("|")])
+    return rows
+
+
+def test_golden_hand_worked_example():
+    g = _read_golden("gla_hand_t3.txt")
+    q, k, v = (g[n][None, None] for n in ("q", "k", "v"))
+    log_g = np.log(g["alpha"])[None, None]
+    S0 = g["S0"][None, None]
+    O, ST = oracle.gla_forward(q, k, v, log_g, oracle.GATE_PER_KEY, S0)
+    np.testing.assert_allclose(O[0, 0], g["O"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(ST[0, 0], g["ST"], rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute_force(q, k, v, log_g, gate, S0):
+    """Unrolled Eq. 3: S_t = sum_i (prod_{j=i+1..t} alpha_j)^T 1 (.) k_i^T v_i (+ prod_{j<=t} alpha_j (.) S0).
+
+    Products of alpha are formed explicitly, one factor at a time.
+    """
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    glog = _gate_log(log_g, gate, B, H, T, dk)
+    alpha = np.exp(glog)
+    O = np.zeros((B, H, T, dv))
+    ST = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                S = np.zeros((dk, dv))
+                for i in range(t + 1):
+                    p = np.ones(dk)
+                    for j in range(i + 1, t + 1):
+                        p = p * alpha[b, h, j]
+                    S += p[:, None] * np.outer(k[b, h, i], v[b, h, i])
+                if S0 is not None:
+                    p = np.ones(dk)
+                    for j in range(0, t + 1):
+                        p = p * alpha[b, h, j]
+                    S += p[:, None] * S0[b, h]
+                O[b, h, t] = q[b, h, t] @ S
+                if t == T - 1:
+                    ST[b, h] = S
+    return O, ST
+
+
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+def test_brute_force_tiny(gate):
+    q, k, v, g, gate, S0 = _case(B=2, H=2, T=6, dk=3, dv=4, gate=gate, s0=0.7, seed=3)
+    O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
+    Ob, STb = _brute_force(q, k, v, g, gate, S0)
+    np.testing.assert_allclose(O, Ob, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(ST, STb, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- quadratic forms
+
+def _quadratic_logspace(q, k, v, log_g, gate, S0):
+    """[GLA] §4.1 Eq. 4: P_ij = sum_k Q_ik K_jk exp(logB_ik - logB_jk) for i >= j, O = (P (.) M) V.
+
+    The S0 contribution follows from the same unrolling: o_t gains (q_t (.) b_t) S0,
+    and S_T = sum_i (b_T / b_i)^T 1 (.) k_i^T v_i + (b_T^T 1) (.) S0.
+    """
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    lb = _logb(log_g, gate, B, H, T, dk)
+    O = np.zeros((B, H, T, dv))
+    ST = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            L = lb[b, h]
+            D = L[:, None, :] - L[None, :, :]               # [i, j, k] = logB_ik - logB_jk
+            mask = np.tril(np.ones((T, T), dtype=bool))       # M_ij = 1 iff i >= j
+            E = np.where(mask[:, :, None], np.exp(np.where(mask[:, :, None], D, 0.0)), 0.0)
+            P = np.einsum("ik,jk,ijk->ij", q[b, h], k[b, h], E)
+            O[b, h] = P @ v[b, h]
+            if S0 is not None:
+                O[b, h] += (q[b, h] * np.exp(L)) @ S0[b, h]
+            w = np.exp(L[-1][None, :] - L)                   # (b_T / b_i), [T, dk]
+            ST[b, h] = (k[b, h] * w).T @ v[b, h]
+            if S0 is not None:
+                ST[b, h] += np.exp(L[-1])[:, None] * S0[b, h]
+    return O, ST
+
+
+def _parallel_direct(q, k, v, log_g, gate, S0):
+    """[GLA] §4.1 parallel form O = (((Q (.) B)(K / B)^T) (.) M) V, b_t = prod_{j<=t} alpha_j.
+
+    Numerically usable only while b_t stays far from underflow (tiny T, mild gates).
+    """
+    B_, H, T, dk = q.shape
+    lb = _logb(log_g, gate, B_, H, T, dk)
+    Bm = np.exp(lb)
+    O = np.zeros(v.shape[:-1] + (v.shape[-1],))
+    for b in range(B_):
+        for h in range(H):
+            P = (q[b, h] * Bm[b, h]) @ (k[b, h] / Bm[b, h]).T
+            O[b, h] = np.tril(P) @ v[b, h]
+            if S0 is not None:
+                O[b, h] += (q[b, h] * Bm[b, h]) @ S0[b, h]
+    return O
+
+
+@pytest.mark.parametrize("gate,dist", [(gi.GATE_NONE, "logsigmoid16"),
+                                       (gi.GATE_HEAD_SCALAR, "logsigmoid16"),
+                                       (gi.GATE_PER_KEY, "logsigmoid16"),
+                                       (gi.GATE_PER_KEY, "steep")])
+def test_quadratic_logspace_form(gate, dist):
+    q, k, v, g, gate, S0 = _case(B=1, H=3, T=96, dk=8, dv=5, gate=gate, dist=dist, s0=0.3, seed=5)
+    O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
+    Oq, STq = _quadratic_logspace(q, k, v, g, gate, S0)
+    scale = np.abs(Oq).max()
+    np.testing.assert_allclose(O, Oq, rtol=0, atol=1e-12 * scale)
+    np.testing.assert_allclose(ST, STq, rtol=0, atol=1e-12 * np.abs(STq).max())
+
+
+def test_parallel_direct_form_tiny():
+    q, k, v, g, gate, S0 = _case(B=2, H=1, T=24, dk=6, dv=7, s0=0.2, seed=7)
+    O, _ = oracle.gla_forward(q, k, v, g, gate, S0)
+    Op = _parallel_direct(q, k, v, g, gate, S0)
+    np.testing.assert_allclose(O, Op, rtol=0, atol=1e-12 * np.abs(Op).max())
+
+
+def test_ungated_is_causal_linear_attention():
+    """[GLA] §2.1: alpha = 1 gives O = ((Q K^T) (.) M) V with M_ij = 1 iff i >= j."""
+    q, k, v, _, _, _ = _case(B=2, H=2, T=70, dk=16, dv=9, gate=gi.GATE_NONE, s0=0.0, seed=9)
+    O, ST = oracle.gla_forward(q, k, v, None, oracle.GATE_NONE, None)
+    Ol = np.tril(q @ np.swapaxes(k, -1, -2)) @ v
+    np.testing.assert_allclose(O, Ol, rtol=0, atol=1e-13 * np.abs(Ol).max())
+    np.testing.assert_allclose(ST, np.swapaxes(k, -1, -2) @ v, rtol=0, atol=1e-12)
+
+
+def test_scalar_decay_closed_form():
+    """[LA2] §3.2.1: o_t = sum_{i<=t} lambda^(t-i) (q_t . k_i) v_i, plus lambda^t-weighted S0 term."""
+    q, k, v, g, gate, S0 = _case(B=1, H=4, T=50, dk=5, dv=3, gate=gi.GATE_HEAD_SCALAR, s0=0.4, seed=11)
+    O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
+    T = q.shape[2]
+    for h in range(4):
+        lam = math.exp(g[h])
+        i = np.arange(T)
+        M = np.where(i[:, None] >= i[None, :], lam ** (i[:, None] - i[None, :]).clip(min=0), 0.0)
+        ref = ((q[0, h] @ k[0, h].T) * M) @ v[0, h]
+        ref += (lam ** (i + 1))[:, None] * (q[0, h] @ S0[0, h])
+        np.testing.assert_allclose(O[0, h], ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+        st = sum(lam ** (T - 1 - j) * np.outer(k[0, h, j], v[0, h, j]) for j in range(T)) + lam ** T * S0[0, h]
+        np.testing.assert_allclose(ST[0, h], st, rtol=0, atol=1e-12 * np.abs(st).max())
+
+
+# ---------------------------------------------------------------- chunkwise form
+
+def _chunked(q, k, v, log_g, gate, S0, C):
+    """[GLA] §4.2 chunkwise form, in fp64, for any chunk size C (last chunk may be short).
+
+    Lambda = b_{iC+j}/b_{iC}, Gamma = b_{(i+1)C}/b_{iC+j}, gamma = b_{(i+1)C}/b_{iC};
+    S_[i+1] = (gamma^T 1) (.) S_[i] + (K (.) Gamma)^T V;
+    O = (Q (.) Lambda) S_[i] + (((Q (.) Lambda)(K / Lambda)^T) (.) M) V.
+    Ratios are taken as exp of differences of the cumulative log-decay.
+    """
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    lb = _logb(log_g, gate, B, H, T, dk)
+    O = np.zeros((B, H, T, dv))
+    ST = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((dk, dv)) if S0 is None else S0[b, h].copy()
+            for s in range(0, T, C):
+                e = min(s + C, T)
+                base = lb[b, h, s - 1] if s > 0 else np.zeros(dk)
+                L = lb[b, h, s:e] - base             # log Lambda, rows of this chunk
+                Lend = lb[b, h, e - 1] - base         # log gamma
+                Qc, Kc, Vc = q[b, h, s:e], k[b, h, s:e], v[b, h, s:e]
+                Lam = np.exp(L)
+                Gam = np.exp(Lend[None, :] - L)
+                O[b, h, s:e] = (Qc * Lam) @ S + np.tril((Qc * Lam) @ (Kc / Lam).T) @ Vc
+                S = np.exp(Lend)[:, None] * S + (Kc * Gam).T @ Vc
+            ST[b, h] = S
+    return O, ST
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 7, 16, 64, 100])
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+def test_chunk_size_invariance(C, gate):
+    """[GLA] §2.2 / §4.2: the chunkwise form equals the recurrence for every C (C=1 and C=T are its limits)."""
+    q, k, v, g, gate, S0 = _case(B=1, H=2, T=100, dk=8, dv=6, gate=gate, s0=0.5, seed=13)
+    O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
+    Oc, STc = _chunked(q, k, v, g, gate, S0, C)
+    np.testing.assert_allclose(O, Oc, rtol=0, atol=1e-12 * np.abs(Oc).max())
+    np.testing.assert_allclose(ST, STc, rtol=0, atol=1e-12 * np.abs(STc).max())
+
+
+# ---------------------------------------------------------------- invariants and limits
+
+def test_steep_gate_limit():
+    """Eq. 3 with log alpha = -60 everywhere: S_t = k_t^T v_t + O(e^-60), so o_t = (q_t . k_t) v_t."""
+    q, k, v, _, _, _ = _case(B=1, H=2, T=40, dk=8, dv=5, s0=0.0, seed=17)
+    g = np.full(q.shape, -60.0)
+    O, ST = oracle.gla_forward(q, k, v, g, oracle.GATE_PER_KEY, None)
+    ref = np.sum(q * k, axis=-1, keepdims=True) * v
+    # e^-60 ~ 9e-27: far below rounding of the dot product itself
+    np.testing.assert_allclose(O, ref, rtol=0, atol=1e-14 * np.abs(ref).max())
+    np.testing.assert_allclose(ST, np.einsum("bhk,bhv->bhkv", k[:, :, -1], v[:, :, -1]), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+def test_initial_state_linearity(gate):
+    """O(S0) - O(0) = (Q (.) B) S0 and S_T(S0) - S_T(0) = Diag(b_T) S0."""
+    q, k, v, g, gate, S0 = _case(B=2, H=2, T=45, dk=7, dv=4, gate=gate, s0=1.0, seed=19)
+    O1, ST1 = oracle.gla_forward(q, k, v, g, gate, S0)
+    O0, ST0 = oracle.gla_forward(q, k, v, g, gate, None)
+    lb = _logb(g, gate, *q.shape)
+    np.testing.assert_allclose(O1 - O0, np.einsum("bhtk,bhkv->bhtv", q * np.exp(lb), S0), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ST1 - ST0, np.exp(lb[:, :, -1])[..., None] * S0, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("T1", [1, 17, 64])
+def test_segment_composition(T1):
+    """[GLA] §2.2: S_[0] may come from the previous segment; running T1 steps and then
+    the rest from S_T1 equals one run over all T steps."""
+    q, k, v, g, gate, S0 = _case(B=1, H=2, T=90, dk=6, dv=5, s0=0.3, seed=23)
+    O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
+    Oa, STa = oracle.gla_forward(q[:, :, :T1], k[:, :, :T1], v[:, :, :T1], g[:, :, :T1], gate, S0)
+    Ob, STb = oracle.gla_forward(q[:, :, T1:], k[:, :, T1:], v[:, :, T1:], g[:, :, T1:], gate, STa)
+    np.testing.assert_allclose(np.concatenate([Oa, Ob], axis=2), O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(STb, ST, rtol=0, atol=1e-12)
+
+
+def test_linearity_in_v_and_column_subsets():
+    q, k, v, g, gate, _ = _case(B=1, H=1, T=33, dk=5, dv=8, s0=0.0, seed=29)
+    O, _ = oracle.gla_forward(q, k, v, g, gate, None)
+    O2, _ = oracle.gla_forward(q, k, 2.0 * v, g, gate, None)
+    np.testing.assert_allclose(O2, 2.0 * O, rtol=1e-14, atol=1e-14)
+    cols = [6, 1, 3]
+    Os, _ = oracle.gla_forward(q, k, v[..., cols], g, gate, None)
+    np.testing.assert_allclose(Os, O[..., cols], rtol=0, atol=1e-14)
+
+
+def test_empty_sequence_returns_initial_state():
+    q = np.zeros((1, 2, 0, 4)); v = np.zeros((1, 2, 0, 3))
+    S0 = np.arange(24, dtype=np.float64).reshape(1, 2, 4, 3)
+    O, ST = oracle.gla_forward(q, q, v, np.zeros((1, 2, 0, 4)), oracle.GATE_PER_KEY, S0)
+    assert O.shape == (1, 2, 0, 3)
+    np.testing.assert_array_equal(ST, S0)
+
+
+def test_threads_do_not_change_result():
+    q, k, v, g, gate, S0 = _case(B=2, H=2, T=64, dk=8, dv=130, s0=0.2, seed=31)
+    O1, ST1 = oracle.gla_forward(q, k, v, g, gate, S0, nthreads=1)
+    O8, ST8 = oracle.gla_forward(q, k, v, g, gate, S0, nthreads=8)
+    np.testing.assert_array_equal(O1, O8)
+    np.testing.assert_array_equal(ST1, ST8)
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7])
+def test_pins_catch_planted_mistakes(mutant):
+    """Each deliberate mistake planted in the oracle must fail at least one pin."""
+    q, k, v, g, gate, S0 = _case(B=1, H=2, T=40, dk=6, dv=6, s0=0.5, seed=37)
+    O, ST = oracle.gla_forward(q, k, v, g, gate, S0, mutant=mutant)
+    Oq, STq = _quadratic_logspace(q, k, v, g, gate, S0)
+    Oc, STc = _chunked(q, k, v, g, gate, S0, 16)
+    err = max(np.abs(O - Oq).max(), np.abs(ST - STq).max(), np.abs(O - Oc).max())
+    assert err > 1e-6, f"mutant {mutant} not caught (err {err})"
+    # the golden example catches the mutants that touch the gate, S0 or the output order
+    gd = _read_golden("gla_hand_t3.txt")
+    if mutant != 3:
+        Og, STg = oracle.gla_forward(gd["q"][None, None], gd["k"][None, None], gd["v"][None, None],
+                                     np.log(gd["alpha"])[None, None], oracle.GATE_PER_KEY,
+                                     gd["S0"][None, None], mutant=mutant)
+        assert max(np.abs(Og[0, 0] - gd["O"]).max(), np.abs(STg[0, 0] - gd["ST"]).max()) > 1e-6
