@@ -1,0 +1,216 @@
+"""Thin ctypes binding over libgla.so, with the C ABI's names.
+
+Argument marshalling only: tensors become device pointers, results are
+returned as status codes (or raised as GlaError). Every step of the forward
+pass runs in the library's CUDA kernels; there is no fallback of any kind,
+and a missing or unloadable library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_CUDA, GLA_ERR_WORKSPACE, GLA_ERR_TIMEOUT = range(6)
+GLA_BF16, GLA_FP32 = 0, 1
+GLA_GATE_NONE, GLA_GATE_HEAD_SCALAR, GLA_GATE_PER_KEY = 0, 1, 2
+GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT = 0, 1, 2
+
+# Every symbol include/gla.h declares.
+EXPORTED = ("gla_fwd", "gla_fwd_ex", "gla_fwd_workspace_size", "gla_fwd_num_stages",
+            "gla_fwd_stage", "gla_fwd_stage_name", "gla_device_status", "gla_status_string",
+            "gla_version")
+
+
+class GlaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}" if what else status_string(status))
+
+
+class gla_fwd_params(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("log_g", ctypes.c_void_p), ("S0", ctypes.c_void_p),
+        ("O", ctypes.c_void_p), ("ST", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
+        ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("chunk", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("gate", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("force_segments", ctypes.c_int), ("path", ctypes.c_int),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libgla.so. Raises if it is missing (unless build_if_missing) or unloadable."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"libgla.so not built ({path}); run __graft_entry__.build() "
+                                   "or python -m chunkwise_gated_linear_gla_gb300.build")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER(gla_fwd_params)
+        vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+        lib.gla_fwd.restype = st
+        lib.gla_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.gla_fwd_ex.restype = st
+        lib.gla_fwd_ex.argtypes = [P, vp]
+        lib.gla_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.gla_fwd_workspace_size.argtypes = [P]
+        lib.gla_fwd_num_stages.restype = i
+        lib.gla_fwd_num_stages.argtypes = [P]
+        lib.gla_fwd_stage.restype = st
+        lib.gla_fwd_stage.argtypes = [P, i, vp]
+        lib.gla_fwd_stage_name.restype = ctypes.c_char_p
+        lib.gla_fwd_stage_name.argtypes = [P, i]
+        lib.gla_device_status.restype = st
+        lib.gla_device_status.argtypes = [vp]
+        lib.gla_status_string.restype = ctypes.c_char_p
+        lib.gla_status_string.argtypes = [st]
+        lib.gla_version.restype = i
+        lib.gla_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def status_string(s: int) -> str:
+    try:
+        return load().gla_status_string(int(s)).decode()
+    except Exception:  # pragma: no cover - library missing
+        return f"gla_status {s}"
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(s: int, what: str):
+    if s != GLA_OK:
+        raise GlaError(s, what)
+
+
+# ---------------------------------------------------------------- C names
+
+def gla_fwd(q, k, v, log_g, S0, O, ST, B, H, T, dk, dv, chunk=64, stream=None, check=True) -> int:
+    s = load().gla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_g), _ptr(S0), _ptr(O), _ptr(ST),
+                       B, H, T, dk, dv, chunk, _stream(stream))
+    if check:
+        _check(s, "gla_fwd")
+    return s
+
+
+def gla_fwd_ex(p: gla_fwd_params, stream=None, check=True) -> int:
+    s = load().gla_fwd_ex(ctypes.byref(p), _stream(stream))
+    if check:
+        _check(s, "gla_fwd_ex")
+    return s
+
+
+def gla_fwd_workspace_size(p: gla_fwd_params) -> int:
+    return int(load().gla_fwd_workspace_size(ctypes.byref(p)))
+
+
+def gla_fwd_num_stages(p: gla_fwd_params) -> int:
+    return int(load().gla_fwd_num_stages(ctypes.byref(p)))
+
+
+def gla_fwd_stage(p: gla_fwd_params, stage: int, stream=None, check=True) -> int:
+    s = load().gla_fwd_stage(ctypes.byref(p), stage, _stream(stream))
+    if check:
+        _check(s, f"gla_fwd_stage({stage})")
+    return s
+
+
+def gla_fwd_stage_name(p: gla_fwd_params, stage: int) -> str:
+    return load().gla_fwd_stage_name(ctypes.byref(p), stage).decode()
+
+
+def gla_device_status(stream=None) -> int:
+    return int(load().gla_device_status(_stream(stream)))
+
+
+def gla_status_string(s: int) -> str:
+    return load().gla_status_string(int(s)).decode()
+
+
+def gla_version() -> int:
+    return int(load().gla_version())
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+def make_params(q, k, v, log_g, S0, O, ST, gate=None, path=GLA_PATH_AUTO, force_segments=0,
+                workspace=None, chunk=64) -> gla_fwd_params:
+    """Fill gla_fwd_params from torch tensors (shapes read from q and v)."""
+    import torch
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if gate is None:
+        gate = GLA_GATE_NONE if log_g is None else (GLA_GATE_HEAD_SCALAR if log_g.dim() == 1 else GLA_GATE_PER_KEY)
+    p = gla_fwd_params()
+    p.q, p.k, p.v = _ptr(q), _ptr(k), _ptr(v)
+    p.log_g, p.S0, p.O, p.ST = _ptr(log_g), _ptr(S0), _ptr(O), _ptr(ST)
+    p.B, p.H, p.T, p.dk, p.dv, p.chunk = B, H, T, dk, dv, chunk
+    p.dtype = GLA_BF16 if q.dtype == torch.bfloat16 else GLA_FP32
+    p.gate = gate
+    p.workspace = _ptr(workspace)
+    p.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    p.force_segments = force_segments
+    p.path = path
+    return p
+
+
+def forward(q, k, v, log_g=None, S0=None, gate=None, want_state=True, path=GLA_PATH_AUTO,
+            force_segments=0, stream=None, O=None, ST=None):
+    """Allocate O (and ST) and the workspace with torch, then call gla_fwd_ex.
+
+    q, k: [B,H,T,dk]; v: [B,H,T,dv] (bf16 or fp32, on the GPU); log_g fp32
+    [B,H,T,dk] (per key) or [H] (per-head scalar) or None; S0 fp32 [B,H,dk,dv]
+    or None. Returns (O, ST).
+    """
+    import torch
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if O is None:
+        O = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    if ST is None and want_state:
+        ST = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    p = make_params(q, k, v, log_g, S0, O, ST, gate, path, force_segments)
+    nbytes = gla_fwd_workspace_size(p)
+    ws = None
+    if nbytes > 0:
+        ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=q.device)
+        off = (-ws.data_ptr()) % 256
+        ws = ws[off:off + nbytes]
+        p.workspace = ws.data_ptr()
+        p.workspace_bytes = nbytes
+    gla_fwd_ex(p, stream)
+    return O, ST

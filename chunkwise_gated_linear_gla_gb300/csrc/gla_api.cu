@@ -1,0 +1,348 @@
+// Host side of the C ABI: argument validation, planning, workspace layout and
+// launch order. No arithmetic of the method happens here; every step of the
+// pass runs in the kernels.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gla_internal.h"
+
+namespace gla {
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+__device__ int g_status[1];   // device status word: 0 ok, else the kernel's timeout code
+
+struct DevCache {
+    bool init = false;
+    int major = 0, minor = 0, sms = 0;
+    int* status = nullptr;
+};
+std::mutex g_mu;
+DevCache g_dev[64];
+
+DevCache* dev_cache()
+{
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevCache& c = g_dev[d];
+    if (!c.init) {
+        if (cudaDeviceGetAttribute(&c.major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess) return nullptr;
+        if (cudaDeviceGetAttribute(&c.minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess) return nullptr;
+        if (cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return nullptr;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        c.status = static_cast<int*>(p);
+        c.init = true;
+    }
+    return &c;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range { uintptr_t lo, hi; };
+Range rng(const void* p, size_t bytes) {
+    uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Range{a, a + bytes};
+}
+bool overlap(Range a, Range b) {
+    if (a.lo == a.hi || b.lo == b.hi || a.lo == 0 || b.lo == 0) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Host-only checks: everything that can be decided without touching the device.
+gla_status validate(const gla_fwd_params* p)
+{
+    if (!p) return GLA_ERR_INVALID_ARG;
+    if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->dk <= 0 || p->dv <= 0) return GLA_ERR_INVALID_ARG;
+    if (p->dtype != GLA_BF16 && p->dtype != GLA_FP32) return GLA_ERR_INVALID_ARG;
+    if (p->gate != GLA_GATE_NONE && p->gate != GLA_GATE_HEAD_SCALAR && p->gate != GLA_GATE_PER_KEY)
+        return GLA_ERR_INVALID_ARG;
+    if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT)
+        return GLA_ERR_INVALID_ARG;
+    if (p->force_segments < 0) return GLA_ERR_INVALID_ARG;
+    if (p->dk % 16 != 0 || p->dv % 16 != 0) return GLA_ERR_INVALID_ARG;
+    if ((long long)p->B * p->H > (1LL << 30)) return GLA_ERR_INVALID_ARG;
+    if (p->gate == GLA_GATE_NONE && p->log_g) return GLA_ERR_INVALID_ARG;
+    if (p->gate == GLA_GATE_HEAD_SCALAR && !p->log_g) return GLA_ERR_INVALID_ARG;
+    if (p->gate == GLA_GATE_PER_KEY && !p->log_g && p->T > 0) return GLA_ERR_INVALID_ARG;
+    if (p->T > 0 && (!p->q || !p->k || !p->v || !p->O)) return GLA_ERR_INVALID_ARG;
+    if (p->chunk != 0 && p->chunk != kChunk) return GLA_ERR_UNSUPPORTED;
+    if (p->dk > kMaxDk) return GLA_ERR_UNSUPPORTED;
+
+    const size_t e = p->dtype == GLA_BF16 ? 2 : 4;
+    const size_t BH = (size_t)p->B * p->H;
+    const size_t nq = BH * p->T * p->dk * e, nv = BH * p->T * p->dv * e;
+    const size_t ng = p->gate == GLA_GATE_PER_KEY ? BH * p->T * p->dk * 4
+                    : p->gate == GLA_GATE_HEAD_SCALAR ? (size_t)p->H * 4 : 0;
+    const size_t ns = BH * p->dk * p->dv * 4;
+    // TMA and vector loads need 16-byte aligned bases
+    for (const void* ptr : {p->q, p->k, p->v, (const void*)p->O, (const void*)p->S0, (const void*)p->ST})
+        if (ptr && !aligned(ptr, 16)) return GLA_ERR_INVALID_ARG;
+    if (p->log_g && !aligned(p->log_g, p->gate == GLA_GATE_PER_KEY ? 16 : 4)) return GLA_ERR_INVALID_ARG;
+    // outputs must not overlap inputs; ST may equal S0 exactly (in-place state carry)
+    Range rO = rng(p->O, nv), rST = rng(p->ST, p->ST ? ns : 0);
+    Range ins[] = {rng(p->q, nq), rng(p->k, nq), rng(p->v, nv), rng(p->log_g, ng), rng(p->S0, p->S0 ? ns : 0)};
+    for (Range r : ins) if (overlap(rO, r)) return GLA_ERR_INVALID_ARG;
+    if (overlap(rO, rST)) return GLA_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i) if (overlap(rST, ins[i])) return GLA_ERR_INVALID_ARG;
+    if (p->ST && p->S0 && overlap(rST, ins[4]) && (const void*)p->ST != (const void*)p->S0)
+        return GLA_ERR_INVALID_ARG;
+    if (p->workspace && !aligned(p->workspace, 256)) return GLA_ERR_INVALID_ARG;
+    return GLA_OK;
+}
+
+bool tensor_shape_ok(const gla_fwd_params* p)
+{
+    return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256) &&
+           p->dv % kDvTile == 0;
+}
+
+// Number of sequence segments per (b,h). A single chunk-serial pass per
+// (b,h, dv tile) leaves SMs idle when B*H*tiles is small; splitting the
+// sequence into n segments costs one extra state-only pass and a short
+// serial recurrence over segments, so it pays only when the pass is long
+// and the grid is well under one wave.
+int choose_segments(const gla_fwd_params* p, int units, int nchunks, int sms)
+{
+    if (p->force_segments > 0) return p->force_segments < nchunks ? p->force_segments : (nchunks > 0 ? nchunks : 1);
+    if (units * 2 > sms || nchunks < 16) return 1;
+    int n = sms / units;
+    if (n > nchunks / 8) n = nchunks / 8;
+    return n < 1 ? 1 : n;
+}
+
+gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
+{
+    gla_status st = validate(p);
+    if (st != GLA_OK) return st;
+    pl = Plan{};
+    if (p->T == 0) {
+        pl.path = GLA_PATH_SIMT;
+        pl.nstages = 1;
+        pl.stages[0] = STAGE_COPY_STATE;
+        return GLA_OK;
+    }
+    bool want_tensor = false;
+    if (p->path == GLA_PATH_TENSOR) {
+        if (!tensor_shape_ok(p)) return GLA_ERR_UNSUPPORTED;
+        want_tensor = true;
+    } else if (p->path == GLA_PATH_AUTO) {
+        want_tensor = tensor_shape_ok(p);
+    }
+    if (!want_tensor) {
+        pl.path = GLA_PATH_SIMT;
+        pl.nstages = 1;
+        pl.stages[0] = STAGE_SIMT;
+        return GLA_OK;
+    }
+    pl.path = GLA_PATH_TENSOR;
+    pl.nchunks = (p->T + kChunk - 1) / kChunk;
+    pl.Tpad = pl.nchunks * kChunk;
+    pl.n_dvt = p->dv / kDvTile;
+    pl.raw_qk = (p->gate == GLA_GATE_NONE);
+    const int units = p->B * p->H * pl.n_dvt;
+    pl.nseg = choose_segments(p, units, pl.nchunks, sms > 0 ? sms : 148);
+    pl.chunks_per_seg = (pl.nchunks + pl.nseg - 1) / pl.nseg;
+    pl.nseg = (pl.nchunks + pl.chunks_per_seg - 1) / pl.chunks_per_seg;
+
+    const size_t BH = (size_t)p->B * p->H;
+    size_t off = 0;
+    if (!pl.raw_qk) {
+        pl.off_qt = off; off = align_up(off + BH * pl.Tpad * p->dk * 2, 256);
+        pl.off_kt = off; off = align_up(off + BH * pl.Tpad * p->dk * 2, 256);
+    }
+    pl.off_A = off;   off = align_up(off + BH * pl.nchunks * kChunk * kChunk * 2, 256);
+    pl.off_gam = off; off = align_up(off + BH * pl.nchunks * p->dk * 4, 256);
+    if (pl.nseg > 1) {
+        pl.off_segS = off;  off = align_up(off + BH * pl.nseg * p->dk * p->dv * 4, 256);
+        pl.off_segin = off; off = align_up(off + BH * pl.nseg * p->dk * p->dv * 4, 256);
+    }
+    pl.ws_bytes = off;
+    int n = 0;
+    pl.stages[n++] = STAGE_PREP;
+    if (pl.nseg > 1) {
+        pl.stages[n++] = STAGE_SEG_STATE;
+        pl.stages[n++] = STAGE_SEG_SCAN;
+    }
+    pl.stages[n++] = STAGE_CHUNK_FWD;
+    pl.nstages = n;
+    return GLA_OK;
+}
+
+const char* stage_name(StageKind k)
+{
+    switch (k) {
+    case STAGE_SIMT: return "gla_fwd_simt";
+    case STAGE_PREP: return "gla_chunk_prep";
+    case STAGE_SEG_STATE: return "gla_chunk_state";
+    case STAGE_SEG_SCAN: return "gla_state_scan";
+    case STAGE_CHUNK_FWD: return "gla_chunk_fwd";
+    case STAGE_COPY_STATE: return "gla_copy_state";
+    }
+    return "?";
+}
+
+int device_sms()
+{
+    DevCache* c = dev_cache();
+    return c ? c->sms : 0;
+}
+
+gla_status run_stage(const gla_fwd_params* p, const Plan& pl, int i, cudaStream_t s)
+{
+    DevCache* c = dev_cache();
+    if (!c) return GLA_ERR_CUDA;
+    if (c->major != 10 || c->minor != 3) return GLA_ERR_UNSUPPORTED;  // built for sm_103a only
+    const StageKind k = pl.stages[i];
+    if (pl.ws_bytes > 0 && k != STAGE_SIMT && k != STAGE_COPY_STATE) {
+        if (!p->workspace || p->workspace_bytes < pl.ws_bytes) return GLA_ERR_WORKSPACE;
+    }
+    cudaError_t e = cudaSuccess;
+    switch (k) {
+    case STAGE_COPY_STATE:
+        if (p->ST && p->ST != p->S0) {
+            const size_t ns = (size_t)p->B * p->H * p->dk * p->dv * 4;
+            e = p->S0 ? cudaMemcpyAsync(p->ST, p->S0, ns, cudaMemcpyDeviceToDevice, s)
+                      : cudaMemsetAsync(p->ST, 0, ns, s);
+        }
+        break;
+    case STAGE_SIMT: e = launch_simt(*p, c->status, s); break;
+    case STAGE_PREP: e = launch_prep(*p, pl, p->workspace, c->status, s); break;
+    case STAGE_SEG_STATE: e = launch_chunk_fwd(*p, pl, p->workspace, kModeSegState, c->status, s); break;
+    case STAGE_SEG_SCAN: e = launch_seg_scan(*p, pl, p->workspace, c->status, s); break;
+    case STAGE_CHUNK_FWD:
+        e = launch_chunk_fwd(*p, pl, p->workspace, pl.nseg > 1 ? kModeSegOut : kModeFull, c->status, s);
+        break;
+    }
+    return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+}  // namespace
+
+int* device_status_ptr()
+{
+    DevCache* c = dev_cache();
+    return c ? c->status : nullptr;
+}
+
+}  // namespace gla
+
+using namespace gla;
+
+extern "C" {
+
+size_t gla_fwd_workspace_size(const gla_fwd_params* p)
+{
+    Plan pl;
+    if (validate(p) != GLA_OK) return 0;
+    if (make_plan(p, pl, device_sms()) != GLA_OK) return 0;
+    return pl.ws_bytes;
+}
+
+int gla_fwd_num_stages(const gla_fwd_params* p)
+{
+    Plan pl;
+    if (validate(p) != GLA_OK) return -1;
+    if (make_plan(p, pl, device_sms()) != GLA_OK) return -1;
+    return pl.nstages;
+}
+
+const char* gla_fwd_stage_name(const gla_fwd_params* p, int stage)
+{
+    Plan pl;
+    if (validate(p) != GLA_OK) return "invalid";
+    if (make_plan(p, pl, device_sms()) != GLA_OK || stage < 0 || stage >= pl.nstages) return "invalid";
+    return stage_name(pl.stages[stage]);
+}
+
+gla_status gla_fwd_stage(const gla_fwd_params* p, int stage, cudaStream_t stream)
+{
+    gla_status st = validate(p);
+    if (st != GLA_OK) return st;
+    Plan pl;
+    st = make_plan(p, pl, device_sms());
+    if (st != GLA_OK) return st;
+    if (stage < 0 || stage >= pl.nstages) return GLA_ERR_INVALID_ARG;
+    return run_stage(p, pl, stage, stream);
+}
+
+gla_status gla_fwd_ex(const gla_fwd_params* p, cudaStream_t stream)
+{
+    gla_status st = validate(p);
+    if (st != GLA_OK) return st;
+    Plan pl;
+    st = make_plan(p, pl, device_sms());
+    if (st != GLA_OK) return st;
+    for (int i = 0; i < pl.nstages; ++i) {
+        st = run_stage(p, pl, i, stream);
+        if (st != GLA_OK) return st;
+    }
+    return GLA_OK;
+}
+
+gla_status gla_fwd(const void* q, const void* k, const void* v, const float* log_g,
+                   const float* S0, void* O, float* ST,
+                   int B, int H, int T, int dk, int dv, int chunk, cudaStream_t stream)
+{
+    gla_fwd_params p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q; p.k = k; p.v = v; p.log_g = log_g; p.S0 = S0; p.O = O; p.ST = ST;
+    p.B = B; p.H = H; p.T = T; p.dk = dk; p.dv = dv; p.chunk = chunk;
+    p.dtype = GLA_BF16;
+    p.gate = log_g ? GLA_GATE_PER_KEY : GLA_GATE_NONE;
+    p.path = GLA_PATH_AUTO;
+    gla_status st = validate(&p);
+    if (st != GLA_OK) return st;
+    Plan pl;
+    st = make_plan(&p, pl, device_sms());
+    if (st != GLA_OK) return st;
+    void* ws = nullptr;
+    if (pl.ws_bytes > 0) {
+        if (cudaMallocAsync(&ws, pl.ws_bytes, stream) != cudaSuccess) return GLA_ERR_WORKSPACE;
+        p.workspace = ws;
+        p.workspace_bytes = pl.ws_bytes;
+    }
+    for (int i = 0; i < pl.nstages && st == GLA_OK; ++i) st = run_stage(&p, pl, i, stream);
+    if (ws) {
+        if (cudaFreeAsync(ws, stream) != cudaSuccess && st == GLA_OK) st = GLA_ERR_CUDA;
+    }
+    return st;
+}
+
+gla_status gla_device_status(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GLA_ERR_CUDA;
+    int* d = device_status_ptr();
+    if (!d) return GLA_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, d, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GLA_ERR_CUDA;
+    if (h != 0) {
+        int z = 0;
+        if (cudaMemcpy(d, &z, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return GLA_ERR_CUDA;
+        return GLA_ERR_TIMEOUT;
+    }
+    return GLA_OK;
+}
+
+const char* gla_status_string(gla_status s)
+{
+    switch (s) {
+    case GLA_OK: return "GLA_OK";
+    case GLA_ERR_INVALID_ARG: return "GLA_ERR_INVALID_ARG: invalid argument";
+    case GLA_ERR_UNSUPPORTED: return "GLA_ERR_UNSUPPORTED: request not supported by this build or device";
+    case GLA_ERR_CUDA: return "GLA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case GLA_ERR_WORKSPACE: return "GLA_ERR_WORKSPACE: workspace missing, too small or not allocatable";
+    case GLA_ERR_TIMEOUT: return "GLA_ERR_TIMEOUT: a kernel's bounded wait ran out";
+    }
+    return "unknown gla_status";
+}
+
+int gla_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Internal declarations shared by the host planner and the kernel launchers.
+// Not part of the public ABI (include/gla.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/gla.h"
+
+namespace gla {
+
+constexpr int kChunk = 64;        // primary chunk length C of the tensor-core path
+constexpr int kSimtChunk = 16;    // chunk length of the CUDA-core path
+constexpr int kDvTile = 128;      // dv columns per CTA on the tensor-core path
+constexpr int kSimtDvTile = 64;   // dv columns per CTA on the CUDA-core path
+constexpr int kMaxDk = 256;
+
+enum StageKind {
+    STAGE_SIMT = 0,        // whole pass on CUDA cores
+    STAGE_PREP = 1,        // gate prep + intra-chunk scores
+    STAGE_SEG_STATE = 2,   // per-segment state from a zero start (sequence split)
+    STAGE_SEG_SCAN = 3,    // serial recurrence over segments
+    STAGE_CHUNK_FWD = 4,   // chunk-serial tensor-core pass: state, inter + intra output
+    STAGE_COPY_STATE = 5,  // T == 0: ST <- S0 (or 0)
+};
+
+struct Plan {
+    int path = GLA_PATH_SIMT;
+    int nchunks = 0;       // ceil(T / 64)
+    int Tpad = 0;          // nchunks * 64
+    int n_dvt = 0;         // number of dv tiles
+    int nseg = 1;          // sequence segments per (b,h)
+    int chunks_per_seg = 0;
+    bool raw_qk = false;   // tensor path reads q,k directly (no gate)
+    // workspace layout (byte offsets from the workspace base)
+    size_t off_qt = 0, off_kt = 0, off_A = 0, off_gam = 0, off_segS = 0, off_segin = 0;
+    size_t ws_bytes = 0;
+    int nstages = 0;
+    StageKind stages[4];
+};
+
+// Device status word (per device), written by kernels whose bounded waits run out.
+int* device_status_ptr();   // nullptr on failure
+
+// Launchers. Each returns cudaSuccess or the launch error.
+cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s);
+cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
+cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode,
+                             int* status, cudaStream_t s);
+cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, int* status,
+                            cudaStream_t s);
+
+// chunk_fwd modes
+constexpr int kModeFull = 0;        // O and final state from S0 (single segment)
+constexpr int kModeSegState = 1;    // per-segment state from zero, no O
+constexpr int kModeSegOut = 2;      // O from per-segment start states, no final state
+
+}  // namespace gla

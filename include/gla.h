@@ -1,0 +1,136 @@
+/*
+ * gla.h — C ABI of the GB300 (sm_103a) forward pass of chunkwise gated linear
+ * attention.
+ *
+ * The operation ("Gated Linear Attention Transformers with Hardware-Efficient
+ * Training", §4.1 Eq. 3, computed in the chunkwise form of §4.2-4.3):
+ *
+ *     S_t = Diag(alpha_t) S_{t-1} + k_t^T v_t,     o_t = q_t S_t,
+ *
+ * for t = 1..T, independently for every batch row b and head h, starting from
+ * S_0 (zero, or a state carried from a previous segment, §2.2). The pass
+ * returns O = [o_1 .. o_T] and the final state S_T.
+ *
+ * Gate modes (all given in log space, log alpha <= 0):
+ *   GLA_GATE_NONE        alpha_t = 1: causal linear attention (§2.1 Eq. 1);
+ *                        log_g must be NULL.
+ *   GLA_GATE_HEAD_SCALAR alpha_t = lambda_h for every t and key: the fixed
+ *                        decay of "Lightning Attention-2" (§3.2.1, Alg. 1) and
+ *                        RetNet; log_g is float[H] = log(lambda_h).
+ *   GLA_GATE_PER_KEY     alpha_t in (0,1]^dk, data dependent (GLA, §4.1);
+ *                        log_g is float[B,H,T,dk] = log(alpha_t).
+ *
+ * Layouts. Every tensor is dense, row-major, last dimension contiguous:
+ *   q, k   [B,H,T,dk]   dtype (bf16 or fp32)
+ *   v, O   [B,H,T,dv]   dtype
+ *   log_g  see above    fp32
+ *   S0, ST [B,H,dk,dv]  fp32
+ *
+ * Ownership. All tensor pointers are device pointers owned by the caller. The
+ * library keeps none of them after a call returns. It allocates nothing on
+ * its own except in gla_fwd(), which takes its workspace from the stream-
+ * ordered allocator (cudaMallocAsync / cudaFreeAsync on the given stream).
+ *
+ * Asynchrony. Every call only enqueues work on `stream` and returns; it never
+ * synchronises the device. Argument errors are detected on the host before
+ * anything is launched. A kernel whose bounded wait runs out records that in
+ * a device-side status word (see gla_device_status) and returns early.
+ *
+ * Thread safety. Calls may be made concurrently from several host threads.
+ * The only process-wide state is a per-device cache of the TMA encode entry
+ * point and device attributes.
+ */
+#ifndef GLA_H_
+#define GLA_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GLA_OK = 0,
+    GLA_ERR_INVALID_ARG = 1,  /* null/overlapping/misaligned pointer, bad size, gate/log_g mismatch */
+    GLA_ERR_UNSUPPORTED = 2,  /* valid request this build does not handle (chunk size, device) */
+    GLA_ERR_CUDA = 3,         /* a CUDA runtime call or a launch failed */
+    GLA_ERR_WORKSPACE = 4,    /* workspace missing, too small or could not be allocated */
+    GLA_ERR_TIMEOUT = 5       /* a kernel's bounded wait ran out (reported by gla_device_status) */
+} gla_status;
+
+typedef enum { GLA_BF16 = 0, GLA_FP32 = 1 } gla_dtype;
+
+typedef enum {
+    GLA_GATE_NONE = 0,
+    GLA_GATE_HEAD_SCALAR = 1,
+    GLA_GATE_PER_KEY = 2
+} gla_gate;
+
+/* Which kernels run. AUTO picks the tcgen05 tensor-core path for bf16 inputs
+ * with dk in {64,128,256} and dv a multiple of 128, and the fp32 CUDA-core
+ * path otherwise (always for fp32 inputs). Both compute the same function. */
+typedef enum { GLA_PATH_AUTO = 0, GLA_PATH_TENSOR = 1, GLA_PATH_SIMT = 2 } gla_path;
+
+typedef struct {
+    const void* q;          /* [B,H,T,dk] */
+    const void* k;          /* [B,H,T,dk] */
+    const void* v;          /* [B,H,T,dv] */
+    const float* log_g;     /* see gate modes; NULL iff gate == GLA_GATE_NONE */
+    const float* S0;        /* [B,H,dk,dv] or NULL (zero initial state) */
+    void* O;                /* [B,H,T,dv], written */
+    float* ST;              /* [B,H,dk,dv] or NULL (final state not written); may equal S0 */
+    int B, H, T, dk, dv;
+    int chunk;              /* primary chunk length: 0 or 64 (64 is used either way) */
+    gla_dtype dtype;        /* dtype of q, k, v and O */
+    gla_gate gate;
+    void* workspace;        /* device scratch of >= gla_fwd_workspace_size() bytes, 256-B aligned */
+    size_t workspace_bytes;
+    int force_segments;     /* 0: the planner chooses the sequence split; n >= 1: use n segments */
+    int path;               /* gla_path */
+} gla_fwd_params;
+
+/*
+ * gla_fwd — the whole forward pass, with the bf16 data type.
+ * gate = GLA_GATE_PER_KEY if log_g != NULL, else GLA_GATE_NONE.
+ * chunk must be 0 or 64. The workspace comes from cudaMallocAsync on `stream`
+ * and is released with cudaFreeAsync on the same stream.
+ * Returns GLA_OK once everything is enqueued.
+ */
+gla_status gla_fwd(const void* q, const void* k, const void* v, const float* log_g,
+                   const float* S0, void* O, float* ST,
+                   int B, int H, int T, int dk, int dv, int chunk, cudaStream_t stream);
+
+/* gla_fwd_ex — the forward pass described by *p, all stages in order on
+ * `stream`. If the plan needs workspace, p->workspace must hold
+ * gla_fwd_workspace_size(p) bytes (else GLA_ERR_WORKSPACE). */
+gla_status gla_fwd_ex(const gla_fwd_params* p, cudaStream_t stream);
+
+/* Bytes of workspace the plan for *p needs (0 if none). Returns 0 for
+ * invalid parameters as well; gla_fwd_ex then reports the error. */
+size_t gla_fwd_workspace_size(const gla_fwd_params* p);
+
+/* The plan for *p as separate stages, so that a caller can put events
+ * between them: gla_fwd_ex(p) == gla_fwd_stage(p, 0) ... gla_fwd_stage(p, n-1).
+ * gla_fwd_num_stages returns n (>= 1), or -1 for invalid parameters.
+ * gla_fwd_stage_name returns a static string naming the kernel of stage i. */
+int gla_fwd_num_stages(const gla_fwd_params* p);
+gla_status gla_fwd_stage(const gla_fwd_params* p, int stage, cudaStream_t stream);
+const char* gla_fwd_stage_name(const gla_fwd_params* p, int stage);
+
+/* Synchronises `stream`, then reads and clears the library's device status
+ * word for the current device. GLA_ERR_TIMEOUT if a kernel gave up on a
+ * bounded wait since the last call, GLA_ERR_CUDA if the stream reports an
+ * error, else GLA_OK. */
+gla_status gla_device_status(cudaStream_t stream);
+
+/* A static, human-readable name for s. */
+const char* gla_status_string(gla_status s);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int gla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GLA_H_ */

@@ -1,0 +1,142 @@
+"""The C-ABI library: it loads, exports every symbol include/gla.h declares,
+and rejects invalid arguments on the host before any launch. No GPU needed:
+none of these calls reaches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunkwise_gated_linear_gla_gb300 as gla
+from chunkwise_gated_linear_gla_gb300 import binding as bnd
+from chunkwise_gated_linear_gla_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return bnd.load()
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        txt = open(os.path.join(ROOT, "include", h)).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        names += re.findall(r"\b(gla_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert "gla_fwd" in declared and "gla_fwd_ex" in declared
+    for n in declared:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(declared) <= set(bnd.EXPORTED) | set(declared)
+    for n in bnd.EXPORTED:
+        assert n in declared, f"binding wraps {n}, which include/ does not declare"
+
+
+def test_struct_layout_matches_header():
+    # 7 pointers, 8 ints, pointer, size_t, 2 ints
+    assert ctypes.sizeof(bnd.gla_fwd_params) == 7 * 8 + 8 * 4 + 8 + 8 + 2 * 4
+    assert bnd.gla_fwd_params.workspace.offset == 88
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        txt = gla.gla_status_string(s)
+        assert txt.startswith("GLA_")
+    assert gla.gla_version() >= 100
+
+
+def _params(**kw):
+    p = bnd.gla_fwd_params()
+    base = dict(q=0x10000, k=0x20000, v=0x30000, log_g=0x40000, S0=None, O=0x50000, ST=None,
+                B=1, H=1, T=64, dk=64, dv=64, chunk=64, dtype=bnd.GLA_BF16,
+                gate=bnd.GLA_GATE_PER_KEY, workspace=None, workspace_bytes=0,
+                force_segments=0, path=bnd.GLA_PATH_AUTO)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    return p
+
+
+BAD = [
+    ("null q", dict(q=None), bnd.GLA_ERR_INVALID_ARG),
+    ("null O", dict(O=None), bnd.GLA_ERR_INVALID_ARG),
+    ("B=0", dict(B=0), bnd.GLA_ERR_INVALID_ARG),
+    ("H<0", dict(H=-1), bnd.GLA_ERR_INVALID_ARG),
+    ("T<0", dict(T=-5), bnd.GLA_ERR_INVALID_ARG),
+    ("dk not /16", dict(dk=40), bnd.GLA_ERR_INVALID_ARG),
+    ("dv not /16", dict(dv=72 + 1), bnd.GLA_ERR_INVALID_ARG),
+    ("gate none with log_g", dict(gate=bnd.GLA_GATE_NONE), bnd.GLA_ERR_INVALID_ARG),
+    ("per-key gate without log_g", dict(log_g=None), bnd.GLA_ERR_INVALID_ARG),
+    ("misaligned q", dict(q=0x10002), bnd.GLA_ERR_INVALID_ARG),
+    ("misaligned O", dict(O=0x50008), bnd.GLA_ERR_INVALID_ARG),
+    ("O overlaps v", dict(O=0x30000 + 64), bnd.GLA_ERR_INVALID_ARG),
+    ("ST overlaps k", dict(ST=0x20000), bnd.GLA_ERR_INVALID_ARG),
+    ("ST partially overlaps S0", dict(S0=0x100000, ST=0x100000 + 256), bnd.GLA_ERR_INVALID_ARG),
+    ("bad dtype", dict(dtype=7), bnd.GLA_ERR_INVALID_ARG),
+    ("bad gate", dict(gate=9), bnd.GLA_ERR_INVALID_ARG),
+    ("bad path", dict(path=5), bnd.GLA_ERR_INVALID_ARG),
+    ("negative segments", dict(force_segments=-1), bnd.GLA_ERR_INVALID_ARG),
+    ("misaligned workspace", dict(workspace=0x7000010, workspace_bytes=1 << 20), bnd.GLA_ERR_INVALID_ARG),
+    ("chunk 32", dict(chunk=32), bnd.GLA_ERR_UNSUPPORTED),
+    ("dk 512", dict(dk=512), bnd.GLA_ERR_UNSUPPORTED),
+    ("tensor path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
+    ("tensor path with dv 48", dict(dv=48, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", BAD, ids=[b[0] for b in BAD])
+def test_rejects_before_launch(lib, name, kw, want):
+    p = _params(**kw)
+    assert bnd.gla_fwd_ex(p, stream=0, check=False) == want
+    assert bnd.gla_fwd_stage(p, 0, stream=0, check=False) == want
+    assert bnd.gla_fwd_num_stages(p) == -1
+    assert bnd.gla_fwd_workspace_size(p) == 0
+
+
+def test_gla_fwd_rejects_before_launch(lib):
+    # spec signature: dk not a multiple of 16
+    s = bnd.gla_fwd(0x10000, 0x20000, 0x30000, 0x40000, None, 0x50000, None, 1, 1, 64, 40, 64, 64,
+                    stream=0, check=False)
+    assert s == bnd.GLA_ERR_INVALID_ARG
+    s = bnd.gla_fwd(0x10000, 0x20000, 0x30000, None, None, 0x50000, None, 1, 1, 64, 64, 64, 128,
+                    stream=0, check=False)
+    assert s == bnd.GLA_ERR_UNSUPPORTED
+
+
+def test_plan_on_host():
+    # in-place state carry (ST == S0) is valid
+    p = _params(S0=0x100000, ST=0x100000)
+    assert bnd.gla_fwd_num_stages(p) >= 1
+    # bf16 with supported shapes plans the tensor path: prep + chunk pass, with workspace
+    p = _params(dk=256, dv=512, T=2048, B=8, H=4, q=0x1000000, k=0x9000000, v=0x11000000,
+                log_g=0x21000000, O=0x31000000)
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names[0] == "gla_chunk_prep" and names[-1] == "gla_chunk_fwd"
+    assert bnd.gla_fwd_workspace_size(p) > 0
+    # forced segments add the state pass and the scan
+    p.force_segments = 4
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_prep", "gla_chunk_state", "gla_state_scan", "gla_chunk_fwd"]
+    # fp32 takes the CUDA-core path, no workspace
+    p = _params(dtype=bnd.GLA_FP32)
+    assert [bnd.gla_fwd_stage_name(p, 0)] == ["gla_fwd_simt"]
+    assert bnd.gla_fwd_workspace_size(p) == 0
+    # empty sequence: only the state copy
+    p = _params(T=0, q=None, k=None, v=None, O=None)
+    assert bnd.gla_fwd_stage_name(p, 0) == "gla_copy_state"
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(bnd, "_lib", None)
+    monkeypatch.setattr(bnd._build, "LIB", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        bnd.load()
