@@ -1,0 +1,369 @@
+"""Benchmark of the chunkwise GLA forward pass on GB300.
+
+Workload: the GLA layer shaped like the 1.3B model, B=8, H=4, T=2048,
+dk=256, dv=512, bf16 q/k/v, fp32 per-key log gate logsigmoid(N(0,1))/16,
+S0 ~ 0.02 N(0,1); synthetic seeded inputs (no dataset exists for this).
+
+One step = one whole forward pass (every stage of the plan) over one batch.
+`value` is tokens/s over all ranks with inputs resident in HBM and L2
+flushed between steps; `e2e` is the same metric through the spec C
+call gla_fwd with the inputs copied from pinned host memory and O, S_T read
+back inside the timed region. With N > 1 ranks each rank runs its own
+replica batch (the path shards over (b, h) with no exchange): weak scaling.
+
+`--impl reference` times the fp64 CPU oracle on this machine's host cores
+on a bounded sample of the same workload (it is the only other
+implementation of this method available here).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "gla_1p3b"
+METRIC = "GLA fwd tokens/s and TFLOP/s (fraction of GB300 bf16 peak) at B=8,T=2048,dk256,dv512"
+FALLBACK_HBM = 6800.0
+FALLBACK_BF16 = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-rows", type=int, default=8,
+                    help="batch rows of the workload the oracle runs for cpu_baseline")
+    ap.add_argument("--ref-sample-rows", type=int, default=1,
+                    help="batch rows per step of the reference arm")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
+
+
+def algorithmic(w):
+    """Algorithmic FLOPs and bytes of one forward pass of workload w (per rank).
+
+    FLOPs per token per head: 4 dk dv (state update + inter-chunk term) +
+    (C+1)(dk+dv) (causal intra-chunk scores and their product with V).
+    Bytes: q, k, v read and O written once (e bytes each element), the fp32
+    per-key log gate read once, S0 read and S_T written once (fp32).
+    """
+    e = 2
+    BH, T, dk, dv, C = w.B * w.H, w.T, w.dk, w.dv, w.chunk
+    flops = BH * T * (4 * dk * dv + (C + 1) * (dk + dv))
+    byts = BH * T * (e * (2 * dk + dv) + e * dv + 4 * dk) + BH * dk * dv * 4 * (2 if w.s0_std > 0 else 1)
+    return flops, byts
+
+
+def stage_bytes(w, name):
+    """Compulsory bytes one launch of a stage moves (each operand once), bf16 e=2."""
+    BH, T, dk, dv, C = w.B * w.H, w.T, w.dk, w.dv, w.chunk
+    nch = (T + C - 1) // C
+    Tp = nch * C
+    if name == "gla_chunk_prep":
+        return BH * (T * dk * 2 * 2 + T * dk * 4 + Tp * dk * 2 * 2 + nch * C * C * 2 + nch * dk * 4)
+    if name == "gla_chunk_fwd":
+        return BH * (Tp * dk * 2 * 2 + nch * C * C * 2 + nch * dk * 4 + T * dv * 2 * 2) + BH * dk * dv * 4 * 2
+    return 0
+
+
+def kernel_source_sha(name):
+    files = {"gla_chunk_fwd": ["gla_chunk_fwd.cu", "sm100.cuh"], "gla_chunk_prep": ["gla_prep.cu"]}.get(name, [])
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "chunkwise_gated_linear_gla_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)[name]
+        if d.get("source_sha") != kernel_source_sha(name):
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampling (200 ms) during the timed region."""
+
+    FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_reference(args, w):
+    """The oracle (fp64 recurrence, C, all host cores) on a bounded sample of the workload."""
+    import oracle
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle.build()
+    rows = args.ref_sample_rows
+    ws = w.with_(B=rows)
+    x = gi.make_inputs(ws, seed=0)
+    cores = oracle.default_threads()
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=cores)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    tok = rows * w.T
+    mean = sum(times) / len(times)
+    value = tok / mean
+    sample = f"{rows} of {w.B} batch rows (all {w.H} heads, T={w.T}) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, rows):
+    import oracle
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    oracle.build()
+    x = gi.make_inputs(w.with_(B=rows), seed=0)
+    cores = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": rows * w.T / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} of {w.B} batch rows (all {w.H} heads, T={w.T}), {dt:.1f} s"}
+
+
+def main():
+    args = parse()
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    w = gi.WORKLOADS[WORKLOAD]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import chunkwise_gated_linear_gla_gb300 as gla
+    from chunkwise_gated_linear_gla_gb300 import binding as bnd
+    from chunkwise_gated_linear_gla_gb300 import build as gbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        gbuild.build()
+    if world > 1:
+        dist.barrier()
+    bnd.load()
+
+    # CPU baseline first (before any GPU work of this process is in flight)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_sample_rows)
+
+    x = gi.make_inputs(w, seed=rank)
+    dev = torch.device("cuda", local)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    g, S0 = x["log_g"].to(dev), x["S0"].to(dev)
+    O = torch.empty((w.B, w.H, w.T, w.dv), dtype=torch.bfloat16, device=dev)
+    ST = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    p = bnd.make_params(q, k, v, g, S0, O, ST)
+    nbytes = bnd.gla_fwd_workspace_size(p)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), nbytes
+    nst = bnd.gla_fwd_num_stages(p)
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(nst)]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 129 MB of L2
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        for i in range(nst):
+            if evs is not None:
+                evs[i].record(stream)
+            bnd.gla_fwd_stage(p, i, stream)
+        if evs is not None:
+            evs[nst].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if bnd.gla_device_status(stream) != 0:
+        raise SystemExit("device status error after warm-up")
+
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.zero_()
+        step(evsets[s])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    if bnd.gla_device_status(stream) != 0:
+        raise SystemExit("device status error in timed region")
+    stage_ms = [0.0] * nst
+    step_ms = 0.0
+    for evs in evsets:
+        for i in range(nst):
+            stage_ms[i] += evs[i].elapsed_time(evs[i + 1])
+        step_ms += evs[0].elapsed_time(evs[nst])
+    stage_ms = [t / args.steps for t in stage_ms]
+    step_ms /= args.steps
+    t = torch.tensor([step_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    step_ms = float(t.item())
+
+    # end to end through gla_fwd with host buffers
+    hq, hk, hv, hg, hs = (x[n].pin_memory() for n in ("q", "k", "v", "log_g", "S0"))
+    hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    hST = torch.empty(ST.shape, dtype=ST.dtype).pin_memory()
+    h2d = sum(tt.numel() * tt.element_size() for tt in (hq, hk, hv, hg, hs))
+    d2h = hO.numel() * hO.element_size() + hST.numel() * hST.element_size()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
+        g.copy_(hg, non_blocking=True); S0.copy_(hs, non_blocking=True)
+        bnd.gla_fwd(q, k, v, g, S0, O, ST, w.B, w.H, w.T, w.dk, w.dv, 64, stream)
+        hO.copy_(O, non_blocking=True); hST.copy_(ST, non_blocking=True)
+
+    for _ in range(max(2, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    te = torch.tensor([e2e_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_ms = float(te.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    hbm, bf16, bf16_sus, src = peaks()
+    flops, byts = algorithmic(w)
+    tokens = w.B * w.T * world
+    value = tokens / (step_ms * 1e-3)
+    tflops = flops * world / (step_ms * 1e-3) / 1e12
+    dom = max(range(nst), key=lambda i: stage_ms[i])
+    dname = names[dom]
+    dbytes = stage_bytes(w, dname)
+    ach = dbytes / (stage_ms[dom] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": {"workload": f"{w.name}: GLA layer B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv} chunk=64, "
+                               "per-key log gate, S0 given", "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                   "l2": "flushed between steps (256 MB write, outside the timed events)",
+                   "stages": names, "stage_ms": stage_ms},
+        "tflops": tflops, "tflops_frac_bf16_peak": tflops / bf16,
+        "path_gbs": byts * world / (step_ms * 1e-3) / 1e9, "path_frac_hbm": byts / (step_ms * 1e-3) / 1e9 / hbm,
+        "roofline": {"kernel": dname, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                     "frac": ach / hbm, "traffic": ncu_traffic(dname), "peak_source": src,
+                     "bytes_per_launch": dbytes},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": nst * args.steps,
+        "clocks": clk,
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -99,8 +99,10 @@ gla_status validate(const gla_fwd_params* p)
 
 bool tensor_shape_ok(const gla_fwd_params* p)
 {
+    const long long BH = (long long)p->B * p->H;
+    const long long Tpad = ((long long)p->T + kChunk - 1) / kChunk * kChunk;
     return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256) &&
-           p->dv % kDvTile == 0;
+           p->dv % kDvTile == 0 && BH <= 65535 && BH * Tpad < (1LL << 31);
 }
 
 // Number of sequence segments per (b,h). A single chunk-serial pass per

@@ -1,0 +1,399 @@
+// gla_chunk_fwd: the chunk-serial tensor-core pass of the chunkwise GLA forward
+// ("Gated Linear Attention Transformers with Hardware-Efficient Training",
+// §4.2; the non-materialised FlashLinearAttention loop of §3.3 / Alg. 1 with
+// the gated chunk recurrence). One CTA owns one (b, h), one tile of 128
+// columns of dv and one segment of chunks; per chunk n of C = 64 rows:
+//
+//   S-group   Sb  <- bf16(S_[n-1])            (TMEM -> TMEM, A operand)
+//             S   <- Diag(gamma_n) S_[n-1]    (TMEM fp32, gate scales rows)
+//   MMA       S^T += V_n^T (K_n (.) Gamma_n)  (state, M=128 N=dk K=64)
+//             O^T  = Sb^T (Q_n (.) Lambda_n)^T (inter, A from TMEM, N=64 K=dk)
+//             O^T += V_n^T (P_n (.) M)^T      (intra, N=64 K=64)
+//   O-group   O^T TMEM -> registers -> bf16 smem tile -> TMA store
+//
+// Everything is transposed (M = dv) so each MMA uses all 128 TMEM lanes and
+// the state's columns (dk) line up with the per-key gate. The state stays in
+// tensor memory for the whole segment and never goes to HBM; Q (.) Lambda,
+// K (.) Gamma, gamma and the masked intra-chunk scores come from
+// gla_chunk_prep. Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM
+// owner), 2-5 state group, 6-9 output group. Every wait is bounded; on a
+// timeout the CTA records an error code and winds down.
+#include <cuda_bf16.h>
+
+#include "gla_internal.h"
+#include "sm100.cuh"
+#include "tma_host.h"
+
+namespace gla {
+namespace {
+
+using namespace sm100;
+
+constexpr int C = kChunk;
+constexpr int DVT = kDvTile;
+constexpr int NSTAGE = 2;
+constexpr int NT = 320;
+constexpr int BAR_S = 1, BAR_O = 2, BAR_O2 = 3;   // named barriers (0 is __syncthreads)
+constexpr int O_LEADER = 6 * 32;
+constexpr uint64_t kTimeoutNs = 2000000000ull;    // 2 s per wait
+
+enum { ERR_PRODUCER = 0x101, ERR_MMA = 0x102, ERR_STATE = 0x103, ERR_OUT = 0x104 };
+
+struct FwdArgs {
+    const float* S_in;  long long s_in_bh, s_in_seg;
+    float* S_out;       long long s_out_bh, s_out_seg;
+    const float* gam;   // [BH][nchunks][dk], null without a gate
+    int* status;
+    int dv, nchunks, cps, mode, gated;
+};
+
+template <int DK>
+struct Lay {
+    static constexpr int QB = DK * C * 2;
+    static constexpr int KB = DK * C * 2;
+    static constexpr int VB = DVT * C * 2;
+    static constexpr int AB = C * C * 2;
+    static constexpr int GB = DK * 4;
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = QB;
+    static constexpr int V_OFF = QB + KB;
+    static constexpr int A_OFF = V_OFF + VB;
+    static constexpr int G_OFF = A_OFF + AB;
+    static constexpr int STAGE = (G_OFF + GB + 1023) / 1024 * 1024;
+    static constexpr int OB = C * DVT * 2;
+    static constexpr int O_OFF = NSTAGE * STAGE;
+    static constexpr int BAR_OFF = O_OFF + 2 * OB;
+    static constexpr int SMEM = BAR_OFF + 256 + 1024;
+    static constexpr int TCOLS_USED = DK + DK / 2 + 2 * 64;
+    static constexpr int TCOLS = TCOLS_USED <= 256 ? 256 : 512;
+    static_assert(TCOLS_USED <= 512, "TMEM budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void fail(int* status, volatile int* abort_flag, int code) {
+    *abort_flag = 1;
+    atomicExch(status, code);
+}
+
+// All `n` threads of a named-barrier group agree on success (bar.red.or).
+__device__ __forceinline__ bool group_all_ok(bool ok, int id, int n) {
+    uint32_t bad;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(bad)
+        : "r"(ok ? 0u : 1u), "r"(id), "r"(n)
+        : "memory");
+    return bad == 0;
+}
+
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+template <int DK>
+__global__ void __launch_bounds__(NT, 1)
+gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmO)
+{
+    using L = Lay<DK>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
+    uint64_t* full = bar + 0;      // [2] stage filled (TMA transaction count)
+    uint64_t* empty = bar + 2;     // [2] stage consumed (MMA commit)
+    uint64_t* s_ready = bar + 4;   // state decayed and staged (128 arrivals)
+    uint64_t* s_done = bar + 5;    // state MMA of the chunk complete
+    uint64_t* sb_free = bar + 6;   // inter MMA complete: bf16 state copy reusable
+    uint64_t* o_full = bar + 7;    // [2] O accumulator complete
+    uint64_t* o_empty = bar + 9;   // [2] O accumulator drained (128 arrivals)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 11);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 12);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int bh = blockIdx.y, seg = blockIdx.z;
+    const int dv0 = blockIdx.x * DVT;
+    const int c_begin = seg * a.cps;
+    const int c_end = min(a.nchunks, c_begin + a.cps);
+    const int nloc = max(0, c_end - c_begin);
+    const bool want_out = a.mode != kModeSegState;
+    const bool gated = a.gated != 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&full[0], 1); mbar_init(&full[1], 1);
+        mbar_init(&empty[0], 1); mbar_init(&empty[1], 1);
+        mbar_init(s_ready, 128); mbar_init(s_done, 1); mbar_init(sb_free, 1);
+        mbar_init(&o_full[0], 1); mbar_init(&o_full[1], 1);
+        mbar_init(&o_empty[0], 128); mbar_init(&o_empty[1], 128);
+        *abort_flag = 0;
+        mbar_fence_init();
+        prefetch_tmap(&tmQ); prefetch_tmap(&tmK); prefetch_tmap(&tmV); prefetch_tmap(&tmA); prefetch_tmap(&tmO);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, L::TCOLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t tS = tmem, tSb = tmem + DK, tO0 = tmem + DK + DK / 2;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int n = 0; n < nloc; ++n) {
+                if (*abort_flag) break;
+                const int st = n & 1, c = c_begin + n;
+                if (n >= 2 && !mbar_wait(&empty[st], ((n >> 1) - 1) & 1, kTimeoutNs)) {
+                    fail(a.status, abort_flag, ERR_PRODUCER);
+                    break;
+                }
+                uint8_t* sb = sm + st * L::STAGE;
+                const uint32_t bytes = L::KB + L::VB + (gated ? L::GB : 0) + (want_out ? L::QB + L::AB : 0);
+                mbar_arrive_expect_tx(&full[st], bytes);
+#pragma unroll
+                for (int i = 0; i < DK / 64; ++i)
+                    tma_load_3d(sb + L::K_OFF + i * 8192, &tmK, &full[st], i * 64, c * C, bh);
+                tma_load_3d(sb + L::V_OFF, &tmV, &full[st], dv0, c * C, bh);
+                tma_load_3d(sb + L::V_OFF + 8192, &tmV, &full[st], dv0 + 64, c * C, bh);
+                if (gated) bulk_load(sb + L::G_OFF, a.gam + ((size_t)bh * a.nchunks + c) * DK, L::GB, &full[st]);
+                if (want_out) {
+#pragma unroll
+                    for (int i = 0; i < DK / 64; ++i)
+                        tma_load_3d(sb + L::Q_OFF + i * 8192, &tmQ, &full[st], i * 64, c * C, bh);
+                    tma_load_2d(sb + L::A_OFF, &tmA, &full[st], 0, (bh * a.nchunks + c) * C);
+                }
+                issued = n + 1;
+            }
+            // no copy may land after the CTA exits: wait for the last fills
+            for (int n = max(0, issued - 2); n < issued; ++n) mbar_wait(&full[n & 1], (n >> 1) & 1, kTimeoutNs);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t id_state = idesc_bf16(128, DK, true, true);
+            const uint32_t id_inter = idesc_bf16(128, 64, false, false);
+            const uint32_t id_intra = idesc_bf16(128, 64, true, false);
+            for (int n = 0; n < nloc; ++n) {
+                if (*abort_flag) break;
+                const int st = n & 1;
+                bool ok = mbar_wait(&full[st], (n >> 1) & 1, kTimeoutNs);
+                ok = ok && mbar_wait(s_ready, n & 1, kTimeoutNs);
+                if (ok && want_out && n >= 2) ok = mbar_wait(&o_empty[n & 1], ((n >> 1) - 1) & 1, kTimeoutNs);
+                if (!ok) {
+                    fail(a.status, abort_flag, ERR_MMA);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sb = smem_u32(sm + st * L::STAGE);
+                const uint32_t sQ = sb + L::Q_OFF, sK = sb + L::K_OFF, sV = sb + L::V_OFF, sA = sb + L::A_OFF;
+                // state: S^T += V^T (K (.) Gamma); both operands MN-major
+#pragma unroll
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tS, sdesc(sV + kk * 2048, 8192, 1024, kSwizzle128),
+                           sdesc(sK + kk * 2048, 8192, 1024, kSwizzle128), id_state, 1);
+                mma_commit(s_done);
+                if (want_out) {
+                    const uint32_t tO = tO0 + (n & 1) * 64;
+                    // inter: O^T = Sb^T (Q (.) Lambda)^T, A (the bf16 state) from TMEM
+#pragma unroll
+                    for (int kk = 0; kk < DK / 16; ++kk)
+                        mma_ts(tO, tSb + kk * 8, sdesc(sQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128),
+                               id_inter, kk > 0);
+                    mma_commit(sb_free);
+                    // intra: O^T += V^T (P (.) M)^T
+#pragma unroll
+                    for (int kk = 0; kk < C / 16; ++kk)
+                        mma_ss(tO, sdesc(sV + kk * 2048, 8192, 1024, kSwizzle128),
+                               sdesc(sA + kk * 32, 16, 1024, kSwizzle128), id_intra, 1);
+                    mma_commit(&o_full[n & 1]);
+                }
+                mma_commit(&empty[st]);
+            }
+        }
+    } else if (warp < 6) {
+        // ---------------------------------------------------------- state group
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+        const int d = (warp & 3) * 32 + lane;   // dv column within the tile
+        {
+            const float* sin = a.S_in ? a.S_in + bh * a.s_in_bh + seg * a.s_in_seg + dv0 + d : nullptr;
+#pragma unroll 1
+            for (int c0 = 0; c0 < DK; c0 += 32) {
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = sin ? __float_as_uint(sin[(size_t)(c0 + i) * a.dv]) : 0u;
+                tmem_st32(tS + lb + c0, r);
+            }
+            tmem_wait_st();
+        }
+        bool alive = true;
+        for (int n = 0; n < nloc; ++n) {
+            bool ok = true;
+            if (n >= 1) ok = mbar_wait(s_done, (n - 1) & 1, kTimeoutNs);
+            if (ok && want_out && n >= 1) ok = mbar_wait(sb_free, (n - 1) & 1, kTimeoutNs);
+            if (ok && gated) ok = mbar_wait(&full[n & 1], (n >> 1) & 1, kTimeoutNs);
+            if (!group_all_ok(ok, BAR_S, 128)) {
+                if (threadIdx.x == 64) fail(a.status, abort_flag, ERR_STATE);
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            const float* g = reinterpret_cast<const float*>(sm + (n & 1) * L::STAGE + L::G_OFF);
+#pragma unroll 1
+            for (int c0 = 0; c0 < DK; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tS + lb + c0, r);
+                tmem_wait_ld();
+                if (want_out) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    tmem_st16(tSb + lb + c0 / 2, pk);
+                }
+                if (gated) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * g[c0 + i]);
+                    tmem_st32(tS + lb + c0, r);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(s_ready);
+        }
+        if (alive && nloc > 0) {
+            const bool ok = mbar_wait(s_done, (nloc - 1) & 1, kTimeoutNs);
+            if (group_all_ok(ok, BAR_S, 128)) {
+                tc_fence_after();
+                if (a.S_out) {
+                    float* so = a.S_out + bh * a.s_out_bh + seg * a.s_out_seg + dv0 + d;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < DK; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tS + lb + c0, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) so[(size_t)(c0 + i) * a.dv] = __uint_as_float(r[i]);
+                    }
+                }
+            } else if (threadIdx.x == 64) {
+                fail(a.status, abort_flag, ERR_STATE);
+            }
+        }
+    } else if (want_out) {
+        // ---------------------------------------------------------- output group
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+        const int d = (warp & 3) * 32 + lane;
+        const int half = d >> 6, col = d & 63;
+        for (int n = 0; n < nloc; ++n) {
+            const int b = n & 1;
+            const bool ok = mbar_wait(&o_full[b], (n >> 1) & 1, kTimeoutNs);
+            if (!group_all_ok(ok, BAR_O, 128)) {
+                if (threadIdx.x == O_LEADER) fail(a.status, abort_flag, ERR_OUT);
+                break;
+            }
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tO0 + b * 64 + lb, r0);
+            tmem_ld32(tO0 + b * 64 + lb + 32, r1);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&o_empty[b]);
+            // the store issued from this buffer two chunks ago must have read it
+            if (threadIdx.x == O_LEADER) bulk_wait_read1();
+            named_bar_sync(BAR_O2, 128);
+            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(sm + L::O_OFF + b * L::OB) + half * (C * 64) + col;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) ob[t * 64] = __float2bfloat16_rn(__uint_as_float(r0[t]));
+#pragma unroll
+            for (int t = 0; t < 32; ++t) ob[(t + 32) * 64] = __float2bfloat16_rn(__uint_as_float(r1[t]));
+            fence_proxy_async_smem();
+            named_bar_sync(BAR_O2, 128);
+            if (threadIdx.x == O_LEADER) {
+                const uint8_t* src = sm + L::O_OFF + b * L::OB;
+                const int c = c_begin + n;
+                tma_store_3d(&tmO, src, dv0, c * C, bh);
+                tma_store_3d(&tmO, src + C * 64 * 2, dv0 + 64, c * C, bh);
+                bulk_commit();
+            }
+        }
+        if (threadIdx.x == O_LEADER) bulk_wait0();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TCOLS);
+    }
+}
+
+bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, CUtensorMapSwizzle swz) {
+    uint64_t dims[3] = {d0, d1, d2};
+    uint64_t str[2] = {d0 * 2, d0 * d1 * 2};
+    uint32_t box[3] = {64, 64, 1};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, swz);
+}
+
+template <int DK>
+cudaError_t launch_dk(const FwdArgs& a, dim3 grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                      const CUtensorMap& A, const CUtensorMap& o, cudaStream_t s) {
+    using L = Lay<DK>;
+    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) return e;
+    gla_chunk_fwd_kernel<DK><<<grid, NT, L::SMEM, s>>>(a, q, k, v, A, o);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode, int* status, cudaStream_t s)
+{
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const uint64_t BH = (uint64_t)p.B * p.H;
+    const void* qb = pl.raw_qk ? p.q : base + pl.off_qt;
+    const void* kb = pl.raw_qk ? p.k : base + pl.off_kt;
+    const uint64_t qrows = pl.raw_qk ? (uint64_t)p.T : (uint64_t)pl.Tpad;
+    CUtensorMap mq, mk, mv, ma, mo;
+    if (!map3(&mq, qb, p.dk, qrows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (!map3(&mk, kb, p.dk, qrows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (!map3(&mv, p.v, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (!map3(&mo, p.O, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    {
+        uint64_t dims[2] = {64, BH * (uint64_t)pl.nchunks * 64};
+        uint64_t str[1] = {128};
+        uint32_t box[2] = {64, 64};
+        if (!make_tmap(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base + pl.off_A, dims, str, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    FwdArgs a;
+    const long long st = (long long)p.dk * p.dv;
+    a.S_in = nullptr; a.s_in_bh = 0; a.s_in_seg = 0;
+    a.S_out = nullptr; a.s_out_bh = 0; a.s_out_seg = 0;
+    if (mode == kModeFull) {
+        a.S_in = p.S0; a.s_in_bh = st;
+        a.S_out = p.ST; a.s_out_bh = st;
+    } else if (mode == kModeSegState) {
+        a.S_out = reinterpret_cast<float*>(base + pl.off_segS); a.s_out_bh = st * pl.nseg; a.s_out_seg = st;
+    } else {
+        a.S_in = reinterpret_cast<const float*>(base + pl.off_segin); a.s_in_bh = st * pl.nseg; a.s_in_seg = st;
+    }
+    a.gam = reinterpret_cast<const float*>(base + pl.off_gam);
+    a.status = status;
+    a.dv = p.dv; a.nchunks = pl.nchunks;
+    a.cps = (mode == kModeFull) ? pl.nchunks : pl.chunks_per_seg;
+    a.mode = mode;
+    a.gated = p.gate != GLA_GATE_NONE;
+    dim3 grid(pl.n_dvt, (unsigned)BH, mode == kModeFull ? 1 : pl.nseg);
+    switch (p.dk) {
+    case 64: return launch_dk<64>(a, grid, mq, mk, mv, ma, mo, s);
+    case 128: return launch_dk<128>(a, grid, mq, mk, mv, ma, mo, s);
+    case 256: return launch_dk<256>(a, grid, mq, mk, mv, ma, mo, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gla
