@@ -21,7 +21,7 @@ GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT = 0, 1, 2
 # Every symbol include/gla.h declares.
 EXPORTED = ("gla_fwd", "gla_fwd_ex", "gla_fwd_workspace_size", "gla_fwd_num_stages",
             "gla_fwd_stage", "gla_fwd_stage_name", "gla_device_status", "gla_status_string",
-            "gla_version")
+            "gla_version", "gla_fwd_noalloc")
 
 
 class GlaError(RuntimeError):
@@ -68,6 +68,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
         lib.gla_fwd.restype = st
         lib.gla_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.gla_fwd_noalloc.restype = st
+        lib.gla_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.gla_fwd_ex.restype = st
         lib.gla_fwd_ex.argtypes = [P, vp]
         lib.gla_fwd_workspace_size.restype = ctypes.c_size_t
@@ -124,6 +126,15 @@ def gla_fwd(q, k, v, log_g, S0, O, ST, B, H, T, dk, dv, chunk=64, stream=None, c
                        B, H, T, dk, dv, chunk, _stream(stream))
     if check:
         _check(s, "gla_fwd")
+    return s
+
+
+def gla_fwd_noalloc(q, k, v, log_g, S0, O, ST, B, H, T, dk, dv, chunk=64, stream=None, check=True) -> int:
+    """gla_fwd without any device allocation (library-owned fixed scratch); see include/gla.h."""
+    s = load().gla_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_g), _ptr(S0), _ptr(O), _ptr(ST),
+                               B, H, T, dk, dv, chunk, _stream(stream))
+    if check:
+        _check(s, "gla_fwd_noalloc")
     return s
 
 

@@ -118,6 +118,33 @@ int gla_fwd_num_stages(const gla_fwd_params* p);
 gla_status gla_fwd_stage(const gla_fwd_params* p, int stage, cudaStream_t stream);
 const char* gla_fwd_stage_name(const gla_fwd_params* p, int stage);
 
+/*
+ * gla_fwd_noalloc — gla_fwd for callers that cannot allocate device memory.
+ * (No counterpart in the papers: this is a deployment convenience.)
+ *
+ * Some hosts cannot call cudaMalloc/cudaMallocAsync: a framework that has
+ * given nearly all device memory to its own pool, a latency-critical loop
+ * where allocation is banned because it can synchronise the device, or a
+ * plugin interface that offers the kernel no allocator. This entry point
+ * takes the same arguments as gla_fwd and allocates nothing; its workspace
+ * is a fixed array of GLA_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library holds until the process exits. The plan
+ * never splits the sequence here.
+ *
+ * Returns GLA_ERR_WORKSPACE, before launching anything, when the call would
+ * need more than GLA_NOALLOC_SCRATCH_BYTES of workspace (with a per-key gate
+ * and dk = 256 that is about B*H*T > 28,000 token-heads); use gla_fwd_ex with
+ * a caller-owned workspace for larger calls. The first call on a device looks
+ * up the array's device address (with that device current); make it before
+ * any stream capture. All calls on a device share the array: calls that
+ * overlap on the GPU race on it, so the caller must order them (one stream,
+ * or events between streams).
+ */
+#define GLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+gla_status gla_fwd_noalloc(const void* q, const void* k, const void* v, const float* log_g,
+                           const float* S0, void* O, float* ST,
+                           int B, int H, int T, int dk, int dv, int chunk, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the library's device status
  * word for the current device. GLA_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last call, GLA_ERR_CUDA if the stream reports an
