@@ -24,6 +24,12 @@
 // inside one sub-chunk is taken out of the MMA and added pairwise in fp32 log
 // space instead (Eq. 4), which is the paper's full-precision intra-sub-chunk
 // rule, applied only where it is needed.
+//
+// Thread layout of the element-wise phase: thread t owns 8 consecutive key
+// columns (one 16-byte vector of bf16) and RPT = dk/32 consecutive rows, so
+// every warp reads and writes whole rows with 16-byte accesses. The
+// cumulative gate is a two-level scan: a serial sum over the thread's rows,
+// then the totals of the row groups above it.
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
@@ -32,12 +38,13 @@ namespace gla {
 namespace {
 
 constexpr int C = kChunk;
-constexpr int SC = 16;                 // sub-chunk rows
-constexpr int NSUB = C / SC;           // 4
-constexpr int NPAIR = NSUB * (NSUB + 1) / 2;   // 10 lower (j >= u) blocks
-constexpr int NTRI = SC * (SC + 1) / 2;        // 136 pairs r >= s in a block
+constexpr int SC = 16;                          // sub-chunk rows
+constexpr int NSUB = C / SC;                    // 4
+constexpr int NPAIR = NSUB * (NSUB + 1) / 2;    // 10 lower (j >= u) blocks
+constexpr int NTRI = SC * (SC + 1) / 2;         // 136 pairs r >= s in a block
 constexpr int NT = 256;
 constexpr int NWARP = NT / 32;
+constexpr int ALD = C + 8;                      // bf16 row stride of the staged A tile
 constexpr float kGuard = 60.f;
 
 struct PrepArgs {
@@ -48,10 +55,26 @@ struct PrepArgs {
     __nv_bfloat16* Kt;
     float* gam;
     __nv_bfloat16* A;
-    int H, T, dk, nchunks, Tpad, gate;
+    int H, T, nchunks, Tpad, gate;
 };
 
-__device__ __forceinline__ int pair_index(int j, int u) { return j * (j + 1) / 2 + u; }
+template <int DK>
+struct PL {
+    static constexpr int NCG = DK / 8;          // column groups of 8
+    static constexpr int NRG = NT / NCG;        // row groups
+    static constexpr int RPT = C / NRG;         // rows per thread (dk / 32)
+    static constexpr int LD = DK + 8;           // bf16 row stride: keeps mma fragment loads conflict-free
+    static constexpr int QS_OFF = 0;
+    static constexpr int KS_OFF = QS_OFF + C * LD * 2;
+    static constexpr int W_OFF = KS_OFF + C * LD * 2;             // [NPAIR][DK] fp32
+    static constexpr int X_OFF = W_OFF + NPAIR * DK * 4;          // [2][NRG][DK] fp32 (totals, then first/last)
+    static constexpr int CORR_OFF = X_OFF + 2 * NRG * DK * 4;     // [NSUB][NTRI] fp32
+    static constexpr int STEEP_OFF = CORR_OFF + NSUB * NTRI * 4;  // [NSUB][DK] u8
+    static constexpr int ANY_OFF = STEEP_OFF + NSUB * DK;         // [NSUB] int
+    static constexpr int SMEM = ANY_OFF + 16;
+    static_assert(RPT >= 1 && SC % RPT == 0, "a thread's rows lie in one sub-chunk");
+    static_assert(C * ALD * 2 <= 2 * C * LD * 2, "A staging fits in the Q/K tiles");
+};
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
@@ -69,146 +92,205 @@ __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t x, float w0, float w1)
     return *reinterpret_cast<uint32_t*>(&r);
 }
 
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return u;
+}
+
+template <int DK>
 __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
 {
+    using L = PL<DK>;
+    constexpr int RPT = L::RPT, NRG = L::NRG, LD = L::LD;
     extern __shared__ __align__(16) uint8_t smem[];
-    const int dk = a.dk;
-    const int LD = dk + 8;  // bf16 row stride: 4-word skew keeps mma fragment loads conflict-free
-    __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem);           // [C][LD]  Q (.) exp(Bc - f_j)
-    __nv_bfloat16* Ks = Qs + C * LD;                                      // [C][LD]  K (.) exp(l_u - Bc)
-    float* W = reinterpret_cast<float*>(Ks + C * LD);                     // [NPAIR][dk] exp(f_j - l_u)
-    float* part = W + NPAIR * dk;                                         // [NWARP][NSUB][NTRI]
-    int* steep_any = reinterpret_cast<int*>(part + NWARP * NSUB * NTRI);  // [NSUB]
+    __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem + L::QS_OFF);   // [C][LD]  Q (.) exp(Bc - f_j)
+    __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem + L::KS_OFF);   // [C][LD]  K (.) exp(l_u - Bc)
+    float* W = reinterpret_cast<float*>(smem + L::W_OFF);                     // [NPAIR][DK] exp(f_j - l_u)
+    float* X = reinterpret_cast<float*>(smem + L::X_OFF);
+    float* corr = reinterpret_cast<float*>(smem + L::CORR_OFF);               // [NSUB][NTRI]
+    uint8_t* steep = smem + L::STEEP_OFF;                                     // [NSUB][DK]
+    int* steep_any = reinterpret_cast<int*>(smem + L::ANY_OFF);
+    __nv_bfloat16* As = Qs;                                                   // [C][ALD], after the MMAs
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int c = blockIdx.x, bh = blockIdx.y, h = bh % a.H;
     const int t0 = c * C;
     const int nr = min(C, a.T - t0);
     const bool gated = a.gate != GLA_GATE_NONE;
+    const int cg = tid % L::NCG, rg = tid / L::NCG;
+    const int col0 = cg * 8, row0 = rg * RPT;
+    const int j = row0 / SC;   // the sub-chunk this thread's rows lie in
+    const float lam = (a.gate == GLA_GATE_HEAD_SCALAR) ? a.log_g[h] : 0.f;
 
     if (tid < NSUB) steep_any[tid] = 0;
-    __syncthreads();
+    for (int i = tid; i < NSUB * DK; i += NT) steep[i] = 0;
 
-    // ---------------- phase 1: one thread per key column
-    const int kk = tid;
-    const bool active = kk < dk;
-    float Bc[C];
-    float f[NSUB], l[NSUB];
-    bool steep[NSUB];
-    if (active) {
-        float run = 0.f;
-        const float lam = (a.gate == GLA_GATE_HEAD_SCALAR) ? a.log_g[h] : 0.f;
-        const float* g = (a.gate == GLA_GATE_PER_KEY) ? a.log_g + ((size_t)bh * a.T + t0) * dk + kk : nullptr;
+    // ---- 1. log gates of my rows and their running sum
+    float Bc[RPT][8];
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            float gl = 0.f;
-            if (r < nr) gl = g ? __ldg(g + (size_t)r * dk) : lam;
-            run += gl;
-            Bc[r] = run;
-        }
-        const float gend = Bc[C - 1];
-#pragma unroll
-        for (int j = 0; j < NSUB; ++j) {
-            f[j] = Bc[j * SC];
-            l[j] = Bc[j * SC + SC - 1];
-        }
-#pragma unroll
-        for (int j = 0; j < NSUB; ++j) {
-#pragma unroll
-            for (int u = 0; u <= j; ++u) {
-                float w;
-                if (u < j) {
-                    w = __expf(f[j] - l[u]);
-                } else {
-                    steep[j] = (f[j] - l[j]) > kGuard;
-                    w = steep[j] ? 0.f : __expf(f[j] - l[j]);
-                }
-                W[pair_index(j, u) * dk + kk] = w;
+    for (int r = 0; r < RPT; ++r) {
+        const bool ok = row0 + r < nr;
+        if (a.gate == GLA_GATE_PER_KEY) {
+            float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+            if (ok) {
+                const float4* g = reinterpret_cast<const float4*>(a.log_g + ((size_t)bh * a.T + t0 + row0 + r) * DK + col0);
+                x0 = __ldg(g);
+                x1 = __ldg(g + 1);
             }
-            if (steep[j]) atomicOr(&steep_any[j], 1);
-        }
-        if (gated) a.gam[((size_t)bh * a.nchunks + c) * dk + kk] = __expf(gend);
-
-        const __nv_bfloat16* qp = a.q + ((size_t)bh * a.T + t0) * dk + kk;
-        const __nv_bfloat16* kp = a.k + ((size_t)bh * a.T + t0) * dk + kk;
-        __nv_bfloat16* qo = a.Qt + ((size_t)bh * a.Tpad + t0) * dk + kk;
-        __nv_bfloat16* ko = a.Kt + ((size_t)bh * a.Tpad + t0) * dk + kk;
-#pragma unroll
-        for (int j = 0; j < NSUB; ++j) {
-            const float ef = __expf(f[j]);          // Lambda at the sub-chunk's first row
-            const float eg = __expf(gend - l[j]);   // Gamma at the sub-chunk's last row
-#pragma unroll
-            for (int i = 0; i < SC; ++i) {
-                const int r = j * SC + i;
-                float qv = 0.f, kv = 0.f;
-                if (r < nr) {
-                    qv = __bfloat162float(qp[(size_t)r * dk]);
-                    kv = __bfloat162float(kp[(size_t)r * dk]);
-                }
-                const float e1 = __expf(Bc[r] - f[j]);   // <= 1
-                const float e2 = __expf(l[j] - Bc[r]);   // <= 1
-                const float qs = qv * e1, ks = kv * e2;
-                Qs[r * LD + kk] = __float2bfloat16_rn(qs);
-                Ks[r * LD + kk] = __float2bfloat16_rn(ks);
-                if (gated) {
-                    qo[(size_t)r * dk] = __float2bfloat16_rn(qs * ef);
-                    ko[(size_t)r * dk] = __float2bfloat16_rn(ks * eg);
-                }
-            }
-        }
-    }
-
-    // exact log-space scores for steep key columns of diagonal blocks
-#pragma unroll 1
-    for (int j = 0; j < NSUB; ++j) {
-        const bool mine = active && steep[j];
-        float* pw = part + (warp * NSUB + j) * NTRI;
-        if (__any_sync(0xffffffffu, mine)) {
-            float qv[SC], kv[SC], bc[SC];
-            const float* g = (a.gate == GLA_GATE_PER_KEY) ? a.log_g + ((size_t)bh * a.T + t0) * dk + kk : nullptr;
-            const float lam = (a.gate == GLA_GATE_HEAD_SCALAR) ? a.log_g[h] : 0.f;
-            float run = 0.f;
-#pragma unroll
-            for (int i = 0; i < SC; ++i) {
-                const int r = j * SC + i;
-                qv[i] = kv[i] = 0.f;
-                float gl = 0.f;
-                if (mine && r < nr) {
-                    qv[i] = __bfloat162float(a.q[((size_t)bh * a.T + t0 + r) * dk + kk]);
-                    kv[i] = __bfloat162float(a.k[((size_t)bh * a.T + t0 + r) * dk + kk]);
-                    gl = g ? g[(size_t)r * dk] : lam;
-                }
-                // cumulative log gate inside the sub-chunk; only differences are used
-                run += gl;
-                bc[i] = run;
-            }
-#pragma unroll
-            for (int r = 0; r < SC; ++r) {
-#pragma unroll
-                for (int s = 0; s <= r; ++s) {
-                    float v = mine ? qv[r] * kv[s] * __expf(bc[r] - bc[s]) : 0.f;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0) pw[r * (r + 1) / 2 + s] = v;
-                }
-            }
+            Bc[r][0] = x0.x; Bc[r][1] = x0.y; Bc[r][2] = x0.z; Bc[r][3] = x0.w;
+            Bc[r][4] = x1.x; Bc[r][5] = x1.y; Bc[r][6] = x1.z; Bc[r][7] = x1.w;
         } else {
-            for (int p = lane; p < NTRI; p += 32) pw[p] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) Bc[r][i] = ok ? lam : 0.f;
         }
+    }
+#pragma unroll
+    for (int r = 1; r < RPT; ++r)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) Bc[r][i] += Bc[r - 1][i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) X[rg * DK + col0 + i] = Bc[RPT - 1][i];
+    __syncthreads();
+    {
+        float off[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int rr = 0; rr < rg; ++rr)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) off[i] += X[rr * DK + col0 + i];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) Bc[r][i] += off[i];
+    }
+    __syncthreads();   // totals read by everyone; the region now holds first/last rows
+    float* first = X;
+    float* last = X + NRG * DK;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        first[rg * DK + col0 + i] = Bc[0][i];
+        last[rg * DK + col0 + i] = Bc[RPT - 1][i];
     }
     __syncthreads();
 
-    // ---------------- phase 2: lower blocks of A on the tensor cores
-    __nv_bfloat16* Ao = a.A + ((size_t)bh * a.nchunks + c) * C * C;
+    // ---- 2. sub-chunk references, scaled operands, Q (.) Lambda and K (.) Gamma
+    float f[8], l[8], ef[8], eg[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[i] = first[(j * SC / RPT) * DK + col0 + i];
+        l[i] = last[((j * SC + SC - 1) / RPT) * DK + col0 + i];
+        const float gend = last[(NRG - 1) * DK + col0 + i];
+        ef[i] = __expf(f[i]);
+        eg[i] = __expf(gend - l[i]);
+    }
+    if (row0 == j * SC) {
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const bool s = (f[i] - l[i]) > kGuard;
+            steep[j * DK + col0 + i] = s ? 1 : 0;
+            any |= s;
+        }
+        if (any) atomicOr(&steep_any[j], 1);
+    }
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int row = row0 + r;
+        uint4 qu = make_uint4(0, 0, 0, 0), ku = qu;
+        if (row < nr) {
+            qu = __ldg(reinterpret_cast<const uint4*>(a.q + ((size_t)bh * a.T + t0 + row) * DK + col0));
+            ku = __ldg(reinterpret_cast<const uint4*>(a.k + ((size_t)bh * a.T + t0 + row) * DK + col0));
+        }
+        float qv[8], kv[8], qs[8], ks[8];
+        unpack8(qu, qv);
+        unpack8(ku, kv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            qs[i] = qv[i] * __expf(Bc[r][i] - f[i]);   // factor <= 1
+            ks[i] = kv[i] * __expf(l[i] - Bc[r][i]);   // factor <= 1
+        }
+        *reinterpret_cast<uint4*>(Qs + row * LD + col0) = pack8(qs);
+        *reinterpret_cast<uint4*>(Ks + row * LD + col0) = pack8(ks);
+        if (gated) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                qs[i] *= ef[i];
+                ks[i] *= eg[i];
+            }
+            *reinterpret_cast<uint4*>(a.Qt + ((size_t)bh * a.Tpad + t0 + row) * DK + col0) = pack8(qs);
+            *reinterpret_cast<uint4*>(a.Kt + ((size_t)bh * a.Tpad + t0 + row) * DK + col0) = pack8(ks);
+        }
+    }
+    for (int p = tid; p < NPAIR * DK; p += NT) {
+        const int pr = p / DK, col = p % DK;
+        int jj = 0;
+        while ((jj + 1) * (jj + 2) / 2 <= pr) ++jj;
+        const int uu = pr - jj * (jj + 1) / 2;
+        const float fj = first[(jj * SC / RPT) * DK + col];
+        const float lu = last[((uu * SC + SC - 1) / RPT) * DK + col];
+        float w = __expf(fj - lu);
+        if (jj == uu && (fj - lu) > kGuard) w = 0.f;
+        W[p] = w;
+    }
+    if (gated)
+        for (int col = tid; col < DK; col += NT)
+            a.gam[((size_t)bh * a.nchunks + c) * DK + col] = __expf(last[(NRG - 1) * DK + col]);
+    __syncthreads();
+
+    // ---- 3. exact log-space scores for steep key columns of diagonal blocks
+#pragma unroll 1
+    for (int jj = 0; jj < NSUB; ++jj) {
+        if (!steep_any[jj]) continue;   // block-uniform
+        for (int p = tid; p < NTRI; p += NT) {
+            int r = 0;
+            while ((r + 1) * (r + 2) / 2 <= p) ++r;
+            const int s = p - r * (r + 1) / 2;
+            const int R = jj * SC + r, S = jj * SC + s;
+            float acc = 0.f;
+            if (R < nr) {
+                for (int col = 0; col < DK; ++col) {
+                    if (!steep[jj * DK + col]) continue;
+                    float lg = 0.f;   // log(b_R / b_S) = sum of log gates over rows S+1..R
+                    for (int i = S + 1; i <= R; ++i)
+                        lg += (a.gate == GLA_GATE_PER_KEY) ? a.log_g[((size_t)bh * a.T + t0 + i) * DK + col] : lam;
+                    const float qv = __bfloat162float(a.q[((size_t)bh * a.T + t0 + R) * DK + col]);
+                    const float kv = __bfloat162float(a.k[((size_t)bh * a.T + t0 + S) * DK + col]);
+                    acc += qv * kv * __expf(lg);
+                }
+            }
+            corr[jj * NTRI + p] = acc;
+        }
+    }
+
+    // ---- 4. lower blocks of A on the tensor cores
     const int g8 = lane / 4, c4 = lane % 4;
-    for (int blk = warp; blk < NPAIR; blk += NWARP) {
-        int j = 0;
-        while ((j + 1) * (j + 2) / 2 <= blk) ++j;
-        const int u = blk - j * (j + 1) / 2;
-        const float* w = W + blk * dk;
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const __nv_bfloat16* qa = Qs + (j * SC + g8) * LD + 2 * c4;
-        for (int k0 = 0; k0 < dk; k0 += 16) {
+    float acc[2][2][4];
+#pragma unroll
+    for (int bi = 0; bi < 2; ++bi) {
+        const int blk = warp + bi * NWARP;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[bi][nt][e] = 0.f;
+        if (blk >= NPAIR) continue;
+        int jb = 0;
+        while ((jb + 1) * (jb + 2) / 2 <= blk) ++jb;
+        const int ub = blk - jb * (jb + 1) / 2;
+        const float* w = W + blk * DK;
+        const __nv_bfloat16* qa = Qs + (jb * SC + g8) * LD + 2 * c4;
+#pragma unroll 4
+        for (int k0 = 0; k0 < DK; k0 += 16) {
             const uint32_t a0 = *reinterpret_cast<const uint32_t*>(qa + k0);
             const uint32_t a1 = *reinterpret_cast<const uint32_t*>(qa + 8 * LD + k0);
             const uint32_t a2 = *reinterpret_cast<const uint32_t*>(qa + k0 + 8);
@@ -217,50 +299,67 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
             const float2 w89 = *reinterpret_cast<const float2*>(w + k0 + 2 * c4 + 8);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const __nv_bfloat16* kb = Ks + (u * SC + nt * 8 + g8) * LD + 2 * c4 + k0;
+                const __nv_bfloat16* kb = Ks + (ub * SC + nt * 8 + g8) * LD + 2 * c4 + k0;
                 uint32_t b0 = *reinterpret_cast<const uint32_t*>(kb);
                 uint32_t b1 = *reinterpret_cast<const uint32_t*>(kb + 8);
                 if (gated) {
                     b0 = scale_bf16x2(b0, w01.x, w01.y);
                     b1 = scale_bf16x2(b1, w89.x, w89.y);
                 }
-                mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+                mma_bf16_16816(acc[bi][nt], a0, a1, a2, a3, b0, b1);
             }
         }
-        const bool diag = (j == u);
-        const bool corr = diag && steep_any[j];
+    }
+    __syncthreads();   // every warp is done reading Qs/Ks; As reuses that space
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+    for (int bi = 0; bi < 2; ++bi) {
+        const int blk = warp + bi * NWARP;
+        if (blk >= NPAIR) continue;
+        int jb = 0;
+        while ((jb + 1) * (jb + 2) / 2 <= blk) ++jb;
+        const int ub = blk - jb * (jb + 1) / 2;
+        const bool diag = (jb == ub);
+        const bool fix = diag && steep_any[jb];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
-                const int rl = g8 + hr * 8;               // row within the block
-                const int sl = nt * 8 + 2 * c4;           // first of two columns
-                float v0 = acc[nt][hr * 2 + 0], v1 = acc[nt][hr * 2 + 1];
+                const int rl = g8 + hr * 8;
+                const int sl = nt * 8 + 2 * c4;
+                float v0 = acc[bi][nt][hr * 2 + 0], v1 = acc[bi][nt][hr * 2 + 1];
                 if (diag) {
-                    if (corr) {
-                        for (int wq = 0; wq < NWARP; ++wq) {
-                            const float* pw = part + (wq * NSUB + j) * NTRI;
-                            if (sl <= rl) v0 += pw[rl * (rl + 1) / 2 + sl];
-                            if (sl + 1 <= rl) v1 += pw[rl * (rl + 1) / 2 + sl + 1];
-                        }
+                    if (fix) {
+                        if (sl <= rl) v0 += corr[jb * NTRI + rl * (rl + 1) / 2 + sl];
+                        if (sl + 1 <= rl) v1 += corr[jb * NTRI + rl * (rl + 1) / 2 + sl + 1];
                     }
                     if (sl > rl) v0 = 0.f;
                     if (sl + 1 > rl) v1 = 0.f;
                 }
-                __nv_bfloat162 o = __floats2bfloat162_rn(v0, v1);
-                *reinterpret_cast<__nv_bfloat162*>(Ao + (j * SC + rl) * C + u * SC + sl) = o;
+                *reinterpret_cast<__nv_bfloat162*>(As + (jb * SC + rl) * ALD + ub * SC + sl) =
+                    __floats2bfloat162_rn(v0, v1);
             }
-        }
     }
     // upper blocks (j < u) are zero
     for (int idx = tid; idx < C * C / 2; idx += NT) {
         const int r = idx / (C / 2), s = (idx % (C / 2)) * 2;
-        if (s / SC > r / SC) *reinterpret_cast<uint32_t*>(Ao + r * C + s) = 0u;
+        if (s / SC > r / SC) *reinterpret_cast<uint32_t*>(As + r * ALD + s) = 0u;
+    }
+    __syncthreads();
+    __nv_bfloat16* Ao = a.A + ((size_t)bh * a.nchunks + c) * C * C;
+    for (int idx = tid; idx < C * C / 8; idx += NT) {
+        const int r = idx / (C / 8), s = (idx % (C / 8)) * 8;
+        *reinterpret_cast<uint4*>(Ao + r * C + s) = *reinterpret_cast<const uint4*>(As + r * ALD + s);
     }
 }
 
-size_t prep_smem_bytes(int dk) {
-    return (size_t)2 * C * (dk + 8) * 2 + (size_t)NPAIR * dk * 4 + (size_t)NWARP * NSUB * NTRI * 4 + NSUB * 4;
+template <int DK>
+cudaError_t launch_prep_dk(const PrepArgs& a, dim3 grid, cudaStream_t s)
+{
+    using L = PL<DK>;
+    cudaError_t e = cudaFuncSetAttribute(gla_chunk_prep_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) return e;
+    gla_chunk_prep_kernel<DK><<<grid, NT, L::SMEM, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -277,13 +376,14 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     a.Kt = pl.raw_qk ? nullptr : reinterpret_cast<__nv_bfloat16*>(base + pl.off_kt);
     a.gam = reinterpret_cast<float*>(base + pl.off_gam);
     a.A = reinterpret_cast<__nv_bfloat16*>(base + pl.off_A);
-    a.H = p.H; a.T = p.T; a.dk = p.dk; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
-    const size_t smem = prep_smem_bytes(p.dk);
-    cudaError_t e = cudaFuncSetAttribute(gla_chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
     dim3 grid(pl.nchunks, p.B * p.H);
-    gla_chunk_prep_kernel<<<grid, NT, smem, s>>>(a);
-    return cudaGetLastError();
+    switch (p.dk) {
+    case 64: return launch_prep_dk<64>(a, grid, s);
+    case 128: return launch_prep_dk<128>(a, grid, s);
+    case 256: return launch_prep_dk<256>(a, grid, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gla
