@@ -4,20 +4,25 @@
 // the gated chunk recurrence). One CTA owns one (b, h), one tile of 128
 // columns of dv and one segment of chunks; per chunk n of C = 64 rows:
 //
-//   S-group   Sb  <- bf16(S_[n-1])            (TMEM -> TMEM, A operand)
-//             S   <- Diag(gamma_n) S_[n-1]    (TMEM fp32, gate scales rows)
+//   epilogue  S   <- Diag(gamma_n) S_[n-1]    (TMEM fp32, gate scales rows)
 //   MMA       S^T += V_n^T (K_n (.) Gamma_n)  (state, M=128 N=dk K=64)
-//             O^T  = Sb^T (Q_n (.) Lambda_n)^T (inter, A from TMEM, N=64 K=dk)
+//   epilogue  Sb  <- bf16(S_[n-1])            (TMEM, A operand; written once
+//                                              the previous inter MMA is done)
+//   MMA       O^T  = Sb^T (Q_n (.) Lambda_n)^T (inter, A from TMEM, N=64 K=dk)
 //             O^T += V_n^T (P_n (.) M)^T      (intra, N=64 K=64)
-//   O-group   O^T TMEM -> registers -> bf16 smem tile -> TMA store
+//   epilogue  O^T TMEM -> registers -> bf16 smem tile -> TMA store
 //
 // Everything is transposed (M = dv) so each MMA uses all 128 TMEM lanes and
 // the state's columns (dk) line up with the per-key gate. The state stays in
 // tensor memory for the whole segment and never goes to HBM; Q (.) Lambda,
 // K (.) Gamma, gamma and the masked intra-chunk scores come from
 // gla_chunk_prep. Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM
-// owner), 2-5 state group, 6-9 output group. Every wait is bounded; on a
-// timeout the CTA records an error code and winds down.
+// owner), 2-9 epilogue in two groups of four warps, each owning half of the
+// state's columns and half of each output tile. Only the decay of the state
+// sits on the chunk-to-chunk critical path (state MMA -> decay -> next state
+// MMA); the bf16 copy, the inter and intra MMAs and the output drain overlap
+// with it. Every wait is bounded; on a timeout the CTA records an error code
+// and winds down.
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
@@ -33,11 +38,11 @@ constexpr int C = kChunk;
 constexpr int DVT = kDvTile;
 constexpr int NSTAGE = 2;
 constexpr int NT = 320;
-constexpr int BAR_S = 1, BAR_O = 2, BAR_O2 = 3;   // named barriers (0 is __syncthreads)
-constexpr int O_LEADER = 6 * 32;
+constexpr int NEPI = 256;                         // epilogue threads (warps 2-9)
+constexpr int BAR_EPI = 1, BAR_G0 = 2;            // named barriers (0 is __syncthreads)
 constexpr uint64_t kTimeoutNs = 2000000000ull;    // 2 s per wait
 
-enum { ERR_PRODUCER = 0x101, ERR_MMA = 0x102, ERR_STATE = 0x103, ERR_OUT = 0x104 };
+enum { ERR_PRODUCER = 0x101, ERR_MMA = 0x102, ERR_EPI = 0x103 };
 
 struct FwdArgs {
     const float* S_in;  long long s_in_bh, s_in_seg;
@@ -98,18 +103,20 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                      const __grid_constant__ CUtensorMap tmO)
 {
     using L = Lay<DK>;
+    constexpr int HC = DK / 2;   // state columns per epilogue thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
     uint64_t* full = bar + 0;      // [2] stage filled (TMA transaction count)
     uint64_t* empty = bar + 2;     // [2] stage consumed (MMA commit)
-    uint64_t* s_ready = bar + 4;   // state decayed and staged (128 arrivals)
+    uint64_t* s_ready = bar + 4;   // state decayed in TMEM (256 arrivals)
     uint64_t* s_done = bar + 5;    // state MMA of the chunk complete
     uint64_t* sb_free = bar + 6;   // inter MMA complete: bf16 state copy reusable
     uint64_t* o_full = bar + 7;    // [2] O accumulator complete
-    uint64_t* o_empty = bar + 9;   // [2] O accumulator drained (128 arrivals)
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 11);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 12);
+    uint64_t* o_empty = bar + 9;   // [2] O accumulator drained (256 arrivals)
+    uint64_t* sb_ready = bar + 11; // bf16 state copy written (256 arrivals)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 13);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.y, seg = blockIdx.z;
@@ -123,9 +130,9 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1); mbar_init(&full[1], 1);
         mbar_init(&empty[0], 1); mbar_init(&empty[1], 1);
-        mbar_init(s_ready, 128); mbar_init(s_done, 1); mbar_init(sb_free, 1);
+        mbar_init(s_ready, NEPI); mbar_init(s_done, 1); mbar_init(sb_free, 1); mbar_init(sb_ready, NEPI);
         mbar_init(&o_full[0], 1); mbar_init(&o_full[1], 1);
-        mbar_init(&o_empty[0], 128); mbar_init(&o_empty[1], 128);
+        mbar_init(&o_empty[0], NEPI); mbar_init(&o_empty[1], NEPI);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tmap(&tmQ); prefetch_tmap(&tmK); prefetch_tmap(&tmV); prefetch_tmap(&tmA); prefetch_tmap(&tmO);
@@ -154,12 +161,12 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 uint8_t* sb = sm + st * L::STAGE;
                 const uint32_t bytes = L::KB + L::VB + (gated ? L::GB : 0) + (want_out ? L::QB + L::AB : 0);
                 mbar_arrive_expect_tx(&full[st], bytes);
+                if (gated) bulk_load(sb + L::G_OFF, a.gam + ((size_t)bh * a.nchunks + c) * DK, L::GB, &full[st]);
 #pragma unroll
                 for (int i = 0; i < DK / 64; ++i)
                     tma_load_3d(sb + L::K_OFF + i * 8192, &tmK, &full[st], i * 64, c * C, bh);
                 tma_load_3d(sb + L::V_OFF, &tmV, &full[st], dv0, c * C, bh);
                 tma_load_3d(sb + L::V_OFF + 8192, &tmV, &full[st], dv0 + 64, c * C, bh);
-                if (gated) bulk_load(sb + L::G_OFF, a.gam + ((size_t)bh * a.nchunks + c) * DK, L::GB, &full[st]);
                 if (want_out) {
 #pragma unroll
                     for (int i = 0; i < DK / 64; ++i)
@@ -182,7 +189,6 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 const int st = n & 1;
                 bool ok = mbar_wait(&full[st], (n >> 1) & 1, kTimeoutNs);
                 ok = ok && mbar_wait(s_ready, n & 1, kTimeoutNs);
-                if (ok && want_out && n >= 2) ok = mbar_wait(&o_empty[n & 1], ((n >> 1) - 1) & 1, kTimeoutNs);
                 if (!ok) {
                     fail(a.status, abort_flag, ERR_MMA);
                     break;
@@ -197,6 +203,13 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                            sdesc(sK + kk * 2048, 8192, 1024, kSwizzle128), id_state, 1);
                 mma_commit(s_done);
                 if (want_out) {
+                    ok = mbar_wait(sb_ready, n & 1, kTimeoutNs);
+                    if (ok && n >= 2) ok = mbar_wait(&o_empty[n & 1], ((n >> 1) - 1) & 1, kTimeoutNs);
+                    if (!ok) {
+                        fail(a.status, abort_flag, ERR_MMA);
+                        break;
+                    }
+                    tc_fence_after();
                     const uint32_t tO = tO0 + (n & 1) * 64;
                     // inter: O^T = Sb^T (Q (.) Lambda)^T, A (the bf16 state) from TMEM
 #pragma unroll
@@ -214,14 +227,20 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 mma_commit(&empty[st]);
             }
         }
-    } else if (warp < 6) {
-        // ---------------------------------------------------------- state group
+    } else {
+        // ---------------------------------------------------------- epilogue warps (2 groups of 4)
+        // Group g owns state columns [g*DK/2, (g+1)*DK/2) and output rows [g*32, g*32+32)
+        // of every chunk; the warp's TMEM lane quarter is (warp % 4).
+        const int grp = (warp - 2) >> 2;
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const int d = (warp & 3) * 32 + lane;   // dv column within the tile
+        const int cb = grp * HC;                 // first state column of this group
+        const int gt = threadIdx.x - 64 - grp * 128;   // thread index within the group
+        const int bar_grp = BAR_G0 + grp;
         {
             const float* sin = a.S_in ? a.S_in + bh * a.s_in_bh + seg * a.s_in_seg + dv0 + d : nullptr;
 #pragma unroll 1
-            for (int c0 = 0; c0 < DK; c0 += 32) {
+            for (int c0 = cb; c0 < cb + HC; c0 += 32) {
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = sin ? __float_as_uint(sin[(size_t)(c0 + i) * a.dv]) : 0u;
@@ -229,48 +248,106 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             }
             tmem_wait_st();
         }
+        // drain the O accumulator of chunk m: TMEM -> registers -> bf16 smem tile -> TMA store
+        auto drain = [&](int m) -> bool {
+            const int b = m & 1;
+            const bool ok = mbar_wait(&o_full[b], (m >> 1) & 1, kTimeoutNs);
+            if (!group_all_ok(ok, BAR_EPI, NEPI)) return false;
+            tc_fence_after();
+            uint32_t r[32];
+            tmem_ld32(tO0 + b * 64 + lb + grp * 32, r);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&o_empty[b]);
+            // the store issued from this half-buffer two chunks ago must have read it
+            if (gt == 0) bulk_wait_read1();
+            named_bar_sync(bar_grp, 128);
+            uint8_t* tile = sm + L::O_OFF + b * L::OB;
+            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(tile) + (d >> 6) * (C * 64) + grp * 32 * 64 + (d & 63);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) ob[t * 64] = __float2bfloat16_rn(__uint_as_float(r[t]));
+            fence_proxy_async_smem();
+            named_bar_sync(bar_grp, 128);
+            if (gt == 0) {
+                const int c = c_begin + m;
+                tma_store_3d(&tmO, tile + grp * 32 * 64 * 2, dv0, c * C + grp * 32, bh);
+                tma_store_3d(&tmO, tile + C * 64 * 2 + grp * 32 * 64 * 2, dv0 + 64, c * C + grp * 32, bh);
+                bulk_commit();
+            }
+            return true;
+        };
         bool alive = true;
-        for (int n = 0; n < nloc; ++n) {
+        uint32_t P[HC / 2];   // bf16 pairs of S_[n-1] (this thread's columns), kept until the copy is free
+        for (int n = 0; n < nloc && alive; ++n) {
             bool ok = true;
             if (n >= 1) ok = mbar_wait(s_done, (n - 1) & 1, kTimeoutNs);
-            if (ok && want_out && n >= 1) ok = mbar_wait(sb_free, (n - 1) & 1, kTimeoutNs);
             if (ok && gated) ok = mbar_wait(&full[n & 1], (n >> 1) & 1, kTimeoutNs);
-            if (!group_all_ok(ok, BAR_S, 128)) {
-                if (threadIdx.x == 64) fail(a.status, abort_flag, ERR_STATE);
+            if (!group_all_ok(ok, BAR_EPI, NEPI)) {
                 alive = false;
                 break;
             }
             tc_fence_after();
-            const float* g = reinterpret_cast<const float*>(sm + (n & 1) * L::STAGE + L::G_OFF);
-#pragma unroll 1
-            for (int c0 = 0; c0 < DK; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tS + lb + c0, r);
+            const float* g = reinterpret_cast<const float*>(sm + (n & 1) * L::STAGE + L::G_OFF) + cb;
+            // part 1: S <- Diag(gamma_n) S_[n-1] (and keep bf16(S_[n-1]) in registers)
+#pragma unroll
+            for (int c2 = 0; c2 < HC; c2 += 64) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tS + lb + cb + c2, r0);
+                tmem_ld32(tS + lb + cb + c2 + 32, r1);
                 tmem_wait_ld();
                 if (want_out) {
-                    uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    tmem_st16(tSb + lb + c0 / 2, pk);
+                    for (int i = 0; i < 16; ++i) {
+                        P[c2 / 2 + i] = pack_bf16(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                        P[c2 / 2 + 16 + i] = pack_bf16(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+                    }
                 }
                 if (gated) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * g[c0 + i]);
-                    tmem_st32(tS + lb + c0, r);
+                    for (int i = 0; i < 32; ++i) {
+                        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * g[c2 + i]);
+                        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * g[c2 + 32 + i]);
+                    }
+                    tmem_st32(tS + lb + cb + c2, r0);
+                    tmem_st32(tS + lb + cb + c2 + 32, r1);
                 }
+            }
+            if (gated) tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(s_ready);
+            if (!want_out) continue;
+            // part 2: bf16 copy of S_[n-1] for the inter MMA, once the previous one is consumed
+            ok = (n == 0) || mbar_wait(sb_free, (n - 1) & 1, kTimeoutNs);
+            if (!group_all_ok(ok, BAR_EPI, NEPI)) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c2 = 0; c2 < HC; c2 += 32) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = P[c2 / 2 + i];
+                tmem_st16(tSb + lb + (cb + c2) / 2, pk);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(s_ready);
+            mbar_arrive(sb_ready);
+            if (n >= 1 && !drain(n - 1)) {
+                alive = false;
+                break;
+            }
         }
+        if (alive && want_out && nloc > 0 && !drain(nloc - 1)) alive = false;
+        if (!alive && gt == 0) fail(a.status, abort_flag, ERR_EPI);
         if (alive && nloc > 0) {
             const bool ok = mbar_wait(s_done, (nloc - 1) & 1, kTimeoutNs);
-            if (group_all_ok(ok, BAR_S, 128)) {
+            if (group_all_ok(ok, BAR_EPI, NEPI)) {
                 tc_fence_after();
                 if (a.S_out) {
                     float* so = a.S_out + bh * a.s_out_bh + seg * a.s_out_seg + dv0 + d;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < DK; c0 += 32) {
+                    for (int c0 = cb; c0 < cb + HC; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32(tS + lb + c0, r);
                         tmem_wait_ld();
@@ -278,48 +355,11 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                         for (int i = 0; i < 32; ++i) so[(size_t)(c0 + i) * a.dv] = __uint_as_float(r[i]);
                     }
                 }
-            } else if (threadIdx.x == 64) {
-                fail(a.status, abort_flag, ERR_STATE);
+            } else if (gt == 0) {
+                fail(a.status, abort_flag, ERR_EPI);
             }
         }
-    } else if (want_out) {
-        // ---------------------------------------------------------- output group
-        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
-        const int d = (warp & 3) * 32 + lane;
-        const int half = d >> 6, col = d & 63;
-        for (int n = 0; n < nloc; ++n) {
-            const int b = n & 1;
-            const bool ok = mbar_wait(&o_full[b], (n >> 1) & 1, kTimeoutNs);
-            if (!group_all_ok(ok, BAR_O, 128)) {
-                if (threadIdx.x == O_LEADER) fail(a.status, abort_flag, ERR_OUT);
-                break;
-            }
-            tc_fence_after();
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tO0 + b * 64 + lb, r0);
-            tmem_ld32(tO0 + b * 64 + lb + 32, r1);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&o_empty[b]);
-            // the store issued from this buffer two chunks ago must have read it
-            if (threadIdx.x == O_LEADER) bulk_wait_read1();
-            named_bar_sync(BAR_O2, 128);
-            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(sm + L::O_OFF + b * L::OB) + half * (C * 64) + col;
-#pragma unroll
-            for (int t = 0; t < 32; ++t) ob[t * 64] = __float2bfloat16_rn(__uint_as_float(r0[t]));
-#pragma unroll
-            for (int t = 0; t < 32; ++t) ob[(t + 32) * 64] = __float2bfloat16_rn(__uint_as_float(r1[t]));
-            fence_proxy_async_smem();
-            named_bar_sync(BAR_O2, 128);
-            if (threadIdx.x == O_LEADER) {
-                const uint8_t* src = sm + L::O_OFF + b * L::OB;
-                const int c = c_begin + n;
-                tma_store_3d(&tmO, src, dv0, c * C, bh);
-                tma_store_3d(&tmO, src + C * 64 * 2, dv0 + 64, c * C, bh);
-                bulk_commit();
-            }
-        }
-        if (threadIdx.x == O_LEADER) bulk_wait0();
+        if (gt == 0) bulk_wait0();
     }
 
     tc_fence_before();
@@ -330,10 +370,11 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     }
 }
 
-bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, CUtensorMapSwizzle swz) {
+bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, CUtensorMapSwizzle swz,
+          uint32_t rows = 64) {
     uint64_t dims[3] = {d0, d1, d2};
     uint64_t str[2] = {d0 * 2, d0 * d1 * 2};
-    uint32_t box[3] = {64, 64, 1};
+    uint32_t box[3] = {64, rows, 1};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, swz);
 }
 
@@ -360,7 +401,7 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     if (!map3(&mq, qb, p.dk, qrows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     if (!map3(&mk, kb, p.dk, qrows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     if (!map3(&mv, p.v, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    if (!map3(&mo, p.O, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    if (!map3(&mo, p.O, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_NONE, 32)) return cudaErrorInvalidValue;
     {
         uint64_t dims[2] = {64, BH * (uint64_t)pl.nchunks * 64};
         uint64_t str[1] = {128};
