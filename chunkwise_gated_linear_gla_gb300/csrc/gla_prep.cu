@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
+#include "sm100.cuh"
 
 namespace gla {
 namespace {
@@ -55,26 +56,40 @@ struct PrepArgs {
     __nv_bfloat16* Kt;
     float* gam;
     __nv_bfloat16* A;
+    int* status;
     int H, T, nchunks, Tpad, gate;
 };
+
+constexpr uint64_t kCopyTimeoutNs = 2000000000ull;   // bounded wait for the q/k bulk copies
+constexpr int ERR_PREP = 0x201;
 
 template <int DK>
 struct PL {
     static constexpr int NCG = DK / 8;          // column groups of 8
     static constexpr int NRG = NT / NCG;        // row groups
     static constexpr int RPT = C / NRG;         // rows per thread (dk / 32)
-    static constexpr int LD = DK + 8;           // bf16 row stride: keeps mma fragment loads conflict-free
-    static constexpr int QS_OFF = 0;
-    static constexpr int KS_OFF = QS_OFF + C * LD * 2;
-    static constexpr int W_OFF = KS_OFF + C * LD * 2;             // [NPAIR][DK] fp32
+    static constexpr int QS_OFF = 0;                              // [C][DK] bf16, 16-byte chunks XOR-swizzled by row
+    static constexpr int KS_OFF = QS_OFF + C * DK * 2;
+    static constexpr int W_OFF = KS_OFF + C * DK * 2;             // [NPAIR][DK] fp32
     static constexpr int X_OFF = W_OFF + NPAIR * DK * 4;          // [2][NRG][DK] fp32 (totals, then first/last)
     static constexpr int CORR_OFF = X_OFF + 2 * NRG * DK * 4;     // [NSUB][NTRI] fp32
     static constexpr int STEEP_OFF = CORR_OFF + NSUB * NTRI * 4;  // [NSUB][DK] u8
     static constexpr int ANY_OFF = STEEP_OFF + NSUB * DK;         // [NSUB] int
-    static constexpr int SMEM = ANY_OFF + 16;
+    static constexpr int BAR_OFF = (ANY_OFF + 16 + 7) / 8 * 8;    // mbarrier of the q/k bulk copies
+    static constexpr int SMEM = BAR_OFF + 16;
     static_assert(RPT >= 1 && SC % RPT == 0, "a thread's rows lie in one sub-chunk");
-    static_assert(C * ALD * 2 <= 2 * C * LD * 2, "A staging fits in the Q/K tiles");
+    static_assert(DK / 8 >= 8, "swizzle needs at least 8 chunks per row");
+    static_assert(NCG % 8 == 0 || 32 % NCG == 0, "a warp owns whole rows");
+    static_assert(C * ALD * 2 <= 2 * C * DK * 2, "A staging fits in the Q/K tiles");
 };
+
+// Element offset of (row, col) in a [C][DK] bf16 tile whose 16-byte chunks are
+// XOR-swizzled by (row % 8): rows 8 apart share banks, so the mma fragment
+// loads of 8 consecutive rows hit 8 different bank groups.
+template <int DK>
+__device__ __forceinline__ int swz(int row, int col) {
+    return row * DK + ((((col >> 3) ^ (row & 7))) << 3) + (col & 7);
+}
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
@@ -114,10 +129,13 @@ template <int DK>
 __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
 {
     using L = PL<DK>;
-    constexpr int RPT = L::RPT, NRG = L::NRG, LD = L::LD;
+    constexpr int RPT = L::RPT, NRG = L::NRG;
     extern __shared__ __align__(16) uint8_t smem[];
-    __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem + L::QS_OFF);   // [C][LD]  Q (.) exp(Bc - f_j)
-    __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem + L::KS_OFF);   // [C][LD]  K (.) exp(l_u - Bc)
+    // Qs/Ks first receive the raw q/k rows of the chunk (bulk copies), then are
+    // overwritten in place, swizzled, with Q (.) exp(Bc - f_j) and K (.) exp(l_u - Bc).
+    __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem + L::QS_OFF);
+    __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem + L::KS_OFF);
+    uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
     float* W = reinterpret_cast<float*>(smem + L::W_OFF);                     // [NPAIR][DK] exp(f_j - l_u)
     float* X = reinterpret_cast<float*>(smem + L::X_OFF);
     float* corr = reinterpret_cast<float*>(smem + L::CORR_OFF);               // [NSUB][NTRI]
@@ -137,6 +155,19 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
 
     if (tid < NSUB) steep_any[tid] = 0;
     for (int i = tid; i < NSUB * DK; i += NT) steep[i] = 0;
+    if (tid == 0) {
+        sm100::mbar_init(cbar, 1);
+        sm100::mbar_fence_init();
+        const uint32_t bytes = (uint32_t)nr * DK * 2;
+        sm100::mbar_arrive_expect_tx(cbar, 2 * bytes);
+        sm100::bulk_load(Qs, a.q + ((size_t)bh * a.T + t0) * DK, bytes, cbar);
+        sm100::bulk_load(Ks, a.k + ((size_t)bh * a.T + t0) * DK, bytes, cbar);
+    }
+    // rows past the end of the sequence are zero (the copies cover rows < nr only)
+    for (int i = nr * DK / 8 + tid; i < C * DK / 8; i += NT) {
+        reinterpret_cast<uint4*>(Qs)[i] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(Ks)[i] = make_uint4(0, 0, 0, 0);
+    }
 
     // ---- 1. log gates of my rows and their running sum
     float Bc[RPT][8];
@@ -204,14 +235,19 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
         }
         if (any) atomicOr(&steep_any[j], 1);
     }
+    {
+        const bool ok = sm100::mbar_wait(cbar, 0, kCopyTimeoutNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicExch(a.status, ERR_PREP);
+            return;
+        }
+    }
 #pragma unroll
     for (int r = 0; r < RPT; ++r) {
         const int row = row0 + r;
-        uint4 qu = make_uint4(0, 0, 0, 0), ku = qu;
-        if (row < nr) {
-            qu = __ldg(reinterpret_cast<const uint4*>(a.q + ((size_t)bh * a.T + t0 + row) * DK + col0));
-            ku = __ldg(reinterpret_cast<const uint4*>(a.k + ((size_t)bh * a.T + t0 + row) * DK + col0));
-        }
+        const uint4 qu = *reinterpret_cast<const uint4*>(Qs + row * DK + col0);
+        const uint4 ku = *reinterpret_cast<const uint4*>(Ks + row * DK + col0);
+        __syncwarp();   // the warp owns whole rows: all raw reads of this row precede the swizzled writes
         float qv[8], kv[8], qs[8], ks[8];
         unpack8(qu, qv);
         unpack8(ku, kv);
@@ -220,8 +256,8 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
             qs[i] = qv[i] * __expf(Bc[r][i] - f[i]);   // factor <= 1
             ks[i] = kv[i] * __expf(l[i] - Bc[r][i]);   // factor <= 1
         }
-        *reinterpret_cast<uint4*>(Qs + row * LD + col0) = pack8(qs);
-        *reinterpret_cast<uint4*>(Ks + row * LD + col0) = pack8(ks);
+        *reinterpret_cast<uint4*>(Qs + swz<DK>(row, col0)) = pack8(qs);
+        *reinterpret_cast<uint4*>(Ks + swz<DK>(row, col0)) = pack8(ks);
         if (gated) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -288,20 +324,20 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
         while ((jb + 1) * (jb + 2) / 2 <= blk) ++jb;
         const int ub = blk - jb * (jb + 1) / 2;
         const float* w = W + blk * DK;
-        const __nv_bfloat16* qa = Qs + (jb * SC + g8) * LD + 2 * c4;
+        const int ra = jb * SC + g8;   // fragment rows ra and ra + 8 (same row % 8)
 #pragma unroll 4
         for (int k0 = 0; k0 < DK; k0 += 16) {
-            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(qa + k0);
-            const uint32_t a1 = *reinterpret_cast<const uint32_t*>(qa + 8 * LD + k0);
-            const uint32_t a2 = *reinterpret_cast<const uint32_t*>(qa + k0 + 8);
-            const uint32_t a3 = *reinterpret_cast<const uint32_t*>(qa + 8 * LD + k0 + 8);
+            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(Qs + swz<DK>(ra, k0 + 2 * c4));
+            const uint32_t a1 = *reinterpret_cast<const uint32_t*>(Qs + swz<DK>(ra + 8, k0 + 2 * c4));
+            const uint32_t a2 = *reinterpret_cast<const uint32_t*>(Qs + swz<DK>(ra, k0 + 8 + 2 * c4));
+            const uint32_t a3 = *reinterpret_cast<const uint32_t*>(Qs + swz<DK>(ra + 8, k0 + 8 + 2 * c4));
             const float2 w01 = *reinterpret_cast<const float2*>(w + k0 + 2 * c4);
             const float2 w89 = *reinterpret_cast<const float2*>(w + k0 + 2 * c4 + 8);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const __nv_bfloat16* kb = Ks + (ub * SC + nt * 8 + g8) * LD + 2 * c4 + k0;
-                uint32_t b0 = *reinterpret_cast<const uint32_t*>(kb);
-                uint32_t b1 = *reinterpret_cast<const uint32_t*>(kb + 8);
+                const int rb = ub * SC + nt * 8 + g8;
+                uint32_t b0 = *reinterpret_cast<const uint32_t*>(Ks + swz<DK>(rb, k0 + 2 * c4));
+                uint32_t b1 = *reinterpret_cast<const uint32_t*>(Ks + swz<DK>(rb, k0 + 8 + 2 * c4));
                 if (gated) {
                     b0 = scale_bf16x2(b0, w01.x, w01.y);
                     b1 = scale_bf16x2(b1, w89.x, w89.y);
@@ -366,7 +402,6 @@ cudaError_t launch_prep_dk(const PrepArgs& a, dim3 grid, cudaStream_t s)
 
 cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s)
 {
-    (void)status;
     uint8_t* base = static_cast<uint8_t*>(ws);
     PrepArgs a;
     a.q = static_cast<const __nv_bfloat16*>(p.q);
@@ -376,6 +411,7 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     a.Kt = pl.raw_qk ? nullptr : reinterpret_cast<__nv_bfloat16*>(base + pl.off_kt);
     a.gam = reinterpret_cast<float*>(base + pl.off_gam);
     a.A = reinterpret_cast<__nv_bfloat16*>(base + pl.off_A);
+    a.status = status;
     a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
     dim3 grid(pl.nchunks, p.B * p.H);
     switch (p.dk) {
