@@ -148,6 +148,7 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     pl.Tpad = pl.nchunks * kChunk;
     pl.n_dvt = p->dv / kDvTile;
     pl.raw_qk = (p->gate == GLA_GATE_NONE);
+    pl.sms = sms;
     const int units = p->B * p->H * pl.n_dvt;
     pl.nseg = choose_segments(p, units, pl.nchunks, sms > 0 ? sms : 148);
     pl.chunks_per_seg = (pl.nchunks + pl.nseg - 1) / pl.nseg;

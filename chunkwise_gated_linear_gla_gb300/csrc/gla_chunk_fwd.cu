@@ -173,6 +173,26 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                         tma_load_3d(sb + L::Q_OFF + i * 8192, &tmQ, &full[st], i * 64, c * C, bh);
                     tma_load_2d(sb + L::A_OFF, &tmA, &full[st], 0, (bh * a.nchunks + c) * C);
                 }
+                // L2 prefetch two chunks ahead, beyond what the two shared-memory stages
+                // hold; the tiles all dv-tile CTAs of this head share are split among them
+                const int cp = c + 2;
+                if (cp < c_end) {
+                    prefetch_l2_tile_3d(&tmV, dv0, cp * C, bh);
+                    prefetch_l2_tile_3d(&tmV, dv0 + 64, cp * C, bh);
+                    const int nt = gridDim.x, me = blockIdx.x;
+                    int item = 0;
+#pragma unroll
+                    for (int i = 0; i < DK / 64; ++i, ++item)
+                        if (item % nt == me) prefetch_l2_tile_3d(&tmK, i * 64, cp * C, bh);
+                    if (want_out) {
+#pragma unroll
+                        for (int i = 0; i < DK / 64; ++i, ++item)
+                            if (item % nt == me) prefetch_l2_tile_3d(&tmQ, i * 64, cp * C, bh);
+                        if (item % nt == me) prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
+                        ++item;
+                    }
+                    if (gated && item % nt == me) prefetch_l2(a.gam + ((size_t)bh * a.nchunks + cp) * DK, L::GB);
+                }
                 issued = n + 1;
             }
             // no copy may land after the CTA exits: wait for the last fills

@@ -33,6 +33,7 @@ struct Plan {
     int nseg = 1;          // sequence segments per (b,h)
     int chunks_per_seg = 0;
     bool raw_qk = false;   // tensor path reads q,k directly (no gate)
+    int sms = 0;           // multiprocessors of the device the plan was made for
     // workspace layout (byte offsets from the workspace base)
     size_t off_qt = 0, off_kt = 0, off_A = 0, off_gam = 0, off_segS = 0, off_segin = 0;
     size_t ws_bytes = 0;

@@ -57,7 +57,7 @@ struct PrepArgs {
     float* gam;
     __nv_bfloat16* A;
     int* status;
-    int H, T, nchunks, Tpad, gate;
+    int BH, H, T, nchunks, Tpad, gate;
 };
 
 constexpr uint64_t kCopyTimeoutNs = 2000000000ull;   // bounded wait for the q/k bulk copies
@@ -144,7 +144,16 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
     __nv_bfloat16* As = Qs;                                                   // [C][ALD], after the MMAs
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int c = blockIdx.x, bh = blockIdx.y, h = bh % a.H;
+    if (tid == 0) {
+        sm100::mbar_init(cbar, 1);
+        sm100::mbar_fence_init();
+    }
+    __syncthreads();
+    // Persistent: work items (b*H+h, chunk) in order, strided by the grid. While
+    // one item is computed, the next one's rows are prefetched into L2.
+    const int total = a.BH * a.nchunks;
+    for (int item = blockIdx.x, it = 0; item < total; item += gridDim.x, ++it) {
+    const int c = item % a.nchunks, bh = item / a.nchunks, h = bh % a.H;
     const int t0 = c * C;
     const int nr = min(C, a.T - t0);
     const bool gated = a.gate != GLA_GATE_NONE;
@@ -156,12 +165,18 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
     if (tid < NSUB) steep_any[tid] = 0;
     for (int i = tid; i < NSUB * DK; i += NT) steep[i] = 0;
     if (tid == 0) {
-        sm100::mbar_init(cbar, 1);
-        sm100::mbar_fence_init();
         const uint32_t bytes = (uint32_t)nr * DK * 2;
         sm100::mbar_arrive_expect_tx(cbar, 2 * bytes);
         sm100::bulk_load(Qs, a.q + ((size_t)bh * a.T + t0) * DK, bytes, cbar);
         sm100::bulk_load(Ks, a.k + ((size_t)bh * a.T + t0) * DK, bytes, cbar);
+        const int nx = item + gridDim.x;
+        if (nx < total) {
+            const int c2 = nx % a.nchunks, bh2 = nx / a.nchunks, nr2 = min(C, a.T - c2 * C);
+            const size_t row = (size_t)bh2 * a.T + (size_t)c2 * C;
+            sm100::prefetch_l2(a.q + row * DK, (uint32_t)nr2 * DK * 2);
+            sm100::prefetch_l2(a.k + row * DK, (uint32_t)nr2 * DK * 2);
+            if (a.gate == GLA_GATE_PER_KEY) sm100::prefetch_l2(a.log_g + row * DK, (uint32_t)nr2 * DK * 4);
+        }
     }
     // rows past the end of the sequence are zero (the copies cover rows < nr only)
     for (int i = nr * DK / 8 + tid; i < C * DK / 8; i += NT) {
@@ -236,7 +251,7 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
         if (any) atomicOr(&steep_any[j], 1);
     }
     {
-        const bool ok = sm100::mbar_wait(cbar, 0, kCopyTimeoutNs);
+        const bool ok = sm100::mbar_wait(cbar, it & 1, kCopyTimeoutNs);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) atomicExch(a.status, ERR_PREP);
             return;
@@ -386,12 +401,16 @@ __global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
         const int r = idx / (C / 8), s = (idx % (C / 8)) * 8;
         *reinterpret_cast<uint4*>(Ao + r * C + s) = *reinterpret_cast<const uint4*>(As + r * ALD + s);
     }
+    __syncthreads();   // shared tiles are refilled by the next item
+    }
 }
 
 template <int DK>
-cudaError_t launch_prep_dk(const PrepArgs& a, dim3 grid, cudaStream_t s)
+cudaError_t launch_prep_dk(const PrepArgs& a, int sms, cudaStream_t s)
 {
     using L = PL<DK>;
+    const int total = a.BH * a.nchunks;
+    const dim3 grid(total < 2 * sms ? total : 2 * sms);   // two resident CTAs per SM
     cudaError_t e = cudaFuncSetAttribute(gla_chunk_prep_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
     gla_chunk_prep_kernel<DK><<<grid, NT, L::SMEM, s>>>(a);
@@ -412,12 +431,12 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     a.gam = reinterpret_cast<float*>(base + pl.off_gam);
     a.A = reinterpret_cast<__nv_bfloat16*>(base + pl.off_A);
     a.status = status;
-    a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
-    dim3 grid(pl.nchunks, p.B * p.H);
+    a.BH = p.B * p.H; a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
+    const int sms = pl.sms > 0 ? pl.sms : 148;
     switch (p.dk) {
-    case 64: return launch_prep_dk<64>(a, grid, s);
-    case 128: return launch_prep_dk<128>(a, grid, s);
-    case 256: return launch_prep_dk<256>(a, grid, s);
+    case 64: return launch_prep_dk<64>(a, sms, s);
+    case 128: return launch_prep_dk<128>(a, sms, s);
+    case 256: return launch_prep_dk<256>(a, sms, s);
     }
     return cudaErrorInvalidValue;
 }
