@@ -161,6 +161,21 @@ class Clocks:
         return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x, dist=None, device=None):
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, step_ms):
+    """Whole-job throughput: every rank processes its own batch (weak scaling)."""
+    return tokens_per_rank * world / (step_ms * 1e-3)
+
+
 def run_reference(args, w):
     """The oracle (fp64 recurrence, C, all host cores) on a bounded sample of the workload."""
     import oracle
@@ -294,10 +309,7 @@ def main():
         step_ms += evs[0].elapsed_time(evs[nst])
     stage_ms = [t / args.steps for t in stage_ms]
     step_ms /= args.steps
-    t = torch.tensor([step_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, dist, dev)
 
     # end to end through gla_fwd with host buffers
     hq, hk, hv, hg, hs = (x[n].pin_memory() for n in ("q", "k", "v", "log_g", "S0"))
@@ -322,10 +334,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    te = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     if rank != 0:
         if world > 1:
@@ -334,7 +343,7 @@ def main():
     hbm, bf16, bf16_sus, src = peaks()
     flops, byts = algorithmic(w)
     tokens = w.B * w.T * world
-    value = tokens / (step_ms * 1e-3)
+    value = job_tokens_per_s(w.B * w.T, world, step_ms)
     tflops = flops * world / (step_ms * 1e-3) / 1e12
     dom = max(range(nst), key=lambda i: stage_ms[i])
     dname = names[dom]
