@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload to time (default: the 1.3B-shaped GLA layer the metric is quoted on)")
+    ap.add_argument("--segments", type=int, default=0, help="force the sequence split (0: planner decides)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-rows", type=int, default=8,
                     help="batch rows of the workload the oracle runs for cpu_baseline")
@@ -59,6 +62,11 @@ def peaks():
         return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
 
 
+def workload(args):
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    return gi.WORKLOADS[args.workload]
+
+
 def algorithmic(w):
     """Algorithmic FLOPs and bytes of one forward pass of workload w (per rank).
 
@@ -67,23 +75,54 @@ def algorithmic(w):
     Bytes: q, k, v read and O written once (e bytes each element), the fp32
     per-key log gate read once, S0 read and S_T written once (fp32).
     """
-    e = 2
+    import torch
+    e = 2 if w.dtype == torch.bfloat16 else 4
     BH, T, dk, dv, C = w.B * w.H, w.T, w.dk, w.dv, w.chunk
+    gate_bytes = 4 * dk if w.gate == 2 else 0
     flops = BH * T * (4 * dk * dv + (C + 1) * (dk + dv))
-    byts = BH * T * (e * (2 * dk + dv) + e * dv + 4 * dk) + BH * dk * dv * 4 * (2 if w.s0_std > 0 else 1)
+    byts = BH * T * (e * (2 * dk + dv) + e * dv + gate_bytes) + BH * dk * dv * 4 * (2 if w.s0_std > 0 else 1)
     return flops, byts
 
 
-def stage_bytes(w, name):
-    """Compulsory bytes one launch of a stage moves (each operand once), bf16 e=2."""
+def stage_bytes(w, name, nseg=1):
+    """Compulsory bytes one launch of a stage moves (each operand once, bf16 tiles).
+
+    Qt/Kt (Q (.) Lambda, K (.) Gamma) exist only with a gate; without one the
+    chunk pass reads q and k directly. S0/S_T are counted when present.
+    """
     BH, T, dk, dv, C = w.B * w.H, w.T, w.dk, w.dv, w.chunk
     nch = (T + C - 1) // C
     Tp = nch * C
+    gated = w.gate != 0
+    gate_in = T * dk * 4 if w.gate == 2 else 0
+    s0 = BH * dk * dv * 4 if w.s0_std > 0 else 0
+    st = BH * dk * dv * 4
+    qk_tiles = (Tp if gated else T) * dk * 2 * 2
+    gam = nch * dk * 4 if gated else 0
     if name == "gla_chunk_prep":
-        return BH * (T * dk * 2 * 2 + T * dk * 4 + Tp * dk * 2 * 2 + nch * C * C * 2 + nch * dk * 4)
+        return BH * (T * dk * 2 * 2 + gate_in + (Tp * dk * 2 * 2 if gated else 0) + nch * C * C * 2 + gam)
     if name == "gla_chunk_fwd":
-        return BH * (Tp * dk * 2 * 2 + nch * C * C * 2 + nch * dk * 4 + T * dv * 2 * 2) + BH * dk * dv * 4 * 2
+        last_state = (s0 + st) if nseg == 1 else BH * nseg * dk * dv * 4
+        return BH * (qk_tiles + nch * C * C * 2 + gam + T * dv * 2 * 2) + last_state
+    if name == "gla_chunk_state":
+        return BH * (qk_tiles // 2 + gam + T * dv * 2) + BH * nseg * dk * dv * 4
+    if name == "gla_state_scan":
+        return 2 * BH * nseg * dk * dv * 4 + s0 + st + BH * nch * dk * 4 * (1 if gated else 0)
     return 0
+
+
+def planned_segments(w, force, sms):
+    """Segments per (b,h) the library's planner picks (same rule as csrc/gla_api.cu)."""
+    nch = (w.T + w.chunk - 1) // w.chunk
+    units = w.B * w.H * (w.dv // 128)
+    if force > 0:
+        n = min(force, nch)
+    elif units * 2 > sms or nch < 16:
+        n = 1
+    else:
+        n = max(1, min(sms // units, nch // 8))
+    cps = (nch + n - 1) // n
+    return (nch + cps - 1) // cps
 
 
 def kernel_source_sha(name):
@@ -232,7 +271,7 @@ def cpu_baseline(w, rows):
 def main():
     args = parse()
     from chunkwise_gated_linear_gla_gb300 import inputs as gi
-    w = gi.WORKLOADS[WORKLOAD]
+    w = workload(args)
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -263,10 +302,11 @@ def main():
     x = gi.make_inputs(w, seed=rank)
     dev = torch.device("cuda", local)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-    g, S0 = x["log_g"].to(dev), x["S0"].to(dev)
-    O = torch.empty((w.B, w.H, w.T, w.dv), dtype=torch.bfloat16, device=dev)
+    g = None if x["log_g"] is None else x["log_g"].to(dev)
+    S0 = None if x["S0"] is None else x["S0"].to(dev)
+    O = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev)
     ST = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
-    p = bnd.make_params(q, k, v, g, S0, O, ST)
+    p = bnd.make_params(q, k, v, g, S0, O, ST, force_segments=args.segments)
     nbytes = bnd.gla_fwd_workspace_size(p)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), nbytes
@@ -317,16 +357,22 @@ def main():
     step_ms = max_over_ranks(step_ms, dist, dev)
 
     # end to end through gla_fwd with host buffers
-    hq, hk, hv, hg, hs = (x[n].pin_memory() for n in ("q", "k", "v", "log_g", "S0"))
+    pairs = [(x[n].pin_memory(), d) for n, d in (("q", q), ("k", k), ("v", v), ("log_g", g), ("S0", S0))
+             if x[n] is not None]
     hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
     hST = torch.empty(ST.shape, dtype=ST.dtype).pin_memory()
-    h2d = sum(tt.numel() * tt.element_size() for tt in (hq, hk, hv, hg, hs))
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
     d2h = hO.numel() * hO.element_size() + hST.numel() * hST.element_size()
+    # the spec call takes bf16 with a per-key gate or none; other workloads go through gla_fwd_ex
+    use_fwd = w.dtype == torch.bfloat16 and w.gate in (0, 2) and args.segments == 0
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True); k.copy_(hk, non_blocking=True); v.copy_(hv, non_blocking=True)
-        g.copy_(hg, non_blocking=True); S0.copy_(hs, non_blocking=True)
-        bnd.gla_fwd(q, k, v, g, S0, O, ST, w.B, w.H, w.T, w.dk, w.dv, 64, stream)
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
+        if use_fwd:
+            bnd.gla_fwd(q, k, v, g, S0, O, ST, w.B, w.H, w.T, w.dk, w.dv, 64, stream)
+        else:
+            bnd.gla_fwd_ex(p, stream)
         hO.copy_(O, non_blocking=True); hST.copy_(ST, non_blocking=True)
 
     for _ in range(max(2, args.warmup)):
@@ -352,14 +398,19 @@ def main():
     tflops = flops * world / (step_ms * 1e-3) / 1e12
     dom = max(range(nst), key=lambda i: stage_ms[i])
     dname = names[dom]
-    dbytes = stage_bytes(w, dname)
+    nseg = planned_segments(w, args.segments, torch.cuda.get_device_properties(dev).multi_processor_count) \
+        if "gla_chunk_state" in names else 1
+    dbytes = stage_bytes(w, dname, nseg)
     ach = dbytes / (stage_ms[dom] * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shapes and distributions of the workload)",
-        "config": {"workload": f"{w.name}: GLA layer B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv} chunk=64, "
-                               "per-key log gate, S0 given", "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": {"workload": f"{w.name}: {w.notes}, B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv} chunk=64, "
+                               f"gate={['none', 'per-head scalar', 'per-key'][w.gate]}, "
+                               f"S0={'given' if w.s0_std > 0 else 'zero'}",
+                   "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "segments": nseg,
                    "l2": "flushed between steps (256 MB write, outside the timed events)",
                    "stages": names, "stage_ms": stage_ms},
         "tflops": tflops, "tflops_frac_bf16_peak": tflops / bf16,
