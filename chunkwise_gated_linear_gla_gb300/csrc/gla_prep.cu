@@ -125,8 +125,13 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return u;
 }
 
+// Resident CTAs per SM: the kernel is latency-bound, so smaller heads run three
+// CTAs per SM (shared memory allows it; registers are bounded to fit).
 template <int DK>
-__global__ void __launch_bounds__(NT, 2) gla_chunk_prep_kernel(PrepArgs a)
+constexpr int prep_ctas_per_sm() { return DK <= 128 ? 3 : 2; }
+
+template <int DK>
+__global__ void __launch_bounds__(NT, prep_ctas_per_sm<DK>()) gla_chunk_prep_kernel(PrepArgs a)
 {
     using L = PL<DK>;
     constexpr int RPT = L::RPT, NRG = L::NRG;
@@ -410,7 +415,8 @@ cudaError_t launch_prep_dk(const PrepArgs& a, int sms, cudaStream_t s)
 {
     using L = PL<DK>;
     const int total = a.BH * a.nchunks;
-    const dim3 grid(total < 2 * sms ? total : 2 * sms);   // two resident CTAs per SM
+    const int resident = prep_ctas_per_sm<DK>() * sms;
+    const dim3 grid(total < resident ? total : resident);
     cudaError_t e = cudaFuncSetAttribute(gla_chunk_prep_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
     gla_chunk_prep_kernel<DK><<<grid, NT, L::SMEM, s>>>(a);
