@@ -410,6 +410,173 @@ __global__ void __launch_bounds__(NT, prep_ctas_per_sm<DK>()) gla_chunk_prep_ker
     }
 }
 
+// Uniform gates (none, or one fixed decay lambda per head): the cumulative log
+// gate of row r in a chunk is (r+1) log(lambda) for every key, so Lambda, Gamma
+// and gamma are per-row scalars and the intra-chunk scores have the closed
+// form P_rs = (q_r . k_s) lambda^(r-s), r >= s (the decay mask M_ij =
+// lambda^(i-j) of "Lightning Attention-2", §3.2.1 Alg. 1). The scores are one
+// plain q k^T product per 16-row block (mma.sync) scaled in the epilogue; no
+// per-element exponentials and no steep-gate fallback are needed.
+template <int DK>
+constexpr int prep_uniform_ctas_per_sm() { return DK <= 128 ? 4 : 3; }
+
+template <int DK>
+__global__ void __launch_bounds__(NT, prep_uniform_ctas_per_sm<DK>()) gla_chunk_prep_uniform_kernel(PrepArgs a)
+{
+    using L = PL<DK>;
+    constexpr int RPT = L::RPT;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem);      // [C][DK], raw q, swizzled
+    __nv_bfloat16* Ks = Qs + C * DK;                                   // [C][DK], raw k, swizzled
+    uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + 2 * C * DK * 2);
+    __nv_bfloat16* As = Qs;                                            // [C][ALD], after the MMAs
+
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    if (tid == 0) {
+        sm100::mbar_init(cbar, 1);
+        sm100::mbar_fence_init();
+    }
+    __syncthreads();
+    const int total = a.BH * a.nchunks;
+    const bool gated = a.gate != GLA_GATE_NONE;
+    for (int item = blockIdx.x, it = 0; item < total; item += gridDim.x, ++it) {
+    const int c = item % a.nchunks, bh = item / a.nchunks, h = bh % a.H;
+    const int t0 = c * C;
+    const int nr = min(C, a.T - t0);
+    const float lam = gated ? a.log_g[h] : 0.f;   // log(lambda_h) <= 0
+    const int cg = tid % L::NCG, rg = tid / L::NCG;
+    const int col0 = cg * 8, row0 = rg * RPT;
+
+    if (tid == 0) {
+        const uint32_t bytes = (uint32_t)nr * DK * 2;
+        sm100::mbar_arrive_expect_tx(cbar, 2 * bytes);
+        sm100::bulk_load(Qs, a.q + ((size_t)bh * a.T + t0) * DK, bytes, cbar);
+        sm100::bulk_load(Ks, a.k + ((size_t)bh * a.T + t0) * DK, bytes, cbar);
+        const int nx = item + gridDim.x;
+        if (nx < total) {
+            const int c2 = nx % a.nchunks, bh2 = nx / a.nchunks, nr2 = min(C, a.T - c2 * C);
+            const size_t row = (size_t)bh2 * a.T + (size_t)c2 * C;
+            sm100::prefetch_l2(a.q + row * DK, (uint32_t)nr2 * DK * 2);
+            sm100::prefetch_l2(a.k + row * DK, (uint32_t)nr2 * DK * 2);
+        }
+    }
+    for (int i = nr * DK / 8 + tid; i < C * DK / 8; i += NT) {
+        reinterpret_cast<uint4*>(Qs)[i] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(Ks)[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (gated && tid < DK) a.gam[((size_t)bh * a.nchunks + c) * DK + tid] = __expf(nr * lam);
+    {
+        const bool ok = sm100::mbar_wait(cbar, it & 1, kCopyTimeoutNs);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicExch(a.status, ERR_PREP);
+            return;
+        }
+    }
+    // swizzle in place for the fragment loads; Q (.) Lambda and K (.) Gamma with per-row factors
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int row = row0 + r;
+        const uint4 qu = *reinterpret_cast<const uint4*>(Qs + row * DK + col0);
+        const uint4 ku = *reinterpret_cast<const uint4*>(Ks + row * DK + col0);
+        __syncwarp();   // the warp owns whole rows: all raw reads of this row precede the swizzled writes
+        *reinterpret_cast<uint4*>(Qs + swz<DK>(row, col0)) = qu;
+        *reinterpret_cast<uint4*>(Ks + swz<DK>(row, col0)) = ku;
+        if (gated) {
+            const bool valid = row < nr;
+            const float lq = valid ? __expf((row + 1) * lam) : 0.f;       // b_row / b_start
+            const float lk = valid ? __expf((nr - 1 - row) * lam) : 0.f;  // b_end / b_row
+            float qv[8], kv[8];
+            unpack8(qu, qv);
+            unpack8(ku, kv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                qv[i] *= lq;
+                kv[i] *= lk;
+            }
+            *reinterpret_cast<uint4*>(a.Qt + ((size_t)bh * a.Tpad + t0 + row) * DK + col0) = pack8(qv);
+            *reinterpret_cast<uint4*>(a.Kt + ((size_t)bh * a.Tpad + t0 + row) * DK + col0) = pack8(kv);
+        }
+    }
+    __syncthreads();
+
+    // lower blocks of q k^T on the tensor cores, scaled by lambda^(r-s) and masked
+    const int g8 = lane / 4, c4 = lane % 4;
+    float acc[2][2][4];
+#pragma unroll
+    for (int bi = 0; bi < 2; ++bi) {
+        const int blk = warp + bi * NWARP;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[bi][nt][e] = 0.f;
+        if (blk >= NPAIR) continue;
+        int jb = 0;
+        while ((jb + 1) * (jb + 2) / 2 <= blk) ++jb;
+        const int ub = blk - jb * (jb + 1) / 2;
+        const int ra = jb * SC + g8;
+#pragma unroll 4
+        for (int k0 = 0; k0 < DK; k0 += 16) {
+            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(Qs + swz<DK>(ra, k0 + 2 * c4));
+            const uint32_t a1 = *reinterpret_cast<const uint32_t*>(Qs + swz<DK>(ra + 8, k0 + 2 * c4));
+            const uint32_t a2 = *reinterpret_cast<const uint32_t*>(Qs + swz<DK>(ra, k0 + 8 + 2 * c4));
+            const uint32_t a3 = *reinterpret_cast<const uint32_t*>(Qs + swz<DK>(ra + 8, k0 + 8 + 2 * c4));
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int rb = ub * SC + nt * 8 + g8;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(Ks + swz<DK>(rb, k0 + 2 * c4));
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(Ks + swz<DK>(rb, k0 + 8 + 2 * c4));
+                mma_bf16_16816(acc[bi][nt], a0, a1, a2, a3, b0, b1);
+            }
+        }
+    }
+    __syncthreads();   // every warp is done reading Qs/Ks; As reuses that space
+#pragma unroll
+    for (int bi = 0; bi < 2; ++bi) {
+        const int blk = warp + bi * NWARP;
+        if (blk >= NPAIR) continue;
+        int jb = 0;
+        while ((jb + 1) * (jb + 2) / 2 <= blk) ++jb;
+        const int ub = blk - jb * (jb + 1) / 2;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = jb * SC + g8 + hr * 8;
+                const int s0 = ub * SC + nt * 8 + 2 * c4;
+                float v0 = acc[bi][nt][hr * 2 + 0], v1 = acc[bi][nt][hr * 2 + 1];
+                v0 = (s0 <= r) ? (gated ? v0 * __expf((r - s0) * lam) : v0) : 0.f;
+                v1 = (s0 + 1 <= r) ? (gated ? v1 * __expf((r - s0 - 1) * lam) : v1) : 0.f;
+                *reinterpret_cast<__nv_bfloat162*>(As + r * ALD + s0) = __floats2bfloat162_rn(v0, v1);
+            }
+    }
+    for (int idx = tid; idx < C * C / 2; idx += NT) {
+        const int r = idx / (C / 2), s2 = (idx % (C / 2)) * 2;
+        if (s2 / SC > r / SC) *reinterpret_cast<uint32_t*>(As + r * ALD + s2) = 0u;
+    }
+    __syncthreads();
+    __nv_bfloat16* Ao = a.A + ((size_t)bh * a.nchunks + c) * C * C;
+    for (int idx = tid; idx < C * C / 8; idx += NT) {
+        const int r = idx / (C / 8), s2 = (idx % (C / 8)) * 8;
+        *reinterpret_cast<uint4*>(Ao + r * C + s2) = *reinterpret_cast<const uint4*>(As + r * ALD + s2);
+    }
+    __syncthreads();   // shared tiles are refilled by the next item
+    }
+}
+
+template <int DK>
+cudaError_t launch_prep_uniform_dk(const PrepArgs& a, int sms, cudaStream_t s)
+{
+    const int smem = 2 * C * DK * 2 + 16;
+    const int total = a.BH * a.nchunks;
+    const int resident = prep_uniform_ctas_per_sm<DK>() * sms;
+    const dim3 grid(total < resident ? total : resident);
+    cudaError_t e = cudaFuncSetAttribute(gla_chunk_prep_uniform_kernel<DK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    gla_chunk_prep_uniform_kernel<DK><<<grid, NT, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int DK>
 cudaError_t launch_prep_dk(const PrepArgs& a, int sms, cudaStream_t s)
 {
@@ -439,6 +606,14 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     a.status = status;
     a.BH = p.B * p.H; a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
     const int sms = pl.sms > 0 ? pl.sms : 148;
+    if (p.gate != GLA_GATE_PER_KEY) {
+        switch (p.dk) {
+        case 64: return launch_prep_uniform_dk<64>(a, sms, s);
+        case 128: return launch_prep_uniform_dk<128>(a, sms, s);
+        case 256: return launch_prep_uniform_dk<256>(a, sms, s);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (p.dk) {
     case 64: return launch_prep_dk<64>(a, sms, s);
     case 128: return launch_prep_dk<128>(a, sms, s);
