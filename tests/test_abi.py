@@ -140,3 +140,24 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(bnd._build, "LIB", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="not built"):
         bnd.load()
+
+
+def test_bench_segment_rule_matches_library_plan():
+    """bench.py mirrors the library's segment rule to count bytes; the workspace the
+    library plans (which holds two fp32 states per segment) must agree with it."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    for name in ("linear_attn", "scalar_decay", "gla_1p3b", "gla_long"):
+        w = gi.WORKLOADS[name]
+        p = _params(B=w.B, H=w.H, T=w.T, dk=w.dk, dv=w.dv, gate=w.gate,
+                    log_g=None if w.gate == 0 else 0x40000000, q=0x100000000, k=0x200000000,
+                    v=0x300000000, O=0x400000000)
+        nseg = bench.planned_segments(w, 0, 148)   # the library plans for 148 SMs without a device
+        BH = w.B * w.H
+        nch = (w.T + 63) // 64
+        base = (0 if w.gate == 0 else 2 * BH * nch * 64 * w.dk * 2) + BH * nch * 64 * 64 * 2 + BH * nch * w.dk * 4
+        seg = 2 * BH * nseg * w.dk * w.dv * 4 if nseg > 1 else 0
+        got = bnd.gla_fwd_workspace_size(p)
+        assert abs(got - (base + seg)) < 4096, (name, got, base + seg, nseg)

@@ -220,3 +220,43 @@ def test_full_gla_1p3b_sampled():
 
 def test_full_gla_long_sampled():
     _sampled("gla_long", [(0, 0), (0, 3)])
+
+
+# ---------------------------------------------------------------- degenerate and extreme shapes
+
+def test_zero_per_key_gate_equals_no_gate():
+    """log alpha = 0 through the per-key path is causal linear attention."""
+    w = gi.Workload("t", B=1, H=2, T=200, dk=128, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY,
+                    gate_dist="zero", s0_std=0.05)
+    x = gi.make_inputs(w, seed=21)
+    c = _dev(x)
+    O1, S1 = gla.forward(c["q"], c["k"], c["v"], c["log_g"], c["S0"], path=gla.GLA_PATH_TENSOR)
+    O2, S2 = gla.forward(c["q"], c["k"], c["v"], None, c["S0"], path=gla.GLA_PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert_close(to_np(O1), to_np(O2), torch.bfloat16, "O per-key zero gate vs no gate")
+    Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], None, gi.GATE_NONE, x["S0"])
+    assert_close(to_np(O1), Oref, torch.bfloat16, "O")
+    assert_close(to_np(S1), STref, torch.bfloat16, "ST")
+
+
+def test_wide_dv_eight_tiles():
+    w = gi.Workload("t", B=1, H=1, T=257, dk=128, dv=1024, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY, s0_std=0.02)
+    _check_full(w, seed=22)
+
+
+def test_many_small_heads():
+    w = gi.Workload("t", B=32, H=8, T=70, dk=64, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY, s0_std=0.02)
+    _check_full(w, seed=23)
+
+
+def test_steep_scalar_decay():
+    """lambda = e^-30: the closed-form scores lambda^(r-s) underflow to zero off the diagonal."""
+    w = gi.Workload("t", B=1, H=2, T=150, dk=64, dv=128, dtype=torch.bfloat16, gate=gi.GATE_HEAD_SCALAR, s0_std=0.1)
+    x = gi.make_inputs(w, seed=24)
+    x["log_g"] = torch.tensor([-30.0, -0.5], dtype=torch.float32)
+    c = _dev(x)
+    O, ST = gla.forward(c["q"], c["k"], c["v"], c["log_g"], c["S0"], path=gla.GLA_PATH_TENSOR)
+    torch.cuda.synchronize()
+    Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
+    assert_close(to_np(O), Oref, torch.bfloat16, "O")
+    assert_close(to_np(ST), STref, torch.bfloat16, "ST")
