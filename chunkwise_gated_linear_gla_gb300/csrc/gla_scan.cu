@@ -8,15 +8,20 @@
 // the state correction of the FlashQLA talk ("core technical principles":
 // a wrongly started segment is fixed by one matrix per rank), which for a
 // diagonal gate collapses from a dk x dk matrix to the vector Gamma_s. With
-// S_in(0) = S0 this also yields S_T = S_in(nseg). One CTA handles 8 rows of
-// the state of one (b,h) for all dv columns.
+// S_in(0) = S0 this also yields S_T = S_in(nseg).
+//
+// One CTA covers 256 consecutive state elements of one (b,h) (they share a
+// key row k when dv >= 256, else two rows); one thread per element. The
+// per-segment decays of the CTA's rows are formed first (one warp per
+// (row, segment), a product over that segment's chunks); then each thread
+// runs the recurrence with the loads of the next segments already in flight.
 #include "gla_internal.h"
 
 namespace gla {
 namespace {
 
-constexpr int ROWS = 8;
 constexpr int NT = 256;
+constexpr int AHEAD = 4;   // segment loads kept in flight per thread
 
 struct ScanArgs {
     const float* S0;     // [BH][dk][dv] or null
@@ -29,31 +34,49 @@ struct ScanArgs {
 
 __global__ void __launch_bounds__(NT) gla_state_scan_kernel(ScanArgs a)
 {
-    extern __shared__ float Gs[];   // [nseg][ROWS]
-    const int bh = blockIdx.x, k0 = blockIdx.y * ROWS;
-    for (int p = threadIdx.x; p < a.nseg * ROWS; p += NT) {
-        const int s = p / ROWS, r = p % ROWS;
+    extern __shared__ float Gs[];   // [rows][nseg]
+    const int bh = blockIdx.y;
+    const size_t st = (size_t)a.dk * a.dv;
+    const size_t e0 = (size_t)blockIdx.x * NT;           // first element of this CTA
+    const int k0 = (int)(e0 / a.dv);
+    const int rows = (int)((e0 + NT - 1) / a.dv) - k0 + 1;
+    // Gamma per (row, segment): one warp per product, lanes stride over the chunks
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int p = warp; p < rows * a.nseg; p += NT / 32) {
+        const int r = p / a.nseg, s = p % a.nseg;
         float g = 1.f;
         if (a.gam) {
             const int c0 = s * a.cps, c1 = min(a.nchunks, c0 + a.cps);
-            const float* gp = a.gam + ((size_t)bh * a.nchunks) * a.dk + k0 + r;
-            for (int c = c0; c < c1; ++c) g *= gp[(size_t)c * a.dk];
+            const float* gp = a.gam + (size_t)bh * a.nchunks * a.dk + k0 + r;
+            for (int c = c0 + lane; c < c1; c += 32) g *= gp[(size_t)c * a.dk];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) g *= __shfl_xor_sync(0xffffffffu, g, o);
         }
-        Gs[p] = g;
+        if (lane == 0) Gs[p] = g;
     }
     __syncthreads();
-    const size_t st = (size_t)a.dk * a.dv;
-    for (int e = threadIdx.x; e < ROWS * a.dv; e += NT) {
-        const int r = e / a.dv, j = e % a.dv;
-        const size_t off = (size_t)(k0 + r) * a.dv + j;
-        float S = a.S0 ? a.S0[(size_t)bh * st + off] : 0.f;
-        for (int s = 0; s < a.nseg; ++s) {
-            const size_t o = ((size_t)bh * a.nseg + s) * st + off;
-            a.segin[o] = S;
-            S = fmaf(Gs[s * ROWS + r], S, a.segS[o]);
+    const size_t e = e0 + threadIdx.x;
+    if (e >= st) return;
+    const int r = (int)(e / a.dv) - k0;
+    const float* sp = a.segS + (size_t)bh * a.nseg * st + e;
+    float* ip = a.segin + (size_t)bh * a.nseg * st + e;
+    float S = a.S0 ? a.S0[(size_t)bh * st + e] : 0.f;
+    float buf[AHEAD];
+#pragma unroll
+    for (int i = 0; i < AHEAD; ++i) buf[i] = (i < a.nseg) ? sp[(size_t)i * st] : 0.f;
+    for (int s = 0; s < a.nseg; s += AHEAD) {
+#pragma unroll
+        for (int i = 0; i < AHEAD; ++i) {
+            const int ss = s + i;
+            if (ss < a.nseg) {
+                const float cur = buf[i];
+                if (ss + AHEAD < a.nseg) buf[i] = sp[(size_t)(ss + AHEAD) * st];
+                ip[(size_t)ss * st] = S;
+                S = fmaf(Gs[r * a.nseg + ss], S, cur);
+            }
         }
-        if (a.ST) a.ST[(size_t)bh * st + off] = S;
     }
+    if (a.ST) a.ST[(size_t)bh * st + e] = S;
 }
 
 }  // namespace
@@ -69,8 +92,11 @@ cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, i
     a.segS = reinterpret_cast<const float*>(base + pl.off_segS);
     a.segin = reinterpret_cast<float*>(base + pl.off_segin);
     a.dk = p.dk; a.dv = p.dv; a.nchunks = pl.nchunks; a.nseg = pl.nseg; a.cps = pl.chunks_per_seg;
-    dim3 grid(p.B * p.H, p.dk / ROWS);
-    const size_t smem = (size_t)pl.nseg * ROWS * sizeof(float);
+    const size_t st = (size_t)p.dk * p.dv;
+    dim3 grid((unsigned)((st + NT - 1) / NT), p.B * p.H);
+    // rows one CTA touches: NT elements span at most NT / dv + 2 rows
+    const int max_rows = NT / p.dv + 2;
+    const size_t smem = (size_t)max_rows * pl.nseg * sizeof(float);
     gla_state_scan_kernel<<<grid, NT, smem, s>>>(a);
     return cudaGetLastError();
 }
