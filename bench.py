@@ -126,7 +126,8 @@ def planned_segments(w, force, sms):
 
 
 def kernel_source_sha(name):
-    files = {"gla_chunk_fwd": ["gla_chunk_fwd.cu", "sm100.cuh"], "gla_chunk_prep": ["gla_prep.cu"]}.get(name, [])
+    files = {"gla_chunk_fwd": ["gla_chunk_fwd.cu", "sm100.cuh"],
+             "gla_chunk_prep": ["gla_prep.cu", "sm100.cuh"]}.get(name, [])
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "chunkwise_gated_linear_gla_gb300", "csrc", f), "rb") as fh:
