@@ -217,7 +217,7 @@ gla_status run_stage(const gla_fwd_params* p, const Plan& pl, int i, cudaStream_
         break;
     case STAGE_SIMT: e = launch_simt(*p, c->status, s); break;
     case STAGE_PREP: e = launch_prep(*p, pl, p->workspace, c->status, s); break;
-    case STAGE_SEG_STATE: e = launch_chunk_fwd(*p, pl, p->workspace, kModeSegState, c->status, s); break;
+    case STAGE_SEG_STATE: e = launch_seg_state(*p, pl, p->workspace, c->status, s); break;
     case STAGE_SEG_SCAN: e = launch_seg_scan(*p, pl, p->workspace, c->status, s); break;
     case STAGE_CHUNK_FWD:
         e = launch_chunk_fwd(*p, pl, p->workspace, pl.nseg > 1 ? kModeSegOut : kModeFull, c->status, s);

@@ -49,6 +49,7 @@ cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s);
 cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode,
                              int* status, cudaStream_t s);
+cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, int* status,
                             cudaStream_t s);
 
