@@ -21,7 +21,7 @@ GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT = 0, 1, 2
 # Every symbol include/gla.h declares.
 EXPORTED = ("gla_fwd", "gla_fwd_ex", "gla_fwd_workspace_size", "gla_fwd_num_stages",
             "gla_fwd_stage", "gla_fwd_stage_name", "gla_device_status", "gla_status_string",
-            "gla_version", "gla_fwd_noalloc")
+            "gla_version", "gla_fwd_noalloc", "gla_fwd_host", "gla_host_release")
 
 
 class GlaError(RuntimeError):
@@ -80,6 +80,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.gla_fwd_stage.argtypes = [P, i, vp]
         lib.gla_fwd_stage_name.restype = ctypes.c_char_p
         lib.gla_fwd_stage_name.argtypes = [P, i]
+        lib.gla_fwd_host.restype = st
+        lib.gla_fwd_host.argtypes = [P, ctypes.c_size_t, vp]
+        lib.gla_host_release.restype = st
+        lib.gla_host_release.argtypes = []
         lib.gla_device_status.restype = st
         lib.gla_device_status.argtypes = [vp]
         lib.gla_status_string.restype = ctypes.c_char_p
@@ -142,6 +146,21 @@ def gla_fwd_ex(p: gla_fwd_params, stream=None, check=True) -> int:
     s = load().gla_fwd_ex(ctypes.byref(p), _stream(stream))
     if check:
         _check(s, "gla_fwd_ex")
+    return s
+
+
+def gla_fwd_host(p: gla_fwd_params, slice_bytes=0, stream=None, check=True) -> int:
+    """gla_fwd_ex with host tensors (see include/gla.h); returns once O and S_T are on the host."""
+    s = load().gla_fwd_host(ctypes.byref(p), slice_bytes, _stream(stream))
+    if check:
+        _check(s, "gla_fwd_host")
+    return s
+
+
+def gla_host_release(check=True) -> int:
+    s = load().gla_host_release()
+    if check:
+        _check(s, "gla_host_release")
     return s
 
 

@@ -55,8 +55,10 @@ bool overlap(Range a, Range b) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Host-only checks: everything that can be decided without touching the device.
-gla_status validate(const gla_fwd_params* p)
+}  // namespace
+
+// Host-only checks of sizes, modes and which pointers are present.
+gla_status validate_args(const gla_fwd_params* p)
 {
     if (!p) return GLA_ERR_INVALID_ARG;
     if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->dk <= 0 || p->dv <= 0) return GLA_ERR_INVALID_ARG;
@@ -74,17 +76,27 @@ gla_status validate(const gla_fwd_params* p)
     if (p->T > 0 && (!p->q || !p->k || !p->v || !p->O)) return GLA_ERR_INVALID_ARG;
     if (p->chunk != 0 && p->chunk != kChunk) return GLA_ERR_UNSUPPORTED;
     if (p->dk > kMaxDk) return GLA_ERR_UNSUPPORTED;
+    return GLA_OK;
+}
 
+// Checks of the pointer values: outputs overlap no input (ST may equal S0
+// exactly), and, for device pointers, the alignment the kernels' TMA and
+// vector accesses need.
+gla_status validate_pointers(const gla_fwd_params* p, bool device)
+{
     const size_t e = p->dtype == GLA_BF16 ? 2 : 4;
     const size_t BH = (size_t)p->B * p->H;
     const size_t nq = BH * p->T * p->dk * e, nv = BH * p->T * p->dv * e;
     const size_t ng = p->gate == GLA_GATE_PER_KEY ? BH * p->T * p->dk * 4
                     : p->gate == GLA_GATE_HEAD_SCALAR ? (size_t)p->H * 4 : 0;
     const size_t ns = BH * p->dk * p->dv * 4;
-    // TMA and vector loads need 16-byte aligned bases
-    for (const void* ptr : {p->q, p->k, p->v, (const void*)p->O, (const void*)p->S0, (const void*)p->ST})
-        if (ptr && !aligned(ptr, 16)) return GLA_ERR_INVALID_ARG;
-    if (p->log_g && !aligned(p->log_g, p->gate == GLA_GATE_PER_KEY ? 16 : 4)) return GLA_ERR_INVALID_ARG;
+    if (device) {
+        // TMA and vector loads need 16-byte aligned bases
+        for (const void* ptr : {p->q, p->k, p->v, (const void*)p->O, (const void*)p->S0, (const void*)p->ST})
+            if (ptr && !aligned(ptr, 16)) return GLA_ERR_INVALID_ARG;
+        if (p->log_g && !aligned(p->log_g, p->gate == GLA_GATE_PER_KEY ? 16 : 4)) return GLA_ERR_INVALID_ARG;
+        if (p->workspace && !aligned(p->workspace, 256)) return GLA_ERR_INVALID_ARG;
+    }
     // outputs must not overlap inputs; ST may equal S0 exactly (in-place state carry)
     Range rO = rng(p->O, nv), rST = rng(p->ST, p->ST ? ns : 0);
     Range ins[] = {rng(p->q, nq), rng(p->k, nq), rng(p->v, nv), rng(p->log_g, ng), rng(p->S0, p->S0 ? ns : 0)};
@@ -93,8 +105,15 @@ gla_status validate(const gla_fwd_params* p)
     for (int i = 0; i < 4; ++i) if (overlap(rST, ins[i])) return GLA_ERR_INVALID_ARG;
     if (p->ST && p->S0 && overlap(rST, ins[4]) && (const void*)p->ST != (const void*)p->S0)
         return GLA_ERR_INVALID_ARG;
-    if (p->workspace && !aligned(p->workspace, 256)) return GLA_ERR_INVALID_ARG;
     return GLA_OK;
+}
+
+namespace {
+
+gla_status validate(const gla_fwd_params* p)
+{
+    gla_status st = validate_args(p);
+    return st != GLA_OK ? st : validate_pointers(p, true);
 }
 
 bool tensor_shape_ok(const gla_fwd_params* p)
@@ -119,9 +138,10 @@ int choose_segments(const gla_fwd_params* p, int units, int nchunks, int sms)
     return n < 1 ? 1 : n;
 }
 
+// Callers check the pointers (validate or validate_pointers) themselves.
 gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
 {
-    gla_status st = validate(p);
+    gla_status st = validate_args(p);
     if (st != GLA_OK) return st;
     pl = Plan{};
     if (p->T == 0) {
@@ -227,6 +247,14 @@ gla_status run_stage(const gla_fwd_params* p, const Plan& pl, int i, cudaStream_
 }
 
 }  // namespace
+
+gla_status plan_workspace(const gla_fwd_params* p, size_t* bytes)
+{
+    Plan pl;
+    gla_status st = make_plan(p, pl, device_sms());
+    *bytes = st == GLA_OK ? pl.ws_bytes : 0;
+    return st;
+}
 
 int* device_status_ptr()
 {

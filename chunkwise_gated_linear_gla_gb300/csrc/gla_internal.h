@@ -41,6 +41,15 @@ struct Plan {
     StageKind stages[4];
 };
 
+// Argument checks of the C ABI (gla_api.cu). validate_args: sizes, modes and
+// which pointers are present. validate_pointers: no output overlaps an input
+// (ST may equal S0 exactly) and, when `device`, the alignment the kernels need.
+gla_status validate_args(const gla_fwd_params* p);
+gla_status validate_pointers(const gla_fwd_params* p, bool device);
+// Workspace bytes of the plan for *p from its shapes alone (the pointers are
+// not looked at); the status of validate_args or of planning.
+gla_status plan_workspace(const gla_fwd_params* p, size_t* bytes);
+
 // Device status word (per device), written by kernels whose bounded waits run out.
 int* device_status_ptr();   // nullptr on failure
 

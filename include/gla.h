@@ -26,19 +26,21 @@
  *   log_g  see above    fp32
  *   S0, ST [B,H,dk,dv]  fp32
  *
- * Ownership. All tensor pointers are device pointers owned by the caller. The
- * library keeps none of them after a call returns. It allocates nothing on
- * its own except in gla_fwd(), which takes its workspace from the stream-
- * ordered allocator (cudaMallocAsync / cudaFreeAsync on the given stream).
+ * Ownership. All tensor pointers are device pointers owned by the caller,
+ * except in gla_fwd_host(), which takes host pointers. The library keeps none
+ * of them after a call returns. It allocates nothing on its own except in
+ * gla_fwd(), which takes its workspace from the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on the given stream), and gla_fwd_host(),
+ * which stages through a pool of its own.
  *
- * Asynchrony. Every call only enqueues work on `stream` and returns; it never
- * synchronises the device. Argument errors are detected on the host before
- * anything is launched. A kernel whose bounded wait runs out records that in
+ * Asynchrony. Every call but gla_fwd_host() only enqueues work on `stream`
+ * and returns; none of them synchronises the device. Argument errors are
+ * detected on the host before anything is launched. A kernel whose bounded wait runs out records that in
  * a device-side status word (see gla_device_status) and returns early.
  *
  * Thread safety. Calls may be made concurrently from several host threads.
- * The only process-wide state is a per-device cache of the TMA encode entry
- * point and device attributes.
+ * The process-wide state is a per-device cache of the TMA encode entry point
+ * and device attributes, and gla_fwd_host()'s streams and memory pool.
  */
 #ifndef GLA_H_
 #define GLA_H_
@@ -144,6 +146,34 @@ const char* gla_fwd_stage_name(const gla_fwd_params* p, int stage);
 gla_status gla_fwd_noalloc(const void* q, const void* k, const void* v, const float* log_g,
                            const float* S0, void* O, float* ST,
                            int B, int H, int T, int dk, int dv, int chunk, cudaStream_t stream);
+
+/*
+ * gla_fwd_host — the forward pass described by *p with every tensor pointer
+ * (q, k, v, log_g, S0, O, ST) in HOST memory. (No counterpart in the papers:
+ * this is a deployment convenience.)
+ *
+ * The call copies the inputs to the device, runs the pass and copies O and
+ * S_T back, one slice of the batch at a time (whole batch rows, or groups of
+ * heads of one row when B is small) of about `slice_bytes` of copy traffic
+ * each (0: 48 MiB; the last slices are cut smaller), so that the copy-in of
+ * one slice, the compute of the one before and the copy-out of the one
+ * before that overlap. Host memory may be pinned (page-locked, which the
+ * overlap needs) or pageable, with no alignment rule. p->workspace and
+ * p->workspace_bytes are ignored.
+ *
+ * Device memory: three slices' buffers and one workspace, from a memory pool
+ * private to the library that keeps its pages between calls so that repeated
+ * calls map no memory; gla_host_release() gives them back. The work runs on
+ * three streams of the library, after all work already enqueued on `stream`,
+ * and `stream` waits for it. Unlike the other entry points the call is
+ * synchronous: it returns once O and S_T are written in host memory (or on
+ * an error, after the library's streams are idle). Calls on one device take
+ * turns. The argument rules are gla_fwd_ex's except pointer alignment.
+ */
+gla_status gla_fwd_host(const gla_fwd_params* p, size_t slice_bytes, cudaStream_t stream);
+
+/* Returns the pages of the current device's gla_fwd_host pool to the driver. */
+gla_status gla_host_release(void);
 
 /* Synchronises `stream`, then reads and clears the library's device status
  * word for the current device. GLA_ERR_TIMEOUT if a kernel gave up on a

@@ -103,7 +103,7 @@ def test_rejects_before_launch(lib, name, kw, want):
 
 
 def test_gla_fwd_rejects_before_launch(lib):
-    # spec signature: dk not a multiple of 16
+    # gla_fwd's signature: dk not a multiple of 16
     s = bnd.gla_fwd(0x10000, 0x20000, 0x30000, 0x40000, None, 0x50000, None, 1, 1, 64, 40, 64, 64,
                     stream=0, check=False)
     assert s == bnd.GLA_ERR_INVALID_ARG

@@ -181,7 +181,7 @@ def test_in_place_state_carry_with_split():
     assert_close(to_np(S), STref, torch.bfloat16, "ST")
 
 
-def test_gla_fwd_north_star_signature():
+def test_gla_fwd_public_signature():
     """gla_fwd(q,k,v,log_g,S0,O,ST,B,H,T,dk,dv,chunk,stream): per-key gate, stream-ordered workspace."""
     w = gi.Workload("t", B=2, H=2, T=130, dk=128, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY, s0_std=0.02)
     x = gi.make_inputs(w, seed=12)
