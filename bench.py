@@ -20,6 +20,7 @@ implementation of this method available here).
 from __future__ import annotations
 
 import argparse
+import platform
 import hashlib
 import json
 import os
@@ -240,7 +241,7 @@ def run_reference(args, w):
     tok = rows * w.T
     mean = sum(times) / len(times)
     value = tok / mean
-    sample = f"{rows} of {w.B} batch rows (all {w.H} heads, T={w.T}) per step"
+    sample = f"{rows} of {w.B} batch rows (all {w.H} heads, T={w.T}) per step, {cpu_model()}"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
@@ -251,6 +252,36 @@ def run_reference(args, w):
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+def cpu_model():
+    """The host CPU's name as /proc/cpuinfo gives it (Arm kernels give implementer/part codes)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model", "Hardware"):
+        for line in info.splitlines():
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    parts = sorted({line.split(":", 1)[1].strip() for line in info.splitlines()
+                    if line.startswith(("CPU implementer", "CPU part")) and ":" in line})
+    return f"{platform.machine()} ({', '.join(parts)})" if parts else platform.machine()
+
+
+def cpu_one_core(w):
+    """Oracle tokens/s on one thread, from one head of one batch row (T capped at 2048),
+    scaled to whole tokens (all H heads) so it compares with the all-core figure."""
+    import oracle
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    ws = w.with_(B=1, H=1, T=min(w.T, 2048))
+    x = gi.make_inputs(ws, seed=0)
+    if x["gate"] == gi.GATE_HEAD_SCALAR:
+        x["log_g"] = x["log_g"][:1]
+    t0 = time.perf_counter()
+    oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=1)
+    dt = time.perf_counter() - t0
+    return ws.T / dt / w.H, f"1 head x T={ws.T}, {dt:.2f} s"
 
 
 def cpu_baseline(w, rows):
@@ -267,8 +298,10 @@ def cpu_baseline(w, rows):
         dt = time.perf_counter() - t0
         if dt >= 10.0 or reps >= 40:
             break
+    one, one_sample = cpu_one_core(w)
     return {"value": reps * rows * w.T / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{rows} of {w.B} batch rows (all {w.H} heads, T={w.T}) x {reps} passes, {dt:.1f} s"}
+            "sample": f"{rows} of {w.B} batch rows (all {w.H} heads, T={w.T}) x {reps} passes, {dt:.1f} s",
+            "cpu_model": cpu_model(), "value_1core": one, "sample_1core": one_sample}
 
 
 def main():
@@ -366,6 +399,16 @@ def main():
     stage_ms = [t / args.steps for t in stage_ms]
     step_ms /= args.steps
     step_ms = max_over_ranks(step_ms, dist, dev)
+    per_step = sorted(evs[0].elapsed_time(evs[nst]) for evs in evsets)
+
+    # the same steps back to back without the flush (inputs partly in L2 from the step before)
+    uevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in uevs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    unflushed = sorted(a.elapsed_time(b) for a, b in uevs)
 
     # end to end through gla_fwd_host: pinned host tensors in, host tensors out; the
     # library slices the batch so that copies in, compute and copies out overlap
@@ -432,6 +475,9 @@ def main():
                      "bytes_per_launch": dbytes},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "timing": {"mean_ms": step_ms, "median_ms": per_step[len(per_step) // 2], "min_ms": per_step[0],
+                   "unflushed_median_ms": unflushed[len(unflushed) // 2],
+                   "note": "mean is the value's basis; unflushed = the same steps back to back, no L2 flush"},
         "gpu_launches": nst * args.steps,
         "clocks": clk,
     }

@@ -15,7 +15,11 @@ Attention-2 pages use:
 * head shapes of the 1.3B GLA layer, d_model = 2048, d_k = d/2, d_v = d,
   4 heads (same paper, §4.4 and §5.1);
 * the fixed per-head decay of Lightning Attention-2 / RetNet,
-  lambda_h = 1 - 2^-(5 + 5h/H) ("Lightning Attention-2", §3.2.1).
+  lambda_h = 1 - 2^-(5 + 5h/H) ("Lightning Attention-2", §3.2.1);
+* the data-dependent scalar gate, one gamma_t per token and head shared by
+  every key (the Mamba-2, mLSTM and Gated Retention rows of Table 1 in the
+  GLA paper, §4.1), drawn like Gated Retention's sigmoid(x)^(1/tau) with
+  tau = 16: log gamma_t = logsigmoid(N(0,1)) / 16.
 
 Draw order is fixed: q, k, v, gate pre-activation, S0 (all fp32 from one
 ``torch.Generator('cpu')``), then each tensor is cast to its dtype (bf16 by
@@ -32,8 +36,10 @@ import torch
 GATE_NONE = 0
 GATE_HEAD_SCALAR = 1
 GATE_PER_KEY = 2
+GATE_TOKEN_SCALAR = 3
 
-_GATE_NAMES = {"none": GATE_NONE, "scalar": GATE_HEAD_SCALAR, "per_key": GATE_PER_KEY}
+_GATE_NAMES = {"none": GATE_NONE, "scalar": GATE_HEAD_SCALAR, "per_key": GATE_PER_KEY,
+               "token_scalar": GATE_TOKEN_SCALAR}
 
 
 @dataclass
@@ -47,7 +53,7 @@ class Workload:
     dk: int
     dv: int
     dtype: torch.dtype          # dtype of q, k, v and O
-    gate: int                   # GATE_NONE / GATE_HEAD_SCALAR / GATE_PER_KEY
+    gate: int                   # GATE_NONE / GATE_HEAD_SCALAR / GATE_PER_KEY / GATE_TOKEN_SCALAR
     qkv_scale: str = "all"      # "all": q,k,v * dk^-0.5 ; "q": only q
     k_l2norm: bool = False      # k normalised to unit L2 norm per row
     s0_std: float = 0.0         # 0 => S0 absent (zero state)
@@ -80,6 +86,10 @@ WORKLOADS = {
     "gla_1p3b": Workload(
         "gla_1p3b", B=8, H=4, T=2048, dk=256, dv=512, dtype=torch.bfloat16,
         gate=GATE_PER_KEY, s0_std=0.02, notes="GLA layer shaped like the 1.3B model"),
+    "token_gate": Workload(
+        "token_gate", B=8, H=4, T=2048, dk=256, dv=512, dtype=torch.bfloat16,
+        gate=GATE_TOKEN_SCALAR, s0_std=0.02,
+        notes="data-dependent scalar gate per token and head (Mamba-2 / mLSTM form), 1.3B layer shape"),
     "gla_long": Workload(
         "gla_long", B=1, H=4, T=65536, dk=256, dv=512, dtype=torch.bfloat16,
         gate=GATE_PER_KEY, notes="long sequence, low B*H"),
@@ -97,7 +107,8 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
 
     Returns a dict with q, k, v (``w.dtype``), log_g (fp32 or None), S0 (fp32 or
     None) and the shape fields. Layouts: q, k, log_g are [B,H,T,dk]; v is
-    [B,H,T,dv]; S0 is [B,H,dk,dv]; for the per-head scalar gate log_g is [H].
+    [B,H,T,dv]; S0 is [B,H,dk,dv]; for the per-head scalar gate log_g is [H],
+    for the per-token scalar gate [B,H,T].
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
@@ -114,17 +125,18 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
         k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
 
     log_g = None
-    if w.gate == GATE_PER_KEY:
+    if w.gate in (GATE_PER_KEY, GATE_TOKEN_SCALAR):
+        shape = (B, H, T, dk) if w.gate == GATE_PER_KEY else (B, H, T)
         if w.gate_dist == "logsigmoid16":
-            pre = torch.randn((B, H, T, dk), generator=g, dtype=torch.float32)
+            pre = torch.randn(shape, generator=g, dtype=torch.float32)
             log_g = torch.nn.functional.logsigmoid(pre) / 16.0
         elif w.gate_dist == "steep":
-            u = torch.rand((B, H, T, dk), generator=g, dtype=torch.float32)
+            u = torch.rand(shape, generator=g, dtype=torch.float32)
             log_g = -4.0 * u
         elif w.gate_dist.startswith("const:"):
-            log_g = torch.full((B, H, T, dk), float(w.gate_dist[6:]), dtype=torch.float32)
+            log_g = torch.full(shape, float(w.gate_dist[6:]), dtype=torch.float32)
         elif w.gate_dist == "zero":
-            log_g = torch.zeros((B, H, T, dk), dtype=torch.float32)
+            log_g = torch.zeros(shape, dtype=torch.float32)
         else:
             raise ValueError(f"unknown gate distribution {w.gate_dist!r}")
     elif w.gate == GATE_HEAD_SCALAR:

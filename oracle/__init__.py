@@ -26,7 +26,7 @@ _LIB_PATH = os.path.join(_BUILD, "libgla_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-GATE_NONE, GATE_HEAD_SCALAR, GATE_PER_KEY = 0, 1, 2
+GATE_NONE, GATE_HEAD_SCALAR, GATE_PER_KEY, GATE_TOKEN_SCALAR = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -82,13 +82,16 @@ def gla_forward(q, k, v, log_g=None, gate=None, S0=None, want_state=True,
     """Run the fp64 recurrence. Returns (O, ST) as fp64 numpy arrays (ST None if not wanted).
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv]; log_g: [B,H,T,dk] (per-key), [H] (per-head
-    scalar) or None (alpha = 1); S0: [B,H,dk,dv] or None.
+    scalar), [B,H,T] (per-token scalar) or None (alpha = 1); S0: [B,H,dk,dv] or None.
     """
     qa, ka, va = _f64(q), _f64(k), _f64(v)
     B, H, T, dk = qa.shape
     dv = va.shape[-1]
     if gate is None:
-        gate = GATE_NONE if log_g is None else (GATE_HEAD_SCALAR if np.ndim(_f64(log_g)) == 1 else GATE_PER_KEY)
+        if log_g is None:
+            gate = GATE_NONE
+        else:
+            gate = {1: GATE_HEAD_SCALAR, 3: GATE_TOKEN_SCALAR}.get(np.ndim(_f64(log_g)), GATE_PER_KEY)
     ga = _f64(log_g) if gate != GATE_NONE else None
     sa = _f64(S0)
     O = np.empty((B, H, T, dv), dtype=np.float64)
@@ -115,7 +118,7 @@ def gla_forward_rows(q, k, v, log_g, gate, S0, bh_list, nthreads=None):
     sa = _f64(S0)
     for (b, h) in bh_list:
         g1 = None
-        if gate == GATE_PER_KEY:
+        if gate in (GATE_PER_KEY, GATE_TOKEN_SCALAR):
             g1 = ga[b:b + 1, h:h + 1]
         elif gate == GATE_HEAD_SCALAR:
             g1 = ga[h:h + 1]

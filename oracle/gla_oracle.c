@@ -20,6 +20,9 @@
  *   0  alpha_t = 1                         (log_g unused)
  *   1  alpha_t = exp(log_g[h]) for all t,k (log_g is [H])
  *   2  alpha_t = exp(log_g[b,h,t,:])       (log_g is [B,H,T,dk])
+ *   3  alpha_t = exp(log_g[b,h,t]) for all k (log_g is [B,H,T]): the
+ *      data-dependent scalar gate G_t = gamma_t 1^T 1 of the Mamba-2, mLSTM
+ *      and Gated Retention rows of Table 1 (GLA paper, §4.1)
  *
  * Layouts (row-major, contiguous): q [B,H,T,dk], k [B,H,T,dk], v [B,H,T,dv],
  * O [B,H,T,dv], S0 and ST [B,H,dk,dv]. S0 may be NULL (zero state); ST may be
@@ -58,6 +61,7 @@ static double gate_alpha(const job_t* J, long t, long i)
 {
     if (J->gate == 0) return 1.0;
     if (J->gate == 1) return exp(J->log_g[J->bh % J->H]);
+    if (J->gate == 3) return exp(J->log_g[J->bh * J->T + t]);
     return exp(J->log_g[(J->bh * J->T + t) * J->dk + i]);
 }
 
@@ -161,7 +165,7 @@ int gla_oracle_fwd(const double* q, const double* k, const double* v,
                    int nthreads, int mutant)
 {
     if (!q || !k || !v || !O || B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
-    if (gate < 0 || gate > 2 || (gate != 0 && !log_g)) return 1;
+    if (gate < 0 || gate > 3 || (gate != 0 && !log_g)) return 1;
     if (mutant == 3 && dk != dv) return 1;
     if (T == 0) {
         if (ST) {

@@ -10,6 +10,9 @@ Sources (page title, section):
   [LA2]   "Lightning Attention-2: A Free Lunch for Handling Unlimited Sequence
           Lengths in Large Language Models", §3.2.1 Alg. 1 (decay mask
           M_ij = lambda^(i-j) for i >= j).
+  [GLA Table 1] the data-dependent scalar gate G_t = gamma_t 1^T 1 (Mamba-2,
+          mLSTM, Gated Retention rows): alpha_t has the same value gamma_t
+          for every key.
 All of these run on the CPU.
 """
 import math
@@ -41,6 +44,8 @@ def _logb(log_g, gate, B, H, T, dk):
     if gate == gi.GATE_HEAD_SCALAR:
         steps = np.arange(1, T + 1, dtype=np.float64)
         return np.broadcast_to(log_g[None, :, None, None] * steps[None, None, :, None], (B, H, T, dk)).copy()
+    if gate == gi.GATE_TOKEN_SCALAR:
+        return np.broadcast_to(np.cumsum(log_g, axis=2)[..., None], (B, H, T, dk)).copy()
     return np.cumsum(log_g, axis=2)
 
 
@@ -49,6 +54,8 @@ def _gate_log(log_g, gate, B, H, T, dk):
         return np.zeros((B, H, T, dk))
     if gate == gi.GATE_HEAD_SCALAR:
         return np.broadcast_to(log_g[None, :, None, None], (B, H, T, dk)).copy()
+    if gate == gi.GATE_TOKEN_SCALAR:
+        return np.broadcast_to(log_g[..., None], (B, H, T, dk)).copy()
     return log_g
 
 
@@ -109,7 +116,7 @@ def _brute_force(q, k, v, log_g, gate, S0):
     return O, ST
 
 
-@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
 def test_brute_force_tiny(gate):
     q, k, v, g, gate, S0 = _case(B=2, H=2, T=6, dk=3, dv=4, gate=gate, s0=0.7, seed=3)
     O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
@@ -169,7 +176,9 @@ def _parallel_direct(q, k, v, log_g, gate, S0):
 @pytest.mark.parametrize("gate,dist", [(gi.GATE_NONE, "logsigmoid16"),
                                        (gi.GATE_HEAD_SCALAR, "logsigmoid16"),
                                        (gi.GATE_PER_KEY, "logsigmoid16"),
-                                       (gi.GATE_PER_KEY, "steep")])
+                                       (gi.GATE_PER_KEY, "steep"),
+                                       (gi.GATE_TOKEN_SCALAR, "logsigmoid16"),
+                                       (gi.GATE_TOKEN_SCALAR, "steep")])
 def test_quadratic_logspace_form(gate, dist):
     q, k, v, g, gate, S0 = _case(B=1, H=3, T=96, dk=8, dv=5, gate=gate, dist=dist, s0=0.3, seed=5)
     O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
@@ -211,6 +220,47 @@ def test_scalar_decay_closed_form():
         np.testing.assert_allclose(ST[0, h], st, rtol=0, atol=1e-12 * np.abs(st).max())
 
 
+def test_token_scalar_decay_matrix_form():
+    """[GLA Table 1] with alpha_t = gamma_t 1: O = ((Q K^T) (.) L) V with the lower-triangular
+    decay matrix L_ts = prod_{u=s+1..t} gamma_u, built here by explicit running products
+    (no logarithms), plus the (prod_{u<=t} gamma_u) q_t S0 term; S_T likewise."""
+    q, k, v, g, gate, S0 = _case(B=2, H=2, T=40, dk=5, dv=4, gate=gi.GATE_TOKEN_SCALAR, s0=0.4, seed=41)
+    O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
+    T = q.shape[2]
+    gam = np.exp(g)
+    for b in range(2):
+        for h in range(2):
+            L = np.zeros((T, T))
+            for t in range(T):
+                p = 1.0
+                L[t, t] = 1.0
+                for s_ in range(t - 1, -1, -1):
+                    p *= gam[b, h, s_ + 1]
+                    L[t, s_] = p
+            pre = np.cumprod(gam[b, h])                     # prod_{u<=t} gamma_u
+            ref = ((q[b, h] @ k[b, h].T) * L) @ v[b, h] + pre[:, None] * (q[b, h] @ S0[b, h])
+            np.testing.assert_allclose(O[b, h], ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+            st = (k[b, h] * L[T - 1][:, None]).T @ v[b, h] + pre[-1] * S0[b, h]
+            np.testing.assert_allclose(ST[b, h], st, rtol=0, atol=1e-12 * np.abs(st).max())
+
+
+def test_token_scalar_special_cases():
+    """The per-token scalar gate is the per-key gate with every key's log alpha equal, and with a
+    constant per head it is the fixed per-head decay: both reductions hold exactly."""
+    q, k, v, g, gate, S0 = _case(B=2, H=3, T=50, dk=6, dv=5, gate=gi.GATE_TOKEN_SCALAR, s0=0.3, seed=43)
+    O, ST = oracle.gla_forward(q, k, v, g, gate, S0)
+    gk = np.broadcast_to(g[..., None], q.shape).copy()
+    Ok, STk = oracle.gla_forward(q, k, v, gk, oracle.GATE_PER_KEY, S0)
+    np.testing.assert_array_equal(O, Ok)
+    np.testing.assert_array_equal(ST, STk)
+    lam = np.array([-0.01, -0.2, -1.5])
+    gc = np.broadcast_to(lam[None, :, None], g.shape).copy()
+    Oc, STc = oracle.gla_forward(q, k, v, gc, oracle.GATE_TOKEN_SCALAR, S0)
+    Oh, STh = oracle.gla_forward(q, k, v, lam, oracle.GATE_HEAD_SCALAR, S0)
+    np.testing.assert_array_equal(Oc, Oh)
+    np.testing.assert_array_equal(STc, STh)
+
+
 # ---------------------------------------------------------------- chunkwise form
 
 def _chunked(q, k, v, log_g, gate, S0, C):
@@ -244,7 +294,7 @@ def _chunked(q, k, v, log_g, gate, S0, C):
 
 
 @pytest.mark.parametrize("C", [1, 2, 3, 7, 16, 64, 100])
-@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
 def test_chunk_size_invariance(C, gate):
     """[GLA] §2.2 / §4.2: the chunkwise form equals the recurrence for every C (C=1 and C=T are its limits)."""
     q, k, v, g, gate, S0 = _case(B=1, H=2, T=100, dk=8, dv=6, gate=gate, s0=0.5, seed=13)
@@ -267,7 +317,7 @@ def test_steep_gate_limit():
     np.testing.assert_allclose(ST, np.einsum("bhk,bhv->bhkv", k[:, :, -1], v[:, :, -1]), rtol=0, atol=1e-15)
 
 
-@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
 def test_initial_state_linearity(gate):
     """O(S0) - O(0) = (Q (.) B) S0 and S_T(S0) - S_T(0) = Diag(b_T) S0."""
     q, k, v, g, gate, S0 = _case(B=2, H=2, T=45, dk=7, dv=4, gate=gate, s0=1.0, seed=19)
@@ -322,6 +372,13 @@ def test_threads_do_not_change_result():
 def test_pins_catch_planted_mistakes(mutant):
     """Each deliberate mistake planted in the oracle must fail at least one pin."""
     q, k, v, g, gate, S0 = _case(B=1, H=2, T=40, dk=6, dv=6, s0=0.5, seed=37)
+    if mutant != 3:
+        # the same mistakes under the per-token scalar gate (where rows and columns of the
+        # gate coincide, so mutant 3 is no mistake there)
+        qt, kt, vt, gt, gatet, S0t = _case(B=1, H=2, T=40, dk=6, dv=6, gate=gi.GATE_TOKEN_SCALAR, s0=0.5, seed=38)
+        Ot, STt = oracle.gla_forward(qt, kt, vt, gt, gatet, S0t, mutant=mutant)
+        Oqt, STqt = _quadratic_logspace(qt, kt, vt, gt, gatet, S0t)
+        assert max(np.abs(Ot - Oqt).max(), np.abs(STt - STqt).max()) > 1e-6, f"mutant {mutant} (token gate)"
     O, ST = oracle.gla_forward(q, k, v, g, gate, S0, mutant=mutant)
     Oq, STq = _quadratic_logspace(q, k, v, g, gate, S0)
     Oc, STc = _chunked(q, k, v, g, gate, S0, 16)
