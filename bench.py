@@ -76,12 +76,13 @@ def algorithmic(w):
     FLOPs per token per head: 4 dk dv (state update + inter-chunk term) +
     (C+1)(dk+dv) (causal intra-chunk scores and their product with V).
     Bytes: q, k, v read and O written once (e bytes each element), the fp32
-    per-key log gate read once, S0 read and S_T written once (fp32).
+    log gate read once (dk values per token per head for the per-key gate, one for
+    the per-token scalar gate), S0 read and S_T written once (fp32).
     """
     import torch
     e = 2 if w.dtype == torch.bfloat16 else 4
     BH, T, dk, dv, C = w.B * w.H, w.T, w.dk, w.dv, w.chunk
-    gate_bytes = 4 * dk if w.gate == 2 else 0
+    gate_bytes = 4 * dk if w.gate == 2 else 4 if w.gate == 3 else 0
     flops = BH * T * (4 * dk * dv + (C + 1) * (dk + dv))
     byts = BH * T * (e * (2 * dk + dv) + e * dv + gate_bytes) + BH * dk * dv * 4 * (2 if w.s0_std > 0 else 1)
     return flops, byts
@@ -97,7 +98,7 @@ def stage_bytes(w, name, nseg=1):
     nch = (T + C - 1) // C
     Tp = nch * C
     gated = w.gate != 0
-    gate_in = T * dk * 4 if w.gate == 2 else 0
+    gate_in = T * dk * 4 if w.gate == 2 else T * 4 if w.gate == 3 else 0
     s0 = BH * dk * dv * 4 if w.s0_std > 0 else 0
     st = BH * dk * dv * 4
     qk_tiles = (Tp if gated else T) * dk * 2 * 2
@@ -463,7 +464,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
         "config": {"workload": f"{w.name}: {w.notes}, B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv} chunk=64, "
-                               f"gate={['none', 'per-head scalar', 'per-key'][w.gate]}, "
+                               f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar'][w.gate]}, "
                                f"S0={'given' if w.s0_std > 0 else 'zero'}",
                    "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "segments": nseg,
                    "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",

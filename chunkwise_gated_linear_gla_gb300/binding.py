@@ -15,7 +15,7 @@ from . import build as _build
 
 GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_CUDA, GLA_ERR_WORKSPACE, GLA_ERR_TIMEOUT = range(6)
 GLA_BF16, GLA_FP32 = 0, 1
-GLA_GATE_NONE, GLA_GATE_HEAD_SCALAR, GLA_GATE_PER_KEY = 0, 1, 2
+GLA_GATE_NONE, GLA_GATE_HEAD_SCALAR, GLA_GATE_PER_KEY, GLA_GATE_TOKEN_SCALAR = 0, 1, 2, 3
 GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT = 0, 1, 2
 
 # Every symbol include/gla.h declares.
@@ -204,7 +204,10 @@ def make_params(q, k, v, log_g, S0, O, ST, gate=None, path=GLA_PATH_AUTO, force_
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     if gate is None:
-        gate = GLA_GATE_NONE if log_g is None else (GLA_GATE_HEAD_SCALAR if log_g.dim() == 1 else GLA_GATE_PER_KEY)
+        if log_g is None:
+            gate = GLA_GATE_NONE
+        else:
+            gate = {1: GLA_GATE_HEAD_SCALAR, 3: GLA_GATE_TOKEN_SCALAR}.get(log_g.dim(), GLA_GATE_PER_KEY)
     p = gla_fwd_params()
     p.q, p.k, p.v = _ptr(q), _ptr(k), _ptr(v)
     p.log_g, p.S0, p.O, p.ST = _ptr(log_g), _ptr(S0), _ptr(O), _ptr(ST)

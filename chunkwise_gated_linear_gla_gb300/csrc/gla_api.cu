@@ -63,7 +63,8 @@ gla_status validate_args(const gla_fwd_params* p)
     if (!p) return GLA_ERR_INVALID_ARG;
     if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->dk <= 0 || p->dv <= 0) return GLA_ERR_INVALID_ARG;
     if (p->dtype != GLA_BF16 && p->dtype != GLA_FP32) return GLA_ERR_INVALID_ARG;
-    if (p->gate != GLA_GATE_NONE && p->gate != GLA_GATE_HEAD_SCALAR && p->gate != GLA_GATE_PER_KEY)
+    if (p->gate != GLA_GATE_NONE && p->gate != GLA_GATE_HEAD_SCALAR && p->gate != GLA_GATE_PER_KEY &&
+        p->gate != GLA_GATE_TOKEN_SCALAR)
         return GLA_ERR_INVALID_ARG;
     if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT)
         return GLA_ERR_INVALID_ARG;
@@ -72,7 +73,8 @@ gla_status validate_args(const gla_fwd_params* p)
     if ((long long)p->B * p->H > (1LL << 30)) return GLA_ERR_INVALID_ARG;
     if (p->gate == GLA_GATE_NONE && p->log_g) return GLA_ERR_INVALID_ARG;
     if (p->gate == GLA_GATE_HEAD_SCALAR && !p->log_g) return GLA_ERR_INVALID_ARG;
-    if (p->gate == GLA_GATE_PER_KEY && !p->log_g && p->T > 0) return GLA_ERR_INVALID_ARG;
+    if ((p->gate == GLA_GATE_PER_KEY || p->gate == GLA_GATE_TOKEN_SCALAR) && !p->log_g && p->T > 0)
+        return GLA_ERR_INVALID_ARG;
     if (p->T > 0 && (!p->q || !p->k || !p->v || !p->O)) return GLA_ERR_INVALID_ARG;
     if (p->chunk != 0 && p->chunk != kChunk) return GLA_ERR_UNSUPPORTED;
     if (p->dk > kMaxDk) return GLA_ERR_UNSUPPORTED;
@@ -88,6 +90,7 @@ gla_status validate_pointers(const gla_fwd_params* p, bool device)
     const size_t BH = (size_t)p->B * p->H;
     const size_t nq = BH * p->T * p->dk * e, nv = BH * p->T * p->dv * e;
     const size_t ng = p->gate == GLA_GATE_PER_KEY ? BH * p->T * p->dk * 4
+                    : p->gate == GLA_GATE_TOKEN_SCALAR ? BH * p->T * 4
                     : p->gate == GLA_GATE_HEAD_SCALAR ? (size_t)p->H * 4 : 0;
     const size_t ns = BH * p->dk * p->dv * 4;
     if (device) {

@@ -134,7 +134,7 @@ Sizes unit_sizes(const gla_fwd_params& p)
     Sizes z;
     z.q = (size_t)p.T * p.dk * e;
     z.v = (size_t)p.T * p.dv * e;
-    z.g = p.gate == GLA_GATE_PER_KEY ? (size_t)p.T * p.dk * 4 : 0;
+    z.g = p.gate == GLA_GATE_PER_KEY ? (size_t)p.T * p.dk * 4 : p.gate == GLA_GATE_TOKEN_SCALAR ? (size_t)p.T * 4 : 0;
     z.s = (size_t)p.dk * p.dv * 4;
     return z;
 }
@@ -246,7 +246,7 @@ extern "C" gla_status gla_fwd_host(const gla_fwd_params* hp, size_t slice_bytes,
         t.q = b + o_q;
         t.k = b + o_k;
         t.v = b + o_v;
-        t.log_g = p.gate == GLA_GATE_PER_KEY ? reinterpret_cast<const float*>(b + o_g)
+        t.log_g = z.g ? reinterpret_cast<const float*>(b + o_g)
                 : p.gate == GLA_GATE_HEAD_SCALAR ? dscal + x.h0 : nullptr;
         t.S0 = p.S0 ? reinterpret_cast<const float*>(b + o_s0) : nullptr;
         t.O = b + o_o;

@@ -172,9 +172,12 @@ __device__ __forceinline__ void score_mma(const uint8_t* Qs, const uint8_t* Ks, 
 // the stage is written only after the named barrier free_bar (free_n threads)
 // says its other readers are done.
 // lam: log of the per-head decay (scores scaled by lambda^(r-s)), 0 otherwise.
+// TOK (per-token scalar gate): Lc is the chunk's inclusive cumulative log gate in
+// shared memory; the scores are then scaled by exp(Lc[r] - Lc[s]) and lam is unused.
+template <bool TOK = false>
 __device__ __forceinline__ bool score_readout(uint32_t tmem, uint64_t* bar, uint32_t phase, int nr, float lam,
                                               __nv_bfloat16* stage, const CUtensorMap* tmA, int arow,
-                                              int free_bar = -1, int free_n = 0) {
+                                              int free_bar = -1, int free_n = 0, const float* Lc = nullptr) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const bool ok = mbar_wait(bar, phase, kTimeoutNs);
     tc_fence_after();
@@ -182,6 +185,7 @@ __device__ __forceinline__ bool score_readout(uint32_t tmem, uint64_t* bar, uint
     const uint32_t lb = (uint32_t)(warp * 32) << 16;
     uint4* dst = reinterpret_cast<uint4*>(stage + r * 64);
     uint32_t p[2][16];
+    const float lr = TOK ? Lc[r] : 0.f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {   // columns 32h .. 32h + 31, one half at a time
         uint32_t v[32];
@@ -193,8 +197,11 @@ __device__ __forceinline__ bool score_readout(uint32_t tmem, uint64_t* bar, uint
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int s = 32 * h + 2 * i + e;
-                const bool keep = s <= r && r < nr;   // the decay only where s <= r: lambda^(r-s) <= 1
-                x[e] = keep ? __uint_as_float(v[2 * i + e]) * (lam != 0.f ? __expf((r - s) * lam) : 1.f) : 0.f;
+                const bool keep = s <= r && r < nr;   // the decay only where s <= r: it is <= 1 there
+                if (TOK)
+                    x[e] = keep ? __uint_as_float(v[2 * i + e]) * __expf(lr - Lc[s]) : 0.f;
+                else
+                    x[e] = keep ? __uint_as_float(v[2 * i + e]) * (lam != 0.f ? __expf((r - s) * lam) : 1.f) : 0.f;
             }
             p[h][i] = pack_bf16(x[0], x[1]);
         }
@@ -534,7 +541,11 @@ gla_chunk_prep_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const
 // gate of row r in a chunk is (r+1) log(lambda) for every key, so Lambda, Gamma
 // and gamma are per-row scalars and the intra-chunk scores have the closed
 // form P_rs = (q_r . k_s) lambda^(r-s), r >= s (the decay mask M_ij =
-// lambda^(i-j) of "Lightning Attention-2", §3.2.1 Alg. 1). The scores are one
+// lambda^(i-j) of "Lightning Attention-2", §3.2.1 Alg. 1). The per-token scalar
+// gate (G_t = gamma_t 1^T 1, Table 1 of the GLA paper, §4.1) has the same
+// structure with a data-dependent decay: with B_r the chunk's inclusive cumulative
+// log gate, P_rs = (q_r . k_s) exp(B_r - B_s), Q rows scale by exp(B_r), K rows by
+// exp(B_end - B_r) and gamma = exp(B_end), every factor <= 1. The scores are one
 // plain q k^T product on the tensor cores (tcgen05), scaled and masked when
 // they are read out; no per-element exponentials of q or k are needed.
 // Items of a CTA run in order (load, product, readout), so the SM is kept busy by
@@ -545,9 +556,16 @@ constexpr int prep_uniform_bufs() { return 1; }
 template <int DK, int NTU>
 constexpr int prep_uniform_ctas_per_sm() { return DK > 128 ? 3 : (NTU == 128 ? 6 : 4); }
 template <int DK>
-constexpr int prep_uniform_smem() { return prep_uniform_bufs<DK>() * 2 * C * DK * 2 + 64 + 1024; }
+constexpr int prep_uniform_smem() { return prep_uniform_bufs<DK>() * 2 * C * DK * 2 + 64 + C * 4 + 1024; }
 
-template <int DK, int NTU>
+// L2 prefetch hints for the bytes [p, p + n) (n > 0) of a row of 4-byte values;
+// only addresses of elements inside the row are named.
+__device__ __forceinline__ void prefetch_row_l2(const float* p, int n) {
+    for (int i = 0; i < n; i += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + i));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p + n - 1));
+}
+
+template <int DK, int NTU, int GATE>
 __global__ void __launch_bounds__(NTU, prep_uniform_ctas_per_sm<DK, NTU>())
 gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                               const __grid_constant__ CUtensorMap tmA)
@@ -563,6 +581,7 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + NBUF * 2 * TILE * 2);   // [NBUF] tile loads
     uint64_t* mbar = cbar + 2;                                                  // score MMA
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(cbar + 3);
+    float* Lc = reinterpret_cast<float*>(cbar + 8);   // [C] cumulative log gate (per-token gate)
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     if (tid == 0) {
@@ -580,7 +599,8 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const int total = a.BH * a.nchunks;
-    const bool gated = a.gate != GLA_GATE_NONE;
+    constexpr bool gated = GATE != GLA_GATE_NONE;
+    constexpr bool tok = GATE == GLA_GATE_TOKEN_SCALAR;
     // the q/k tiles of an item (every box full-size: rows at or past T arrive as zeros)
     auto load = [&](int item, int b) {
         const int c = item % a.nchunks, bh = item / a.nchunks;
@@ -605,7 +625,7 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     const int c = item % a.nchunks, bh = item / a.nchunks, h = bh % a.H;
     const int t0 = c * C;
     const int nr = min(C, a.T - t0);
-    const float lam = gated ? a.log_g[h] : 0.f;   // log(lambda_h) <= 0
+    const float lam = GATE == GLA_GATE_HEAD_SCALAR ? a.log_g[h] : 0.f;   // log(lambda_h) <= 0
     const int cg = tid % NCG, rg = tid / NCG;
     const int col0 = cg * 8, row0 = rg * RPT;
     const int b = NBUF == 2 ? (it & 1) : 0;
@@ -629,10 +649,26 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
             const size_t row = (size_t)bh2 * a.T + (size_t)c2 * C;
             prefetch_l2(a.q + row * DK, (uint32_t)nr2 * DK * 2);
             prefetch_l2(a.k + row * DK, (uint32_t)nr2 * DK * 2);
+            if (tok) prefetch_row_l2(a.log_g + row, nr2);
         }
     }
-    if (gated)
+    if (gated && !tok)
         for (int col = tid; col < DK; col += NTU) a.gam[((size_t)bh * a.nchunks + c) * DK + col] = __expf(nr * lam);
+    if (tok && warp == 2) {
+        // inclusive cumulative log gate of the chunk's rows, two rows per lane; rows at or
+        // past T add 0 (the previous item's readers of Lc finished at its last barrier)
+        const float* gr = a.log_g + (size_t)bh * a.T + t0;
+        const float g0 = 2 * lane < nr ? gr[2 * lane] : 0.f;
+        const float g1 = 2 * lane + 1 < nr ? gr[2 * lane + 1] : 0.f;
+        float run = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, run, o);
+            if (lane >= o) run += u;
+        }
+        Lc[2 * lane] = run - g1;
+        Lc[2 * lane + 1] = run;
+    }
     // The tiles come from TMA and are not written here, so the product can start as soon
     // as they land; Q (.) Lambda (warps 2-3, meanwhile) and K (.) Gamma (warps 0-1, after
     // the readout) are per-row scalings of the same tiles.
@@ -650,6 +686,8 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
         if (tid == 0) atomicExch(a.status, ERR_PREP);
         break;
     }
+    if (tok)
+        for (int col = tid; col < DK; col += NTU) a.gam[((size_t)bh * a.nchunks + c) * DK + col] = __expf(Lc[C - 1]);
     // Q (pass 0) or K (pass 1), rows [r0, r1), by nth threads
     auto scale_rows = [&](int pass, int r0, int r1, int t, int nth) {
         const __nv_bfloat16* T = pass == 0 ? Qs : Ks;
@@ -657,6 +695,7 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
         for (int idx = r0 * NCG + t; idx < r1 * NCG; idx += nth) {
             const int row = idx / NCG, col = (idx % NCG) * 8;
             const float fac = row >= nr ? 0.f
+                            : tok ? (pass == 0 ? __expf(Lc[row]) : __expf(Lc[C - 1] - Lc[row]))
                             : pass == 0 ? __expf((row + 1) * lam)          // b_row / b_start
                                         : __expf((nr - 1 - row) * lam);    // b_end / b_row
             float v[8];
@@ -670,7 +709,7 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     // (named barrier 2); the K rows are split in proportion to the threads
     constexpr int KSPLIT = C * (NTU - 64) / NTU;
     if (warp < 2) {
-        ok = score_readout(tmem, mbar, mphase, nr, lam, Qs, &tmA, (bh * a.nchunks + c) * C, 2, NTU);
+        ok = score_readout<tok>(tmem, mbar, mphase, nr, lam, Qs, &tmA, (bh * a.nchunks + c) * C, 2, NTU, Lc);
         if (gated) scale_rows(1, KSPLIT, C, tid, 64);
     } else {
         if (gated) scale_rows(0, 0, C, tid - 64, NTU - 64);
@@ -706,7 +745,7 @@ bool map_rows(CUtensorMap* m, const void* base, int dk, int T, int BH) {
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int DK, int NTU>
+template <int DK, int NTU, int GATE>
 cudaError_t launch_prep_uniform_nt(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                                    const CUtensorMap& mA, int sms, cudaStream_t s)
 {
@@ -714,10 +753,10 @@ cudaError_t launch_prep_uniform_nt(const PrepArgs& a, const CUtensorMap& mq, con
     const int total = a.BH * a.nchunks;
     const int resident = prep_uniform_ctas_per_sm<DK, NTU>() * sms;
     const dim3 grid(total < resident ? total : resident);
-    cudaError_t e = cudaFuncSetAttribute(gla_chunk_prep_uniform_kernel<DK, NTU>,
+    cudaError_t e = cudaFuncSetAttribute(gla_chunk_prep_uniform_kernel<DK, NTU, GATE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    gla_chunk_prep_uniform_kernel<DK, NTU><<<grid, NTU, smem, s>>>(a, mq, mk, mA);
+    gla_chunk_prep_uniform_kernel<DK, NTU, GATE><<<grid, NTU, smem, s>>>(a, mq, mk, mA);
     return cudaGetLastError();
 }
 
@@ -725,8 +764,12 @@ template <int DK>
 cudaError_t launch_prep_uniform_dk(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                                    const CUtensorMap& mA, int sms, cudaStream_t s)
 {
-    return a.gate == GLA_GATE_NONE ? launch_prep_uniform_nt<DK, 128>(a, mq, mk, mA, sms, s)
-                                   : launch_prep_uniform_nt<DK, 256>(a, mq, mk, mA, sms, s);
+    switch (a.gate) {
+    case GLA_GATE_NONE: return launch_prep_uniform_nt<DK, 128, GLA_GATE_NONE>(a, mq, mk, mA, sms, s);
+    case GLA_GATE_HEAD_SCALAR: return launch_prep_uniform_nt<DK, 256, GLA_GATE_HEAD_SCALAR>(a, mq, mk, mA, sms, s);
+    case GLA_GATE_TOKEN_SCALAR: return launch_prep_uniform_nt<DK, 256, GLA_GATE_TOKEN_SCALAR>(a, mq, mk, mA, sms, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <int DK>

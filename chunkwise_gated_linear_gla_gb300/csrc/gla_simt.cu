@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
     const Tin* v = static_cast<const Tin*>(a.v) + (size_t)bh * a.T * a.dv;
     Tin* O = static_cast<Tin*>(a.O) + (size_t)bh * a.T * a.dv;
     const float* g = (a.gate == GLA_GATE_PER_KEY) ? a.log_g + (size_t)bh * a.T * dk : nullptr;
+    const float* gtok = (a.gate == GLA_GATE_TOKEN_SCALAR) ? a.log_g + (size_t)bh * a.T : nullptr;
     const float lam = (a.gate == GLA_GATE_HEAD_SCALAR) ? a.log_g[h] : 0.f;
 
     // S <- S0 tile (or 0)
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
                 float gl = 0.f;
                 if (r < nr) {
                     if (g) gl = g[(size_t)(t0 + r) * dk + kk];
+                    else if (gtok) gl = gtok[t0 + r];
                     else gl = lam;
                 }
                 run += gl;

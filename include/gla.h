@@ -19,6 +19,10 @@
  *                        RetNet; log_g is float[H] = log(lambda_h).
  *   GLA_GATE_PER_KEY     alpha_t in (0,1]^dk, data dependent (GLA, §4.1);
  *                        log_g is float[B,H,T,dk] = log(alpha_t).
+ *   GLA_GATE_TOKEN_SCALAR alpha_t = gamma_t for every key, data dependent:
+ *                        G_t = gamma_t 1^T 1, the Mamba-2 / mLSTM / Gated
+ *                        Retention rows of the GLA paper's Table 1 (§4.1);
+ *                        log_g is float[B,H,T] = log(gamma_t).
  *
  * Layouts. Every tensor is dense, row-major, last dimension contiguous:
  *   q, k   [B,H,T,dk]   dtype (bf16 or fp32)
@@ -66,7 +70,8 @@ typedef enum { GLA_BF16 = 0, GLA_FP32 = 1 } gla_dtype;
 typedef enum {
     GLA_GATE_NONE = 0,
     GLA_GATE_HEAD_SCALAR = 1,
-    GLA_GATE_PER_KEY = 2
+    GLA_GATE_PER_KEY = 2,
+    GLA_GATE_TOKEN_SCALAR = 3
 } gla_gate;
 
 /* Which kernels run. AUTO picks the tcgen05 tensor-core path for bf16 inputs

@@ -46,7 +46,7 @@ def _device_run(x, w, want_state=True, path=bnd.GLA_PATH_AUTO):
 
 def _unit_bytes(w):
     e = 2 if w.dtype == torch.bfloat16 else 4
-    g = w.T * w.dk * 4 if w.gate == gi.GATE_PER_KEY else 0
+    g = w.T * w.dk * 4 if w.gate == gi.GATE_PER_KEY else w.T * 4 if w.gate == gi.GATE_TOKEN_SCALAR else 0
     return 2 * w.T * w.dk * e + 2 * w.T * w.dv * e + g + 2 * w.dk * w.dv * 4
 
 
@@ -58,6 +58,8 @@ CASES = [
                                              gate=gi.GATE_PER_KEY, s0_std=0.02), 4),
     ("head slices, scalar gate", gi.Workload("t", B=1, H=5, T=300, dk=128, dv=128, dtype=torch.bfloat16,
                                               gate=gi.GATE_HEAD_SCALAR, s0_std=0.02), 3),
+    ("head slices, per-token gate", gi.Workload("t", B=1, H=6, T=333, dk=128, dv=128, dtype=torch.bfloat16,
+                                                 gate=gi.GATE_TOKEN_SCALAR, s0_std=0.02), 4),
     ("head slices of two rows, scalar gate", gi.Workload("t", B=2, H=4, T=100, dk=64, dv=128,
                                                           dtype=torch.bfloat16, gate=gi.GATE_HEAD_SCALAR,
                                                           s0_std=0.02), 8),

@@ -38,7 +38,7 @@ def test_fp32_workload_full_size():
     assert_close(ST, STref, torch.float32, "ST")
 
 
-@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
 @pytest.mark.parametrize("T", [1, 15, 16, 63, 65, 200])
 def test_fp32_gates_ragged(gate, T):
     w = gi.Workload("t", B=2, H=3, T=T, dk=32, dv=80, dtype=torch.float32, gate=gate, s0_std=0.1)
@@ -47,7 +47,7 @@ def test_fp32_gates_ragged(gate, T):
     assert_close(ST, STref, torch.float32, "ST")
 
 
-@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
 def test_bf16_simt(gate):
     w = gi.Workload("t", B=1, H=2, T=130, dk=64, dv=96, dtype=torch.bfloat16, gate=gate, s0_std=0.02)
     x, O, ST, Oref, STref = _run(w, seed=3)

@@ -89,7 +89,7 @@ def test_prep_stage_outputs():
 
 # ---------------------------------------------------------------- small shapes
 
-@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY])
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
 def test_gates_and_ragged_T(gate, T):
     w = gi.Workload("t", B=2, H=2, T=T, dk=128, dv=128, dtype=torch.bfloat16, gate=gate, s0_std=0.02)
@@ -109,7 +109,7 @@ def test_forced_segments(nseg):
     _check_full(w, seed=3, force_segments=nseg)
 
 
-@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR])
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_TOKEN_SCALAR])
 def test_forced_segments_other_gates(gate):
     w = gi.Workload("t", B=1, H=2, T=700, dk=64, dv=128, dtype=torch.bfloat16, gate=gate, s0_std=0.02)
     _check_full(w, seed=4, force_segments=5)
@@ -220,6 +220,42 @@ def test_full_gla_1p3b_sampled():
 
 def test_full_gla_long_sampled():
     _sampled("gla_long", [(0, 0), (0, 3)])
+
+
+def test_full_token_gate_sampled():
+    _sampled("token_gate", [(0, 0), (7, 3), (2, 1)])
+
+
+# ---------------------------------------------------------------- per-token scalar gate
+
+@pytest.mark.parametrize("dk", [64, 128, 256])
+def test_token_gate_head_sizes(dk):
+    w = gi.Workload("t", B=2, H=2, T=300, dk=dk, dv=256, dtype=torch.bfloat16, gate=gi.GATE_TOKEN_SCALAR,
+                    s0_std=0.02)
+    _check_full(w, seed=30 + dk)
+
+
+@pytest.mark.parametrize("dist", ["steep", "const:-60", "zero"])
+def test_token_gate_extremes(dist):
+    """log gamma_t = -U(0,4), a constant -60 (every earlier token forgotten) and 0 (no decay):
+    every factor stays <= 1, so the tensor path needs no fallback."""
+    w = gi.Workload("t", B=1, H=2, T=200, dk=128, dv=128, dtype=torch.bfloat16, gate=gi.GATE_TOKEN_SCALAR,
+                    gate_dist=dist, s0_std=0.3)
+    _check_full(w, seed=35)
+
+
+def test_token_gate_equals_per_key_broadcast():
+    """The per-token gate through its own prep equals the per-key path fed the same gate on every key."""
+    w = gi.Workload("t", B=2, H=2, T=190, dk=128, dv=128, dtype=torch.bfloat16, gate=gi.GATE_TOKEN_SCALAR,
+                    s0_std=0.05)
+    x = gi.make_inputs(w, seed=36)
+    c = _dev(x)
+    O1, S1 = gla.forward(c["q"], c["k"], c["v"], c["log_g"], c["S0"], path=gla.GLA_PATH_TENSOR)
+    gk = c["log_g"][..., None].expand(*c["q"].shape).contiguous()
+    O2, S2 = gla.forward(c["q"], c["k"], c["v"], gk, c["S0"], path=gla.GLA_PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert_close(to_np(O1), to_np(O2).astype(np.float64), torch.bfloat16, "O token vs per-key")
+    assert_close(to_np(S1), to_np(S2).astype(np.float64), torch.bfloat16, "ST token vs per-key")
 
 
 # ---------------------------------------------------------------- degenerate and extreme shapes
