@@ -41,8 +41,8 @@ FALLBACK_BF16 = 1900.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload to time (default: the 1.3B-shaped GLA layer the metric is quoted on)")
@@ -131,7 +131,8 @@ def planned_segments(w, force, sms):
 
 def kernel_source_sha(name):
     files = {"gla_chunk_fwd": ["gla_chunk_fwd.cu", "sm100.cuh"],
-             "gla_chunk_prep": ["gla_prep.cu", "sm100.cuh"]}.get(name, [])
+             "gla_chunk_prep": ["gla_prep.cu", "sm100.cuh"],
+             "gla_chunk_state": ["gla_state.cu", "sm100.cuh"]}.get(name, [])
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "chunkwise_gated_linear_gla_gb300", "csrc", f), "rb") as fh:
@@ -139,11 +140,12 @@ def kernel_source_sha(name):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(name):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+def ncu_traffic(workload, name):
+    """DRAM bytes per launch of kernel `name` on `workload` from the committed ncu summary,
+    if one was captured for that pair and the kernel's source still matches it."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-            d = json.load(f)[name]
+            d = json.load(f)[workload][name]
         if d.get("source_sha") != kernel_source_sha(name):
             return None
         return float(d["dram_bytes_per_launch"])
@@ -472,7 +474,7 @@ def main():
         "tflops": tflops, "tflops_frac_bf16_peak": tflops / bf16,
         "path_gbs": byts * world / (step_ms * 1e-3) / 1e9, "path_frac_hbm": byts / (step_ms * 1e-3) / 1e9 / hbm,
         "roofline": {"kernel": dname, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                     "frac": ach / hbm, "traffic": ncu_traffic(dname), "peak_source": src,
+                     "frac": ach / hbm, "traffic": ncu_traffic(w.name, dname), "peak_source": src,
                      "bytes_per_launch": dbytes},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

@@ -1,6 +1,6 @@
 // gla_state_scan: the short serial recurrence over sequence segments that
 // lets small B*H fill the GPU. Each segment s was first run from a zero state
-// (gla_chunk_fwd in state-only mode), giving S*_s. Because the recurrence is
+// (gla_chunk_state), giving S*_s. Because the recurrence is
 // linear in S and the gate only scales rows, the true state entering segment
 // s+1 is
 //     S_in(s+1) = Diag(Gamma_s) S_in(s) + S*_s,   Gamma_s = prod over the
