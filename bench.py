@@ -267,9 +267,16 @@ def cpu_model():
         for line in info.splitlines():
             if line.startswith(key) and ":" in line:
                 return line.split(":", 1)[1].strip()
-    parts = sorted({line.split(":", 1)[1].strip() for line in info.splitlines()
-                    if line.startswith(("CPU implementer", "CPU part")) and ":" in line})
-    return f"{platform.machine()} ({', '.join(parts)})" if parts else platform.machine()
+    # Arm kernels name no model: map the (implementer, part) codes of common server cores
+    arm = {("0x41", "0xd0c"): "Arm Neoverse N1", ("0x41", "0xd40"): "Arm Neoverse V1",
+           ("0x41", "0xd49"): "Arm Neoverse N2", ("0x41", "0xd4f"): "Arm Neoverse V2"}
+    get = lambda key: sorted({line.split(":", 1)[1].strip() for line in info.splitlines()
+                              if line.startswith(key) and ":" in line})
+    impl, part = get("CPU implementer"), get("CPU part")
+    if len(impl) == 1 and len(part) == 1 and (impl[0], part[0]) in arm:
+        return f"{arm[(impl[0], part[0])]} ({platform.machine()})"
+    codes = impl + part
+    return f"{platform.machine()} ({', '.join(codes)})" if codes else platform.machine()
 
 
 def cpu_one_core(w):
