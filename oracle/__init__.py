@@ -8,7 +8,8 @@ arrays drawn by the seeded generator.
 The oracle is the token-by-token recurrence of "Gated Linear Attention
 Transformers with Hardware-Efficient Training", §4.1 Eq. 3, written in C
 (``gla_oracle.c``) and evaluated in fp64 on exactly the values the GPU sees
-(bf16 inputs are widened losslessly).
+(bf16 inputs are widened losslessly). Its backward is the same recurrence's
+adjoint (reverse-mode differentiation written out), also in C and fp64.
 """
 from __future__ import annotations
 
@@ -48,6 +49,10 @@ def _load():
             d = ctypes.POINTER(ctypes.c_double)
             lib.gla_oracle_fwd.restype = ctypes.c_int
             lib.gla_oracle_fwd.argtypes = [d, d, d, d, ctypes.c_int, d, d, d,
+                                           ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                           ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_int]
+            lib.gla_oracle_bwd.restype = ctypes.c_int
+            lib.gla_oracle_bwd.argtypes = [d, d, d, d, ctypes.c_int, d, d, d, d, d, d, d, d,
                                            ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                            ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_int]
             _lib = lib
@@ -102,6 +107,31 @@ def gla_forward(q, k, v, log_g=None, gate=None, S0=None, want_state=True,
     if rc != 0:
         raise RuntimeError(f"gla_oracle_fwd failed with status {rc}")
     return O, ST
+
+
+def gla_backward(q, k, v, log_g, gate, S0, dO, dST=None, want_dS0=True, nthreads=None, mutant=0):
+    """Gradients of L = <dO, O> + <dST, S_T> through the recurrence (the adjoint
+    recurrence, fp64). Returns (dq, dk, dv, dlog_g, dS0) as numpy arrays;
+    dlog_g is shaped like log_g (None without a gate), dS0 None unless wanted."""
+    qa, ka, va = _f64(q), _f64(k), _f64(v)
+    B, H, T, dk = qa.shape
+    dv = va.shape[-1]
+    if gate is None:
+        if log_g is None:
+            gate = GATE_NONE
+        else:
+            gate = {1: GATE_HEAD_SCALAR, 3: GATE_TOKEN_SCALAR}.get(np.ndim(_f64(log_g)), GATE_PER_KEY)
+    ga = _f64(log_g) if gate != GATE_NONE else None
+    sa, doa, dsta = _f64(S0), _f64(dO), _f64(dST)
+    dq = np.empty((B, H, T, dk)); dk_ = np.empty((B, H, T, dk)); dv_ = np.empty((B, H, T, dv))
+    dg = None if gate == GATE_NONE else np.empty(ga.shape)
+    dS0 = np.empty((B, H, dk, dv)) if want_dS0 else None
+    rc = _load().gla_oracle_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), int(gate), _ptr(sa), _ptr(doa),
+                                _ptr(dsta), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dS0),
+                                B, H, T, dk, dv, int(nthreads or default_threads()), int(mutant))
+    if rc != 0:
+        raise RuntimeError(f"gla_oracle_bwd failed with status {rc}")
+    return dq, dk_, dv_, dg, dS0
 
 
 def gla_forward_rows(q, k, v, log_g, gate, S0, bh_list, nthreads=None):

@@ -210,3 +210,206 @@ int gla_oracle_fwd(const double* q, const double* k, const double* v,
     free(jobs);
     return st;
 }
+
+/* ---------------------------------------------------------------- backward
+ *
+ * Gradients of a scalar loss L through the recurrence, given dO = dL/dO and
+ * dST = dL/dS_T (NULL: zero). This is reverse-mode differentiation of Eq. 3
+ * written out as the adjoint recurrence, with D_t = dL/dS_t counting every
+ * later use of S_t:
+ *   D_{T-1} = dST + q_{T-1}^T do_{T-1},
+ *   D_t     = Diag(alpha_{t+1}) D_{t+1} + q_t^T do_t,
+ *   dq_t = S_t do_t^T,   dk_t = D_t v_t^T,   dv_t = k_t D_t,
+ *   dlog alpha_t[i] = alpha_t[i] sum_j D_t[i][j] S_{t-1}[i][j],
+ *   dS0 = Diag(alpha_0) D_0.
+ * Per gate mode, the gradient of log_g is dlog alpha itself (per key), its
+ * sum over keys (per token) or its sum over keys, tokens and batch rows (per
+ * head). S_{t-1} is needed in reverse order: the states at every CK-th step
+ * are kept and the ones between recomputed from them by the same forward
+ * steps, so every value is the one a run storing all states would use.
+ *
+ * Backward mutants (tests only): 11 dlog alpha without the factor alpha_t;
+ * 12 D decayed before q_t^T do_t is added; 13 dq_t read from S_{t-1};
+ * 14 the decay of D skipped at t = 0 (dS0 = D_0).
+ */
+typedef struct {
+    const double *q, *k, *v, *log_g, *S0, *dO, *dST;
+    double *gq, *gk, *gv, *dlg, *dS0; /* gradients of q, k, v; dlg: [T][dk] dlog alpha of this (b, h) */
+    long H, T, dk, dv, bh;
+    int gate, mutant, status;
+} bjob_t;
+
+static double bgate(const bjob_t* J, long t, long i)
+{
+    if (J->gate == 0) return 1.0;
+    if (J->gate == 1) return exp(J->log_g[J->bh % J->H]);
+    if (J->gate == 3) return exp(J->log_g[J->bh * J->T + t]);
+    return exp(J->log_g[(J->bh * J->T + t) * J->dk + i]);
+}
+
+/* S_out = Diag(alpha_t) S_in + k_t^T v_t (Eq. 3), full width dv */
+static void bstep(const bjob_t* J, long t, const double* Sin, double* Sout)
+{
+    const long dk = J->dk, dv = J->dv;
+    const double* kt = J->k + (J->bh * J->T + t) * dk;
+    const double* vt = J->v + (J->bh * J->T + t) * dv;
+    for (long i = 0; i < dk; ++i) {
+        const double a = bgate(J, t, i), ki = kt[i];
+        for (long j = 0; j < dv; ++j) Sout[i * dv + j] = a * Sin[i * dv + j] + ki * vt[j];
+    }
+}
+
+static void bwd_job(bjob_t* J)
+{
+    const long dk = J->dk, dv = J->dv, T = J->T, n = dk * dv;
+    long CK = 64;
+    while (CK * CK < T) CK *= 2;
+    const long nck = (T + CK - 1) / CK;
+    double* ck = (double*)malloc((size_t)(nck > 0 ? nck : 1) * n * sizeof(double));
+    double* blk = (double*)malloc((size_t)(CK + 1) * n * sizeof(double));
+    double* D = (double*)malloc((size_t)n * sizeof(double));
+    double* S = (double*)malloc((size_t)n * sizeof(double));
+    double* S2 = (double*)malloc((size_t)n * sizeof(double));
+    if (!ck || !blk || !D || !S || !S2) {
+        J->status = 1;
+        free(ck); free(blk); free(D); free(S); free(S2);
+        return;
+    }
+    /* forward, keeping the state entering every CK-th step */
+    for (long e = 0; e < n; ++e) S[e] = J->S0 ? J->S0[J->bh * n + e] : 0.0;
+    for (long t = 0; t < T; ++t) {
+        if (t % CK == 0) memcpy(ck + (t / CK) * n, S, (size_t)n * sizeof(double));
+        bstep(J, t, S, S2);
+        double* tmp = S; S = S2; S2 = tmp;
+    }
+    /* reverse */
+    for (long e = 0; e < n; ++e) D[e] = J->dST ? J->dST[J->bh * n + e] : 0.0;
+    for (long c = nck - 1; c >= 0; --c) {
+        const long t0 = c * CK, t1 = (t0 + CK < T) ? t0 + CK : T;
+        memcpy(blk, ck + c * n, (size_t)n * sizeof(double));
+        for (long t = t0; t < t1; ++t) bstep(J, t, blk + (t - t0) * n, blk + (t - t0 + 1) * n);
+        for (long t = t1 - 1; t >= t0; --t) {
+            const double* Sprev = blk + (t - t0) * n;
+            const double* Scur = blk + (t - t0 + 1) * n;
+            const double* qt = J->q + (J->bh * T + t) * dk;
+            const double* kt = J->k + (J->bh * T + t) * dk;
+            const double* vt = J->v + (J->bh * T + t) * dv;
+            const double* dot = J->dO + (J->bh * T + t) * dv;
+            double* dqt = J->gq + (J->bh * T + t) * dk;
+            double* dkt = J->gk + (J->bh * T + t) * dk;
+            double* dvt = J->gv + (J->bh * T + t) * dv;
+            if (J->mutant == 12)
+                for (long i = 0; i < dk; ++i) {
+                    const double a = bgate(J, t, i);
+                    for (long j = 0; j < dv; ++j) D[i * dv + j] *= a;
+                }
+            /* D_t = (decayed later adjoint) + q_t^T do_t */
+            for (long i = 0; i < dk; ++i)
+                for (long j = 0; j < dv; ++j) D[i * dv + j] += qt[i] * dot[j];
+            const double* Sq = (J->mutant == 13) ? Sprev : Scur;
+            for (long i = 0; i < dk; ++i) {
+                double aq = 0.0, ak = 0.0, ag = 0.0;
+                for (long j = 0; j < dv; ++j) {
+                    aq += Sq[i * dv + j] * dot[j];
+                    ak += D[i * dv + j] * vt[j];
+                    ag += D[i * dv + j] * Sprev[i * dv + j];
+                }
+                dqt[i] = aq;
+                dkt[i] = ak;
+                J->dlg[t * dk + i] = (J->mutant == 11) ? ag : bgate(J, t, i) * ag;
+            }
+            for (long j = 0; j < dv; ++j) {
+                double a = 0.0;
+                for (long i = 0; i < dk; ++i) a += kt[i] * D[i * dv + j];
+                dvt[j] = a;
+            }
+            /* the part of dL/dS_{t-1} that flows through S_t */
+            if (J->mutant != 12 && !(J->mutant == 14 && t == 0))
+                for (long i = 0; i < dk; ++i) {
+                    const double a = bgate(J, t, i);
+                    for (long j = 0; j < dv; ++j) D[i * dv + j] *= a;
+                }
+        }
+    }
+    if (J->dS0) memcpy(J->dS0 + J->bh * n, D, (size_t)n * sizeof(double));
+    free(ck); free(blk); free(D); free(S); free(S2);
+}
+
+typedef struct {
+    bjob_t* jobs;
+    long njobs, next;
+    pthread_mutex_t mu;
+} bpool_t;
+
+static void* bworker(void* arg)
+{
+    bpool_t* P = (bpool_t*)arg;
+    for (;;) {
+        pthread_mutex_lock(&P->mu);
+        long idx = P->next++;
+        pthread_mutex_unlock(&P->mu);
+        if (idx >= P->njobs) break;
+        bwd_job(&P->jobs[idx]);
+    }
+    return NULL;
+}
+
+/* Returns 0 on success, 1 on bad arguments, 2 on allocation failure.
+ * dq, dk [B,H,T,dk]; dv [B,H,T,dv]; dlog_g shaped like log_g (NULL or
+ * gate 0: not written); dS0 [B,H,dk,dv] or NULL. One job per (b, h). */
+int gla_oracle_bwd(const double* q, const double* k, const double* v,
+                   const double* log_g, int gate, const double* S0,
+                   const double* dO, const double* dST,
+                   double* dq, double* dk_out, double* dv_out, double* dlog_g, double* dS0,
+                   long B, long H, long T, long dk, long dv, int nthreads, int mutant)
+{
+    if (!dO || !dq || !dk_out || !dv_out || B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
+    if (T > 0 && (!q || !k || !v)) return 1;
+    if (gate < 0 || gate > 3 || (gate != 0 && !log_g)) return 1;
+    const long BH = B * H;
+    double* dlg = (double*)calloc((size_t)(BH * T * dk > 0 ? BH * T * dk : 1), sizeof(double));
+    bjob_t* jobs = (bjob_t*)calloc((size_t)BH, sizeof(bjob_t));
+    if (!dlg || !jobs) { free(dlg); free(jobs); return 2; }
+    for (long bh = 0; bh < BH; ++bh) {
+        bjob_t* J = &jobs[bh];
+        J->q = q; J->k = k; J->v = v; J->log_g = log_g; J->S0 = S0; J->dO = dO; J->dST = dST;
+        J->gq = dq; J->gk = dk_out; J->gv = dv_out; J->dlg = dlg + bh * T * dk; J->dS0 = dS0;
+        J->H = H; J->T = T; J->dk = dk; J->dv = dv; J->bh = bh; J->gate = gate; J->mutant = mutant;
+    }
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > BH) nthreads = (int)BH;
+    bpool_t P;
+    P.jobs = jobs; P.njobs = BH; P.next = 0;
+    pthread_mutex_init(&P.mu, NULL);
+    pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
+    int started = 0;
+    if (th)
+        for (int i = 0; i + 1 < nthreads; ++i)
+            if (pthread_create(&th[started], NULL, bworker, &P) == 0) ++started;
+    bworker(&P);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&P.mu);
+    int st = 0;
+    for (long i = 0; i < BH; ++i) if (jobs[i].status) st = 2;
+    if (st == 0 && dlog_g && gate != 0) {
+        if (gate == 2) {
+            memcpy(dlog_g, dlg, (size_t)(BH * T * dk) * sizeof(double));
+        } else if (gate == 3) {
+            for (long bt = 0; bt < BH * T; ++bt) {
+                double s = 0.0;
+                for (long i = 0; i < dk; ++i) s += dlg[bt * dk + i];
+                dlog_g[bt] = s;
+            }
+        } else {
+            for (long h = 0; h < H; ++h) {
+                double s = 0.0;
+                for (long b = 0; b < B; ++b)
+                    for (long e = 0; e < T * dk; ++e) s += dlg[(b * H + h) * T * dk + e];
+                dlog_g[h] = s;
+            }
+        }
+    }
+    free(dlg); free(jobs);
+    return st;
+}
