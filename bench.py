@@ -48,6 +48,8 @@ def parse():
                     help="workload to time (default: the 1.3B-shaped GLA layer the metric is quoted on)")
     ap.add_argument("--segments", type=int, default=0, help="force the sequence split (0: planner decides)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--direction", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd: time the backward pass (gla_bwd) instead and print its own line")
     ap.add_argument("--cpu-sample-rows", type=int, default=8,
                     help="batch rows of the workload the oracle runs for cpu_baseline")
     ap.add_argument("--ref-sample-rows", type=int, default=1,
@@ -314,12 +316,112 @@ def cpu_baseline(w, rows):
             "cpu_model": cpu_model(), "value_1core": one, "sample_1core": one_sample}
 
 
+# fp32 FFMA peak from the nominal unit counts: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+BWD_METRIC = "GLA bwd tokens/s at B=8,T=2048,dk256,dv512 (gradients of q, k, v, log_g, S0)"
+
+
+def algorithmic_bwd(w):
+    """FLOPs of the backward per token per head: 10 dk dv (the forward state sweep, the
+    gradient-of-state update, and dq, dk, dv through the chunk states) + 2 (C+1)(dk+dv)
+    (the intra-chunk scores and their three products), C = 16 on the CUDA-core path."""
+    C = 16
+    return w.B * w.H * w.T * (10 * w.dk * w.dv + 2 * (C + 1) * (w.dk + w.dv))
+
+
+def run_backward(args, w):
+    """Times gla_bwd (inputs resident in HBM, L2 flushed between steps) and prints one line."""
+    import torch
+    import chunkwise_gated_linear_gla_gb300 as gla
+    from chunkwise_gated_linear_gla_gb300 import binding as bnd
+    from chunkwise_gated_linear_gla_gb300 import build as gbuild
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    torch.cuda.set_device(0)
+    gbuild.build()
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        ws_ = w.with_(B=1, H=1, T=min(w.T, 512))
+        xs = gi.make_inputs(ws_, seed=0)
+        if xs["gate"] == gi.GATE_HEAD_SCALAR:
+            xs["log_g"] = xs["log_g"][:1]
+        dOs = torch.randn((1, 1, ws_.T, w.dv)).to(w.dtype)
+        cores = oracle.default_threads()
+        t0 = time.perf_counter()
+        oracle.gla_backward(xs["q"], xs["k"], xs["v"], xs["log_g"], xs["gate"], xs["S0"], dOs, None, nthreads=cores)
+        dt = time.perf_counter() - t0
+        cpu = {"value": ws_.T / dt / w.H, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"1 head x T={ws_.T} (one (b,h) job runs on one thread), {dt:.2f} s, {cpu_model()}"}
+    x = gi.make_inputs(w, seed=0)
+    dev = torch.device("cuda", 0)
+    c = lambda t: None if t is None else t.to(dev)
+    q, k, v, g, S0 = c(x["q"]), c(x["k"]), c(x["v"]), c(x["log_g"]), c(x["S0"])
+    gen = torch.Generator().manual_seed(1)
+    dO = torch.randn((w.B, w.H, w.T, w.dv), generator=gen).to(w.dtype).to(dev)
+    dST = (torch.randn((w.B, w.H, w.dk, w.dv), generator=gen) * 0.1).to(dev)
+    f32 = lambda *shape: torch.empty(shape, dtype=torch.float32, device=dev)
+    dq, dk, dv = f32(w.B, w.H, w.T, w.dk), f32(w.B, w.H, w.T, w.dk), f32(w.B, w.H, w.T, w.dv)
+    dg = None if g is None else torch.empty(g.shape, dtype=torch.float32, device=dev)
+    dS0 = f32(w.B, w.H, w.dk, w.dv)
+    p = bnd.make_bwd_params(q, k, v, g, S0, dO, dST, dq, dk, dv, dg, dS0, gate=x["gate"])
+    nbytes = bnd.gla_bwd_workspace_size(p)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), nbytes
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_(); clean.sum()
+        bnd.gla_bwd(p, stream)
+    torch.cuda.synchronize()
+    if bnd.gla_device_status(stream) != 0:
+        raise SystemExit("device status error after warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = Clocks(0)
+    clocks.start()
+    for a, b in evs:
+        flush.zero_(); clean.sum()
+        a.record(stream)
+        bnd.gla_bwd(p, stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    times = sorted(a.elapsed_time(b) for a, b in evs)
+    ms = sum(times) / len(times)
+    flops = algorithmic_bwd(w)
+    tflops = flops / (ms * 1e-3) / 1e12
+    launches = 4 + (1 if w.gate in (gi.GATE_TOKEN_SCALAR, gi.GATE_HEAD_SCALAR) else 0) - (1 if w.gate == 0 else 0)
+    line = {
+        "metric": BWD_METRIC, "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if w.dtype == torch.float32 else "bf16 in, f32 arithmetic",
+        "data": "synthetic (seeded inputs of the workload; dO ~ N(0,1), dST ~ 0.1 N(0,1))",
+        "config": {"workload": f"{w.name} backward: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
+                               f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar'][w.gate]}",
+                   "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",
+                   "workspace_bytes": nbytes},
+        "roofline": {"kernel": "gla_bwd (CUDA cores, all stages)", "bound": "alu", "achieved": tflops,
+                     "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tflops / FP32_ALU_TFLOPS, "traffic": None,
+                     "peak_source": "nominal fp32 FFMA rate: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz"},
+        "timing": {"mean_ms": ms, "median_ms": times[len(times) // 2], "min_ms": times[0]},
+        "cpu_baseline": cpu,
+        "e2e": None,
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from chunkwise_gated_linear_gla_gb300 import inputs as gi
     w = workload(args)
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if args.direction == "bwd":
+        run_backward(args, w)
         return
 
     import torch

@@ -21,7 +21,8 @@ GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT = 0, 1, 2
 # Every symbol include/gla.h declares.
 EXPORTED = ("gla_fwd", "gla_fwd_ex", "gla_fwd_workspace_size", "gla_fwd_num_stages",
             "gla_fwd_stage", "gla_fwd_stage_name", "gla_device_status", "gla_status_string",
-            "gla_version", "gla_fwd_noalloc", "gla_fwd_host", "gla_host_release")
+            "gla_version", "gla_fwd_noalloc", "gla_fwd_host", "gla_host_release", "gla_bwd",
+            "gla_bwd_workspace_size")
 
 
 class GlaError(RuntimeError):
@@ -40,6 +41,20 @@ class gla_fwd_params(ctypes.Structure):
         ("dtype", ctypes.c_int), ("gate", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("force_segments", ctypes.c_int), ("path", ctypes.c_int),
+    ]
+
+
+class gla_bwd_params(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("log_g", ctypes.c_void_p), ("S0", ctypes.c_void_p),
+        ("grad_O", ctypes.c_void_p), ("grad_ST", ctypes.c_void_p),
+        ("grad_q", ctypes.c_void_p), ("grad_k", ctypes.c_void_p), ("grad_v", ctypes.c_void_p),
+        ("grad_log_g", ctypes.c_void_p), ("grad_S0", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
+        ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("gate", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -80,6 +95,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.gla_fwd_stage.argtypes = [P, i, vp]
         lib.gla_fwd_stage_name.restype = ctypes.c_char_p
         lib.gla_fwd_stage_name.argtypes = [P, i]
+        lib.gla_bwd.restype = st
+        lib.gla_bwd.argtypes = [ctypes.POINTER(gla_bwd_params), vp]
+        lib.gla_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.gla_bwd_workspace_size.argtypes = [ctypes.POINTER(gla_bwd_params)]
         lib.gla_fwd_host.restype = st
         lib.gla_fwd_host.argtypes = [P, ctypes.c_size_t, vp]
         lib.gla_host_release.restype = st
@@ -162,6 +181,62 @@ def gla_host_release(check=True) -> int:
     if check:
         _check(s, "gla_host_release")
     return s
+
+
+def gla_bwd(p: gla_bwd_params, stream=None, check=True) -> int:
+    s = load().gla_bwd(ctypes.byref(p), _stream(stream))
+    if check:
+        _check(s, "gla_bwd")
+    return s
+
+
+def gla_bwd_workspace_size(p: gla_bwd_params) -> int:
+    return int(load().gla_bwd_workspace_size(ctypes.byref(p)))
+
+
+def make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dlog_g, dS0, gate=None,
+                    workspace=None) -> gla_bwd_params:
+    """Fill gla_bwd_params from torch tensors (shapes read from q and v)."""
+    import torch
+    B, H, T, dk_ = q.shape
+    if gate is None:
+        if log_g is None:
+            gate = GLA_GATE_NONE
+        else:
+            gate = {1: GLA_GATE_HEAD_SCALAR, 3: GLA_GATE_TOKEN_SCALAR}.get(log_g.dim(), GLA_GATE_PER_KEY)
+    p = gla_bwd_params()
+    p.q, p.k, p.v, p.log_g, p.S0 = _ptr(q), _ptr(k), _ptr(v), _ptr(log_g), _ptr(S0)
+    p.grad_O, p.grad_ST = _ptr(dO), _ptr(dST)
+    p.grad_q, p.grad_k, p.grad_v, p.grad_log_g, p.grad_S0 = _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlog_g), _ptr(dS0)
+    p.B, p.H, p.T, p.dk, p.dv = B, H, T, dk_, v.shape[-1]
+    p.dtype = GLA_BF16 if q.dtype == torch.bfloat16 else GLA_FP32
+    p.gate = gate
+    p.workspace = _ptr(workspace)
+    p.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return p
+
+
+def backward(q, k, v, log_g, S0, dO, dST=None, gate=None, want_dS0=True, stream=None):
+    """Allocate the gradients and the workspace with torch, then call gla_bwd.
+
+    Returns (dq, dk, dv, dlog_g, dS0), fp32; dlog_g is None without a gate and
+    dS0 None unless wanted.
+    """
+    import torch
+    B, H, T, dk_ = q.shape
+    dv_ = v.shape[-1]
+    dev = q.device
+    dq = torch.empty((B, H, T, dk_), dtype=torch.float32, device=dev)
+    dk = torch.empty((B, H, T, dk_), dtype=torch.float32, device=dev)
+    dv = torch.empty((B, H, T, dv_), dtype=torch.float32, device=dev)
+    dg = None if log_g is None else torch.empty(log_g.shape, dtype=torch.float32, device=dev)
+    dS0 = torch.empty((B, H, dk_, dv_), dtype=torch.float32, device=dev) if want_dS0 else None
+    p = make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dg, dS0, gate)
+    n = gla_bwd_workspace_size(p)
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), n
+    gla_bwd(p, stream)
+    return dq, dk, dv, dg, dS0
 
 
 def gla_fwd_workspace_size(p: gla_fwd_params) -> int:

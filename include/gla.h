@@ -180,6 +180,53 @@ gla_status gla_fwd_host(const gla_fwd_params* p, size_t slice_bytes, cudaStream_
 /* Returns the pages of the current device's gla_fwd_host pool to the driver. */
 gla_status gla_host_release(void);
 
+/*
+ * gla_bwd — the backward pass: gradients of a scalar loss L through the
+ * forward pass described by the same inputs, given grad_O = dL/dO and
+ * grad_ST = dL/dS_T (NULL: zero). It returns dL/dq, dL/dk, dL/dv, dL/dlog_g
+ * (shaped like log_g: per key, per token, or per head summed over batch
+ * rows) and dL/dS0 (even when S0 is NULL, i.e. zero). The chunkwise form
+ * follows the GLA paper's §3.3 / §4.2: a forward sweep keeps the state after
+ * every 16-row chunk, a reverse sweep carries dL/dS through the chunks, and
+ * the gate gradient is the reverse cumulative sum over tokens of
+ * q (.) dq - k (.) dk (plus rowsum(grad_ST (.) S_T) at the last token).
+ * It runs on CUDA cores in fp32 for every gate mode and dtype (q, k, v and
+ * grad_O in `dtype`; all gradients fp32), dk <= 256. (The backward is the
+ * next step after the forward pass; no page gives numbers for it.)
+ *
+ * Ownership and asynchrony are as for gla_fwd_ex: every pointer is a device
+ * pointer owned by the caller, work is enqueued on `stream`, and the caller
+ * supplies a workspace of gla_bwd_workspace_size(p) bytes (256-byte aligned;
+ * it holds the chunk states, BH * ceil(T/16) * dk * dv * 4 bytes, and the
+ * per-tile partial gradients). grad_log_g and grad_S0 may be NULL (not
+ * wanted); grad_log_g must be NULL without a gate. Outputs may not overlap
+ * inputs or each other. Results are bitwise reproducible.
+ */
+typedef struct {
+    const void* q;          /* [B,H,T,dk] dtype */
+    const void* k;          /* [B,H,T,dk] dtype */
+    const void* v;          /* [B,H,T,dv] dtype */
+    const float* log_g;     /* as in gla_fwd_params */
+    const float* S0;        /* [B,H,dk,dv] or NULL */
+    const void* grad_O;     /* [B,H,T,dv] dtype */
+    const float* grad_ST;   /* [B,H,dk,dv] or NULL */
+    float* grad_q;          /* [B,H,T,dk] */
+    float* grad_k;          /* [B,H,T,dk] */
+    float* grad_v;          /* [B,H,T,dv] */
+    float* grad_log_g;      /* shaped like log_g, or NULL */
+    float* grad_S0;         /* [B,H,dk,dv] or NULL */
+    int B, H, T, dk, dv;
+    gla_dtype dtype;
+    gla_gate gate;
+    void* workspace;
+    size_t workspace_bytes;
+} gla_bwd_params;
+
+gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream);
+
+/* Bytes of workspace gla_bwd needs for *p (0 for invalid parameters). */
+size_t gla_bwd_workspace_size(const gla_bwd_params* p);
+
 /* Synchronises `stream`, then reads and clears the library's device status
  * word for the current device. GLA_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last call, GLA_ERR_CUDA if the stream reports an

@@ -1,0 +1,226 @@
+"""The backward pass (gla_bwd, CUDA cores, fp32) against the fp64 backward
+oracle (tests/test_oracle_bwd_pins.py pins it), through the C ABI.
+
+Tolerance. Every gradient is accumulated in fp32 from inputs that the oracle
+sees exactly (bf16 values widened), with factors exp(x), x <= 0, so the error
+is fp32 rounding of sums of at most T * (dk + dv) terms. dq, dk, dv and dS0 are
+held to a relative Frobenius error of 2e-5 and a max-abs error of
+2e-4 * max|ref| per tensor. The gate gradient is a sum of the terms
+q (.) dq - k (.) dk (and rowsum(dST (.) S_T)) over later tokens, and over keys
+and batch rows for the scalar gates; it can nearly cancel, so each element is
+held to 1e-5 times the same sum taken over the terms' absolute values.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import chunkwise_gated_linear_gla_gb300 as gla
+from chunkwise_gated_linear_gla_gb300 import binding as bnd
+from chunkwise_gated_linear_gla_gb300 import build as gbuild
+from chunkwise_gated_linear_gla_gb300 import inputs as gi
+
+from _util import errors, to_np
+
+REL_FRO, MAX_ABS = 2e-5, 2e-4
+GATES = [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR]
+
+
+def _inputs(w, seed, dst=True):
+    x = gi.make_inputs(w, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1000)
+    dO = torch.randn((w.B, w.H, w.T, w.dv), generator=g).to(w.dtype)
+    dST = torch.randn((w.B, w.H, w.dk, w.dv), generator=g) * 0.1 if dst else None
+    return x, dO, dST
+
+
+def _gpu(x, dO, dST):
+    c = lambda t: None if t is None else t.cuda()
+    out = gla.backward(c(x["q"]), c(x["k"]), c(x["v"]), c(x["log_g"]), c(x["S0"]), c(dO), c(dST), gate=x["gate"])
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    return [None if t is None else to_np(t) for t in out]
+
+
+def _gate_abs_sum(x, dST, ref):
+    """The gate gradient's reductions applied to the absolute values of its terms."""
+    q, k = to_np(x["q"]), to_np(x["k"])
+    terms = np.abs(q * ref[0]) + np.abs(k * ref[1])
+    if dST is not None and q.shape[2] > 0:
+        _, ST = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
+        terms[:, :, -1] += np.sum(np.abs(to_np(dST) * ST), axis=-1)
+    rev = np.flip(np.cumsum(np.flip(terms, axis=2), axis=2), axis=2)
+    if x["gate"] == gi.GATE_TOKEN_SCALAR:
+        return rev.sum(axis=-1)
+    if x["gate"] == gi.GATE_HEAD_SCALAR:
+        return rev.sum(axis=(0, 2, 3))
+    return rev
+
+
+def _check(w, seed=0, dst=True, report=None):
+    x, dO, dST = _inputs(w, seed, dst)
+    got = _gpu(x, dO, dST)
+    ref = oracle.gla_backward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], dO, dST)
+    names = ["dq", "dk", "dv", "dlog_g", "dS0"]
+    for n, a, r in zip(names, got, ref):
+        if r is None:
+            assert a is None
+            continue
+        assert np.all(np.isfinite(a)), n
+        rf, ma = errors(a, r)
+        if report is not None:
+            report.append((n, rf, ma))
+        if n == "dlog_g":
+            bound = 1e-5 * _gate_abs_sum(x, dST, ref) + 1e-30
+            assert np.all(np.abs(a - r) <= bound), (n, np.abs(a - r).max(), bound.max())
+        else:
+            assert rf <= REL_FRO and ma <= MAX_ABS, (n, rf, ma)
+    return got
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("gate", GATES)
+@pytest.mark.parametrize("T", [1, 16, 17, 100])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_bwd_gates_ragged(gate, T, dtype):
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=2, H=2, T=T, dk=64, dv=80, dtype=dtype, gate=gate, s0_std=0.3)
+    rep = []
+    _check(w, seed=T + 7 * gate, report=rep)
+    print(gate, T, dtype, [(n, f"{rf:.1e}", f"{ma:.1e}") for n, rf, ma in rep])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("gate", [gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
+def test_bwd_no_state_terms(gate):
+    """S0 = 0 and dST = 0: dS0 is then sum_t (q_t (.) b_t)^T do_t."""
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=1, H=3, T=77, dk=128, dv=128, dtype=torch.bfloat16, gate=gate)
+    _check(w, seed=5, dst=False)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dist", ["steep", "const:-60", "zero"])
+def test_bwd_extreme_gates(dist):
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=1, H=2, T=90, dk=64, dv=64, dtype=torch.float32, gate=gi.GATE_PER_KEY,
+                    gate_dist=dist, s0_std=0.2, qkv_scale="q")
+    _check(w, seed=6)
+
+
+@pytest.mark.gpu
+def test_bwd_long_wide():
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=2, H=2, T=1000, dk=128, dv=256, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY,
+                    s0_std=0.02)
+    _check(w, seed=8)
+
+
+@pytest.mark.gpu
+def test_bwd_dk256_many_tiles():
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=1, H=2, T=130, dk=256, dv=512, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY,
+                    s0_std=0.02)
+    _check(w, seed=9)
+
+
+@pytest.mark.gpu
+def test_bwd_empty_sequence():
+    gbuild.build(); oracle.build()
+    for gate in GATES:
+        w = gi.Workload("t", B=2, H=2, T=0, dk=64, dv=64, dtype=torch.bfloat16, gate=gate, s0_std=0.3)
+        x, dO, dST = _inputs(w, 10)
+        dq, dk, dv, dg, dS0 = _gpu(x, dO, dST)
+        np.testing.assert_array_equal(dS0, dST.numpy())
+        if gate == gi.GATE_HEAD_SCALAR:
+            np.testing.assert_array_equal(dg, np.zeros(2))
+
+
+@pytest.mark.gpu
+def test_bwd_bitwise_reproducible():
+    gbuild.build()
+    w = gi.Workload("t", B=2, H=2, T=200, dk=128, dv=128, dtype=torch.bfloat16, gate=gi.GATE_TOKEN_SCALAR,
+                    s0_std=0.1)
+    x, dO, dST = _inputs(w, 11)
+    a, b = _gpu(x, dO, dST), _gpu(x, dO, dST)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
+
+
+@pytest.mark.gpu
+def test_bwd_full_gla_layer_sampled_heads():
+    """The 1.3B-shaped layer (B=8 H=4 T=2048 dk=256 dv=512) in one launch; two heads held to the oracle."""
+    gbuild.build(); oracle.build()
+    w = gi.WORKLOADS["gla_1p3b"]
+    x, dO, dST = _inputs(w, 12)
+    got = _gpu(x, dO, dST)
+    for (b, h) in [(0, 0), (7, 3)]:
+        sl = lambda t: None if t is None else t[b:b + 1, h:h + 1]
+        ref = oracle.gla_backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["log_g"]), x["gate"], sl(x["S0"]),
+                                  sl(dO), sl(dST))
+        for n, a, r in zip(["dq", "dk", "dv", "dlog_g", "dS0"], got, ref):
+            a = a[b:b + 1, h:h + 1]
+            rf, ma = errors(a, r)
+            if n == "dlog_g":
+                xs = {m: sl(x[m]) for m in ("q", "k", "v", "log_g", "S0")}
+                xs["gate"] = x["gate"]
+                bound = 1e-5 * _gate_abs_sum(xs, sl(dST), ref)
+                assert np.all(np.abs(a - r) <= bound), (n, b, h, np.abs(a - r).max())
+            else:
+                assert rf <= REL_FRO and ma <= MAX_ABS, (n, b, h, rf, ma)
+
+
+# ---------------------------------------------------------------- host-side checks (no GPU)
+
+def test_bwd_struct_layout():
+    # 12 pointers, 7 ints (padded to 8 bytes), pointer, size_t
+    assert ctypes.sizeof(bnd.gla_bwd_params) == 12 * 8 + 8 * 4 + 8 + 8
+    assert bnd.gla_bwd_params.workspace.offset == 128
+
+
+def _bp(**kw):
+    p = bnd.gla_bwd_params()
+    base = dict(q=0x10000, k=0x20000, v=0x30000, log_g=0x40000, S0=None, grad_O=0x50000, grad_ST=None,
+                grad_q=0x60000, grad_k=0x70000, grad_v=0x80000, grad_log_g=0x90000, grad_S0=None,
+                B=1, H=1, T=64, dk=64, dv=64, dtype=bnd.GLA_BF16, gate=bnd.GLA_GATE_PER_KEY,
+                workspace=None, workspace_bytes=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    return p
+
+
+BAD = [
+    ("null grad_O", dict(grad_O=None), bnd.GLA_ERR_INVALID_ARG),
+    ("null grad_q", dict(grad_q=None), bnd.GLA_ERR_INVALID_ARG),
+    ("dk not /16", dict(dk=40), bnd.GLA_ERR_INVALID_ARG),
+    ("gate none with log_g", dict(gate=bnd.GLA_GATE_NONE), bnd.GLA_ERR_INVALID_ARG),
+    ("gate none with grad_log_g", dict(gate=bnd.GLA_GATE_NONE, log_g=None), bnd.GLA_ERR_INVALID_ARG),
+    ("per-key gate without log_g", dict(log_g=None), bnd.GLA_ERR_INVALID_ARG),
+    ("grad_q overlaps q", dict(grad_q=0x10000 + 64), bnd.GLA_ERR_INVALID_ARG),
+    ("grad_k overlaps grad_q", dict(grad_k=0x60000 + 4), bnd.GLA_ERR_INVALID_ARG),
+    ("misaligned grad_v", dict(grad_v=0x80002), bnd.GLA_ERR_INVALID_ARG),
+    ("misaligned workspace", dict(workspace=0x7000010, workspace_bytes=1 << 20), bnd.GLA_ERR_INVALID_ARG),
+    ("bad dtype", dict(dtype=5), bnd.GLA_ERR_INVALID_ARG),
+    ("dk 512", dict(dk=512), bnd.GLA_ERR_UNSUPPORTED),
+    ("no workspace", dict(), bnd.GLA_ERR_WORKSPACE),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", BAD, ids=[b[0] for b in BAD])
+def test_bwd_rejects_before_launch(name, kw, want):
+    gbuild.build()
+    assert bnd.gla_bwd(_bp(**kw), stream=0, check=False) == want
+
+
+def test_bwd_workspace_size():
+    gbuild.build()
+    far = {n: (i + 1) << 28 for i, n in enumerate(["q", "k", "v", "log_g", "grad_O", "grad_q", "grad_k", "grad_v",
+                                                   "grad_log_g"])}
+    p = _bp(B=2, H=3, T=100, dk=64, dv=128, **far)
+    n = bnd.gla_bwd_workspace_size(p)
+    nch, ndvt, BH = 7, 2, 6
+    assert n >= 4 * (BH * nch * 64 * 128 + 2 * ndvt * BH * 100 * 64 + BH * 100 * 64)
+    assert bnd.gla_bwd_workspace_size(_bp(dk=40)) == 0
