@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload to time (default: the 1.3B-shaped GLA layer the metric is quoted on)")
     ap.add_argument("--segments", type=int, default=0, help="force the sequence split (0: planner decides)")
+    ap.add_argument("--shape", default="", help="B,H,T,dk,dv: the workload's gate and dtype at another shape")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--direction", default="fwd", choices=["fwd", "bwd"],
                     help="bwd: time the backward pass (gla_bwd) instead and print its own line")
@@ -69,7 +70,11 @@ def peaks():
 
 def workload(args):
     from chunkwise_gated_linear_gla_gb300 import inputs as gi
-    return gi.WORKLOADS[args.workload]
+    w = gi.WORKLOADS[args.workload]
+    if args.shape:
+        B, H, T, dk, dv = (int(x) for x in args.shape.split(","))
+        w = w.with_(name=f"{w.name}@{args.shape}", B=B, H=H, T=T, dk=dk, dv=dv)
+    return w
 
 
 def algorithmic(w):
