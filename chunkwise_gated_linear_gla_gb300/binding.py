@@ -55,6 +55,7 @@ class gla_bwd_params(ctypes.Structure):
         ("dk", ctypes.c_int), ("dv", ctypes.c_int),
         ("dtype", ctypes.c_int), ("gate", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("path", ctypes.c_int),
     ]
 
 
@@ -195,7 +196,7 @@ def gla_bwd_workspace_size(p: gla_bwd_params) -> int:
 
 
 def make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dlog_g, dS0, gate=None,
-                    workspace=None) -> gla_bwd_params:
+                    workspace=None, path=GLA_PATH_AUTO) -> gla_bwd_params:
     """Fill gla_bwd_params from torch tensors (shapes read from q and v)."""
     import torch
     B, H, T, dk_ = q.shape
@@ -213,10 +214,11 @@ def make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dlog_g, dS0, gate=N
     p.gate = gate
     p.workspace = _ptr(workspace)
     p.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    p.path = path
     return p
 
 
-def backward(q, k, v, log_g, S0, dO, dST=None, gate=None, want_dS0=True, stream=None):
+def backward(q, k, v, log_g, S0, dO, dST=None, gate=None, want_dS0=True, stream=None, path=GLA_PATH_AUTO):
     """Allocate the gradients and the workspace with torch, then call gla_bwd.
 
     Returns (dq, dk, dv, dlog_g, dS0), fp32; dlog_g is None without a gate and
@@ -231,7 +233,7 @@ def backward(q, k, v, log_g, S0, dO, dST=None, gate=None, want_dS0=True, stream=
     dv = torch.empty((B, H, T, dv_), dtype=torch.float32, device=dev)
     dg = None if log_g is None else torch.empty(log_g.shape, dtype=torch.float32, device=dev)
     dS0 = torch.empty((B, H, dk_, dv_), dtype=torch.float32, device=dev) if want_dS0 else None
-    p = make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dg, dS0, gate)
+    p = make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dg, dS0, gate, path=path)
     n = gla_bwd_workspace_size(p)
     ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), n

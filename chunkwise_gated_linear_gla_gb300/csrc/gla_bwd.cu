@@ -41,11 +41,12 @@ struct BwdArgs {
     const float* log_g; const float* S0; const float* dST;
     float* gq; float* gk; float* gv; float* glog; float* gS0;
     float* Sst;    // [BH][nch][dk][dv] state after each chunk
-    float* Pq;     // [ndvt][BH][T][dk] dq partial per dv tile
-    float* Pk;     // [ndvt][BH][T][dk] dk partial per dv tile
+    float* Pq;     // [nplanes][BH][T][dk] dq partials: one per dv tile (+ the intra plane on the bf16 path)
+    float* Pk;     // [nplanes][BH][T][dk] dk partials, likewise
+    float* Ag;     // [BH][nch][CS][CS] intra-chunk scores (bf16 path)
     float* bnd;    // [ndvt][BH][dk] rowsum(dST (.) S_T) partial per dv tile
     float* dla;    // [BH][T][dk] dlog b, then dlog alpha (per key)
-    int B, H, T, dk, dv, gate, nch, ndvt;
+    int B, H, T, dk, dv, gate, nch, ndvt, nplanes;
 };
 
 template <typename T> __device__ __forceinline__ float ld_in(const T* p, size_t i);
@@ -333,6 +334,360 @@ __global__ void __launch_bounds__(NT) gla_bwd_chunks_kernel(BwdArgs a)
         }
 }
 
+// ---------------------------------------------------------------- the bf16 path: intra kernel + tensor-core sweep
+// For bf16 inputs with dk in {64, 128, 256} the reverse sweep is split in two:
+//  * gla_bwd_intra, parallel over (b,h, chunk): the pair walk (t >= s, exact in fp32 log
+//    space) over the full dv width gives the intra parts of dq and dk (written as one
+//    more partial plane) and the scores P_ts (kept for the dv product);
+//  * gla_bwd_sweep_tc, serial over chunks per (b,h, 64 dv columns): the chunk products
+//      dq_inter = dO S_[n-1]^T, dk_inter = V D_[n]^T, dv = (K (.) Gamma) D_[n] + P^T dO,
+//      D_[n-1] = Diag(gamma) D_[n] + (Q (.) Lambda)^T dO
+//    on the tensor cores (mma.sync m16n8k16, fp32 accumulate). Operands that are not bf16
+//    inputs (the state, D, Q (.) Lambda, K (.) Gamma) are split into hi + lo bf16 parts and
+//    multiplied as hi*x + lo*x (+ hi*lo for dv), so each product keeps about 16 mantissa
+//    bits: the bf16 path is as accurate as the fp32 one. D is carried in fp32 accumulator
+//    registers from chunk to chunk.
+constexpr int BP = 8;              // bf16 row padding: rows 16 bytes apart in the banks
+
+__device__ __forceinline__ void ldsm_x4(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x2(const void* p, uint32_t& r0, uint32_t& r1) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x2_t(const void* p, uint32_t& r0, uint32_t& r1) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(a));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// x = hi + lo with hi, lo bf16 (lo carries the next 8 mantissa bits)
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+    hi = __float2bfloat16_rn(x);
+    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+// ---- intra kernel: grid (BH, nch), one thread per key; the pair walk over the full dv width
+__global__ void __launch_bounds__(NT) gla_bwd_intra_kernel(BwdArgs a, float* Ag)
+{
+    extern __shared__ __align__(16) float smi[];
+    const int dk = a.dk, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    float* qr = smi;                 // [CS][dk]
+    float* kr = qr + CS * dk;        // [CS][dk]
+    float* bc = kr + CS * dk;        // [CS][dk]
+    float* VD = bc + CS * dk;        // [CS][CS] v_s . do_t over all dv columns
+    float* Aw = VD + CS * CS;        // [NT / 32][CS][CS]
+    const int bh = blockIdx.x, c = blockIdx.y, BH = gridDim.x;
+    const int t0 = c * CS, nr = min(CS, a.T - t0);
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (size_t)bh * a.T * dk;
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k) + (size_t)bh * a.T * dk;
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v) + ((size_t)bh * a.T + t0) * a.dv;
+    const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(a.dO) + ((size_t)bh * a.T + t0) * a.dv;
+    for (int i = tid; i < CS * dk; i += NT) {
+        const int r = i / dk, x = i % dk;
+        const bool ok = r < nr;
+        qr[i] = ok ? __bfloat162float(q[(size_t)(t0 + r) * dk + x]) : 0.f;
+        kr[i] = ok ? __bfloat162float(k[(size_t)(t0 + r) * dk + x]) : 0.f;
+    }
+    const int kk = tid;
+    const bool key_on = kk < dk, warp_on = (tid & ~31) < dk;
+    if (key_on) {
+        float run = 0.f;
+#pragma unroll
+        for (int r = 0; r < CS; ++r) {
+            run += r < nr ? log_alpha(a, bh, t0 + r, kk) : 0.f;
+            bc[r * dk + kk] = run;
+        }
+    }
+    // v_s . do_t for t >= s: 2 threads per pair (halves of dv), rows past nr are zero;
+    // every thread runs the same CS * CS / (NT / 2) iterations, so the shuffle is uniform
+    static_assert((CS * CS) % (NT / 2) == 0, "pairs split evenly over the threads");
+    for (int p = tid / 2; p < CS * CS; p += NT / 2) {
+        const int half = tid % 2, t = p / CS, s = p % CS;
+        float acc = 0.f;
+        if (s <= t && t < nr) {
+            const int jb = half * (a.dv / 2), je = jb + a.dv / 2;
+            for (int j = jb; j < je; ++j)
+                acc = fmaf(__bfloat162float(dO[(size_t)t * a.dv + j]), __bfloat162float(v[(size_t)s * a.dv + j]), acc);
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (half == 0) VD[p] = acc;
+    }
+    __syncthreads();
+    float dqi[CS], dki[CS];
+#pragma unroll
+    for (int r = 0; r < CS; ++r) dqi[r] = dki[r] = 0.f;
+    if (warp_on) {
+#pragma unroll
+        for (int t = 0; t < CS; ++t) {
+            const float bt = key_on ? bc[t * dk + kk] : 0.f;
+            const float qt = key_on ? qr[t * dk + kk] : 0.f;
+#pragma unroll
+            for (int s = 0; s <= t; ++s) {
+                const float e = key_on ? expf(bt - bc[s * dk + kk]) : 0.f;
+                const float ks = key_on ? kr[s * dk + kk] : 0.f;
+                const float w = VD[t * CS + s];
+                dqi[t] = fmaf(e * ks, w, dqi[t]);
+                dki[s] = fmaf(e * qt, w, dki[s]);
+                float pk = qt * ks * e;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) pk += __shfl_xor_sync(0xffffffffu, pk, o);
+                if (lane == 0) Aw[warp * CS * CS + t * CS + s] = pk;
+            }
+        }
+    }
+    if (key_on) {   // the intra plane of the dq / dk partials
+        const size_t prow = ((size_t)a.ndvt * BH + bh) * a.T + t0;
+#pragma unroll
+        for (int t = 0; t < CS; ++t)
+            if (t < nr) {
+                a.Pq[(prow + t) * dk + kk] = dqi[t];
+                a.Pk[(prow + t) * dk + kk] = dki[t];
+            }
+    }
+    __syncthreads();
+    for (int p = tid; p < CS * CS; p += NT) {
+        const int t = p / CS, s = p % CS;
+        float acc = 0.f;
+        if (s <= t)
+            for (int wp = 0; wp * 32 < dk; ++wp) acc += Aw[wp * CS * CS + p];
+        Ag[((size_t)bh * a.nch + c) * CS * CS + p] = acc;
+    }
+}
+
+size_t intra_smem(int dk) { return sizeof(float) * (3 * (size_t)CS * dk + CS * CS + (NT / 32) * CS * CS); }
+
+template <int DK>
+struct TcLay {
+    static constexpr int RS = DVT + BP;          // bf16 row of a [rows][64] tile
+    static constexpr int RK = DK + BP;           // bf16 row of a [16][DK] tile
+    static constexpr int SPH = 0;                                  // bf16 [DK][RS] state entering the chunk, hi
+    static constexpr int SPL = SPH + DK * RS * 2;                  //   and lo
+    static constexpr int DBH = SPL + DK * RS * 2;                  // bf16 [DK][RS] D, hi
+    static constexpr int DBL = DBH + DK * RS * 2;                  //   and lo
+    static constexpr int DDB = DBL + DK * RS * 2;                  // bf16 [CS][RS] dO
+    static constexpr int VVB = DDB + CS * RS * 2;                  // bf16 [CS][RS] v
+    static constexpr int QLH = VVB + CS * RS * 2;                  // bf16 [CS][RK] q (.) Lambda, hi
+    static constexpr int QLL = QLH + CS * RK * 2;                  //   and lo
+    static constexpr int KGH = QLL + CS * RK * 2;                  // bf16 [CS][RK] k (.) Gamma, hi
+    static constexpr int KGL = KGH + CS * RK * 2;                  //   and lo
+    static constexpr int BC = KGL + CS * RK * 2;                   // fp32 [CS][DK] cumulative log gate
+    static constexpr int AA = BC + CS * DK * 4;                    // fp32 [CS][CS] scores of the chunk
+    static constexpr int GAM = AA + CS * CS * 4;                   // fp32 [DK]
+    static constexpr int BYTES = GAM + DK * 4;
+    static constexpr int TPW = DK / 16;                            // D accumulator tiles per warp
+    static constexpr int NPW = DK / 64;                            // dq / dk n-tiles (8 keys) per warp
+    static_assert(BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(SPL % 16 == 0 && DBH % 16 == 0 && DDB % 16 == 0 && QLH % 16 == 0 && KGH % 16 == 0 &&
+                  KGL % 16 == 0 && BC % 16 == 0, "ldmatrix rows 16-byte aligned");
+};
+
+template <int DK>
+__global__ void __launch_bounds__(NT, 1) gla_bwd_sweep_tc_kernel(BwdArgs a, const float* Ag)
+{
+    using L = TcLay<DK>;
+    extern __shared__ __align__(16) uint8_t smb[];
+    __nv_bfloat16* Sph = reinterpret_cast<__nv_bfloat16*>(smb + L::SPH);
+    __nv_bfloat16* Spl = reinterpret_cast<__nv_bfloat16*>(smb + L::SPL);
+    __nv_bfloat16* Dbh = reinterpret_cast<__nv_bfloat16*>(smb + L::DBH);
+    __nv_bfloat16* Dbl = reinterpret_cast<__nv_bfloat16*>(smb + L::DBL);
+    __nv_bfloat16* ddb = reinterpret_cast<__nv_bfloat16*>(smb + L::DDB);
+    __nv_bfloat16* vvb = reinterpret_cast<__nv_bfloat16*>(smb + L::VVB);
+    __nv_bfloat16* qlh = reinterpret_cast<__nv_bfloat16*>(smb + L::QLH);
+    __nv_bfloat16* qll = reinterpret_cast<__nv_bfloat16*>(smb + L::QLL);
+    __nv_bfloat16* kgh = reinterpret_cast<__nv_bfloat16*>(smb + L::KGH);
+    __nv_bfloat16* kgl = reinterpret_cast<__nv_bfloat16*>(smb + L::KGL);
+    float* bc = reinterpret_cast<float*>(smb + L::BC);
+    float* A = reinterpret_cast<float*>(smb + L::AA);
+    float* gam = reinterpret_cast<float*>(smb + L::GAM);
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32, g = lane / 4, tq = lane % 4;
+    const int bh = blockIdx.x, tile = blockIdx.y, BH = gridDim.x;
+    const int j0 = tile * DVT, jn = min(DVT, a.dv - j0);
+    const size_t ST = (size_t)DK * a.dv;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (size_t)bh * a.T * DK;
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k) + (size_t)bh * a.T * DK;
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v) + (size_t)bh * a.T * a.dv;
+    const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(a.dO) + (size_t)bh * a.T * a.dv;
+
+    // D (fp32 accumulator fragments): warp tile u covers keys 16 m .. +15 and columns
+    // 8 n .. +7; element e sits at key 16 m + g + 8 (e / 2), column 8 n + 2 tq + (e % 2)
+    float Dacc[L::TPW][4];
+#pragma unroll
+    for (int u = 0; u < L::TPW; ++u) {
+        const int id = warp * L::TPW + u, m = id / 8, n = id % 8;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int key = 16 * m + g + 8 * (e / 2), j = 8 * n + 2 * tq + (e % 2);
+            const float d = (a.dST && j < jn) ? a.dST[(size_t)bh * ST + (size_t)key * a.dv + j0 + j] : 0.f;
+            Dacc[u][e] = d;
+            split_bf16(d, Dbh[key * L::RS + j], Dbl[key * L::RS + j]);
+        }
+    }
+    if (a.bnd) {
+        const float* Sfin = a.nch > 0 ? a.Sst + ((size_t)bh * a.nch + a.nch - 1) * ST : nullptr;
+        for (int x = tid; x < DK; x += NT) {
+            float s = 0.f;
+            if (a.dST && Sfin)
+                for (int j = 0; j < jn; ++j)
+                    s = fmaf(a.dST[(size_t)bh * ST + (size_t)x * a.dv + j0 + j], Sfin[(size_t)x * a.dv + j0 + j], s);
+            a.bnd[((size_t)tile * BH + bh) * DK + x] = s;
+        }
+    }
+    const int kk = tid;
+    const bool key_on = kk < DK;
+    for (int c = a.nch - 1; c >= 0; --c) {
+        const int t0 = c * CS, nr = min(CS, a.T - t0);
+        __syncthreads();   // the previous chunk is done with every buffer
+        for (int i = tid; i < CS * DVT; i += NT) {
+            const int r = i / DVT, j = i % DVT;
+            const bool ok = r < nr && j < jn;
+            const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+            vvb[r * L::RS + j] = ok ? v[(size_t)(t0 + r) * a.dv + j0 + j] : z;
+            ddb[r * L::RS + j] = ok ? dO[(size_t)(t0 + r) * a.dv + j0 + j] : z;
+        }
+        {
+            const float* src = c > 0 ? a.Sst + ((size_t)bh * a.nch + c - 1) * ST : a.S0 ? a.S0 + (size_t)bh * ST : nullptr;
+            for (int i = tid; i < DK * DVT; i += NT) {
+                const int x = i / DVT, j = i % DVT;
+                split_bf16((src && j < jn) ? src[(size_t)x * a.dv + j0 + j] : 0.f, Sph[x * L::RS + j], Spl[x * L::RS + j]);
+            }
+        }
+        for (int i = tid; i < CS * CS; i += NT) A[i] = Ag[((size_t)bh * a.nch + c) * CS * CS + i];
+        if (key_on) {   // cumulative log gate, gamma, and Q (.) Lambda, K (.) Gamma in hi + lo parts
+            float bcr[CS], run = 0.f;
+#pragma unroll
+            for (int r = 0; r < CS; ++r) {
+                run += r < nr ? log_alpha(a, bh, t0 + r, kk) : 0.f;
+                bcr[r] = run;
+                bc[r * DK + kk] = run;
+            }
+            gam[kk] = expf(run);
+#pragma unroll
+            for (int r = 0; r < CS; ++r) {
+                const bool ok = r < nr;
+                const float qv = ok ? __bfloat162float(q[(size_t)(t0 + r) * DK + kk]) * expf(bcr[r]) : 0.f;
+                const float kv = ok ? __bfloat162float(k[(size_t)(t0 + r) * DK + kk]) * expf(run - bcr[r]) : 0.f;
+                split_bf16(qv, qlh[r * L::RK + kk], qll[r * L::RK + kk]);
+                split_bf16(kv, kgh[r * L::RK + kk], kgl[r * L::RK + kk]);
+            }
+        }
+        __syncthreads();
+        // dq_inter = dO S_[n-1]^T and dk_inter = V D_[n]^T: warp w owns keys 8 NPW w .. + 8 NPW;
+        // scaled by Lambda / Gamma they are this tile's partials of dq and dk
+        {
+            const int arow = (lane % 8) + 8 * ((lane / 8) % 2), acol = 8 * (lane / 16);
+            const int brow = lane % 8, bcol = 8 * ((lane / 8) % 2);
+            float cq[L::NPW][4], ck[L::NPW][4];
+#pragma unroll
+            for (int nt = 0; nt < L::NPW; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cq[nt][e] = ck[nt][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < DVT / 16; ++ks) {
+                uint32_t ad0, ad1, ad2, ad3, av0, av1, av2, av3;
+                ldsm_x4(ddb + arow * L::RS + 16 * ks + acol, ad0, ad1, ad2, ad3);
+                ldsm_x4(vvb + arow * L::RS + 16 * ks + acol, av0, av1, av2, av3);
+#pragma unroll
+                for (int nt = 0; nt < L::NPW; ++nt) {
+                    const int key0 = 8 * (warp * L::NPW + nt);
+                    uint32_t b0, b1;
+                    ldsm_x2(Sph + (key0 + brow) * L::RS + 16 * ks + bcol, b0, b1);
+                    mma16816(cq[nt], ad0, ad1, ad2, ad3, b0, b1);
+                    ldsm_x2(Spl + (key0 + brow) * L::RS + 16 * ks + bcol, b0, b1);
+                    mma16816(cq[nt], ad0, ad1, ad2, ad3, b0, b1);
+                    ldsm_x2(Dbh + (key0 + brow) * L::RS + 16 * ks + bcol, b0, b1);
+                    mma16816(ck[nt], av0, av1, av2, av3, b0, b1);
+                    ldsm_x2(Dbl + (key0 + brow) * L::RS + 16 * ks + bcol, b0, b1);
+                    mma16816(ck[nt], av0, av1, av2, av3, b0, b1);
+                }
+            }
+            const size_t prow = ((size_t)tile * BH + bh) * a.T + t0;
+#pragma unroll
+            for (int nt = 0; nt < L::NPW; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = g + 8 * (e / 2), key = 8 * (warp * L::NPW + nt) + 2 * tq + (e % 2);
+                    if (t < nr) {
+                        const float b = bc[t * DK + key], bend = bc[(CS - 1) * DK + key];
+                        a.Pq[(prow + t) * DK + key] = expf(b) * cq[nt][e];
+                        a.Pk[(prow + t) * DK + key] = expf(bend - b) * ck[nt][e];
+                    }
+                }
+        }
+        // dv (this tile) = (K (.) Gamma) D_[n] + P^T dO: warp w owns columns 8 w .. 8 w + 7
+        {
+            const int arow = (lane % 8) + 8 * ((lane / 8) % 2), acol = 8 * (lane / 16);
+            const int brow = (lane % 8) + 8 * ((lane / 8) % 2);
+            float cv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int ks = 0; ks < DK / 16; ++ks) {
+                uint32_t ah0, ah1, ah2, ah3, al0, al1, al2, al3, bh0, bh1, bl0, bl1;
+                ldsm_x4(kgh + arow * L::RK + 16 * ks + acol, ah0, ah1, ah2, ah3);
+                ldsm_x4(kgl + arow * L::RK + 16 * ks + acol, al0, al1, al2, al3);
+                ldsm_x2_t(Dbh + (16 * ks + brow) * L::RS + 8 * warp, bh0, bh1);
+                ldsm_x2_t(Dbl + (16 * ks + brow) * L::RS + 8 * warp, bl0, bl1);
+                mma16816(cv, ah0, ah1, ah2, ah3, bh0, bh1);
+                mma16816(cv, ah0, ah1, ah2, ah3, bl0, bl1);
+                mma16816(cv, al0, al1, al2, al3, bh0, bh1);
+            }
+            const int j = 8 * warp + 2 * tq;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s = g + 8 * (e / 2), jj = j + (e % 2);
+                float acc = cv[e];
+                for (int t = s; t < CS; ++t) acc = fmaf(A[t * CS + s], __bfloat162float(ddb[t * L::RS + jj]), acc);
+                if (s < nr && jj < jn) a.gv[((size_t)bh * a.T + t0 + s) * a.dv + j0 + jj] = acc;
+            }
+        }
+        __syncthreads();   // D's bf16 parts are read above and rewritten below
+        // D <- Diag(gamma) D + (Q (.) Lambda)^T dO, then its hi + lo parts
+        {
+            const int brow = (lane % 8) + 8 * ((lane / 8) % 2);
+            const int mi = lane / 8, arow = (lane % 8) + 8 * (mi / 2), acol = 8 * (mi % 2);
+#pragma unroll
+            for (int u = 0; u < L::TPW; ++u) {
+                const int id = warp * L::TPW + u, m = id / 8, n = id % 8;
+                uint32_t a0, a1, a2, a3, b0, b1;
+                ldsm_x2_t(ddb + brow * L::RS + 8 * n, b0, b1);
+                const float g0 = gam[16 * m + g], g1 = gam[16 * m + g + 8];
+                Dacc[u][0] *= g0; Dacc[u][1] *= g0; Dacc[u][2] *= g1; Dacc[u][3] *= g1;
+                ldsm_x4_t(qlh + arow * L::RK + 16 * m + acol, a0, a1, a2, a3);
+                mma16816(Dacc[u], a0, a1, a2, a3, b0, b1);
+                ldsm_x4_t(qll + arow * L::RK + 16 * m + acol, a0, a1, a2, a3);
+                mma16816(Dacc[u], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = 16 * m + g + 8 * (e / 2), j = 8 * n + 2 * tq + (e % 2);
+                    split_bf16(Dacc[u][e], Dbh[key * L::RS + j], Dbl[key * L::RS + j]);
+                }
+            }
+        }
+    }
+    if (a.gS0)
+#pragma unroll
+        for (int u = 0; u < L::TPW; ++u) {
+            const int id = warp * L::TPW + u, m = id / 8, n = id % 8;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = 16 * m + g + 8 * (e / 2), j = 8 * n + 2 * tq + (e % 2);
+                if (j < jn) a.gS0[(size_t)bh * ST + (size_t)key * a.dv + j0 + j] = Dacc[u][e];
+            }
+        }
+}
+
 // ---------------------------------------------------------------- dq, dk and dlog b
 template <typename Tin>
 __global__ void __launch_bounds__(NT) gla_bwd_finish_kernel(BwdArgs a)
@@ -341,7 +696,7 @@ __global__ void __launch_bounds__(NT) gla_bwd_finish_kernel(BwdArgs a)
     const int BH = a.B * a.H;
     for (size_t e = (size_t)blockIdx.x * NT + threadIdx.x; e < n; e += (size_t)gridDim.x * NT) {
         float sq = 0.f, sk = 0.f;
-        for (int tl = 0; tl < a.ndvt; ++tl) {
+        for (int tl = 0; tl < a.nplanes; ++tl) {
             sq += a.Pq[tl * plane + e];
             sk += a.Pk[tl * plane + e];
         }
@@ -431,7 +786,7 @@ size_t chunks_smem(int dk) {
 
 struct BwdPlan {
     int nch = 0, ndvt = 0;
-    size_t off_S = 0, off_Pq = 0, off_Pk = 0, off_bnd = 0, off_dla = 0, bytes = 0;
+    size_t off_S = 0, off_Pq = 0, off_Pk = 0, off_Ag = 0, off_bnd = 0, off_dla = 0, bytes = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -444,12 +799,17 @@ BwdPlan bwd_plan(const gla_bwd_params* p)
     pl.ndvt = (p->dv + DVT - 1) / DVT;
     size_t off = 0;
     pl.off_S = off;   off = up256(off + BH * pl.nch * p->dk * p->dv * 4);
-    pl.off_Pq = off;  off = up256(off + (size_t)pl.ndvt * BH * p->T * p->dk * 4);
-    pl.off_Pk = off;  off = up256(off + (size_t)pl.ndvt * BH * p->T * p->dk * 4);
+    pl.off_Pq = off;  off = up256(off + (size_t)(pl.ndvt + 1) * BH * p->T * p->dk * 4);
+    pl.off_Pk = off;  off = up256(off + (size_t)(pl.ndvt + 1) * BH * p->T * p->dk * 4);
+    pl.off_Ag = off;  off = up256(off + BH * pl.nch * CS * CS * 4);
     pl.off_bnd = off; off = up256(off + (size_t)pl.ndvt * BH * p->dk * 4);
     pl.off_dla = off; off = up256(off + BH * p->T * p->dk * 4);
     pl.bytes = off;
     return pl;
+}
+
+bool tc_shape_ok(const gla_bwd_params* p) {
+    return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256);
 }
 
 bool span_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -471,7 +831,10 @@ gla_status bwd_validate(const gla_bwd_params* p)
         return GLA_ERR_INVALID_ARG;
     if (p->T > 0 && (!p->q || !p->k || !p->v || !p->grad_O || !p->grad_q || !p->grad_k || !p->grad_v))
         return GLA_ERR_INVALID_ARG;
+    if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT)
+        return GLA_ERR_INVALID_ARG;
     if (p->dk > NT) return GLA_ERR_UNSUPPORTED;
+    if (p->path == GLA_PATH_TENSOR && !tc_shape_ok(p)) return GLA_ERR_UNSUPPORTED;
     const size_t e = p->dtype == GLA_BF16 ? 2 : 4;
     const size_t BH = (size_t)p->B * p->H;
     const size_t nq = BH * p->T * p->dk, nv = BH * p->T * p->dv, ns = BH * p->dk * p->dv;
@@ -498,8 +861,28 @@ gla_status bwd_validate(const gla_bwd_params* p)
     return GLA_OK;
 }
 
+template <int DK>
+cudaError_t launch_chunks_tc(const BwdArgs& a, int BH, cudaStream_t s)
+{
+    cudaError_t e;
+    if (a.nch > 0) {
+        const int sm1 = (int)intra_smem(DK);
+        if ((e = cudaFuncSetAttribute(gla_bwd_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1)) !=
+            cudaSuccess)
+            return e;
+        gla_bwd_intra_kernel<<<dim3(BH, a.nch), NT, sm1, s>>>(a, a.Ag);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const int smem = TcLay<DK>::BYTES;
+    if ((e = cudaFuncSetAttribute(gla_bwd_sweep_tc_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+        cudaSuccess)
+        return e;
+    gla_bwd_sweep_tc_kernel<DK><<<dim3(BH, a.ndvt), NT, smem, s>>>(a, a.Ag);
+    return cudaGetLastError();
+}
+
 template <typename Tin>
-cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s)
+cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s, bool use_tc)
 {
     cudaError_t e;
     const int BH = p.B * p.H;
@@ -512,12 +895,21 @@ cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // the reverse sweep (with no chunks it only sets dS0 = dST)
-    const size_t sm2 = chunks_smem(p.dk);
-    if ((e = cudaFuncSetAttribute(gla_bwd_chunks_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)sm2)) != cudaSuccess)
-        return e;
-    gla_bwd_chunks_kernel<Tin><<<dim3(BH, a.ndvt), NT, sm2, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (use_tc) {
+        switch (p.dk) {
+        case 64: e = launch_chunks_tc<64>(a, BH, s); break;
+        case 128: e = launch_chunks_tc<128>(a, BH, s); break;
+        default: e = launch_chunks_tc<256>(a, BH, s); break;
+        }
+        if (e != cudaSuccess) return e;
+    } else {
+        const size_t sm2 = chunks_smem(p.dk);
+        if ((e = cudaFuncSetAttribute(gla_bwd_chunks_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)sm2)) != cudaSuccess)
+            return e;
+        gla_bwd_chunks_kernel<Tin><<<dim3(BH, a.ndvt), NT, sm2, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     const size_t n = (size_t)BH * p.T * p.dk;
     if (n > 0) {
         const int grid = (int)((n + NT - 1) / NT < 4096 ? (n + NT - 1) / NT : 4096);
@@ -567,11 +959,14 @@ extern "C" gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream)
     a.Sst = reinterpret_cast<float*>(w + pl.off_S);
     a.Pq = reinterpret_cast<float*>(w + pl.off_Pq);
     a.Pk = reinterpret_cast<float*>(w + pl.off_Pk);
+    a.Ag = reinterpret_cast<float*>(w + pl.off_Ag);
     a.bnd = p->grad_log_g ? reinterpret_cast<float*>(w + pl.off_bnd) : nullptr;
     a.dla = p->grad_log_g ? reinterpret_cast<float*>(w + pl.off_dla) : nullptr;
     a.B = p->B; a.H = p->H; a.T = p->T; a.dk = p->dk; a.dv = p->dv; a.gate = p->gate;
     a.nch = pl.nch; a.ndvt = pl.ndvt;
-    const cudaError_t e = p->dtype == GLA_FP32 ? launch_all<float>(a, *p, stream)
-                                               : launch_all<__nv_bfloat16>(a, *p, stream);
+    const bool use_tc = p->path != GLA_PATH_SIMT && tc_shape_ok(p);
+    a.nplanes = pl.ndvt + (use_tc ? 1 : 0);
+    const cudaError_t e = p->dtype == GLA_FP32 ? launch_all<float>(a, *p, stream, false)
+                                               : launch_all<__nv_bfloat16>(a, *p, stream, use_tc);
     return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }

@@ -190,9 +190,12 @@ gla_status gla_host_release(void);
  * every 16-row chunk, a reverse sweep carries dL/dS through the chunks, and
  * the gate gradient is the reverse cumulative sum over tokens of
  * q (.) dq - k (.) dk (plus rowsum(grad_ST (.) S_T) at the last token).
- * It runs on CUDA cores in fp32 for every gate mode and dtype (q, k, v and
- * grad_O in `dtype`; all gradients fp32), dk <= 256. (The backward is the
- * next step after the forward pass; no page gives numbers for it.)
+ * Every gate mode and dtype is supported (q, k, v and grad_O in `dtype`; all
+ * gradients fp32; dk <= 256). For bf16 inputs with dk in {64, 128, 256} the
+ * chunk products run on the tensor cores with bf16 operands and fp32
+ * accumulation (like the forward tensor path); otherwise, or with
+ * path = GLA_PATH_SIMT, everything runs in fp32 on CUDA cores. (The backward
+ * is the next step after the forward pass; no page gives numbers for it.)
  *
  * Ownership and asynchrony are as for gla_fwd_ex: every pointer is a device
  * pointer owned by the caller, work is enqueued on `stream`, and the caller
@@ -220,6 +223,8 @@ typedef struct {
     gla_gate gate;
     void* workspace;
     size_t workspace_bytes;
+    int path;               /* gla_path: AUTO takes the tensor-core products for bf16 with dk in
+                               {64,128,256}, else the fp32 CUDA-core path */
 } gla_bwd_params;
 
 gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream);
