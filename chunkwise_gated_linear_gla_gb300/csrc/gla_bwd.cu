@@ -105,16 +105,20 @@ __global__ void __launch_bounds__(NT) gla_bwd_states_kernel(BwdArgs a)
             vv[i] = (r < nr && j < jn) ? ld_in<Tin>(v, (size_t)(t0 + r) * a.dv + j0 + j) : 0.f;
         }
         for (int x = tid; x < dk; x += NT) {
-            float bcr[CS], run = 0.f;
+            float lg[CS], kv[CS], bcr[CS], run = 0.f;
+#pragma unroll
+            for (int r = 0; r < CS; ++r) {   // every load first, then the arithmetic
+                lg[r] = r < nr ? log_alpha(a, bh, t0 + r, x) : 0.f;
+                kv[r] = r < nr ? ld_in<Tin>(k, (size_t)(t0 + r) * dk + x) : 0.f;
+            }
 #pragma unroll
             for (int r = 0; r < CS; ++r) {
-                run += r < nr ? log_alpha(a, bh, t0 + r, x) : 0.f;
+                run += lg[r];
                 bcr[r] = run;
             }
             gam[x] = expf(run);
 #pragma unroll
-            for (int r = 0; r < CS; ++r)
-                kt[r * dk + x] = r < nr ? ld_in<Tin>(k, (size_t)(t0 + r) * dk + x) * expf(run - bcr[r]) : 0.f;
+            for (int r = 0; r < CS; ++r) kt[r * dk + x] = kv[r] * expf(run - bcr[r]);
         }
         __syncthreads();
         // S <- Diag(gamma) S + (K (.) Gamma)^T V, 16 columns of one row per step, and keep it
@@ -558,30 +562,58 @@ __global__ void __launch_bounds__(NT, 1) gla_bwd_sweep_tc_kernel(BwdArgs a, cons
             vvb[r * L::RS + j] = ok ? v[(size_t)(t0 + r) * a.dv + j0 + j] : z;
             ddb[r * L::RS + j] = ok ? dO[(size_t)(t0 + r) * a.dv + j0 + j] : z;
         }
-        {
-            const float* src = c > 0 ? a.Sst + ((size_t)bh * a.nch + c - 1) * ST : a.S0 ? a.S0 + (size_t)bh * ST : nullptr;
-            for (int i = tid; i < DK * DVT; i += NT) {
-                const int x = i / DVT, j = i % DVT;
-                split_bf16((src && j < jn) ? src[(size_t)x * a.dv + j0 + j] : 0.f, Sph[x * L::RS + j], Spl[x * L::RS + j]);
+        // every global load of the chunk is issued before any of them is used
+        constexpr int NV = DK * DVT / 4 / NT;   // float4 groups of the state per thread
+        float4 sv[NV];
+        if (c > 0) {   // the stored state: workspace rows, 16-byte aligned
+            const float* src = a.Sst + ((size_t)bh * a.nch + c - 1) * ST + j0;
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const int i = tid + u * NT, x = i / (DVT / 4), j = 4 * (i % (DVT / 4));
+                sv[u] = j < jn ? ld4(src + (size_t)x * a.dv + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        } else {       // S0 (caller memory, 4-byte aligned) or zero
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const int i = tid + u * NT, x = i / (DVT / 4), j = 4 * (i % (DVT / 4));
+                const float* r = a.S0 ? a.S0 + (size_t)bh * ST + (size_t)x * a.dv + j0 + j : nullptr;
+                sv[u] = (r && j < jn) ? make_float4(r[0], r[1], r[2], r[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        for (int i = tid; i < CS * CS; i += NT) A[i] = Ag[((size_t)bh * a.nch + c) * CS * CS + i];
+        float lg[CS], qv[CS], kv[CS];
+        if (key_on) {
+#pragma unroll
+            for (int r = 0; r < CS; ++r) {
+                const bool ok = r < nr;
+                lg[r] = ok ? log_alpha(a, bh, t0 + r, kk) : 0.f;
+                qv[r] = ok ? __bfloat162float(q[(size_t)(t0 + r) * DK + kk]) : 0.f;
+                kv[r] = ok ? __bfloat162float(k[(size_t)(t0 + r) * DK + kk]) : 0.f;
+            }
+        }
+        const float Ai = Ag[((size_t)bh * a.nch + c) * CS * CS + tid];
+        static_assert(CS * CS == NT, "one score per thread");
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int i = tid + u * NT, x = i / (DVT / 4), j = 4 * (i % (DVT / 4));
+            __nv_bfloat16* h = Sph + x * L::RS + j;
+            __nv_bfloat16* l = Spl + x * L::RS + j;
+            split_bf16(sv[u].x, h[0], l[0]); split_bf16(sv[u].y, h[1], l[1]);
+            split_bf16(sv[u].z, h[2], l[2]); split_bf16(sv[u].w, h[3], l[3]);
+        }
+        A[tid] = Ai;
         if (key_on) {   // cumulative log gate, gamma, and Q (.) Lambda, K (.) Gamma in hi + lo parts
             float bcr[CS], run = 0.f;
 #pragma unroll
             for (int r = 0; r < CS; ++r) {
-                run += r < nr ? log_alpha(a, bh, t0 + r, kk) : 0.f;
+                run += lg[r];
                 bcr[r] = run;
                 bc[r * DK + kk] = run;
             }
             gam[kk] = expf(run);
 #pragma unroll
             for (int r = 0; r < CS; ++r) {
-                const bool ok = r < nr;
-                const float qv = ok ? __bfloat162float(q[(size_t)(t0 + r) * DK + kk]) * expf(bcr[r]) : 0.f;
-                const float kv = ok ? __bfloat162float(k[(size_t)(t0 + r) * DK + kk]) * expf(run - bcr[r]) : 0.f;
-                split_bf16(qv, qlh[r * L::RK + kk], qll[r * L::RK + kk]);
-                split_bf16(kv, kgh[r * L::RK + kk], kgl[r * L::RK + kk]);
+                split_bf16(qv[r] * expf(bcr[r]), qlh[r * L::RK + kk], qll[r * L::RK + kk]);
+                split_bf16(kv[r] * expf(run - bcr[r]), kgh[r * L::RK + kk], kgl[r * L::RK + kk]);
             }
         }
         __syncthreads();
