@@ -55,6 +55,19 @@ template <> __device__ __forceinline__ float ld_in<__nv_bfloat16>(const __nv_bfl
     return __bfloat162float(p[i]);
 }
 
+// L2 prefetch hints for the n bytes at p, one per 128-byte step, spread over nth threads;
+// only addresses inside the range are named, so no alignment is required.
+__device__ __forceinline__ void pf_range(const void* p, size_t n, int tid, int nth) {
+    const char* c = static_cast<const char*>(p);
+    for (size_t off = (size_t)tid * 128; off < n; off += (size_t)nth * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
+}
+
+// The inputs of chunk c (rows t0 .. t0 + CS, clipped to T) of head bh into L2: q and k rows,
+// the gate rows, and this tile's v and dO columns.
+__device__ __forceinline__ void pf_chunk_inputs(const struct BwdArgs& a, int bh, int c, int j0, int jn, size_t esz,
+                                                bool with_q, bool with_do, int tid);
+
 // log alpha_t for key kk of head bh (0 without a gate)
 __device__ __forceinline__ float log_alpha(const BwdArgs& a, int bh, int t, int kk) {
     switch (a.gate) {
@@ -80,6 +93,22 @@ __device__ __forceinline__ float dot4(float4 u, float4 w, float acc) {
     return fmaf(u.x, w.x, fmaf(u.y, w.y, fmaf(u.z, w.z, fmaf(u.w, w.w, acc))));
 }
 
+__device__ __forceinline__ void pf_chunk_inputs(const BwdArgs& a, int bh, int c, int j0, int jn, size_t esz,
+                                                bool with_q, bool with_do, int tid) {
+    const int t0 = c * CS, nr = min(CS, a.T - t0);
+    if (nr <= 0) return;
+    const size_t row = (size_t)bh * a.T + t0;
+    if (with_q) pf_range(static_cast<const char*>(a.q) + row * a.dk * esz, (size_t)nr * a.dk * esz, tid, NT);
+    pf_range(static_cast<const char*>(a.k) + row * a.dk * esz, (size_t)nr * a.dk * esz, tid, NT);
+    if (a.gate == GLA_GATE_PER_KEY) pf_range(a.log_g + row * a.dk, (size_t)nr * a.dk * 4, tid, NT);
+    if (a.gate == GLA_GATE_TOKEN_SCALAR) pf_range(a.log_g + row, (size_t)nr * 4, tid, NT);
+    if (tid < nr) {   // one row of this tile's v (and dO) columns per thread
+        const size_t off = (row + tid) * a.dv + j0;
+        pf_range(static_cast<const char*>(a.v) + off * esz, (size_t)jn * esz, 0, 1);
+        if (with_do) pf_range(static_cast<const char*>(a.dO) + off * esz, (size_t)jn * esz, 0, 1);
+    }
+}
+
 // ---------------------------------------------------------------- forward sweep: chunk states
 template <typename Tin>
 __global__ void __launch_bounds__(NT) gla_bwd_states_kernel(BwdArgs a)
@@ -100,6 +129,7 @@ __global__ void __launch_bounds__(NT) gla_bwd_states_kernel(BwdArgs a)
     for (int c = 0; c < a.nch; ++c) {
         const int t0 = c * CS, nr = min(CS, a.T - t0);
         __syncthreads();
+        if (c + 1 < a.nch) pf_chunk_inputs(a, bh, c + 1, j0, jn, sizeof(Tin), false, false, tid);
         for (int i = tid; i < CS * DVT; i += NT) {
             const int r = i / DVT, j = i % DVT;
             vv[i] = (r < nr && j < jn) ? ld_in<Tin>(v, (size_t)(t0 + r) * a.dv + j0 + j) : 0.f;
@@ -555,6 +585,12 @@ __global__ void __launch_bounds__(NT, 1) gla_bwd_sweep_tc_kernel(BwdArgs a, cons
     for (int c = a.nch - 1; c >= 0; --c) {
         const int t0 = c * CS, nr = min(CS, a.T - t0);
         __syncthreads();   // the previous chunk is done with every buffer
+        if (c > 0) {   // the next chunk of the sweep into L2 while this one computes
+            pf_chunk_inputs(a, bh, c - 1, j0, jn, 2, true, true, tid);
+            if (c > 1 && tid < DK)
+                pf_range(a.Sst + ((size_t)bh * a.nch + c - 2) * ST + (size_t)tid * a.dv + j0, (size_t)jn * 4, 0, 1);
+            if (tid == 0) pf_range(Ag + ((size_t)bh * a.nch + c - 1) * CS * CS, CS * CS * 4, 0, 1);
+        }
         for (int i = tid; i < CS * DVT; i += NT) {
             const int r = i / DVT, j = i % DVT;
             const bool ok = r < nr && j < jn;
