@@ -19,7 +19,11 @@ Attention-2 pages use:
 * the data-dependent scalar gate, one gamma_t per token and head shared by
   every key (the Mamba-2, mLSTM and Gated Retention rows of Table 1 in the
   GLA paper, §4.1), drawn like Gated Retention's sigmoid(x)^(1/tau) with
-  tau = 16: log gamma_t = logsigmoid(N(0,1)) / 16.
+  tau = 16: log gamma_t = logsigmoid(N(0,1)) / 16;
+* the bilinear gate G_t = alpha_t^T beta_t (Table 1's DFW row, alpha and beta
+  sigmoids of projections of x), drawn like the GLA gate on both sides:
+  log alpha = logsigmoid(N(0,1)) / 16 per key and log beta likewise per value
+  column.
 
 Draw order is fixed: q, k, v, gate pre-activation, S0 (all fp32 from one
 ``torch.Generator('cpu')``), then each tensor is cast to its dtype (bf16 by
@@ -37,9 +41,10 @@ GATE_NONE = 0
 GATE_HEAD_SCALAR = 1
 GATE_PER_KEY = 2
 GATE_TOKEN_SCALAR = 3
+GATE_BILINEAR = 4
 
 _GATE_NAMES = {"none": GATE_NONE, "scalar": GATE_HEAD_SCALAR, "per_key": GATE_PER_KEY,
-               "token_scalar": GATE_TOKEN_SCALAR}
+               "token_scalar": GATE_TOKEN_SCALAR, "bilinear": GATE_BILINEAR}
 
 
 @dataclass
@@ -53,7 +58,7 @@ class Workload:
     dk: int
     dv: int
     dtype: torch.dtype          # dtype of q, k, v and O
-    gate: int                   # GATE_NONE / GATE_HEAD_SCALAR / GATE_PER_KEY / GATE_TOKEN_SCALAR
+    gate: int                   # GATE_NONE / HEAD_SCALAR / PER_KEY / TOKEN_SCALAR / BILINEAR
     qkv_scale: str = "all"      # "all": q,k,v * dk^-0.5 ; "q": only q
     k_l2norm: bool = False      # k normalised to unit L2 norm per row
     s0_std: float = 0.0         # 0 => S0 absent (zero state)
@@ -90,6 +95,10 @@ WORKLOADS = {
         "token_gate", B=8, H=4, T=2048, dk=256, dv=512, dtype=torch.bfloat16,
         gate=GATE_TOKEN_SCALAR, s0_std=0.02,
         notes="data-dependent scalar gate per token and head (Mamba-2 / mLSTM form), 1.3B layer shape"),
+    "bilinear": Workload(
+        "bilinear", B=8, H=4, T=2048, dk=256, dv=512, dtype=torch.bfloat16,
+        gate=GATE_BILINEAR, s0_std=0.02,
+        notes="bilinear gate alpha_t^T beta_t (DFW form), 1.3B layer shape"),
     "gla_long": Workload(
         "gla_long", B=1, H=4, T=65536, dk=256, dv=512, dtype=torch.bfloat16,
         gate=GATE_PER_KEY, notes="long sequence, low B*H"),
@@ -108,7 +117,8 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     Returns a dict with q, k, v (``w.dtype``), log_g (fp32 or None), S0 (fp32 or
     None) and the shape fields. Layouts: q, k, log_g are [B,H,T,dk]; v is
     [B,H,T,dv]; S0 is [B,H,dk,dv]; for the per-head scalar gate log_g is [H],
-    for the per-token scalar gate [B,H,T].
+    for the per-token scalar gate [B,H,T]. The bilinear gate adds log_b
+    [B,H,T,dv] (drawn after log_g); log_b is None in every other mode.
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
@@ -124,21 +134,24 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     if w.k_l2norm:
         k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
 
-    log_g = None
-    if w.gate in (GATE_PER_KEY, GATE_TOKEN_SCALAR):
-        shape = (B, H, T, dk) if w.gate == GATE_PER_KEY else (B, H, T)
+    def draw_gate(shape):
         if w.gate_dist == "logsigmoid16":
             pre = torch.randn(shape, generator=g, dtype=torch.float32)
-            log_g = torch.nn.functional.logsigmoid(pre) / 16.0
-        elif w.gate_dist == "steep":
+            return torch.nn.functional.logsigmoid(pre) / 16.0
+        if w.gate_dist == "steep":
             u = torch.rand(shape, generator=g, dtype=torch.float32)
-            log_g = -4.0 * u
-        elif w.gate_dist.startswith("const:"):
-            log_g = torch.full(shape, float(w.gate_dist[6:]), dtype=torch.float32)
-        elif w.gate_dist == "zero":
-            log_g = torch.zeros(shape, dtype=torch.float32)
-        else:
-            raise ValueError(f"unknown gate distribution {w.gate_dist!r}")
+            return -4.0 * u
+        if w.gate_dist.startswith("const:"):
+            return torch.full(shape, float(w.gate_dist[6:]), dtype=torch.float32)
+        if w.gate_dist == "zero":
+            return torch.zeros(shape, dtype=torch.float32)
+        raise ValueError(f"unknown gate distribution {w.gate_dist!r}")
+
+    log_g = log_b = None
+    if w.gate in (GATE_PER_KEY, GATE_TOKEN_SCALAR, GATE_BILINEAR):
+        log_g = draw_gate((B, H, T, dk) if w.gate != GATE_TOKEN_SCALAR else (B, H, T))
+        if w.gate == GATE_BILINEAR:
+            log_b = draw_gate((B, H, T, dv))
     elif w.gate == GATE_HEAD_SCALAR:
         log_g = scalar_log_decay(H)
 
@@ -150,6 +163,7 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
         q=q.to(w.dtype).contiguous(), k=k.to(w.dtype).contiguous(),
         v=v.to(w.dtype).contiguous(),
         log_g=None if log_g is None else log_g.contiguous(),
+        log_b=None if log_b is None else log_b.contiguous(),
         S0=None if S0 is None else S0.contiguous(),
         gate=w.gate, B=B, H=H, T=T, dk=dk, dv=dv, chunk=w.chunk, dtype=w.dtype,
     )

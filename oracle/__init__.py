@@ -27,7 +27,7 @@ _LIB_PATH = os.path.join(_BUILD, "libgla_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-GATE_NONE, GATE_HEAD_SCALAR, GATE_PER_KEY, GATE_TOKEN_SCALAR = 0, 1, 2, 3
+GATE_NONE, GATE_HEAD_SCALAR, GATE_PER_KEY, GATE_TOKEN_SCALAR, GATE_BILINEAR = 0, 1, 2, 3, 4
 
 
 def build(force: bool = False) -> str:
@@ -48,7 +48,7 @@ def _load():
             lib = ctypes.CDLL(build())
             d = ctypes.POINTER(ctypes.c_double)
             lib.gla_oracle_fwd.restype = ctypes.c_int
-            lib.gla_oracle_fwd.argtypes = [d, d, d, d, ctypes.c_int, d, d, d,
+            lib.gla_oracle_fwd.argtypes = [d, d, d, d, d, ctypes.c_int, d, d, d,
                                            ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                            ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_int]
             lib.gla_oracle_bwd.restype = ctypes.c_int
@@ -83,11 +83,12 @@ def default_threads() -> int:
 
 
 def gla_forward(q, k, v, log_g=None, gate=None, S0=None, want_state=True,
-                nthreads=None, mutant=0):
+                nthreads=None, mutant=0, log_b=None):
     """Run the fp64 recurrence. Returns (O, ST) as fp64 numpy arrays (ST None if not wanted).
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv]; log_g: [B,H,T,dk] (per-key), [H] (per-head
     scalar), [B,H,T] (per-token scalar) or None (alpha = 1); S0: [B,H,dk,dv] or None.
+    The bilinear gate (gate = GATE_BILINEAR) also takes log_b: [B,H,T,dv].
     """
     qa, ka, va = _f64(q), _f64(k), _f64(v)
     B, H, T, dk = qa.shape
@@ -98,10 +99,11 @@ def gla_forward(q, k, v, log_g=None, gate=None, S0=None, want_state=True,
         else:
             gate = {1: GATE_HEAD_SCALAR, 3: GATE_TOKEN_SCALAR}.get(np.ndim(_f64(log_g)), GATE_PER_KEY)
     ga = _f64(log_g) if gate != GATE_NONE else None
+    ba = _f64(log_b) if gate == GATE_BILINEAR else None
     sa = _f64(S0)
     O = np.empty((B, H, T, dv), dtype=np.float64)
     ST = np.empty((B, H, dk, dv), dtype=np.float64) if want_state else None
-    rc = _load().gla_oracle_fwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), int(gate), _ptr(sa),
+    rc = _load().gla_oracle_fwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), _ptr(ba), int(gate), _ptr(sa),
                                 _ptr(O), _ptr(ST), B, H, T, dk, dv,
                                 int(nthreads or default_threads()), int(mutant))
     if rc != 0:
@@ -134,7 +136,7 @@ def gla_backward(q, k, v, log_g, gate, S0, dO, dST=None, want_dS0=True, nthreads
     return dq, dk_, dv_, dg, dS0
 
 
-def gla_forward_rows(q, k, v, log_g, gate, S0, bh_list, nthreads=None):
+def gla_forward_rows(q, k, v, log_g, gate, S0, bh_list, nthreads=None, log_b=None):
     """Oracle restricted to a subset of (b,h) pairs; returns {bh: (O[T,dv], ST[dk,dv])}.
 
     Used to check full-size launches on sampled heads: each (b,h) is an
@@ -153,7 +155,10 @@ def gla_forward_rows(q, k, v, log_g, gate, S0, bh_list, nthreads=None):
         elif gate == GATE_HEAD_SCALAR:
             g1 = ga[h:h + 1]
         s1 = None if sa is None else sa[b:b + 1, h:h + 1]
+        b1 = None if gate != GATE_BILINEAR else _f64(log_b)[b:b + 1, h:h + 1]
+        if gate == GATE_BILINEAR:
+            g1 = ga[b:b + 1, h:h + 1]
         O, ST = gla_forward(qa[b:b + 1, h:h + 1], ka[b:b + 1, h:h + 1], va[b:b + 1, h:h + 1],
-                            g1, gate, s1, True, nthreads)
+                            g1, gate, s1, True, nthreads, log_b=b1)
         out[(b, h)] = (O[0, 0], ST[0, 0])
     return out

@@ -23,6 +23,10 @@
  *   3  alpha_t = exp(log_g[b,h,t]) for all k (log_g is [B,H,T]): the
  *      data-dependent scalar gate G_t = gamma_t 1^T 1 of the Mamba-2, mLSTM
  *      and Gated Retention rows of Table 1 (GLA paper, §4.1)
+ *   4  the bilinear gate G_t = alpha_t^T beta_t of Table 1's DFW row: the state
+ *      update is S_t[i][j] = alpha_t[i] beta_t[j] S_{t-1}[i][j] + k_t[i] v_t[j]
+ *      with alpha_t = exp(log_g[b,h,t,:]) ([B,H,T,dk]) and
+ *      beta_t = exp(log_b[b,h,t,:]) ([B,H,T,dv])
  *
  * Layouts (row-major, contiguous): q [B,H,T,dk], k [B,H,T,dk], v [B,H,T,dv],
  * O [B,H,T,dv], S0 and ST [B,H,dk,dv]. S0 may be NULL (zero state); ST may be
@@ -48,7 +52,7 @@
 #include <string.h>
 
 typedef struct {
-    const double *q, *k, *v, *log_g, *S0;
+    const double *q, *k, *v, *log_g, *log_b, *S0;
     double *O, *ST;
     long B, H, T, dk, dv;
     int gate, mutant;
@@ -71,9 +75,10 @@ static void run_job(job_t* J)
     double* S = (double*)calloc((size_t)(dk * w), sizeof(double));
     double* Sprev = (J->mutant == 2 || J->mutant == 7) ? (double*)calloc((size_t)(dk * w), sizeof(double)) : NULL;
     double* alpha = (double*)malloc((size_t)dk * sizeof(double));
-    if (!S || !alpha || ((J->mutant == 2 || J->mutant == 7) && !Sprev)) {
+    double* beta = (double*)malloc((size_t)w * sizeof(double));
+    if (!S || !alpha || !beta || ((J->mutant == 2 || J->mutant == 7) && !Sprev)) {
         J->status = 1;
-        free(S); free(Sprev); free(alpha);
+        free(S); free(Sprev); free(alpha); free(beta);
         return;
     }
     const double* q = J->q + J->bh * T * dk;
@@ -95,6 +100,9 @@ static void run_job(job_t* J)
         for (long i = 0; i < dk; ++i) alpha[i] = gate_alpha(J, tg, i);
         if (J->mutant == 4 && t == 0)
             for (long i = 0; i < dk; ++i) alpha[i] = 1.0;
+        /* beta_t (one value per column j of S; 1 unless the gate is bilinear) */
+        for (long j = 0; j < w; ++j)
+            beta[j] = (J->gate == 4) ? exp(J->log_b[(J->bh * T + t) * dv + J->j0 + j]) : 1.0;
         if (Sprev) memcpy(Sprev, S, (size_t)(dk * w) * sizeof(double));
 
         const double* kt = k + t * dk;
@@ -111,6 +119,9 @@ static void run_job(job_t* J)
             } else if (J->mutant == 3) {
                 /* gate indexed by the column instead of the row */
                 for (long j = 0; j < w; ++j) Si[j] = alpha[J->j0 + j] * Si[j] + ki * vt[j];
+            } else if (J->gate == 4) {
+                /* S_t[i][j] = alpha_t[i] beta_t[j] S_{t-1}[i][j] + k_t[i] v_t[j] */
+                for (long j = 0; j < w; ++j) Si[j] = a * beta[j] * Si[j] + ki * vt[j];
             } else {
                 /* Eq. 3: S_t[i][j] = alpha_t[i] * S_{t-1}[i][j] + k_t[i] * v_t[j] */
                 for (long j = 0; j < w; ++j) Si[j] = a * Si[j] + ki * vt[j];
@@ -121,7 +132,7 @@ static void run_job(job_t* J)
             } else if (J->mutant == 7) {
                 /* q_t (Diag(alpha_t) S_{t-1}): the k_t^T v_t term left out */
                 const double* Pi = Sprev + i * w;
-                for (long j = 0; j < w; ++j) ot[j] += qi * a * Pi[j];
+                for (long j = 0; j < w; ++j) ot[j] += qi * a * beta[j] * Pi[j];
             } else {
                 /* o_t[j] = sum_i q_t[i] * S_t[i][j] */
                 for (long j = 0; j < w; ++j) ot[j] += qi * Si[j];
@@ -134,7 +145,7 @@ static void run_job(job_t* J)
         for (long i = 0; i < dk; ++i)
             for (long j = 0; j < w; ++j) st[i * dv + J->j0 + j] = S[i * w + j];
     }
-    free(S); free(Sprev); free(alpha);
+    free(S); free(Sprev); free(alpha); free(beta);
 }
 
 typedef struct {
@@ -159,13 +170,13 @@ static void* worker(void* arg)
 
 /* Returns 0 on success, 1 on bad arguments, 2 on allocation failure. */
 int gla_oracle_fwd(const double* q, const double* k, const double* v,
-                   const double* log_g, int gate, const double* S0,
+                   const double* log_g, const double* log_b, int gate, const double* S0,
                    double* O, double* ST,
                    long B, long H, long T, long dk, long dv,
                    int nthreads, int mutant)
 {
     if (!q || !k || !v || !O || B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
-    if (gate < 0 || gate > 3 || (gate != 0 && !log_g)) return 1;
+    if (gate < 0 || gate > 4 || (gate != 0 && !log_g) || (gate == 4 && !log_b)) return 1;
     if (mutant == 3 && dk != dv) return 1;
     if (T == 0) {
         if (ST) {
@@ -184,7 +195,7 @@ int gla_oracle_fwd(const double* q, const double* k, const double* v,
     for (long bh = 0; bh < B * H; ++bh)
         for (long c = 0; c < nblk; ++c) {
             job_t* J = &jobs[bh * nblk + c];
-            J->q = q; J->k = k; J->v = v; J->log_g = log_g; J->S0 = S0;
+            J->q = q; J->k = k; J->v = v; J->log_g = log_g; J->log_b = log_b; J->S0 = S0;
             J->O = O; J->ST = ST;
             J->B = B; J->H = H; J->T = T; J->dk = dk; J->dv = dv;
             J->gate = gate; J->mutant = mutant;

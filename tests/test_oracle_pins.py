@@ -12,7 +12,7 @@ Sources (page title, section):
           M_ij = lambda^(i-j) for i >= j).
   [GLA Table 1] the data-dependent scalar gate G_t = gamma_t 1^T 1 (Mamba-2,
           mLSTM, Gated Retention rows): alpha_t has the same value gamma_t
-          for every key.
+          for every key; the bilinear gate G_t = alpha_t^T beta_t (DFW row).
 All of these run on the CPU.
 """
 import math
@@ -259,6 +259,102 @@ def test_token_scalar_special_cases():
     Oh, STh = oracle.gla_forward(q, k, v, lam, oracle.GATE_HEAD_SCALAR, S0)
     np.testing.assert_array_equal(Oc, Oh)
     np.testing.assert_array_equal(STc, STh)
+
+
+# ---------------------------------------------------------------- bilinear gate
+
+def _bilinear_case(B=1, H=2, T=37, dk=6, dv=5, seed=61, dist="logsigmoid16", s0=0.5):
+    w = gi.Workload("pin", B=B, H=H, T=T, dk=dk, dv=dv, dtype=torch.float32, gate=gi.GATE_BILINEAR,
+                    s0_std=s0, gate_dist=dist)
+    x = gi.make_inputs(w, seed=seed)
+    f = lambda t: None if t is None else t.to(torch.float64).numpy()
+    return f(x["q"]), f(x["k"]), f(x["v"]), f(x["log_g"]), f(x["log_b"]), f(x["S0"])
+
+
+def test_bilinear_brute_force():
+    """[GLA Table 1, DFW] G_t = alpha_t^T beta_t: S_t = sum_i (prod alpha) x (prod beta) (.) k_i^T v_i
+    (+ the same products over all steps (.) S0), products formed one factor at a time."""
+    q, k, v, ga, gb, S0 = _bilinear_case(B=2, H=2, T=6, dk=3, dv=4, seed=61)
+    O, ST = oracle.gla_forward(q, k, v, ga, gi.GATE_BILINEAR, S0, log_b=gb)
+    al, be = np.exp(ga), np.exp(gb)
+    for b in range(2):
+        for h in range(2):
+            for t in range(6):
+                S = np.zeros((3, 4))
+                for i in range(t + 1):
+                    pa, pb = np.ones(3), np.ones(4)
+                    for j in range(i + 1, t + 1):
+                        pa = pa * al[b, h, j]
+                        pb = pb * be[b, h, j]
+                    S += np.outer(pa, pb) * np.outer(k[b, h, i], v[b, h, i])
+                pa, pb = np.ones(3), np.ones(4)
+                for j in range(t + 1):
+                    pa = pa * al[b, h, j]
+                    pb = pb * be[b, h, j]
+                S += np.outer(pa, pb) * S0[b, h]
+                np.testing.assert_allclose(O[b, h, t], q[b, h, t] @ S, rtol=1e-13, atol=1e-13)
+                if t == 5:
+                    np.testing.assert_allclose(ST[b, h], S, rtol=1e-13, atol=1e-13)
+
+
+def _bilinear_quadratic(q, k, v, ga, gb, S0):
+    """Log-space pairwise form: o_t[j] = sum_{s<=t} sum_k q_tk k_sk e^(B_tk - B_sk) v_sj e^(B'_tj - B'_sj)
+    plus sum_k q_tk e^(B_tk) S0_kj e^(B'_tj); S_T likewise, with B, B' the cumulative log gates."""
+    Bk, Bv = np.cumsum(ga, axis=2), np.cumsum(gb, axis=2)
+    B_, H, T, dk = q.shape
+    O = np.zeros(v.shape)
+    ST = np.zeros((B_, H, dk, v.shape[-1]))
+    for b in range(B_):
+        for h in range(H):
+            for t in range(T):
+                for s_ in range(t + 1):
+                    sc = np.sum(q[b, h, t] * k[b, h, s_] * np.exp(Bk[b, h, t] - Bk[b, h, s_]))
+                    O[b, h, t] += sc * v[b, h, s_] * np.exp(Bv[b, h, t] - Bv[b, h, s_])
+                O[b, h, t] += ((q[b, h, t] * np.exp(Bk[b, h, t])) @ S0[b, h]) * np.exp(Bv[b, h, t])
+            wk = np.exp(Bk[b, h, -1][None, :] - Bk[b, h])
+            wv = np.exp(Bv[b, h, -1][None, :] - Bv[b, h])
+            ST[b, h] = (k[b, h] * wk).T @ (v[b, h] * wv)
+            ST[b, h] += np.outer(np.exp(Bk[b, h, -1]), np.exp(Bv[b, h, -1])) * S0[b, h]
+    return O, ST
+
+
+@pytest.mark.parametrize("dist", ["logsigmoid16", "steep"])
+def test_bilinear_quadratic_form(dist):
+    q, k, v, ga, gb, S0 = _bilinear_case(B=1, H=2, T=50, dk=5, dv=6, seed=62, dist=dist, s0=0.3)
+    O, ST = oracle.gla_forward(q, k, v, ga, gi.GATE_BILINEAR, S0, log_b=gb)
+    Oq, STq = _bilinear_quadratic(q, k, v, ga, gb, S0)
+    np.testing.assert_allclose(O, Oq, rtol=0, atol=1e-12 * np.abs(Oq).max())
+    np.testing.assert_allclose(ST, STq, rtol=0, atol=1e-12 * np.abs(STq).max())
+
+
+def test_bilinear_reductions():
+    """beta = 1 is the per-key gate exactly; alpha = 1 is linear attention with a per-column decay,
+    o_t[j] = sum_{s<=t} (q_t . k_s) v_s[j] prod_{u=s+1..t} beta_u[j]."""
+    q, k, v, ga, gb, S0 = _bilinear_case(B=2, H=2, T=40, dk=6, dv=5, seed=63)
+    O1, S1 = oracle.gla_forward(q, k, v, ga, gi.GATE_BILINEAR, S0, log_b=np.zeros_like(gb))
+    O2, S2 = oracle.gla_forward(q, k, v, ga, gi.GATE_PER_KEY, S0)
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(S1, S2)
+    O3, _ = oracle.gla_forward(q, k, v, np.zeros_like(ga), gi.GATE_BILINEAR, None, log_b=gb)
+    be = np.exp(gb)
+    for b in range(2):
+        for h in range(2):
+            for t in range(40):
+                ref = np.zeros(5)
+                for s_ in range(t + 1):
+                    p = np.ones(5)
+                    for u in range(s_ + 1, t + 1):
+                        p = p * be[b, h, u]
+                    ref += (q[b, h, t] @ k[b, h, s_]) * v[b, h, s_] * p
+                np.testing.assert_allclose(O3[b, h, t], ref, rtol=0, atol=1e-12 * max(1.0, np.abs(ref).max()))
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7])
+def test_bilinear_pins_catch_planted_mistakes(mutant):
+    q, k, v, ga, gb, S0 = _bilinear_case(B=1, H=2, T=30, dk=5, dv=5, seed=64)
+    O, ST = oracle.gla_forward(q, k, v, ga, gi.GATE_BILINEAR, S0, mutant=mutant, log_b=gb)
+    Oq, STq = _bilinear_quadratic(q, k, v, ga, gb, S0)
+    assert max(np.abs(O - Oq).max(), np.abs(ST - STq).max()) > 1e-6, f"mutant {mutant} not caught"
 
 
 # ---------------------------------------------------------------- chunkwise form
