@@ -84,12 +84,13 @@ def algorithmic(w):
     (C+1)(dk+dv) (causal intra-chunk scores and their product with V).
     Bytes: q, k, v read and O written once (e bytes each element), the fp32
     log gate read once (dk values per token per head for the per-key gate, one for
-    the per-token scalar gate), S0 read and S_T written once (fp32).
+    the per-token scalar gate, dk + dv for the bilinear gate), S0 read and S_T
+    written once (fp32).
     """
     import torch
     e = 2 if w.dtype == torch.bfloat16 else 4
     BH, T, dk, dv, C = w.B * w.H, w.T, w.dk, w.dv, w.chunk
-    gate_bytes = 4 * dk if w.gate == 2 else 4 if w.gate == 3 else 0
+    gate_bytes = 4 * dk if w.gate == 2 else 4 if w.gate == 3 else 4 * (dk + dv) if w.gate == 4 else 0
     flops = BH * T * (4 * dk * dv + (C + 1) * (dk + dv))
     byts = BH * T * (e * (2 * dk + dv) + e * dv + gate_bytes) + BH * dk * dv * 4 * (2 if w.s0_std > 0 else 1)
     return flops, byts
@@ -244,7 +245,8 @@ def run_reference(args, w):
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=cores)
+        oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=cores,
+                           log_b=x.get("log_b"))
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -296,7 +298,7 @@ def cpu_one_core(w):
     if x["gate"] == gi.GATE_HEAD_SCALAR:
         x["log_g"] = x["log_g"][:1]
     t0 = time.perf_counter()
-    oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=1)
+    oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=1, log_b=x.get("log_b"))
     dt = time.perf_counter() - t0
     return ws.T / dt / w.H, f"1 head x T={ws.T}, {dt:.2f} s"
 
@@ -310,7 +312,8 @@ def cpu_baseline(w, rows):
     # repeat the sample until about 10 s of CPU work has been timed (at most 40 passes)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=cores)
+        oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], nthreads=cores,
+                           log_b=x.get("log_b"))
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= 10.0 or reps >= 40:
@@ -456,10 +459,11 @@ def main():
     dev = torch.device("cuda", local)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     g = None if x["log_g"] is None else x["log_g"].to(dev)
+    lb = None if x.get("log_b") is None else x["log_b"].to(dev)
     S0 = None if x["S0"] is None else x["S0"].to(dev)
     O = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev)
     ST = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
-    p = bnd.make_params(q, k, v, g, S0, O, ST, force_segments=args.segments)
+    p = bnd.make_params(q, k, v, g, S0, O, ST, force_segments=args.segments, log_b=lb)
     nbytes = bnd.gla_fwd_workspace_size(p)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), nbytes
@@ -529,11 +533,11 @@ def main():
 
     # end to end through gla_fwd_host: pinned host tensors in, host tensors out; the
     # library slices the batch so that copies in, compute and copies out overlap
-    hx = {n: (None if x[n] is None else x[n].pin_memory()) for n in ("q", "k", "v", "log_g", "S0")}
+    hx = {n: (None if x.get(n) is None else x[n].pin_memory()) for n in ("q", "k", "v", "log_g", "log_b", "S0")}
     hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
     hST = torch.empty(ST.shape, dtype=ST.dtype).pin_memory()
     hp = bnd.make_params(hx["q"], hx["k"], hx["v"], hx["log_g"], hx["S0"], hO, hST,
-                         force_segments=args.segments)
+                         force_segments=args.segments, log_b=hx["log_b"])
     h2d = sum(t.numel() * t.element_size() for t in hx.values() if t is not None)
     d2h = hO.numel() * hO.element_size() + hST.numel() * hST.element_size()
 
@@ -574,22 +578,31 @@ def main():
         if "gla_chunk_state" in names else 1
     dbytes = stage_bytes(w, dname, nseg)
     ach = dbytes / (stage_ms[dom] * 1e-3) / 1e9
+    if dname == "gla_fwd_simt":
+        # the CUDA-core pass: fp32 FFMA work against the nominal FFMA rate
+        alu = flops / (stage_ms[dom] * 1e-3) / 1e12
+        roof = {"kernel": dname, "bound": "alu", "achieved": alu, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                "frac": alu / FP32_ALU_TFLOPS, "traffic": None,
+                "peak_source": "nominal fp32 FFMA rate: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
+                "flops_per_launch": flops}
+    else:
+        roof = {"kernel": dname, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "traffic": ncu_traffic(w.name, dname), "peak_source": src,
+                "bytes_per_launch": dbytes}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
         "config": {"workload": f"{w.name}: {w.notes}, B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv} chunk=64, "
-                               f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar'][w.gate]}, "
+                               f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar', 'bilinear'][w.gate]}, "
                                f"S0={'given' if w.s0_std > 0 else 'zero'}",
                    "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "segments": nseg,
                    "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",
                    "stages": names, "stage_ms": stage_ms},
         "tflops": tflops, "tflops_frac_bf16_peak": tflops / bf16,
         "path_gbs": byts * world / (step_ms * 1e-3) / 1e9, "path_frac_hbm": byts / (step_ms * 1e-3) / 1e9 / hbm,
-        "roofline": {"kernel": dname, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                     "frac": ach / hbm, "traffic": ncu_traffic(w.name, dname), "peak_source": src,
-                     "bytes_per_launch": dbytes},
+        "roofline": roof,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "timing": {"mean_ms": step_ms, "median_ms": per_step[len(per_step) // 2], "min_ms": per_step[0],

@@ -15,7 +15,7 @@ from . import build as _build
 
 GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_CUDA, GLA_ERR_WORKSPACE, GLA_ERR_TIMEOUT = range(6)
 GLA_BF16, GLA_FP32 = 0, 1
-GLA_GATE_NONE, GLA_GATE_HEAD_SCALAR, GLA_GATE_PER_KEY, GLA_GATE_TOKEN_SCALAR = 0, 1, 2, 3
+GLA_GATE_NONE, GLA_GATE_HEAD_SCALAR, GLA_GATE_PER_KEY, GLA_GATE_TOKEN_SCALAR, GLA_GATE_BILINEAR = 0, 1, 2, 3, 4
 GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT = 0, 1, 2
 
 # Every symbol include/gla.h declares.
@@ -41,6 +41,7 @@ class gla_fwd_params(ctypes.Structure):
         ("dtype", ctypes.c_int), ("gate", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("force_segments", ctypes.c_int), ("path", ctypes.c_int),
+        ("log_b", ctypes.c_void_p),
     ]
 
 
@@ -275,11 +276,14 @@ def gla_version() -> int:
 # ---------------------------------------------------------------- marshalling helpers
 
 def make_params(q, k, v, log_g, S0, O, ST, gate=None, path=GLA_PATH_AUTO, force_segments=0,
-                workspace=None, chunk=64) -> gla_fwd_params:
-    """Fill gla_fwd_params from torch tensors (shapes read from q and v)."""
+                workspace=None, chunk=64, log_b=None) -> gla_fwd_params:
+    """Fill gla_fwd_params from torch tensors (shapes read from q and v).
+    log_b (the bilinear gate's log beta, [B,H,T,dv]) selects GLA_GATE_BILINEAR."""
     import torch
     B, H, T, dk = q.shape
     dv = v.shape[-1]
+    if gate is None and log_b is not None:
+        gate = GLA_GATE_BILINEAR
     if gate is None:
         if log_g is None:
             gate = GLA_GATE_NONE
@@ -295,11 +299,12 @@ def make_params(q, k, v, log_g, S0, O, ST, gate=None, path=GLA_PATH_AUTO, force_
     p.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     p.force_segments = force_segments
     p.path = path
+    p.log_b = _ptr(log_b)
     return p
 
 
 def forward(q, k, v, log_g=None, S0=None, gate=None, want_state=True, path=GLA_PATH_AUTO,
-            force_segments=0, stream=None, O=None, ST=None):
+            force_segments=0, stream=None, O=None, ST=None, log_b=None):
     """Allocate O (and ST) and the workspace with torch, then call gla_fwd_ex.
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv] (bf16 or fp32, on the GPU); log_g fp32
@@ -313,7 +318,7 @@ def forward(q, k, v, log_g=None, S0=None, gate=None, want_state=True, path=GLA_P
         O = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
     if ST is None and want_state:
         ST = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    p = make_params(q, k, v, log_g, S0, O, ST, gate, path, force_segments)
+    p = make_params(q, k, v, log_g, S0, O, ST, gate, path, force_segments, log_b=log_b)
     nbytes = gla_fwd_workspace_size(p)
     ws = None
     if nbytes > 0:

@@ -64,7 +64,9 @@ gla_status validate_args(const gla_fwd_params* p)
     if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->dk <= 0 || p->dv <= 0) return GLA_ERR_INVALID_ARG;
     if (p->dtype != GLA_BF16 && p->dtype != GLA_FP32) return GLA_ERR_INVALID_ARG;
     if (p->gate != GLA_GATE_NONE && p->gate != GLA_GATE_HEAD_SCALAR && p->gate != GLA_GATE_PER_KEY &&
-        p->gate != GLA_GATE_TOKEN_SCALAR)
+        p->gate != GLA_GATE_TOKEN_SCALAR && p->gate != GLA_GATE_BILINEAR)
+        return GLA_ERR_INVALID_ARG;
+    if ((p->gate == GLA_GATE_BILINEAR) != (p->log_b != nullptr) && !(p->gate == GLA_GATE_BILINEAR && p->T == 0))
         return GLA_ERR_INVALID_ARG;
     if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT)
         return GLA_ERR_INVALID_ARG;
@@ -73,7 +75,8 @@ gla_status validate_args(const gla_fwd_params* p)
     if ((long long)p->B * p->H > (1LL << 30)) return GLA_ERR_INVALID_ARG;
     if (p->gate == GLA_GATE_NONE && p->log_g) return GLA_ERR_INVALID_ARG;
     if (p->gate == GLA_GATE_HEAD_SCALAR && !p->log_g) return GLA_ERR_INVALID_ARG;
-    if ((p->gate == GLA_GATE_PER_KEY || p->gate == GLA_GATE_TOKEN_SCALAR) && !p->log_g && p->T > 0)
+    if ((p->gate == GLA_GATE_PER_KEY || p->gate == GLA_GATE_TOKEN_SCALAR || p->gate == GLA_GATE_BILINEAR) &&
+        !p->log_g && p->T > 0)
         return GLA_ERR_INVALID_ARG;
     if (p->T > 0 && (!p->q || !p->k || !p->v || !p->O)) return GLA_ERR_INVALID_ARG;
     if (p->chunk != 0 && p->chunk != kChunk) return GLA_ERR_UNSUPPORTED;
@@ -89,7 +92,7 @@ gla_status validate_pointers(const gla_fwd_params* p, bool device)
     const size_t e = p->dtype == GLA_BF16 ? 2 : 4;
     const size_t BH = (size_t)p->B * p->H;
     const size_t nq = BH * p->T * p->dk * e, nv = BH * p->T * p->dv * e;
-    const size_t ng = p->gate == GLA_GATE_PER_KEY ? BH * p->T * p->dk * 4
+    const size_t ng = (p->gate == GLA_GATE_PER_KEY || p->gate == GLA_GATE_BILINEAR) ? BH * p->T * p->dk * 4
                     : p->gate == GLA_GATE_TOKEN_SCALAR ? BH * p->T * 4
                     : p->gate == GLA_GATE_HEAD_SCALAR ? (size_t)p->H * 4 : 0;
     const size_t ns = BH * p->dk * p->dv * 4;
@@ -98,12 +101,15 @@ gla_status validate_pointers(const gla_fwd_params* p, bool device)
         for (const void* ptr : {p->q, p->k, p->v, (const void*)p->O, (const void*)p->S0, (const void*)p->ST})
             if (ptr && !aligned(ptr, 16)) return GLA_ERR_INVALID_ARG;
         if (p->log_g && !aligned(p->log_g, p->gate == GLA_GATE_PER_KEY ? 16 : 4)) return GLA_ERR_INVALID_ARG;
+        if (p->log_b && !aligned(p->log_b, 4)) return GLA_ERR_INVALID_ARG;
         if (p->workspace && !aligned(p->workspace, 256)) return GLA_ERR_INVALID_ARG;
     }
     // outputs must not overlap inputs; ST may equal S0 exactly (in-place state carry)
     Range rO = rng(p->O, nv), rST = rng(p->ST, p->ST ? ns : 0);
     Range ins[] = {rng(p->q, nq), rng(p->k, nq), rng(p->v, nv), rng(p->log_g, ng), rng(p->S0, p->S0 ? ns : 0)};
     for (Range r : ins) if (overlap(rO, r)) return GLA_ERR_INVALID_ARG;
+    const Range rb = rng(p->log_b, p->log_b ? BH * p->T * p->dv * 4 : 0);
+    if (overlap(rO, rb) || overlap(rST, rb)) return GLA_ERR_INVALID_ARG;
     if (overlap(rO, rST)) return GLA_ERR_INVALID_ARG;
     for (int i = 0; i < 4; ++i) if (overlap(rST, ins[i])) return GLA_ERR_INVALID_ARG;
     if (p->ST && p->S0 && overlap(rST, ins[4]) && (const void*)p->ST != (const void*)p->S0)
@@ -123,7 +129,7 @@ bool tensor_shape_ok(const gla_fwd_params* p)
 {
     const long long BH = (long long)p->B * p->H;
     const long long Tpad = ((long long)p->T + kChunk - 1) / kChunk * kChunk;
-    return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256) &&
+    return p->dtype == GLA_BF16 && p->gate != GLA_GATE_BILINEAR && (p->dk == 64 || p->dk == 128 || p->dk == 256) &&
            p->dv % kDvTile == 0 && BH <= 65535 && BH * Tpad < (1LL << 31);
 }
 

@@ -125,7 +125,7 @@ std::vector<Slice> plan_slices(const gla_fwd_params& p, size_t per_unit, size_t 
 }
 
 struct Sizes {   // bytes per (b, h) pair of each tensor
-    size_t q, v, g, s;
+    size_t q, v, g, b, s;
 };
 
 Sizes unit_sizes(const gla_fwd_params& p)
@@ -134,7 +134,9 @@ Sizes unit_sizes(const gla_fwd_params& p)
     Sizes z;
     z.q = (size_t)p.T * p.dk * e;
     z.v = (size_t)p.T * p.dv * e;
-    z.g = p.gate == GLA_GATE_PER_KEY ? (size_t)p.T * p.dk * 4 : p.gate == GLA_GATE_TOKEN_SCALAR ? (size_t)p.T * 4 : 0;
+    z.g = (p.gate == GLA_GATE_PER_KEY || p.gate == GLA_GATE_BILINEAR) ? (size_t)p.T * p.dk * 4
+        : p.gate == GLA_GATE_TOKEN_SCALAR ? (size_t)p.T * 4 : 0;
+    z.b = p.gate == GLA_GATE_BILINEAR ? (size_t)p.T * p.dv * 4 : 0;
     z.s = (size_t)p.dk * p.dv * 4;
     return z;
 }
@@ -162,7 +164,7 @@ extern "C" gla_status gla_fwd_host(const gla_fwd_params* hp, size_t slice_bytes,
     if (st != GLA_OK) return st;
     const gla_fwd_params& p = *hp;
     const Sizes z = unit_sizes(p);
-    const size_t per_unit = 2 * z.q + 2 * z.v + z.g + (p.S0 ? z.s : 0) + (p.ST ? z.s : 0);
+    const size_t per_unit = 2 * z.q + 2 * z.v + z.g + z.b + (p.S0 ? z.s : 0) + (p.ST ? z.s : 0);
     const std::vector<Slice> sl = plan_slices(p, per_unit, slice_bytes ? slice_bytes : kDefaultSliceBytes);
     const int nsl = (int)sl.size();
     const int nslot = std::min(kSlots, nsl);
@@ -179,7 +181,7 @@ extern "C" gla_status gla_fwd_host(const gla_fwd_params* hp, size_t slice_bytes,
         ws = std::max(ws, w);
     }
     const size_t o_q = 0, o_k = o_q + up256(umax * z.q), o_v = o_k + up256(umax * z.q);
-    const size_t o_g = o_v + up256(umax * z.v), o_s0 = o_g + up256(umax * z.g);
+    const size_t o_g = o_v + up256(umax * z.v), o_b = o_g + up256(umax * z.g), o_s0 = o_b + up256(umax * z.b);
     const size_t o_o = o_s0 + up256(p.S0 ? umax * z.s : 0), o_st = o_o + up256(umax * z.v);
     const size_t slot = o_st + up256(p.ST ? umax * z.s : 0);
     const size_t scal = p.gate == GLA_GATE_HEAD_SCALAR ? up256((size_t)p.H * 4) : 0;
@@ -196,6 +198,7 @@ extern "C" gla_status gla_fwd_host(const gla_fwd_params* hp, size_t slice_bytes,
     const uint8_t* hk = static_cast<const uint8_t*>(p.k);
     const uint8_t* hv = static_cast<const uint8_t*>(p.v);
     const uint8_t* hg = reinterpret_cast<const uint8_t*>(p.log_g);
+    const uint8_t* hb = reinterpret_cast<const uint8_t*>(p.log_b);
     const uint8_t* hs0 = reinterpret_cast<const uint8_t*>(p.S0);
     uint8_t* ho = static_cast<uint8_t*>(p.O);
     uint8_t* hst = reinterpret_cast<uint8_t*>(p.ST);
@@ -235,6 +238,7 @@ extern "C" gla_status gla_fwd_host(const gla_fwd_params* hp, size_t slice_bytes,
         ok = ok && h2d(b + o_k, hk + u0 * z.q, nu * z.q, c.s_in) == cudaSuccess;
         ok = ok && h2d(b + o_v, hv + u0 * z.v, nu * z.v, c.s_in) == cudaSuccess;
         if (z.g) ok = ok && h2d(b + o_g, hg + u0 * z.g, nu * z.g, c.s_in) == cudaSuccess;
+        if (z.b) ok = ok && h2d(b + o_b, hb + u0 * z.b, nu * z.b, c.s_in) == cudaSuccess;
         if (p.S0) ok = ok && h2d(b + o_s0, hs0 + u0 * z.s, nu * z.s, c.s_in) == cudaSuccess;
         ok = ok && cudaEventRecord(c.ev_in[s], c.s_in) == cudaSuccess;
         ok = ok && cudaStreamWaitEvent(c.s_cmp, c.ev_in[s], 0) == cudaSuccess;
@@ -248,6 +252,7 @@ extern "C" gla_status gla_fwd_host(const gla_fwd_params* hp, size_t slice_bytes,
         t.v = b + o_v;
         t.log_g = z.g ? reinterpret_cast<const float*>(b + o_g)
                 : p.gate == GLA_GATE_HEAD_SCALAR ? dscal + x.h0 : nullptr;
+        t.log_b = z.b ? reinterpret_cast<const float*>(b + o_b) : nullptr;
         t.S0 = p.S0 ? reinterpret_cast<const float*>(b + o_s0) : nullptr;
         t.O = b + o_o;
         t.ST = p.ST ? reinterpret_cast<float*>(b + o_st) : nullptr;

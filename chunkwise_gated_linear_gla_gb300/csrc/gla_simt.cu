@@ -13,6 +13,13 @@
 // §4.3). Every exponent is <= 0, so no factor exceeds 1 and no gate, however
 // steep, overflows. Each CTA owns one (b,h) and 64 columns of dv; columns of
 // S are independent because the gate scales rows only.
+//
+// The bilinear gate G_t = alpha_t^T beta_t (Table 1's DFW row) adds a decay of
+// the value columns: with B'_r the in-chunk cumulative log beta of column j,
+//   O_chunk[r][j] = exp(B'_r[j]) ((Q (.) Lambda) S)[r][j]
+//                   + sum_{s<=r} P_rs v_s[j] exp(B'_r[j] - B'_s[j]),
+//   S[k][j] <- gamma[k] gamma'[j] S[k][j] + sum_r (K (.) Gamma)[r][k] v_r[j] exp(B'_end[j] - B'_r[j]),
+// every exponent again <= 0.
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
@@ -26,7 +33,7 @@ constexpr int NT = 256;
 
 struct SimtArgs {
     const void* q; const void* k; const void* v;
-    const float* log_g; const float* S0;
+    const float* log_g; const float* log_b; const float* S0;
     void* O; float* ST;
     int B, H, T, dk, dv, gate;
 };
@@ -56,6 +63,10 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
     float* vv  = kt + CS * dk;         // [CS][DVT]
     float* A   = vv + CS * DVT;        // [CS][CS] masked intra scores
     float* gam = A + CS * CS;          // [dk] chunk decay gamma
+    float* bcv = gam + dk;             // [CS][DVT] in-chunk cumulative log beta (bilinear gate)
+    float* vg  = bcv + CS * DVT;       // [CS][DVT] v (.) Gamma' (bilinear gate)
+    float* gv  = vg + CS * DVT;        // [DVT] chunk decay gamma' of the columns (bilinear gate)
+    const bool bil = a.gate == GLA_GATE_BILINEAR;
 
     const int tid = threadIdx.x;
     const int bh = blockIdx.x;
@@ -66,7 +77,8 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
     const Tin* k = static_cast<const Tin*>(a.k) + (size_t)bh * a.T * dk;
     const Tin* v = static_cast<const Tin*>(a.v) + (size_t)bh * a.T * a.dv;
     Tin* O = static_cast<Tin*>(a.O) + (size_t)bh * a.T * a.dv;
-    const float* g = (a.gate == GLA_GATE_PER_KEY) ? a.log_g + (size_t)bh * a.T * dk : nullptr;
+    const float* g = (a.gate == GLA_GATE_PER_KEY || bil) ? a.log_g + (size_t)bh * a.T * dk : nullptr;
+    const float* lb = bil ? a.log_b + (size_t)bh * a.T * a.dv : nullptr;
     const float* gtok = (a.gate == GLA_GATE_TOKEN_SCALAR) ? a.log_g + (size_t)bh * a.T : nullptr;
     const float lam = (a.gate == GLA_GATE_HEAD_SCALAR) ? a.log_g[h] : 0.f;
 
@@ -115,6 +127,16 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
                 kt[r * dk + kk] = kr[r * dk + kk] * expf(last - b);
             }
         }
+        if (bil)   // in-chunk cumulative log beta per value column, gamma', and V (.) Gamma'
+            for (int j = tid; j < DVT; j += NT) {
+                float run = 0.f;
+                for (int r = 0; r < CS; ++r) {
+                    run += (r < nr && j < jn) ? lb[(size_t)(t0 + r) * a.dv + j0 + j] : 0.f;
+                    bcv[r * DVT + j] = run;
+                }
+                gv[j] = expf(run);
+                for (int r = 0; r < CS; ++r) vg[r * DVT + j] = vv[r * DVT + j] * expf(run - bcv[r * DVT + j]);
+            }
         __syncthreads();
         // intra-chunk scores, pairwise in log space (r >= s)
         for (int p = tid; p < CS * (CS + 1) / 2; p += NT) {
@@ -137,15 +159,23 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
             float acc = 0.f;
             const float* qrow = qt + r * dk;
             for (int kk = 0; kk < dk; ++kk) acc = fmaf(qrow[kk], S[kk * DVT + j], acc);
-            for (int s = 0; s <= r; ++s) acc = fmaf(A[r * CS + s], vv[s * DVT + j], acc);
+            if (bil) {
+                const float br = bcv[r * DVT + j];
+                acc *= expf(br);
+                for (int s = 0; s <= r; ++s)
+                    acc = fmaf(A[r * CS + s], vv[s * DVT + j] * expf(br - bcv[s * DVT + j]), acc);
+            } else {
+                for (int s = 0; s <= r; ++s) acc = fmaf(A[r * CS + s], vv[s * DVT + j], acc);
+            }
             st_out<Tin>(O, (size_t)(t0 + r) * a.dv + j0 + j, acc);
         }
         __syncthreads();
         // state: S <- (gamma^T 1) (.) S + (K (.) Gamma)^T V
+        const float* vs = bil ? vg : vv;
         for (int i = tid; i < dk * DVT; i += NT) {
             const int kk = i / DVT, j = i % DVT;
-            float acc = gam[kk] * S[i];
-            for (int r = 0; r < CS; ++r) acc = fmaf(kt[r * dk + kk], vv[r * DVT + j], acc);
+            float acc = gam[kk] * (bil ? gv[j] : 1.f) * S[i];
+            for (int r = 0; r < CS; ++r) acc = fmaf(kt[r * dk + kk], vs[r * DVT + j], acc);
             S[i] = acc;
         }
     }
@@ -159,7 +189,7 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
 }
 
 size_t simt_smem_bytes(int dk) {
-    return sizeof(float) * ((size_t)dk * DVT + 5 * CS * dk + CS * DVT + CS * CS + dk);
+    return sizeof(float) * ((size_t)dk * DVT + 5 * CS * dk + CS * DVT + CS * CS + dk + 2 * CS * DVT + DVT);
 }
 
 }  // namespace
@@ -168,7 +198,7 @@ cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s)
 {
     (void)status;
     SimtArgs a;
-    a.q = p.q; a.k = p.k; a.v = p.v; a.log_g = p.log_g; a.S0 = p.S0; a.O = p.O; a.ST = p.ST;
+    a.q = p.q; a.k = p.k; a.v = p.v; a.log_g = p.log_g; a.log_b = p.log_b; a.S0 = p.S0; a.O = p.O; a.ST = p.ST;
     a.B = p.B; a.H = p.H; a.T = p.T; a.dk = p.dk; a.dv = p.dv; a.gate = p.gate;
     const size_t smem = simt_smem_bytes(p.dk);
     dim3 grid(p.B * p.H, (p.dv + DVT - 1) / DVT);

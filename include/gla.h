@@ -23,6 +23,10 @@
  *                        G_t = gamma_t 1^T 1, the Mamba-2 / mLSTM / Gated
  *                        Retention rows of the GLA paper's Table 1 (§4.1);
  *                        log_g is float[B,H,T] = log(gamma_t).
+ *   GLA_GATE_BILINEAR    G_t = alpha_t^T beta_t (Table 1's DFW row): the
+ *                        state update is S_t = G_t (.) S_{t-1} + k_t^T v_t;
+ *                        log_g is float[B,H,T,dk] = log(alpha_t) and log_b is
+ *                        float[B,H,T,dv] = log(beta_t). CUDA-core path only.
  *
  * Layouts. Every tensor is dense, row-major, last dimension contiguous:
  *   q, k   [B,H,T,dk]   dtype (bf16 or fp32)
@@ -71,7 +75,8 @@ typedef enum {
     GLA_GATE_NONE = 0,
     GLA_GATE_HEAD_SCALAR = 1,
     GLA_GATE_PER_KEY = 2,
-    GLA_GATE_TOKEN_SCALAR = 3
+    GLA_GATE_TOKEN_SCALAR = 3,
+    GLA_GATE_BILINEAR = 4
 } gla_gate;
 
 /* Which kernels run. AUTO picks the tcgen05 tensor-core path for bf16 inputs
@@ -95,6 +100,7 @@ typedef struct {
     size_t workspace_bytes;
     int force_segments;     /* 0: the planner chooses the sequence split; n >= 1: use n segments */
     int path;               /* gla_path */
+    const float* log_b;     /* [B,H,T,dv] log(beta_t) for GLA_GATE_BILINEAR, else NULL */
 } gla_fwd_params;
 
 /*

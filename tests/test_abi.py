@@ -42,9 +42,10 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_struct_layout_matches_header():
-    # 7 pointers, 8 ints, pointer, size_t, 2 ints
-    assert ctypes.sizeof(bnd.gla_fwd_params) == 7 * 8 + 8 * 4 + 8 + 8 + 2 * 4
+    # 7 pointers, 8 ints, pointer, size_t, 2 ints, pointer
+    assert ctypes.sizeof(bnd.gla_fwd_params) == 7 * 8 + 8 * 4 + 8 + 8 + 2 * 4 + 8
     assert bnd.gla_fwd_params.workspace.offset == 88
+    assert bnd.gla_fwd_params.log_b.offset == 112
 
 
 def test_status_strings(lib):
@@ -86,6 +87,11 @@ BAD = [
     ("bad path", dict(path=5), bnd.GLA_ERR_INVALID_ARG),
     ("negative segments", dict(force_segments=-1), bnd.GLA_ERR_INVALID_ARG),
     ("misaligned workspace", dict(workspace=0x7000010, workspace_bytes=1 << 20), bnd.GLA_ERR_INVALID_ARG),
+    ("bilinear gate without log_b", dict(gate=4), bnd.GLA_ERR_INVALID_ARG),
+    ("log_b with the per-key gate", dict(log_b=0x900000), bnd.GLA_ERR_INVALID_ARG),
+    ("log_b overlaps O", dict(gate=4, log_b=0x50000 + 16), bnd.GLA_ERR_INVALID_ARG),
+    ("tensor path with the bilinear gate", dict(gate=4, log_b=0x900000, path=bnd.GLA_PATH_TENSOR),
+     bnd.GLA_ERR_UNSUPPORTED),
     ("chunk 32", dict(chunk=32), bnd.GLA_ERR_UNSUPPORTED),
     ("dk 512", dict(dk=512), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
