@@ -106,7 +106,8 @@ def stage_bytes(w, name, nseg=1):
     nch = (T + C - 1) // C
     Tp = nch * C
     gated = w.gate != 0
-    gate_in = T * dk * 4 if w.gate == 2 else T * 4 if w.gate == 3 else 0
+    gate_in = T * dk * 4 if w.gate in (2, 4) else T * 4 if w.gate == 3 else 0
+    bil = w.gate == 4
     s0 = BH * dk * dv * 4 if w.s0_std > 0 else 0
     st = BH * dk * dv * 4
     qk_tiles = (Tp if gated else T) * dk * 2 * 2
@@ -115,7 +116,11 @@ def stage_bytes(w, name, nseg=1):
         return BH * (T * dk * 2 * 2 + gate_in + (Tp * dk * 2 * 2 if gated else 0) + nch * C * C * 2 + gam)
     if name == "gla_chunk_fwd":
         last_state = (s0 + st) if nseg == 1 else BH * nseg * dk * dv * 4
-        return BH * (qk_tiles + nch * C * C * 2 + gam + T * dv * 2 * 2) + last_state
+        # bilinear gate: V (.) D' in place of v, plus log beta and the chunks' column decays
+        bil_in = T * dv * 4 + nch * dv * 4 if bil else 0
+        return BH * (qk_tiles + nch * C * C * 2 + gam + T * dv * 2 * 2 + bil_in) + last_state
+    if name == "gla_value_prep":
+        return BH * (T * dv * (2 + 4 + 2) + nch * dv * 4)
     if name == "gla_chunk_state":
         return BH * (qk_tiles // 2 + gam + T * dv * 2) + BH * nseg * dk * dv * 4
     if name == "gla_state_scan":
@@ -140,7 +145,8 @@ def planned_segments(w, force, sms):
 def kernel_source_sha(name):
     files = {"gla_chunk_fwd": ["gla_chunk_fwd.cu", "sm100.cuh"],
              "gla_chunk_prep": ["gla_prep.cu", "sm100.cuh"],
-             "gla_chunk_state": ["gla_state.cu", "sm100.cuh"]}.get(name, [])
+             "gla_chunk_state": ["gla_state.cu", "sm100.cuh"],
+             "gla_value_prep": ["gla_vprep.cu"]}.get(name, [])
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "chunkwise_gated_linear_gla_gb300", "csrc", f), "rb") as fh:

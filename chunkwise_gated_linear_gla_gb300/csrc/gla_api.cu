@@ -129,7 +129,7 @@ bool tensor_shape_ok(const gla_fwd_params* p)
 {
     const long long BH = (long long)p->B * p->H;
     const long long Tpad = ((long long)p->T + kChunk - 1) / kChunk * kChunk;
-    return p->dtype == GLA_BF16 && p->gate != GLA_GATE_BILINEAR && (p->dk == 64 || p->dk == 128 || p->dk == 256) &&
+    return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256) &&
            p->dv % kDvTile == 0 && BH <= 65535 && BH * Tpad < (1LL << 31);
 }
 
@@ -179,7 +179,9 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     pl.raw_qk = (p->gate == GLA_GATE_NONE);
     pl.sms = sms;
     const int units = p->B * p->H * pl.n_dvt;
-    pl.nseg = choose_segments(p, units, pl.nchunks, sms > 0 ? sms : 148);
+    const bool bil = p->gate == GLA_GATE_BILINEAR;
+    // the sequence split carries only a per-key decay between segments: none with the bilinear gate
+    pl.nseg = bil ? 1 : choose_segments(p, units, pl.nchunks, sms > 0 ? sms : 148);
     pl.chunks_per_seg = (pl.nchunks + pl.nseg - 1) / pl.nseg;
     pl.nseg = (pl.nchunks + pl.chunks_per_seg - 1) / pl.chunks_per_seg;
 
@@ -195,14 +197,21 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
         pl.off_segS = off;  off = align_up(off + BH * pl.nseg * p->dk * p->dv * 4, 256);
         pl.off_segin = off; off = align_up(off + BH * pl.nseg * p->dk * p->dv * 4, 256);
     }
+    if (bil) {
+        pl.off_vh = off;   off = align_up(off + BH * p->T * p->dv * 2, 256);
+        pl.off_lbc = off;  off = align_up(off + BH * pl.nchunks * p->dv * 4, 256);
+        pl.off_flag = off; off = align_up(off + BH * 4, 256);
+    }
     pl.ws_bytes = off;
     int n = 0;
     pl.stages[n++] = STAGE_PREP;
+    if (bil) pl.stages[n++] = STAGE_VALUE_PREP;
     if (pl.nseg > 1) {
         pl.stages[n++] = STAGE_SEG_STATE;
         pl.stages[n++] = STAGE_SEG_SCAN;
     }
     pl.stages[n++] = STAGE_CHUNK_FWD;
+    if (bil) pl.stages[n++] = STAGE_SIMT_FLAGGED;
     pl.nstages = n;
     return GLA_OK;
 }
@@ -216,6 +225,8 @@ const char* stage_name(StageKind k)
     case STAGE_SEG_SCAN: return "gla_state_scan";
     case STAGE_CHUNK_FWD: return "gla_chunk_fwd";
     case STAGE_COPY_STATE: return "gla_copy_state";
+    case STAGE_VALUE_PREP: return "gla_value_prep";
+    case STAGE_SIMT_FLAGGED: return "gla_fwd_simt_flagged";
     }
     return "?";
 }
@@ -250,6 +261,10 @@ gla_status run_stage(const gla_fwd_params* p, const Plan& pl, int i, cudaStream_
     case STAGE_SEG_SCAN: e = launch_seg_scan(*p, pl, p->workspace, c->status, s); break;
     case STAGE_CHUNK_FWD:
         e = launch_chunk_fwd(*p, pl, p->workspace, pl.nseg > 1 ? kModeSegOut : kModeFull, c->status, s);
+        break;
+    case STAGE_VALUE_PREP: e = launch_value_prep(*p, pl, p->workspace, s); break;
+    case STAGE_SIMT_FLAGGED:
+        e = launch_simt(*p, c->status, s, reinterpret_cast<const int*>(static_cast<uint8_t*>(p->workspace) + pl.off_flag));
         break;
     }
     return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;

@@ -23,6 +23,15 @@
 // MMA); the bf16 copy, the inter and intra MMAs and the output drain overlap
 // with it. Every wait is bounded; on a timeout the CTA records an error code
 // and winds down.
+//
+// The bilinear gate G_t = alpha_t^T beta_t (Table 1's DFW row; the chunkwise
+// form of the paper's appendix on the general formulation) is the BIL
+// instantiation. V arrives as V^ = V (.) D' (gla_value_prep), so the state
+// and intra MMAs are unchanged; the decay also scales column j by
+// gamma'[j] = exp(B'_C[j]); the inter MMA's bf16 state is S_[n-1] Diag(gamma');
+// and the drain scales O[r][j] by exp(B'_r[j] - B'_C[j]), formed from log beta
+// (a prefix sum for the first 32 rows, a suffix sum for the last 32). A head
+// that gla_value_prep flagged out of range is left to the CUDA-core pass.
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
@@ -50,9 +59,14 @@ struct FwdArgs {
     const float* gam;   // [BH][nchunks][dk], null without a gate
     int* status;
     int dv, nchunks, cps, mode, gated;
+    // bilinear gate only
+    const float* lbc;   // [BH][nchunks][dv] B'_C, the chunk's total log beta per column
+    const float* lb;    // [BH][T][dv] log beta
+    const int* skip;    // [BH] heads left to the CUDA-core pass
+    int T;
 };
 
-template <int DK>
+template <int DK, bool BIL>
 struct Lay {
     static constexpr int QB = DK * C * 2;
     static constexpr int KB = DK * C * 2;
@@ -64,7 +78,9 @@ struct Lay {
     static constexpr int V_OFF = QB + KB;
     static constexpr int A_OFF = V_OFF + VB;
     static constexpr int G_OFF = A_OFF + AB;
-    static constexpr int STAGE = (G_OFF + GB + 1023) / 1024 * 1024;
+    static constexpr int GVB = BIL ? DVT * 4 : 0;
+    static constexpr int GV_OFF = G_OFF + GB;
+    static constexpr int STAGE = (GV_OFF + GVB + 1023) / 1024 * 1024;
     static constexpr int OB = C * DVT * 2;
     static constexpr int O_OFF = NSTAGE * STAGE;
     static constexpr int BAR_OFF = O_OFF + 2 * OB;
@@ -96,14 +112,17 @@ __device__ __forceinline__ bool group_all_ok(bool ok, int id, int n) {
 
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
-template <int DK>
+template <int DK, bool BIL>
 __global__ void __launch_bounds__(NT, 1)
 gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmO)
 {
-    using L = Lay<DK>;
+    using L = Lay<DK, BIL>;
     constexpr int HC = DK / 2;   // state columns per epilogue thread
+    if constexpr (BIL) {
+        if (a.skip[blockIdx.y]) return;   // the whole CTA leaves before any setup
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
@@ -159,9 +178,11 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     break;
                 }
                 uint8_t* sb = sm + st * L::STAGE;
-                const uint32_t bytes = L::KB + L::VB + (gated ? L::GB : 0) + (want_out ? L::QB + L::AB : 0);
+                const uint32_t bytes = L::KB + L::VB + (gated ? L::GB : 0) + (want_out ? L::QB + L::AB : 0) + L::GVB;
                 mbar_arrive_expect_tx(&full[st], bytes);
                 if (gated) bulk_load(sb + L::G_OFF, a.gam + ((size_t)bh * a.nchunks + c) * DK, L::GB, &full[st]);
+                if constexpr (BIL)
+                    bulk_load(sb + L::GV_OFF, a.lbc + ((size_t)bh * a.nchunks + c) * a.dv + dv0, L::GVB, &full[st]);
 #pragma unroll
                 for (int i = 0; i < DK / 64; ++i)
                     tma_load_3d(sb + L::K_OFF + i * 8192, &tmK, &full[st], i * 64, c * C, bh);
@@ -268,9 +289,23 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             }
             tmem_wait_st();
         }
-        // drain the O accumulator of chunk m: TMEM -> registers -> bf16 smem tile -> TMA store
-        auto drain = [&](int m) -> bool {
+        // drain the O accumulator of chunk m: TMEM -> registers -> bf16 smem tile -> TMA store;
+        // lbc_m is B'_C[d] of chunk m (bilinear gate)
+        auto drain = [&](int m, float lbc_m) -> bool {
             const int b = m & 1;
+            float w[32];
+            if constexpr (BIL) {
+                // log beta of this thread's 32 rows of chunk m (rows past T add nothing), and an
+                // L2 prefetch of chunk m+2's rows, one 128-byte line per thread
+                const int row0 = (c_begin + m) * C + grp * 32;
+                const float* lp = a.lb + ((size_t)bh * a.T + row0) * a.dv + dv0 + d;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) w[t] = row0 + t < a.T ? lp[(size_t)t * a.dv] : 0.f;
+                const int prow = (c_begin + m + 2) * C + gt / 4 + grp * 32;
+                if (c_begin + m + 2 < c_end && prow < a.T)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.lb + ((size_t)bh * a.T + prow) * a.dv + dv0 +
+                                                                 (gt & 3) * 32));
+            }
             const bool ok = mbar_wait(&o_full[b], (m >> 1) & 1, kTimeoutNs);
             if (!group_all_ok(ok, BAR_EPI, NEPI)) return false;
             tc_fence_after();
@@ -279,6 +314,27 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&o_empty[b]);
+            if constexpr (BIL) {
+                // exp(B'_r - B'_C): rows 0-31 from the prefix sum, rows 32-63 from the suffix sum
+                if (grp == 0) {
+                    float acc = -lbc_m;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        acc += w[t];
+                        w[t] = expf(acc);
+                    }
+                } else {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int t = 31; t >= 0; --t) {
+                        const float x = w[t];
+                        w[t] = expf(acc);
+                        acc -= x;
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * w[t]);
+            }
             // the store issued from this half-buffer two chunks ago must have read it
             if (gt == 0) bulk_wait_read1();
             named_bar_sync(bar_grp, 128);
@@ -298,6 +354,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         };
         bool alive = true;
         uint32_t P[HC / 2];   // bf16 pairs of S_[n-1] (this thread's columns), kept until the copy is free
+        float lbc_prev = 0.f, lbc_cur = 0.f;   // B'_C[d] of chunks n-1 and n (bilinear gate)
         for (int n = 0; n < nloc && alive; ++n) {
             bool ok = true;
             if (n >= 1) ok = mbar_wait(s_done, (n - 1) & 1, kTimeoutNs);
@@ -308,6 +365,11 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             }
             tc_fence_after();
             const float* g = reinterpret_cast<const float*>(sm + (n & 1) * L::STAGE + L::G_OFF) + cb;
+            float gvd = 1.f;   // gamma'[d] (bilinear gate)
+            if constexpr (BIL) {
+                lbc_cur = reinterpret_cast<const float*>(sm + (n & 1) * L::STAGE + L::GV_OFF)[d];
+                gvd = expf(lbc_cur);
+            }
             // part 1: S <- Diag(gamma_n) S_[n-1] (and keep bf16(S_[n-1]) in registers)
 #pragma unroll
             for (int c2 = 0; c2 < HC; c2 += 64) {
@@ -315,6 +377,13 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 tmem_ld32(tS + lb + cb + c2, r0);
                 tmem_ld32(tS + lb + cb + c2 + 32, r1);
                 tmem_wait_ld();
+                if constexpr (BIL) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gvd);
+                        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * gvd);
+                    }
+                }
                 if (want_out) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -353,12 +422,13 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(sb_ready);
-            if (n >= 1 && !drain(n - 1)) {
+            if (n >= 1 && !drain(n - 1, lbc_prev)) {
                 alive = false;
                 break;
             }
+            lbc_prev = lbc_cur;
         }
-        if (alive && want_out && nloc > 0 && !drain(nloc - 1)) alive = false;
+        if (alive && want_out && nloc > 0 && !drain(nloc - 1, lbc_prev)) alive = false;
         if (!alive && gt == 0) fail(a.status, abort_flag, ERR_EPI);
         if (alive && nloc > 0) {
             const bool ok = mbar_wait(s_done, (nloc - 1) & 1, kTimeoutNs);
@@ -398,13 +468,14 @@ bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, swz);
 }
 
-template <int DK>
+template <int DK, bool BIL>
 cudaError_t launch_dk(const FwdArgs& a, dim3 grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                       const CUtensorMap& A, const CUtensorMap& o, cudaStream_t s) {
-    using L = Lay<DK>;
-    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    using L = Lay<DK, BIL>;
+    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK, BIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::SMEM);
     if (e != cudaSuccess) return e;
-    gla_chunk_fwd_kernel<DK><<<grid, NT, L::SMEM, s>>>(a, q, k, v, A, o);
+    gla_chunk_fwd_kernel<DK, BIL><<<grid, NT, L::SMEM, s>>>(a, q, k, v, A, o);
     return cudaGetLastError();
 }
 
@@ -420,7 +491,9 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     CUtensorMap mq, mk, mv, ma, mo;
     if (!map3(&mq, qb, p.dk, qrows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     if (!map3(&mk, kb, p.dk, qrows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    if (!map3(&mv, p.v, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    const bool bil = p.gate == GLA_GATE_BILINEAR;
+    const void* vb = bil ? base + pl.off_vh : p.v;   // bilinear gate: V (.) D' from gla_value_prep
+    if (!map3(&mv, vb, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     if (!map3(&mo, p.O, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_NONE, 32)) return cudaErrorInvalidValue;
     {
         uint64_t dims[2] = {64, BH * (uint64_t)pl.nchunks * 64};
@@ -448,11 +521,24 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     a.cps = (mode == kModeFull) ? pl.nchunks : pl.chunks_per_seg;
     a.mode = mode;
     a.gated = p.gate != GLA_GATE_NONE;
+    a.lbc = bil ? reinterpret_cast<const float*>(base + pl.off_lbc) : nullptr;
+    a.lb = p.log_b;
+    a.skip = bil ? reinterpret_cast<const int*>(base + pl.off_flag) : nullptr;
+    a.T = p.T;
     dim3 grid(pl.n_dvt, (unsigned)BH, mode == kModeFull ? 1 : pl.nseg);
+    if (bil) {
+        if (mode != kModeFull) return cudaErrorInvalidValue;   // no sequence split with the bilinear gate
+        switch (p.dk) {
+        case 64: return launch_dk<64, true>(a, grid, mq, mk, mv, ma, mo, s);
+        case 128: return launch_dk<128, true>(a, grid, mq, mk, mv, ma, mo, s);
+        case 256: return launch_dk<256, true>(a, grid, mq, mk, mv, ma, mo, s);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (p.dk) {
-    case 64: return launch_dk<64>(a, grid, mq, mk, mv, ma, mo, s);
-    case 128: return launch_dk<128>(a, grid, mq, mk, mv, ma, mo, s);
-    case 256: return launch_dk<256>(a, grid, mq, mk, mv, ma, mo, s);
+    case 64: return launch_dk<64, false>(a, grid, mq, mk, mv, ma, mo, s);
+    case 128: return launch_dk<128, false>(a, grid, mq, mk, mv, ma, mo, s);
+    case 256: return launch_dk<256, false>(a, grid, mq, mk, mv, ma, mo, s);
     }
     return cudaErrorInvalidValue;
 }

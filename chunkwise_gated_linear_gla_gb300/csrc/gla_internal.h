@@ -15,6 +15,9 @@ constexpr int kSimtChunk = 16;    // chunk length of the CUDA-core path
 constexpr int kDvTile = 128;      // dv columns per CTA on the tensor-core path
 constexpr int kSimtDvTile = 64;   // dv columns per CTA on the CUDA-core path
 constexpr int kMaxDk = 256;
+// Bilinear gate on the tensor-core path: the largest |in-chunk partial sum of
+// log beta| for which one reference per chunk stays exact to rounding.
+constexpr float kVGuard = 60.f;
 
 enum StageKind {
     STAGE_SIMT = 0,        // whole pass on CUDA cores
@@ -23,6 +26,8 @@ enum StageKind {
     STAGE_SEG_SCAN = 3,    // serial recurrence over segments
     STAGE_CHUNK_FWD = 4,   // chunk-serial tensor-core pass: state, inter + intra output
     STAGE_COPY_STATE = 5,  // T == 0: ST <- S0 (or 0)
+    STAGE_VALUE_PREP = 6,  // bilinear gate: V (.) D', the chunks' column decays, range flags
+    STAGE_SIMT_FLAGGED = 7,  // bilinear gate: the CUDA-core pass for the heads flagged out of range
 };
 
 struct Plan {
@@ -36,9 +41,10 @@ struct Plan {
     int sms = 0;           // multiprocessors of the device the plan was made for
     // workspace layout (byte offsets from the workspace base)
     size_t off_qt = 0, off_kt = 0, off_A = 0, off_gam = 0, off_segS = 0, off_segin = 0;
+    size_t off_vh = 0, off_lbc = 0, off_flag = 0;   // bilinear gate only
     size_t ws_bytes = 0;
     int nstages = 0;
-    StageKind stages[4];
+    StageKind stages[6];
 };
 
 // Argument checks of the C ABI (gla_api.cu). validate_args: sizes, modes and
@@ -54,7 +60,9 @@ gla_status plan_workspace(const gla_fwd_params* p, size_t* bytes);
 int* device_status_ptr();   // nullptr on failure
 
 // Launchers. Each returns cudaSuccess or the launch error.
-cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s);
+// launch_simt: with `only` non-null, just the heads bh with only[bh] != 0.
+cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s, const int* only = nullptr);
+cudaError_t launch_value_prep(const gla_fwd_params& p, const Plan& pl, void* ws, cudaStream_t s);
 cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode,
                              int* status, cudaStream_t s);

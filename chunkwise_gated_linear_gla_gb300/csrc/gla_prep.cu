@@ -811,7 +811,7 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
         if (!make_tmap(&mA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.A, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
-    if (p.gate != GLA_GATE_PER_KEY) {
+    if (p.gate != GLA_GATE_PER_KEY && p.gate != GLA_GATE_BILINEAR) {   // the bilinear gate's key side is per key
         switch (p.dk) {
         case 64: return launch_prep_uniform_dk<64>(a, mq, mk, mA, sms, s);
         case 128: return launch_prep_uniform_dk<128>(a, mq, mk, mA, sms, s);

@@ -35,6 +35,7 @@ struct SimtArgs {
     const void* q; const void* k; const void* v;
     const float* log_g; const float* log_b; const float* S0;
     void* O; float* ST;
+    const int* only;   // null, or per-head flags: compute only the heads whose flag is set
     int B, H, T, dk, dv, gate;
 };
 
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
 
     const int tid = threadIdx.x;
     const int bh = blockIdx.x;
+    if (a.only && a.only[bh] == 0) return;
     const int h = bh % a.H;
     const int j0 = blockIdx.y * DVT;
     const int jn = min(DVT, a.dv - j0);
@@ -194,10 +196,11 @@ size_t simt_smem_bytes(int dk) {
 
 }  // namespace
 
-cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s)
+cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s, const int* only)
 {
     (void)status;
     SimtArgs a;
+    a.only = only;
     a.q = p.q; a.k = p.k; a.v = p.v; a.log_g = p.log_g; a.log_b = p.log_b; a.S0 = p.S0; a.O = p.O; a.ST = p.ST;
     a.B = p.B; a.H = p.H; a.T = p.T; a.dk = p.dk; a.dv = p.dv; a.gate = p.gate;
     const size_t smem = simt_smem_bytes(p.dk);

@@ -90,8 +90,8 @@ BAD = [
     ("bilinear gate without log_b", dict(gate=4), bnd.GLA_ERR_INVALID_ARG),
     ("log_b with the per-key gate", dict(log_b=0x900000), bnd.GLA_ERR_INVALID_ARG),
     ("log_b overlaps O", dict(gate=4, log_b=0x50000 + 16), bnd.GLA_ERR_INVALID_ARG),
-    ("tensor path with the bilinear gate", dict(gate=4, log_b=0x900000, path=bnd.GLA_PATH_TENSOR),
-     bnd.GLA_ERR_UNSUPPORTED),
+    ("tensor path with the bilinear gate in fp32",
+     dict(gate=4, log_b=0x900000, dtype=bnd.GLA_FP32, dv=128, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("chunk 32", dict(chunk=32), bnd.GLA_ERR_UNSUPPORTED),
     ("dk 512", dict(dk=512), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
@@ -167,3 +167,22 @@ def test_bench_segment_rule_matches_library_plan():
         seg = 2 * BH * nseg * w.dk * w.dv * 4 if nseg > 1 else 0
         got = bnd.gla_fwd_workspace_size(p)
         assert abs(got - (base + seg)) < 4096, (name, got, base + seg, nseg)
+
+
+def test_plan_bilinear_on_host():
+    """The bilinear gate on the tensor path: key prep, value prep, chunk pass, then the CUDA-core
+    pass for flagged heads; never a sequence split; the workspace adds V (.) D' (bf16), the
+    chunks' column decays and one flag per head."""
+    kw = dict(B=1, H=2, T=65536, dk=256, dv=512, q=0x1000000, k=0x11000000, v=0x21000000,
+              log_g=0x31000000, O=0x41000000, gate=4, log_b=0x61000000)
+    p = _params(**kw)
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_prep", "gla_value_prep", "gla_chunk_fwd", "gla_fwd_simt_flagged"]
+    # the per-key gate on the same shapes splits the sequence (2 heads x 4 dv tiles)
+    pk = _params(**dict(kw, gate=bnd.GLA_GATE_PER_KEY, log_b=None))
+    names_pk = [bnd.gla_fwd_stage_name(pk, i) for i in range(bnd.gla_fwd_num_stages(pk))]
+    assert "gla_chunk_state" in names_pk
+    BH, T, dk, dv, nch = 2, 65536, 256, 512, 1024
+    base = 2 * BH * T * dk * 2 + BH * nch * 64 * 64 * 2 + BH * nch * dk * 4
+    extra = BH * T * dv * 2 + BH * nch * dv * 4 + 256
+    assert bnd.gla_fwd_workspace_size(p) == base + extra
