@@ -80,7 +80,7 @@ gla_status validate_args(const gla_fwd_params* p)
         return GLA_ERR_INVALID_ARG;
     if (p->T > 0 && (!p->q || !p->k || !p->v || !p->O)) return GLA_ERR_INVALID_ARG;
     if (p->chunk != 0 && p->chunk != kChunk) return GLA_ERR_UNSUPPORTED;
-    if (p->dk > kMaxDk) return GLA_ERR_UNSUPPORTED;
+    if (p->dk > kSimtMaxDk) return GLA_ERR_UNSUPPORTED;
     return GLA_OK;
 }
 

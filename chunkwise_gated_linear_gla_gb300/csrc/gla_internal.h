@@ -14,7 +14,13 @@ constexpr int kChunk = 64;        // primary chunk length C of the tensor-core p
 constexpr int kSimtChunk = 16;    // chunk length of the CUDA-core path
 constexpr int kDvTile = 128;      // dv columns per CTA on the tensor-core path
 constexpr int kSimtDvTile = 64;   // dv columns per CTA on the CUDA-core path
-constexpr int kMaxDk = 256;
+constexpr int kMaxDk = 256;       // widest keys of the tensor-core path and of the 16-row CUDA-core form
+// CUDA-core forward for dk > kMaxDk: 8-row chunks and 32 columns per CTA keep
+// the fp32 state tile (dk x 32) and five [8 x dk] row buffers within the
+// 227 KB of shared memory a CTA may hold, up to dk = kSimtMaxDk.
+constexpr int kSimtChunkWide = 8;
+constexpr int kSimtDvTileWide = 32;
+constexpr int kSimtMaxDk = 768;
 // Bilinear gate on the tensor-core path: the largest |in-chunk partial sum of
 // log beta| for which one reference per chunk stays exact to rounding.
 constexpr float kVGuard = 60.f;

@@ -3,7 +3,8 @@
 // This is the path for fp32 inputs (where the result must hold to ~1e-5) and
 // for bf16 shapes the tensor-core path does not take. It follows the
 // chunkwise form of "Gated Linear Attention Transformers with
-// Hardware-Efficient Training", §4.2, with chunks of 16 rows:
+// Hardware-Efficient Training", §4.2, with chunks of 16 rows (8 for keys
+// wider than 256, whose state tiles take more shared memory):
 //   Lambda_r = b_r / b_start, Gamma_r = b_end / b_r, gamma = b_end / b_start,
 //   O_chunk = (Q (.) Lambda) S + (P (.) M) V,
 //   S      <- (gamma^T 1) (.) S + (K (.) Gamma)^T V,
@@ -11,8 +12,9 @@
 //   P_rs = sum_k Q_rk K_sk exp(logB_rk - logB_sk),  r >= s
 // (same paper, §4.1 Eq. 4, the "intra-sub-chunk in full precision" part of
 // §4.3). Every exponent is <= 0, so no factor exceeds 1 and no gate, however
-// steep, overflows. Each CTA owns one (b,h) and 64 columns of dv; columns of
-// S are independent because the gate scales rows only.
+// steep, overflows. Each CTA owns one (b,h) and 64 columns of dv (32 for
+// keys wider than 256); columns of S are independent because the gate scales
+// rows only.
 //
 // The bilinear gate G_t = alpha_t^T beta_t (Table 1's DFW row) adds a decay of
 // the value columns: with B'_r the in-chunk cumulative log beta of column j,
@@ -27,8 +29,6 @@
 namespace gla {
 namespace {
 
-constexpr int CS = kSimtChunk;
-constexpr int DVT = kSimtDvTile;
 constexpr int NT = 256;
 
 struct SimtArgs {
@@ -50,7 +50,10 @@ template <> __device__ __forceinline__ void st_out<__nv_bfloat16>(__nv_bfloat16*
     p[i] = __float2bfloat16_rn(x);
 }
 
-template <typename Tin>
+// CS rows per chunk and DVT state columns per CTA: 16 and 64 for dk <= 256;
+// for wider keys 8 and 32, so that the fp32 state tile and the chunk's key
+// rows still fit in shared memory (dk up to kSimtMaxDk).
+template <typename Tin, int CS, int DVT>
 __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
 {
     extern __shared__ float smem[];
@@ -190,8 +193,27 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
     }
 }
 
-size_t simt_smem_bytes(int dk) {
+size_t simt_smem_bytes(int dk, int CS, int DVT) {
     return sizeof(float) * ((size_t)dk * DVT + 5 * CS * dk + CS * DVT + CS * CS + dk + 2 * CS * DVT + DVT);
+}
+
+template <typename Tin, int CS, int DVT>
+cudaError_t launch_cfg(const SimtArgs& a, const gla_fwd_params& p, cudaStream_t s)
+{
+    const size_t smem = simt_smem_bytes(p.dk, CS, DVT);
+    dim3 grid(p.B * p.H, (p.dv + DVT - 1) / DVT);
+    cudaError_t e = cudaFuncSetAttribute(gla_fwd_simt_kernel<Tin, CS, DVT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gla_fwd_simt_kernel<Tin, CS, DVT><<<grid, NT, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_dtype(const SimtArgs& a, const gla_fwd_params& p, cudaStream_t s)
+{
+    if (p.dk <= kMaxDk) return launch_cfg<Tin, kSimtChunk, kSimtDvTile>(a, p, s);
+    return launch_cfg<Tin, kSimtChunkWide, kSimtDvTileWide>(a, p, s);
 }
 
 }  // namespace
@@ -203,19 +225,8 @@ cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s, co
     a.only = only;
     a.q = p.q; a.k = p.k; a.v = p.v; a.log_g = p.log_g; a.log_b = p.log_b; a.S0 = p.S0; a.O = p.O; a.ST = p.ST;
     a.B = p.B; a.H = p.H; a.T = p.T; a.dk = p.dk; a.dv = p.dv; a.gate = p.gate;
-    const size_t smem = simt_smem_bytes(p.dk);
-    dim3 grid(p.B * p.H, (p.dv + DVT - 1) / DVT);
-    cudaError_t e;
-    if (p.dtype == GLA_FP32) {
-        e = cudaFuncSetAttribute(gla_fwd_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        gla_fwd_simt_kernel<float><<<grid, NT, smem, s>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(gla_fwd_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        gla_fwd_simt_kernel<__nv_bfloat16><<<grid, NT, smem, s>>>(a);
-    }
-    return cudaGetLastError();
+    if (p.dk > kSimtMaxDk) return cudaErrorInvalidValue;
+    return p.dtype == GLA_FP32 ? launch_dtype<float>(a, p, s) : launch_dtype<__nv_bfloat16>(a, p, s);
 }
 
 }  // namespace gla

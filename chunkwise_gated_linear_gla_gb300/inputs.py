@@ -99,6 +99,11 @@ WORKLOADS = {
         "bilinear", B=8, H=4, T=2048, dk=256, dv=512, dtype=torch.bfloat16,
         gate=GATE_BILINEAR, s0_std=0.02,
         notes="bilinear gate alpha_t^T beta_t (DFW form), 1.3B layer shape"),
+    "gla_wide_heads": Workload(
+        "gla_wide_heads", B=8, H=2, T=2048, dk=512, dv=1024, dtype=torch.bfloat16,
+        gate=GATE_PER_KEY, s0_std=0.02,
+        notes="the 1.3B layer (d_model 2048, dk = d/2, dv = d) cut into 2 heads instead of 4: "
+              "larger head dimensions, as in the head-count ablation; keys wider than 256"),
     "gla_long": Workload(
         "gla_long", B=1, H=4, T=65536, dk=256, dv=512, dtype=torch.bfloat16,
         gate=GATE_PER_KEY, notes="long sequence, low B*H"),

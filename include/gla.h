@@ -63,7 +63,7 @@ extern "C" {
 typedef enum {
     GLA_OK = 0,
     GLA_ERR_INVALID_ARG = 1,  /* null/overlapping/misaligned pointer, bad size, gate/log_g mismatch */
-    GLA_ERR_UNSUPPORTED = 2,  /* valid request this build does not handle (chunk size, device) */
+    GLA_ERR_UNSUPPORTED = 2,  /* valid request this build does not handle (chunk size, dk > 768, device) */
     GLA_ERR_CUDA = 3,         /* a CUDA runtime call or a launch failed */
     GLA_ERR_WORKSPACE = 4,    /* workspace missing, too small or could not be allocated */
     GLA_ERR_TIMEOUT = 5       /* a kernel's bounded wait ran out (reported by gla_device_status) */
@@ -81,7 +81,9 @@ typedef enum {
 
 /* Which kernels run. AUTO picks the tcgen05 tensor-core path for bf16 inputs
  * with dk in {64,128,256} and dv a multiple of 128, and the fp32 CUDA-core
- * path otherwise (always for fp32 inputs). Both compute the same function. */
+ * path otherwise (always for fp32 inputs). Both compute the same function.
+ * The forward pass takes any dk and dv that are multiples of 16 with
+ * dk <= 768; keys wider than 256 run on the CUDA-core path. */
 typedef enum { GLA_PATH_AUTO = 0, GLA_PATH_TENSOR = 1, GLA_PATH_SIMT = 2 } gla_path;
 
 typedef struct {

@@ -93,7 +93,9 @@ BAD = [
     ("tensor path with the bilinear gate in fp32",
      dict(gate=4, log_b=0x900000, dtype=bnd.GLA_FP32, dv=128, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("chunk 32", dict(chunk=32), bnd.GLA_ERR_UNSUPPORTED),
-    ("dk 512", dict(dk=512), bnd.GLA_ERR_UNSUPPORTED),
+    ("dk 784", dict(dk=784), bnd.GLA_ERR_UNSUPPORTED),
+    ("tensor path with dk 512", dict(dk=512, path=bnd.GLA_PATH_TENSOR, q=0x1000000, k=0x9000000, v=0x11000000,
+                                     log_g=0x21000000, O=0x31000000), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with dv 48", dict(dv=48, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
 ]
@@ -139,6 +141,11 @@ def test_plan_on_host():
     # empty sequence: only the state copy
     p = _params(T=0, q=None, k=None, v=None, O=None)
     assert bnd.gla_fwd_stage_name(p, 0) == "gla_copy_state"
+    # keys wider than 256 (up to 768) take the CUDA-core path in bf16 too
+    for dk in (272, 512, 768):
+        p = _params(dk=dk, dv=1024, q=0x1000000, k=0x9000000, v=0x11000000, log_g=0x21000000, O=0x31000000)
+        assert bnd.gla_fwd_num_stages(p) == 1 and bnd.gla_fwd_stage_name(p, 0) == "gla_fwd_simt"
+        assert bnd.gla_fwd_workspace_size(p) == 0
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

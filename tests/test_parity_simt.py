@@ -30,6 +30,18 @@ def _run(w, seed=0, path=gla.GLA_PATH_SIMT, **kw):
     return x, to_np(O), to_np(ST), Oref, STref
 
 
+def _run_any(w, seed=0, path=gla.GLA_PATH_SIMT):
+    """_run for every gate mode, the bilinear gate's log beta included."""
+    x = gi.make_inputs(w, seed=seed)
+    d = lambda t: None if t is None else t.cuda()
+    O, ST = gla.forward(d(x["q"]), d(x["k"]), d(x["v"]), d(x["log_g"]), d(x["S0"]),
+                        gate=x["gate"], path=path, log_b=d(x.get("log_b")))
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], log_b=x.get("log_b"))
+    return x, to_np(O), to_np(ST), Oref, STref
+
+
 def test_fp32_workload_full_size():
     """The fp32 workload (B=1, H=2, T=256, dk=dv=64, per-key gate) at its full size."""
     w = gi.WORKLOADS["fp32_small"]
@@ -70,6 +82,57 @@ def test_fp32_dk256_dv_tail():
     x, O, ST, Oref, STref = _run(w, seed=7)
     assert_close(O, Oref, torch.float32, "O")
     assert_close(ST, STref, torch.float32, "ST")
+
+
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR,
+                                  gi.GATE_BILINEAR])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_wide_keys(gate, dtype):
+    """Keys wider than 256 (8-row chunks, 32 state columns per CTA): dk = 320 with a
+    ragged last chunk and a ragged last dv tile, every gate mode, both dtypes."""
+    w = gi.Workload("t", B=1, H=2, T=45, dk=320, dv=80, dtype=dtype, gate=gate, s0_std=0.05)
+    x, O, ST, Oref, STref = _run_any(w, seed=11, path=gla.GLA_PATH_AUTO)
+    assert_close(O, Oref, dtype, "O")
+    assert_close(ST, STref, dtype, "ST")
+
+
+@pytest.mark.parametrize("dk,T", [(512, 70), (768, 17)])
+def test_widest_keys(dk, T):
+    """dk = 512 (one head of the 340M model's ablation with a single head: d_model 1024,
+    dk = d/2, dv = d) and the widest supported, dk = 768, with a steep gate."""
+    w = gi.Workload("t", B=1, H=1, T=T, dk=dk, dv=64, dtype=torch.float32, gate=gi.GATE_PER_KEY,
+                    gate_dist="steep", s0_std=0.1)
+    x, O, ST, Oref, STref = _run_any(w, seed=dk, path=gla.GLA_PATH_AUTO)
+    assert_close(O, Oref, torch.float32, "O")
+    assert_close(ST, STref, torch.float32, "ST")
+
+
+def test_wide_heads_workload_sampled():
+    """The wide-head workload (B=8, H=2, T=2048, dk=512, dv=1024, bf16, per-key gate) at
+    its full size, in the launch configuration the bench times, checked on two
+    sampled heads the oracle computes alone."""
+    w = gi.WORKLOADS["gla_wide_heads"]
+    x = gi.make_inputs(w, seed=0)
+    d = lambda t: None if t is None else t.cuda()
+    O, ST = gla.forward(d(x["q"]), d(x["k"]), d(x["v"]), d(x["log_g"]), d(x["S0"]), gate=x["gate"])
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    ref = oracle.gla_forward_rows(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], [(0, 0), (7, 1)])
+    for (b, h), (Oref, STref) in ref.items():
+        assert_close(to_np(O[b, h]), Oref, torch.bfloat16, f"O[{b},{h}]")
+        assert_close(to_np(ST[b, h]), STref, torch.bfloat16, f"ST[{b},{h}]")
+
+
+def test_wide_keys_rejected_on_tensor_path_and_beyond_768():
+    w = gi.Workload("t", B=1, H=1, T=8, dk=512, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY)
+    x = gi.make_inputs(w, seed=0)
+    d = lambda t: None if t is None else t.cuda()
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        gla.forward(d(x["q"]), d(x["k"]), d(x["v"]), d(x["log_g"]), None, gate=x["gate"], path=gla.GLA_PATH_TENSOR)
+    w = w.with_(dk=784)
+    x = gi.make_inputs(w, seed=0)
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        gla.forward(d(x["q"]), d(x["k"]), d(x["v"]), d(x["log_g"]), None, gate=x["gate"])
 
 
 def test_empty_sequence_copies_state():
