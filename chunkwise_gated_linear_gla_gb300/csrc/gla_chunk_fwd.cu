@@ -160,6 +160,20 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         tmem_alloc(tmem_holder, L::TCOLS);
         tmem_relinquish();
     }
+    // Epilogue threads issue every load of their S_in columns (dv column d, HC keys)
+    // before the set-up barrier, so the loads overlap the set-up and are all in flight
+    // at once; they go to tensor memory after the barrier.
+    constexpr int NB = HC / 32;
+    uint32_t s_in[NB][32];
+    if (warp >= 2) {
+        const int d = (warp & 3) * 32 + lane, cb = ((warp - 2) >> 2) * HC;
+        const float* sin = a.S_in ? a.S_in + bh * a.s_in_bh + seg * a.s_in_seg + dv0 + d : nullptr;
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                s_in[b][i] = sin ? __float_as_uint(sin[(size_t)(cb + b * 32 + i) * a.dv]) : 0u;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -278,17 +292,9 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         const int cb = grp * HC;                 // first state column of this group
         const int gt = threadIdx.x - 64 - grp * 128;   // thread index within the group
         const int bar_grp = BAR_G0 + grp;
-        {
-            const float* sin = a.S_in ? a.S_in + bh * a.s_in_bh + seg * a.s_in_seg + dv0 + d : nullptr;
-#pragma unroll 1
-            for (int c0 = cb; c0 < cb + HC; c0 += 32) {
-                uint32_t r[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = sin ? __float_as_uint(sin[(size_t)(c0 + i) * a.dv]) : 0u;
-                tmem_st32(tS + lb + c0, r);
-            }
-            tmem_wait_st();
-        }
+        for (int b = 0; b < NB; ++b) tmem_st32(tS + lb + cb + b * 32, s_in[b]);
+        tmem_wait_st();
         // drain the O accumulator of chunk m: TMEM -> registers -> bf16 smem tile -> TMA store;
         // lbc_m is B'_C[d] of chunk m (bilinear gate)
         auto drain = [&](int m, float lbc_m) -> bool {
@@ -430,27 +436,28 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             }
             lbc_prev = lbc_cur;
         }
-        if (alive && want_out && nloc > 0 && !drain(nloc - 1, lbc_prev)) alive = false;
-        if (!alive && gt == 0) fail(a.status, abort_flag, ERR_EPI);
+        // The final state is complete once the last state MMA is (before the last inter
+        // and intra MMAs): its stores go out while those run, then the last O drain.
         if (alive && nloc > 0) {
             const bool ok = mbar_wait(s_done, (nloc - 1) & 1, kTimeoutNs);
             if (group_all_ok(ok, BAR_EPI, NEPI)) {
                 tc_fence_after();
                 if (a.S_out) {
                     float* so = a.S_out + bh * a.s_out_bh + seg * a.s_out_seg + dv0 + d;
-#pragma unroll 1
-                    for (int c0 = cb; c0 < cb + HC; c0 += 32) {
-                        uint32_t r[32];
-                        tmem_ld32(tS + lb + c0, r);
-                        tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) so[(size_t)(c0 + i) * a.dv] = __uint_as_float(r[i]);
-                    }
+                    for (int b = 0; b < NB; ++b) tmem_ld32(tS + lb + cb + b * 32, s_in[b]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) so[(size_t)(cb + b * 32 + i) * a.dv] = __uint_as_float(s_in[b][i]);
                 }
-            } else if (gt == 0) {
-                fail(a.status, abort_flag, ERR_EPI);
+            } else {
+                alive = false;
             }
         }
+        if (alive && want_out && nloc > 0 && !drain(nloc - 1, lbc_prev)) alive = false;
+        if (!alive && gt == 0) fail(a.status, abort_flag, ERR_EPI);
         if (gt == 0) bulk_wait0();
     }
 

@@ -144,17 +144,34 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
             }
         __syncthreads();
         // intra-chunk scores, pairwise in log space (r >= s)
-        for (int p = tid; p < CS * (CS + 1) / 2; p += NT) {
-            int r = 0;
-            while ((r + 1) * (r + 2) / 2 <= p) ++r;
-            const int s = p - r * (r + 1) / 2;
-            float acc = 0.f;
-            const float* qrow = qr + r * dk;
-            const float* krow = kr + s * dk;
-            const float* br = bc + r * dk;
-            const float* bs = bc + s * dk;
-            for (int kk = 0; kk < dk; ++kk) acc = fmaf(qrow[kk] * krow[kk], expf(br[kk] - bs[kk]), acc);
-            A[r * CS + s] = acc;
+        if constexpr (CS * (CS + 1) / 2 >= NT / 2) {
+            // one thread per pair
+            for (int p = tid; p < CS * (CS + 1) / 2; p += NT) {
+                int r = 0;
+                while ((r + 1) * (r + 2) / 2 <= p) ++r;
+                const int s = p - r * (r + 1) / 2;
+                float acc = 0.f;
+                const float* qrow = qr + r * dk;
+                const float* krow = kr + s * dk;
+                const float* br = bc + r * dk;
+                const float* bs = bc + s * dk;
+                for (int kk = 0; kk < dk; ++kk) acc = fmaf(qrow[kk] * krow[kk], expf(br[kk] - bs[kk]), acc);
+                A[r * CS + s] = acc;
+            }
+        } else {
+            // few pairs and wide keys: one warp per pair, its lanes splitting the keys
+            const int lane = tid & 31;
+            for (int p = tid >> 5; p < CS * (CS + 1) / 2; p += NT / 32) {
+                int r = 0;
+                while ((r + 1) * (r + 2) / 2 <= p) ++r;
+                const int s = p - r * (r + 1) / 2;
+                float acc = 0.f;
+                for (int kk = lane; kk < dk; kk += 32)
+                    acc = fmaf(qr[r * dk + kk] * kr[s * dk + kk], expf(bc[r * dk + kk] - bc[s * dk + kk]), acc);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (lane == 0) A[r * CS + s] = acc;
+            }
         }
         __syncthreads();
         // outputs: inter (Q (.) Lambda) S + intra (P (.) M) V
@@ -176,11 +193,19 @@ __global__ void __launch_bounds__(NT) gla_fwd_simt_kernel(SimtArgs a)
         }
         __syncthreads();
         // state: S <- (gamma^T 1) (.) S + (K (.) Gamma)^T V
+        // (NT is a multiple of DVT, so a thread's column j is the same for every i)
+        static_assert(NT % DVT == 0, "fixed state column per thread");
         const float* vs = bil ? vg : vv;
+        const int jt = tid % DVT;
+        float vcol[CS];
+#pragma unroll
+        for (int r = 0; r < CS; ++r) vcol[r] = vs[r * DVT + jt];
+        const float gcol = bil ? gv[jt] : 1.f;
         for (int i = tid; i < dk * DVT; i += NT) {
-            const int kk = i / DVT, j = i % DVT;
-            float acc = gam[kk] * (bil ? gv[j] : 1.f) * S[i];
-            for (int r = 0; r < CS; ++r) acc = fmaf(kt[r * dk + kk], vs[r * DVT + j], acc);
+            const int kk = i / DVT;
+            float acc = gam[kk] * gcol * S[i];
+#pragma unroll
+            for (int r = 0; r < CS; ++r) acc = fmaf(kt[r * dk + kk], vcol[r], acc);
             S[i] = acc;
         }
     }
