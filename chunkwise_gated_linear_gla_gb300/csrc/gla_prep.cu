@@ -76,7 +76,32 @@ struct PrepArgs {
     __nv_bfloat16* A;
     int* status;
     int BH, H, T, nchunks, Tpad, gate;
+    // read first by the next stages (see prefetch_next_stage): S0, and v by heads
+    const uint8_t* pf_s0;   size_t pf_s0_bytes;
+    const uint8_t* pf_v;    size_t pf_v_stride;   uint32_t pf_v_bytes;
 };
+
+// After its last item a CTA pulls into L2 what the stages after this one read
+// first: the initial state S0 (read before the first chunk can be decayed) and
+// the first two chunks of v of every head. The stages then start from L2
+// instead of competing for DRAM at once. The work goes to the CTAs that have
+// one item fewer than the others, which finish first, one bulk prefetch per
+// piece from one thread each.
+__device__ __forceinline__ void prefetch_next_stage(const PrepArgs& a, int total)
+{
+    const int extra = total % (int)gridDim.x;   // CTAs [0, extra) run one more item
+    const int lo = extra, n = extra ? (int)gridDim.x - extra : (int)gridDim.x;
+    if (threadIdx.x != 0 || (int)blockIdx.x < lo) return;
+    const int me = (int)blockIdx.x - lo;
+    constexpr size_t kPiece = 64 * 1024;
+    if (a.pf_s0) {
+        const size_t per = ((a.pf_s0_bytes + n - 1) / n + 15) / 16 * 16;
+        for (size_t off = (size_t)me * per, end = min(a.pf_s0_bytes, off + per); off < end; off += kPiece)
+            prefetch_l2(a.pf_s0 + off, (uint32_t)min(kPiece, end - off));
+    }
+    if (a.pf_v)
+        for (int bh = me; bh < a.BH; bh += n) prefetch_l2(a.pf_v + (size_t)bh * a.pf_v_stride, a.pf_v_bytes);
+}
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;   // bounded waits: bulk copies, score MMA
 constexpr int ERR_PREP = 0x201;
@@ -528,6 +553,7 @@ gla_chunk_prep_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const
     }
     __syncthreads();   // shared tiles are refilled by the next item
     }
+    prefetch_next_stage(a, total);
     if (tid == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
@@ -728,6 +754,7 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     }
     }
     if (tid == 0 && pend_b >= 0) mbar_wait(&cbar[pend_b], pend_par, kTimeoutNs);
+    prefetch_next_stage(a, total);
     if (tid == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
@@ -801,6 +828,11 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     a.A = reinterpret_cast<__nv_bfloat16*>(base + pl.off_A);
     a.status = status;
     a.BH = p.B * p.H; a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
+    a.pf_s0 = static_cast<const uint8_t*>(static_cast<const void*>(p.S0));
+    a.pf_s0_bytes = p.S0 ? (size_t)a.BH * p.dk * p.dv * 4 : 0;
+    a.pf_v = static_cast<const uint8_t*>(p.v);
+    a.pf_v_stride = (size_t)p.T * p.dv * 2;
+    a.pf_v_bytes = (uint32_t)((size_t)min(p.T, 2 * C) * p.dv * 2);
     const int sms = pl.sms > 0 ? pl.sms : 148;
     CUtensorMap mq, mk, mA;
     if (!map_rows(&mq, p.q, p.dk, p.T, a.BH) || !map_rows(&mk, p.k, p.dk, p.T, a.BH)) return cudaErrorInvalidValue;
