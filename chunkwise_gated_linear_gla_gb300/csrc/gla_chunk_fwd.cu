@@ -59,11 +59,15 @@ struct FwdArgs {
     const float* gam;   // [BH][nchunks][dk], null without a gate
     int* status;
     int dv, nchunks, cps, mode, gated;
-    // bilinear gate only
-    const float* lbc;   // [BH][nchunks][dv] B'_C, the chunk's total log beta per column
-    const float* lb;    // [BH][T][dv] log beta
+    // bilinear gate: lbc = B'_C [BH][nchunks][dv], the chunk's total log beta per column,
+    // lb = log beta [BH][T][dv]. Per-head scalar gate (SCAL): lamh = log lambda [H]; chunks
+    // that pass q_factored take raw q, and the drain scales output row r by lambda^(r+1).
+    // (The union keeps this struct at 128 bytes, which the compiler keeps in registers; a
+    // larger one went to the stack.)
+    const float* lbc;
+    union { const float* lb; const float* lamh; };
     const int* skip;    // [BH] heads left to the CUDA-core pass
-    int T;
+    int T, H;
 };
 
 template <int DK, bool BIL>
@@ -112,11 +116,11 @@ __device__ __forceinline__ bool group_all_ok(bool ok, int id, int n) {
 
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
-template <int DK, bool BIL>
+template <int DK, bool BIL, bool SCAL>
 __global__ void __launch_bounds__(NT, 1)
 gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmO)
+                     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmQr)
 {
     using L = Lay<DK, BIL>;
     constexpr int HC = DK / 2;   // state columns per epilogue thread
@@ -145,6 +149,10 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     const int nloc = max(0, c_end - c_begin);
     const bool want_out = a.mode != kModeSegState;
     const bool gated = a.gated != 0;
+    // per-head scalar gate: whether chunk ch's query factor is left to this pass (the prep
+    // made the same decision on the same float, rows x log lambda)
+    const float lam_h = SCAL ? a.lamh[bh % a.H] : 0.f;
+    auto q_fac = [&](int ch) -> bool { return SCAL && q_factored((float)min(C, a.T - ch * C) * lam_h); };
 
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1); mbar_init(&full[1], 1);
@@ -155,6 +163,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tmap(&tmQ); prefetch_tmap(&tmK); prefetch_tmap(&tmV); prefetch_tmap(&tmA); prefetch_tmap(&tmO);
+        if (SCAL) prefetch_tmap(&tmQr);
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, L::TCOLS);
@@ -203,9 +212,10 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 tma_load_3d(sb + L::V_OFF, &tmV, &full[st], dv0, c * C, bh);
                 tma_load_3d(sb + L::V_OFF + 8192, &tmV, &full[st], dv0 + 64, c * C, bh);
                 if (want_out) {
+                    const CUtensorMap* mq = q_fac(c) ? &tmQr : &tmQ;
 #pragma unroll
                     for (int i = 0; i < DK / 64; ++i)
-                        tma_load_3d(sb + L::Q_OFF + i * 8192, &tmQ, &full[st], i * 64, c * C, bh);
+                        tma_load_3d(sb + L::Q_OFF + i * 8192, mq, &full[st], i * 64, c * C, bh);
                     tma_load_2d(sb + L::A_OFF, &tmA, &full[st], 0, (bh * a.nchunks + c) * C);
                 }
                 // L2 prefetch two chunks ahead, beyond what the two shared-memory stages
@@ -220,9 +230,10 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     for (int i = 0; i < DK / 64; ++i, ++item)
                         if (item % nt == me) prefetch_l2_tile_3d(&tmK, i * 64, cp * C, bh);
                     if (want_out) {
+                        const CUtensorMap* mq = q_fac(cp) ? &tmQr : &tmQ;
 #pragma unroll
                         for (int i = 0; i < DK / 64; ++i, ++item)
-                            if (item % nt == me) prefetch_l2_tile_3d(&tmQ, i * 64, cp * C, bh);
+                            if (item % nt == me) prefetch_l2_tile_3d(mq, i * 64, cp * C, bh);
                         if (item % nt == me) prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
                         ++item;
                     }
@@ -300,6 +311,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         auto drain = [&](int m, float lbc_m) -> bool {
             const int b = m & 1;
             float w[32];
+            const bool fq = SCAL && q_fac(c_begin + m);   // per-head gate: output rows take lambda^(r+1)
             if constexpr (BIL) {
                 // log beta of this thread's 32 rows of chunk m (rows past T add nothing), and an
                 // L2 prefetch of chunk m+2's rows, one 128-byte line per thread
@@ -342,6 +354,11 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 }
 #pragma unroll
                 for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * w[t]);
+            } else if (SCAL && fq) {
+                // (r + 1) log lambda lies in [-kQGuard, 0] for every row r of the chunk
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    r[t] = __float_as_uint(__uint_as_float(r[t]) * __expf((float)(grp * 32 + t + 1) * lam_h));
             }
             // the store issued from this half-buffer two chunks ago must have read it
             if (gt == 0) bulk_wait_read1();
@@ -477,14 +494,14 @@ bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, swz);
 }
 
-template <int DK, bool BIL>
+template <int DK, bool BIL, bool SCAL>
 cudaError_t launch_dk(const FwdArgs& a, dim3 grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                      const CUtensorMap& A, const CUtensorMap& o, cudaStream_t s) {
+                      const CUtensorMap& A, const CUtensorMap& o, const CUtensorMap& qr, cudaStream_t s) {
     using L = Lay<DK, BIL>;
-    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK, BIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK, BIL, SCAL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    gla_chunk_fwd_kernel<DK, BIL><<<grid, NT, L::SMEM, s>>>(a, q, k, v, A, o);
+    gla_chunk_fwd_kernel<DK, BIL, SCAL><<<grid, NT, L::SMEM, s>>>(a, q, k, v, A, o, qr);
     return cudaGetLastError();
 }
 
@@ -497,8 +514,15 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     const void* qb = pl.raw_qk ? p.q : base + pl.off_qt;
     const void* kb = pl.raw_qk ? p.k : base + pl.off_kt;
     const uint64_t qrows = pl.raw_qk ? (uint64_t)p.T : (uint64_t)pl.Tpad;
-    CUtensorMap mq, mk, mv, ma, mo;
+    CUtensorMap mq, mk, mv, ma, mo, mqr;
     if (!map3(&mq, qb, p.dk, qrows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    // raw q for the chunks of a per-head scalar gate whose query factor this pass applies
+    const bool qfac = q_factor_offload(p);
+    if (qfac) {
+        if (!map3(&mqr, p.q, p.dk, p.T, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    } else {
+        mqr = mq;
+    }
     if (!map3(&mk, kb, p.dk, qrows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     const bool bil = p.gate == GLA_GATE_BILINEAR;
     const void* vb = bil ? base + pl.off_vh : p.v;   // bilinear gate: V (.) D' from gla_value_prep
@@ -532,22 +556,31 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     a.gated = p.gate != GLA_GATE_NONE;
     a.lbc = bil ? reinterpret_cast<const float*>(base + pl.off_lbc) : nullptr;
     a.lb = p.log_b;
+    if (qfac) a.lamh = p.log_g;
     a.skip = bil ? reinterpret_cast<const int*>(base + pl.off_flag) : nullptr;
     a.T = p.T;
+    a.H = p.H;
     dim3 grid(pl.n_dvt, (unsigned)BH, mode == kModeFull ? 1 : pl.nseg);
     if (bil) {
         if (mode != kModeFull) return cudaErrorInvalidValue;   // no sequence split with the bilinear gate
         switch (p.dk) {
-        case 64: return launch_dk<64, true>(a, grid, mq, mk, mv, ma, mo, s);
-        case 128: return launch_dk<128, true>(a, grid, mq, mk, mv, ma, mo, s);
-        case 256: return launch_dk<256, true>(a, grid, mq, mk, mv, ma, mo, s);
+        case 64: return launch_dk<64, true, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+        case 128: return launch_dk<128, true, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+        case 256: return launch_dk<256, true, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+        }
+        return cudaErrorInvalidValue;
+    }
+    if (qfac) {
+        switch (p.dk) {
+        case 64: return launch_dk<64, false, true>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+        case 128: return launch_dk<128, false, true>(a, grid, mq, mk, mv, ma, mo, mqr, s);
         }
         return cudaErrorInvalidValue;
     }
     switch (p.dk) {
-    case 64: return launch_dk<64, false>(a, grid, mq, mk, mv, ma, mo, s);
-    case 128: return launch_dk<128, false>(a, grid, mq, mk, mv, ma, mo, s);
-    case 256: return launch_dk<256, false>(a, grid, mq, mk, mv, ma, mo, s);
+    case 64: return launch_dk<64, false, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+    case 128: return launch_dk<128, false, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+    case 256: return launch_dk<256, false, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -24,6 +24,16 @@ constexpr int kSimtMaxDk = 768;
 // Bilinear gate on the tensor-core path: the largest |in-chunk partial sum of
 // log beta| for which one reference per chunk stays exact to rounding.
 constexpr float kVGuard = 60.f;
+// Per-head scalar gate on the tensor-core path: a chunk whose in-chunk log
+// decay B_end = rows * log(lambda) stays above -kQGuard takes the query row
+// factor lambda^(r+1) out of the inter and intra products (the chunk pass reads
+// raw q and scales its output rows), so the prep writes no Q (.) Lambda for it.
+// The prep and the chunk pass decide with this same test on the same float.
+constexpr float kQGuard = 60.f;
+__host__ __device__ __forceinline__ bool q_factored(float b_end) { return b_end >= -kQGuard; }
+// Whether a pass takes that form at all: the per-head scalar gate with dk <= 128 (at
+// dk = 256 the chunk pass's extra drain work spills registers).
+inline bool q_factor_offload(const gla_fwd_params& p) { return p.gate == GLA_GATE_HEAD_SCALAR && p.dk <= 128; }
 
 enum StageKind {
     STAGE_SIMT = 0,        // whole pass on CUDA cores

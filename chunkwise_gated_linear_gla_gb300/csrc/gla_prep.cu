@@ -76,6 +76,7 @@ struct PrepArgs {
     __nv_bfloat16* A;
     int* status;
     int BH, H, T, nchunks, Tpad, gate;
+    int qfac;   // per-head scalar gate: chunks that pass q_factored leave Lambda to the chunk pass
     // read first by the next stages (see prefetch_next_stage): S0, and v by heads
     const uint8_t* pf_s0;   size_t pf_s0_bytes;
     const uint8_t* pf_v;    size_t pf_v_stride;   uint32_t pf_v_bytes;
@@ -199,10 +200,14 @@ __device__ __forceinline__ void score_mma(const uint8_t* Qs, const uint8_t* Ks, 
 // lam: log of the per-head decay (scores scaled by lambda^(r-s)), 0 otherwise.
 // TOK (per-token scalar gate): Lc is the chunk's inclusive cumulative log gate in
 // shared memory; the scores are then scaled by exp(Lc[r] - Lc[s]) and lam is unused.
+// With `fq` (a per-head scalar gate whose chunk passes q_factored) the query
+// row's factor lambda^(r+1) is left out: the scores are (q_r . k_s) lambda^-(s+1),
+// and the chunk pass multiplies output row r by lambda^(r+1).
 template <bool TOK = false>
 __device__ __forceinline__ bool score_readout(uint32_t tmem, uint64_t* bar, uint32_t phase, int nr, float lam,
                                               __nv_bfloat16* stage, const CUtensorMap* tmA, int arow,
-                                              int free_bar = -1, int free_n = 0, const float* Lc = nullptr) {
+                                              int free_bar = -1, int free_n = 0, const float* Lc = nullptr,
+                                              bool fq = false) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const bool ok = mbar_wait(bar, phase, kTimeoutNs);
     tc_fence_after();
@@ -211,6 +216,7 @@ __device__ __forceinline__ bool score_readout(uint32_t tmem, uint64_t* bar, uint
     uint4* dst = reinterpret_cast<uint4*>(stage + r * 64);
     uint32_t p[2][16];
     const float lr = TOK ? Lc[r] : 0.f;
+    const int rr = fq ? -1 : r;   // the per-head gate's exponent (rr - s) lam
 #pragma unroll
     for (int h = 0; h < 2; ++h) {   // columns 32h .. 32h + 31, one half at a time
         uint32_t v[32];
@@ -226,7 +232,7 @@ __device__ __forceinline__ bool score_readout(uint32_t tmem, uint64_t* bar, uint
                 if (TOK)
                     x[e] = keep ? __uint_as_float(v[2 * i + e]) * __expf(lr - Lc[s]) : 0.f;
                 else
-                    x[e] = keep ? __uint_as_float(v[2 * i + e]) * (lam != 0.f ? __expf((r - s) * lam) : 1.f) : 0.f;
+                    x[e] = keep ? __uint_as_float(v[2 * i + e]) * (lam != 0.f ? __expf((rr - s) * lam) : 1.f) : 0.f;
             }
             p[h][i] = pack_bf16(x[0], x[1]);
         }
@@ -714,6 +720,8 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     }
     if (tok)
         for (int col = tid; col < DK; col += NTU) a.gam[((size_t)bh * a.nchunks + c) * DK + col] = __expf(Lc[C - 1]);
+    // per-head gate: a chunk whose decay stays within exp(-kQGuard) leaves Lambda to the chunk pass
+    const bool fq = GATE == GLA_GATE_HEAD_SCALAR && a.qfac && q_factored(nr * lam);
     // Q (pass 0) or K (pass 1), rows [r0, r1), by nth threads
     auto scale_rows = [&](int pass, int r0, int r1, int t, int nth) {
         const __nv_bfloat16* T = pass == 0 ? Qs : Ks;
@@ -735,10 +743,10 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     // (named barrier 2); the K rows are split in proportion to the threads
     constexpr int KSPLIT = C * (NTU - 64) / NTU;
     if (warp < 2) {
-        ok = score_readout<tok>(tmem, mbar, mphase, nr, lam, Qs, &tmA, (bh * a.nchunks + c) * C, 2, NTU, Lc);
+        ok = score_readout<tok>(tmem, mbar, mphase, nr, lam, Qs, &tmA, (bh * a.nchunks + c) * C, 2, NTU, Lc, fq);
         if (gated) scale_rows(1, KSPLIT, C, tid, 64);
     } else {
-        if (gated) scale_rows(0, 0, C, tid - 64, NTU - 64);
+        if (gated && !fq) scale_rows(0, 0, C, tid - 64, NTU - 64);
         named_bar_arrive(2, NTU);
         if (gated) scale_rows(1, 0, KSPLIT, tid - 64, NTU - 64);
     }
@@ -828,6 +836,7 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     a.A = reinterpret_cast<__nv_bfloat16*>(base + pl.off_A);
     a.status = status;
     a.BH = p.B * p.H; a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
+    a.qfac = q_factor_offload(p);
     a.pf_s0 = static_cast<const uint8_t*>(static_cast<const void*>(p.S0));
     a.pf_s0_bytes = p.S0 ? (size_t)a.BH * p.dk * p.dv * 4 : 0;
     a.pf_v = static_cast<const uint8_t*>(p.v);

@@ -87,6 +87,68 @@ def test_prep_stage_outputs():
     assert np.all(qt[:, 100:] == 0) and np.all(kt[:, 100:] == 0)
 
 
+def test_prep_stage_factored_scalar_gate():
+    """Stage 0 under a per-head scalar gate: a chunk whose decay (rows x log lambda) stays
+    above -60 leaves the query factor lambda^(r+1) to the chunk pass, so its scores are
+    (q_r . k_s) lambda^-(s+1) and no Q (.) Lambda rows are written; a steeper head keeps
+    the scores (q_r . k_s) lambda^(r-s) and its Q (.) Lambda rows."""
+    w = gi.Workload("t", B=1, H=2, T=100, dk=64, dv=128, dtype=torch.bfloat16, gate=gi.GATE_HEAD_SCALAR)
+    x = gi.make_inputs(w, seed=2)
+    x["log_g"] = torch.tensor([-0.04, -2.0], dtype=torch.float32)   # 64 x 2.0 > 60: head 1 is not factored
+    c = _dev(x)
+    O = torch.empty(1, 2, 100, 128, dtype=torch.bfloat16, device="cuda")
+    p = bnd.make_params(c["q"], c["k"], c["v"], c["log_g"], None, O, None, path=bnd.GLA_PATH_TENSOR)
+    n = bnd.gla_fwd_workspace_size(p)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    p.workspace, p.workspace_bytes = ws.data_ptr(), n
+    bnd.gla_fwd_stage(p, 0)
+    torch.cuda.synchronize()
+    BH, Tpad, dk, nch = 2, 128, 64, 2
+    off = BH * Tpad * dk * 2
+    qt = ws[:off].view(torch.bfloat16).view(BH, Tpad, dk).float().cpu().numpy()
+    A = ws[2 * off: 2 * off + BH * nch * 64 * 64 * 2].view(torch.bfloat16).view(BH, nch, 64, 64).float().cpu().numpy()
+    q = x["q"].double().numpy().reshape(BH, 100, dk)
+    k = x["k"].double().numpy().reshape(BH, 100, dk)
+    lam = x["log_g"].double().numpy()
+    for bh in range(BH):
+        for ch in range(nch):
+            t0, t1 = ch * 64, min(100, ch * 64 + 64)
+            n_ = t1 - t0
+            r = np.arange(n_)
+            factored = n_ * lam[bh] >= -60.0
+            S = q[bh, t0:t1] @ k[bh, t0:t1].T
+            if factored:
+                P = np.tril(S * np.exp(-(r[None, :] + 1) * lam[bh]))
+                assert np.all(qt[bh, t0:t1] == 0)
+            else:
+                P = np.tril(S * np.exp((r[:, None] - r[None, :]) * lam[bh] * (r[:, None] >= r[None, :])))
+                np.testing.assert_allclose(qt[bh, t0:t1], q[bh, t0:t1] * np.exp((r + 1) * lam[bh])[:, None],
+                                           rtol=1e-2, atol=1e-3)
+            assert errors(A[bh, ch, :n_, :n_], P)[0] < 5e-3, (bh, ch, factored)
+            assert np.all(A[bh, ch][np.triu_indices(64, 1)] == 0)
+
+
+@pytest.mark.parametrize("dk", [64, 128, 256])
+def test_scalar_gate_factored_and_plain_heads(dk):
+    """Per-head decays on both sides of the query-factor guard (rows x log lambda >= -60)
+    in one call, a ragged last chunk, with and without the sequence split; at dk = 256
+    every chunk takes the plain form."""
+    w = gi.Workload("t", B=2, H=3, T=333, dk=dk, dv=128, dtype=torch.bfloat16, gate=gi.GATE_HEAD_SCALAR,
+                    s0_std=0.1)
+    x = gi.make_inputs(w, seed=37 + dk)
+    # 64 rows x 0.9 = 57.6 (factored), x 1.2 = 76.8 (plain; the 13-row tail, 15.6, factored)
+    x["log_g"] = torch.tensor([-0.02, -0.9, -1.2], dtype=torch.float32)
+    for nseg in (0, 3):
+        c = _dev(x)
+        O, ST = gla.forward(c["q"], c["k"], c["v"], c["log_g"], c["S0"], path=gla.GLA_PATH_TENSOR,
+                            force_segments=nseg)
+        torch.cuda.synchronize()
+        assert gla.gla_device_status() == 0
+        Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
+        assert_close(to_np(O), Oref, torch.bfloat16, f"O (segments {nseg})")
+        assert_close(to_np(ST), STref, torch.bfloat16, f"ST (segments {nseg})")
+
+
 # ---------------------------------------------------------------- small shapes
 
 @pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
