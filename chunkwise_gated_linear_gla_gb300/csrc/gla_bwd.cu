@@ -891,6 +891,7 @@ gla_status bwd_validate(const gla_bwd_params* p)
     if (!p) return GLA_ERR_INVALID_ARG;
     if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->dk <= 0 || p->dv <= 0) return GLA_ERR_INVALID_ARG;
     if (p->dtype != GLA_BF16 && p->dtype != GLA_FP32) return GLA_ERR_INVALID_ARG;
+    if (p->gate == GLA_GATE_BILINEAR) return GLA_ERR_UNSUPPORTED;   // its value-side gradient is not built
     if (p->gate < GLA_GATE_NONE || p->gate > GLA_GATE_TOKEN_SCALAR) return GLA_ERR_INVALID_ARG;
     if (p->dk % 16 != 0 || p->dv % 16 != 0) return GLA_ERR_INVALID_ARG;
     if ((long long)p->B * p->H > 65535) return GLA_ERR_INVALID_ARG;

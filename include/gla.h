@@ -198,8 +198,8 @@ gla_status gla_host_release(void);
  * every 16-row chunk, a reverse sweep carries dL/dS through the chunks, and
  * the gate gradient is the reverse cumulative sum over tokens of
  * q (.) dq - k (.) dk (plus rowsum(grad_ST (.) S_T) at the last token).
- * Every gate mode and dtype is supported (q, k, v and grad_O in `dtype`; all
- * gradients fp32; dk <= 256). For bf16 inputs with dk in {64, 128, 256} the
+ * Every gate mode but the bilinear one (GLA_ERR_UNSUPPORTED) and both dtypes
+ * are supported (q, k, v and grad_O in `dtype`; all gradients fp32; dk <= 256). For bf16 inputs with dk in {64, 128, 256} the
  * chunk products run on the tensor cores with bf16 operands and fp32
  * accumulation (like the forward tensor path); otherwise, or with
  * path = GLA_PATH_SIMT, everything runs in fp32 on CUDA cores. (The backward

@@ -232,6 +232,7 @@ BAD = [
     ("misaligned workspace", dict(workspace=0x7000010, workspace_bytes=1 << 20), bnd.GLA_ERR_INVALID_ARG),
     ("bad dtype", dict(dtype=5), bnd.GLA_ERR_INVALID_ARG),
     ("dk 512", dict(dk=512), bnd.GLA_ERR_UNSUPPORTED),
+    ("bilinear gate", dict(gate=4), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with dk 48", dict(dk=48, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("bad path", dict(path=7), bnd.GLA_ERR_INVALID_ARG),
