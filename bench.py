@@ -113,7 +113,10 @@ def stage_bytes(w, name, nseg=1):
     qk_tiles = (Tp if gated else T) * dk * 2 * 2
     gam = nch * dk * 4 if gated else 0
     if name == "gla_chunk_prep":
-        return BH * (T * dk * 2 * 2 + gate_in + (Tp * dk * 2 * 2 if gated else 0) + nch * C * C * 2 + gam)
+        # per-head decay with dk <= 128: chunks whose decay stays within e^-60 (every chunk of the
+        # workloads' lambda_h) leave Q (.) Lambda to the chunk pass, so only K (.) Gamma is written
+        qk_out = 0 if not gated else Tp * dk * 2 * (1 if (w.gate == 1 and dk <= 128) else 2)
+        return BH * (T * dk * 2 * 2 + gate_in + qk_out + nch * C * C * 2 + gam)
     if name == "gla_chunk_fwd":
         last_state = (s0 + st) if nseg == 1 else BH * nseg * dk * dv * 4
         # bilinear gate: V (.) D' in place of v, plus log beta and the chunks' column decays
