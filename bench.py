@@ -117,6 +117,14 @@ def stage_bytes(w, name, nseg=1):
         # workloads' lambda_h) leave Q (.) Lambda to the chunk pass, so only K (.) Gamma is written
         qk_out = 0 if not gated else Tp * dk * 2 * (1 if (w.gate == 1 and dk <= 128) else 2)
         return BH * (T * dk * 2 * 2 + gate_in + qk_out + nch * C * C * 2 + gam)
+    if dk == 512 and name in ("gla_chunk_fwd", "gla_chunk_fwd_keys_hi"):
+        # two chunk passes over key halves: each reads its half of Q (.) Lambda, K (.) Gamma, gamma,
+        # S0 and writes its half of S_T; the first reads the scores and writes O as an fp32
+        # partial, the second reads that partial and writes O
+        half = BH * ((Tp * 256 * 2 * 2) + nch * 256 * 4 + T * dv * 2) + (s0 + st) // 2
+        if name == "gla_chunk_fwd":
+            return half + BH * (nch * C * C * 2 + T * dv * 4)
+        return half + BH * (T * dv * 4 + T * dv * 2)
     if name == "gla_chunk_fwd":
         last_state = (s0 + st) if nseg == 1 else BH * nseg * dk * dv * 4
         # bilinear gate: V (.) D' in place of v, plus log beta and the chunks' column decays

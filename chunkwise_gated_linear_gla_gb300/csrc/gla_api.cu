@@ -129,8 +129,10 @@ bool tensor_shape_ok(const gla_fwd_params* p)
 {
     const long long BH = (long long)p->B * p->H;
     const long long Tpad = ((long long)p->T + kChunk - 1) / kChunk * kChunk;
-    return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256) &&
-           p->dv % kDvTile == 0 && BH <= 65535 && BH * Tpad < (1LL << 31);
+    // dk = 512 runs as two chunk passes over key halves (not with the bilinear gate)
+    const bool dk_ok = p->dk == 64 || p->dk == 128 || p->dk == 256 ||
+                       (p->dk == 512 && p->gate != GLA_GATE_BILINEAR);
+    return p->dtype == GLA_BF16 && dk_ok && p->dv % kDvTile == 0 && BH <= 65535 && BH * Tpad < (1LL << 31);
 }
 
 // Number of sequence segments per (b,h). A single chunk-serial pass per
@@ -181,7 +183,8 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     const int units = p->B * p->H * pl.n_dvt;
     const bool bil = p->gate == GLA_GATE_BILINEAR;
     // the sequence split carries only a per-key decay between segments: none with the bilinear gate
-    pl.nseg = bil ? 1 : choose_segments(p, units, pl.nchunks, sms > 0 ? sms : 148);
+    const bool halves = p->dk == 512;   // two chunk passes over key halves; no sequence split
+    pl.nseg = (bil || halves) ? 1 : choose_segments(p, units, pl.nchunks, sms > 0 ? sms : 148);
     pl.chunks_per_seg = (pl.nchunks + pl.nseg - 1) / pl.nseg;
     pl.nseg = (pl.nchunks + pl.chunks_per_seg - 1) / pl.chunks_per_seg;
 
@@ -197,6 +200,9 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
         pl.off_segS = off;  off = align_up(off + BH * pl.nseg * p->dk * p->dv * 4, 256);
         pl.off_segin = off; off = align_up(off + BH * pl.nseg * p->dk * p->dv * 4, 256);
     }
+    if (halves) {
+        pl.off_opart = off; off = align_up(off + BH * p->T * p->dv * 4, 256);
+    }
     if (bil) {
         pl.off_vh = off;   off = align_up(off + BH * p->T * p->dv * 2, 256);
         pl.off_lbc = off;  off = align_up(off + BH * pl.nchunks * p->dv * 4, 256);
@@ -211,6 +217,7 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
         pl.stages[n++] = STAGE_SEG_SCAN;
     }
     pl.stages[n++] = STAGE_CHUNK_FWD;
+    if (halves) pl.stages[n++] = STAGE_CHUNK_FWD_HI;
     if (bil) pl.stages[n++] = STAGE_SIMT_FLAGGED;
     pl.nstages = n;
     return GLA_OK;
@@ -227,6 +234,7 @@ const char* stage_name(StageKind k)
     case STAGE_COPY_STATE: return "gla_copy_state";
     case STAGE_VALUE_PREP: return "gla_value_prep";
     case STAGE_SIMT_FLAGGED: return "gla_fwd_simt_flagged";
+    case STAGE_CHUNK_FWD_HI: return "gla_chunk_fwd_keys_hi";
     }
     return "?";
 }
@@ -260,8 +268,10 @@ gla_status run_stage(const gla_fwd_params* p, const Plan& pl, int i, cudaStream_
     case STAGE_SEG_STATE: e = launch_seg_state(*p, pl, p->workspace, c->status, s); break;
     case STAGE_SEG_SCAN: e = launch_seg_scan(*p, pl, p->workspace, c->status, s); break;
     case STAGE_CHUNK_FWD:
-        e = launch_chunk_fwd(*p, pl, p->workspace, pl.nseg > 1 ? kModeSegOut : kModeFull, c->status, s);
+        e = launch_chunk_fwd(*p, pl, p->workspace, pl.nseg > 1 ? kModeSegOut : kModeFull, c->status, s,
+                             p->dk == 512 ? 1 : 0);
         break;
+    case STAGE_CHUNK_FWD_HI: e = launch_chunk_fwd(*p, pl, p->workspace, kModeFull, c->status, s, 2); break;
     case STAGE_VALUE_PREP: e = launch_value_prep(*p, pl, p->workspace, s); break;
     case STAGE_SIMT_FLAGGED:
         e = launch_simt(*p, c->status, s, reinterpret_cast<const int*>(static_cast<uint8_t*>(p->workspace) + pl.off_flag));

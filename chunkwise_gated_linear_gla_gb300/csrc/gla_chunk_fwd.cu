@@ -64,7 +64,7 @@ struct FwdArgs {
     // that pass q_factored take raw q, and the drain scales output row r by lambda^(r+1).
     // (The union keeps this struct at 128 bytes, which the compiler keeps in registers; a
     // larger one went to the stack.)
-    const float* lbc;
+    union { const float* lbc; float* Opart; };   // Opart: key halves (KH), fp32 [BH][T][dv]
     union { const float* lb; const float* lamh; };
     const int* skip;    // [BH] heads left to the CUDA-core pass
     int T, H;
@@ -116,7 +116,12 @@ __device__ __forceinline__ bool group_all_ok(bool ok, int id, int n) {
 
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
-template <int DK, bool BIL, bool SCAL>
+// KH (keys wider than the tensor memory holds, dk = 2 DK): 0 = all keys; 1 = keys
+// [0, DK) of 2 DK, O written as an fp32 partial (with the intra-chunk term);
+// 2 = keys [DK, 2 DK), no intra-chunk term, the partial added before the bf16 store.
+// Each half carries its own rows of the state: the gate scales rows, so the two
+// halves' recurrences are independent and only their outputs add.
+template <int DK, bool BIL, bool SCAL, int KH>
 __global__ void __launch_bounds__(NT, 1)
 gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmA,
@@ -124,6 +129,8 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
 {
     using L = Lay<DK, BIL>;
     constexpr int HC = DK / 2;   // state columns per epilogue thread
+    constexpr int DKT = KH ? 2 * DK : DK;    // keys of the head
+    constexpr int KOFF = KH == 2 ? DK : 0;   // this CTA's first key
     if constexpr (BIL) {
         if (a.skip[blockIdx.y]) return;   // the whole CTA leaves before any setup
     }
@@ -201,22 +208,23 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     break;
                 }
                 uint8_t* sb = sm + st * L::STAGE;
-                const uint32_t bytes = L::KB + L::VB + (gated ? L::GB : 0) + (want_out ? L::QB + L::AB : 0) + L::GVB;
+                const uint32_t bytes = L::KB + L::VB + (gated ? L::GB : 0) +
+                                       (want_out ? L::QB + (KH == 2 ? 0 : L::AB) : 0) + L::GVB;
                 mbar_arrive_expect_tx(&full[st], bytes);
-                if (gated) bulk_load(sb + L::G_OFF, a.gam + ((size_t)bh * a.nchunks + c) * DK, L::GB, &full[st]);
+                if (gated) bulk_load(sb + L::G_OFF, a.gam + ((size_t)bh * a.nchunks + c) * DKT + KOFF, L::GB, &full[st]);
                 if constexpr (BIL)
                     bulk_load(sb + L::GV_OFF, a.lbc + ((size_t)bh * a.nchunks + c) * a.dv + dv0, L::GVB, &full[st]);
 #pragma unroll
                 for (int i = 0; i < DK / 64; ++i)
-                    tma_load_3d(sb + L::K_OFF + i * 8192, &tmK, &full[st], i * 64, c * C, bh);
+                    tma_load_3d(sb + L::K_OFF + i * 8192, &tmK, &full[st], KOFF + i * 64, c * C, bh);
                 tma_load_3d(sb + L::V_OFF, &tmV, &full[st], dv0, c * C, bh);
                 tma_load_3d(sb + L::V_OFF + 8192, &tmV, &full[st], dv0 + 64, c * C, bh);
                 if (want_out) {
                     const CUtensorMap* mq = q_fac(c) ? &tmQr : &tmQ;
 #pragma unroll
                     for (int i = 0; i < DK / 64; ++i)
-                        tma_load_3d(sb + L::Q_OFF + i * 8192, mq, &full[st], i * 64, c * C, bh);
-                    tma_load_2d(sb + L::A_OFF, &tmA, &full[st], 0, (bh * a.nchunks + c) * C);
+                        tma_load_3d(sb + L::Q_OFF + i * 8192, mq, &full[st], KOFF + i * 64, c * C, bh);
+                    if (KH != 2) tma_load_2d(sb + L::A_OFF, &tmA, &full[st], 0, (bh * a.nchunks + c) * C);
                 }
                 // L2 prefetch two chunks ahead, beyond what the two shared-memory stages
                 // hold; the tiles all dv-tile CTAs of this head share are split among them
@@ -228,16 +236,17 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     int item = 0;
 #pragma unroll
                     for (int i = 0; i < DK / 64; ++i, ++item)
-                        if (item % nt == me) prefetch_l2_tile_3d(&tmK, i * 64, cp * C, bh);
+                        if (item % nt == me) prefetch_l2_tile_3d(&tmK, KOFF + i * 64, cp * C, bh);
                     if (want_out) {
                         const CUtensorMap* mq = q_fac(cp) ? &tmQr : &tmQ;
 #pragma unroll
                         for (int i = 0; i < DK / 64; ++i, ++item)
-                            if (item % nt == me) prefetch_l2_tile_3d(mq, i * 64, cp * C, bh);
-                        if (item % nt == me) prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
+                            if (item % nt == me) prefetch_l2_tile_3d(mq, KOFF + i * 64, cp * C, bh);
+                        if (KH != 2 && item % nt == me) prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
                         ++item;
                     }
-                    if (gated && item % nt == me) prefetch_l2(a.gam + ((size_t)bh * a.nchunks + cp) * DK, L::GB);
+                    if (gated && item % nt == me)
+                        prefetch_l2(a.gam + ((size_t)bh * a.nchunks + cp) * DKT + KOFF, L::GB);
                 }
                 issued = n + 1;
             }
@@ -283,11 +292,13 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                         mma_ts(tO, tSb + kk * 8, sdesc(sQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128),
                                id_inter, kk > 0);
                     mma_commit(sb_free);
-                    // intra: O^T += V^T (P (.) M)^T
+                    // intra: O^T += V^T (P (.) M)^T (the second key half leaves it to the first)
+                    if (KH != 2) {
 #pragma unroll
-                    for (int kk = 0; kk < C / 16; ++kk)
-                        mma_ss(tO, sdesc(sV + kk * 2048, 8192, 1024, kSwizzle128),
-                               sdesc(sA + kk * 32, 16, 1024, kSwizzle128), id_intra, 1);
+                        for (int kk = 0; kk < C / 16; ++kk)
+                            mma_ss(tO, sdesc(sV + kk * 2048, 8192, 1024, kSwizzle128),
+                                   sdesc(sA + kk * 32, 16, 1024, kSwizzle128), id_intra, 1);
+                    }
                     mma_commit(&o_full[n & 1]);
                 }
                 mma_commit(&empty[st]);
@@ -324,6 +335,13 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(a.lb + ((size_t)bh * a.T + prow) * a.dv + dv0 +
                                                                  (gt & 3) * 32));
             }
+            const int orow = (c_begin + m) * C + grp * 32;   // this thread's first row of chunk m
+            if constexpr (KH == 2) {
+                // the first key half's fp32 partial of this thread's 32 rows (rows past T: none)
+                const float* pp = a.Opart + ((size_t)bh * a.T + orow) * a.dv + dv0 + d;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) w[t] = orow + t < a.T ? pp[(size_t)t * a.dv] : 0.f;
+            }
             const bool ok = mbar_wait(&o_full[b], (m >> 1) & 1, kTimeoutNs);
             if (!group_all_ok(ok, BAR_EPI, NEPI)) return false;
             tc_fence_after();
@@ -334,8 +352,8 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             mbar_arrive(&o_empty[b]);
             if constexpr (BIL) {
                 // exp(B'_r - B'_C): rows 0-31 from the prefix sum, rows 32-63 from the suffix sum.
-                // Exponents are within [-kVGuard, kVGuard], so __expf's error (its argument scaled
-                // by log2 e in fp32, then ex2.approx) stays below 1e-5 relative.
+                // Exponents are within [-kVGuard, kVGuard]; the fast exponential's error there is
+                // far below the bf16 rounding of O (the parity tests hold the bf16 tolerance).
                 if (grp == 0) {
                     float acc = -lbc_m;
 #pragma unroll
@@ -359,6 +377,18 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
 #pragma unroll
                 for (int t = 0; t < 32; ++t)
                     r[t] = __float_as_uint(__uint_as_float(r[t]) * __expf((float)(grp * 32 + t + 1) * lam_h));
+            }
+            if constexpr (KH == 2) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) + w[t]);
+            }
+            if constexpr (KH == 1) {
+                // the partial goes out in fp32, one coalesced 128-byte row segment per warp and row
+                float* pp = a.Opart + ((size_t)bh * a.T + orow) * a.dv + dv0 + d;
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    if (orow + t < a.T) pp[(size_t)t * a.dv] = __uint_as_float(r[t]);
+                return true;
             }
             // the store issued from this half-buffer two chunks ago must have read it
             if (gt == 0) bulk_wait_read1();
@@ -494,20 +524,21 @@ bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, swz);
 }
 
-template <int DK, bool BIL, bool SCAL>
+template <int DK, bool BIL, bool SCAL, int KH = 0>
 cudaError_t launch_dk(const FwdArgs& a, dim3 grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                       const CUtensorMap& A, const CUtensorMap& o, const CUtensorMap& qr, cudaStream_t s) {
     using L = Lay<DK, BIL>;
-    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK, BIL, SCAL>,
+    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK, BIL, SCAL, KH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    gla_chunk_fwd_kernel<DK, BIL, SCAL><<<grid, NT, L::SMEM, s>>>(a, q, k, v, A, o, qr);
+    gla_chunk_fwd_kernel<DK, BIL, SCAL, KH><<<grid, NT, L::SMEM, s>>>(a, q, k, v, A, o, qr);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode, int* status, cudaStream_t s)
+cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode, int* status, cudaStream_t s,
+                             int kh)
 {
     uint8_t* base = static_cast<uint8_t*>(ws);
     const uint64_t BH = (uint64_t)p.B * p.H;
@@ -561,6 +592,17 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     a.T = p.T;
     a.H = p.H;
     dim3 grid(pl.n_dvt, (unsigned)BH, mode == kModeFull ? 1 : pl.nseg);
+    if (kh) {
+        // dk = 512 in two key halves of 256: each half its own rows of S0 / S_T, the first
+        // half's O an fp32 partial in the workspace that the second half adds
+        if (mode != kModeFull || bil || qfac || p.dk != 512) return cudaErrorInvalidValue;
+        const size_t koff = kh == 2 ? 256 : 0;
+        a.S_in = p.S0 ? p.S0 + koff * p.dv : nullptr;
+        a.S_out = p.ST ? p.ST + koff * p.dv : nullptr;
+        a.Opart = reinterpret_cast<float*>(base + pl.off_opart);
+        return kh == 1 ? launch_dk<256, false, false, 1>(a, grid, mq, mk, mv, ma, mo, mqr, s)
+                       : launch_dk<256, false, false, 2>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+    }
     if (bil) {
         if (mode != kModeFull) return cudaErrorInvalidValue;   // no sequence split with the bilinear gate
         switch (p.dk) {

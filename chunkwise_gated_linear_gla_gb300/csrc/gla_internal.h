@@ -44,6 +44,7 @@ enum StageKind {
     STAGE_COPY_STATE = 5,  // T == 0: ST <- S0 (or 0)
     STAGE_VALUE_PREP = 6,  // bilinear gate: V (.) D', the chunks' column decays, range flags
     STAGE_SIMT_FLAGGED = 7,  // bilinear gate: the CUDA-core pass for the heads flagged out of range
+    STAGE_CHUNK_FWD_HI = 8,  // dk = 512: the chunk pass over keys 256-511, adding the first half's partial O
 };
 
 struct Plan {
@@ -58,9 +59,10 @@ struct Plan {
     // workspace layout (byte offsets from the workspace base)
     size_t off_qt = 0, off_kt = 0, off_A = 0, off_gam = 0, off_segS = 0, off_segin = 0;
     size_t off_vh = 0, off_lbc = 0, off_flag = 0;   // bilinear gate only
+    size_t off_opart = 0;  // dk = 512: the first key half's O, fp32 [BH][T][dv]
     size_t ws_bytes = 0;
     int nstages = 0;
-    StageKind stages[6];
+    StageKind stages[8];
 };
 
 // Argument checks of the C ABI (gla_api.cu). validate_args: sizes, modes and
@@ -80,8 +82,10 @@ int* device_status_ptr();   // nullptr on failure
 cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s, const int* only = nullptr);
 cudaError_t launch_value_prep(const gla_fwd_params& p, const Plan& pl, void* ws, cudaStream_t s);
 cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
+// kh: 0, or for dk = 512 the key half (1: keys 0-255 with the intra term, O as an fp32
+// partial; 2: keys 256-511, adding that partial)
 cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode,
-                             int* status, cudaStream_t s);
+                             int* status, cudaStream_t s, int kh = 0);
 cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, int* status,
                             cudaStream_t s);

@@ -256,7 +256,7 @@ __device__ __forceinline__ bool score_readout(uint32_t tmem, uint64_t* bar, uint
 // Resident CTAs per SM: the kernel is latency-bound, so smaller heads run three
 // CTAs per SM (shared memory allows it; registers are bounded to fit).
 template <int DK>
-constexpr int prep_ctas_per_sm() { return DK <= 128 ? 3 : 2; }
+constexpr int prep_ctas_per_sm() { return DK <= 128 ? 3 : DK <= 256 ? 2 : 1; }
 
 template <int DK>
 __global__ void __launch_bounds__(NT, prep_ctas_per_sm<DK>())
@@ -586,7 +586,7 @@ gla_chunk_prep_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const
 template <int DK>
 constexpr int prep_uniform_bufs() { return 1; }
 template <int DK, int NTU>
-constexpr int prep_uniform_ctas_per_sm() { return DK > 128 ? 3 : (NTU == 128 ? 6 : 4); }
+constexpr int prep_uniform_ctas_per_sm() { return DK > 256 ? 1 : DK > 128 ? 3 : (NTU == 128 ? 6 : 4); }
 template <int DK>
 constexpr int prep_uniform_smem() { return prep_uniform_bufs<DK>() * 2 * C * DK * 2 + 64 + C * 4 + 1024; }
 
@@ -857,6 +857,7 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
         case 64: return launch_prep_uniform_dk<64>(a, mq, mk, mA, sms, s);
         case 128: return launch_prep_uniform_dk<128>(a, mq, mk, mA, sms, s);
         case 256: return launch_prep_uniform_dk<256>(a, mq, mk, mA, sms, s);
+        case 512: return launch_prep_uniform_dk<512>(a, mq, mk, mA, sms, s);
         }
         return cudaErrorInvalidValue;
     }
@@ -864,6 +865,7 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     case 64: return launch_prep_dk<64>(a, mq, mk, mA, sms, s);
     case 128: return launch_prep_dk<128>(a, mq, mk, mA, sms, s);
     case 256: return launch_prep_dk<256>(a, mq, mk, mA, sms, s);
+    case 512: return launch_prep_dk<512>(a, mq, mk, mA, sms, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -94,7 +94,7 @@ BAD = [
      dict(gate=4, log_b=0x900000, dtype=bnd.GLA_FP32, dv=128, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("chunk 32", dict(chunk=32), bnd.GLA_ERR_UNSUPPORTED),
     ("dk 784", dict(dk=784), bnd.GLA_ERR_UNSUPPORTED),
-    ("tensor path with dk 512", dict(dk=512, path=bnd.GLA_PATH_TENSOR, q=0x1000000, k=0x9000000, v=0x11000000,
+    ("tensor path with dk 384", dict(dk=384, path=bnd.GLA_PATH_TENSOR, q=0x1000000, k=0x9000000, v=0x11000000,
                                      log_g=0x21000000, O=0x31000000), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with dv 48", dict(dv=48, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
@@ -141,11 +141,22 @@ def test_plan_on_host():
     # empty sequence: only the state copy
     p = _params(T=0, q=None, k=None, v=None, O=None)
     assert bnd.gla_fwd_stage_name(p, 0) == "gla_copy_state"
-    # keys wider than 256 (up to 768) take the CUDA-core path in bf16 too
-    for dk in (272, 512, 768):
+    # keys wider than 256 (up to 768) take the CUDA-core path in bf16 too, except dk = 512
+    for dk in (272, 384, 768):
         p = _params(dk=dk, dv=1024, q=0x1000000, k=0x9000000, v=0x11000000, log_g=0x21000000, O=0x31000000)
         assert bnd.gla_fwd_num_stages(p) == 1 and bnd.gla_fwd_stage_name(p, 0) == "gla_fwd_simt"
         assert bnd.gla_fwd_workspace_size(p) == 0
+    # dk = 512: the tensor path in two key halves, never split along the sequence; the
+    # workspace holds the first half's fp32 output
+    p = _params(dk=512, dv=1024, T=2048, B=8, H=2, q=0x100000000, k=0x200000000, v=0x300000000,
+                log_g=0x400000000, O=0x500000000, force_segments=0)
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_prep", "gla_chunk_fwd", "gla_chunk_fwd_keys_hi"]
+    assert bnd.gla_fwd_workspace_size(p) >= 8 * 2 * 2048 * 1024 * 4
+    p.force_segments = 4
+    assert [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))] == names
+    p.gate, p.log_b = bnd.GLA_GATE_BILINEAR, 0x600000000
+    assert [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))] == ["gla_fwd_simt"]
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

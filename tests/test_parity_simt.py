@@ -109,8 +109,8 @@ def test_widest_keys(dk, T):
 
 def test_wide_heads_workload_sampled():
     """The wide-head workload (B=8, H=2, T=2048, dk=512, dv=1024, bf16, per-key gate) at
-    its full size, in the launch configuration the bench times, checked on two
-    sampled heads the oracle computes alone."""
+    its full size, in the launch configuration the bench times (the tensor path in two
+    key halves), checked on two sampled heads the oracle computes alone."""
     w = gi.WORKLOADS["gla_wide_heads"]
     x = gi.make_inputs(w, seed=0)
     d = lambda t: None if t is None else t.cuda()
@@ -124,7 +124,8 @@ def test_wide_heads_workload_sampled():
 
 
 def test_wide_keys_rejected_on_tensor_path_and_beyond_768():
-    w = gi.Workload("t", B=1, H=1, T=8, dk=512, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY)
+    """dk = 384 has no tensor path (dk = 512 does, in key halves); dk = 784 none at all."""
+    w = gi.Workload("t", B=1, H=1, T=8, dk=384, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY)
     x = gi.make_inputs(w, seed=0)
     d = lambda t: None if t is None else t.cuda()
     with pytest.raises(RuntimeError, match="UNSUPPORTED"):

@@ -358,3 +358,44 @@ def test_steep_scalar_decay():
     Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
     assert_close(to_np(O), Oref, torch.bfloat16, "O")
     assert_close(to_np(ST), STref, torch.bfloat16, "ST")
+
+
+# ---------------------------------------------------------------- dk = 512 in two key halves
+
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR])
+@pytest.mark.parametrize("T", [1, 65, 200])
+def test_dk512_key_halves(gate, T):
+    """dk = 512 on the tensor path: two chunk passes, each over 256 keys with its own rows of
+    the state, the second adding the first's fp32 partial output; every gate mode but the
+    bilinear one, ragged T, S0 given."""
+    w = gi.Workload("t", B=1, H=2, T=T, dk=512, dv=256, dtype=torch.bfloat16, gate=gate, s0_std=0.02)
+    x = gi.make_inputs(w, seed=50 + T + gate)
+    c = _dev(x)
+    O = torch.empty(x["v"].shape, dtype=torch.bfloat16, device="cuda")
+    ST = torch.empty(1, 2, 512, 256, device="cuda")
+    p = bnd.make_params(c["q"], c["k"], c["v"], c["log_g"], c["S0"], O, ST, gate=x["gate"],
+                        path=bnd.GLA_PATH_TENSOR)
+    assert [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))][-2:] == \
+        ["gla_chunk_fwd", "gla_chunk_fwd_keys_hi"]
+    O, ST = gla.forward(c["q"], c["k"], c["v"], c["log_g"], c["S0"], gate=x["gate"], path=gla.GLA_PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
+    assert_close(to_np(O), Oref, torch.bfloat16, "O")
+    assert_close(to_np(ST), STref, torch.bfloat16, "ST")
+
+
+def test_dk512_steep_gate_and_in_place_state():
+    """dk = 512 with log alpha = -U(0,4) (the prep's sub-chunk form at 512 keys) and ST == S0
+    (each key half updates its own rows of the state in place)."""
+    w = gi.Workload("t", B=1, H=2, T=150, dk=512, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY,
+                    gate_dist="steep", s0_std=0.3)
+    x = gi.make_inputs(w, seed=58)
+    c = _dev(x)
+    S = c["S0"].clone()
+    O, ST = gla.forward(c["q"], c["k"], c["v"], c["log_g"], S, path=gla.GLA_PATH_TENSOR, ST=S)
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
+    assert_close(to_np(O), Oref, torch.bfloat16, "O")
+    assert_close(to_np(S), STref, torch.bfloat16, "ST (in place)")
