@@ -414,6 +414,98 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
     lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// ---- forward sweep on the tensor cores (bf16 inputs, dk in {64, 128, 256})
+// The same recurrence as gla_bwd_states_kernel, S <- Diag(gamma) S + (K (.) Gamma)^T V per
+// 16-row chunk, with the state held in the warps' fp32 mma.sync accumulators: warp w owns
+// the 16 x 8 tiles w * TPW .. w * TPW + TPW - 1 (key tile m = id / 8, column tile n = id % 8).
+// K (.) Gamma is split into hi + lo bf16 parts and v is bf16, so each product keeps about
+// 16 mantissa bits, as in the reverse sweep. Each chunk's state goes to the workspace from
+// the accumulators: 8-byte pairs, every 32-byte sector written whole.
+template <int DK>
+struct StLay {
+    static constexpr int RS = DVT + BP;                  // bf16 row of a [CS][64] tile
+    static constexpr int RK = DK + BP;                   // bf16 row of a [CS][DK] tile
+    static constexpr int VVB = 0;                        // bf16 [CS][RS] v, this tile's columns
+    static constexpr int KGH = VVB + CS * RS * 2;        // bf16 [CS][RK] k (.) Gamma, hi
+    static constexpr int KGL = KGH + CS * RK * 2;        //   and lo
+    static constexpr int GAM = KGL + CS * RK * 2;        // fp32 [DK] chunk decay
+    static constexpr int BYTES = GAM + DK * 4;
+    static constexpr int TPW = DK / 16;                  // accumulator tiles per warp
+    static_assert(KGH % 16 == 0 && KGL % 16 == 0 && GAM % 16 == 0, "ldmatrix rows 16-byte aligned");
+};
+
+template <int DK>
+__global__ void __launch_bounds__(NT, 2) gla_bwd_states_tc_kernel(BwdArgs a)
+{
+    using L = StLay<DK>;
+    extern __shared__ __align__(16) uint8_t sst[];
+    __nv_bfloat16* vvb = reinterpret_cast<__nv_bfloat16*>(sst + L::VVB);
+    __nv_bfloat16* kgh = reinterpret_cast<__nv_bfloat16*>(sst + L::KGH);
+    __nv_bfloat16* kgl = reinterpret_cast<__nv_bfloat16*>(sst + L::KGL);
+    float* gam = reinterpret_cast<float*>(sst + L::GAM);
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, g = lane / 4, tq = lane % 4;
+    const int bh = blockIdx.x, j0 = blockIdx.y * DVT, jn = min(DVT, a.dv - j0);
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k) + (size_t)bh * a.T * DK;
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v) + (size_t)bh * a.T * a.dv;
+
+    float Sacc[L::TPW][4];
+#pragma unroll
+    for (int u = 0; u < L::TPW; ++u) {
+        const int id = warp * L::TPW + u, m = id / 8, n = id % 8;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int key = 16 * m + g + 8 * (e / 2), j = 8 * n + 2 * tq + (e % 2);
+            Sacc[u][e] = (a.S0 && j < jn) ? a.S0[((size_t)bh * DK + key) * a.dv + j0 + j] : 0.f;
+        }
+    }
+    const int brow = (lane % 8) + 8 * ((lane / 8) % 2);
+    const int mi = lane / 8, arow = (lane % 8) + 8 * (mi / 2), acol = 8 * (mi % 2);
+    for (int c = 0; c < a.nch; ++c) {
+        const int t0 = c * CS, nr = min(CS, a.T - t0);
+        __syncthreads();   // the previous chunk's products are done with the tiles
+        if (c + 1 < a.nch) pf_chunk_inputs(a, bh, c + 1, j0, jn, 2, false, false, tid);
+        for (int i = tid; i < CS * DVT; i += NT) {
+            const int r = i / DVT, j = i % DVT;
+            vvb[r * L::RS + j] = (r < nr && j < jn) ? v[(size_t)(t0 + r) * a.dv + j0 + j] : __float2bfloat16_rn(0.f);
+        }
+        for (int x = tid; x < DK; x += NT) {
+            float lg[CS], kv[CS], bcr[CS], run = 0.f;
+#pragma unroll
+            for (int r = 0; r < CS; ++r) {   // every load first, then the arithmetic
+                lg[r] = r < nr ? log_alpha(a, bh, t0 + r, x) : 0.f;
+                kv[r] = r < nr ? __bfloat162float(k[(size_t)(t0 + r) * DK + x]) : 0.f;
+            }
+#pragma unroll
+            for (int r = 0; r < CS; ++r) {
+                run += lg[r];
+                bcr[r] = run;
+            }
+            gam[x] = expf(run);
+#pragma unroll
+            for (int r = 0; r < CS; ++r) split_bf16(kv[r] * expf(run - bcr[r]), kgh[r * L::RK + x], kgl[r * L::RK + x]);
+        }
+        __syncthreads();
+        float* out = a.Sst + ((size_t)bh * a.nch + c) * DK * a.dv + j0;
+#pragma unroll
+        for (int u = 0; u < L::TPW; ++u) {
+            const int id = warp * L::TPW + u, m = id / 8, n = id % 8;
+            uint32_t a0, a1, a2, a3, b0, b1;
+            ldsm_x2_t(vvb + brow * L::RS + 8 * n, b0, b1);
+            const float g0 = gam[16 * m + g], g1 = gam[16 * m + g + 8];
+            Sacc[u][0] *= g0; Sacc[u][1] *= g0; Sacc[u][2] *= g1; Sacc[u][3] *= g1;
+            ldsm_x4_t(kgh + arow * L::RK + 16 * m + acol, a0, a1, a2, a3);
+            mma16816(Sacc[u], a0, a1, a2, a3, b0, b1);
+            ldsm_x4_t(kgl + arow * L::RK + 16 * m + acol, a0, a1, a2, a3);
+            mma16816(Sacc[u], a0, a1, a2, a3, b0, b1);
+            const int key = 16 * m + g, j = 8 * n + 2 * tq;   // j even, jn a multiple of 16
+            if (j < jn) {
+                *reinterpret_cast<float2*>(out + (size_t)key * a.dv + j) = make_float2(Sacc[u][0], Sacc[u][1]);
+                *reinterpret_cast<float2*>(out + (size_t)(key + 8) * a.dv + j) = make_float2(Sacc[u][2], Sacc[u][3]);
+            }
+        }
+    }
+}
+
 // ---- intra kernel: grid (BH, nch), one thread per key; the pair walk over the full dv width
 __global__ void __launch_bounds__(NT) gla_bwd_intra_kernel(BwdArgs a, float* Ag)
 {
@@ -950,12 +1042,29 @@ cudaError_t launch_chunks_tc(const BwdArgs& a, int BH, cudaStream_t s)
     return cudaGetLastError();
 }
 
+template <int DK>
+cudaError_t launch_states_tc(const BwdArgs& a, int BH, cudaStream_t s)
+{
+    const int smem = StLay<DK>::BYTES;
+    cudaError_t e = cudaFuncSetAttribute(gla_bwd_states_tc_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    gla_bwd_states_tc_kernel<DK><<<dim3(BH, a.ndvt), NT, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename Tin>
 cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s, bool use_tc)
 {
     cudaError_t e;
     const int BH = p.B * p.H;
-    if (a.nch > 0) {
+    if (a.nch > 0 && use_tc) {
+        switch (p.dk) {
+        case 64: e = launch_states_tc<64>(a, BH, s); break;
+        case 128: e = launch_states_tc<128>(a, BH, s); break;
+        default: e = launch_states_tc<256>(a, BH, s); break;
+        }
+        if (e != cudaSuccess) return e;
+    } else if (a.nch > 0) {
         const size_t sm1 = states_smem(p.dk);
         if ((e = cudaFuncSetAttribute(gla_bwd_states_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)sm1)) != cudaSuccess)

@@ -399,3 +399,33 @@ def test_dk512_steep_gate_and_in_place_state():
     Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
     assert_close(to_np(O), Oref, torch.bfloat16, "O")
     assert_close(to_np(S), STref, torch.bfloat16, "ST (in place)")
+
+
+# ---------------------------------------------------------------- maximum sizes
+
+def test_max_heads_grid_limit():
+    """B*H = 65535, the most heads the tensor path takes (the chunk pass gives every head
+    its own grid row): every output element written, sampled heads against the oracle."""
+    w = gi.Workload("t", B=65535, H=1, T=3, dk=64, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY)
+    x = gi.make_inputs(w, seed=61)
+    c = _dev(x)
+    O = torch.full(x["v"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    gla.forward(c["q"], c["k"], c["v"], c["log_g"], None, path=gla.GLA_PATH_TENSOR, want_state=False, O=O)
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    assert not torch.isnan(O).any()
+    heads = [(0, 0), (32767, 0), (65534, 0)]
+    ref = oracle.gla_forward_rows(x["q"], x["k"], x["v"], x["log_g"], x["gate"], None, heads)
+    for (b, h), (Oref, _) in ref.items():
+        assert_close(to_np(O[b, h]), Oref, torch.bfloat16, f"O[{b},{h}]")
+
+
+def test_long_sequence_many_chunks():
+    """One head of T = 2^18 + 37 rows (4097 chunks with a ragged tail; the planner splits the
+    sequence), per-key gate and S0, against the oracle over the whole sequence."""
+    w = gi.Workload("t", B=1, H=1, T=(1 << 18) + 37, dk=64, dv=128, dtype=torch.bfloat16,
+                    gate=gi.GATE_PER_KEY, s0_std=0.1)
+    x, O, ST = _run(w, seed=62, path=gla.GLA_PATH_TENSOR)
+    Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
+    assert_close(to_np(O), Oref, torch.bfloat16, "O")
+    assert_close(to_np(ST), STref, torch.bfloat16, "ST")
