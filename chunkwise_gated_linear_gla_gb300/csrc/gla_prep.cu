@@ -318,12 +318,11 @@ gla_chunk_prep_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const
             tma_load_3d(Qs + i * C * 64, &tmq, cbar, i * 64, t0, bh);
             tma_load_3d(Ks + i * C * 64, &tmk, cbar, i * 64, t0, bh);
         }
+        // the next item's log gates (read by plain loads) into L2; its q and k tiles come by TMA
         const int nx = item + gridDim.x;
         if (nx < total) {
             const int c2 = nx % a.nchunks, bh2 = nx / a.nchunks, nr2 = min(C, a.T - c2 * C);
             const size_t row = (size_t)bh2 * a.T + (size_t)c2 * C;
-            prefetch_l2(a.q + row * DK, (uint32_t)nr2 * DK * 2);
-            prefetch_l2(a.k + row * DK, (uint32_t)nr2 * DK * 2);
             prefetch_l2(a.log_g + row * DK, (uint32_t)nr2 * DK * 4);
         }
     }
