@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(NT) gla_bwd_chunks_kernel(BwdArgs a)
 //    bits: the bf16 path is as accurate as the fp32 one. D is carried in fp32 accumulator
 //    registers from chunk to chunk.
 constexpr int BP = 8;              // bf16 row padding: rows 16 bytes apart in the banks
+constexpr int VDC = 256;           // dv columns per staged slice in the intra kernel's v . dO products
 
 __device__ __forceinline__ void ldsm_x4(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -516,6 +517,8 @@ __global__ void __launch_bounds__(NT) gla_bwd_intra_kernel(BwdArgs a, float* Ag)
     float* bc = kr + CS * dk;        // [CS][dk]
     float* VD = bc + CS * dk;        // [CS][CS] v_s . do_t over all dv columns
     float* Aw = VD + CS * CS;        // [NT / 32][CS][CS]
+    __nv_bfloat16* dsl = reinterpret_cast<__nv_bfloat16*>(Aw + (NT / 32) * CS * CS);   // [CS][VDC] dO slice
+    __nv_bfloat16* vsl = dsl + CS * VDC;                                                 // [CS][VDC] v slice
     const int bh = blockIdx.x, c = blockIdx.y, BH = gridDim.x;
     const int t0 = c * CS, nr = min(CS, a.T - t0);
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + (size_t)bh * a.T * dk;
@@ -538,19 +541,70 @@ __global__ void __launch_bounds__(NT) gla_bwd_intra_kernel(BwdArgs a, float* Ag)
             bc[r * dk + kk] = run;
         }
     }
-    // v_s . do_t for t >= s: 2 threads per pair (halves of dv), rows past nr are zero;
-    // every thread runs the same CS * CS / (NT / 2) iterations, so the shuffle is uniform
-    static_assert((CS * CS) % (NT / 2) == 0, "pairs split evenly over the threads");
-    for (int p = tid / 2; p < CS * CS; p += NT / 2) {
-        const int half = tid % 2, t = p / CS, s = p % CS;
-        float acc = 0.f;
-        if (s <= t && t < nr) {
-            const int jb = half * (a.dv / 2), je = jb + a.dv / 2;
-            for (int j = jb; j < je; ++j)
-                acc = fmaf(__bfloat162float(dO[(size_t)t * a.dv + j]), __bfloat162float(v[(size_t)s * a.dv + j]), acc);
+    // v_s . do_t for t >= s over every dv column (rows past nr are zero): VDC columns at a
+    // time, the chunk's dO and v rows staged in shared memory by 16-byte loads; one warp per
+    // pair, its lanes splitting the columns, partial sums in registers until the end
+    constexpr int NPW = (CS * (CS + 1) / 2 + NT / 32 - 1) / (NT / 32);   // pairs per warp
+    float vdp[NPW];
+#pragma unroll
+    for (int i = 0; i < NPW; ++i) vdp[i] = 0.f;
+    // 16-byte loads need 16-byte aligned bases (rows are, dv being a multiple of 16)
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.dO)) & 15) == 0;
+    for (int j0 = 0; j0 < a.dv; j0 += VDC) {
+        __syncthreads();   // the previous slice has been read
+        for (int i = tid; i < CS * VDC / 8; i += NT) {
+            const int r = i / (VDC / 8), j = (i % (VDC / 8)) * 8;
+            uint4 d8 = make_uint4(0u, 0u, 0u, 0u), v8 = d8;
+            if (r < nr && j0 + j < a.dv) {
+                const size_t off = (size_t)r * a.dv + j0 + j;
+                if (vec) {
+                    d8 = *reinterpret_cast<const uint4*>(dO + off);
+                    v8 = *reinterpret_cast<const uint4*>(v + off);
+                } else {
+                    __nv_bfloat16* dp = reinterpret_cast<__nv_bfloat16*>(&d8);
+                    __nv_bfloat16* vp = reinterpret_cast<__nv_bfloat16*>(&v8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        dp[e] = dO[off + e];
+                        vp[e] = v[off + e];
+                    }
+                }
+            }
+            *reinterpret_cast<uint4*>(dsl + r * VDC + j) = d8;
+            *reinterpret_cast<uint4*>(vsl + r * VDC + j) = v8;
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        if (half == 0) VD[p] = acc;
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NPW; ++i) {
+            const int p = warp + i * (NT / 32);
+            if (p < CS * (CS + 1) / 2) {
+                int t = 0;
+                while ((t + 1) * (t + 2) / 2 <= p) ++t;
+                const int s2 = p - t * (t + 1) / 2;
+                const __nv_bfloat162* dr = reinterpret_cast<const __nv_bfloat162*>(dsl + t * VDC);
+                const __nv_bfloat162* vr = reinterpret_cast<const __nv_bfloat162*>(vsl + s2 * VDC);
+                float acc = vdp[i];
+#pragma unroll
+                for (int j = lane; j < VDC / 2; j += 32) {
+                    const float2 x = __bfloat1622float2(dr[j]), y = __bfloat1622float2(vr[j]);
+                    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+                }
+                vdp[i] = acc;
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NPW; ++i) {
+        float acc = vdp[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        const int p = warp + i * (NT / 32);
+        if (lane == 0 && p < CS * (CS + 1) / 2) {
+            int t = 0;
+            while ((t + 1) * (t + 2) / 2 <= p) ++t;
+            const int s2 = p - t * (t + 1) / 2;
+            VD[t * CS + s2] = acc;
+        }
     }
     __syncthreads();
     float dqi[CS], dki[CS];
@@ -594,7 +648,9 @@ __global__ void __launch_bounds__(NT) gla_bwd_intra_kernel(BwdArgs a, float* Ag)
     }
 }
 
-size_t intra_smem(int dk) { return sizeof(float) * (3 * (size_t)CS * dk + CS * CS + (NT / 32) * CS * CS); }
+size_t intra_smem(int dk) {
+    return sizeof(float) * (3 * (size_t)CS * dk + CS * CS + (NT / 32) * CS * CS) + 2 * (size_t)CS * VDC * 2;
+}
 
 template <int DK>
 struct TcLay {

@@ -179,6 +179,33 @@ def test_bwd_bitwise_reproducible():
 
 
 @pytest.mark.gpu
+def test_bwd_unaligned_inputs_match_aligned():
+    """v and dO at bases 2 bytes past a 16-byte boundary (the backward asks only for element
+    alignment): the intra kernel stages them element by element instead of in 16-byte
+    pieces, and every gradient is bitwise the same as from aligned copies."""
+    gbuild.build()
+    w = gi.Workload("t", B=1, H=2, T=100, dk=128, dv=320, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY,
+                    s0_std=0.1)
+    x, dO, dST = _inputs(w, 12)
+    ref = _gpu(x, dO, dST)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device="cuda")
+        u = buf[1:1 + t.numel()].view(t.shape)
+        u.copy_(t.cuda())
+        assert u.data_ptr() % 16 == 2
+        return u
+    c = lambda t: None if t is None else t.cuda()
+    out = gla.backward(c(x["q"]), c(x["k"]), shifted(x["v"]), c(x["log_g"]), c(x["S0"]), shifted(dO), c(dST),
+                       gate=x["gate"])
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    for u, v in zip(ref, out):
+        if u is not None:
+            np.testing.assert_array_equal(u, to_np(v))
+
+
+@pytest.mark.gpu
 def test_bwd_full_gla_layer_sampled_heads():
     """The 1.3B-shaped layer (B=8 H=4 T=2048 dk=256 dv=512) in one launch; two heads held to the oracle."""
     gbuild.build(); oracle.build()
