@@ -155,6 +155,7 @@ def planned_segments(w, force, sms):
 
 def kernel_source_sha(name):
     files = {"gla_chunk_fwd": ["gla_chunk_fwd.cu", "sm100.cuh"],
+             "gla_chunk_fwd_keys_hi": ["gla_chunk_fwd.cu", "sm100.cuh"],
              "gla_chunk_prep": ["gla_prep.cu", "sm100.cuh"],
              "gla_chunk_state": ["gla_state.cu", "sm100.cuh"],
              "gla_value_prep": ["gla_vprep.cu"]}.get(name, [])
