@@ -80,10 +80,11 @@ typedef enum {
 } gla_gate;
 
 /* Which kernels run. AUTO picks the tcgen05 tensor-core path for bf16 inputs
- * with dk in {64,128,256} and dv a multiple of 128, and the fp32 CUDA-core
- * path otherwise (always for fp32 inputs). Both compute the same function.
- * The forward pass takes any dk and dv that are multiples of 16 with
- * dk <= 768; keys wider than 256 run on the CUDA-core path. */
+ * with dk in {64,128,256} and dv a multiple of 128 (also dk = 512, as two
+ * chunk passes over key halves, for every gate but the bilinear one), and the
+ * fp32 CUDA-core path otherwise (always for fp32 inputs). Both compute the
+ * same function. The forward pass takes any dk and dv that are multiples of
+ * 16 with dk <= 768. */
 typedef enum { GLA_PATH_AUTO = 0, GLA_PATH_TENSOR = 1, GLA_PATH_SIMT = 2 } gla_path;
 
 typedef struct {
