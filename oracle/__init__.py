@@ -54,7 +54,7 @@ def _load():
             lib.gla_oracle_bwd.restype = ctypes.c_int
             lib.gla_oracle_bwd.argtypes = [d, d, d, d, ctypes.c_int, d, d, d, d, d, d, d, d,
                                            ctypes.c_long, ctypes.c_long, ctypes.c_long,
-                                           ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_int]
+                                           ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_int, d, d]
             _lib = lib
     return _lib
 
@@ -111,10 +111,11 @@ def gla_forward(q, k, v, log_g=None, gate=None, S0=None, want_state=True,
     return O, ST
 
 
-def gla_backward(q, k, v, log_g, gate, S0, dO, dST=None, want_dS0=True, nthreads=None, mutant=0):
+def gla_backward(q, k, v, log_g, gate, S0, dO, dST=None, want_dS0=True, nthreads=None, mutant=0, log_b=None):
     """Gradients of L = <dO, O> + <dST, S_T> through the recurrence (the adjoint
     recurrence, fp64). Returns (dq, dk, dv, dlog_g, dS0) as numpy arrays;
-    dlog_g is shaped like log_g (None without a gate), dS0 None unless wanted."""
+    dlog_g is shaped like log_g (None without a gate), dS0 None unless wanted.
+    The bilinear gate (gate = GATE_BILINEAR, log_b [B,H,T,dv]) appends dlog_b."""
     qa, ka, va = _f64(q), _f64(k), _f64(v)
     B, H, T, dk = qa.shape
     dv = va.shape[-1]
@@ -125,14 +126,19 @@ def gla_backward(q, k, v, log_g, gate, S0, dO, dST=None, want_dS0=True, nthreads
             gate = {1: GATE_HEAD_SCALAR, 3: GATE_TOKEN_SCALAR}.get(np.ndim(_f64(log_g)), GATE_PER_KEY)
     ga = _f64(log_g) if gate != GATE_NONE else None
     sa, doa, dsta = _f64(S0), _f64(dO), _f64(dST)
+    lba = _f64(log_b) if gate == GATE_BILINEAR else None
+    dlb = np.empty((B, H, T, dv)) if gate == GATE_BILINEAR else None
     dq = np.empty((B, H, T, dk)); dk_ = np.empty((B, H, T, dk)); dv_ = np.empty((B, H, T, dv))
     dg = None if gate == GATE_NONE else np.empty(ga.shape)
     dS0 = np.empty((B, H, dk, dv)) if want_dS0 else None
     rc = _load().gla_oracle_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), int(gate), _ptr(sa), _ptr(doa),
                                 _ptr(dsta), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dS0),
-                                B, H, T, dk, dv, int(nthreads or default_threads()), int(mutant))
+                                B, H, T, dk, dv, int(nthreads or default_threads()), int(mutant),
+                                _ptr(lba), _ptr(dlb))
     if rc != 0:
         raise RuntimeError(f"gla_oracle_bwd failed with status {rc}")
+    if gate == GATE_BILINEAR:
+        return dq, dk_, dv_, dg, dS0, dlb
     return dq, dk_, dv_, dg, dS0
 
 

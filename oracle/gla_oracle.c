@@ -239,13 +239,20 @@ int gla_oracle_fwd(const double* q, const double* k, const double* v,
  * are kept and the ones between recomputed from them by the same forward
  * steps, so every value is the one a run storing all states would use.
  *
+ * The bilinear gate (mode 4, S_t = Diag(alpha_t) S_{t-1} Diag(beta_t) + k_t^T v_t)
+ * decays D by both factors, D_t = Diag(alpha_{t+1}) D_{t+1} Diag(beta_{t+1}) + q_t^T do_t,
+ * dS0 = Diag(alpha_0) D_0 Diag(beta_0), and adds
+ *   dlog alpha_t[i] = alpha_t[i] sum_j D_t[i][j] beta_t[j] S_{t-1}[i][j],
+ *   dlog beta_t[j]  = beta_t[j]  sum_i D_t[i][j] alpha_t[i] S_{t-1}[i][j].
+ *
  * Backward mutants (tests only): 11 dlog alpha without the factor alpha_t;
  * 12 D decayed before q_t^T do_t is added; 13 dq_t read from S_{t-1};
- * 14 the decay of D skipped at t = 0 (dS0 = D_0).
+ * 14 the decay of D skipped at t = 0 (dS0 = D_0); 15 dlog beta without the
+ * factor beta_t; 16 D decayed by alpha only (beta left out).
  */
 typedef struct {
-    const double *q, *k, *v, *log_g, *S0, *dO, *dST;
-    double *gq, *gk, *gv, *dlg, *dS0; /* gradients of q, k, v; dlg: [T][dk] dlog alpha of this (b, h) */
+    const double *q, *k, *v, *log_g, *log_b, *S0, *dO, *dST;
+    double *gq, *gk, *gv, *dlg, *dlb, *dS0; /* dlg: [T][dk] dlog alpha, dlb: [T][dv] dlog beta of this (b, h) */
     long H, T, dk, dv, bh;
     int gate, mutant, status;
 } bjob_t;
@@ -258,7 +265,13 @@ static double bgate(const bjob_t* J, long t, long i)
     return exp(J->log_g[(J->bh * J->T + t) * J->dk + i]);
 }
 
-/* S_out = Diag(alpha_t) S_in + k_t^T v_t (Eq. 3), full width dv */
+/* beta_t[j] of the bilinear gate, 1 in every other mode */
+static double bbeta(const bjob_t* J, long t, long j)
+{
+    return J->gate == 4 ? exp(J->log_b[(J->bh * J->T + t) * J->dv + j]) : 1.0;
+}
+
+/* S_out = Diag(alpha_t) S_in Diag(beta_t) + k_t^T v_t (Eq. 3), full width dv */
 static void bstep(const bjob_t* J, long t, const double* Sin, double* Sout)
 {
     const long dk = J->dk, dv = J->dv;
@@ -266,7 +279,17 @@ static void bstep(const bjob_t* J, long t, const double* Sin, double* Sout)
     const double* vt = J->v + (J->bh * J->T + t) * dv;
     for (long i = 0; i < dk; ++i) {
         const double a = bgate(J, t, i), ki = kt[i];
-        for (long j = 0; j < dv; ++j) Sout[i * dv + j] = a * Sin[i * dv + j] + ki * vt[j];
+        for (long j = 0; j < dv; ++j) Sout[i * dv + j] = a * bbeta(J, t, j) * Sin[i * dv + j] + ki * vt[j];
+    }
+}
+
+/* D <- Diag(alpha_t) D Diag(beta_t) (mutant 16: alpha only) */
+static void bdecay(const bjob_t* J, long t, double* D)
+{
+    const long dk = J->dk, dv = J->dv;
+    for (long i = 0; i < dk; ++i) {
+        const double a = bgate(J, t, i);
+        for (long j = 0; j < dv; ++j) D[i * dv + j] *= a * (J->mutant == 16 ? 1.0 : bbeta(J, t, j));
     }
 }
 
@@ -309,11 +332,7 @@ static void bwd_job(bjob_t* J)
             double* dqt = J->gq + (J->bh * T + t) * dk;
             double* dkt = J->gk + (J->bh * T + t) * dk;
             double* dvt = J->gv + (J->bh * T + t) * dv;
-            if (J->mutant == 12)
-                for (long i = 0; i < dk; ++i) {
-                    const double a = bgate(J, t, i);
-                    for (long j = 0; j < dv; ++j) D[i * dv + j] *= a;
-                }
+            if (J->mutant == 12) bdecay(J, t, D);
             /* D_t = (decayed later adjoint) + q_t^T do_t */
             for (long i = 0; i < dk; ++i)
                 for (long j = 0; j < dv; ++j) D[i * dv + j] += qt[i] * dot[j];
@@ -323,23 +342,23 @@ static void bwd_job(bjob_t* J)
                 for (long j = 0; j < dv; ++j) {
                     aq += Sq[i * dv + j] * dot[j];
                     ak += D[i * dv + j] * vt[j];
-                    ag += D[i * dv + j] * Sprev[i * dv + j];
+                    ag += D[i * dv + j] * bbeta(J, t, j) * Sprev[i * dv + j];
                 }
                 dqt[i] = aq;
                 dkt[i] = ak;
                 J->dlg[t * dk + i] = (J->mutant == 11) ? ag : bgate(J, t, i) * ag;
             }
             for (long j = 0; j < dv; ++j) {
-                double a = 0.0;
-                for (long i = 0; i < dk; ++i) a += kt[i] * D[i * dv + j];
+                double a = 0.0, ab = 0.0;
+                for (long i = 0; i < dk; ++i) {
+                    a += kt[i] * D[i * dv + j];
+                    ab += D[i * dv + j] * bgate(J, t, i) * Sprev[i * dv + j];
+                }
                 dvt[j] = a;
+                if (J->gate == 4 && J->dlb) J->dlb[t * dv + j] = (J->mutant == 15) ? ab : bbeta(J, t, j) * ab;
             }
             /* the part of dL/dS_{t-1} that flows through S_t */
-            if (J->mutant != 12 && !(J->mutant == 14 && t == 0))
-                for (long i = 0; i < dk; ++i) {
-                    const double a = bgate(J, t, i);
-                    for (long j = 0; j < dv; ++j) D[i * dv + j] *= a;
-                }
+            if (J->mutant != 12 && !(J->mutant == 14 && t == 0)) bdecay(J, t, D);
         }
     }
     if (J->dS0) memcpy(J->dS0 + J->bh * n, D, (size_t)n * sizeof(double));
@@ -372,19 +391,22 @@ int gla_oracle_bwd(const double* q, const double* k, const double* v,
                    const double* log_g, int gate, const double* S0,
                    const double* dO, const double* dST,
                    double* dq, double* dk_out, double* dv_out, double* dlog_g, double* dS0,
-                   long B, long H, long T, long dk, long dv, int nthreads, int mutant)
+                   long B, long H, long T, long dk, long dv, int nthreads, int mutant,
+                   const double* log_b, double* dlog_b)
 {
     if (!dO || !dq || !dk_out || !dv_out || B <= 0 || H <= 0 || T < 0 || dk <= 0 || dv <= 0) return 1;
     if (T > 0 && (!q || !k || !v)) return 1;
-    if (gate < 0 || gate > 3 || (gate != 0 && !log_g)) return 1;
+    if (gate < 0 || gate > 4 || (gate != 0 && !log_g)) return 1;
+    if (gate == 4 && T > 0 && !log_b) return 1;
     const long BH = B * H;
     double* dlg = (double*)calloc((size_t)(BH * T * dk > 0 ? BH * T * dk : 1), sizeof(double));
     bjob_t* jobs = (bjob_t*)calloc((size_t)BH, sizeof(bjob_t));
     if (!dlg || !jobs) { free(dlg); free(jobs); return 2; }
     for (long bh = 0; bh < BH; ++bh) {
         bjob_t* J = &jobs[bh];
-        J->q = q; J->k = k; J->v = v; J->log_g = log_g; J->S0 = S0; J->dO = dO; J->dST = dST;
+        J->q = q; J->k = k; J->v = v; J->log_g = log_g; J->log_b = log_b; J->S0 = S0; J->dO = dO; J->dST = dST;
         J->gq = dq; J->gk = dk_out; J->gv = dv_out; J->dlg = dlg + bh * T * dk; J->dS0 = dS0;
+        J->dlb = (gate == 4 && dlog_b) ? dlog_b + bh * T * dv : NULL;
         J->H = H; J->T = T; J->dk = dk; J->dv = dv; J->bh = bh; J->gate = gate; J->mutant = mutant;
     }
     if (nthreads < 1) nthreads = 1;
@@ -404,7 +426,7 @@ int gla_oracle_bwd(const double* q, const double* k, const double* v,
     int st = 0;
     for (long i = 0; i < BH; ++i) if (jobs[i].status) st = 2;
     if (st == 0 && dlog_g && gate != 0) {
-        if (gate == 2) {
+        if (gate == 2 || gate == 4) {
             memcpy(dlog_g, dlg, (size_t)(BH * T * dk) * sizeof(double));
         } else if (gate == 3) {
             for (long bt = 0; bt < BH * T; ++bt) {

@@ -139,3 +139,112 @@ def test_pins_catch_planted_backward_mistakes(mutant):
     err_bad = max(np.abs(a - r.numpy()).max() for a, r in zip(bad, refs))
     assert err_good < 1e-10
     assert err_bad > 1e-6, f"mutant {mutant} not caught"
+
+
+# ---------------------------------------------------------------- bilinear gate (mode 4)
+
+def _bil_case(B=1, H=2, T=5, dk=3, dv=2, seed=71, dist="logsigmoid16"):
+    w = gi.Workload("pin", B=B, H=H, T=T, dk=dk, dv=dv, dtype=torch.float32, gate=gi.GATE_BILINEAR,
+                    s0_std=0.5, gate_dist=dist)
+    x = gi.make_inputs(w, seed=seed)
+    f = lambda t: None if t is None else t.to(torch.float64).numpy()
+    rng = np.random.default_rng(seed)
+    dO = rng.standard_normal((B, H, T, dv))
+    dST = rng.standard_normal((B, H, dk, dv))
+    return f(x["q"]), f(x["k"]), f(x["v"]), f(x["log_g"]), f(x["log_b"]), f(x["S0"]), dO, dST
+
+
+def _bil_loss(q, k, v, g, b, S0, dO, dST):
+    O, ST = oracle.gla_forward(q, k, v, g, gi.GATE_BILINEAR, S0, log_b=b)
+    return float((O * dO).sum()) + float((ST * dST).sum())
+
+
+def test_bilinear_finite_differences():
+    """Every gradient of the bilinear gate, log beta included, against central differences
+    of the (pinned) forward oracle."""
+    q, k, v, g, b, S0, dO, dST = _bil_case()
+    dq, dk, dv, dg, dS0, db = oracle.gla_backward(q, k, v, g, gi.GATE_BILINEAR, S0, dO, dST, log_b=b)
+    args = dict(q=q, k=k, v=v, g=g, b=b, S0=S0)
+    grads = dict(q=dq, k=dk, v=dv, g=dg, b=db, S0=dS0)
+    h = 1e-6
+    for name, arr in args.items():
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            p, m = dict(args), dict(args)
+            p[name] = arr.copy(); p[name][idx] += h
+            m[name] = arr.copy(); m[name][idx] -= h
+            fd[idx] = (_bil_loss(**p, dO=dO, dST=dST) - _bil_loss(**m, dO=dO, dST=dST)) / (2 * h)
+        scale = max(1.0, np.abs(fd).max())
+        np.testing.assert_allclose(grads[name], fd, rtol=0, atol=1e-7 * scale, err_msg=name)
+
+
+@pytest.mark.parametrize("T", [1, 33, 150])
+def test_bilinear_autograd_of_plain_recurrence(T):
+    """torch.autograd through S_t = Diag(alpha_t) S_{t-1} Diag(beta_t) + k_t^T v_t written
+    in plain fp64 torch operations (T = 150 spans checkpoint blocks)."""
+    q, k, v, g, b, S0, dO, dST = _bil_case(B=2, H=1, T=T, dk=6, dv=5, seed=72 + T)
+    t = lambda a: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+    tq, tk, tv, tg, tb, tS0 = t(q), t(k), t(v), t(g), t(b), t(S0)
+    S = tS0
+    outs = []
+    for s in range(T):
+        S = torch.exp(tg[:, :, s])[..., None] * S * torch.exp(tb[:, :, s])[..., None, :] + \
+            tk[:, :, s, :, None] * tv[:, :, s, None, :]
+        outs.append(torch.einsum("bhk,bhkv->bhv", tq[:, :, s], S))
+    L = (torch.stack(outs, dim=2) * torch.tensor(dO)).sum() + (S * torch.tensor(dST)).sum()
+    L.backward()
+    got = oracle.gla_backward(q, k, v, g, gi.GATE_BILINEAR, S0, dO, dST, log_b=b)
+    for name, x, ref in zip(("dq", "dk", "dv", "dlog_g", "dS0", "dlog_b"), got,
+                            (tq.grad, tk.grad, tv.grad, tg.grad, tS0.grad, tb.grad)):
+        ref = ref.numpy()
+        np.testing.assert_allclose(x, ref, rtol=0, atol=1e-11 * max(1.0, np.abs(ref).max()), err_msg=name)
+
+
+def test_bilinear_unit_beta_is_the_per_key_backward():
+    """beta = 1: every gradient but dlog beta equals the per-key gate's."""
+    q, k, v, g, b, S0, dO, dST = _bil_case(B=2, H=2, T=40, dk=4, dv=3, seed=73)
+    got = oracle.gla_backward(q, k, v, g, gi.GATE_BILINEAR, S0, dO, dST, log_b=np.zeros_like(b))
+    ref = oracle.gla_backward(q, k, v, g, gi.GATE_PER_KEY, S0, dO, dST)
+    for name, x, y in zip(("dq", "dk", "dv", "dlog_g", "dS0"), got[:5], ref):
+        np.testing.assert_allclose(x, y, rtol=0, atol=1e-12 * max(1.0, np.abs(y).max()), err_msg=name)
+
+
+@pytest.mark.parametrize("dist", ["logsigmoid16", "steep"])
+def test_bilinear_gate_gradients_closed_form(dist):
+    """The gate gradients in closed form, from the other gradients and the outputs (what a
+    chunked backward uses instead of the state products): with c_t the reverse cumulative
+    sum over tokens t' >= t,
+      dlog alpha_t = c_t( q (.) dq - k (.) dk ) + [t' = T-1] rowsum(dST (.) S_T),
+      dlog beta_t  = c_t( o (.) do - v (.) dv ) + [t' = T-1] colsum(dST (.) S_T),
+    where each term is the derivative through the cumulative decays b_t, b'_t that the
+    parallel form O = ((Q (.) B)(K / B)^T (.) M (.) B'/B') V + (Q (.) B) S0 Diag(B') contains."""
+    q, k, v, g, b, S0, dO, dST = _bil_case(B=1, H=2, T=70, dk=5, dv=4, seed=74, dist=dist)
+    dq, dk, dv, dg, dS0, db = oracle.gla_backward(q, k, v, g, gi.GATE_BILINEAR, S0, dO, dST, log_b=b)
+    O, ST = oracle.gla_forward(q, k, v, g, gi.GATE_BILINEAR, S0, log_b=b)
+    ea = q * dq - k * dk
+    eb = O * dO - v * dv
+    ea[:, :, -1] += (dST * ST).sum(-1)
+    eb[:, :, -1] += (dST * ST).sum(-2)
+    rc = lambda x: np.flip(np.cumsum(np.flip(x, 2), 2), 2)
+    for name, got, ref in (("dlog_g", dg, rc(ea)), ("dlog_b", db, rc(eb))):
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-10 * max(1.0, np.abs(ref).max()), err_msg=name)
+
+
+@pytest.mark.parametrize("mutant", [15, 16])
+def test_bilinear_pins_catch_planted_mistakes(mutant):
+    """dlog beta without its factor beta_t (15) and D decayed by alpha only (16) each fail
+    the finite-difference pin on some gradient."""
+    q, k, v, g, b, S0, dO, dST = _bil_case(seed=75)
+    bad = oracle.gla_backward(q, k, v, g, gi.GATE_BILINEAR, S0, dO, dST, log_b=b, mutant=mutant)
+    args = dict(q=q, k=k, v=v, g=g, b=b, S0=S0)
+    grads = dict(q=bad[0], k=bad[1], v=bad[2], g=bad[3], S0=bad[4], b=bad[5])
+    h = 1e-6
+    worst = 0.0
+    for name, arr in args.items():
+        for idx in np.ndindex(arr.shape):
+            p, m = dict(args), dict(args)
+            p[name] = arr.copy(); p[name][idx] += h
+            m[name] = arr.copy(); m[name][idx] -= h
+            fd = (_bil_loss(**p, dO=dO, dST=dST) - _bil_loss(**m, dO=dO, dST=dST)) / (2 * h)
+            worst = max(worst, abs(grads[name][idx] - fd))
+    assert worst > 1e-4
