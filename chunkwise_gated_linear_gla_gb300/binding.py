@@ -57,6 +57,7 @@ class gla_bwd_params(ctypes.Structure):
         ("dtype", ctypes.c_int), ("gate", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("path", ctypes.c_int),
+        ("log_b", ctypes.c_void_p), ("grad_log_b", ctypes.c_void_p),
     ]
 
 
@@ -197,10 +198,13 @@ def gla_bwd_workspace_size(p: gla_bwd_params) -> int:
 
 
 def make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dlog_g, dS0, gate=None,
-                    workspace=None, path=GLA_PATH_AUTO) -> gla_bwd_params:
-    """Fill gla_bwd_params from torch tensors (shapes read from q and v)."""
+                    workspace=None, path=GLA_PATH_AUTO, log_b=None, dlog_b=None) -> gla_bwd_params:
+    """Fill gla_bwd_params from torch tensors (shapes read from q and v).
+    log_b (the bilinear gate's log beta) selects GLA_GATE_BILINEAR; dlog_b receives its gradient."""
     import torch
     B, H, T, dk_ = q.shape
+    if gate is None and log_b is not None:
+        gate = GLA_GATE_BILINEAR
     if gate is None:
         if log_g is None:
             gate = GLA_GATE_NONE
@@ -216,14 +220,17 @@ def make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dlog_g, dS0, gate=N
     p.workspace = _ptr(workspace)
     p.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     p.path = path
+    p.log_b, p.grad_log_b = _ptr(log_b), _ptr(dlog_b)
     return p
 
 
-def backward(q, k, v, log_g, S0, dO, dST=None, gate=None, want_dS0=True, stream=None, path=GLA_PATH_AUTO):
+def backward(q, k, v, log_g, S0, dO, dST=None, gate=None, want_dS0=True, stream=None, path=GLA_PATH_AUTO,
+             log_b=None):
     """Allocate the gradients and the workspace with torch, then call gla_bwd.
 
     Returns (dq, dk, dv, dlog_g, dS0), fp32; dlog_g is None without a gate and
-    dS0 None unless wanted.
+    dS0 None unless wanted. With the bilinear gate (log_b given) dlog_b is
+    appended.
     """
     import torch
     B, H, T, dk_ = q.shape
@@ -234,11 +241,14 @@ def backward(q, k, v, log_g, S0, dO, dST=None, gate=None, want_dS0=True, stream=
     dv = torch.empty((B, H, T, dv_), dtype=torch.float32, device=dev)
     dg = None if log_g is None else torch.empty(log_g.shape, dtype=torch.float32, device=dev)
     dS0 = torch.empty((B, H, dk_, dv_), dtype=torch.float32, device=dev) if want_dS0 else None
-    p = make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dg, dS0, gate, path=path)
+    db = None if log_b is None else torch.empty(log_b.shape, dtype=torch.float32, device=dev)
+    p = make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dg, dS0, gate, path=path, log_b=log_b, dlog_b=db)
     n = gla_bwd_workspace_size(p)
     ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), n
     gla_bwd(p, stream)
+    if log_b is not None:
+        return dq, dk, dv, dg, dS0, db
     return dq, dk, dv, dg, dS0
 
 

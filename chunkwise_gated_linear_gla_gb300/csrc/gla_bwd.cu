@@ -46,6 +46,9 @@ struct BwdArgs {
     float* Ag;     // [BH][nch][CS][CS] intra-chunk scores (bf16 path)
     float* bnd;    // [ndvt][BH][dk] rowsum(dST (.) S_T) partial per dv tile
     float* dla;    // [BH][T][dk] dlog b, then dlog alpha (per key)
+    // bilinear gate: log beta, its gradient, and the per-token terms o (.) do - v (.) dv
+    // (plus colsum(dST (.) S_T) at the last token) whose reverse cumulative sum it is
+    const float* log_b; float* glb; float* dlbe;   // [BH][T][dv] each
     int B, H, T, dk, dv, gate, nch, ndvt, nplanes;
 };
 
@@ -73,7 +76,8 @@ __device__ __forceinline__ float log_alpha(const BwdArgs& a, int bh, int t, int 
     switch (a.gate) {
     case GLA_GATE_HEAD_SCALAR: return a.log_g[bh % a.H];
     case GLA_GATE_TOKEN_SCALAR: return a.log_g[(size_t)bh * a.T + t];
-    case GLA_GATE_PER_KEY: return a.log_g[((size_t)bh * a.T + t) * a.dk + kk];
+    case GLA_GATE_PER_KEY:
+    case GLA_GATE_BILINEAR: return a.log_g[((size_t)bh * a.T + t) * a.dk + kk];
     }
     return 0.f;
 }
@@ -100,7 +104,8 @@ __device__ __forceinline__ void pf_chunk_inputs(const BwdArgs& a, int bh, int c,
     const size_t row = (size_t)bh * a.T + t0;
     if (with_q) pf_range(static_cast<const char*>(a.q) + row * a.dk * esz, (size_t)nr * a.dk * esz, tid, NT);
     pf_range(static_cast<const char*>(a.k) + row * a.dk * esz, (size_t)nr * a.dk * esz, tid, NT);
-    if (a.gate == GLA_GATE_PER_KEY) pf_range(a.log_g + row * a.dk, (size_t)nr * a.dk * 4, tid, NT);
+    if (a.gate == GLA_GATE_PER_KEY || a.gate == GLA_GATE_BILINEAR)
+        pf_range(a.log_g + row * a.dk, (size_t)nr * a.dk * 4, tid, NT);
     if (a.gate == GLA_GATE_TOKEN_SCALAR) pf_range(a.log_g + row, (size_t)nr * 4, tid, NT);
     if (tid < nr) {   // one row of this tile's v (and dO) columns per thread
         const size_t off = (row + tid) * a.dv + j0;
@@ -119,6 +124,8 @@ __global__ void __launch_bounds__(NT) gla_bwd_states_kernel(BwdArgs a)
     float* kt = S + dk * DVT;        // [CS][dk] k (.) Gamma
     float* vv = kt + CS * dk;        // [CS][DVT]
     float* gam = vv + CS * DVT;      // [dk]
+    float* gvb = gam + dk;           // [DVT] bilinear gate: the chunk's column decay gamma'
+    const bool bil = a.gate == GLA_GATE_BILINEAR;
     const int bh = blockIdx.x, j0 = blockIdx.y * DVT, jn = min(DVT, a.dv - j0);
     const Tin* k = static_cast<const Tin*>(a.k) + (size_t)bh * a.T * dk;
     const Tin* v = static_cast<const Tin*>(a.v) + (size_t)bh * a.T * a.dv;
@@ -150,8 +157,24 @@ __global__ void __launch_bounds__(NT) gla_bwd_states_kernel(BwdArgs a)
 #pragma unroll
             for (int r = 0; r < CS; ++r) kt[r * dk + x] = kv[r] * expf(run - bcr[r]);
         }
+        if (bil) {
+            // the column side: B'_r the in-chunk cumulative log beta, gamma' = exp(B'_end), and
+            // V (.) Gamma' with Gamma'_r = exp(B'_end - B'_r) <= 1 (rows past nr are zero)
+            __syncthreads();
+            for (int j = tid; j < DVT; j += NT) {
+                float bcv[CS], run = 0.f;
+#pragma unroll
+                for (int r = 0; r < CS; ++r) {
+                    run += (r < nr && j < jn) ? a.log_b[((size_t)bh * a.T + t0 + r) * a.dv + j0 + j] : 0.f;
+                    bcv[r] = run;
+                }
+                gvb[j] = expf(run);
+#pragma unroll
+                for (int r = 0; r < CS; ++r) vv[r * DVT + j] *= expf(run - bcv[r]);
+            }
+        }
         __syncthreads();
-        // S <- Diag(gamma) S + (K (.) Gamma)^T V, 16 columns of one row per step, and keep it
+        // S <- Diag(gamma) S Diag(gamma') + (K (.) Gamma)^T (V (.) Gamma'), 16 columns of one row per step
         float* out = a.Sst + ((size_t)bh * a.nch + c) * dk * a.dv + j0;
         for (int it = tid; it < dk * (DVT / 16); it += NT) {
             const int x = it % dk, g0 = (it / dk) * 4;
@@ -160,7 +183,8 @@ __global__ void __launch_bounds__(NT) gla_bwd_states_kernel(BwdArgs a)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float4 w = ld4(S + swz(x, 4 * (g0 + u)));
-                acc[u] = make_float4(gx * w.x, gx * w.y, gx * w.z, gx * w.w);
+                const float4 c = bil ? ld4(gvb + 4 * (g0 + u)) : make_float4(1.f, 1.f, 1.f, 1.f);
+                acc[u] = make_float4(gx * w.x * c.x, gx * w.y * c.y, gx * w.z * c.z, gx * w.w * c.w);
             }
 #pragma unroll
             for (int r = 0; r < CS; ++r) {
@@ -194,6 +218,13 @@ __global__ void __launch_bounds__(NT) gla_bwd_chunks_kernel(BwdArgs a)
     float* VD = A + CS * CS;         // [CS][CS] v_s . do_t over this tile's columns, t >= s
     float* Aw = VD + CS * CS;        // [NT / 32][CS][CS] per-warp partial scores, summed in a fixed order
     float* gam = Aw + (NT / 32) * CS * CS;   // [dk]
+    // bilinear gate only: the column side of the chunk
+    float* bcv = gam + dk;           // [CS][DVT] in-chunk cumulative log beta, B'
+    float* ddL = bcv + CS * DVT;     // [CS][DVT] dO (.) Lambda', Lambda'_r = exp(B'_r)
+    float* vvG = ddL + CS * DVT;     // [CS][DVT] v (.) Gamma', Gamma'_r = exp(B'_end - B'_r)
+    float* gvb = vvG + CS * DVT;     // [DVT] gamma' = exp(B'_end)
+    float* cst = gvb + DVT;          // [DVT] colsum(dST (.) S_T), added at the last token
+    const bool bil = a.gate == GLA_GATE_BILINEAR;
     const int bh = blockIdx.x, tile = blockIdx.y, BH = gridDim.x;
     const int j0 = tile * DVT, jn = min(DVT, a.dv - j0);
     const size_t ST = (size_t)dk * a.dv;
@@ -214,6 +245,16 @@ __global__ void __launch_bounds__(NT) gla_bwd_chunks_kernel(BwdArgs a)
                 for (int j = 0; j < jn; ++j)
                     s = fmaf(a.dST[(size_t)bh * ST + (size_t)x * a.dv + j0 + j], Sfin[(size_t)x * a.dv + j0 + j], s);
             a.bnd[((size_t)tile * BH + bh) * dk + x] = s;
+        }
+    }
+    if (bil) {
+        const float* Sfin = a.nch > 0 ? a.Sst + ((size_t)bh * a.nch + a.nch - 1) * ST : nullptr;
+        for (int j = tid; j < DVT; j += NT) {
+            float s = 0.f;
+            if (a.dST && Sfin && j < jn)
+                for (int x = 0; x < dk; ++x)
+                    s = fmaf(a.dST[(size_t)bh * ST + (size_t)x * a.dv + j0 + j], Sfin[(size_t)x * a.dv + j0 + j], s);
+            cst[j] = s;
         }
     }
     const int kk = tid;                       // the key a thread owns in the per-key phases
@@ -256,12 +297,37 @@ __global__ void __launch_bounds__(NT) gla_bwd_chunks_kernel(BwdArgs a)
             gam[kk] = expf(run);
         }
         __syncthreads();
+        if (bil) {   // the column side: B', gamma', dO (.) Lambda', v (.) Gamma' (rows past nr are zero)
+            for (int j = tid; j < DVT; j += NT) {
+                float run = 0.f;
+#pragma unroll
+                for (int r = 0; r < CS; ++r) {
+                    run += (r < nr && j < jn) ? a.log_b[((size_t)bh * a.T + t0 + r) * a.dv + j0 + j] : 0.f;
+                    bcv[r * DVT + j] = run;
+                }
+                gvb[j] = expf(run);
+#pragma unroll
+                for (int r = 0; r < CS; ++r) {
+                    const float b = bcv[r * DVT + j];
+                    ddL[r * DVT + j] = dd[r * DVT + j] * expf(b);
+                    vvG[r * DVT + j] = vv[r * DVT + j] * expf(run - b);
+                }
+            }
+            __syncthreads();
+        }
         for (int p = tid; p < CS * CS; p += NT) {
             const int t = p / CS, s = p % CS;
             float acc = 0.f;
-            if (s <= t)
+            if (s <= t) {
+                if (bil) {   // v_s . do_t with the column decay exp(B'_t - B'_s) <= 1
+                    for (int j = 0; j < DVT; ++j)
+                        acc = fmaf(dd[t * DVT + j] * vv[s * DVT + j], expf(bcv[t * DVT + j] - bcv[s * DVT + j]), acc);
+                } else {
 #pragma unroll
-                for (int g = 0; g < DVT / 4; ++g) acc = dot4(ld4(dd + t * DVT + 4 * g), ld4(vv + s * DVT + 4 * g), acc);
+                    for (int g = 0; g < DVT / 4; ++g)
+                        acc = dot4(ld4(dd + t * DVT + 4 * g), ld4(vv + s * DVT + 4 * g), acc);
+                }
+            }
             VD[p] = acc;
         }
         __syncthreads();
@@ -303,13 +369,15 @@ __global__ void __launch_bounds__(NT) gla_bwd_chunks_kernel(BwdArgs a)
             float aq[CS], ak[CS];
 #pragma unroll
             for (int t = 0; t < CS; ++t) aq[t] = ak[t] = 0.f;
+            const float* ddq = bil ? ddL : dd;   // dO (.) Lambda' and v (.) Gamma' with the bilinear gate
+            const float* vvk = bil ? vvG : vv;
 #pragma unroll 2
             for (int g = 0; g < DVT / 4; ++g) {
                 const float4 sp = ld4(Sp + swz(kk, 4 * g)), dg = ld4(D + swz(kk, 4 * g));
 #pragma unroll
                 for (int t = 0; t < CS; ++t) {
-                    aq[t] = dot4(sp, ld4(dd + t * DVT + 4 * g), aq[t]);
-                    ak[t] = dot4(dg, ld4(vv + t * DVT + 4 * g), ak[t]);
+                    aq[t] = dot4(sp, ld4(ddq + t * DVT + 4 * g), aq[t]);
+                    ak[t] = dot4(dg, ld4(vvk + t * DVT + 4 * g), ak[t]);
                 }
             }
             const float bend = bc[(CS - 1) * dk + kk];
@@ -331,12 +399,42 @@ __global__ void __launch_bounds__(NT) gla_bwd_chunks_kernel(BwdArgs a)
         {
             const int s = tid / (DVT / 4), g = tid % (DVT / 4);
             static_assert(CS * (DVT / 4) == NT, "one float4 of dv per thread");
-            if (s < nr && 4 * g < jn) {
+            if (s < nr && 4 * g < jn && !bil) {
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int x = 0; x < dk; ++x) fma4(acc, kr[s * dk + x], ld4(D + swz(x, 4 * g)));
                 for (int t = s; t < CS; ++t) fma4(acc, A[t * CS + s], ld4(dd + t * DVT + 4 * g));
                 float* o = a.gv + ((size_t)bh * a.T + t0 + s) * a.dv + j0 + 4 * g;
                 o[0] = acc.x; o[1] = acc.y; o[2] = acc.z; o[3] = acc.w;
+            } else if (s < nr && 4 * g < jn) {
+                // bilinear gate, per column j: dv_s = Gamma'_s (K (.) Gamma)_s D + sum_{t>=s} P_ts do_t
+                // exp(B'_t - B'_s); and the output o_s = Lambda'_s (Q (.) Lambda)_s S_[n-1] +
+                // sum_{t<=s} P_st v_t exp(B'_s - B'_t), for the term o_s do_s - v_s dv_s of dlog beta
+                float kd[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int x = 0; x < dk; ++x) {
+                    const float4 dx = ld4(D + swz(x, 4 * g)), sx = ld4(Sp + swz(x, 4 * g));
+                    const float kx = kr[s * dk + x], qx = qr[s * dk + x];
+                    kd[0] = fmaf(kx, dx.x, kd[0]); kd[1] = fmaf(kx, dx.y, kd[1]);
+                    kd[2] = fmaf(kx, dx.z, kd[2]); kd[3] = fmaf(kx, dx.w, kd[3]);
+                    qs[0] = fmaf(qx, sx.x, qs[0]); qs[1] = fmaf(qx, sx.y, qs[1]);
+                    qs[2] = fmaf(qx, sx.z, qs[2]); qs[3] = fmaf(qx, sx.w, qs[3]);
+                }
+                const size_t row = (size_t)bh * a.T + t0 + s;
+                float* o = a.gv + row * a.dv + j0 + 4 * g;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = 4 * g + c;
+                    const float bs = bcv[s * DVT + j], bend = bcv[(CS - 1) * DVT + j];
+                    float dvj = kd[c] * expf(bend - bs);
+                    for (int t = s; t < CS; ++t)
+                        dvj = fmaf(A[t * CS + s] * dd[t * DVT + j], expf(bcv[t * DVT + j] - bs), dvj);
+                    float oj = qs[c] * expf(bs);
+                    for (int t = 0; t <= s; ++t)
+                        oj = fmaf(A[s * CS + t] * vv[t * DVT + j], expf(bs - bcv[t * DVT + j]), oj);
+                    o[c] = dvj;
+                    float e = oj * dd[s * DVT + j] - vv[s * DVT + j] * dvj;
+                    if (t0 + s == a.T - 1) e += cst[j];
+                    a.dlbe[row * a.dv + j0 + j] = e;
+                }
             }
         }
         __syncthreads();
@@ -344,17 +442,19 @@ __global__ void __launch_bounds__(NT) gla_bwd_chunks_kernel(BwdArgs a)
         for (int it = tid; it < dk * (DVT / 16); it += NT) {
             const int x = it % dk, g0 = (it / dk) * 4;
             const float gx = gam[x];
+            const float* ddu = bil ? ddL : dd;   // bilinear gate: D Diag(gamma') and dO (.) Lambda'
             float4 acc[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float4 w = ld4(D + swz(x, 4 * (g0 + u)));
-                acc[u] = make_float4(gx * w.x, gx * w.y, gx * w.z, gx * w.w);
+                const float4 c = bil ? ld4(gvb + 4 * (g0 + u)) : make_float4(1.f, 1.f, 1.f, 1.f);
+                acc[u] = make_float4(gx * w.x * c.x, gx * w.y * c.y, gx * w.z * c.z, gx * w.w * c.w);
             }
 #pragma unroll
             for (int r = 0; r < CS; ++r) {
                 const float qx = qr[r * dk + x];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) fma4(acc[u], qx, ld4(dd + r * DVT + 4 * (g0 + u)));
+                for (int u = 0; u < 4; ++u) fma4(acc[u], qx, ld4(ddu + r * DVT + 4 * (g0 + u)));
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) st4(D + swz(x, 4 * (g0 + u)), acc[u]);
@@ -932,29 +1032,30 @@ __global__ void __launch_bounds__(NT) gla_bwd_finish_kernel(BwdArgs a)
 }
 
 // ---------------------------------------------------------------- reverse cumulative sum over tokens
-// grid (BH, ceil(dk / 32)); 8 segments of tokens x 32 keys per CTA
+// of a [BH][T][width] array (dlog b over keys, or the bilinear gate's terms over value
+// columns); grid (BH, ceil(width / 32)); 8 segments of tokens x 32 columns per CTA
 constexpr int RS_SEG = NT / 32;
-__global__ void __launch_bounds__(NT) gla_bwd_revsum_kernel(BwdArgs a, float* out)
+__global__ void __launch_bounds__(NT) gla_bwd_revsum_kernel(BwdArgs a, const float* src, float* out, int width)
 {
     __shared__ float tot[RS_SEG][32];
     const int bh = blockIdx.x, lane = threadIdx.x % 32, seg = threadIdx.x / 32;
     const int kk = blockIdx.y * 32 + lane;
     const int L = (a.T + RS_SEG - 1) / RS_SEG;
     const int ta = seg * L, tb = min(a.T, ta + L);
-    const bool on = kk < a.dk;
-    const float* in = a.dla + (size_t)bh * a.T * a.dk + kk;
+    const bool on = kk < width;
+    const float* in = src + (size_t)bh * a.T * width + kk;
     float s = 0.f;
     if (on)
-        for (int t = ta; t < tb; ++t) s += in[(size_t)t * a.dk];
+        for (int t = ta; t < tb; ++t) s += in[(size_t)t * width];
     tot[seg][lane] = s;
     __syncthreads();
     float run = 0.f;
     for (int g = RS_SEG - 1; g > seg; --g) run += tot[g][lane];
     if (on) {
-        float* o = out + (size_t)bh * a.T * a.dk + kk;
+        float* o = out + (size_t)bh * a.T * width + kk;
         for (int t = tb - 1; t >= ta; --t) {
-            run += in[(size_t)t * a.dk];
-            o[(size_t)t * a.dk] = run;
+            run += in[(size_t)t * width];
+            o[(size_t)t * width] = run;
         }
     }
 }
@@ -994,15 +1095,15 @@ __global__ void __launch_bounds__(NT) gla_bwd_head_gate_kernel(BwdArgs a)
     if (threadIdx.x == 0) a.glog[h] = part[0];
 }
 
-size_t states_smem(int dk) { return sizeof(float) * ((size_t)dk * DVT + (size_t)CS * dk + CS * DVT + dk); }
+size_t states_smem(int dk) { return sizeof(float) * ((size_t)dk * DVT + (size_t)CS * dk + CS * DVT + dk + DVT); }
 size_t chunks_smem(int dk) {
     return sizeof(float) * (2 * (size_t)dk * DVT + 3 * (size_t)CS * dk + 2 * CS * DVT + 2 * CS * CS +
-                            (NT / 32) * CS * CS + dk);
+                            (NT / 32) * CS * CS + dk + 3 * CS * DVT + 2 * DVT);
 }
 
 struct BwdPlan {
     int nch = 0, ndvt = 0;
-    size_t off_S = 0, off_Pq = 0, off_Pk = 0, off_Ag = 0, off_bnd = 0, off_dla = 0, bytes = 0;
+    size_t off_S = 0, off_Pq = 0, off_Pk = 0, off_Ag = 0, off_bnd = 0, off_dla = 0, off_dlbe = 0, bytes = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1020,12 +1121,15 @@ BwdPlan bwd_plan(const gla_bwd_params* p)
     pl.off_Ag = off;  off = up256(off + BH * pl.nch * CS * CS * 4);
     pl.off_bnd = off; off = up256(off + (size_t)pl.ndvt * BH * p->dk * 4);
     pl.off_dla = off; off = up256(off + BH * p->T * p->dk * 4);
+    if (p->gate == GLA_GATE_BILINEAR) {
+        pl.off_dlbe = off; off = up256(off + BH * p->T * p->dv * 4);
+    }
     pl.bytes = off;
     return pl;
 }
 
 bool tc_shape_ok(const gla_bwd_params* p) {
-    return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256);
+    return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256) && p->gate != GLA_GATE_BILINEAR;
 }
 
 bool span_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -1039,8 +1143,10 @@ gla_status bwd_validate(const gla_bwd_params* p)
     if (!p) return GLA_ERR_INVALID_ARG;
     if (p->B <= 0 || p->H <= 0 || p->T < 0 || p->dk <= 0 || p->dv <= 0) return GLA_ERR_INVALID_ARG;
     if (p->dtype != GLA_BF16 && p->dtype != GLA_FP32) return GLA_ERR_INVALID_ARG;
-    if (p->gate == GLA_GATE_BILINEAR) return GLA_ERR_UNSUPPORTED;   // its value-side gradient is not built
-    if (p->gate < GLA_GATE_NONE || p->gate > GLA_GATE_TOKEN_SCALAR) return GLA_ERR_INVALID_ARG;
+    if (p->gate < GLA_GATE_NONE || p->gate > GLA_GATE_BILINEAR) return GLA_ERR_INVALID_ARG;
+    const bool bil = p->gate == GLA_GATE_BILINEAR;
+    if (bil != (p->log_b != nullptr) && !(bil && p->T == 0)) return GLA_ERR_INVALID_ARG;
+    if (!bil && p->grad_log_b) return GLA_ERR_INVALID_ARG;
     if (p->dk % 16 != 0 || p->dv % 16 != 0) return GLA_ERR_INVALID_ARG;
     if ((long long)p->B * p->H > 65535) return GLA_ERR_INVALID_ARG;
     if (p->gate == GLA_GATE_NONE && (p->log_g || p->grad_log_g)) return GLA_ERR_INVALID_ARG;
@@ -1053,9 +1159,13 @@ gla_status bwd_validate(const gla_bwd_params* p)
     if (p->dk > NT) return GLA_ERR_UNSUPPORTED;
     if (p->path == GLA_PATH_TENSOR && !tc_shape_ok(p)) return GLA_ERR_UNSUPPORTED;
     const size_t e = p->dtype == GLA_BF16 ? 2 : 4;
+    if ((p->log_b && reinterpret_cast<uintptr_t>(p->log_b) % 4) ||
+        (p->grad_log_b && reinterpret_cast<uintptr_t>(p->grad_log_b) % 4))
+        return GLA_ERR_INVALID_ARG;
     const size_t BH = (size_t)p->B * p->H;
     const size_t nq = BH * p->T * p->dk, nv = BH * p->T * p->dv, ns = BH * p->dk * p->dv;
-    const size_t ng = p->gate == GLA_GATE_PER_KEY ? nq : p->gate == GLA_GATE_TOKEN_SCALAR ? BH * p->T
+    const size_t ng = (p->gate == GLA_GATE_PER_KEY || p->gate == GLA_GATE_BILINEAR) ? nq
+                    : p->gate == GLA_GATE_TOKEN_SCALAR ? BH * p->T
                     : p->gate == GLA_GATE_HEAD_SCALAR ? (size_t)p->H : 0;
     for (const void* ptr : {p->q, p->k, p->v, p->grad_O})
         if (ptr && reinterpret_cast<uintptr_t>(ptr) % e) return GLA_ERR_INVALID_ARG;
@@ -1065,14 +1175,14 @@ gla_status bwd_validate(const gla_bwd_params* p)
         if (ptr && reinterpret_cast<uintptr_t>(ptr) % 4) return GLA_ERR_INVALID_ARG;
     if (p->workspace && reinterpret_cast<uintptr_t>(p->workspace) % 256) return GLA_ERR_INVALID_ARG;
     // outputs overlap no input and no other output
-    const void* outs[] = {p->grad_q, p->grad_k, p->grad_v, p->grad_log_g, p->grad_S0};
-    const size_t osz[] = {nq * 4, nq * 4, nv * 4, ng * 4, ns * 4};
-    const void* ins[] = {p->q, p->k, p->v, p->grad_O, p->log_g, p->S0, p->grad_ST};
-    const size_t isz[] = {nq * e, nq * e, nv * e, nv * e, ng * 4, ns * 4, ns * 4};
-    for (int i = 0; i < 5; ++i) {
-        for (int j = 0; j < 7; ++j)
+    const void* outs[] = {p->grad_q, p->grad_k, p->grad_v, p->grad_log_g, p->grad_S0, p->grad_log_b};
+    const size_t osz[] = {nq * 4, nq * 4, nv * 4, ng * 4, ns * 4, nv * 4};
+    const void* ins[] = {p->q, p->k, p->v, p->grad_O, p->log_g, p->S0, p->grad_ST, p->log_b};
+    const size_t isz[] = {nq * e, nq * e, nv * e, nv * e, ng * 4, ns * 4, ns * 4, nv * 4};
+    for (int i = 0; i < 6; ++i) {
+        for (int j = 0; j < 8; ++j)
             if (span_overlap(outs[i], osz[i], ins[j], isz[j])) return GLA_ERR_INVALID_ARG;
-        for (int j = i + 1; j < 5; ++j)
+        for (int j = i + 1; j < 6; ++j)
             if (span_overlap(outs[i], osz[i], outs[j], osz[j])) return GLA_ERR_INVALID_ARG;
     }
     return GLA_OK;
@@ -1151,7 +1261,8 @@ cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.glog && n > 0) {
-        gla_bwd_revsum_kernel<<<dim3(BH, (p.dk + 31) / 32), NT, 0, s>>>(a, p.gate == GLA_GATE_PER_KEY ? a.glog : a.dla);
+        const bool per_key = p.gate == GLA_GATE_PER_KEY || p.gate == GLA_GATE_BILINEAR;
+        gla_bwd_revsum_kernel<<<dim3(BH, (p.dk + 31) / 32), NT, 0, s>>>(a, a.dla, per_key ? a.glog : a.dla, p.dk);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (p.gate == GLA_GATE_TOKEN_SCALAR) {
             const size_t rows = (size_t)BH * p.T;
@@ -1159,6 +1270,10 @@ cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s
             gla_bwd_token_gate_kernel<<<grid, NT, 0, s>>>(a);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
+    }
+    if (a.glb && n > 0) {   // bilinear gate: dlog beta from the chunk sweep's per-token terms
+        gla_bwd_revsum_kernel<<<dim3(BH, (p.dv + 31) / 32), NT, 0, s>>>(a, a.dlbe, a.glb, p.dv);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.glog && p.gate == GLA_GATE_HEAD_SCALAR) {
         if (n == 0) return cudaMemsetAsync(a.glog, 0, (size_t)p.H * sizeof(float), s);
@@ -1197,6 +1312,9 @@ extern "C" gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream)
     a.bnd = p->grad_log_g ? reinterpret_cast<float*>(w + pl.off_bnd) : nullptr;
     a.dla = p->grad_log_g ? reinterpret_cast<float*>(w + pl.off_dla) : nullptr;
     a.B = p->B; a.H = p->H; a.T = p->T; a.dk = p->dk; a.dv = p->dv; a.gate = p->gate;
+    a.log_b = p->log_b;
+    a.glb = p->grad_log_b;
+    a.dlbe = p->gate == GLA_GATE_BILINEAR ? reinterpret_cast<float*>(w + pl.off_dlbe) : nullptr;
     a.nch = pl.nch; a.ndvt = pl.ndvt;
     const bool use_tc = p->path != GLA_PATH_SIMT && tc_shape_ok(p);
     a.nplanes = pl.ndvt + (use_tc ? 1 : 0);

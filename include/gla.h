@@ -199,8 +199,11 @@ gla_status gla_host_release(void);
  * every 16-row chunk, a reverse sweep carries dL/dS through the chunks, and
  * the gate gradient is the reverse cumulative sum over tokens of
  * q (.) dq - k (.) dk (plus rowsum(grad_ST (.) S_T) at the last token).
- * Every gate mode but the bilinear one (GLA_ERR_UNSUPPORTED) and both dtypes
- * are supported (q, k, v and grad_O in `dtype`; all gradients fp32; dk <= 256). For bf16 inputs with dk in {64, 128, 256} the
+ * Every gate mode and both dtypes are supported (q, k, v and grad_O in
+ * `dtype`; all gradients fp32; dk <= 256). The bilinear gate takes log_b and
+ * returns dL/dlog_b in grad_log_b ([B,H,T,dv]), on the CUDA-core path; its
+ * gradient is the reverse cumulative sum over tokens of o (.) do - v (.) dv
+ * (plus colsum(grad_ST (.) S_T) at the last token), with o recomputed. For bf16 inputs with dk in {64, 128, 256} the
  * chunk products run on the tensor cores with bf16 operands and fp32
  * accumulation (like the forward tensor path); otherwise, or with
  * path = GLA_PATH_SIMT, everything runs in fp32 on CUDA cores. (The backward
@@ -233,7 +236,9 @@ typedef struct {
     void* workspace;
     size_t workspace_bytes;
     int path;               /* gla_path: AUTO takes the tensor-core products for bf16 with dk in
-                               {64,128,256}, else the fp32 CUDA-core path */
+                               {64,128,256} (not with the bilinear gate), else the fp32 CUDA-core path */
+    const float* log_b;     /* [B,H,T,dv] log(beta_t) for GLA_GATE_BILINEAR, else NULL */
+    float* grad_log_b;      /* [B,H,T,dv] dL/dlog_b, or NULL (not wanted; bilinear gate only) */
 } gla_bwd_params;
 
 gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream);

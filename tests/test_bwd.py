@@ -228,10 +228,12 @@ def test_bwd_full_gla_layer_sampled_heads():
 # ---------------------------------------------------------------- host-side checks (no GPU)
 
 def test_bwd_struct_layout():
-    # 12 pointers, 7 ints (padded to 8 bytes), pointer, size_t, int (padded)
-    assert ctypes.sizeof(bnd.gla_bwd_params) == 12 * 8 + 8 * 4 + 8 + 8 + 8
+    # 12 pointers, 7 ints (padded to 8 bytes), pointer, size_t, int (padded), 2 pointers
+    assert ctypes.sizeof(bnd.gla_bwd_params) == 12 * 8 + 8 * 4 + 8 + 8 + 8 + 2 * 8
     assert bnd.gla_bwd_params.workspace.offset == 128
     assert bnd.gla_bwd_params.path.offset == 144
+    assert bnd.gla_bwd_params.log_b.offset == 152
+    assert bnd.gla_bwd_params.grad_log_b.offset == 160
 
 
 def _bp(**kw):
@@ -259,7 +261,10 @@ BAD = [
     ("misaligned workspace", dict(workspace=0x7000010, workspace_bytes=1 << 20), bnd.GLA_ERR_INVALID_ARG),
     ("bad dtype", dict(dtype=5), bnd.GLA_ERR_INVALID_ARG),
     ("dk 512", dict(dk=512), bnd.GLA_ERR_UNSUPPORTED),
-    ("bilinear gate", dict(gate=4), bnd.GLA_ERR_UNSUPPORTED),
+    ("bilinear gate without log_b", dict(gate=4), bnd.GLA_ERR_INVALID_ARG),
+    ("log_b with the per-key gate", dict(log_b=0x900000), bnd.GLA_ERR_INVALID_ARG),
+    ("bilinear gate on the tensor path", dict(gate=4, log_b=0x900000, path=bnd.GLA_PATH_TENSOR),
+     bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with dk 48", dict(dk=48, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("bad path", dict(path=7), bnd.GLA_ERR_INVALID_ARG),
