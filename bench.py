@@ -375,7 +375,8 @@ def run_backward(args, w):
         dOs = torch.randn((1, 1, ws_.T, w.dv)).to(w.dtype)
         cores = oracle.default_threads()
         t0 = time.perf_counter()
-        oracle.gla_backward(xs["q"], xs["k"], xs["v"], xs["log_g"], xs["gate"], xs["S0"], dOs, None, nthreads=cores)
+        oracle.gla_backward(xs["q"], xs["k"], xs["v"], xs["log_g"], xs["gate"], xs["S0"], dOs, None, nthreads=cores,
+                            log_b=xs.get("log_b"))
         dt = time.perf_counter() - t0
         cpu = {"value": ws_.T / dt / w.H, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"1 head x T={ws_.T} (one (b,h) job runs on one thread), {dt:.2f} s, {cpu_model()}"}
@@ -390,7 +391,9 @@ def run_backward(args, w):
     dq, dk, dv = f32(w.B, w.H, w.T, w.dk), f32(w.B, w.H, w.T, w.dk), f32(w.B, w.H, w.T, w.dv)
     dg = None if g is None else torch.empty(g.shape, dtype=torch.float32, device=dev)
     dS0 = f32(w.B, w.H, w.dk, w.dv)
-    p = bnd.make_bwd_params(q, k, v, g, S0, dO, dST, dq, dk, dv, dg, dS0, gate=x["gate"])
+    lb = c(x.get("log_b"))
+    db = None if lb is None else f32(w.B, w.H, w.T, w.dv)
+    p = bnd.make_bwd_params(q, k, v, g, S0, dO, dST, dq, dk, dv, dg, dS0, gate=x["gate"], log_b=lb, dlog_b=db)
     nbytes = bnd.gla_bwd_workspace_size(p)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), nbytes
@@ -424,7 +427,7 @@ def run_backward(args, w):
         "vs_baseline": None, "dtype": "f32" if w.dtype == torch.float32 else "bf16 in, f32 arithmetic",
         "data": "synthetic (seeded inputs of the workload; dO ~ N(0,1), dST ~ 0.1 N(0,1))",
         "config": {"workload": f"{w.name} backward: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
-                               f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar'][w.gate]}",
+                               f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar', 'bilinear'][w.gate]}",
                    "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",
                    "workspace_bytes": nbytes},
         "roofline": {"kernel": "gla_bwd (CUDA cores, all stages)", "bound": "alu", "achieved": tflops,
