@@ -17,6 +17,14 @@
 // M) V (+ (Q (.) B) S0) and S_T = Diag(b_T)(S0 + sum_s (k_s / b_s)^T v_s):
 //   dlog b_t = q_t (.) dq_t - k_t (.) dk_t  (+ rowsum(dST (.) S_T) at t = T-1),
 //   dlog alpha_t = sum_{t' >= t} dlog b_t'.
+// The bilinear gate (Table 1's DFW row, S_t = Diag(alpha_t) S_{t-1} Diag(beta_t) +
+// k_t^T v_t) adds the same structure on the value columns: with b'_t the cumulative
+// beta, Lambda' = b'_t / b'_start, Gamma' = b'_end / b'_t and gamma' = b'_end / b'_start,
+//   D_[n-1] = Diag(gamma) D_[n] Diag(gamma') + (Q (.) Lambda)^T (dO (.) Lambda'),
+// the inter products take dO (.) Lambda' and V (.) Gamma', the pair dots v_s . do_t
+// and the dv intra term carry exp(B'_t - B'_s) per column, and
+//   dlog beta_t = sum_{t' >= t} (o_t' (.) do_t' - v_t' (.) dv_t')  (+ colsum(dST (.) S_T) at T-1)
+// with o recomputed in the reverse sweep (CUDA-core path only).
 //
 // Kernels: gla_bwd_states (forward sweep, writes the state after every
 // chunk), gla_bwd_chunks (reverse sweep per (b,h, 64 dv columns): partial dq
