@@ -201,11 +201,12 @@ gla_status gla_host_release(void);
  * q (.) dq - k (.) dk (plus rowsum(grad_ST (.) S_T) at the last token).
  * Every gate mode and both dtypes are supported (q, k, v and grad_O in
  * `dtype`; all gradients fp32; dk <= 256). The bilinear gate takes log_b and
- * returns dL/dlog_b in grad_log_b ([B,H,T,dv]), on the CUDA-core path; its
- * gradient is the reverse cumulative sum over tokens of o (.) do - v (.) dv
- * (plus colsum(grad_ST (.) S_T) at the last token), with o recomputed. For bf16 inputs with dk in {64, 128, 256} the
- * chunk products run on the tensor cores with bf16 operands and fp32
- * accumulation (like the forward tensor path); otherwise, or with
+ * returns dL/dlog_b in grad_log_b ([B,H,T,dv], may be NULL), on the CUDA-core
+ * path; that gradient is the reverse cumulative sum over tokens of
+ * o (.) do - v (.) dv (plus colsum(grad_ST (.) S_T) at the last token), with o
+ * recomputed inside. For bf16 inputs with dk in {64, 128, 256} and the other
+ * gates, the chunk products run on the tensor cores (mma.sync, operands split
+ * into hi + lo bf16 parts, fp32 accumulation); otherwise, or with
  * path = GLA_PATH_SIMT, everything runs in fp32 on CUDA cores. (The backward
  * is the next step after the forward pass; no page gives numbers for it.)
  *
