@@ -48,6 +48,32 @@ def test_struct_layout_matches_header():
     assert bnd.gla_fwd_params.log_b.offset == 112
 
 
+def test_plain_c_client_sees_the_binding_layout(lib, tmp_path):
+    """include/gla.h compiles as C99 and links against libgla.so; the parameter structs
+    have the layout the Python binding declares."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    build = os.path.dirname(bnd.library_path())
+    exe = str(tmp_path / "abi_client")
+    cmd = [cc, "-std=c99", "-Wall", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+           os.path.join(ROOT, "tests", "csrc", "abi_client.c"), "-L", build, "-lgla", "-Wl,-rpath," + build,
+           "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    fwd = [int(x) for x in out[0].split()[1:]]
+    bwd = [int(x) for x in out[1].split()[1:]]
+    F, Bw = bnd.gla_fwd_params, bnd.gla_bwd_params
+    assert fwd == [ctypes.sizeof(F), F.workspace.offset, F.path.offset, F.log_b.offset]
+    assert bwd == [ctypes.sizeof(Bw), Bw.workspace.offset, Bw.path.offset, Bw.log_b.offset, Bw.grad_log_b.offset]
+    assert out[2].startswith("status GLA_ERR_INVALID_ARG")
+    assert int(out[3].split()[1]) == gla.gla_version()
+
+
 def test_status_strings(lib):
     for s in range(6):
         txt = gla.gla_status_string(s)
