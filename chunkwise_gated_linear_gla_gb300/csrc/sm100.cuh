@@ -64,6 +64,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps until it
+// completes (or the hint elapses) instead of returning at once, so waiting threads do not
+// keep the barrier and shared-memory pipes busy with polls.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, for at most
 // `timeout_ns` of wall time. Returns false if the wait ran out; the caller
 // records the error and winds down.
@@ -75,6 +90,95 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
         if (globaltimer() - t0 > timeout_ns) return false;
     }
 }
+
+// ---------------------------------------------------------------- thread-block clusters
+// Distributed shared memory: a CTA addresses another CTA's shared memory through
+// the cluster window (mapa); mbarriers there can be arrived on, bulk copies and
+// st.async stores can land there and signal their byte counts on a barrier there.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: arrive (release) then wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The cluster-window address of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its cluster-window address (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_caddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_caddr) : "memory");
+}
+
+// try_wait with acquire at cluster scope: for barriers that other CTAs of the
+// cluster arrive on or whose data other CTAs write.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Orders this thread's later accesses after what other CTAs of the cluster released (and
+// its earlier ones before what it releases): one fence after a wait that spun at CTA scope.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Bounded wait that also gives up as soon as *abort_flag is set. It spins at CTA scope (a
+// cluster-scope acquire in a polling loop slows the whole SM) and ends with one cluster-scope
+// fence, for waits whose data or signal comes from other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                                  const volatile int* abort_flag) {
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = globaltimer();
+        while (true) {
+            if (mbar_try_wait_sleep(bar, parity, 100000u)) {
+                ok = true;
+                break;
+            }
+            if (*abort_flag) break;
+            if (globaltimer() - t0 > timeout_ns) break;
+        }
+    }
+    if (ok) fence_acq_rel_cluster();
+    return ok;
+}
+
+// Bulk copy from this CTA's shared memory to another CTA's (both 16-byte aligned, bytes a
+// multiple of 16); the destination barrier (cluster-window address) receives the bytes.
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_caddr, const void* src, uint32_t bytes, uint32_t bar_caddr) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst_caddr), "r"(smem_u32(src)), "r"(bytes), "r"(bar_caddr)
+                 : "memory");
+}
+
+// Asynchronous 8-byte store into another CTA's shared memory, counted on its barrier.
+__device__ __forceinline__ void st_async_f2(uint32_t dst_caddr, float x, float y, uint32_t bar_caddr) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 ::"r"(dst_caddr), "f"(x), "f"(y), "r"(bar_caddr)
+                 : "memory");
+}
+
+// Register budget of the executing warpgroup (every warp of the group runs the same one).
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
 // ---------------------------------------------------------------- TMA
 
@@ -199,6 +303,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+// 32 lanes x 16 columns of 32-bit: thread i of the warp gets lane (base + i), columns [col, col+16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -238,6 +352,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 constexpr uint32_t kSwizzle128 = 2;
+constexpr uint32_t kNoSwizzle = 0;   // interleaved 8-row x 16-byte core matrices
 
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32
 // accumulator. a_mn / b_mn select the MN-major (transposed) operand layout.
