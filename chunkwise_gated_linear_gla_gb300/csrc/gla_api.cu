@@ -68,7 +68,8 @@ gla_status validate_args(const gla_fwd_params* p)
         return GLA_ERR_INVALID_ARG;
     if ((p->gate == GLA_GATE_BILINEAR) != (p->log_b != nullptr) && !(p->gate == GLA_GATE_BILINEAR && p->T == 0))
         return GLA_ERR_INVALID_ARG;
-    if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT)
+    if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT &&
+        p->path != GLA_PATH_STAGED && p->path != GLA_PATH_FUSED)
         return GLA_ERR_INVALID_ARG;
     if (p->force_segments < 0) return GLA_ERR_INVALID_ARG;
     if (p->dk % 16 != 0 || p->dv % 16 != 0) return GLA_ERR_INVALID_ARG;
@@ -161,8 +162,21 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
         pl.stages[0] = STAGE_COPY_STATE;
         return GLA_OK;
     }
+    if (p->path == GLA_PATH_FUSED) {
+        // the fused per-key pass: one kernel, no workspace, never a sequence split
+        if (!fused_shape_ok(*p) || (sms > 0 && !fused_available(p->dv))) return GLA_ERR_UNSUPPORTED;
+        pl.path = GLA_PATH_TENSOR;
+        pl.nchunks = (p->T + kChunk - 1) / kChunk;
+        pl.Tpad = pl.nchunks * kChunk;
+        pl.n_dvt = p->dv / kDvTile;
+        pl.sms = sms;
+        pl.nstages = 1;
+        pl.stages[0] = STAGE_FUSED;
+        pl.ws_bytes = 0;
+        return GLA_OK;
+    }
     bool want_tensor = false;
-    if (p->path == GLA_PATH_TENSOR) {
+    if (p->path == GLA_PATH_TENSOR || p->path == GLA_PATH_STAGED) {
         if (!tensor_shape_ok(p)) return GLA_ERR_UNSUPPORTED;
         want_tensor = true;
     } else if (p->path == GLA_PATH_AUTO) {
@@ -235,6 +249,7 @@ const char* stage_name(StageKind k)
     case STAGE_VALUE_PREP: return "gla_value_prep";
     case STAGE_SIMT_FLAGGED: return "gla_fwd_simt_flagged";
     case STAGE_CHUNK_FWD_HI: return "gla_chunk_fwd_keys_hi";
+    case STAGE_FUSED: return "gla_chunk_fused";
     }
     return "?";
 }
@@ -272,6 +287,7 @@ gla_status run_stage(const gla_fwd_params* p, const Plan& pl, int i, cudaStream_
                              p->dk == 512 ? 1 : 0);
         break;
     case STAGE_CHUNK_FWD_HI: e = launch_chunk_fwd(*p, pl, p->workspace, kModeFull, c->status, s, 2); break;
+    case STAGE_FUSED: e = launch_fused(*p, c->status, s); break;
     case STAGE_VALUE_PREP: e = launch_value_prep(*p, pl, p->workspace, s); break;
     case STAGE_SIMT_FLAGGED:
         e = launch_simt(*p, c->status, s, reinterpret_cast<const int*>(static_cast<uint8_t*>(p->workspace) + pl.off_flag));

@@ -45,6 +45,7 @@ enum StageKind {
     STAGE_VALUE_PREP = 6,  // bilinear gate: V (.) D', the chunks' column decays, range flags
     STAGE_SIMT_FLAGGED = 7,  // bilinear gate: the CUDA-core pass for the heads flagged out of range
     STAGE_CHUNK_FWD_HI = 8,  // dk = 512: the chunk pass over keys 256-511, adding the first half's partial O
+    STAGE_FUSED = 9,         // per-key gate, dk = 256: gate prep inside the chunk pass (one cluster per head)
 };
 
 struct Plan {
@@ -86,6 +87,11 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
 // partial; 2: keys 256-511, adding that partial)
 cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode,
                              int* status, cudaStream_t s, int kh = 0);
+// The fused per-key pass (gla_fused.cu): the shapes it takes, whether the device can run
+// its clusters, and the launch.
+bool fused_shape_ok(const gla_fwd_params& p);
+bool fused_available(int dv);
+cudaError_t launch_fused(const gla_fwd_params& p, int* status, cudaStream_t s);
 cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, int* status,
                             cudaStream_t s);

@@ -82,10 +82,29 @@ typedef enum {
 /* Which kernels run. AUTO picks the tcgen05 tensor-core path for bf16 inputs
  * with dk in {64,128,256} and dv a multiple of 128 (also dk = 512, as two
  * chunk passes over key halves, for every gate but the bilinear one), and the
- * fp32 CUDA-core path otherwise (always for fp32 inputs). Both compute the
+ * fp32 CUDA-core path otherwise (always for fp32 inputs). All compute the
  * same function. The forward pass takes any dk and dv that are multiples of
- * 16 with dk <= 768. */
-typedef enum { GLA_PATH_AUTO = 0, GLA_PATH_TENSOR = 1, GLA_PATH_SIMT = 2 } gla_path;
+ * 16 with dk <= 768.
+ *   GLA_PATH_TENSOR  the tensor-core path, as AUTO plans it (a gate-prep kernel
+ *                    writing Q (.) Lambda, K (.) Gamma, the chunk decays and the
+ *                    masked intra-chunk scores to the workspace, then the
+ *                    chunk-serial pass; a sequence split when B*H is small)
+ *   GLA_PATH_STAGED  the same, under its explicit name
+ *   GLA_PATH_FUSED   per-key gate, bf16, dk = 256, dv in {256, 512}, one pass
+ *                    over the sequence: one kernel in which a thread-block
+ *                    cluster of the head's dv-tile CTAs prepares the gates and
+ *                    scores itself and shares them through distributed shared
+ *                    memory; it needs no workspace (gla_fwd_workspace_size
+ *                    returns 0), at the cost of speed on this hardware (the
+ *                    cross-CTA exchange of every chunk sits on the chain).
+ *                    GLA_ERR_UNSUPPORTED for other shapes or gates. */
+typedef enum {
+    GLA_PATH_AUTO = 0,
+    GLA_PATH_TENSOR = 1,
+    GLA_PATH_SIMT = 2,
+    GLA_PATH_STAGED = 3,
+    GLA_PATH_FUSED = 4
+} gla_path;
 
 typedef struct {
     const void* q;          /* [B,H,T,dk] */

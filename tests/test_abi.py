@@ -154,8 +154,24 @@ def test_plan_on_host():
     p = _params(dk=256, dv=512, T=2048, B=8, H=4, q=0x1000000, k=0x9000000, v=0x11000000,
                 log_g=0x21000000, O=0x31000000)
     names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
-    assert names[0] == "gla_chunk_prep" and names[-1] == "gla_chunk_fwd"
+    assert names == ["gla_chunk_prep", "gla_chunk_fwd"]
     assert bnd.gla_fwd_workspace_size(p) > 0
+    # the fused per-key pass on request: one kernel, no workspace, never a sequence split
+    p.path = bnd.GLA_PATH_FUSED
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_fused"]
+    assert bnd.gla_fwd_workspace_size(p) == 0
+    p.force_segments = 4
+    assert [bnd.gla_fwd_stage_name(p, 0)] == ["gla_chunk_fused"]
+    # shapes and gates it does not take
+    for kw in (dict(dk=128), dict(dv=1024), dict(gate=bnd.GLA_GATE_TOKEN_SCALAR), dict(dtype=bnd.GLA_FP32)):
+        q = _params(dk=256, dv=512, T=2048, B=8, H=4, q=0x1000000, k=0x9000000, v=0x11000000,
+                    log_g=0x21000000, O=0x31000000, path=bnd.GLA_PATH_FUSED)
+        for key, val in kw.items():
+            setattr(q, key, val)
+        assert bnd.gla_fwd_num_stages(q) == -1 and bnd.gla_fwd_ex(q, stream=0, check=False) == bnd.GLA_ERR_UNSUPPORTED
+    p = _params(dk=256, dv=512, T=2048, B=8, H=4, q=0x1000000, k=0x9000000, v=0x11000000,
+                log_g=0x21000000, O=0x31000000)
     # forced segments add the state pass and the scan
     p.force_segments = 4
     names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
@@ -209,8 +225,15 @@ def test_bench_segment_rule_matches_library_plan():
         nch = (w.T + 63) // 64
         base = (0 if w.gate == 0 else 2 * BH * nch * 64 * w.dk * 2) + BH * nch * 64 * 64 * 2 + BH * nch * w.dk * 4
         seg = 2 * BH * nseg * w.dk * w.dv * 4 if nseg > 1 else 0
+        assert bnd.gla_fwd_workspace_size(p) == got_staged(p), name
         got = bnd.gla_fwd_workspace_size(p)
         assert abs(got - (base + seg)) < 4096, (name, got, base + seg, nseg)
+
+
+def got_staged(p):
+    q = bnd.gla_fwd_params.from_buffer_copy(p)
+    q.path = bnd.GLA_PATH_STAGED
+    return bnd.gla_fwd_workspace_size(q)
 
 
 def test_plan_bilinear_on_host():
