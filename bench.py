@@ -55,6 +55,9 @@ def parse():
                     help="batch rows of the workload the oracle runs for cpu_baseline")
     ap.add_argument("--ref-sample-rows", type=int, default=1,
                     help="batch rows per step of the reference arm")
+    ap.add_argument("--other-workloads", default="linear_attn,scalar_decay,gla_long",
+                    help="bf16 configurations also timed (same discipline) and reported inside the line "
+                         "under config.other_workloads; empty: none")
     return ap.parse_args()
 
 
@@ -112,6 +115,9 @@ def stage_bytes(w, name, nseg=1):
     st = BH * dk * dv * 4
     qk_tiles = (Tp if gated else T) * dk * 2 * 2
     gam = nch * dk * 4 if gated else 0
+    if name == "gla_chunk_fused":
+        # the whole pass in one kernel: q, k, v, the log gate read once, O written once, S0 / S_T
+        return algorithmic(w)[1]
     if name == "gla_chunk_prep":
         # per-head decay with dk <= 128: chunks whose decay stays within e^-60 (every chunk of the
         # workloads' lambda_h) leave Q (.) Lambda to the chunk pass, so only K (.) Gamma is written
@@ -154,7 +160,8 @@ def planned_segments(w, force, sms):
 
 
 def kernel_source_sha(name):
-    files = {"gla_chunk_fwd": ["gla_chunk_fwd.cu", "sm100.cuh"],
+    files = {"gla_chunk_fused": ["gla_fused.cu", "sm100.cuh"],
+             "gla_chunk_fwd": ["gla_chunk_fwd.cu", "sm100.cuh"],
              "gla_chunk_fwd_keys_hi": ["gla_chunk_fwd.cu", "sm100.cuh"],
              "gla_chunk_prep": ["gla_prep.cu", "sm100.cuh"],
              "gla_chunk_state": ["gla_state.cu", "sm100.cuh"],
@@ -442,6 +449,73 @@ def run_backward(args, w):
     print(json.dumps(line), flush=True)
 
 
+def time_plan(bnd, p, steps, warmup, stream, flush_l2, record_clocks=None):
+    """Times the plan of params p stage by stage with CUDA events on `stream`: `warmup`
+    untimed steps, then `steps` timed ones, L2 flushed before each (outside the events).
+    Returns (stage names, mean ms per stage, mean ms per step, sorted per-step ms)."""
+    import torch
+    nst = bnd.gla_fwd_num_stages(p)
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(nst)]
+
+    def step(evs=None):
+        for i in range(nst):
+            if evs is not None:
+                evs[i].record(stream)
+            bnd.gla_fwd_stage(p, i, stream)
+        if evs is not None:
+            evs[nst].record(stream)
+
+    for _ in range(warmup):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    if bnd.gla_device_status(stream) != 0:
+        raise SystemExit("device status error after warm-up")
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    if record_clocks:
+        record_clocks.start()
+    torch.cuda.synchronize()
+    for s in range(steps):
+        flush_l2()
+        step(evsets[s])
+    torch.cuda.synchronize()
+    clk = record_clocks.stop() if record_clocks else None
+    if bnd.gla_device_status(stream) != 0:
+        raise SystemExit("device status error in timed region")
+    stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evsets) / steps for i in range(nst)]
+    per = sorted(e[0].elapsed_time(e[nst]) for e in evsets)
+    return names, stage_ms, sum(per) / steps, per, clk
+
+
+def other_workloads(bnd, gi, names_csv, args, dev, stream, flush_l2, hbm):
+    """The other bf16 configurations, timed like the headline one and summarised."""
+    import torch
+    out = {}
+    for name in [n for n in names_csv.split(",") if n]:
+        w = gi.WORKLOADS[name]
+        x = gi.make_inputs(w, seed=0)
+        c = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+        O = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev)
+        ST = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+        p = bnd.make_params(c["q"], c["k"], c["v"], c["log_g"], c["S0"], O, ST, gate=x["gate"])
+        nb = bnd.gla_fwd_workspace_size(p)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+        p.workspace, p.workspace_bytes = ws.data_ptr(), nb
+        names, stage_ms, ms, per, _ = time_plan(bnd, p, min(args.steps, 20), max(3, min(args.warmup, 5)),
+                                               stream, flush_l2)
+        flops, byts = algorithmic(w)
+        out[name] = {"shape": f"B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}",
+                     "gate": ["none", "per-head scalar", "per-key", "per-token scalar", "bilinear"][w.gate],
+                     "ms_per_step": ms, "median_ms": per[len(per) // 2],
+                     "tokens_per_s": w.B * w.T / (ms * 1e-3),
+                     "tflops": flops / (ms * 1e-3) / 1e12,
+                     "algorithmic_bytes": byts, "path_frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm,
+                     "stages": names, "stage_ms": stage_ms, "workspace_bytes": nb}
+        del c, O, ST, ws, p
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     from chunkwise_gated_linear_gla_gb300 import inputs as gi
@@ -584,11 +658,26 @@ def main():
                 float((got.float() - r).norm()) > 5e-3 * max(float(r.norm()), 1e-30):
             raise SystemExit("gla_fwd_host result differs from the device-path result")
 
+    hbm, bf16, bf16_sus, src = peaks()
+    others = None
+    if rank == 0 and world == 1 and args.other_workloads and w.name == WORKLOAD and not args.shape:
+        others = other_workloads(bnd, gi, args.other_workloads, args, dev, stream, flush_l2, hbm)
+    # the same workload through the fused path (one kernel, no workspace), where it applies
+    fused = None
+    if rank == 0 and world == 1 and args.segments == 0:
+        pf = bnd.make_params(q, k, v, g, S0, O, ST, log_b=lb, path=bnd.GLA_PATH_FUSED)
+        if bnd.gla_fwd_num_stages(pf) == 1:
+            fnames, fstage, fms, fper, _ = time_plan(bnd, pf, min(args.steps, 20), max(3, min(args.warmup, 5)),
+                                                     stream, flush_l2)
+            fused = {"path": "GLA_PATH_FUSED", "stages": fnames, "ms_per_step": fms,
+                     "median_ms": fper[len(fper) // 2], "tokens_per_s": w.B * w.T / (fms * 1e-3),
+                     "path_frac_hbm": algorithmic(w)[1] / (fms * 1e-3) / 1e9 / hbm, "workspace_bytes": 0,
+                     "note": "opt-in path: the gate prep inside the chunk pass, shared by a cluster of the "
+                             "head's dv-tile CTAs through distributed shared memory; not the value's basis"}
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
-    hbm, bf16, bf16_sus, src = peaks()
     flops, byts = algorithmic(w)
     tokens = w.B * w.T * world
     value = job_tokens_per_s(w.B * w.T, world, step_ms)
@@ -597,8 +686,6 @@ def main():
     dname = names[dom]
     nseg = planned_segments(w, args.segments, torch.cuda.get_device_properties(dev).multi_processor_count) \
         if "gla_chunk_state" in names else 1
-    dbytes = stage_bytes(w, dname, nseg)
-    ach = dbytes / (stage_ms[dom] * 1e-3) / 1e9
     if dname == "gla_fwd_simt":
         # the CUDA-core pass: fp32 FFMA work against the nominal FFMA rate
         alu = flops / (stage_ms[dom] * 1e-3) / 1e12
@@ -607,9 +694,22 @@ def main():
                 "peak_source": "nominal fp32 FFMA rate: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
                 "flops_per_launch": flops}
     else:
-        roof = {"kernel": dname, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "traffic": ncu_traffic(w.name, dname), "peak_source": src,
-                "bytes_per_launch": dbytes}
+        # achieved = the method's algorithmic bytes (q, k, v, log gate in; O out; S0 in, S_T out)
+        # over the time of the kernels that move them: the one launch of a one-kernel plan, the
+        # whole step otherwise (each kernel's own compulsory bytes are listed separately)
+        span_ms = stage_ms[0] if nst == 1 else step_ms
+        ach = byts / (span_ms * 1e-3) / 1e9
+        per_kernel = [{"kernel": n, "ms": t, "compulsory_bytes": stage_bytes(w, n, nseg),
+                       "compulsory_gbs": stage_bytes(w, n, nseg) / (t * 1e-3) / 1e9,
+                       "dram_bytes_ncu": ncu_traffic(w.name, n)} for n, t in zip(names, stage_ms)]
+        tr = [k["dram_bytes_ncu"] for k in per_kernel]
+        traffic = sum(tr) if tr and all(t is not None for t in tr) else None
+        roof = {"kernel": names[0] if nst == 1 else "+".join(names), "bound": "hbm", "achieved": ach,
+                "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
+                "traffic_over_algorithmic": None if traffic is None else traffic / byts,
+                "peak_source": src, "bytes_per_launch": byts,
+                "bytes_basis": "algorithmic: q, k, v, log gate read once, O written once, S0 read, S_T written",
+                "kernels": per_kernel}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -620,7 +720,7 @@ def main():
                                f"S0={'given' if w.s0_std > 0 else 'zero'}",
                    "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "segments": nseg,
                    "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",
-                   "stages": names, "stage_ms": stage_ms},
+                   "stages": names, "stage_ms": stage_ms, "other_workloads": others, "fused_path": fused},
         "tflops": tflops, "tflops_frac_bf16_peak": tflops / bf16,
         "path_gbs": byts * world / (step_ms * 1e-3) / 1e9, "path_frac_hbm": byts / (step_ms * 1e-3) / 1e9 / hbm,
         "roofline": roof,
