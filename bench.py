@@ -165,6 +165,7 @@ def kernel_source_sha(name):
              "gla_chunk_fwd_keys_hi": ["gla_chunk_fwd.cu", "sm100.cuh"],
              "gla_chunk_prep": ["gla_prep.cu", "sm100.cuh"],
              "gla_chunk_state": ["gla_state.cu", "sm100.cuh"],
+             "gla_state_scan": ["gla_scan.cu"],
              "gla_value_prep": ["gla_vprep.cu"]}.get(name, [])
     h = hashlib.sha256()
     for f in files:
