@@ -168,3 +168,46 @@ def gla_forward_rows(q, k, v, log_g, gate, S0, bh_list, nthreads=None, log_b=Non
                             g1, gate, s1, True, nthreads, log_b=b1)
         out[(b, h)] = (O[0, 0], ST[0, 0])
     return out
+
+
+def segment_pair(k, v, log_g=None, gate=None):
+    """The exchange pair of one sequence segment ("Gated Linear Attention Transformers
+    with Hardware-Efficient Training", §2.2: the state a segment hands to the next).
+
+    log_Gamma [B,H,dk]: the sum over the segment's tokens of log alpha_t per key (the
+    log of the product of the gates; T log lambda_h for a per-head gate, 0 without one).
+    S_star [B,H,dk,dv]: the recurrence's final state from S0 = 0 (q does not enter it).
+    Both fp64 numpy arrays; not for the bilinear gate.
+    """
+    ka, va = _f64(k), _f64(v)
+    B, H, T, dk = ka.shape
+    if gate is None:
+        gate = GATE_NONE if log_g is None else {1: GATE_HEAD_SCALAR, 3: GATE_TOKEN_SCALAR}.get(
+            np.ndim(_f64(log_g)), GATE_PER_KEY)
+    if gate == GATE_BILINEAR:
+        raise ValueError("the bilinear gate's decay is a dk x dv matrix, not a key vector")
+    _, S_star = gla_forward(ka, ka, va, log_g, gate, None)
+    ga = None if gate == GATE_NONE else _f64(log_g)
+    if gate == GATE_NONE:
+        lg = np.zeros((B, H, dk))
+    elif gate == GATE_HEAD_SCALAR:
+        lg = np.broadcast_to((T * ga)[None, :, None], (B, H, dk)).copy()
+    elif gate == GATE_PER_KEY:
+        lg = ga.sum(axis=2)
+    else:
+        lg = np.broadcast_to(ga.sum(axis=2)[..., None], (B, H, dk)).copy()
+    return lg, S_star
+
+
+def pair_scan(log_Gammas, S_stars, S0=None):
+    """The states entering P consecutive segments and the state after the last, from
+    their pairs in sequence order: S = S0 (or 0); for each segment d, S_in[d] = S and
+    S = Diag(exp(log_Gamma_d)) S + S*_d. Returns (S_in [P,B,H,dk,dv], S_T), fp64."""
+    lgs = [_f64(x) for x in log_Gammas]
+    sss = [_f64(x) for x in S_stars]
+    S = np.zeros_like(sss[0]) if S0 is None else _f64(S0).copy()
+    S_in = []
+    for lg, ss in zip(lgs, sss):
+        S_in.append(S.copy())
+        S = np.exp(lg)[..., None] * S + ss
+    return np.stack(S_in), S

@@ -487,3 +487,43 @@ def test_pins_catch_planted_mistakes(mutant):
                                      np.log(gd["alpha"])[None, None], oracle.GATE_PER_KEY,
                                      gd["S0"][None, None], mutant=mutant)
         assert max(np.abs(Og[0, 0] - gd["O"]).max(), np.abs(STg[0, 0] - gd["ST"]).max()) > 1e-6
+
+
+# ---------------------------------------------------------------- the sequence exchange pair
+
+@pytest.mark.parametrize("gate", [gi.GATE_PER_KEY, gi.GATE_HEAD_SCALAR, gi.GATE_TOKEN_SCALAR, gi.GATE_NONE])
+def test_segment_pair_is_the_segments_affine_map(gate):
+    """[GLA] §2.2: a segment run from any S0 ends in Diag(Gamma) S0 + S*, Gamma the product of
+    the gates and S* the zero-start state. Checked against the recurrence run from two
+    different S0 (so a wrong Gamma, e.g. a dropped token or a sign, fails)."""
+    q, k, v, g, gt, S0 = _case(B=2, H=2, T=45, dk=6, dv=5, gate=gate, s0=0.7, seed=41)
+    lg, Sst = oracle.segment_pair(k, v, g, gt)
+    for s0 in (S0, -2.0 * S0 + 0.25):
+        _, ST = oracle.gla_forward(q, k, v, g, gt, s0)
+        np.testing.assert_allclose(ST, np.exp(lg)[..., None] * s0 + Sst, rtol=0, atol=1e-12)
+    # the zero-start state does not depend on q
+    _, ST0 = oracle.gla_forward(np.zeros_like(q), k, v, g, gt, None)
+    np.testing.assert_array_equal(ST0, Sst)
+
+
+def test_segment_pair_of_an_empty_segment_is_the_identity():
+    k = np.zeros((1, 2, 0, 4)); v = np.zeros((1, 2, 0, 3))
+    lg, Sst = oracle.segment_pair(k, v, np.zeros((1, 2, 0, 4)), oracle.GATE_PER_KEY)
+    np.testing.assert_array_equal(lg, 0.0)
+    np.testing.assert_array_equal(Sst, 0.0)
+
+
+@pytest.mark.parametrize("cuts", [[], [1], [17, 64], [5, 6, 40, 77]])
+def test_pair_scan_chains_segments_into_the_whole_sequence(cuts):
+    """Pairs of consecutive segments, chained by the scan, give the recurrence's state at
+    every segment boundary of the whole sequence (the FlashQLA talk, "core technical
+    principles": one correction per segment after a serial recurrence over segments)."""
+    q, k, v, g, gt, S0 = _case(B=1, H=2, T=90, dk=6, dv=5, s0=0.4, seed=43)
+    edges = [0] + cuts + [90]
+    pairs = [oracle.segment_pair(k[:, :, a:b], v[:, :, a:b], g[:, :, a:b], gt) for a, b in zip(edges, edges[1:])]
+    S_in, S_T = oracle.pair_scan([p[0] for p in pairs], [p[1] for p in pairs], S0)
+    for d, a in enumerate(edges[:-1]):
+        _, S_a = oracle.gla_forward(q[:, :, :a], k[:, :, :a], v[:, :, :a], g[:, :, :a], gt, S0)
+        np.testing.assert_allclose(S_in[d], S_a, rtol=0, atol=1e-12)
+    _, ST = oracle.gla_forward(q, k, v, g, gt, S0)
+    np.testing.assert_allclose(S_T, ST, rtol=0, atol=1e-12)
