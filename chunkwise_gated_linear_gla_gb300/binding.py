@@ -22,7 +22,8 @@ GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT, GLA_PATH_STAGED, GLA_PATH_FUSED =
 EXPORTED = ("gla_fwd", "gla_fwd_ex", "gla_fwd_workspace_size", "gla_fwd_num_stages",
             "gla_fwd_stage", "gla_fwd_stage_name", "gla_device_status", "gla_status_string",
             "gla_version", "gla_fwd_noalloc", "gla_fwd_host", "gla_host_release", "gla_bwd",
-            "gla_bwd_workspace_size")
+            "gla_bwd_workspace_size", "gla_segment_pair_workspace_size", "gla_segment_pair",
+            "gla_pair_scan", "gla_pair_combine", "gla_selftest_bounded_wait")
 
 
 class GlaError(RuntimeError):
@@ -112,6 +113,16 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.gla_status_string.argtypes = [st]
         lib.gla_version.restype = i
         lib.gla_version.argtypes = []
+        lib.gla_segment_pair_workspace_size.restype = ctypes.c_size_t
+        lib.gla_segment_pair_workspace_size.argtypes = [P]
+        lib.gla_segment_pair.restype = st
+        lib.gla_segment_pair.argtypes = [P, vp, vp, vp]
+        lib.gla_pair_scan.restype = st
+        lib.gla_pair_scan.argtypes = [i, vp, vp, vp, vp, vp, i, i, i, i, vp]
+        lib.gla_selftest_bounded_wait.restype = st
+        lib.gla_selftest_bounded_wait.argtypes = [ctypes.c_uint, i, vp]
+        lib.gla_pair_combine.restype = st
+        lib.gla_pair_combine.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
         _lib = lib
         return lib
 
@@ -283,6 +294,40 @@ def gla_version() -> int:
     return int(load().gla_version())
 
 
+def gla_segment_pair_workspace_size(p: gla_fwd_params) -> int:
+    return int(load().gla_segment_pair_workspace_size(ctypes.byref(p)))
+
+
+def gla_segment_pair(p: gla_fwd_params, log_Gamma, S_star, stream=None, check=True) -> int:
+    s = load().gla_segment_pair(ctypes.byref(p), _ptr(log_Gamma), _ptr(S_star), _stream(stream))
+    if check:
+        _check(s, "gla_segment_pair")
+    return s
+
+
+def gla_pair_scan(P, log_Gamma, S_star, S0, S_in, S_T, B, H, dk, dv, stream=None, check=True) -> int:
+    s = load().gla_pair_scan(P, _ptr(log_Gamma), _ptr(S_star), _ptr(S0), _ptr(S_in), _ptr(S_T),
+                             B, H, dk, dv, _stream(stream))
+    if check:
+        _check(s, "gla_pair_scan")
+    return s
+
+
+def gla_pair_combine(log_Gamma2, S2, log_Gamma1, S1, B, H, dk, dv, stream=None, check=True) -> int:
+    s = load().gla_pair_combine(_ptr(log_Gamma2), _ptr(S2), _ptr(log_Gamma1), _ptr(S1), B, H, dk, dv,
+                                _stream(stream))
+    if check:
+        _check(s, "gla_pair_combine")
+    return s
+
+
+def gla_selftest_bounded_wait(limit_us: int, arrive: bool = False, stream=None, check=True) -> int:
+    s = load().gla_selftest_bounded_wait(int(limit_us), 1 if arrive else 0, _stream(stream))
+    if check:
+        _check(s, "gla_selftest_bounded_wait")
+    return s
+
+
 # ---------------------------------------------------------------- marshalling helpers
 
 def make_params(q, k, v, log_g, S0, O, ST, gate=None, path=GLA_PATH_AUTO, force_segments=0,
@@ -339,3 +384,48 @@ def forward(q, k, v, log_g=None, S0=None, gate=None, want_state=True, path=GLA_P
         p.workspace_bytes = nbytes
     gla_fwd_ex(p, stream)
     return O, ST
+
+
+def _aligned_workspace(nbytes, device):
+    import torch
+    if nbytes == 0:
+        return None
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + nbytes]
+
+
+def segment_pair(k, v, log_g=None, gate=None, q=None, path=GLA_PATH_AUTO, stream=None):
+    """The exchange pair (log Gamma [B,H,dk], S* [B,H,dk,dv], both fp32) of the segment
+    whose k, v, gate are given, from a zero start (gla_segment_pair)."""
+    import torch
+    B, H, T, dk = k.shape
+    dv = v.shape[-1]
+    log_G = torch.empty((B, H, dk), dtype=torch.float32, device=k.device)
+    S_star = torch.empty((B, H, dk, dv), dtype=torch.float32, device=k.device)
+    p = make_params(k, k, v, log_g, None, None, None, gate, path)
+    p.q = _ptr(q)
+    ws = _aligned_workspace(gla_segment_pair_workspace_size(p), k.device)
+    if ws is not None:
+        p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    gla_segment_pair(p, log_G, S_star, stream)
+    return log_G, S_star
+
+
+def pair_scan(log_Gamma, S_star, S0=None, want_S_in=True, stream=None):
+    """States entering each of P segments and after the last, from pairs stacked in
+    sequence order (log_Gamma [P,B,H,dk], S_star [P,B,H,dk,dv]): (S_in [P,...] or None, S_T)."""
+    import torch
+    P, B, H, dk = log_Gamma.shape
+    dv = S_star.shape[-1]
+    S_in = torch.empty_like(S_star) if want_S_in else None
+    S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=S_star.device)
+    gla_pair_scan(P, log_Gamma, S_star, S0, S_in, S_T, B, H, dk, dv, stream)
+    return S_in, S_T
+
+
+def pair_combine(log_Gamma2, S2, log_Gamma1, S1, stream=None):
+    """In place: (log_Gamma1, S1) <- (log_Gamma2, S2) o (log_Gamma1, S1); pair 1 is the earlier segment."""
+    B, H, dk, dv = S1.shape
+    gla_pair_combine(log_Gamma2, S2, log_Gamma1, S1, B, H, dk, dv, stream)
+    return log_Gamma1, S1

@@ -296,6 +296,71 @@ gla_status run_stage(const gla_fwd_params* p, const Plan& pl, int i, cudaStream_
     return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }
 
+// The sequence-exchange pair of one segment: the call's parameters as the segment's
+// forward pass sees them, and where each part of the work goes.
+struct PairPlan {
+    gla_fwd_params pp;     // *p with S0 = none, ST = S_star, q = k when absent
+    bool tensor = false;   // gate prep + state-only pass (else the CUDA-core pass, O discarded)
+    Plan pl;               // tensor route: the prep's workspace layout, one segment
+    size_t off_o = 0;      // CUDA-core route: the discarded O
+    size_t off_sum = 0;    // the log gate's partial sums
+    size_t ws_bytes = 0;
+};
+
+// shapes_only: check sizes, modes and which inputs are present, not the pointer values
+// (the workspace query, which gets no output pointers).
+gla_status plan_pair(const gla_fwd_params* p, const float* log_Gamma, const float* S_star, int sms, PairPlan& pp,
+                     bool shapes_only = false)
+{
+    if (!p || (!shapes_only && (!log_Gamma || !S_star))) return GLA_ERR_INVALID_ARG;
+    if (p->gate == GLA_GATE_BILINEAR) return GLA_ERR_UNSUPPORTED;   // its decay is a dk x dv matrix
+    gla_fwd_params& q = pp.pp;
+    q = *p;
+    q.S0 = nullptr;
+    q.ST = const_cast<float*>(S_star);
+    q.force_segments = 1;
+    if (!q.q) q.q = q.k;   // read by the gate prep; the pair does not depend on it
+    // presence checks want an O; the pair never writes the caller's
+    q.O = const_cast<void*>(q.v);
+    gla_status st = validate_args(&q);
+    if (st != GLA_OK) return st;
+    q.O = nullptr;
+    const size_t BH = (size_t)q.B * q.H;
+    const size_t e = q.dtype == GLA_BF16 ? 2 : 4;
+    if (!shapes_only) {
+        st = validate_pointers(&q, true);
+        if (st != GLA_OK) return st;
+        if (!aligned(log_Gamma, 4)) return GLA_ERR_INVALID_ARG;
+        const Range rG = rng(log_Gamma, BH * q.dk * 4);
+        const size_t ng = q.gate == GLA_GATE_PER_KEY ? BH * q.T * q.dk * 4
+                        : q.gate == GLA_GATE_TOKEN_SCALAR ? BH * q.T * 4
+                        : q.gate == GLA_GATE_HEAD_SCALAR ? (size_t)q.H * 4 : 0;
+        const Range ins[] = {rng(p->q, BH * q.T * q.dk * e), rng(q.k, BH * q.T * q.dk * e),
+                             rng(q.v, BH * q.T * q.dv * e), rng(q.log_g, ng), rng(S_star, BH * q.dk * q.dv * 4)};
+        for (const Range& r : ins) if (overlap(rG, r)) return GLA_ERR_INVALID_ARG;
+    }
+    size_t off = 0;
+    pp.tensor = q.T > 0 && p->path != GLA_PATH_SIMT && tensor_shape_ok(&q) && q.dk <= kMaxDk;
+    if (q.T > 0) {
+        if (pp.tensor) {
+            gla_fwd_params t = q;
+            t.O = const_cast<void*>(q.v);   // placeholder for the presence check; prep and state ignore O
+            t.path = GLA_PATH_STAGED;
+            st = make_plan(&t, pp.pl, sms);
+            if (st != GLA_OK) return st;
+            if (pp.pl.nseg != 1) return GLA_ERR_UNSUPPORTED;
+            off = pp.pl.ws_bytes;
+        } else {
+            pp.off_o = off;
+            off = align_up(off + BH * q.T * q.dv * e, 256);
+        }
+    }
+    pp.off_sum = off;
+    off = align_up(off + seg_logsum_ws_bytes(q), 256);
+    pp.ws_bytes = off;
+    return GLA_OK;
+}
+
 }  // namespace
 
 gla_status plan_workspace(const gla_fwd_params* p, size_t* bytes)
@@ -394,6 +459,87 @@ gla_status gla_fwd(const void* q, const void* k, const void* v, const float* log
         if (cudaFreeAsync(ws, stream) != cudaSuccess && st == GLA_OK) st = GLA_ERR_CUDA;
     }
     return st;
+}
+
+size_t gla_segment_pair_workspace_size(const gla_fwd_params* p)
+{
+    PairPlan pp;
+    if (plan_pair(p, nullptr, nullptr, device_sms(), pp, true) != GLA_OK) return 0;
+    return pp.ws_bytes;
+}
+
+gla_status gla_segment_pair(const gla_fwd_params* p, float* log_Gamma, float* S_star, cudaStream_t stream)
+{
+    PairPlan pp;
+    gla_status st = plan_pair(p, log_Gamma, S_star, device_sms(), pp);
+    if (st != GLA_OK) return st;
+    DevCache* c = dev_cache();
+    if (!c) return GLA_ERR_CUDA;
+    if (c->major != 10 || c->minor != 3) return GLA_ERR_UNSUPPORTED;
+    gla_fwd_params& q = pp.pp;
+    if (pp.ws_bytes > 0 && (!p->workspace || p->workspace_bytes < pp.ws_bytes)) return GLA_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+    const size_t ns = (size_t)q.B * q.H * q.dk * q.dv * 4;
+    cudaError_t e = cudaSuccess;
+    if (q.T == 0) {
+        e = cudaMemsetAsync(S_star, 0, ns, stream);
+    } else if (pp.tensor) {
+        e = launch_prep(q, pp.pl, ws, c->status, stream);
+        if (e == cudaSuccess) e = launch_seg_state(q, pp.pl, ws, c->status, stream, S_star);
+    } else {
+        q.O = ws + pp.off_o;
+        e = launch_simt(q, c->status, stream);
+    }
+    if (e == cudaSuccess) e = launch_seg_logsum(q, log_Gamma, ws ? ws + pp.off_sum : nullptr, stream);
+    return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+gla_status gla_pair_scan(int P, const float* log_Gamma, const float* S_star, const float* S0, float* S_in,
+                         float* S_T, int B, int H, int dk, int dv, cudaStream_t stream)
+{
+    if (P < 0 || B <= 0 || H <= 0 || dk <= 0 || dv <= 0) return GLA_ERR_INVALID_ARG;
+    if (P > 0 && (!log_Gamma || !S_star)) return GLA_ERR_INVALID_ARG;
+    if (!S_in && !S_T) return GLA_ERR_INVALID_ARG;
+    const size_t BH = (size_t)B * H, ns = BH * dk * dv * 4;
+    for (const void* ptr : {(const void*)log_Gamma, (const void*)S_star, (const void*)S0, (const void*)S_in,
+                            (const void*)S_T})
+        if (ptr && !aligned(ptr, 4)) return GLA_ERR_INVALID_ARG;
+    const Range rG = rng(log_Gamma, P * BH * dk * 4), rS = rng(S_star, P * ns), r0 = rng(S0, S0 ? ns : 0);
+    const Range rI = rng(S_in, S_in ? P * ns : 0), rT = rng(S_T, S_T ? ns : 0);
+    // S_in may be S_star exactly and S_T may be S0 exactly (each element is read before it is written)
+    if (overlap(rI, rG) || overlap(rI, r0) || overlap(rI, rT)) return GLA_ERR_INVALID_ARG;
+    if (overlap(rI, rS) && (const void*)S_in != (const void*)S_star) return GLA_ERR_INVALID_ARG;
+    if (overlap(rT, rG) || overlap(rT, rS)) return GLA_ERR_INVALID_ARG;
+    if (overlap(rT, r0) && (const void*)S_T != (const void*)S0) return GLA_ERR_INVALID_ARG;
+    if (!dev_cache()) return GLA_ERR_CUDA;
+    return launch_pair_scan(P, log_Gamma, S_star, S0, S_in, S_T, (long long)BH, dk, dv, device_sms(), stream) ==
+                   cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+gla_status gla_pair_combine(const float* log_Gamma2, const float* S2, float* log_Gamma1, float* S1,
+                            int B, int H, int dk, int dv, cudaStream_t stream)
+{
+    if (!log_Gamma2 || !S2 || !log_Gamma1 || !S1 || B <= 0 || H <= 0 || dk <= 0 || dv <= 0)
+        return GLA_ERR_INVALID_ARG;
+    for (const void* ptr : {(const void*)log_Gamma2, (const void*)S2, (const void*)log_Gamma1, (const void*)S1})
+        if (!aligned(ptr, 4)) return GLA_ERR_INVALID_ARG;
+    const size_t BH = (size_t)B * H, ns = BH * dk * dv * 4, ng = BH * dk * 4;
+    const Range a[] = {rng(log_Gamma2, ng), rng(S2, ns)}, b[] = {rng(log_Gamma1, ng), rng(S1, ns)};
+    for (const Range& x : a)
+        for (const Range& y : b) if (overlap(x, y)) return GLA_ERR_INVALID_ARG;
+    if (overlap(b[0], b[1])) return GLA_ERR_INVALID_ARG;
+    if (!dev_cache()) return GLA_ERR_CUDA;
+    return launch_pair_combine(log_Gamma2, S2, log_Gamma1, S1, (long long)BH, dk, dv, device_sms(), stream) ==
+                   cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+gla_status gla_selftest_bounded_wait(unsigned limit_us, int arrive, cudaStream_t stream)
+{
+    if (limit_us == 0 || limit_us > 1000000u) return GLA_ERR_INVALID_ARG;
+    DevCache* c = dev_cache();
+    if (!c) return GLA_ERR_CUDA;
+    if (c->major != 10 || c->minor != 3) return GLA_ERR_UNSUPPORTED;
+    return launch_wait_selftest(c->status, limit_us, arrive != 0, stream) == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
 }
 
 gla_status gla_device_status(cudaStream_t stream)

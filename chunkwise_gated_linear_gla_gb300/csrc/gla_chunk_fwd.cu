@@ -147,6 +147,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     uint64_t* sb_ready = bar + 11; // bf16 state copy written (256 arrivals)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 13);
+    uint64_t* mma_fin = bar + 14;  // every MMA of the CTA complete (the issuer's last commit)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.y, seg = blockIdx.z;
@@ -167,6 +168,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         mbar_init(s_ready, NEPI); mbar_init(s_done, 1); mbar_init(sb_free, 1); mbar_init(sb_ready, NEPI);
         mbar_init(&o_full[0], 1); mbar_init(&o_full[1], 1);
         mbar_init(&o_empty[0], NEPI); mbar_init(&o_empty[1], NEPI);
+        mbar_init(mma_fin, 1);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tmap(&tmQ); prefetch_tmap(&tmK); prefetch_tmap(&tmV); prefetch_tmap(&tmA); prefetch_tmap(&tmO);
@@ -303,6 +305,10 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 }
                 mma_commit(&empty[st]);
             }
+            // one last commit tracks every MMA issued above: after an abort as on the normal
+            // path, none may still run when the TMEM is freed at the end
+            mma_commit(mma_fin);
+            mbar_wait(mma_fin, 0, kTimeoutNs);
         }
     } else {
         // ---------------------------------------------------------- epilogue warps (2 groups of 4)

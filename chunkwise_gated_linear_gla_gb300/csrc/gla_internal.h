@@ -92,9 +92,26 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
 bool fused_shape_ok(const gla_fwd_params& p);
 bool fused_available(int dv);
 cudaError_t launch_fused(const gla_fwd_params& p, int* status, cudaStream_t s);
-cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
+// launch_seg_state: with S_out non-null and a one-segment plan, the segment's state goes
+// there ([BH][dk][dv]) instead of the workspace.
+cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s,
+                             float* S_out = nullptr);
 cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, int* status,
                             cudaStream_t s);
+
+// The sequence exchange (gla_seqpar.cu): log Gamma of a segment (the per-key sum of the log
+// gate; ws holds seg_logsum_ws_bytes(p) bytes, 8-byte aligned), the recurrence over P pairs,
+// and one composition of two pairs.
+size_t seg_logsum_ws_bytes(const gla_fwd_params& p);
+cudaError_t launch_seg_logsum(const gla_fwd_params& p, float* log_Gamma, void* ws, cudaStream_t s);
+cudaError_t launch_pair_scan(int P, const float* log_G, const float* S_star, const float* S0, float* S_in,
+                             float* S_T, long long BH, int dk, int dv, int sms, cudaStream_t s);
+cudaError_t launch_pair_combine(const float* log_G2, const float* S2, float* log_G1, float* S1, long long BH,
+                                int dk, int dv, int sms, cudaStream_t s);
+
+// One warp waiting, with the pipelined kernels' bounded mbarrier wait, on a barrier that
+// nothing arrives on (unless `arrive`): a timeout recorded in the status word (gla_selftest.cu).
+cudaError_t launch_wait_selftest(int* status, unsigned limit_us, bool arrive, cudaStream_t s);
 
 // chunk_fwd modes
 constexpr int kModeFull = 0;        // O and final state from S0 (single segment)

@@ -181,7 +181,12 @@ gla_chunk_state_kernel(StateArgs a, const __grid_constant__ CUtensorMap tmK, con
                            sdesc(sb + L::K_OFF + kk * 2048, 8192, 1024, kSwizzle128), id_state, (j > 0 || kk > 0));
                 mma_commit(&empty[st]);
             }
-            if (ok) mma_commit(done);
+            // the commit tracks every MMA issued above; the lane waits for it, so that on an
+            // abort as on the normal path no MMA still runs when the TMEM is freed (the
+            // readout warps also check the abort flag before they trust `done`)
+            mma_commit(done);
+            mbar_wait(done, 0, kTimeoutNs);
+            (void)ok;
         }
     } else {
         // ---------------------------------------------------------- K scaling, then the state readout
@@ -288,8 +293,10 @@ cudaError_t launch_state_dk(const StateArgs& a, dim3 grid, const CUtensorMap& k,
 
 }  // namespace
 
-cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s)
+cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s,
+                             float* S_out)
 {
+    if (S_out && pl.nseg != 1) return cudaErrorInvalidValue;
     uint8_t* base = static_cast<uint8_t*>(ws);
     const uint64_t BH = (uint64_t)p.B * p.H;
     const void* kb = pl.raw_qk ? p.k : base + pl.off_kt;
@@ -300,7 +307,7 @@ cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, 
     StateArgs a;
     const long long st = (long long)p.dk * p.dv;
     a.gam = reinterpret_cast<const float*>(base + pl.off_gam);
-    a.S_out = reinterpret_cast<float*>(base + pl.off_segS);
+    a.S_out = S_out ? S_out : reinterpret_cast<float*>(base + pl.off_segS);
     a.s_out_bh = st * pl.nseg;
     a.s_out_seg = st;
     a.status = status;

@@ -209,6 +209,72 @@ gla_status gla_fwd_host(const gla_fwd_params* p, size_t slice_bytes, cudaStream_
 gla_status gla_host_release(void);
 
 /*
+ * Sequence exchange: one long sequence cut into P consecutive segments, e.g.
+ * one per GPU, each device holding its segment's q, k, v and gate.
+ *
+ * A segment started from a state S_in leaves S_out = Diag(Gamma) S_in + S*,
+ * with Gamma the product of alpha_t over the segment's tokens (per key) and S*
+ * the state the segment leaves from a zero start: the state S_[0] carried from
+ * one segment to the next ("Gated Linear Attention Transformers with
+ * Hardware-Efficient Training", §2.2), and the FlashQLA talk's correction of a
+ * wrongly started segment by one matrix per rank followed by a short serial
+ * recurrence over ranks ("core technical principles"). So each device:
+ *   1. gla_segment_pair: its segment's pair (log Gamma, S*), from a zero start;
+ *   2. exchanges pairs with the devices before it (the caller's collective:
+ *      an all-gather, or a send/recv chain of gla_pair_combine results);
+ *   3. gla_pair_scan: S_in = the state entering its segment, from the pairs
+ *      of the segments before it and the sequence's initial state S0;
+ *   4. gla_fwd_ex with S0 = S_in: its part of O, and (last segment) S_T.
+ * Pairs compose as (Gamma_2, S*_2) o (Gamma_1, S*_1) =
+ * (Gamma_2 Gamma_1, Diag(Gamma_2) S*_1 + S*_2), an associative operation, so a
+ * tree of gla_pair_combine calls gives the same states as the serial scan (up
+ * to fp32 rounding). Gamma travels as log Gamma (float[B,H,dk]; for the scalar
+ * gates every key holds the same value), so a long segment's decay does not
+ * underflow in transit. Each pair is B*H*dk*(dv+1)*4 bytes.
+ *
+ * gla_segment_pair — the pair of the segment that *p describes (its T tokens;
+ * B, H, dk, dv, dtype, gate, log_g, k and v as for gla_fwd_ex). q may be NULL
+ * (the pair does not depend on it; when given it must be valid, as the gate
+ * prep shared with the forward pass reads it); S0, O and ST are ignored.
+ * log_Gamma: device float[B,H,dk], written with the sum over the segment of
+ * log alpha_t (T log lambda_h for the per-head gate, 0 without a gate).
+ * S_star: device float[B,H,dk,dv], written with the state from a zero start.
+ * For bf16 with dk in {64,128,256} (p->path != GLA_PATH_SIMT) the pair comes
+ * from the tensor-core gate prep and state-only pass; otherwise from the
+ * CUDA-core forward pass, whose O goes to the workspace. p->workspace must
+ * hold gla_segment_pair_workspace_size(p) bytes (256-byte aligned), else
+ * GLA_ERR_WORKSPACE. T = 0 gives (0, 0). GLA_ERR_UNSUPPORTED for the bilinear
+ * gate (its decay is a dk x dv matrix, not a key vector). Outputs may not
+ * overlap the inputs or each other. Asynchronous on `stream`.
+ */
+size_t gla_segment_pair_workspace_size(const gla_fwd_params* p);
+gla_status gla_segment_pair(const gla_fwd_params* p, float* log_Gamma, float* S_star, cudaStream_t stream);
+
+/*
+ * gla_pair_scan — the states entering P consecutive segments:
+ *   S = S0 (NULL: zero); for d = 0..P-1: S_in[d] = S, S = Diag(exp(log_Gamma[d])) S + S_star[d];
+ *   S_T = S.
+ * log_Gamma: device float[P,B,H,dk]; S_star: device float[P,B,H,dk,dv] (pair d
+ * at index d, in sequence order); S0: device float[B,H,dk,dv] or NULL; S_in:
+ * device float[P,B,H,dk,dv] or NULL; S_T: device float[B,H,dk,dv] or NULL (one
+ * of the two outputs must be given). Segment d's own S_in is the S_T of a
+ * call with the first d pairs (P = d; P = 0 copies S0, or writes zeros).
+ * S_in may be S_star exactly and S_T may be S0 exactly; no other overlap.
+ * Asynchronous on `stream`.
+ */
+gla_status gla_pair_scan(int P, const float* log_Gamma, const float* S_star, const float* S0, float* S_in,
+                         float* S_T, int B, int H, int dk, int dv, cudaStream_t stream);
+
+/*
+ * gla_pair_combine — in place, (log_Gamma1, S1) <- (log_Gamma2, S2) o (log_Gamma1, S1):
+ *   S1 = Diag(exp(log_Gamma2)) S1 + S2,  log_Gamma1 = log_Gamma2 + log_Gamma1,
+ * where pair 1 is the earlier segment. Device float[B,H,dk] and float[B,H,dk,dv]
+ * each; pair 2 is not written and may not overlap pair 1. Asynchronous on `stream`.
+ */
+gla_status gla_pair_combine(const float* log_Gamma2, const float* S2, float* log_Gamma1, float* S1,
+                            int B, int H, int dk, int dv, cudaStream_t stream);
+
+/*
  * gla_bwd — the backward pass: gradients of a scalar loss L through the
  * forward pass described by the same inputs, given grad_O = dL/dO and
  * grad_ST = dL/dS_T (NULL: zero). It returns dL/dq, dL/dk, dL/dv, dL/dlog_g
@@ -271,6 +337,21 @@ size_t gla_bwd_workspace_size(const gla_bwd_params* p);
  * bounded wait since the last call, GLA_ERR_CUDA if the stream reports an
  * error, else GLA_OK. */
 gla_status gla_device_status(cudaStream_t stream);
+
+/*
+ * gla_selftest_bounded_wait — exercises the failure path of the kernels'
+ * bounded waits without faulting anything. (No counterpart in the papers: a
+ * diagnostic.) Enqueues on `stream` a one-warp kernel that waits, with the
+ * same bounded mbarrier wait the pipelined kernels use, on a shared-memory
+ * barrier. With arrive = 0 nothing ever arrives: after limit_us microseconds
+ * the wait gives up, the kernel records a timeout in the device status word
+ * and returns, so the next gla_device_status() reports GLA_ERR_TIMEOUT and the
+ * context stays usable. With arrive != 0 the kernel arrives on the barrier
+ * first and the wait succeeds at once. The kernel holds no tensor memory and
+ * issues no asynchronous copy. limit_us must be in 1..1000000, else
+ * GLA_ERR_INVALID_ARG.
+ */
+gla_status gla_selftest_bounded_wait(unsigned limit_us, int arrive, cudaStream_t stream);
 
 /* A static, human-readable name for s. */
 const char* gla_status_string(gla_status s);

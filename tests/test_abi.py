@@ -253,3 +253,52 @@ def test_plan_bilinear_on_host():
     base = 2 * BH * T * dk * 2 + BH * nch * 64 * 64 * 2 + BH * nch * dk * 4
     extra = BH * T * dv * 2 + BH * nch * dv * 4 + 256
     assert bnd.gla_fwd_workspace_size(p) == base + extra
+
+
+def test_segment_pair_plan_on_host(lib):
+    """Workspace of the sequence-exchange pair: the tensor route's gate-prep workspace (one
+    segment) plus the log gate's fp64 partial sums; the CUDA-core route's discarded O."""
+    BH, T, dk, dv = 4, 300, 128, 256
+    nch = (T + 63) // 64
+    big = dict(q=0x1000000, k=0x9000000, v=0x11000000, log_g=0x21000000, O=None,
+               B=2, H=2, T=T, dk=dk, dv=dv)
+    prep = 2 * BH * nch * 64 * dk * 2 + BH * nch * 64 * 64 * 2 + BH * nch * dk * 4
+    sums = -(-(1 * BH * dk * 8) // 256) * 256            # one 1024-token slice
+    assert bnd.gla_segment_pair_workspace_size(_params(**big)) == prep + sums
+    # no q: the pair does not need it
+    assert bnd.gla_segment_pair_workspace_size(_params(**dict(big, q=None))) == prep + sums
+    # fp32 inputs: the CUDA-core pass, O to the workspace
+    o32 = BH * T * dv * 4
+    assert bnd.gla_segment_pair_workspace_size(_params(**dict(big, dtype=bnd.GLA_FP32))) == o32 + sums
+    # per-head scalar gate: no partial sums; bilinear gate: not supported (0); T = 0: nothing
+    hs = bnd.gla_segment_pair_workspace_size(_params(**dict(big, gate=bnd.GLA_GATE_HEAD_SCALAR)))
+    assert hs == prep
+    assert bnd.gla_segment_pair_workspace_size(_params(**dict(big, gate=bnd.GLA_GATE_BILINEAR,
+                                                              log_b=0x41000000))) == 0
+    assert bnd.gla_segment_pair_workspace_size(_params(**dict(big, T=0))) == 0
+
+
+def test_segment_pair_and_scan_reject_before_launch(lib):
+    p = _params(q=0x1000000, k=0x9000000, v=0x11000000, log_g=0x21000000, O=None, B=1, H=2, T=64, dk=128, dv=128)
+    G, S = 0x31000000, 0x41000000
+    assert bnd.gla_segment_pair(p, G, None, stream=0, check=False) == bnd.GLA_ERR_INVALID_ARG
+    assert bnd.gla_segment_pair(p, S, S, stream=0, check=False) == bnd.GLA_ERR_INVALID_ARG    # aliased outputs
+    assert bnd.gla_segment_pair(p, G, 0x9000000, stream=0, check=False) == bnd.GLA_ERR_INVALID_ARG  # S* over k
+    pb = _params(gate=bnd.GLA_GATE_BILINEAR, log_b=0x900000)
+    assert bnd.gla_segment_pair(pb, G, S, stream=0, check=False) == bnd.GLA_ERR_UNSUPPORTED
+    sc = lambda *a: bnd.gla_pair_scan(*a, stream=0, check=False)
+    dims = (1, 2, 128, 128)
+    ns = 2 * 128 * 128 * 4
+    assert sc(-1, G, S, None, 0x51000000, None, *dims) == bnd.GLA_ERR_INVALID_ARG        # P < 0
+    assert sc(2, G, S, None, None, None, *dims) == bnd.GLA_ERR_INVALID_ARG               # no output
+    assert sc(2, None, S, None, 0x51000000, None, *dims) == bnd.GLA_ERR_INVALID_ARG      # pairs missing
+    assert sc(2, G, S, None, S + ns, None, *dims) == bnd.GLA_ERR_INVALID_ARG             # S_in inside S*
+    assert sc(1, G, S, 0x61000000, None, 0x61000000 + 64, *dims) == bnd.GLA_ERR_INVALID_ARG  # S_T over S0
+    cb = lambda *a: bnd.gla_pair_combine(*a, 1, 2, 128, 128, stream=0, check=False)
+    assert cb(G, S, G, 0x51000000) == bnd.GLA_ERR_INVALID_ARG                            # pair 1 aliases pair 2
+    assert cb(G, S, 0x51000000, 0x51000000 + 64) == bnd.GLA_ERR_INVALID_ARG              # log Gamma1 inside S1
+
+
+def test_selftest_wait_limit_checked_before_launch(lib):
+    assert bnd.gla_selftest_bounded_wait(0, stream=0, check=False) == bnd.GLA_ERR_INVALID_ARG
+    assert bnd.gla_selftest_bounded_wait(1000001, stream=0, check=False) == bnd.GLA_ERR_INVALID_ARG
