@@ -451,9 +451,12 @@ def run_backward(args, w):
 
 
 def time_plan(bnd, p, steps, warmup, stream, flush_l2, record_clocks=None):
-    """Times the plan of params p stage by stage with CUDA events on `stream`: `warmup`
-    untimed steps, then `steps` timed ones, L2 flushed before each (outside the events).
-    Returns (stage names, mean ms per stage, mean ms per step, sorted per-step ms)."""
+    """Times the plan of params p with CUDA events on `stream`: `warmup` untimed steps,
+    then `steps` timed ones, L2 flushed before each (outside the events). A step is the
+    whole pass as gla_fwd_ex runs it (its stages back to back, nothing recorded between
+    them, so a stage may start while the one before finishes); the per-stage breakdown
+    comes from as many further steps with an event between stages. Returns (stage names,
+    mean ms per stage, mean ms per step, sorted per-step ms, clocks)."""
     import torch
     nst = bnd.gla_fwd_num_stages(p)
     names = [bnd.gla_fwd_stage_name(p, i) for i in range(nst)]
@@ -466,25 +469,38 @@ def time_plan(bnd, p, steps, warmup, stream, flush_l2, record_clocks=None):
         if evs is not None:
             evs[nst].record(stream)
 
+    def whole(e0, e1):
+        e0.record(stream)
+        for i in range(nst):
+            bnd.gla_fwd_stage(p, i, stream)
+        e1.record(stream)
+
     for _ in range(warmup):
         flush_l2()
         step()
     torch.cuda.synchronize()
     if bnd.gla_device_status(stream) != 0:
         raise SystemExit("device status error after warm-up")
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if record_clocks:
         record_clocks.start()
     torch.cuda.synchronize()
     for s in range(steps):
         flush_l2()
-        step(evsets[s])
+        whole(*pairs[s])
     torch.cuda.synchronize()
     clk = record_clocks.stop() if record_clocks else None
     if bnd.gla_device_status(stream) != 0:
         raise SystemExit("device status error in timed region")
+    per = sorted(a.elapsed_time(b) for a, b in pairs)
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    for s in range(steps):
+        flush_l2()
+        step(evsets[s])
+    torch.cuda.synchronize()
+    if bnd.gla_device_status(stream) != 0:
+        raise SystemExit("device status error in the stage-by-stage steps")
     stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evsets) / steps for i in range(nst)]
-    per = sorted(e[0].elapsed_time(e[nst]) for e in evsets)
     return names, stage_ms, sum(per) / steps, per, clk
 
 
@@ -591,7 +607,10 @@ def main():
     if bnd.gla_device_status(stream) != 0:
         raise SystemExit("device status error after warm-up")
 
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    # The timed steps: each the whole pass as gla_fwd_ex runs it, its stages back to back
+    # with nothing recorded between them (a stage may start while the one before finishes),
+    # an event before and after.
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
     if clocks:
         clocks.start()
@@ -600,23 +619,27 @@ def main():
     torch.cuda.synchronize()
     for s in range(args.steps):
         flush_l2()
-        step(evsets[s])
+        pairs[s][0].record(stream)
+        step()
+        pairs[s][1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
     if bnd.gla_device_status(stream) != 0:
         raise SystemExit("device status error in timed region")
-    stage_ms = [0.0] * nst
-    step_ms = 0.0
-    for evs in evsets:
-        for i in range(nst):
-            stage_ms[i] += evs[i].elapsed_time(evs[i + 1])
-        step_ms += evs[0].elapsed_time(evs[nst])
-    stage_ms = [t / args.steps for t in stage_ms]
-    step_ms /= args.steps
+    per_step = sorted(a.elapsed_time(b) for a, b in pairs)
+    step_ms = sum(per_step) / args.steps
     step_ms = max_over_ranks(step_ms, dist, dev)
-    per_step = sorted(evs[0].elapsed_time(evs[nst]) for evs in evsets)
+    # the per-stage breakdown: as many further steps, an event between stages
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush_l2()
+        step(evsets[s])
+    torch.cuda.synchronize()
+    if bnd.gla_device_status(stream) != 0:
+        raise SystemExit("device status error in the stage-by-stage steps")
+    stage_ms = [sum(evs[i].elapsed_time(evs[i + 1]) for evs in evsets) / args.steps for i in range(nst)]
 
     # the same steps back to back without the flush (inputs partly in L2 from the step before)
     uevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -729,7 +752,9 @@ def main():
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "timing": {"mean_ms": step_ms, "median_ms": per_step[len(per_step) // 2], "min_ms": per_step[0],
                    "unflushed_median_ms": unflushed[len(unflushed) // 2],
-                   "note": "mean is the value's basis; unflushed = the same steps back to back, no L2 flush"},
+                   "note": "mean is the value's basis: whole passes, events only before and after each; "
+                           "stage_ms comes from as many further steps with an event between stages; "
+                           "unflushed = the same steps back to back, no L2 flush"},
         "gpu_launches": nst * args.steps,
         "clocks": clk,
     }

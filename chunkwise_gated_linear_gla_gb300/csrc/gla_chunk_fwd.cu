@@ -16,13 +16,16 @@
 // the state's columns (dk) line up with the per-key gate. The state stays in
 // tensor memory for the whole segment and never goes to HBM; Q (.) Lambda,
 // K (.) Gamma, gamma and the masked intra-chunk scores come from
-// gla_chunk_prep. Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM
-// owner), 2-9 epilogue in two groups of four warps, each owning half of the
-// state's columns and half of each output tile. Only the decay of the state
-// sits on the chunk-to-chunk critical path (state MMA -> decay -> next state
-// MMA); the bf16 copy, the inter and intra MMAs and the output drain overlap
-// with it. Every wait is bounded; on a timeout the CTA records an error code
-// and winds down.
+// gla_chunk_prep. Warp roles, by warpgroup: warp 0 TMA producer and warp 1
+// MMA issuer (and TMEM owner) in the first; the state epilogue in the second
+// and third (two groups of four warps, each owning half of the state's
+// columns); the output drain in the fourth (four warps, one per TMEM lane
+// quarter, every row of each output tile). setmaxnreg moves registers from
+// the producer/MMA and drain warpgroups to the state epilogue. Only the decay
+// of the state sits on the chunk-to-chunk critical path (state MMA -> decay ->
+// next state MMA); the bf16 copy, the inter and intra MMAs and the output
+// drain, on warps of their own, overlap with it. Every wait is bounded; on a
+// timeout the CTA records an error code and winds down.
 //
 // The bilinear gate G_t = alpha_t^T beta_t (Table 1's DFW row; the chunkwise
 // form of the paper's appendix on the general formulation) is the BIL
@@ -46,12 +49,25 @@ using namespace sm100;
 constexpr int C = kChunk;
 constexpr int DVT = kDvTile;
 constexpr int NSTAGE = 2;
-constexpr int NT = 320;
-constexpr int NEPI = 256;                         // epilogue threads (warps 2-9)
-constexpr int BAR_EPI = 1, BAR_G0 = 2;            // named barriers (0 is __syncthreads)
+constexpr int NG = 4;                             // gate ring slots
+constexpr int G_AHEAD = 2;                        // gate loads run this many chunks ahead of the stages
+constexpr int PF_AHEAD = 3;                       // L2 prefetches run this many chunks ahead of the stage loads
+constexpr int NT = 512;
+constexpr int NEPI = 256;                         // state epilogue threads (warps 4-11)
+constexpr int NDR = 128;                          // output drain threads (warps 12-15)
+constexpr int BAR_EPI = 1, BAR_DR = 2;            // named barriers (0 is __syncthreads)
 constexpr uint64_t kTimeoutNs = 2000000000ull;    // 2 s per wait
+// Registers per thread of each warpgroup after setmaxnreg (the launch gives 128 each):
+// producer/MMA, state epilogue (two warpgroups), drain.
+// The split that compiles without spills differs between instantiations.
+template <int DK, bool BIL>
+struct Regs {
+    static constexpr bool wide = DK == 256 && !BIL;
+    static constexpr int ctl = wide ? 64 : 80, epi = wide ? 176 : 160, drain = wide ? 96 : 112;
+    static_assert(128 * (ctl + 2 * epi + drain) <= NT * 128, "register split");
+};
 
-enum { ERR_PRODUCER = 0x101, ERR_MMA = 0x102, ERR_EPI = 0x103 };
+enum { ERR_PRODUCER = 0x101, ERR_MMA = 0x102, ERR_EPI = 0x103, ERR_DRAIN = 0x104 };
 
 struct FwdArgs {
     const float* S_in;  long long s_in_bh, s_in_seg;
@@ -81,12 +97,14 @@ struct Lay {
     static constexpr int K_OFF = QB;
     static constexpr int V_OFF = QB + KB;
     static constexpr int A_OFF = V_OFF + VB;
-    static constexpr int G_OFF = A_OFF + AB;
+    static constexpr int STAGE = (A_OFF + AB + 1023) / 1024 * 1024;
+    // the gate ring: slot = the chunk's key decays gamma (and, bilinear gate, its column
+    // decays' logs B'_C), NG chunks deep, so the decay of the state never waits for a stage
     static constexpr int GVB = BIL ? DVT * 4 : 0;
-    static constexpr int GV_OFF = G_OFF + GB;
-    static constexpr int STAGE = (GV_OFF + GVB + 1023) / 1024 * 1024;
+    static constexpr int GSL = GB + GVB;
+    static constexpr int GR_OFF = NSTAGE * STAGE;
     static constexpr int OB = C * DVT * 2;
-    static constexpr int O_OFF = NSTAGE * STAGE;
+    static constexpr int O_OFF = GR_OFF + NG * GSL;
     static constexpr int BAR_OFF = O_OFF + 2 * OB;
     static constexpr int SMEM = BAR_OFF + 256 + 1024;
     static constexpr int TCOLS_USED = DK + DK / 2 + 2 * 64;
@@ -137,17 +155,21 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
-    uint64_t* full = bar + 0;      // [2] stage filled (TMA transaction count)
+    uint64_t* full = bar + 0;      // [2] stage's K and V tiles landed (TMA transaction count)
     uint64_t* empty = bar + 2;     // [2] stage consumed (MMA commit)
     uint64_t* s_ready = bar + 4;   // state decayed in TMEM (256 arrivals)
     uint64_t* s_done = bar + 5;    // state MMA of the chunk complete
     uint64_t* sb_free = bar + 6;   // inter MMA complete: bf16 state copy reusable
     uint64_t* o_full = bar + 7;    // [2] O accumulator complete
-    uint64_t* o_empty = bar + 9;   // [2] O accumulator drained (256 arrivals)
+    uint64_t* o_empty = bar + 9;   // [2] O accumulator drained (128 arrivals)
     uint64_t* sb_ready = bar + 11; // bf16 state copy written (256 arrivals)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 13);
     uint64_t* mma_fin = bar + 14;  // every MMA of the CTA complete (the issuer's last commit)
+    uint64_t* gfull = bar + 15;    // [NG] gate ring slot filled (transaction count)
+    uint64_t* gempty = bar + 15 + NG;   // [NG] gate ring slot read (256 arrivals)
+    uint64_t* full_qa = bar + 15 + 2 * NG;   // [2] stage's Q and score tiles landed
+    volatile int* issued_ctr = reinterpret_cast<volatile int*>(bar + 17 + 2 * NG);   // chunks whose loads are out
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.y, seg = blockIdx.z;
@@ -164,11 +186,17 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
 
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1); mbar_init(&full[1], 1);
+        mbar_init(&full_qa[0], 1); mbar_init(&full_qa[1], 1);
+        *issued_ctr = 0;
         mbar_init(&empty[0], 1); mbar_init(&empty[1], 1);
         mbar_init(s_ready, NEPI); mbar_init(s_done, 1); mbar_init(sb_free, 1); mbar_init(sb_ready, NEPI);
         mbar_init(&o_full[0], 1); mbar_init(&o_full[1], 1);
-        mbar_init(&o_empty[0], NEPI); mbar_init(&o_empty[1], NEPI);
+        mbar_init(&o_empty[0], NDR); mbar_init(&o_empty[1], NDR);
         mbar_init(mma_fin, 1);
+        for (int i = 0; i < NG; ++i) {
+            mbar_init(&gfull[i], 1);
+            mbar_init(&gempty[i], NEPI);
+        }
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tmap(&tmQ); prefetch_tmap(&tmK); prefetch_tmap(&tmV); prefetch_tmap(&tmA); prefetch_tmap(&tmO);
@@ -178,30 +206,35 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         tmem_alloc(tmem_holder, L::TCOLS);
         tmem_relinquish();
     }
-    // Epilogue threads issue every load of their S_in columns (dv column d, HC keys)
-    // before the set-up barrier, so the loads overlap the set-up and are all in flight
-    // at once; they go to tensor memory after the barrier.
     constexpr int NB = HC / 32;
-    uint32_t s_in[NB][32];
-    if (warp >= 2) {
-        const int d = (warp & 3) * 32 + lane, cb = ((warp - 2) >> 2) * HC;
-        const float* sin = a.S_in ? a.S_in + bh * a.s_in_bh + seg * a.s_in_seg + dv0 + d : nullptr;
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                s_in[b][i] = sin ? __float_as_uint(sin[(size_t)(cb + b * 32 + i) * a.dv]) : 0u;
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const uint32_t tS = tmem, tSb = tmem + DK, tO0 = tmem + DK + DK / 2;
 
+    const int wg = warp >> 2;
+    if (wg == 0) regs_dec<Regs<DK, BIL>::ctl>();   // warps 2 and 3 have no role
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
-            int issued = 0;
+            // chunk j's gate decays into ring slot j % NG, once chunk j - NG's decay has read it
+            auto load_g = [&](int j) -> bool {
+                const int sl = j % NG, c = c_begin + j;
+                if (j >= NG && !mbar_wait(&gempty[sl], ((j / NG) - 1) & 1, kTimeoutNs)) return false;
+                uint8_t* gs = sm + L::GR_OFF + sl * L::GSL;
+                mbar_arrive_expect_tx(&gfull[sl], L::GSL);
+                bulk_load(gs, a.gam + ((size_t)bh * a.nchunks + c) * DKT + KOFF, L::GB, &gfull[sl]);
+                if constexpr (BIL)
+                    bulk_load(gs + L::GB, a.lbc + ((size_t)bh * a.nchunks + c) * a.dv + dv0, L::GVB, &gfull[sl]);
+                return true;
+            };
+            // launched with programmatic stream serialization (see launch_dk), the grid ahead
+            // (gate prep or segment scan) may still run: wait for its writes before any load
+            grid_dependency_wait();
+            int issued = 0, gissued = 0;
+            if (gated)
+                for (; gissued < G_AHEAD && gissued < nloc; ++gissued) load_g(gissued);
             for (int n = 0; n < nloc; ++n) {
                 if (*abort_flag) break;
                 const int st = n & 1, c = c_begin + n;
@@ -210,50 +243,76 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     break;
                 }
                 uint8_t* sb = sm + st * L::STAGE;
-                const uint32_t bytes = L::KB + L::VB + (gated ? L::GB : 0) +
-                                       (want_out ? L::QB + (KH == 2 ? 0 : L::AB) : 0) + L::GVB;
-                mbar_arrive_expect_tx(&full[st], bytes);
-                if (gated) bulk_load(sb + L::G_OFF, a.gam + ((size_t)bh * a.nchunks + c) * DKT + KOFF, L::GB, &full[st]);
-                if constexpr (BIL)
-                    bulk_load(sb + L::GV_OFF, a.lbc + ((size_t)bh * a.nchunks + c) * a.dv + dv0, L::GVB, &full[st]);
+                // K and V first (the state MMA, on the chunk-to-chunk chain, needs only them),
+                // then Q and the scores (the output MMAs) on a barrier of their own
+                mbar_arrive_expect_tx(&full[st], L::KB + L::VB);
 #pragma unroll
                 for (int i = 0; i < DK / 64; ++i)
                     tma_load_3d(sb + L::K_OFF + i * 8192, &tmK, &full[st], KOFF + i * 64, c * C, bh);
                 tma_load_3d(sb + L::V_OFF, &tmV, &full[st], dv0, c * C, bh);
                 tma_load_3d(sb + L::V_OFF + 8192, &tmV, &full[st], dv0 + 64, c * C, bh);
                 if (want_out) {
+                    mbar_arrive_expect_tx(&full_qa[st], L::QB + (KH == 2 ? 0 : L::AB));
                     const CUtensorMap* mq = q_fac(c) ? &tmQr : &tmQ;
 #pragma unroll
                     for (int i = 0; i < DK / 64; ++i)
-                        tma_load_3d(sb + L::Q_OFF + i * 8192, mq, &full[st], KOFF + i * 64, c * C, bh);
-                    if (KH != 2) tma_load_2d(sb + L::A_OFF, &tmA, &full[st], 0, (bh * a.nchunks + c) * C);
+                        tma_load_3d(sb + L::Q_OFF + i * 8192, mq, &full_qa[st], KOFF + i * 64, c * C, bh);
+                    if (KH != 2) tma_load_2d(sb + L::A_OFF, &tmA, &full_qa[st], 0, (bh * a.nchunks + c) * C);
                 }
-                // L2 prefetch two chunks ahead, beyond what the two shared-memory stages
-                // hold; the tiles all dv-tile CTAs of this head share are split among them
-                const int cp = c + 2;
-                if (cp < c_end) {
-                    prefetch_l2_tile_3d(&tmV, dv0, cp * C, bh);
-                    prefetch_l2_tile_3d(&tmV, dv0 + 64, cp * C, bh);
-                    const int nt = gridDim.x, me = blockIdx.x;
-                    int item = 0;
-#pragma unroll
-                    for (int i = 0; i < DK / 64; ++i, ++item)
-                        if (item % nt == me) prefetch_l2_tile_3d(&tmK, KOFF + i * 64, cp * C, bh);
-                    if (want_out) {
-                        const CUtensorMap* mq = q_fac(cp) ? &tmQr : &tmQ;
-#pragma unroll
-                        for (int i = 0; i < DK / 64; ++i, ++item)
-                            if (item % nt == me) prefetch_l2_tile_3d(mq, KOFF + i * 64, cp * C, bh);
-                        if (KH != 2 && item % nt == me) prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
-                        ++item;
-                    }
-                    if (gated && item % nt == me)
-                        prefetch_l2(a.gam + ((size_t)bh * a.nchunks + cp) * DKT + KOFF, L::GB);
-                }
+                *issued_ctr = n + 1;   // paces the L2 prefetches of warp 2
                 issued = n + 1;
+                if (gated && gissued < nloc) {
+                    if (!load_g(gissued)) {
+                        fail(a.status, abort_flag, ERR_PRODUCER);
+                        break;
+                    }
+                    ++gissued;
+                }
             }
             // no copy may land after the CTA exits: wait for the last fills
-            for (int n = max(0, issued - 2); n < issued; ++n) mbar_wait(&full[n & 1], (n >> 1) & 1, kTimeoutNs);
+            for (int n = max(0, issued - 2); n < issued; ++n) {
+                mbar_wait(&full[n & 1], (n >> 1) & 1, kTimeoutNs);
+                if (want_out) mbar_wait(&full_qa[n & 1], (n >> 1) & 1, kTimeoutNs);
+            }
+            for (int j = max(0, gissued - NG); j < gissued; ++j) mbar_wait(&gfull[j % NG], (j / NG) & 1, kTimeoutNs);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------- L2 prefetcher
+        // Once the producer has issued chunk m's loads, pull chunk m + PF_AHEAD's tiles into
+        // L2, so that the stage loads, issued only when a stage frees up, find them there.
+        // The tiles all dv-tile CTAs of this head share are split among them. Prefetches are
+        // hints: if the producer stops (an abort) this thread just stops too.
+        if (lane == 0) {
+            const uint64_t t_start = globaltimer();
+            for (int m = 0; m + PF_AHEAD < nloc; ++m) {
+                bool go = true;
+                while (*issued_ctr <= m) {
+                    if (*abort_flag || globaltimer() - t_start > kTimeoutNs) {
+                        go = false;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                if (!go) break;
+                const int cp = c_begin + m + PF_AHEAD;
+                prefetch_l2_tile_3d(&tmV, dv0, cp * C, bh);
+                prefetch_l2_tile_3d(&tmV, dv0 + 64, cp * C, bh);
+                const int nt = gridDim.x, me = blockIdx.x;
+                int item = 0;
+#pragma unroll
+                for (int i = 0; i < DK / 64; ++i, ++item)
+                    if (item % nt == me) prefetch_l2_tile_3d(&tmK, KOFF + i * 64, cp * C, bh);
+                if (want_out) {
+                    const CUtensorMap* mq = q_fac(cp) ? &tmQr : &tmQ;
+#pragma unroll
+                    for (int i = 0; i < DK / 64; ++i, ++item)
+                        if (item % nt == me) prefetch_l2_tile_3d(mq, KOFF + i * 64, cp * C, bh);
+                    if (KH != 2 && item % nt == me) prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
+                    ++item;
+                }
+                if (gated && item % nt == me && cp + G_AHEAD < c_end)
+                    prefetch_l2(a.gam + ((size_t)bh * a.nchunks + cp + G_AHEAD) * DKT + KOFF, L::GB);
+            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -261,6 +320,14 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             const uint32_t id_state = idesc_bf16(128, DK, true, true);
             const uint32_t id_inter = idesc_bf16(128, 64, false, false);
             const uint32_t id_intra = idesc_bf16(128, 64, true, false);
+            // Operand descriptors of stage 0, built once; a stage or a K step only moves the
+            // start address, the low 14-bit field (addr >> 4) of the descriptor, and every
+            // shared address here is below 2^18, so adding the offset >> 4 never carries out.
+            const uint32_t s0 = smem_u32(sm);
+            const uint64_t dV0 = sdesc(s0 + L::V_OFF, 8192, 1024, kSwizzle128);
+            const uint64_t dK0 = sdesc(s0 + L::K_OFF, 8192, 1024, kSwizzle128);
+            const uint64_t dQ0 = sdesc(s0 + L::Q_OFF, 16, 1024, kSwizzle128);
+            const uint64_t dA0 = sdesc(s0 + L::A_OFF, 16, 1024, kSwizzle128);
             for (int n = 0; n < nloc; ++n) {
                 if (*abort_flag) break;
                 const int st = n & 1;
@@ -271,17 +338,17 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sb = smem_u32(sm + st * L::STAGE);
-                const uint32_t sQ = sb + L::Q_OFF, sK = sb + L::K_OFF, sV = sb + L::V_OFF, sA = sb + L::A_OFF;
+                const uint64_t so = (uint64_t)((st * L::STAGE) >> 4);
+                const uint64_t dV = dV0 + so, dK = dK0 + so, dQ = dQ0 + so, dA = dA0 + so;
                 // state: S^T += V^T (K (.) Gamma); both operands MN-major
 #pragma unroll
                 for (int kk = 0; kk < C / 16; ++kk)
-                    mma_ss(tS, sdesc(sV + kk * 2048, 8192, 1024, kSwizzle128),
-                           sdesc(sK + kk * 2048, 8192, 1024, kSwizzle128), id_state, 1);
+                    mma_ss(tS, dV + kk * (2048 >> 4), dK + kk * (2048 >> 4), id_state, 1);
                 mma_commit(s_done);
                 if (want_out) {
                     ok = mbar_wait(sb_ready, n & 1, kTimeoutNs);
                     if (ok && n >= 2) ok = mbar_wait(&o_empty[n & 1], ((n >> 1) - 1) & 1, kTimeoutNs);
+                    if (ok) ok = mbar_wait(&full_qa[st], (n >> 1) & 1, kTimeoutNs);
                     if (!ok) {
                         fail(a.status, abort_flag, ERR_MMA);
                         break;
@@ -291,15 +358,13 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     // inter: O^T = Sb^T (Q (.) Lambda)^T, A (the bf16 state) from TMEM
 #pragma unroll
                     for (int kk = 0; kk < DK / 16; ++kk)
-                        mma_ts(tO, tSb + kk * 8, sdesc(sQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128),
-                               id_inter, kk > 0);
+                        mma_ts(tO, tSb + kk * 8, dQ + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), id_inter, kk > 0);
                     mma_commit(sb_free);
                     // intra: O^T += V^T (P (.) M)^T (the second key half leaves it to the first)
                     if (KH != 2) {
 #pragma unroll
                         for (int kk = 0; kk < C / 16; ++kk)
-                            mma_ss(tO, sdesc(sV + kk * 2048, 8192, 1024, kSwizzle128),
-                                   sdesc(sA + kk * 32, 16, 1024, kSwizzle128), id_intra, 1);
+                            mma_ss(tO, dV + kk * (2048 >> 4), dA + kk * (32 >> 4), id_intra, 1);
                     }
                     mma_commit(&o_full[n & 1]);
                 }
@@ -310,158 +375,81 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             mma_commit(mma_fin);
             mbar_wait(mma_fin, 0, kTimeoutNs);
         }
-    } else {
-        // ---------------------------------------------------------- epilogue warps (2 groups of 4)
-        // Group g owns state columns [g*DK/2, (g+1)*DK/2) and output rows [g*32, g*32+32)
-        // of every chunk; the warp's TMEM lane quarter is (warp % 4).
-        const int grp = (warp - 2) >> 2;
+    } else if (wg == 1 || wg == 2) {
+        // ---------------------------------------------------------- state epilogue (2 groups of 4 warps)
+        // Group g owns state columns [g*DK/2, (g+1)*DK/2); the warp's TMEM lane quarter is
+        // (warp % 4) and its thread's dv column d.
+        regs_inc<Regs<DK, BIL>::epi>();
+        const int grp = wg - 1;
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const int d = (warp & 3) * 32 + lane;   // dv column within the tile
         const int cb = grp * HC;                 // first state column of this group
-        const int gt = threadIdx.x - 64 - grp * 128;   // thread index within the group
-        const int bar_grp = BAR_G0 + grp;
+        const int gt = threadIdx.x - 128 - grp * 128;   // thread index within the group
+        // S0 is the caller's and no earlier grid of the pass writes it; the segment scan's
+        // start states (sequence split) come from the grid ahead
+        if (a.mode != kModeFull) grid_dependency_wait();
+        {
+            // S_in of this thread's column and HC keys: every load in flight at once, then to TMEM
+            const float* sin = a.S_in ? a.S_in + bh * a.s_in_bh + seg * a.s_in_seg + dv0 + d : nullptr;
+            uint32_t s_in[NB][32];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) tmem_st32(tS + lb + cb + b * 32, s_in[b]);
-        tmem_wait_st();
-        // drain the O accumulator of chunk m: TMEM -> registers -> bf16 smem tile -> TMA store;
-        // lbc_m is B'_C[d] of chunk m (bilinear gate)
-        auto drain = [&](int m, float lbc_m) -> bool {
-            const int b = m & 1;
-            float w[32];
-            const bool fq = SCAL && q_fac(c_begin + m);   // per-head gate: output rows take lambda^(r+1)
-            if constexpr (BIL) {
-                // log beta of this thread's 32 rows of chunk m (rows past T add nothing), and an
-                // L2 prefetch of chunk m+2's rows, one 128-byte line per thread
-                const int row0 = (c_begin + m) * C + grp * 32;
-                const float* lp = a.lb + ((size_t)bh * a.T + row0) * a.dv + dv0 + d;
+            for (int b = 0; b < NB; ++b)
 #pragma unroll
-                for (int t = 0; t < 32; ++t) w[t] = row0 + t < a.T ? lp[(size_t)t * a.dv] : 0.f;
-                const int prow = (c_begin + m + 2) * C + gt / 4 + grp * 32;
-                if (c_begin + m + 2 < c_end && prow < a.T)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.lb + ((size_t)bh * a.T + prow) * a.dv + dv0 +
-                                                                 (gt & 3) * 32));
-            }
-            const int orow = (c_begin + m) * C + grp * 32;   // this thread's first row of chunk m
-            if constexpr (KH == 2) {
-                // the first key half's fp32 partial of this thread's 32 rows (rows past T: none)
-                const float* pp = a.Opart + ((size_t)bh * a.T + orow) * a.dv + dv0 + d;
+                for (int i = 0; i < 32; ++i)
+                    s_in[b][i] = sin ? __float_as_uint(sin[(size_t)(cb + b * 32 + i) * a.dv]) : 0u;
 #pragma unroll
-                for (int t = 0; t < 32; ++t) w[t] = orow + t < a.T ? pp[(size_t)t * a.dv] : 0.f;
-            }
-            const bool ok = mbar_wait(&o_full[b], (m >> 1) & 1, kTimeoutNs);
-            if (!group_all_ok(ok, BAR_EPI, NEPI)) return false;
-            tc_fence_after();
-            uint32_t r[32];
-            tmem_ld32(tO0 + b * 64 + lb + grp * 32, r);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&o_empty[b]);
-            if constexpr (BIL) {
-                // exp(B'_r - B'_C): rows 0-31 from the prefix sum, rows 32-63 from the suffix sum.
-                // Exponents are within [-kVGuard, kVGuard]; the fast exponential's error there is
-                // far below the bf16 rounding of O (the parity tests hold the bf16 tolerance).
-                if (grp == 0) {
-                    float acc = -lbc_m;
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        acc += w[t];
-                        w[t] = __expf(acc);
-                    }
-                } else {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int t = 31; t >= 0; --t) {
-                        const float x = w[t];
-                        w[t] = __expf(acc);
-                        acc -= x;
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * w[t]);
-            } else if (SCAL && fq) {
-                // (r + 1) log lambda lies in [-kQGuard, 0] for every row r of the chunk
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    r[t] = __float_as_uint(__uint_as_float(r[t]) * __expf((float)(grp * 32 + t + 1) * lam_h));
-            }
-            if constexpr (KH == 2) {
-#pragma unroll
-                for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) + w[t]);
-            }
-            if constexpr (KH == 1) {
-                // the partial goes out in fp32, one coalesced 128-byte row segment per warp and row
-                float* pp = a.Opart + ((size_t)bh * a.T + orow) * a.dv + dv0 + d;
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    if (orow + t < a.T) pp[(size_t)t * a.dv] = __uint_as_float(r[t]);
-                return true;
-            }
-            // the store issued from this half-buffer two chunks ago must have read it
-            if (gt == 0) bulk_wait_read1();
-            named_bar_sync(bar_grp, 128);
-            uint8_t* tile = sm + L::O_OFF + b * L::OB;
-            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(tile) + (d >> 6) * (C * 64) + grp * 32 * 64 + (d & 63);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) ob[t * 64] = __float2bfloat16_rn(__uint_as_float(r[t]));
-            fence_proxy_async_smem();
-            named_bar_sync(bar_grp, 128);
-            if (gt == 0) {
-                const int c = c_begin + m;
-                tma_store_3d(&tmO, tile + grp * 32 * 64 * 2, dv0, c * C + grp * 32, bh);
-                tma_store_3d(&tmO, tile + C * 64 * 2 + grp * 32 * 64 * 2, dv0 + 64, c * C + grp * 32, bh);
-                bulk_commit();
-            }
-            return true;
-        };
+            for (int b = 0; b < NB; ++b) tmem_st32(tS + lb + cb + b * 32, s_in[b]);
+            tmem_wait_st();
+        }
         bool alive = true;
         uint32_t P[HC / 2];   // bf16 pairs of S_[n-1] (this thread's columns), kept until the copy is free
-        float lbc_prev = 0.f, lbc_cur = 0.f;   // B'_C[d] of chunks n-1 and n (bilinear gate)
         for (int n = 0; n < nloc && alive; ++n) {
             bool ok = true;
             if (n >= 1) ok = mbar_wait(s_done, (n - 1) & 1, kTimeoutNs);
-            if (ok && gated) ok = mbar_wait(&full[n & 1], (n >> 1) & 1, kTimeoutNs);
+            if (ok && gated) ok = mbar_wait(&gfull[n % NG], (n / NG) & 1, kTimeoutNs);
             if (!group_all_ok(ok, BAR_EPI, NEPI)) {
                 alive = false;
                 break;
             }
             tc_fence_after();
-            const float* g = reinterpret_cast<const float*>(sm + (n & 1) * L::STAGE + L::G_OFF) + cb;
+            const uint8_t* gs = sm + L::GR_OFF + (n % NG) * L::GSL;
+            const float* g = reinterpret_cast<const float*>(gs) + cb;
             float gvd = 1.f;   // gamma'[d] (bilinear gate)
-            if constexpr (BIL) {
-                lbc_cur = reinterpret_cast<const float*>(sm + (n & 1) * L::STAGE + L::GV_OFF)[d];
-                gvd = expf(lbc_cur);
-            }
-            // part 1: S <- Diag(gamma_n) S_[n-1] (and keep bf16(S_[n-1]) in registers)
+            if constexpr (BIL) gvd = expf(reinterpret_cast<const float*>(gs + L::GB)[d]);
+            // part 1: S <- Diag(gamma_n) S_[n-1] (and keep bf16(S_[n-1]) in registers), 32
+            // columns per step. The step's gate values are read from shared memory before its
+            // tensor-memory load is issued, so their latency hides behind that load's.
 #pragma unroll
-            for (int c2 = 0; c2 < HC; c2 += 64) {
-                uint32_t r0[32], r1[32];
+            for (int c2 = 0; c2 < HC; c2 += 32) {
+                float4 gv[8];
+                if (gated) {
+                    const float4* g4 = reinterpret_cast<const float4*>(g + c2);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) gv[i] = g4[i];
+                }
+                uint32_t r0[32];
                 tmem_ld32(tS + lb + cb + c2, r0);
-                tmem_ld32(tS + lb + cb + c2 + 32, r1);
                 tmem_wait_ld();
                 if constexpr (BIL) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gvd);
-                        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * gvd);
-                    }
+                    for (int i = 0; i < 32; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gvd);
                 }
                 if (want_out) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 16; ++i)
                         P[c2 / 2 + i] = pack_bf16(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-                        P[c2 / 2 + 16 + i] = pack_bf16(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
-                    }
                 }
                 if (gated) {
+                    // two columns per packed multiply (each lane rounds as a single fp32 multiply)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * g[c2 + i]);
-                        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * g[c2 + 32 + i]);
+                    for (int i = 0; i < 8; ++i) {
+                        mul2_inplace(r0[4 * i], r0[4 * i + 1], make_float2(gv[i].x, gv[i].y));
+                        mul2_inplace(r0[4 * i + 2], r0[4 * i + 3], make_float2(gv[i].z, gv[i].w));
                     }
                     tmem_st32(tS + lb + cb + c2, r0);
-                    tmem_st32(tS + lb + cb + c2 + 32, r1);
                 }
             }
+            if (gated) mbar_arrive(&gempty[n % NG]);   // this thread has read its gate slot
             if (gated) tmem_wait_st();
             tc_fence_before();
             mbar_arrive(s_ready);
@@ -483,35 +471,145 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(sb_ready);
-            if (n >= 1 && !drain(n - 1, lbc_prev)) {
-                alive = false;
-                break;
-            }
-            lbc_prev = lbc_cur;
         }
         // The final state is complete once the last state MMA is (before the last inter
-        // and intra MMAs): its stores go out while those run, then the last O drain.
+        // and intra MMAs): its stores go out while those run.
         if (alive && nloc > 0) {
             const bool ok = mbar_wait(s_done, (nloc - 1) & 1, kTimeoutNs);
             if (group_all_ok(ok, BAR_EPI, NEPI)) {
                 tc_fence_after();
                 if (a.S_out) {
                     float* so = a.S_out + bh * a.s_out_bh + seg * a.s_out_seg + dv0 + d;
+#pragma unroll 1
+                    for (int b = 0; b < NB; ++b) {
+                        uint32_t r[32];
+                        tmem_ld32(tS + lb + cb + b * 32, r);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) tmem_ld32(tS + lb + cb + b * 32, s_in[b]);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int b = 0; b < NB; ++b)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) so[(size_t)(cb + b * 32 + i) * a.dv] = __uint_as_float(s_in[b][i]);
+                        for (int i = 0; i < 32; ++i) so[(size_t)(cb + b * 32 + i) * a.dv] = __uint_as_float(r[i]);
+                    }
                 }
             } else {
                 alive = false;
             }
         }
-        if (alive && want_out && nloc > 0 && !drain(nloc - 1, lbc_prev)) alive = false;
         if (!alive && gt == 0) fail(a.status, abort_flag, ERR_EPI);
-        if (gt == 0) bulk_wait0();
+    } else if (wg == 3) {
+        // ---------------------------------------------------------- output drain (4 warps)
+        // Thread (warp % 4, lane) owns dv column d of the tile in all 64 rows of each chunk:
+        // O^T TMEM -> registers -> bf16 smem tile -> TMA store, 32 rows at a time.
+        regs_dec<Regs<DK, BIL>::drain>();
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+        const int d = (warp & 3) * 32 + lane;
+        const int dt = threadIdx.x - 384;   // thread index within the drain warps
+        auto drain = [&](int m) -> bool {
+            const int b = m & 1;
+            const int c = c_begin + m;
+            float lbc_m = 0.f;   // B'_C[d] of chunk m (bilinear gate)
+            if constexpr (BIL) lbc_m = a.lbc[((size_t)bh * a.nchunks + c) * a.dv + dv0 + d];
+            const bool fq = SCAL && q_fac(c);   // per-head gate: output rows take lambda^(r+1)
+            const bool ok = mbar_wait(&o_full[b], (m >> 1) & 1, kTimeoutNs);
+            if (!group_all_ok(ok, BAR_DR, NDR)) return false;
+            tc_fence_after();
+            uint8_t* tile = sm + L::O_OFF + b * L::OB;
+            if constexpr (KH != 1) {
+                // the store issued from this tile two chunks ago must have read it
+                if (dt == 0) bulk_wait_read1();
+                named_bar_sync(BAR_DR, NDR);
+            }
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float w[32];
+                const int orow = c * C + h * 32;   // first row of this half
+                if constexpr (BIL) {
+                    // log beta of these 32 rows (rows past T add nothing), and an L2 prefetch of
+                    // chunk m+2's rows, one 128-byte line per thread
+                    const float* lp = a.lb + ((size_t)bh * a.T + orow) * a.dv + dv0 + d;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) w[t] = orow + t < a.T ? lp[(size_t)t * a.dv] : 0.f;
+                    const int prow = (c + 2) * C + h * 32 + dt / 4;
+                    if (c + 2 < c_end && prow < a.T)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.lb + ((size_t)bh * a.T + prow) * a.dv + dv0 +
+                                                                     (dt & 3) * 32));
+                }
+                if constexpr (KH == 2) {
+                    // the first key half's fp32 partial of these rows (rows past T: none)
+                    const float* pp = a.Opart + ((size_t)bh * a.T + orow) * a.dv + dv0 + d;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) w[t] = orow + t < a.T ? pp[(size_t)t * a.dv] : 0.f;
+                }
+                uint32_t r[32];
+                tmem_ld32(tO0 + b * 64 + lb + h * 32, r);
+                tmem_wait_ld();
+                if (h == 1) {
+                    tc_fence_before();
+                    mbar_arrive(&o_empty[b]);
+                }
+                if constexpr (BIL) {
+                    // exp(B'_r - B'_C): rows 0-31 from the prefix sum, rows 32-63 from the suffix
+                    // sum. Exponents are within [-kVGuard, kVGuard]; the fast exponential's error
+                    // there is far below the bf16 rounding of O (the parity tests hold the bf16
+                    // tolerance).
+                    if (h == 0) {
+                        float acc = -lbc_m;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            acc += w[t];
+                            w[t] = __expf(acc);
+                        }
+                    } else {
+                        float acc = 0.f;
+#pragma unroll
+                        for (int t = 31; t >= 0; --t) {
+                            const float x = w[t];
+                            w[t] = __expf(acc);
+                            acc -= x;
+                        }
+                    }
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * w[t]);
+                } else if (SCAL && fq) {
+                    // (r + 1) log lambda lies in [-kQGuard, 0] for every row r of the chunk
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        r[t] = __float_as_uint(__uint_as_float(r[t]) * __expf((float)(h * 32 + t + 1) * lam_h));
+                }
+                if constexpr (KH == 2) {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) + w[t]);
+                }
+                if constexpr (KH == 1) {
+                    // the partial goes out in fp32, one coalesced 128-byte row segment per warp and row
+                    float* pp = a.Opart + ((size_t)bh * a.T + orow) * a.dv + dv0 + d;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (orow + t < a.T) pp[(size_t)t * a.dv] = __uint_as_float(r[t]);
+                } else {
+                    __nv_bfloat16* ob =
+                        reinterpret_cast<__nv_bfloat16*>(tile) + (d >> 6) * (C * 64) + h * 32 * 64 + (d & 63);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) ob[t * 64] = __float2bfloat16_rn(__uint_as_float(r[t]));
+                }
+            }
+            if constexpr (KH != 1) {
+                fence_proxy_async_smem();
+                named_bar_sync(BAR_DR, NDR);
+                if (dt == 0) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        tma_store_3d(&tmO, tile + h * 32 * 64 * 2, dv0, c * C + h * 32, bh);
+                        tma_store_3d(&tmO, tile + C * 64 * 2 + h * 32 * 64 * 2, dv0 + 64, c * C + h * 32, bh);
+                    }
+                    bulk_commit();
+                }
+            }
+            return true;
+        };
+        bool alive = true;
+        if (want_out)
+            for (int m = 0; m < nloc && alive; ++m) alive = drain(m);
+        if (!alive && dt == 0) fail(a.status, abort_flag, ERR_DRAIN);
+        if (dt == 0) bulk_wait0();
     }
 
     tc_fence_before();
@@ -537,8 +635,27 @@ cudaError_t launch_dk(const FwdArgs& a, dim3 grid, const CUtensorMap& q, const C
     cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK, BIL, SCAL, KH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    gla_chunk_fwd_kernel<DK, BIL, SCAL, KH><<<grid, NT, L::SMEM, s>>>(a, q, k, v, A, o, qr);
-    return cudaGetLastError();
+    // the setmaxnreg split redistributes the 128 registers per thread the launch provides
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, gla_chunk_fwd_kernel<DK, BIL, SCAL, KH>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
+    // Programmatic stream serialization lets the CTAs start (barriers, tensor memory, S0)
+    // while the grid ahead finishes; the producer (and, for segment start states, the state
+    // epilogue) waits for that grid before reading what it wrote. Not for the bilinear gate
+    // (its head flags and column decays are read at once) or the second key half (it reads
+    // the first half's partial output).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (!BIL && KH != 2) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gla_chunk_fwd_kernel<DK, BIL, SCAL, KH>, a, q, k, v, A, o, qr);
 }
 
 }  // namespace

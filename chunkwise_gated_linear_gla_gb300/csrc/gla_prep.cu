@@ -263,6 +263,9 @@ __global__ void __launch_bounds__(NT, prep_ctas_per_sm<DK>())
 gla_chunk_prep_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmA)
 {
+    // the chunk pass may start (its set-up, its S0 loads) while this grid's last items run;
+    // it waits for this grid's writes before it reads them
+    launch_dependents();
     using L = PL<DK>;
     constexpr int RPT = L::RPT, NRG = L::NRG;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -601,6 +604,7 @@ __global__ void __launch_bounds__(NTU, prep_uniform_ctas_per_sm<DK, NTU>())
 gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                               const __grid_constant__ CUtensorMap tmA)
 {
+    launch_dependents();   // as in gla_chunk_prep_kernel
     constexpr int NCG = DK / 8, NRG = NTU / NCG, RPT = C / NRG;
     static_assert(RPT >= 1 && C % NRG == 0, "rows split evenly over the row groups");
     extern __shared__ __align__(16) uint8_t smem_raw[];

@@ -34,6 +34,8 @@ struct ScanArgs {
 
 __global__ void __launch_bounds__(NT) gla_state_scan_kernel(ScanArgs a)
 {
+    // the chunk pass may start its set-up now; it waits for this grid's writes before it reads them
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ float Gs[];   // [rows][nseg]
     const int bh = blockIdx.y;
     const size_t st = (size_t)a.dk * a.dv;

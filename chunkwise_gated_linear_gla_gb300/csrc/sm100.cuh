@@ -91,6 +91,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     }
 }
 
+// Two fp32 products in one packed instruction; each half rounds as one fp32 multiply
+// (round to nearest even), so the result is the same as two scalar multiplies.
+__device__ __forceinline__ void mul2_inplace(uint32_t& x0, uint32_t& x1, float2 g) {
+    asm("{\n\t.reg .b64 a, b;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "mul.rn.f32x2 a, a, b;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+r"(x0), "+r"(x1)
+        : "r"(__float_as_uint(g.x)), "r"(__float_as_uint(g.y)));
+}
+
+// Programmatic dependent launch. A grid launched with programmatic stream serialization
+// may start before the grid ahead of it in the stream has finished; grid_dependency_wait
+// blocks the calling thread until that grid has completed and its writes are visible (at
+// once when the grid was launched without the attribute). launch_dependents lets such a
+// dependent grid start once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- thread-block clusters
 // Distributed shared memory: a CTA addresses another CTA's shared memory through
 // the cluster window (mapa); mbarriers there can be arrived on, bulk copies and
