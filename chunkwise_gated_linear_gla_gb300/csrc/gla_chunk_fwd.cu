@@ -51,7 +51,7 @@ constexpr int DVT = kDvTile;
 constexpr int NSTAGE = 2;
 constexpr int NG = 4;                             // gate ring slots
 constexpr int G_AHEAD = 2;                        // gate loads run this many chunks ahead of the stages
-constexpr int PF_AHEAD = 3;                       // L2 prefetches run this many chunks ahead of the stage loads
+constexpr int PF_AHEAD = 2;                       // L2 prefetches run this many chunks ahead of the stage loads
 constexpr int NT = 512;
 constexpr int NEPI = 256;                         // state epilogue threads (warps 4-11)
 constexpr int NDR = 128;                          // output drain threads (warps 12-15)
