@@ -42,7 +42,7 @@ class gla_fwd_params(ctypes.Structure):
         ("dtype", ctypes.c_int), ("gate", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("force_segments", ctypes.c_int), ("path", ctypes.c_int),
-        ("log_b", ctypes.c_void_p),
+        ("log_b", ctypes.c_void_p), ("window_chunks", ctypes.c_int),
     ]
 
 
@@ -331,7 +331,7 @@ def gla_selftest_bounded_wait(limit_us: int, arrive: bool = False, stream=None, 
 # ---------------------------------------------------------------- marshalling helpers
 
 def make_params(q, k, v, log_g, S0, O, ST, gate=None, path=GLA_PATH_AUTO, force_segments=0,
-                workspace=None, chunk=64, log_b=None) -> gla_fwd_params:
+                workspace=None, chunk=64, log_b=None, window_chunks=0) -> gla_fwd_params:
     """Fill gla_fwd_params from torch tensors (shapes read from q and v).
     log_b (the bilinear gate's log beta, [B,H,T,dv]) selects GLA_GATE_BILINEAR."""
     import torch
@@ -355,11 +355,12 @@ def make_params(q, k, v, log_g, S0, O, ST, gate=None, path=GLA_PATH_AUTO, force_
     p.force_segments = force_segments
     p.path = path
     p.log_b = _ptr(log_b)
+    p.window_chunks = window_chunks
     return p
 
 
 def forward(q, k, v, log_g=None, S0=None, gate=None, want_state=True, path=GLA_PATH_AUTO,
-            force_segments=0, stream=None, O=None, ST=None, log_b=None):
+            force_segments=0, stream=None, O=None, ST=None, log_b=None, window_chunks=0):
     """Allocate O (and ST) and the workspace with torch, then call gla_fwd_ex.
 
     q, k: [B,H,T,dk]; v: [B,H,T,dv] (bf16 or fp32, on the GPU); log_g fp32
@@ -373,7 +374,8 @@ def forward(q, k, v, log_g=None, S0=None, gate=None, want_state=True, path=GLA_P
         O = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
     if ST is None and want_state:
         ST = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    p = make_params(q, k, v, log_g, S0, O, ST, gate, path, force_segments, log_b=log_b)
+    p = make_params(q, k, v, log_g, S0, O, ST, gate, path, force_segments, log_b=log_b,
+                    window_chunks=window_chunks)
     nbytes = gla_fwd_workspace_size(p)
     ws = None
     if nbytes > 0:

@@ -71,7 +71,7 @@ gla_status validate_args(const gla_fwd_params* p)
     if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT &&
         p->path != GLA_PATH_STAGED && p->path != GLA_PATH_FUSED)
         return GLA_ERR_INVALID_ARG;
-    if (p->force_segments < 0) return GLA_ERR_INVALID_ARG;
+    if (p->force_segments < 0 || p->window_chunks < 0) return GLA_ERR_INVALID_ARG;
     if (p->dk % 16 != 0 || p->dv % 16 != 0) return GLA_ERR_INVALID_ARG;
     if ((long long)p->B * p->H > (1LL << 30)) return GLA_ERR_INVALID_ARG;
     if (p->gate == GLA_GATE_NONE && p->log_g) return GLA_ERR_INVALID_ARG;
@@ -201,6 +201,7 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     pl.nseg = (bil || halves) ? 1 : choose_segments(p, units, pl.nchunks, sms > 0 ? sms : 148);
     pl.chunks_per_seg = (pl.nchunks + pl.nseg - 1) / pl.nseg;
     pl.nseg = (pl.nchunks + pl.chunks_per_seg - 1) / pl.chunks_per_seg;
+    pl.window = pl.nseg > 1 ? p->window_chunks : 0;
 
     const size_t BH = (size_t)p->B * p->H;
     size_t off = 0;
@@ -226,7 +227,9 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     int n = 0;
     pl.stages[n++] = STAGE_PREP;
     if (bil) pl.stages[n++] = STAGE_VALUE_PREP;
-    if (pl.nseg > 1) {
+    if (pl.nseg > 1 && pl.window > 0) {
+        pl.stages[n++] = STAGE_SEG_WINDOW;
+    } else if (pl.nseg > 1) {
         pl.stages[n++] = STAGE_SEG_STATE;
         pl.stages[n++] = STAGE_SEG_SCAN;
     }
@@ -250,6 +253,7 @@ const char* stage_name(StageKind k)
     case STAGE_SIMT_FLAGGED: return "gla_fwd_simt_flagged";
     case STAGE_CHUNK_FWD_HI: return "gla_chunk_fwd_keys_hi";
     case STAGE_FUSED: return "gla_chunk_fused";
+    case STAGE_SEG_WINDOW: return "gla_chunk_state_window";
     }
     return "?";
 }
@@ -282,6 +286,7 @@ gla_status run_stage(const gla_fwd_params* p, const Plan& pl, int i, cudaStream_
     case STAGE_PREP: e = launch_prep(*p, pl, p->workspace, c->status, s); break;
     case STAGE_SEG_STATE: e = launch_seg_state(*p, pl, p->workspace, c->status, s); break;
     case STAGE_SEG_SCAN: e = launch_seg_scan(*p, pl, p->workspace, c->status, s); break;
+    case STAGE_SEG_WINDOW: e = launch_seg_window(*p, pl, p->workspace, c->status, s); break;
     case STAGE_CHUNK_FWD:
         e = launch_chunk_fwd(*p, pl, p->workspace, pl.nseg > 1 ? kModeSegOut : kModeFull, c->status, s,
                              p->dk == 512 ? 1 : 0);

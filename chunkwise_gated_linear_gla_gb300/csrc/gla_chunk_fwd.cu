@@ -478,7 +478,8 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             const bool ok = mbar_wait(s_done, (nloc - 1) & 1, kTimeoutNs);
             if (group_all_ok(ok, BAR_EPI, NEPI)) {
                 tc_fence_after();
-                if (a.S_out) {
+                // (with per-segment start states, only the last segment's end state is kept)
+                if (a.S_out && (a.mode != kModeSegOut || seg == (int)gridDim.z - 1)) {
                     float* so = a.S_out + bh * a.s_out_bh + seg * a.s_out_seg + dv0 + d;
 #pragma unroll 1
                     for (int b = 0; b < NB; ++b) {
@@ -701,6 +702,8 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
         a.S_out = reinterpret_cast<float*>(base + pl.off_segS); a.s_out_bh = st * pl.nseg; a.s_out_seg = st;
     } else {
         a.S_in = reinterpret_cast<const float*>(base + pl.off_segin); a.s_in_bh = st * pl.nseg; a.s_in_seg = st;
+        // the sliding-window split has no scan to give S_T: the last segment's pass writes it
+        if (pl.window > 0 && p.ST) { a.S_out = p.ST; a.s_out_bh = st; a.s_out_seg = 0; }
     }
     a.gam = reinterpret_cast<const float*>(base + pl.off_gam);
     a.status = status;

@@ -46,6 +46,7 @@ enum StageKind {
     STAGE_SIMT_FLAGGED = 7,  // bilinear gate: the CUDA-core pass for the heads flagged out of range
     STAGE_CHUNK_FWD_HI = 8,  // dk = 512: the chunk pass over keys 256-511, adding the first half's partial O
     STAGE_FUSED = 9,         // per-key gate, dk = 256: gate prep inside the chunk pass (one cluster per head)
+    STAGE_SEG_WINDOW = 10,   // sliding-window split: each segment's start state from the window before it
 };
 
 struct Plan {
@@ -55,6 +56,7 @@ struct Plan {
     int n_dvt = 0;         // number of dv tiles
     int nseg = 1;          // sequence segments per (b,h)
     int chunks_per_seg = 0;
+    int window = 0;        // sliding-window split: chunks of the window (0: exact split)
     bool raw_qk = false;   // tensor path reads q,k directly (no gate)
     int sms = 0;           // multiprocessors of the device the plan was made for
     // workspace layout (byte offsets from the workspace base)
@@ -96,6 +98,9 @@ cudaError_t launch_fused(const gla_fwd_params& p, int* status, cudaStream_t s);
 // there ([BH][dk][dv]) instead of the workspace.
 cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s,
                              float* S_out = nullptr);
+// The sliding-window split: segment 0's start state is S0 (or zero); segment s > 0's is the
+// state the pl.window chunks before it leave from a zero start.
+cudaError_t launch_seg_window(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, int* status,
                             cudaStream_t s);
 

@@ -45,6 +45,7 @@ struct StateArgs {
     long long s_out_bh, s_out_seg;
     int* status;
     int dv, nchunks, cps, gated;
+    int win;            // > 0: segment s covers the win chunks before chunk s * cps (sliding window)
 };
 
 template <int DK>
@@ -98,8 +99,8 @@ gla_chunk_state_kernel(StateArgs a, const __grid_constant__ CUtensorMap tmK, con
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.y, seg = blockIdx.z;
     const int dv0 = blockIdx.x * DVT;
-    const int c_begin = seg * a.cps;
-    const int c_end = min(a.nchunks, c_begin + a.cps);
+    const int c_begin = a.win > 0 ? max(0, seg * a.cps - a.win) : seg * a.cps;
+    const int c_end = a.win > 0 ? seg * a.cps : min(a.nchunks, c_begin + a.cps);
     const int nloc = max(0, c_end - c_begin);
     const bool gated = a.gated != 0;
 
@@ -313,6 +314,42 @@ cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, 
     a.status = status;
     a.dv = p.dv; a.nchunks = pl.nchunks; a.cps = pl.chunks_per_seg;
     a.gated = p.gate != GLA_GATE_NONE;
+    a.win = 0;
+    dim3 grid(pl.n_dvt, (unsigned)BH, pl.nseg);
+    switch (p.dk) {
+    case 64: return launch_state_dk<64>(a, grid, mk, mv, s);
+    case 128: return launch_state_dk<128>(a, grid, mk, mv, s);
+    case 256: return launch_state_dk<256>(a, grid, mk, mv, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_seg_window(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s)
+{
+    if (pl.window <= 0 || pl.nseg < 2) return cudaErrorInvalidValue;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const uint64_t BH = (uint64_t)p.B * p.H;
+    const size_t st = (size_t)p.dk * p.dv;
+    float* segin = reinterpret_cast<float*>(base + pl.off_segin);
+    // segment 0 starts from S0 (or zero): [BH] blocks of st floats, nseg * st apart
+    cudaError_t e = p.S0 ? cudaMemcpy2DAsync(segin, pl.nseg * st * 4, p.S0, st * 4, st * 4, BH,
+                                             cudaMemcpyDeviceToDevice, s)
+                         : cudaMemset2DAsync(segin, pl.nseg * st * 4, 0, st * 4, BH, s);
+    if (e != cudaSuccess) return e;
+    const void* kb = pl.raw_qk ? p.k : base + pl.off_kt;
+    const uint64_t krows = pl.raw_qk ? (uint64_t)p.T : (uint64_t)pl.Tpad;
+    CUtensorMap mk, mv;
+    if (!map_tiles(&mk, kb, p.dk, krows, BH)) return cudaErrorInvalidValue;
+    if (!map_tiles(&mv, p.v, p.dv, p.T, BH)) return cudaErrorInvalidValue;
+    StateArgs a;
+    a.gam = reinterpret_cast<const float*>(base + pl.off_gam);
+    a.S_out = segin;   // segment s's window state goes to its start state; segment 0 has no window
+    a.s_out_bh = (long long)st * pl.nseg;
+    a.s_out_seg = (long long)st;
+    a.status = status;
+    a.dv = p.dv; a.nchunks = pl.nchunks; a.cps = pl.chunks_per_seg;
+    a.gated = p.gate != GLA_GATE_NONE;
+    a.win = pl.window;
     dim3 grid(pl.n_dvt, (unsigned)BH, pl.nseg);
     switch (p.dk) {
     case 64: return launch_state_dk<64>(a, grid, mk, mv, s);

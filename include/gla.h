@@ -123,7 +123,28 @@ typedef struct {
     int force_segments;     /* 0: the planner chooses the sequence split; n >= 1: use n segments */
     int path;               /* gla_path */
     const float* log_b;     /* [B,H,T,dv] log(beta_t) for GLA_GATE_BILINEAR, else NULL */
+    int window_chunks;      /* 0 (default): exact. n > 0: the sliding-window split, see below */
 } gla_fwd_params;
+
+/*
+ * The sliding-window split (window_chunks = n > 0; off by default, and not
+ * exact). With a gate that decays, a state's influence on later tokens fades
+ * by the product of the gates in between, so a state started from zero a long
+ * enough window earlier is close to the true one (the FlashQLA talk, the
+ * "sliding window" property). When the plan splits the sequence into
+ * segments (GLA_PATH_TENSOR / STAGED / AUTO, force_segments or the planner),
+ * each segment after the first starts from the state that the n chunks of 64
+ * tokens before it leave from a zero start, instead of the exact state that
+ * the serial scan over all earlier segments gives; everything older is
+ * dropped, the sequence's S0 included once the window lies past it. The
+ * first segment starts from S0; S_T is the last segment's end state. The
+ * dropped part of segment s's start state is Diag(Gamma_w) S_w, with S_w the
+ * exact state at the window's first token and Gamma_w the product of the
+ * gates over the window, so the start state's error is at most
+ * max_k Gamma_w[k] * |S_w| and vanishes as the window grows. Ignored (the pass
+ * stays exact) when the plan has a single segment; the bilinear gate never
+ * splits. Negative: GLA_ERR_INVALID_ARG.
+ */
 
 /*
  * gla_fwd — the whole forward pass, with the bf16 data type.

@@ -9,8 +9,8 @@
 
 int main(void)
 {
-    printf("fwd %zu %zu %zu %zu\n", sizeof(gla_fwd_params), offsetof(gla_fwd_params, workspace),
-           offsetof(gla_fwd_params, path), offsetof(gla_fwd_params, log_b));
+    printf("fwd %zu %zu %zu %zu %zu\n", sizeof(gla_fwd_params), offsetof(gla_fwd_params, workspace),
+           offsetof(gla_fwd_params, path), offsetof(gla_fwd_params, log_b), offsetof(gla_fwd_params, window_chunks));
     printf("bwd %zu %zu %zu %zu %zu\n", sizeof(gla_bwd_params), offsetof(gla_bwd_params, workspace),
            offsetof(gla_bwd_params, path), offsetof(gla_bwd_params, log_b), offsetof(gla_bwd_params, grad_log_b));
     printf("status %s\n", gla_status_string(GLA_ERR_INVALID_ARG));

@@ -42,10 +42,11 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_struct_layout_matches_header():
-    # 7 pointers, 8 ints, pointer, size_t, 2 ints, pointer
-    assert ctypes.sizeof(bnd.gla_fwd_params) == 7 * 8 + 8 * 4 + 8 + 8 + 2 * 4 + 8
+    # 7 pointers, 8 ints, pointer, size_t, 2 ints, pointer, int (+ 4 bytes of tail padding)
+    assert ctypes.sizeof(bnd.gla_fwd_params) == 7 * 8 + 8 * 4 + 8 + 8 + 2 * 4 + 8 + 4 + 4
     assert bnd.gla_fwd_params.workspace.offset == 88
     assert bnd.gla_fwd_params.log_b.offset == 112
+    assert bnd.gla_fwd_params.window_chunks.offset == 120
 
 
 def test_plain_c_client_sees_the_binding_layout(lib, tmp_path):
@@ -68,7 +69,7 @@ def test_plain_c_client_sees_the_binding_layout(lib, tmp_path):
     fwd = [int(x) for x in out[0].split()[1:]]
     bwd = [int(x) for x in out[1].split()[1:]]
     F, Bw = bnd.gla_fwd_params, bnd.gla_bwd_params
-    assert fwd == [ctypes.sizeof(F), F.workspace.offset, F.path.offset, F.log_b.offset]
+    assert fwd == [ctypes.sizeof(F), F.workspace.offset, F.path.offset, F.log_b.offset, F.window_chunks.offset]
     assert bwd == [ctypes.sizeof(Bw), Bw.workspace.offset, Bw.path.offset, Bw.log_b.offset, Bw.grad_log_b.offset]
     assert out[2].startswith("status GLA_ERR_INVALID_ARG")
     assert int(out[3].split()[1]) == gla.gla_version()
@@ -176,6 +177,20 @@ def test_plan_on_host():
     p.force_segments = 4
     names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
     assert names == ["gla_chunk_prep", "gla_chunk_state", "gla_state_scan", "gla_chunk_fwd"]
+    ws_exact = bnd.gla_fwd_workspace_size(p)
+    # the sliding-window split (opt-in) replaces the state pass and the scan with one window
+    # pass; the same workspace
+    p.window_chunks = 4
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_prep", "gla_chunk_state_window", "gla_chunk_fwd"]
+    assert bnd.gla_fwd_workspace_size(p) == ws_exact
+    # without a split the window changes nothing
+    p.force_segments = 1
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_prep", "gla_chunk_fwd"]
+    p.window_chunks = -1
+    assert bnd.gla_fwd_num_stages(p) == -1 and bnd.gla_fwd_ex(p, stream=0, check=False) == bnd.GLA_ERR_INVALID_ARG
+    p.window_chunks = 0
     # fp32 takes the CUDA-core path, no workspace
     p = _params(dtype=bnd.GLA_FP32)
     assert [bnd.gla_fwd_stage_name(p, 0)] == ["gla_fwd_simt"]
