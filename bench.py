@@ -428,6 +428,18 @@ def run_backward(args, w):
     ms = sum(times) / len(times)
     flops = algorithmic_bwd(w)
     tflops = flops / (ms * 1e-3) / 1e12
+    tensor = w.dtype == torch.bfloat16 and w.dk in (64, 128, 256) and w.gate != gi.GATE_BILINEAR
+    if tensor:
+        # the chunk products run on the tensor cores (mma.sync, bf16 operands split into hi + lo
+        # parts, fp32 accumulation): rated against the bf16 tensor peak, as one product per FLOP
+        _, bf16_burst, _, src = peaks()
+        roof = {"kernel": "gla_bwd (tensor-core chunk products, all stages)", "bound": "tensor",
+                "achieved": tflops, "peak": bf16_burst, "unit": "TFLOP/s", "frac": tflops / bf16_burst,
+                "traffic": None, "peak_source": f"{src} dense bf16 (burst: the pass is timed alone)"}
+    else:
+        roof = {"kernel": "gla_bwd (CUDA cores, all stages)", "bound": "alu", "achieved": tflops,
+                "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tflops / FP32_ALU_TFLOPS, "traffic": None,
+                "peak_source": "nominal fp32 FFMA rate: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz"}
     launches = 4 + (1 if w.gate in (gi.GATE_TOKEN_SCALAR, gi.GATE_HEAD_SCALAR) else 0) - (1 if w.gate == 0 else 0)
     line = {
         "metric": BWD_METRIC, "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
@@ -438,9 +450,7 @@ def run_backward(args, w):
                                f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar', 'bilinear'][w.gate]}",
                    "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",
                    "workspace_bytes": nbytes},
-        "roofline": {"kernel": "gla_bwd (CUDA cores, all stages)", "bound": "alu", "achieved": tflops,
-                     "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tflops / FP32_ALU_TFLOPS, "traffic": None,
-                     "peak_source": "nominal fp32 FFMA rate: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz"},
+        "roofline": roof,
         "timing": {"mean_ms": ms, "median_ms": times[len(times) // 2], "min_ms": times[0]},
         "cpu_baseline": cpu,
         "e2e": None,
