@@ -7,7 +7,8 @@ load the library; the first call does, and raises if it is not built.
 from .binding import (  # noqa: F401
     GLA_BF16, GLA_FP32, GLA_GATE_BILINEAR, GLA_GATE_HEAD_SCALAR, GLA_GATE_NONE, GLA_GATE_PER_KEY,
     GLA_GATE_TOKEN_SCALAR,
-    GLA_PATH_AUTO, GLA_PATH_FUSED, GLA_PATH_SIMT, GLA_PATH_STAGED, GLA_PATH_TENSOR, GlaError, backward, forward, gla_bwd,
+    GLA_PATH_AUTO, GLA_PATH_FUSED, GLA_PATH_SIMT, GLA_PATH_SPLIT, GLA_PATH_STAGED, GLA_PATH_TENSOR, GlaError,
+    backward, forward, gla_bwd,
     gla_bwd_workspace_size, gla_device_status,
     gla_fwd, gla_fwd_ex, gla_fwd_host, gla_fwd_num_stages, gla_fwd_stage, gla_fwd_stage_name,
     gla_fwd_workspace_size, gla_host_release, gla_pair_combine, gla_pair_scan, gla_segment_pair,

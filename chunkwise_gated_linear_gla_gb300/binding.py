@@ -16,7 +16,7 @@ from . import build as _build
 GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_CUDA, GLA_ERR_WORKSPACE, GLA_ERR_TIMEOUT = range(6)
 GLA_BF16, GLA_FP32 = 0, 1
 GLA_GATE_NONE, GLA_GATE_HEAD_SCALAR, GLA_GATE_PER_KEY, GLA_GATE_TOKEN_SCALAR, GLA_GATE_BILINEAR = 0, 1, 2, 3, 4
-GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT, GLA_PATH_STAGED, GLA_PATH_FUSED = 0, 1, 2, 3, 4
+GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT, GLA_PATH_STAGED, GLA_PATH_FUSED, GLA_PATH_SPLIT = 0, 1, 2, 3, 4, 5
 
 # Every symbol include/gla.h declares.
 EXPORTED = ("gla_fwd", "gla_fwd_ex", "gla_fwd_workspace_size", "gla_fwd_num_stages",

@@ -33,6 +33,8 @@
 // tokens), gla_bwd_token_gate / gla_bwd_head_gate (per-token or per-head gate
 // gradients). Every reduction has a fixed order, so results are bitwise
 // reproducible.
+#include <cstring>
+
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
@@ -1140,6 +1142,64 @@ bool tc_shape_ok(const gla_bwd_params* p) {
     return p->dtype == GLA_BF16 && (p->dk == 64 || p->dk == 128 || p->dk == 256) && p->gate != GLA_GATE_BILINEAR;
 }
 
+// The 64-row chunk-parallel form on tcgen05 (gla_bwd_chunk.cu and the chunk pass's state
+// sweeps): bf16, dk in {128, 256}, dv a multiple of 128, q, k, v and grad_O on 16-byte
+// boundaries (tensor-memory-access copies).
+bool chunk_shape_ok(const gla_bwd_params* p) {
+    const long long BH = (long long)p->B * p->H;
+    const long long rows = (((long long)p->T + kChunk - 1) / kChunk) * kChunk;
+    auto al16 = [](const void* x) { return reinterpret_cast<uintptr_t>(x) % 16 == 0; };
+    return p->dtype == GLA_BF16 && (p->dk == 128 || p->dk == 256) && p->dv % kDvTile == 0 &&
+           p->gate != GLA_GATE_BILINEAR && BH <= 65535 && BH * rows < (1LL << 31) && al16(p->q) && al16(p->k) &&
+           al16(p->v) && al16(p->grad_O);
+}
+
+enum BwdKind { BWD_SIMT, BWD_SPLIT, BWD_CHUNK };
+
+BwdKind bwd_kind(const gla_bwd_params* p) {
+    if (p->dtype == GLA_FP32 || p->path == GLA_PATH_SIMT) return BWD_SIMT;
+    if (p->path == GLA_PATH_SPLIT) return BWD_SPLIT;
+    if (p->T > 0 && chunk_shape_ok(p)) return BWD_CHUNK;   // AUTO or TENSOR
+    return tc_shape_ok(p) ? BWD_SPLIT : BWD_SIMT;
+}
+
+// Workspace of the chunk form: the prep's Q (.) Lambda, K (.) Gamma (gated), scores and
+// chunk decays; the two sweeps' chunk states H and D (bf16); S_T and the boundary term
+// (gate gradient with grad_ST); the per-token gate terms.
+struct ChunkPlan {
+    int nch = 0, Tpad = 0;
+    bool raw = false;
+    size_t off_qt = 0, off_kt = 0, off_A = 0, off_gam = 0, off_H = 0, off_D = 0, off_ST = 0, off_bnd = 0,
+           off_dla = 0, bytes = 0;
+};
+
+ChunkPlan chunk_plan(const gla_bwd_params* p)
+{
+    ChunkPlan c;
+    const size_t BH = (size_t)p->B * p->H;
+    c.nch = (p->T + kChunk - 1) / kChunk;
+    c.Tpad = c.nch * kChunk;
+    c.raw = p->gate == GLA_GATE_NONE;
+    size_t off = 0;
+    if (!c.raw) {
+        c.off_qt = off; off = up256(off + BH * c.Tpad * p->dk * 2);
+        c.off_kt = off; off = up256(off + BH * c.Tpad * p->dk * 2);
+    }
+    c.off_A = off;   off = up256(off + BH * c.nch * kChunk * kChunk * 2);
+    c.off_gam = off; off = up256(off + BH * c.nch * p->dk * 4);
+    c.off_H = off;   off = up256(off + BH * c.nch * p->dv * p->dk * 2);
+    c.off_D = off;   off = up256(off + BH * c.nch * p->dv * p->dk * 2);
+    if (p->grad_log_g) {
+        if (p->grad_ST) {
+            c.off_ST = off;  off = up256(off + BH * p->dk * p->dv * 4);
+            c.off_bnd = off; off = up256(off + BH * p->dk * 4);
+        }
+        c.off_dla = off; off = up256(off + BH * p->T * p->dk * 4);
+    }
+    c.bytes = off;
+    return c;
+}
+
 bool span_overlap(const void* a, size_t na, const void* b, size_t nb) {
     if (!a || !b || na == 0 || nb == 0) return false;
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -1162,10 +1222,12 @@ gla_status bwd_validate(const gla_bwd_params* p)
         return GLA_ERR_INVALID_ARG;
     if (p->T > 0 && (!p->q || !p->k || !p->v || !p->grad_O || !p->grad_q || !p->grad_k || !p->grad_v))
         return GLA_ERR_INVALID_ARG;
-    if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT)
+    if (p->path != GLA_PATH_AUTO && p->path != GLA_PATH_TENSOR && p->path != GLA_PATH_SIMT &&
+        p->path != GLA_PATH_SPLIT)
         return GLA_ERR_INVALID_ARG;
     if (p->dk > NT) return GLA_ERR_UNSUPPORTED;
-    if (p->path == GLA_PATH_TENSOR && !tc_shape_ok(p)) return GLA_ERR_UNSUPPORTED;
+    if (p->path == GLA_PATH_TENSOR && !chunk_shape_ok(p)) return GLA_ERR_UNSUPPORTED;
+    if (p->path == GLA_PATH_SPLIT && !tc_shape_ok(p)) return GLA_ERR_UNSUPPORTED;
     const size_t e = p->dtype == GLA_BF16 ? 2 : 4;
     if ((p->log_b && reinterpret_cast<uintptr_t>(p->log_b) % 4) ||
         (p->grad_log_b && reinterpret_cast<uintptr_t>(p->grad_log_b) % 4))
@@ -1226,6 +1288,93 @@ cudaError_t launch_states_tc(const BwdArgs& a, int BH, cudaStream_t s)
     return cudaGetLastError();
 }
 
+// The gate gradient from the per-token terms dla: the reverse cumulative sum over tokens
+// (per key: straight to grad_log_g), then the sums over keys (per token) or over batch rows,
+// tokens and keys (per head).
+cudaError_t launch_gate_tail(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s)
+{
+    cudaError_t e;
+    const int BH = p.B * p.H;
+    const size_t n = (size_t)BH * p.T * p.dk;
+    if (a.glog && n > 0) {
+        const bool per_key = p.gate == GLA_GATE_PER_KEY || p.gate == GLA_GATE_BILINEAR;
+        gla_bwd_revsum_kernel<<<dim3(BH, (p.dk + 31) / 32), NT, 0, s>>>(a, a.dla, per_key ? a.glog : a.dla, p.dk);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (p.gate == GLA_GATE_TOKEN_SCALAR) {
+            const size_t rows = (size_t)BH * p.T;
+            const int grid = (int)((rows * 32 + NT - 1) / NT < 4096 ? (rows * 32 + NT - 1) / NT : 4096);
+            gla_bwd_token_gate_kernel<<<grid, NT, 0, s>>>(a);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+    }
+    if (a.glog && p.gate == GLA_GATE_HEAD_SCALAR) {
+        if (n == 0) return cudaMemsetAsync(a.glog, 0, (size_t)p.H * sizeof(float), s);
+        gla_bwd_head_gate_kernel<<<p.H, NT, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 148;
+    return n;
+}
+
+// The chunk form: prep (Q (.) Lambda, K (.) Gamma, gamma, scores), the state sweep forward
+// (H, and S_T), the sweep of dL/dS backward (D, and dS0), the boundary term, the
+// chunk-parallel gradients, the gate tail.
+cudaError_t launch_chunk_form(const gla_bwd_params& p, const ChunkPlan& cp, uint8_t* w, int* status, cudaStream_t s)
+{
+    cudaError_t e;
+    const int sms = device_sm_count();
+    const int BH = p.B * p.H;
+    const bool gated = p.gate != GLA_GATE_NONE;
+    gla_fwd_params fp;
+    std::memset(&fp, 0, sizeof(fp));
+    fp.q = p.q; fp.k = p.k; fp.v = p.v; fp.log_g = p.log_g; fp.S0 = p.S0;
+    fp.B = p.B; fp.H = p.H; fp.T = p.T; fp.dk = p.dk; fp.dv = p.dv;
+    fp.dtype = p.dtype; fp.gate = p.gate; fp.path = GLA_PATH_TENSOR;
+    Plan pl;
+    pl.path = GLA_PATH_TENSOR;
+    pl.nchunks = cp.nch; pl.Tpad = cp.Tpad; pl.n_dvt = p.dv / kDvTile; pl.raw_qk = cp.raw; pl.sms = sms;
+    pl.off_qt = cp.off_qt; pl.off_kt = cp.off_kt; pl.off_A = cp.off_A; pl.off_gam = cp.off_gam;
+    if ((e = launch_prep(fp, pl, w, status, s, false)) != cudaSuccess) return e;
+    const void* qt = cp.raw ? p.q : static_cast<const void*>(w + cp.off_qt);
+    const void* kt = cp.raw ? p.k : static_cast<const void*>(w + cp.off_kt);
+    const long long kt_rows = cp.raw ? p.T : cp.Tpad;
+    const float* gam = gated ? reinterpret_cast<const float*>(w + cp.off_gam) : nullptr;
+    float* ST = cp.off_ST ? reinterpret_cast<float*>(w + cp.off_ST) : nullptr;
+    float* bnd = cp.off_bnd ? reinterpret_cast<float*>(w + cp.off_bnd) : nullptr;
+    StateSweep fw;
+    fw.kt = kt; fw.kt_rows = kt_rows; fw.v = p.v; fw.gam = gam; fw.S_in = p.S0; fw.S_out = ST;
+    fw.Hst = w + cp.off_H; fw.reverse = false;
+    fw.BH = BH; fw.T = p.T; fw.dk = p.dk; fw.dv = p.dv; fw.nch = cp.nch;
+    if ((e = launch_state_sweep(fw, status, s)) != cudaSuccess) return e;
+    StateSweep rv = fw;
+    rv.kt = qt; rv.v = p.grad_O; rv.S_in = p.grad_ST; rv.S_out = p.grad_S0; rv.Hst = w + cp.off_D; rv.reverse = true;
+    if ((e = launch_state_sweep(rv, status, s)) != cudaSuccess) return e;
+    if (ST && bnd && (e = launch_bwd_boundary(p.grad_ST, ST, bnd, (long long)BH * p.dk, p.dv, sms, s)) != cudaSuccess)
+        return e;
+    BwdGrads g;
+    g.q = p.q; g.k = p.k; g.v = p.v; g.dO = p.grad_O; g.log_g = p.log_g;
+    g.qt = qt; g.kt = kt; g.kt_rows = kt_rows;
+    g.A = w + cp.off_A; g.gam = gam;
+    g.Hst = w + cp.off_H; g.Dst = w + cp.off_D;
+    g.bnd = bnd;
+    g.gq = p.grad_q; g.gk = p.grad_k; g.gv = p.grad_v;
+    g.dla = p.grad_log_g ? reinterpret_cast<float*>(w + cp.off_dla) : nullptr;
+    g.BH = BH; g.H = p.H; g.T = p.T; g.dk = p.dk; g.dv = p.dv; g.gate = p.gate; g.sms = sms;
+    if ((e = launch_bwd_grads(g, status, s)) != cudaSuccess) return e;
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.B = p.B; a.H = p.H; a.T = p.T; a.dk = p.dk; a.dv = p.dv; a.gate = p.gate;
+    a.glog = p.grad_log_g;
+    a.dla = g.dla;
+    return launch_gate_tail(a, p, s);
+}
+
 template <typename Tin>
 cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s, bool use_tc)
 {
@@ -1268,27 +1417,11 @@ cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s
         gla_bwd_finish_kernel<Tin><<<grid, NT, 0, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (a.glog && n > 0) {
-        const bool per_key = p.gate == GLA_GATE_PER_KEY || p.gate == GLA_GATE_BILINEAR;
-        gla_bwd_revsum_kernel<<<dim3(BH, (p.dk + 31) / 32), NT, 0, s>>>(a, a.dla, per_key ? a.glog : a.dla, p.dk);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if (p.gate == GLA_GATE_TOKEN_SCALAR) {
-            const size_t rows = (size_t)BH * p.T;
-            const int grid = (int)((rows * 32 + NT - 1) / NT < 4096 ? (rows * 32 + NT - 1) / NT : 4096);
-            gla_bwd_token_gate_kernel<<<grid, NT, 0, s>>>(a);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        }
-    }
     if (a.glb && n > 0) {   // bilinear gate: dlog beta from the chunk sweep's per-token terms
         gla_bwd_revsum_kernel<<<dim3(BH, (p.dv + 31) / 32), NT, 0, s>>>(a, a.dlbe, a.glb, p.dv);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (a.glog && p.gate == GLA_GATE_HEAD_SCALAR) {
-        if (n == 0) return cudaMemsetAsync(a.glog, 0, (size_t)p.H * sizeof(float), s);
-        gla_bwd_head_gate_kernel<<<p.H, NT, 0, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    return launch_gate_tail(a, p, s);
 }
 
 }  // namespace
@@ -1299,13 +1432,22 @@ using namespace gla;
 extern "C" size_t gla_bwd_workspace_size(const gla_bwd_params* p)
 {
     if (bwd_validate(p) != GLA_OK) return 0;
-    return bwd_plan(p).bytes;
+    return bwd_kind(p) == BWD_CHUNK ? chunk_plan(p).bytes : bwd_plan(p).bytes;
 }
 
 extern "C" gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream)
 {
     gla_status st = bwd_validate(p);
     if (st != GLA_OK) return st;
+    const BwdKind kind = bwd_kind(p);
+    if (kind == BWD_CHUNK) {
+        const ChunkPlan cp = chunk_plan(p);
+        if (!p->workspace || p->workspace_bytes < cp.bytes) return GLA_ERR_WORKSPACE;
+        int* status = device_status_ptr();
+        if (!status) return GLA_ERR_CUDA;
+        const cudaError_t e = launch_chunk_form(*p, cp, static_cast<uint8_t*>(p->workspace), status, stream);
+        return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+    }
     const BwdPlan pl = bwd_plan(p);
     if (!p->workspace || p->workspace_bytes < pl.bytes) return GLA_ERR_WORKSPACE;
     uint8_t* w = static_cast<uint8_t*>(p->workspace);
@@ -1324,7 +1466,7 @@ extern "C" gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream)
     a.glb = p->grad_log_b;
     a.dlbe = p->gate == GLA_GATE_BILINEAR ? reinterpret_cast<float*>(w + pl.off_dlbe) : nullptr;
     a.nch = pl.nch; a.ndvt = pl.ndvt;
-    const bool use_tc = p->path != GLA_PATH_SIMT && tc_shape_ok(p);
+    const bool use_tc = kind == BWD_SPLIT;
     a.nplanes = pl.ndvt + (use_tc ? 1 : 0);
     const cudaError_t e = p->dtype == GLA_FP32 ? launch_all<float>(a, *p, stream, false)
                                                : launch_all<__nv_bfloat16>(a, *p, stream, use_tc);

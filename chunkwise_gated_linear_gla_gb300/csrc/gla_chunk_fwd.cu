@@ -84,7 +84,11 @@ struct FwdArgs {
     union { const float* lb; const float* lamh; };
     const int* skip;    // [BH] heads left to the CUDA-core pass
     int T, H;
+    // state sweeps (kModeSweep / kModeSweepRev): the state entering each chunk's update,
+    // bf16 [BH][nchunks][dv][dk] (row d holds column d of the state)
+    __nv_bfloat16* Hst;
 };
+static_assert(sizeof(FwdArgs) <= 128, "FwdArgs stays within 128 bytes");
 
 template <int DK, bool BIL>
 struct Lay {
@@ -177,7 +181,12 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     const int c_begin = seg * a.cps;
     const int c_end = min(a.nchunks, c_begin + a.cps);
     const int nloc = max(0, c_end - c_begin);
-    const bool want_out = a.mode != kModeSegState;
+    const bool want_out = a.mode == kModeFull || a.mode == kModeSegOut;
+    // the state sweeps keep the state entering every chunk; the reverse one walks the chunks
+    // from the last (the backward's recurrence for dL/dS)
+    const bool sweep = !BIL && !SCAL && KH == 0 && (a.mode == kModeSweep || a.mode == kModeSweepRev);
+    const bool rev = sweep && a.mode == kModeSweepRev;
+    auto chunk_of = [&](int j) { return rev ? c_end - 1 - j : c_begin + j; };
     const bool gated = a.gated != 0;
     // per-head scalar gate: whether chunk ch's query factor is left to this pass (the prep
     // made the same decision on the same float, rows x log lambda)
@@ -220,7 +229,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         if (lane == 0) {
             // chunk j's gate decays into ring slot j % NG, once chunk j - NG's decay has read it
             auto load_g = [&](int j) -> bool {
-                const int sl = j % NG, c = c_begin + j;
+                const int sl = j % NG, c = chunk_of(j);
                 if (j >= NG && !mbar_wait(&gempty[sl], ((j / NG) - 1) & 1, kTimeoutNs)) return false;
                 uint8_t* gs = sm + L::GR_OFF + sl * L::GSL;
                 mbar_arrive_expect_tx(&gfull[sl], L::GSL);
@@ -237,7 +246,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 for (; gissued < G_AHEAD && gissued < nloc; ++gissued) load_g(gissued);
             for (int n = 0; n < nloc; ++n) {
                 if (*abort_flag) break;
-                const int st = n & 1, c = c_begin + n;
+                const int st = n & 1, c = chunk_of(n);
                 if (n >= 2 && !mbar_wait(&empty[st], ((n >> 1) - 1) & 1, kTimeoutNs)) {
                     fail(a.status, abort_flag, ERR_PRODUCER);
                     break;
@@ -294,7 +303,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     __nanosleep(64);
                 }
                 if (!go) break;
-                const int cp = c_begin + m + PF_AHEAD;
+                const int cp = chunk_of(m + PF_AHEAD);
                 prefetch_l2_tile_3d(&tmV, dv0, cp * C, bh);
                 prefetch_l2_tile_3d(&tmV, dv0 + 64, cp * C, bh);
                 const int nt = gridDim.x, me = blockIdx.x;
@@ -310,8 +319,8 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     if (KH != 2 && item % nt == me) prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
                     ++item;
                 }
-                if (gated && item % nt == me && cp + G_AHEAD < c_end)
-                    prefetch_l2(a.gam + ((size_t)bh * a.nchunks + cp + G_AHEAD) * DKT + KOFF, L::GB);
+                if (gated && item % nt == me && m + PF_AHEAD + G_AHEAD < nloc)
+                    prefetch_l2(a.gam + ((size_t)bh * a.nchunks + chunk_of(m + PF_AHEAD + G_AHEAD)) * DKT + KOFF, L::GB);
             }
         }
     } else if (warp == 1) {
@@ -438,6 +447,17 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         P[c2 / 2 + i] = pack_bf16(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                }
+                if (sweep) {
+                    // the state entering this chunk's update, 32 keys of row d: four 16-byte stores
+                    uint4* hp = reinterpret_cast<uint4*>(
+                        a.Hst + (((size_t)bh * a.nchunks + chunk_of(n)) * a.dv + dv0 + d) * DK + cb + c2);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        hp[i] = make_uint4(pack_bf16(__uint_as_float(r0[8 * i]), __uint_as_float(r0[8 * i + 1])),
+                                           pack_bf16(__uint_as_float(r0[8 * i + 2]), __uint_as_float(r0[8 * i + 3])),
+                                           pack_bf16(__uint_as_float(r0[8 * i + 4]), __uint_as_float(r0[8 * i + 5])),
+                                           pack_bf16(__uint_as_float(r0[8 * i + 6]), __uint_as_float(r0[8 * i + 7])));
                 }
                 if (gated) {
                     // two columns per packed multiply (each lane rounds as a single fp32 multiply)
@@ -717,6 +737,7 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     a.skip = bil ? reinterpret_cast<const int*>(base + pl.off_flag) : nullptr;
     a.T = p.T;
     a.H = p.H;
+    a.Hst = nullptr;
     dim3 grid(pl.n_dvt, (unsigned)BH, mode == kModeFull ? 1 : pl.nseg);
     if (kh) {
         // dk = 512 in two key halves of 256: each half its own rows of S0 / S_T, the first
@@ -749,6 +770,38 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     case 64: return launch_dk<64, false, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
     case 128: return launch_dk<128, false, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
     case 256: return launch_dk<256, false, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_state_sweep(const StateSweep& w, int* status, cudaStream_t s)
+{
+    if (w.dv % DVT != 0 || w.nch <= 0 || !w.Hst) return cudaErrorInvalidValue;
+    const uint64_t BH = (uint64_t)w.BH;
+    CUtensorMap mk, mv;
+    if (!map3(&mk, w.kt, w.dk, (uint64_t)w.kt_rows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (!map3(&mv, w.v, w.dv, w.T, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    FwdArgs a;
+    const long long st = (long long)w.dk * w.dv;
+    a.S_in = w.S_in; a.s_in_bh = st; a.s_in_seg = 0;
+    a.S_out = w.S_out; a.s_out_bh = st; a.s_out_seg = 0;
+    a.gam = w.gam;
+    a.status = status;
+    a.dv = w.dv; a.nchunks = w.nch; a.cps = w.nch;
+    a.mode = w.reverse ? kModeSweepRev : kModeSweep;
+    a.gated = w.gam != nullptr;
+    a.lbc = nullptr;
+    a.lb = nullptr;
+    a.skip = nullptr;
+    a.T = w.T;
+    a.H = 1;
+    a.Hst = static_cast<__nv_bfloat16*>(w.Hst);
+    const dim3 grid(w.dv / DVT, (unsigned)BH, 1);
+    // no O, Q or score tile is read in a sweep: the K map stands in for those arguments
+    switch (w.dk) {
+    case 64: return launch_dk<64, false, false>(a, grid, mk, mk, mv, mk, mv, mk, s);
+    case 128: return launch_dk<128, false, false>(a, grid, mk, mk, mv, mk, mv, mk, s);
+    case 256: return launch_dk<256, false, false>(a, grid, mk, mk, mv, mk, mv, mk, s);
     }
     return cudaErrorInvalidValue;
 }

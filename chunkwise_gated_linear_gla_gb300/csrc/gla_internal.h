@@ -84,7 +84,10 @@ int* device_status_ptr();   // nullptr on failure
 // launch_simt: with `only` non-null, just the heads bh with only[bh] != 0.
 cudaError_t launch_simt(const gla_fwd_params& p, int* status, cudaStream_t s, const int* only = nullptr);
 cudaError_t launch_value_prep(const gla_fwd_params& p, const Plan& pl, void* ws, cudaStream_t s);
-cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s);
+// allow_qfac = false: the per-head scalar gate's chunks always get Q (.) Lambda and plain
+// scores (the backward reads them as such)
+cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s,
+                        bool allow_qfac = true);
 // kh: 0, or for dk = 512 the key half (1: keys 0-255 with the intra term, O as an fp32
 // partial; 2: keys 256-511, adding that partial)
 cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, int mode,
@@ -122,5 +125,44 @@ cudaError_t launch_wait_selftest(int* status, unsigned limit_us, bool arrive, cu
 constexpr int kModeFull = 0;        // O and final state from S0 (single segment)
 constexpr int kModeSegState = 1;    // per-segment state from zero, no O
 constexpr int kModeSegOut = 2;      // O from per-segment start states, no final state
+constexpr int kModeSweep = 3;       // no O: the state entering every chunk to Hst, the final state
+constexpr int kModeSweepRev = 4;    // the same over the chunks from the last (dL/dS for the backward)
+
+// The chunk pass as a state sweep for the backward (gla_chunk_fwd.cu): with X = S_in,
+// for each chunk c in order (from the last when `reverse`): Hst[c] <- bf16(X), then
+// X <- Diag(gam[c]) X + KT[c]^T V[c]; S_out <- X at the end. KT: [BH][kt_rows][dk] bf16
+// (rows past T zero), V: [BH][T][dv] bf16, gam: [BH][nch][dk] or null (no gate), S_in,
+// S_out: [BH][dk][dv] fp32 or null, Hst: [BH][nch][dv][dk] bf16. dk in {64, 128, 256},
+// dv a multiple of 128.
+struct StateSweep {
+    const void* kt; long long kt_rows;
+    const void* v;
+    const float* gam;
+    const float* S_in;
+    float* S_out;
+    void* Hst;
+    bool reverse;
+    int BH, T, dk, dv, nch;
+};
+cudaError_t launch_state_sweep(const StateSweep& w, int* status, cudaStream_t s);
+
+// The chunk-parallel gradients of the backward (gla_bwd_chunk.cu): dq, dk, dv and the gate
+// terms q (.) dq - k (.) dk per token, from the prep's Kt, Qt ([BH][kt_rows][dk] bf16), A and
+// gamma, and the two sweeps' H and D ([BH][nch][dv][dk] bf16). dk in {128, 256}, dv a
+// multiple of 128, T > 0. gam null without a gate; bnd ([BH][dk]) and dla may be null.
+struct BwdGrads {
+    const void* q; const void* k; const void* v; const void* dO;
+    const float* log_g;
+    const void* qt; const void* kt; long long kt_rows;
+    const void* A; const float* gam;
+    const void* Hst; const void* Dst;
+    const float* bnd;
+    float* gq; float* gk; float* gv; float* dla;
+    int BH, H, T, dk, dv, gate, sms;
+};
+cudaError_t launch_bwd_grads(const BwdGrads& g, int* status, cudaStream_t s);
+// rowsum(dST (.) ST) over each of `rows` rows of dv values
+cudaError_t launch_bwd_boundary(const float* dST, const float* ST, float* bnd, long long rows, int dv, int sms,
+                                cudaStream_t s);
 
 }  // namespace gla

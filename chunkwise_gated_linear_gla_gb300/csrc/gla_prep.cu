@@ -826,7 +826,8 @@ cudaError_t launch_prep_dk(const PrepArgs& a, const CUtensorMap& mq, const CUten
 
 }  // namespace
 
-cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s)
+cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* status, cudaStream_t s,
+                        bool allow_qfac)
 {
     uint8_t* base = static_cast<uint8_t*>(ws);
     PrepArgs a;
@@ -839,7 +840,7 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     a.A = reinterpret_cast<__nv_bfloat16*>(base + pl.off_A);
     a.status = status;
     a.BH = p.B * p.H; a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
-    a.qfac = q_factor_offload(p);
+    a.qfac = allow_qfac && q_factor_offload(p);
     a.pf_s0 = static_cast<const uint8_t*>(static_cast<const void*>(p.S0));
     a.pf_s0_bytes = p.S0 ? (size_t)a.BH * p.dk * p.dv * 4 : 0;
     a.pf_v = static_cast<const uint8_t*>(p.v);

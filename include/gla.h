@@ -103,7 +103,8 @@ typedef enum {
     GLA_PATH_TENSOR = 1,
     GLA_PATH_SIMT = 2,
     GLA_PATH_STAGED = 3,
-    GLA_PATH_FUSED = 4
+    GLA_PATH_FUSED = 4,
+    GLA_PATH_SPLIT = 5
 } gla_path;
 
 typedef struct {

@@ -10,14 +10,30 @@ q (.) dq - k (.) dk (and rowsum(dST (.) S_T)) over later tokens, and over keys
 and batch rows for the scalar gates; it can nearly cancel, so each element is
 held to 1e-5 times the same sum taken over the terms' absolute values.
 
-The tensor-core path (bf16 inputs, dk in {64, 128, 256}) splits every operand
-that is not a bf16 input (the chunk states, D, q (.) Lambda, k (.) Gamma) into
-hi + lo bf16 parts, so its products keep about 16 mantissa bits (2^-16 ~ 1.5e-5
-relative) with fp32 accumulation. It is held to relative Frobenius 5e-5 and
-max-abs 5e-4 * max|ref|. Its gate gradient, a sum of q (.) dq - k (.) dk in
-which dq and dk carry that error relative to their own (possibly cancelling)
-terms, is held over the whole tensor to relative Frobenius 2e-4 and max-abs
+The split path (GLA_PATH_SPLIT; what AUTO takes for bf16 with dk = 64 or dv
+not a multiple of 128) splits every operand that is not a bf16 input (the
+chunk states, D, q (.) Lambda, k (.) Gamma) into hi + lo bf16 parts, so its
+products keep about 16 mantissa bits (2^-16 ~ 1.5e-5 relative) with fp32
+accumulation. It is held to relative Frobenius 5e-5 and max-abs
+5e-4 * max|ref|. Its gate gradient, a sum of q (.) dq - k (.) dk in which dq
+and dk carry that error relative to their own (possibly cancelling) terms, is
+held over the whole tensor to relative Frobenius 2e-4 and max-abs
 2e-3 * max|ref|.
+
+The chunk form (GLA_PATH_TENSOR; what AUTO takes for bf16 with dk in
+{128, 256} and dv a multiple of 128) computes like the forward pass: bf16
+operands (q (.) Lambda, k (.) Gamma, the scores, the chunk states H and D,
+dO V^T), fp32 accumulation. It is held to the forward's bf16 contract
+(relative Frobenius 5e-3, max-abs 1e-2 * max|ref|) and, per element, to a
+bound on the rounding: each term of a gradient is a product of at most five
+bf16 roundings of exact values (for dv: k (.) Gamma twice, then D, itself a
+sum of rounded q (.) Lambda times dO, rounded once more), so its relative
+error is below 5 * 2^-9 < 2^-6, and the error of the element is below 2^-6
+times the sum of its terms' absolute values. That sum is the oracle's
+gradient of the absolute values of the inputs (every term is a product of
+inputs with a non-negative decay coefficient). The gate gradient, a reverse
+sum of q (.) dq - k (.) dk, is held to 2^-6 times the same sum taken over
+|q| (.) |dq|abs + |k| (.) |dk|abs (and |dST| (.) |S_T|abs at the last token).
 """
 import ctypes
 
@@ -36,11 +52,24 @@ from _util import errors, to_np
 REL_FRO, MAX_ABS = 2e-5, 2e-4
 TC_REL_FRO, TC_MAX_ABS = 5e-5, 5e-4
 TC_GATE_REL_FRO, TC_GATE_MAX_ABS = 2e-4, 2e-3
-AUTO, SIMT = bnd.GLA_PATH_AUTO, bnd.GLA_PATH_SIMT
+CH_REL_FRO, CH_MAX_ABS = 5e-3, 1e-2
+CH_TERM = 2.0 ** -6
+AUTO, SIMT, SPLIT, TENSOR = bnd.GLA_PATH_AUTO, bnd.GLA_PATH_SIMT, bnd.GLA_PATH_SPLIT, bnd.GLA_PATH_TENSOR
+
+
+def _kind(w, path):
+    """Which form runs: "simt", "split" or "chunk" (inputs 16-byte aligned)."""
+    if w.dtype != torch.bfloat16 or path == SIMT:
+        return "simt"
+    if path == SPLIT:
+        return "split"
+    if w.dk in (128, 256) and w.dv % 128 == 0 and w.T > 0 and w.gate != gi.GATE_BILINEAR:
+        return "chunk"
+    return "split" if w.dk in (64, 128, 256) else "simt"
 
 
 def _tensor(w, path):
-    return path != SIMT and w.dtype == torch.bfloat16 and w.dk in (64, 128, 256)
+    return _kind(w, path) == "split"
 GATES = [gi.GATE_NONE, gi.GATE_HEAD_SCALAR, gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR]
 
 
@@ -61,12 +90,29 @@ def _gpu(x, dO, dST, path=AUTO):
     return [None if t is None else to_np(t) for t in out]
 
 
-def _gate_abs_sum(x, dST, ref):
-    """The gate gradient's reductions applied to the absolute values of its terms."""
+def _abs(t):
+    return None if t is None else t.abs()
+
+
+def _mags(x, dO, dST):
+    """Per element, the sum of the absolute values of its terms: the oracle's gradients of
+    the inputs' absolute values under the same gates."""
+    return oracle.gla_backward(_abs(x["q"]), _abs(x["k"]), _abs(x["v"]), x["log_g"], x["gate"], _abs(x["S0"]),
+                               _abs(dO), _abs(dST))
+
+
+def _gate_abs_sum(x, dST, ref, mag=False):
+    """The gate gradient's reductions applied to the absolute values of its terms; with
+    `mag`, ref holds the magnitude gradients (_mags) and the final state is taken on the
+    inputs' absolute values too."""
     q, k = to_np(x["q"]), to_np(x["k"])
     terms = np.abs(q * ref[0]) + np.abs(k * ref[1])
     if dST is not None and q.shape[2] > 0:
-        _, ST = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
+        if mag:
+            _, ST = oracle.gla_forward(_abs(x["q"]), _abs(x["k"]), _abs(x["v"]), x["log_g"], x["gate"],
+                                       _abs(x["S0"]))
+        else:
+            _, ST = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
         terms[:, :, -1] += np.sum(np.abs(to_np(dST) * ST), axis=-1)
     rev = np.flip(np.cumsum(np.flip(terms, axis=2), axis=2), axis=2)
     if x["gate"] == gi.GATE_TOKEN_SCALAR:
@@ -76,12 +122,35 @@ def _gate_abs_sum(x, dST, ref):
     return rev
 
 
+def _check_chunk(x, dO, dST, got, ref, report=None, where=""):
+    """The chunk form's two bars: the bf16 contract per tensor and the rounding bound per element."""
+    mags = _mags(x, dO, dST)
+    for n, a, r, m in zip(["dq", "dk", "dv", "dlog_g", "dS0"], got, ref, mags):
+        if r is None:
+            assert a is None
+            continue
+        assert np.all(np.isfinite(a)), (n, where)
+        rf, ma = errors(a, r)
+        if report is not None:
+            report.append((n, rf, ma))
+        if n == "dlog_g":
+            bound = CH_TERM * _gate_abs_sum(x, dST, mags, mag=True) + 1e-30
+        else:
+            assert rf <= CH_REL_FRO and ma <= CH_MAX_ABS, (n, where, rf, ma)
+            bound = CH_TERM * np.asarray(m) + 1e-30
+        worst = (np.abs(a - r) / bound).max() if r.size else 0.0
+        assert worst <= 1.0, (n, where, "error / bound", worst)
+
+
 def _check(w, seed=0, dst=True, report=None, path=AUTO):
     x, dO, dST = _inputs(w, seed, dst)
     got = _gpu(x, dO, dST, path)
+    ref = oracle.gla_backward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], dO, dST)
+    if _kind(w, path) == "chunk":
+        _check_chunk(x, dO, dST, got, ref, report)
+        return got
     tc = _tensor(w, path)
     rel_fro, max_abs = (TC_REL_FRO, TC_MAX_ABS) if tc else (REL_FRO, MAX_ABS)
-    ref = oracle.gla_backward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], dO, dST)
     names = ["dq", "dk", "dv", "dlog_g", "dS0"]
     for n, a, r in zip(names, got, ref):
         if r is None:
@@ -132,7 +201,7 @@ def test_bwd_extreme_gates(dist):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("path", [AUTO, SIMT])
+@pytest.mark.parametrize("path", [AUTO, SPLIT, SIMT])
 def test_bwd_long_wide(path):
     gbuild.build(); oracle.build()
     w = gi.Workload("t", B=2, H=2, T=1000, dk=128, dv=256, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY,
@@ -143,7 +212,7 @@ def test_bwd_long_wide(path):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("path", [AUTO, SIMT])
+@pytest.mark.parametrize("path", [AUTO, SPLIT, SIMT])
 @pytest.mark.parametrize("gate", [gi.GATE_PER_KEY, gi.GATE_TOKEN_SCALAR, gi.GATE_NONE])
 def test_bwd_dk256_many_tiles(path, gate):
     gbuild.build(); oracle.build()
@@ -152,6 +221,45 @@ def test_bwd_dk256_many_tiles(path, gate):
     rep = []
     _check(w, seed=9, path=path, report=rep)
     print("dk256", path, gate, [(n, f"{rf:.1e}", f"{ma:.1e}") for n, rf, ma in rep])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("gate", GATES)
+@pytest.mark.parametrize("T", [1, 64, 65, 200])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (256, 256)])
+def test_bwd_chunk_form_gates_ragged(gate, T, dk, dv):
+    """The chunk form on every gate: one partial chunk, one whole chunk, a ragged tail,
+    several chunks; one and two key halves, odd and even numbers of dv blocks."""
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=2, H=2, T=T, dk=dk, dv=dv, dtype=torch.bfloat16, gate=gate, s0_std=0.3)
+    assert _kind(w, AUTO) == "chunk"
+    rep = []
+    _check(w, seed=T + 7 * gate + dk, report=rep, path=TENSOR)
+    print(gate, T, dk, dv, [(n, f"{rf:.1e}", f"{ma:.1e}") for n, rf, ma in rep])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dist", ["steep", "const:-60", "const:-1.2", "zero"])
+def test_bwd_chunk_form_extreme_gates(dist):
+    """Gates whose chunk decay falls below exp(-60) on some keys (const:-1.2 over 64 rows, and
+    steeper) take the pairwise intra rule for those keys; the result holds the same bars."""
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=1, H=2, T=150, dk=128, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY,
+                    gate_dist=dist, s0_std=0.2, qkv_scale="q")
+    rep = []
+    _check(w, seed=16, report=rep)
+    print(dist, [(n, f"{rf:.1e}", f"{ma:.1e}") for n, rf, ma in rep])
+
+
+@pytest.mark.gpu
+def test_bwd_chunk_form_many_items_per_cta():
+    """More (b, h, chunk) items than multiprocessors, so each CTA of the persistent gradient
+    kernel takes several chunks, with no S0 and no dST."""
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=3, H=4, T=1000, dk=128, dv=256, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY)
+    rep = []
+    _check(w, seed=17, dst=False, report=rep)
+    print("many items", [(n, f"{rf:.1e}", f"{ma:.1e}") for n, rf, ma in rep])
 
 
 @pytest.mark.gpu
@@ -216,13 +324,8 @@ def test_bwd_full_gla_layer_sampled_heads():
         sl = lambda t: None if t is None else t[b:b + 1, h:h + 1]
         ref = oracle.gla_backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["log_g"]), x["gate"], sl(x["S0"]),
                                   sl(dO), sl(dST))
-        for n, a, r in zip(["dq", "dk", "dv", "dlog_g", "dS0"], got, ref):
-            a = a[b:b + 1, h:h + 1]
-            rf, ma = errors(a, r)
-            if n == "dlog_g":
-                assert rf <= TC_GATE_REL_FRO and ma <= TC_GATE_MAX_ABS, (n, b, h, rf, ma)
-            else:
-                assert rf <= TC_REL_FRO and ma <= TC_MAX_ABS, (n, b, h, rf, ma)
+        xs = {n: (sl(t) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+        _check_chunk(xs, sl(dO), sl(dST), [a[b:b + 1, h:h + 1] for a in got], ref, where=(b, h))
 
 
 # ---------------------------------------------------------------- host-side checks (no GPU)
@@ -267,6 +370,12 @@ BAD = [
      bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
     ("tensor path with dk 48", dict(dk=48, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
+    ("tensor path with dk 64", dict(path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
+    ("tensor path with dv 192", dict(dk=128, dv=192, path=bnd.GLA_PATH_TENSOR), bnd.GLA_ERR_UNSUPPORTED),
+    ("tensor path with q off 16 bytes", dict(dk=128, dv=128, q=0x10008, path=bnd.GLA_PATH_TENSOR),
+     bnd.GLA_ERR_UNSUPPORTED),
+    ("split path with dk 48", dict(dk=48, path=bnd.GLA_PATH_SPLIT), bnd.GLA_ERR_UNSUPPORTED),
+    ("split path with fp32", dict(dtype=bnd.GLA_FP32, path=bnd.GLA_PATH_SPLIT), bnd.GLA_ERR_UNSUPPORTED),
     ("bad path", dict(path=7), bnd.GLA_ERR_INVALID_ARG),
     ("no workspace", dict(), bnd.GLA_ERR_WORKSPACE),
 ]
@@ -287,3 +396,22 @@ def test_bwd_workspace_size():
     nch, ndvt, BH = 7, 2, 6
     assert n >= 4 * (BH * nch * 64 * 128 + 2 * ndvt * BH * 100 * 64 + BH * 100 * 64)
     assert bnd.gla_bwd_workspace_size(_bp(dk=40)) == 0
+
+
+def test_bwd_chunk_form_workspace_size():
+    """The chunk form's workspace: Q (.) Lambda and K (.) Gamma, scores, chunk decays, the two
+    sweeps' bf16 chunk states, S_T and the boundary term (with grad_ST), the per-token gate
+    terms; less than the 16-row form's fp32 chunk states."""
+    gbuild.build()
+    far = {n: (i + 1) << 28 for i, n in enumerate(["q", "k", "v", "log_g", "grad_O", "grad_q", "grad_k", "grad_v",
+                                                   "grad_log_g", "grad_ST"])}
+    B, H, T, dk, dv = 2, 3, 100, 128, 256
+    p = _bp(B=B, H=H, T=T, dk=dk, dv=dv, **far)
+    n = bnd.gla_bwd_workspace_size(p)
+    BH, nch, Tpad = B * H, 2, 128
+    up = lambda x: (x + 255) // 256 * 256
+    want = (2 * up(BH * Tpad * dk * 2) + up(BH * nch * 64 * 64 * 2) + up(BH * nch * dk * 4)
+            + 2 * up(BH * nch * dv * dk * 2) + up(BH * dk * dv * 4) + up(BH * dk * 4) + up(BH * T * dk * 4))
+    assert n == want
+    split = bnd.gla_bwd_workspace_size(_bp(B=B, H=H, T=T, dk=dk, dv=dv, path=bnd.GLA_PATH_SPLIT, **far))
+    assert split > n
