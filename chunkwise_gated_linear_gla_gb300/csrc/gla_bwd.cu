@@ -1165,12 +1165,13 @@ BwdKind bwd_kind(const gla_bwd_params* p) {
 
 // Workspace of the chunk form: the prep's Q (.) Lambda, K (.) Gamma (gated), scores and
 // chunk decays; the two sweeps' chunk states H and D (bf16); S_T and the boundary term
-// (gate gradient with grad_ST); the per-token gate terms.
+// (gate gradient with grad_ST); the per-token gate terms (scalar gates; the per-key
+// gradient takes them in place) and their per-chunk totals.
 struct ChunkPlan {
     int nch = 0, Tpad = 0;
     bool raw = false;
     size_t off_qt = 0, off_kt = 0, off_A = 0, off_gam = 0, off_H = 0, off_D = 0, off_ST = 0, off_bnd = 0,
-           off_dla = 0, bytes = 0;
+           off_dla = 0, off_ctot = 0, bytes = 0;
 };
 
 ChunkPlan chunk_plan(const gla_bwd_params* p)
@@ -1194,7 +1195,10 @@ ChunkPlan chunk_plan(const gla_bwd_params* p)
             c.off_ST = off;  off = up256(off + BH * p->dk * p->dv * 4);
             c.off_bnd = off; off = up256(off + BH * p->dk * 4);
         }
-        c.off_dla = off; off = up256(off + BH * p->T * p->dk * 4);
+        if (p->gate != GLA_GATE_PER_KEY) {   // the per-key gradient is written in place
+            c.off_dla = off; off = up256(off + BH * p->T * p->dk * 4);
+        }
+        c.off_ctot = off; off = up256(off + BH * c.nch * p->dk * 4);
     }
     c.bytes = off;
     return c;
@@ -1364,15 +1368,32 @@ cudaError_t launch_chunk_form(const gla_bwd_params& p, const ChunkPlan& cp, uint
     g.Hst = w + cp.off_H; g.Dst = w + cp.off_D;
     g.bnd = bnd;
     g.gq = p.grad_q; g.gk = p.grad_k; g.gv = p.grad_v;
-    g.dla = p.grad_log_g ? reinterpret_cast<float*>(w + cp.off_dla) : nullptr;
+    const bool per_key = p.gate == GLA_GATE_PER_KEY;
+    g.R = !p.grad_log_g ? nullptr : per_key ? p.grad_log_g : reinterpret_cast<float*>(w + cp.off_dla);
+    g.ctot = p.grad_log_g ? reinterpret_cast<float*>(w + cp.off_ctot) : nullptr;
     g.BH = BH; g.H = p.H; g.T = p.T; g.dk = p.dk; g.dv = p.dv; g.gate = p.gate; g.sms = sms;
     if ((e = launch_bwd_grads(g, status, s)) != cudaSuccess) return e;
+    if (!p.grad_log_g) return cudaSuccess;
+    // the gate gradient: each chunk's terms are already summed over its later rows; add the
+    // totals of the later chunks (their reverse cumulative sum, in place, then a shifted add)
     BwdArgs a;
     std::memset(&a, 0, sizeof(a));
-    a.B = p.B; a.H = p.H; a.T = p.T; a.dk = p.dk; a.dv = p.dv; a.gate = p.gate;
+    a.B = p.B; a.H = p.H; a.T = cp.nch; a.dk = p.dk; a.dv = p.dv; a.gate = p.gate;
+    gla_bwd_revsum_kernel<<<dim3(BH, (p.dk + 31) / 32), NT, 0, s>>>(a, g.ctot, g.ctot, p.dk);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_bwd_gate_fixup(g.R, g.ctot, BH, p.T, p.dk, sms, s)) != cudaSuccess) return e;
+    if (per_key) return cudaSuccess;
+    a.T = p.T;
     a.glog = p.grad_log_g;
-    a.dla = g.dla;
-    return launch_gate_tail(a, p, s);
+    a.dla = g.R;
+    if (p.gate == GLA_GATE_TOKEN_SCALAR) {
+        const size_t rows = (size_t)BH * p.T;
+        const int grid = (int)((rows * 32 + NT - 1) / NT < 4096 ? (rows * 32 + NT - 1) / NT : 4096);
+        gla_bwd_token_gate_kernel<<<grid, NT, 0, s>>>(a);
+    } else {
+        gla_bwd_head_gate_kernel<<<p.H, NT, 0, s>>>(a);
+    }
+    return cudaGetLastError();
 }
 
 template <typename Tin>

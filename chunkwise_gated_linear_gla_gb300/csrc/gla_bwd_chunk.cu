@@ -78,7 +78,11 @@ struct GradArgs {
     const float* gam;         // [BH][nch][dk] or null (no gate)
     const float* bnd;         // [BH][dk] rowsum(dL/dS_T (.) S_T) or null
     float* gq; float* gk; float* gv;
-    float* dla;               // [BH][T][dk] or null
+    // gate terms q (.) dq - k (.) dk (+ the boundary term at T-1), summed over the later rows
+    // of the same chunk: R [BH][T][dk], and each chunk's total ctot [BH][nch][dk]; null
+    // without a gate gradient
+    float* R;
+    float* ctot;
     int* status;
     int BH, H, T, dv, nch, gate;
 };
@@ -415,6 +419,19 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
             }
             // every epilogue thread is past the previous chunk's use of the dA tile
             if (!group_all_ok(ok, BAR_EPI, NEPI)) break;
+            // this key's log gates over the chunk, loaded at once (rows past T read as 0), so
+            // that their latency overlaps the waits for the products
+            const int key = 128 * e + row;
+            float Bc[C];
+            if (e < NKH) {
+                const float* lg = nullptr;
+                size_t st = 0;
+                if (a.gate == GLA_GATE_PER_KEY) { lg = a.log_g + rb * DK + key; st = DK; }
+                else if (a.gate == GLA_GATE_TOKEN_SCALAR) { lg = a.log_g + rb; st = 1; }
+                else if (a.gate == GLA_GATE_HEAD_SCALAR) { lg = a.log_g + bh % a.H; st = 0; }
+#pragma unroll
+                for (int t = 0; t < C; ++t) Bc[t] = (lg && t < nr) ? lg[(size_t)t * st] : 0.f;
+            }
             // phase 2: dA to shared memory (bf16, masked), Kt and Qt to Kg and Qg (the Kt tile
             // and gamma once landed; Kt once the dv products are done with it)
             ok = mbar_wait(res_full, i & 1, kTimeoutNs);
@@ -450,81 +467,93 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
             const int usq = uq % NU;
             if (ok) ok = mbar_wait(&unit_full[usq], (uq / NU) & 1, kTimeoutNs);
             if (ok && gated) scale_keys<DK>(sm + L::UNIT_OFF + usq * 32768, gm, et, NEPI);
-            const int key = 128 * e + row;
             const float gk = (gated && e < NKH) ? gm[key] : 1.f;   // read before the slot is reloaded
             fence_proxy_async_smem();
             if (ok) mbar_arrive(dat_ready);
-            // phase 3: dq and dk of key `key` (warpgroup e = key half e)
+            // phase 3: dq and dk of key `key` (warpgroup e = key half e), rows from the last,
+            // with the gate terms summed over the later rows of the chunk
             if (ok && e < NKH) {
+#pragma unroll
+                for (int t = 1; t < C; ++t) Bc[t] += Bc[t - 1];   // Bc_t; rows past T add 0
+                const float tot = Bc[C - 1];                       // Bc_end
                 ok = __all_sync(0xffffffffu, mbar_wait(dqdk_full, i & 1, kTimeoutNs));
                 if (ok) {
                     tc_fence_after();
-                    float tot = 0.f;   // Bc_end of this key
-                    for (int t = 0; t < nr; ++t) tot += log_alpha<DK>(a, bh, c * C + t, key);
                     const bool steep = gated && !(gk >= kSteepGamma);
-                    float run = 0.f;
                     float* oq = a.gq + rb * DK + key;
                     float* ok_ = a.gk + rb * DK + key;
-                    float* od = a.dla ? a.dla + rb * DK + key : nullptr;
+                    float* oR = a.R ? a.R + rb * DK + key : nullptr;
                     const __nv_bfloat16* qr = a.q + rb * DK + key;
                     const __nv_bfloat16* kr = a.k + rb * DK + key;
                     const float bnd = (a.bnd && c == a.nch - 1) ? a.bnd[(size_t)bh * DK + key] : 0.f;
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t xq[32], xk[32];
-                        tmem_ld32(tmem + lb + TQ + e * 64 + 32 * h, xq);
-                        tmem_ld32(tmem + lb + TK + e * 64 + 32 * h, xk);
+                    float rsum = 0.f;
+#pragma unroll
+                    for (int qd = C / 16 - 1; qd >= 0; --qd) {
+                        uint32_t xq[16], xk[16];
+                        tmem_ld16(tmem + lb + TQ + e * 64 + 16 * qd, xq);
+                        tmem_ld16(tmem + lb + TK + e * 64 + 16 * qd, xk);
+                        float qv[16], kv[16];
+                        if (oR) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int r = 16 * qd + j;
+                                qv[j] = r < nr ? __bfloat162float(qr[(size_t)r * DK]) : 0.f;
+                                kv[j] = r < nr ? __bfloat162float(kr[(size_t)r * DK]) : 0.f;
+                            }
+                        }
                         tmem_wait_ld();
-                        if (h == 1) {
+                        if (qd == 0) {
                             tc_fence_before();
                             mbar_arrive(dqdk_empty);
                         }
-#pragma unroll 4
-                        for (int t = 0; t < 32; ++t) {
-                            const int r = 32 * h + t;
-                            if (r >= nr) break;
-                            run += log_alpha<DK>(a, bh, c * C + r, key);
-                            const float dq = expf(run) * __uint_as_float(xq[t]);
-                            const float dk = expf(tot - run) * __uint_as_float(xk[t]);
-                            oq[(size_t)r * DK] = dq;
-                            ok_[(size_t)r * DK] = dk;
-                            if (od) {
-                                float g = __bfloat162float(qr[(size_t)r * DK]) * dq -
-                                          __bfloat162float(kr[(size_t)r * DK]) * dk;
-                                if (c * C + r == a.T - 1) g += bnd;
-                                od[(size_t)r * DK] = g;
+#pragma unroll
+                        for (int j = 15; j >= 0; --j) {
+                            const int r = 16 * qd + j;
+                            if (r < nr) {
+                                const float dq = expf(Bc[r]) * __uint_as_float(xq[j]);
+                                const float dk = expf(tot - Bc[r]) * __uint_as_float(xk[j]);
+                                oq[(size_t)r * DK] = dq;
+                                ok_[(size_t)r * DK] = dk;
+                                if (oR) {
+                                    rsum += qv[j] * dq - kv[j] * dk;
+                                    if (c * C + r == a.T - 1) rsum += bnd;
+                                    oR[(size_t)r * DK] = rsum;
+                                }
                             }
                         }
                     }
                     if (steep) {
-                        // the intra terms of this key, pairwise: exp(Bc_t - Bc_s) <= 1 for t >= s
+                        // the intra terms of this key, pairwise: exp(Bc_t - Bc_s) <= 1 for t >= s;
+                        // then the gate terms again from the completed dq and dk
                         const uint8_t* dat = sm + L::DA_OFF;
-                        float Bc[C];
+                        float Bs[C];
                         float acc = 0.f;
                         for (int t = 0; t < nr; ++t) {
                             acc += log_alpha<DK>(a, bh, c * C + t, key);
-                            Bc[t] = acc;
+                            Bs[t] = acc;
                         }
                         for (int t = 0; t < nr; ++t) {
                             float sq = 0.f, sk = 0.f;
-                            for (int s = 0; s <= t; ++s)
-                                sq += bf16_at(dat + swz_off(t, s >> 3) + (s & 7) * 2) *
-                                      __bfloat162float(kr[(size_t)s * DK]) * expf(Bc[t] - Bc[s]);
+                            for (int s2 = 0; s2 <= t; ++s2)
+                                sq += bf16_at(dat + swz_off(t, s2 >> 3) + (s2 & 7) * 2) *
+                                      __bfloat162float(kr[(size_t)s2 * DK]) * expf(Bs[t] - Bs[s2]);
                             for (int u2 = t; u2 < nr; ++u2)
                                 sk += bf16_at(dat + swz_off(u2, t >> 3) + (t & 7) * 2) *
-                                      __bfloat162float(qr[(size_t)u2 * DK]) * expf(Bc[u2] - Bc[t]);
-                            const float dq = oq[(size_t)t * DK] + sq;
-                            const float dk = ok_[(size_t)t * DK] + sk;
-                            oq[(size_t)t * DK] = dq;
-                            ok_[(size_t)t * DK] = dk;
-                            if (od) {
-                                float g = __bfloat162float(qr[(size_t)t * DK]) * dq -
-                                          __bfloat162float(kr[(size_t)t * DK]) * dk;
-                                if (c * C + t == a.T - 1) g += bnd;
-                                od[(size_t)t * DK] = g;
+                                      __bfloat162float(qr[(size_t)u2 * DK]) * expf(Bs[u2] - Bs[t]);
+                            oq[(size_t)t * DK] += sq;
+                            ok_[(size_t)t * DK] += sk;
+                        }
+                        if (oR) {
+                            rsum = 0.f;
+                            for (int t = nr - 1; t >= 0; --t) {
+                                rsum += __bfloat162float(qr[(size_t)t * DK]) * oq[(size_t)t * DK] -
+                                        __bfloat162float(kr[(size_t)t * DK]) * ok_[(size_t)t * DK];
+                                if (c * C + t == a.T - 1) rsum += bnd;
+                                oR[(size_t)t * DK] = rsum;
                             }
                         }
                     }
+                    if (a.ctot) a.ctot[((size_t)bh * a.nch + c) * DK + key] = rsum;
                 }
             }
             if (!ok) {
@@ -554,6 +583,28 @@ __global__ void __launch_bounds__(256) gla_bwd_boundary_kernel(const float* dST,
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (lane == 0) bnd[r] = s;
+    }
+}
+
+// out[bh][t][k] += crev[bh][c(t) + 1][k], c(t) = t / C: the gate terms of the later chunks
+// (crev: per chunk, the sum over that chunk and all after it). One float4 of keys per thread.
+__global__ void __launch_bounds__(256) gla_bwd_gate_fixup_kernel(float* out, const float* crev, long long BH, int T,
+                                                                int dk, int nch)
+{
+    const int q4 = dk / 4;
+    const long long n = BH * T * q4;
+    for (long long e = (long long)blockIdx.x * 256 + threadIdx.x; e < n; e += (long long)gridDim.x * 256) {
+        const int kq = (int)(e % q4);
+        const long long bt = e / q4;
+        const int t = (int)(bt % T);
+        const long long bh = bt / T;
+        const int c = t / C + 1;
+        if (c >= nch) continue;
+        float4* o = reinterpret_cast<float4*>(out) + e;
+        const float4 add = reinterpret_cast<const float4*>(crev)[(bh * nch + c) * q4 + kq];
+        float4 v = *o;
+        v.x += add.x; v.y += add.y; v.z += add.z; v.w += add.w;
+        *o = v;
     }
 }
 
@@ -603,11 +654,23 @@ cudaError_t launch_bwd_grads(const BwdGrads& g, int* status, cudaStream_t s)
     a.log_g = g.log_g;
     a.gam = g.gam;
     a.bnd = g.bnd;
-    a.gq = g.gq; a.gk = g.gk; a.gv = g.gv; a.dla = g.dla;
+    a.gq = g.gq; a.gk = g.gk; a.gv = g.gv; a.R = g.R; a.ctot = g.ctot;
     a.status = status;
     a.BH = g.BH; a.H = g.H; a.T = g.T; a.dv = g.dv; a.nch = nch; a.gate = g.gate;
     const int sms = g.sms > 0 ? g.sms : 148;
     return g.dk == 128 ? launch_grads_dk<128>(a, m, sms, s) : launch_grads_dk<256>(a, m, sms, s);
+}
+
+cudaError_t launch_bwd_gate_fixup(float* out, const float* crev, long long BH, int T, int dk, int sms, cudaStream_t s)
+{
+    const int nch = (T + C - 1) / C;
+    if (nch <= 1 || dk % 4 != 0) return nch <= 1 ? cudaSuccess : cudaErrorInvalidValue;
+    const long long n = BH * T * (dk / 4);
+    long long blocks = (n + 255) / 256;
+    const long long cap = (long long)(sms > 0 ? sms : 148) * 8;
+    if (blocks > cap) blocks = cap;
+    gla_bwd_gate_fixup_kernel<<<(unsigned)blocks, 256, 0, s>>>(out, crev, BH, T, dk, nch);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_boundary(const float* dST, const float* ST, float* bnd, long long rows, int dv, int sms,

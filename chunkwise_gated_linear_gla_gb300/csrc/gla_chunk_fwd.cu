@@ -443,21 +443,10 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gvd);
                 }
-                if (want_out) {
+                if (want_out || sweep) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         P[c2 / 2 + i] = pack_bf16(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-                }
-                if (sweep) {
-                    // the state entering this chunk's update, 32 keys of row d: four 16-byte stores
-                    uint4* hp = reinterpret_cast<uint4*>(
-                        a.Hst + (((size_t)bh * a.nchunks + chunk_of(n)) * a.dv + dv0 + d) * DK + cb + c2);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        hp[i] = make_uint4(pack_bf16(__uint_as_float(r0[8 * i]), __uint_as_float(r0[8 * i + 1])),
-                                           pack_bf16(__uint_as_float(r0[8 * i + 2]), __uint_as_float(r0[8 * i + 3])),
-                                           pack_bf16(__uint_as_float(r0[8 * i + 4]), __uint_as_float(r0[8 * i + 5])),
-                                           pack_bf16(__uint_as_float(r0[8 * i + 6]), __uint_as_float(r0[8 * i + 7])));
                 }
                 if (gated) {
                     // two columns per packed multiply (each lane rounds as a single fp32 multiply)
@@ -473,6 +462,15 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             if (gated) tmem_wait_st();
             tc_fence_before();
             mbar_arrive(s_ready);
+            if (sweep) {
+                // the state entering this chunk's update (this thread's row d, HC keys), stored
+                // once the decay is handed back, so the stores stay off the chunk-to-chunk chain
+                uint4* hp = reinterpret_cast<uint4*>(
+                    a.Hst + (((size_t)bh * a.nchunks + chunk_of(n)) * a.dv + dv0 + d) * DK + cb);
+#pragma unroll
+                for (int i = 0; i < HC / 8; ++i) hp[i] = make_uint4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
+                continue;
+            }
             if (!want_out) continue;
             // part 2: bf16 copy of S_[n-1] for the inter MMA, once the previous one is consumed
             ok = (n == 0) || mbar_wait(sb_free, (n - 1) & 1, kTimeoutNs);

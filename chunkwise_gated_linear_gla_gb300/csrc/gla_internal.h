@@ -149,7 +149,9 @@ cudaError_t launch_state_sweep(const StateSweep& w, int* status, cudaStream_t s)
 // The chunk-parallel gradients of the backward (gla_bwd_chunk.cu): dq, dk, dv and the gate
 // terms q (.) dq - k (.) dk per token, from the prep's Kt, Qt ([BH][kt_rows][dk] bf16), A and
 // gamma, and the two sweeps' H and D ([BH][nch][dv][dk] bf16). dk in {128, 256}, dv a
-// multiple of 128, T > 0. gam null without a gate; bnd ([BH][dk]) and dla may be null.
+// multiple of 128, T > 0. gam null without a gate; bnd ([BH][dk]) may be null. With R
+// ([BH][T][dk]) and ctot ([BH][nch][dk]): R gets each gate term summed over the later rows of
+// its chunk, ctot each chunk's total.
 struct BwdGrads {
     const void* q; const void* k; const void* v; const void* dO;
     const float* log_g;
@@ -157,10 +159,12 @@ struct BwdGrads {
     const void* A; const float* gam;
     const void* Hst; const void* Dst;
     const float* bnd;
-    float* gq; float* gk; float* gv; float* dla;
+    float* gq; float* gk; float* gv; float* R; float* ctot;
     int BH, H, T, dk, dv, gate, sms;
 };
 cudaError_t launch_bwd_grads(const BwdGrads& g, int* status, cudaStream_t s);
+// out [BH][T][dk] += crev [BH][nch][dk] of the chunk after each row's (none for the last)
+cudaError_t launch_bwd_gate_fixup(float* out, const float* crev, long long BH, int T, int dk, int sms, cudaStream_t s);
 // rowsum(dST (.) ST) over each of `rows` rows of dv values
 cudaError_t launch_bwd_boundary(const float* dST, const float* ST, float* bnd, long long rows, int dv, int sms,
                                 cudaStream_t s);

@@ -400,8 +400,9 @@ def test_bwd_workspace_size():
 
 def test_bwd_chunk_form_workspace_size():
     """The chunk form's workspace: Q (.) Lambda and K (.) Gamma, scores, chunk decays, the two
-    sweeps' bf16 chunk states, S_T and the boundary term (with grad_ST), the per-token gate
-    terms; less than the 16-row form's fp32 chunk states."""
+    sweeps' bf16 chunk states, S_T and the boundary term (with grad_ST), the per-chunk gate
+    totals (the per-key gate's per-token terms go straight to grad_log_g); less than the
+    16-row form's fp32 chunk states."""
     gbuild.build()
     far = {n: (i + 1) << 28 for i, n in enumerate(["q", "k", "v", "log_g", "grad_O", "grad_q", "grad_k", "grad_v",
                                                    "grad_log_g", "grad_ST"])}
@@ -411,7 +412,7 @@ def test_bwd_chunk_form_workspace_size():
     BH, nch, Tpad = B * H, 2, 128
     up = lambda x: (x + 255) // 256 * 256
     want = (2 * up(BH * Tpad * dk * 2) + up(BH * nch * 64 * 64 * 2) + up(BH * nch * dk * 4)
-            + 2 * up(BH * nch * dv * dk * 2) + up(BH * dk * dv * 4) + up(BH * dk * 4) + up(BH * T * dk * 4))
+            + 2 * up(BH * nch * dv * dk * 2) + up(BH * dk * dv * 4) + up(BH * dk * 4) + up(BH * nch * dk * 4))
     assert n == want
     split = bnd.gla_bwd_workspace_size(_bp(B=B, H=H, T=T, dk=dk, dv=dv, path=bnd.GLA_PATH_SPLIT, **far))
     assert split > n
