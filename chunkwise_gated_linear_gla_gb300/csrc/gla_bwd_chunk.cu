@@ -62,6 +62,7 @@ constexpr int BAR_EPI = 1;              // named barrier of the epilogue warps
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 // exp(-60): a key whose chunk decay gamma is below this takes the pairwise intra rule
 constexpr float kSteepGamma = 8.7565108e-27f;
+constexpr float kLog2e = 1.44269504088896341f;   // 1 / ln 2
 
 enum { ERR_PRODUCER = 0x501, ERR_MMA = 0x502, ERR_EPI = 0x503 };
 
@@ -94,8 +95,8 @@ struct GL {
     static constexpr int KT_OFF = 0;
     static constexpr int A_OFF = KTB;                     // A tile [t][s]
     static constexpr int DA_OFF = A_OFF + 8192;           // dA tile [t][s], bf16, written here
-    static constexpr int GM_OFF = DA_OFF + 8192;          // gamma [DK] fp32
-    static constexpr int BLK_OFF = GM_OFF + (DK * 4 + 1023) / 1024 * 1024;
+    static constexpr int GM_OFF = DA_OFF + 8192;          // gamma [DK] fp32, then 1 / gamma [DK]
+    static constexpr int BLK_OFF = GM_OFF + (DK * 8 + 1023) / 1024 * 1024;
     static constexpr int UNIT_OFF = BLK_OFF + NBR * 32768;
     static constexpr int BAR_OFF = UNIT_OFF + NU * 32768;
     static constexpr int SMEM = BAR_OFF + 512 + 1024;
@@ -138,23 +139,22 @@ __device__ __forceinline__ float bf16_at(const uint8_t* p) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
 }
 
-// Multiplies the keys of a [64 rows x DK] tile (DK/64 swizzled boxes) by 1 / gamma, and
-// zeroes the keys whose gamma is below kSteepGamma. Thread tid of n.
+// Multiplies the keys of a [64 rows x DK] tile (DK/64 swizzled boxes) by the per-key factors
+// f (1 / gamma, or 0 for the keys whose gamma is below kSteepGamma). Thread tid of n.
 template <int DK>
-__device__ __forceinline__ void scale_keys(uint8_t* tile, const float* gm, int tid, int n) {
+__device__ __forceinline__ void scale_keys(uint8_t* tile, const float* f, int tid, int n) {
     for (int idx = tid; idx < DK * 8; idx += n) {
         const int j = idx >> 9, r = (idx >> 3) & 63, cc = idx & 7;
         uint4* p = reinterpret_cast<uint4*>(tile + j * 8192 + swz_off(r, cc));
         uint4 w = *p;
         __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
-        const float* g = gm + 64 * j + 8 * cc;
+        const float4 f0 = *reinterpret_cast<const float4*>(f + 64 * j + 8 * cc);
+        const float4 f1 = *reinterpret_cast<const float4*>(f + 64 * j + 8 * cc + 4);
+        const float fs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float g0 = g[2 * e], g1 = g[2 * e + 1];
-            const float f0 = g0 >= kSteepGamma ? 1.f / g0 : 0.f;
-            const float f1 = g1 >= kSteepGamma ? 1.f / g1 : 0.f;
             const float2 x = __bfloat1622float2(h[e]);
-            h[e] = __floats2bfloat162_rn(x.x * f0, x.y * f1);
+            h[e] = __floats2bfloat162_rn(x.x * fs[2 * e], x.y * fs[2 * e + 1]);
         }
         *p = w;
     }
@@ -183,10 +183,13 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
     uint64_t* da_full = bar + 16;       // every MMA of the chunk's blocks done
     uint64_t* dat_ready = bar + 17;     // dA staged, Kg and Qg rescaled (256 arrivals)
     uint64_t* dqdk_full = bar + 18;
-    uint64_t* dqdk_empty = bar + 19;    // (NKH * 128 arrivals)
-    uint64_t* mma_fin = bar + 20;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 21);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 22);
+    uint64_t* dk_empty = bar + 19;      // dk^T read out (NKH * 128 arrivals)
+    uint64_t* dq_empty = bar + 20;      // dq^T read out (NKH * 128 arrivals)
+    uint64_t* mma_fin = bar + 21;
+    uint64_t* kt_free = bar + 22;       // the chunk's last product reading Kt done
+    uint64_t* p3_done = bar + 23;       // the drain done with the Kg and Qg tiles (NKH * 128 arrivals)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 24);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 25);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int items = a.BH * a.nch;
@@ -200,8 +203,8 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
         for (int i = 0; i < NU; ++i) { mbar_init(&unit_full[i], 1); mbar_init(&unit_empty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&dv_full[i], 1); mbar_init(&dv_empty[i], 128); }
         mbar_init(da_full, 1); mbar_init(dat_ready, NEPI);
-        mbar_init(dqdk_full, 1); mbar_init(dqdk_empty, NKH * 128);
-        mbar_init(mma_fin, 1);
+        mbar_init(dqdk_full, 1); mbar_init(dk_empty, NKH * 128); mbar_init(dq_empty, NKH * 128);
+        mbar_init(mma_fin, 1); mbar_init(kt_free, 1); mbar_init(p3_done, NKH * 128);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tmap(&tmK); prefetch_tmap(&tmQ); prefetch_tmap(&tmA); prefetch_tmap(&tmO);
@@ -221,9 +224,16 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
         if (lane == 0) {
             int u = 0, bc = 0, i = 0, nres = 0;
             bool ok = true;
+            // (a slot that held a chunk's Qt tile is refilled once the drain is done with it too)
+            auto slot_free = [&](int x) -> bool {
+                if (x < NU) return true;
+                const int prev = x - NU;
+                if (!mbar_wait(&unit_empty[x % NU], (prev / NU) & 1, kTimeoutNs)) return false;
+                return prev % u_per != u_per - 1 || mbar_wait(p3_done, (prev / u_per) & 1, kTimeoutNs);
+            };
             auto load_unit = [&](const CUtensorMap* m, int c0, int c1, int c2) -> bool {
                 const int us = u % NU;
-                if (u >= NU && !mbar_wait(&unit_empty[us], ((u / NU) - 1) & 1, kTimeoutNs)) return false;
+                if (!slot_free(u)) return false;
                 uint8_t* ub = sm + L::UNIT_OFF + us * 32768;
                 mbar_arrive_expect_tx(&unit_full[us], 32768);
                 tma_load_3d(ub, m, &unit_full[us], c0, c1, c2);
@@ -234,13 +244,6 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++i) {
                 if (*abort_flag) break;
                 const int bh = it / a.nch, c = it % a.nch, hc = bh * a.nch + c;
-                if (i >= 1 && !mbar_wait(res_empty, (i - 1) & 1, kTimeoutNs)) { ok = false; break; }
-                mbar_arrive_expect_tx(res_full, L::KTB + 8192 + (gated ? DK * 4 : 0));
-#pragma unroll
-                for (int j = 0; j < DK / 64; ++j) tma_load_3d(sm + L::KT_OFF + j * 8192, &tmK, res_full, 64 * j, c * C, bh);
-                tma_load_2d(sm + L::A_OFF, &tmA, res_full, 0, hc * C);
-                if (gated) bulk_load(sm + L::GM_OFF, a.gam + (size_t)hc * DK, DK * 4, res_full);
-                ++nres;
                 for (int b = 0; b < nblk && ok; ++b) {
                     const int slot = bc % NBR;
                     if (bc >= NBR && !mbar_wait(&blk_empty[slot], ((bc / NBR) - 1) & 1, kTimeoutNs)) { ok = false; break; }
@@ -252,12 +255,33 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                     tma_load_3d(bb + 24576, &tmV, &blk_full[slot], 128 * b + 64, c * C, bh);
                     ++bc;
                     for (int kh = 0; kh < NKH && ok; ++kh) ok = load_unit(&tmD, 128 * kh, 128 * b, hc);
+                    if (ok && b == 0) {
+                        // Kt, A and gamma, once the previous chunk's last products are done with
+                        // them (the first block's tiles are already on their way)
+                        if (i >= 1 && (!mbar_wait(res_empty, (i - 1) & 1, kTimeoutNs) ||
+                                       !mbar_wait(p3_done, (i - 1) & 1, kTimeoutNs))) { ok = false; break; }
+                        mbar_arrive_expect_tx(res_full, L::KTB + 8192 + (gated ? DK * 4 : 0));
+#pragma unroll
+                        for (int j = 0; j < DK / 64; ++j)
+                            tma_load_3d(sm + L::KT_OFF + j * 8192, &tmK, res_full, 64 * j, c * C, bh);
+                        tma_load_2d(sm + L::A_OFF, &tmA, res_full, 0, hc * C);
+                        if (gated) bulk_load(sm + L::GM_OFF, a.gam + (size_t)hc * DK, DK * 4, res_full);
+                        ++nres;
+                        // the rows the drain reads (raw q, k and the per-key log gates) into L2
+                        const int nr = min(C, a.T - c * C);
+                        const size_t rb = (size_t)bh * a.T + (size_t)c * C;
+                        prefetch_l2(a.q + rb * DK, (uint32_t)(nr * DK * 2));
+                        prefetch_l2(a.k + rb * DK, (uint32_t)(nr * DK * 2));
+                        const float* lg = a.log_g + rb * DK;
+                        if (a.gate == GLA_GATE_PER_KEY && (reinterpret_cast<uintptr_t>(lg) & 15) == 0)
+                            prefetch_l2(lg, (uint32_t)(nr * DK * 4));
+                    }
                     for (int kh = 0; kh < NKH && ok; ++kh) ok = load_unit(&tmH, 128 * kh, 128 * b, hc);
                 }
                 if (!ok) break;
                 // the chunk's Qt rows, for the dk intra product
                 const int us = u % NU;
-                if (u >= NU && !mbar_wait(&unit_empty[us], ((u / NU) - 1) & 1, kTimeoutNs)) { ok = false; break; }
+                if (!slot_free(u)) { ok = false; break; }
                 uint8_t* ub = sm + L::UNIT_OFF + us * 32768;
                 mbar_arrive_expect_tx(&unit_full[us], L::KTB);
 #pragma unroll
@@ -302,7 +326,7 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                     for (int kh = 0; kh < NKH && ok; ++kh) {
                         const int us = u % NU;
                         ok = mbar_wait(&unit_full[us], (u / NU) & 1, kTimeoutNs);
-                        if (ok && b == 0 && kh == 0 && i >= 1) ok = mbar_wait(dqdk_empty, (i - 1) & 1, kTimeoutNs);
+                        if (ok && b == 0 && kh == 0 && i >= 1) ok = mbar_wait(dk_empty, (i - 1) & 1, kTimeoutNs);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t sU = s0 + L::UNIT_OFF + us * 32768;   // D rows 128b.., keys 128kh..
@@ -324,6 +348,7 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                     if (!ok) break;
                     mma_commit(&dv_full[buf]);
                     ++dvc;
+                    if (b == nblk - 1) mma_commit(kt_free);   // every product reading Kt is issued
                     // dA += dO V^T over these 128 dv columns (rows 64-127 of the product unused)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
@@ -333,6 +358,7 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                     for (int kh = 0; kh < NKH && ok; ++kh) {
                         const int us = u % NU;
                         ok = mbar_wait(&unit_full[us], (u / NU) & 1, kTimeoutNs);
+                        if (ok && b == 0 && kh == 0 && i >= 1) ok = mbar_wait(dq_empty, (i - 1) & 1, kTimeoutNs);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t sU = s0 + L::UNIT_OFF + us * 32768;   // H rows 128b.., keys 128kh..
@@ -395,6 +421,19 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
             const int nr = min(C, a.T - c * C);
             const size_t rb = (size_t)bh * a.T + (size_t)c * C;   // first row of the chunk
             bool ok = *abort_flag == 0;
+            // this key's log gates over the chunk, loaded at once (rows past T read as 0): the
+            // latency overlaps the chunk's products
+            const int key = 128 * e + row;
+            float Bc[C];
+            if (e < NKH) {
+                const float* lg = nullptr;
+                size_t st = 0;
+                if (a.gate == GLA_GATE_PER_KEY) { lg = a.log_g + rb * DK + key; st = DK; }
+                else if (a.gate == GLA_GATE_TOKEN_SCALAR) { lg = a.log_g + rb; st = 1; }
+                else if (a.gate == GLA_GATE_HEAD_SCALAR) { lg = a.log_g + bh % a.H; st = 0; }
+#pragma unroll
+                for (int t = 0; t < C; ++t) Bc[t] = (lg && t < nr) ? lg[(size_t)t * st] : 0.f;
+            }
             // phase 1: this warpgroup's dv blocks (buffer e), each thread one dv column
             for (int b = 0; b < nblk && ok; ++b) {
                 if (((i * nblk + b) & 1) != e) continue;
@@ -419,22 +458,17 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
             }
             // every epilogue thread is past the previous chunk's use of the dA tile
             if (!group_all_ok(ok, BAR_EPI, NEPI)) break;
-            // this key's log gates over the chunk, loaded at once (rows past T read as 0), so
-            // that their latency overlaps the waits for the products
-            const int key = 128 * e + row;
-            float Bc[C];
-            if (e < NKH) {
-                const float* lg = nullptr;
-                size_t st = 0;
-                if (a.gate == GLA_GATE_PER_KEY) { lg = a.log_g + rb * DK + key; st = DK; }
-                else if (a.gate == GLA_GATE_TOKEN_SCALAR) { lg = a.log_g + rb; st = 1; }
-                else if (a.gate == GLA_GATE_HEAD_SCALAR) { lg = a.log_g + bh % a.H; st = 0; }
-#pragma unroll
-                for (int t = 0; t < C; ++t) Bc[t] = (lg && t < nr) ? lg[(size_t)t * st] : 0.f;
-            }
-            // phase 2: dA to shared memory (bf16, masked), Kt and Qt to Kg and Qg (the Kt tile
-            // and gamma once landed; Kt once the dv products are done with it)
+            // phase 2: the per-key factors 1 / gamma (0 for a steep key), Kt to Kg once the dv
+            // products are done with it, dA to shared memory (bf16, masked), Qt to Qg
+            float* ginv = reinterpret_cast<float*>(sm + L::GM_OFF) + DK;
             ok = mbar_wait(res_full, i & 1, kTimeoutNs);
+            if (ok && gated && et < DK) {
+                const float g = gm[et];
+                ginv[et] = g >= kSteepGamma ? 1.f / g : 0.f;
+            }
+            if (!group_all_ok(ok, BAR_EPI, NEPI)) break;
+            ok = mbar_wait(kt_free, i & 1, kTimeoutNs);
+            if (ok && gated) scale_keys<DK>(sm + L::KT_OFF, ginv, et, NEPI);
             if (ok) ok = mbar_wait(da_full, i & 1, kTimeoutNs);
             ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-wide
             if (ok) {
@@ -461,21 +495,26 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                         }
                     }
                 }
-                if (gated) scale_keys<DK>(sm + L::KT_OFF, gm, et, NEPI);
             }
             const int uq = i * u_per + 2 * nblk * NKH;
             const int usq = uq % NU;
             if (ok) ok = mbar_wait(&unit_full[usq], (uq / NU) & 1, kTimeoutNs);
-            if (ok && gated) scale_keys<DK>(sm + L::UNIT_OFF + usq * 32768, gm, et, NEPI);
+            if (ok && gated) scale_keys<DK>(sm + L::UNIT_OFF + usq * 32768, ginv, et, NEPI);
             const float gk = (gated && e < NKH) ? gm[key] : 1.f;   // read before the slot is reloaded
             fence_proxy_async_smem();
-            if (ok) mbar_arrive(dat_ready);
+            // every thread's rescale is done before any drain thread reads a Kg or Qg column (the
+            // tiles stay until the drain is done with them)
+            if (!group_all_ok(ok, BAR_EPI, NEPI)) break;
+            const uint8_t* qcol = sm + L::UNIT_OFF + usq * 32768 + (key >> 6) * 8192 + (key & 7) * 2;
+            const uint8_t* kcol = sm + L::KT_OFF + (key >> 6) * 8192 + (key & 7) * 2;
+            mbar_arrive(dat_ready);
             // phase 3: dq and dk of key `key` (warpgroup e = key half e), rows from the last,
             // with the gate terms summed over the later rows of the chunk
             if (ok && e < NKH) {
+                Bc[0] *= kLog2e;
 #pragma unroll
-                for (int t = 1; t < C; ++t) Bc[t] += Bc[t - 1];   // Bc_t; rows past T add 0
-                const float tot = Bc[C - 1];                       // Bc_end
+                for (int t = 1; t < C; ++t) Bc[t] = fmaf(Bc[t], kLog2e, Bc[t - 1]);   // Bc_t / ln 2; rows past T add 0
+                const float tot = Bc[C - 1];                       // Bc_end / ln 2
                 ok = __all_sync(0xffffffffu, mbar_wait(dqdk_full, i & 1, kTimeoutNs));
                 if (ok) {
                     tc_fence_after();
@@ -486,42 +525,40 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                     const __nv_bfloat16* qr = a.q + rb * DK + key;
                     const __nv_bfloat16* kr = a.k + rb * DK + key;
                     const float bnd = (a.bnd && c == a.nch - 1) ? a.bnd[(size_t)bh * DK + key] : 0.f;
+                    // rows from the last: dq, dk and the gate term q (.) dq - k (.) dk =
+                    // gamma (Qg (.) Xq - Kg (.) Xk) (q Lambda = Qt = gamma Qg, k Gamma = Kt =
+                    // gamma Kg), summed over the later rows of the chunk
+                    const int cc = (key & 63) >> 3;
                     float rsum = 0.f;
 #pragma unroll
                     for (int qd = C / 16 - 1; qd >= 0; --qd) {
                         uint32_t xq[16], xk[16];
                         tmem_ld16(tmem + lb + TQ + e * 64 + 16 * qd, xq);
                         tmem_ld16(tmem + lb + TK + e * 64 + 16 * qd, xk);
-                        float qv[16], kv[16];
-                        if (oR) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int r = 16 * qd + j;
-                                qv[j] = r < nr ? __bfloat162float(qr[(size_t)r * DK]) : 0.f;
-                                kv[j] = r < nr ? __bfloat162float(kr[(size_t)r * DK]) : 0.f;
-                            }
-                        }
                         tmem_wait_ld();
                         if (qd == 0) {
                             tc_fence_before();
-                            mbar_arrive(dqdk_empty);
+                            mbar_arrive(dk_empty);
+                            mbar_arrive(dq_empty);
                         }
 #pragma unroll
                         for (int j = 15; j >= 0; --j) {
                             const int r = 16 * qd + j;
                             if (r < nr) {
-                                const float dq = expf(Bc[r]) * __uint_as_float(xq[j]);
-                                const float dk = expf(tot - Bc[r]) * __uint_as_float(xk[j]);
-                                oq[(size_t)r * DK] = dq;
-                                ok_[(size_t)r * DK] = dk;
+                                const float Xq = __uint_as_float(xq[j]), Xk = __uint_as_float(xk[j]);
+                                oq[(size_t)r * DK] = exp2f(Bc[r]) * Xq;          // Lambda_r Xq
+                                ok_[(size_t)r * DK] = exp2f(tot - Bc[r]) * Xk;   // Gamma_r Xk
                                 if (oR) {
-                                    rsum += qv[j] * dq - kv[j] * dk;
+                                    const float qg = bf16_at(qcol + swz_off(r, cc));
+                                    const float kg = bf16_at(kcol + swz_off(r, cc));
+                                    rsum += gk * (qg * Xq - kg * Xk);
                                     if (c * C + r == a.T - 1) rsum += bnd;
                                     oR[(size_t)r * DK] = rsum;
                                 }
                             }
                         }
                     }
+                    mbar_arrive(p3_done);
                     if (steep) {
                         // the intra terms of this key, pairwise: exp(Bc_t - Bc_s) <= 1 for t >= s;
                         // then the gate terms again from the completed dq and dk
