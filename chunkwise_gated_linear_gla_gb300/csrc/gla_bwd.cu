@@ -1150,8 +1150,8 @@ bool chunk_shape_ok(const gla_bwd_params* p) {
     const long long rows = (((long long)p->T + kChunk - 1) / kChunk) * kChunk;
     auto al16 = [](const void* x) { return reinterpret_cast<uintptr_t>(x) % 16 == 0; };
     return p->dtype == GLA_BF16 && (p->dk == 128 || p->dk == 256) && p->dv % kDvTile == 0 &&
-           p->gate != GLA_GATE_BILINEAR && BH <= 65535 && BH * rows < (1LL << 31) && al16(p->q) && al16(p->k) &&
-           al16(p->v) && al16(p->grad_O);
+           p->gate != GLA_GATE_BILINEAR && BH <= 65535 && BH * rows < (1LL << 31) &&
+           BH * (rows / kChunk) * p->dv < (1LL << 31) && al16(p->q) && al16(p->k) && al16(p->v) && al16(p->grad_O);
 }
 
 enum BwdKind { BWD_SIMT, BWD_SPLIT, BWD_CHUNK };

@@ -463,12 +463,41 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             tc_fence_before();
             mbar_arrive(s_ready);
             if (sweep) {
-                // the state entering this chunk's update (this thread's row d, HC keys), stored
-                // once the decay is handed back, so the stores stay off the chunk-to-chunk chain
-                uint4* hp = reinterpret_cast<uint4*>(
-                    a.Hst + (((size_t)bh * a.nchunks + chunk_of(n)) * a.dv + dv0 + d) * DK + cb);
+                // the state entering this chunk's update, once the decay is handed back (off the
+                // chunk-to-chunk chain): this thread's row d and HC keys
+                if constexpr (DK >= 128) {
+                    // staged in the idle Q tiles as boxes of 64 keys x 128 rows (128-byte
+                    // swizzle; a Q tile holds DK / 128 boxes, so both stages' tiles take the
+                    // DK / 64 boxes), then TMA stores from one thread, once the previous chunk's
+                    // stores have read the tiles
+                    constexpr int BPS = DK / 128;   // boxes per stage's Q tile
+                    static_assert(L::QB == BPS * 16384, "state boxes fill the Q tiles");
+                    if (gt == 0 && grp == 0) bulk_wait_read0();
+                    named_bar_sync(BAR_EPI, NEPI);
 #pragma unroll
-                for (int i = 0; i < HC / 8; ++i) hp[i] = make_uint4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
+                    for (int m = 0; m < HC / 8; ++m) {
+                        const int key = cb + 8 * m, box = key >> 6;
+                        uint8_t* bb = sm + (box / BPS) * L::STAGE + L::Q_OFF + (box % BPS) * 16384;
+                        *reinterpret_cast<uint4*>(bb + d * 128 + ((((key & 63) >> 3) ^ (d & 7)) << 4)) =
+                            make_uint4(P[4 * m], P[4 * m + 1], P[4 * m + 2], P[4 * m + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(BAR_EPI, NEPI);
+                    if (gt == 0 && grp == 0) {
+                        const int row0 = (bh * a.nchunks + chunk_of(n)) * a.dv + dv0;
+#pragma unroll
+                        for (int box = 0; box < DK / 64; ++box)
+                            tma_store_2d(&tmO, sm + (box / BPS) * L::STAGE + L::Q_OFF + (box % BPS) * 16384, 64 * box,
+                                         row0);
+                        bulk_commit();
+                    }
+                } else {
+                    uint4* hp = reinterpret_cast<uint4*>(
+                        a.Hst + (((size_t)bh * a.nchunks + chunk_of(n)) * a.dv + dv0 + d) * DK + cb);
+#pragma unroll
+                    for (int i = 0; i < HC / 8; ++i)
+                        hp[i] = make_uint4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
+                }
                 continue;
             }
             if (!want_out) continue;
@@ -513,6 +542,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             }
         }
         if (!alive && gt == 0) fail(a.status, abort_flag, ERR_EPI);
+        if (sweep && gt == 0 && grp == 0) bulk_wait0();   // the state tiles' stores
     } else if (wg == 3) {
         // ---------------------------------------------------------- output drain (4 warps)
         // Thread (warp % 4, lane) owns dv column d of the tile in all 64 rows of each chunk:
@@ -775,6 +805,7 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
 cudaError_t launch_state_sweep(const StateSweep& w, int* status, cudaStream_t s)
 {
     if (w.dv % DVT != 0 || w.nch <= 0 || !w.Hst) return cudaErrorInvalidValue;
+    if ((long long)w.BH * w.nch * w.dv >= (1LL << 31)) return cudaErrorInvalidValue;   // state rows as TMA coordinates
     const uint64_t BH = (uint64_t)w.BH;
     CUtensorMap mk, mv;
     if (!map3(&mk, w.kt, w.dk, (uint64_t)w.kt_rows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
@@ -795,11 +826,21 @@ cudaError_t launch_state_sweep(const StateSweep& w, int* status, cudaStream_t s)
     a.H = 1;
     a.Hst = static_cast<__nv_bfloat16*>(w.Hst);
     const dim3 grid(w.dv / DVT, (unsigned)BH, 1);
-    // no O, Q or score tile is read in a sweep: the K map stands in for those arguments
+    // the states leave through the O map's slot: [BH * nch * dv rows][dk] bf16, boxes of 64 keys
+    // x 128 rows (128-byte swizzle); no Q, score or O tile is read in a sweep, the K map stands
+    // in for those arguments
+    CUtensorMap mh;
+    {
+        uint64_t dims[2] = {(uint64_t)w.dk, BH * (uint64_t)w.nch * (uint64_t)w.dv};
+        uint64_t str[1] = {(uint64_t)w.dk * 2};
+        uint32_t box[2] = {64, 128};
+        if (!make_tmap(&mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.Hst, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
     switch (w.dk) {
-    case 64: return launch_dk<64, false, false>(a, grid, mk, mk, mv, mk, mv, mk, s);
-    case 128: return launch_dk<128, false, false>(a, grid, mk, mk, mv, mk, mv, mk, s);
-    case 256: return launch_dk<256, false, false>(a, grid, mk, mk, mv, mk, mv, mk, s);
+    case 64: return launch_dk<64, false, false>(a, grid, mk, mk, mv, mk, mh, mk, s);
+    case 128: return launch_dk<128, false, false>(a, grid, mk, mk, mv, mk, mh, mk, s);
+    case 256: return launch_dk<256, false, false>(a, grid, mk, mk, mv, mk, mh, mk, s);
     }
     return cudaErrorInvalidValue;
 }
