@@ -166,7 +166,12 @@ def kernel_source_sha(name):
              "gla_chunk_prep": ["gla_prep.cu", "sm100.cuh"],
              "gla_chunk_state": ["gla_state.cu", "sm100.cuh"],
              "gla_state_scan": ["gla_scan.cu"],
-             "gla_value_prep": ["gla_vprep.cu"]}.get(name, [])
+             "gla_value_prep": ["gla_vprep.cu"],
+             "gla_bwd_state_sweep": ["gla_chunk_fwd.cu", "sm100.cuh"],
+             "gla_bwd_dstate_sweep": ["gla_chunk_fwd.cu", "sm100.cuh"],
+             "gla_bwd_boundary": ["gla_bwd_chunk.cu"],
+             "gla_bwd_grads": ["gla_bwd_chunk.cu", "sm100.cuh"],
+             "gla_bwd_gate_tail": ["gla_bwd.cu", "gla_bwd_chunk.cu"]}.get(name, [])
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "chunkwise_gated_linear_gla_gb300", "csrc", f), "rb") as fh:
@@ -174,12 +179,13 @@ def kernel_source_sha(name):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, name):
-    """DRAM bytes per launch of kernel `name` on `workload` from the committed ncu summary,
-    if one was captured for that pair and the kernel's source still matches it."""
+def ncu_traffic(workload, name, direction="fwd"):
+    """DRAM bytes per launch of kernel `name` on `workload` (the backward's under
+    "<workload>/bwd") from the committed ncu summary, if one was captured for that pair and the
+    kernel's source still matches it."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-            d = json.load(f)[workload][name]
+            d = json.load(f)[workload if direction == "fwd" else f"{workload}/bwd"][name]
         if d.get("source_sha") != kernel_source_sha(name):
             return None
         return float(d["dram_bytes_per_launch"])
@@ -355,18 +361,64 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 BWD_METRIC = "GLA bwd tokens/s at B=8,T=2048,dk256,dv512 (gradients of q, k, v, log_g, S0)"
 
 
+def bwd_chunk_form(w):
+    """Whether gla_bwd takes its 64-row chunk form (tcgen05) for workload w."""
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    return (w.dtype != torch_f32() and w.dk in (128, 256) and w.dv % 128 == 0 and w.T > 0
+            and w.gate != gi.GATE_BILINEAR)
+
+
+def torch_f32():
+    import torch
+    return torch.float32
+
+
 def algorithmic_bwd(w):
-    """FLOPs of the backward per token per head: 10 dk dv (the forward state sweep, the
-    gradient-of-state update, and dq, dk, dv through the chunk states) + 2 (C+1)(dk+dv)
-    (the intra-chunk scores and their three products), C = 16 on the CUDA-core path."""
+    """FLOPs of the backward per token per head. The chunk form (C = 64): 10 dk dv (the two
+    state sweeps' updates and the dv, dk and dq products with the chunk states) +
+    2 C (2 dv + 3 dk) (the scores, dO V^T, and A^T dO, dA K, dA^T Q within the chunk). The
+    16-row forms (C = 16): 10 dk dv + 2 (C + 1)(dk + dv)."""
+    if bwd_chunk_form(w):
+        C = 64
+        return w.B * w.H * w.T * (10 * w.dk * w.dv + 2 * C * (2 * w.dv + 3 * w.dk))
     C = 16
     return w.B * w.H * w.T * (10 * w.dk * w.dv + 2 * (C + 1) * (w.dk + w.dv))
 
 
+def bwd_stage_bytes(w, name, glog=True, dst=True, s0=True):
+    """Compulsory DRAM bytes of one launch of a chunk-form stage: what it must read and write
+    once (inputs, the workspace tensors it consumes and produces, its outputs)."""
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    BH, T, dk, dv = w.B * w.H, w.T, w.dk, w.dv
+    nch = -(-T // 64)
+    Tp = nch * 64
+    gated = w.gate != gi.GATE_NONE
+    lg = {gi.GATE_PER_KEY: T * dk * 4, gi.GATE_TOKEN_SCALAR: T * 4}.get(w.gate, 0)
+    st = dk * dv * 4
+    if name == "gla_chunk_prep":
+        b = 2 * T * dk * 2 + lg + nch * 64 * 64 * 2 + nch * dk * 4 + (2 * Tp * dk * 2 if gated else 0)
+    elif name == "gla_bwd_state_sweep":
+        b = T * dk * 2 + T * dv * 2 + nch * dk * 4 + nch * dv * dk * 2 + (st if s0 else 0) + (st if glog and dst else 0)
+    elif name == "gla_bwd_dstate_sweep":
+        b = T * dk * 2 + T * dv * 2 + nch * dk * 4 + nch * dv * dk * 2 + (st if dst else 0) + st
+    elif name == "gla_bwd_boundary":
+        b = 2 * st + dk * 4
+    elif name == "gla_bwd_grads":
+        b = (2 * nch * dv * dk * 2 + 2 * T * dv * 2 + 2 * Tp * dk * 2 + nch * 64 * 64 * 2 + nch * dk * 4 + lg
+             + 2 * T * dk * 4 + T * dv * 4 + ((T * dk * 4 + nch * dk * 4) if glog else 0))
+    elif name == "gla_bwd_gate_tail":
+        b = 2 * T * dk * 4 + 4 * nch * dk * 4
+    else:
+        return None
+    return BH * b
+
+
 def run_backward(args, w):
-    """Times gla_bwd (inputs resident in HBM, L2 flushed between steps) and prints one line."""
+    """Times gla_bwd (inputs resident in HBM, L2 flushed between steps) and prints one line.
+    A step is the whole backward (its stages back to back through gla_bwd_stage, events only
+    before and after); the per-stage breakdown comes from as many further steps with an event
+    between stages."""
     import torch
-    import chunkwise_gated_linear_gla_gb300 as gla
     from chunkwise_gated_linear_gla_gb300 import binding as bnd
     from chunkwise_gated_linear_gla_gb300 import build as gbuild
     from chunkwise_gated_linear_gla_gb300 import inputs as gi
@@ -405,42 +457,82 @@ def run_backward(args, w):
     nbytes = bnd.gla_bwd_workspace_size(p)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), nbytes
+    nst = bnd.gla_bwd_num_stages(p)
+    names = [bnd.gla_bwd_stage_name(p, i) for i in range(nst)]
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     clean = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        for i in range(nst):
+            if evs is not None:
+                evs[i].record(stream)
+            bnd.gla_bwd_stage(p, i, stream)
+        if evs is not None:
+            evs[nst].record(stream)
+
     for _ in range(args.warmup):
         flush.zero_(); clean.sum()
-        bnd.gla_bwd(p, stream)
+        step()
     torch.cuda.synchronize()
     if bnd.gla_device_status(stream) != 0:
         raise SystemExit("device status error after warm-up")
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = Clocks(0)
     clocks.start()
-    for a, b in evs:
+    torch.cuda.synchronize()
+    for a, b in pairs:
         flush.zero_(); clean.sum()
         a.record(stream)
-        bnd.gla_bwd(p, stream)
+        step()
         b.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    times = sorted(a.elapsed_time(b) for a, b in evs)
+    staged = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    for evs in staged:
+        flush.zero_(); clean.sum()
+        step(evs)
+    torch.cuda.synchronize()
+    if bnd.gla_device_status(stream) != 0:
+        raise SystemExit("device status error in timed region")
+    times = sorted(a.elapsed_time(b) for a, b in pairs)
     ms = sum(times) / len(times)
+    stage_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in staged) / len(staged) for i in range(nst)]
     flops = algorithmic_bwd(w)
     tflops = flops / (ms * 1e-3) / 1e12
-    tensor = w.dtype == torch.bfloat16 and w.dk in (64, 128, 256) and w.gate != gi.GATE_BILINEAR
-    if tensor:
-        # the chunk products run on the tensor cores (mma.sync, bf16 operands split into hi + lo
-        # parts, fp32 accumulation): rated against the bf16 tensor peak, as one product per FLOP
-        _, bf16_burst, _, src = peaks()
-        roof = {"kernel": "gla_bwd (tensor-core chunk products, all stages)", "bound": "tensor",
+    hbm, bf16_burst, _, src = peaks()
+    dom = max(range(nst), key=lambda i: stage_ms[i])
+    if bwd_chunk_form(w):
+        glog, dst_ = g is not None, True
+        per_kernel = []
+        for n_, t_ in zip(names, stage_ms):
+            b_ = bwd_stage_bytes(w, n_, glog=glog, dst=dst_, s0=S0 is not None)
+            per_kernel.append({"kernel": n_, "ms": t_, "compulsory_bytes": b_,
+                               "compulsory_gbs": b_ / (t_ * 1e-3) / 1e9, "dram_bytes_ncu": ncu_traffic(w.name, n_, "bwd")})
+        dk_ = per_kernel[dom]
+        roof = {"kernel": dk_["kernel"], "bound": "hbm", "achieved": dk_["compulsory_gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": dk_["compulsory_gbs"] / hbm, "traffic": dk_["dram_bytes_ncu"],
+                "peak_source": f"{src} HBM copy bandwidth", "bytes_per_launch": dk_["compulsory_bytes"],
+                "bytes_basis": "compulsory bytes of the kernel: its inputs, the workspace tensors it reads and "
+                               "writes, its outputs, each once", "kernels": per_kernel,
+                "pass_gbs": sum(k_["compulsory_bytes"] for k_ in per_kernel) / (ms * 1e-3) / 1e9}
+        kind = "chunk form: 64-row chunks on tcgen05, bf16 operands, fp32 accumulation"
+        launches_per_step = nst + (1 if "gla_bwd_gate_tail" in names else 0) + (
+            1 if w.gate in (gi.GATE_TOKEN_SCALAR, gi.GATE_HEAD_SCALAR) else 0)
+    elif w.dtype == torch.bfloat16 and w.dk in (64, 128, 256) and w.gate != gi.GATE_BILINEAR:
+        roof = {"kernel": "gla_bwd (split form: 16-row chunks, mma.sync on hi + lo bf16 operands)", "bound": "tensor",
                 "achieved": tflops, "peak": bf16_burst, "unit": "TFLOP/s", "frac": tflops / bf16_burst,
                 "traffic": None, "peak_source": f"{src} dense bf16 (burst: the pass is timed alone)"}
+        kind = "split form"
+        launches_per_step = 4 + (1 if w.gate in (gi.GATE_TOKEN_SCALAR, gi.GATE_HEAD_SCALAR) else 0) - (
+            1 if w.gate == 0 else 0)
     else:
         roof = {"kernel": "gla_bwd (CUDA cores, all stages)", "bound": "alu", "achieved": tflops,
                 "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tflops / FP32_ALU_TFLOPS, "traffic": None,
                 "peak_source": "nominal fp32 FFMA rate: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz"}
-    launches = 4 + (1 if w.gate in (gi.GATE_TOKEN_SCALAR, gi.GATE_HEAD_SCALAR) else 0) - (1 if w.gate == 0 else 0)
+        kind = "CUDA-core form"
+        launches_per_step = 4 + (1 if w.gate in (gi.GATE_TOKEN_SCALAR, gi.GATE_HEAD_SCALAR) else 0) - (
+            1 if w.gate == 0 else 0)
     line = {
         "metric": BWD_METRIC, "value": w.B * w.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -448,13 +540,17 @@ def run_backward(args, w):
         "data": "synthetic (seeded inputs of the workload; dO ~ N(0,1), dST ~ 0.1 N(0,1))",
         "config": {"workload": f"{w.name} backward: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
                                f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar', 'bilinear'][w.gate]}",
+                   "form": kind, "stages": names, "stage_ms": stage_ms,
                    "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",
                    "workspace_bytes": nbytes},
+        "tflops": tflops, "tflops_frac_bf16_peak": tflops / bf16_burst,
         "roofline": roof,
-        "timing": {"mean_ms": ms, "median_ms": times[len(times) // 2], "min_ms": times[0]},
+        "timing": {"mean_ms": ms, "median_ms": times[len(times) // 2], "min_ms": times[0],
+                   "note": "mean is the value's basis: whole passes, events only before and after each; "
+                           "stage_ms comes from as many further steps with an event between stages"},
         "cpu_baseline": cpu,
         "e2e": None,
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

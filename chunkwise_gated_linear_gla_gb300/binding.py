@@ -22,7 +22,8 @@ GLA_PATH_AUTO, GLA_PATH_TENSOR, GLA_PATH_SIMT, GLA_PATH_STAGED, GLA_PATH_FUSED, 
 EXPORTED = ("gla_fwd", "gla_fwd_ex", "gla_fwd_workspace_size", "gla_fwd_num_stages",
             "gla_fwd_stage", "gla_fwd_stage_name", "gla_device_status", "gla_status_string",
             "gla_version", "gla_fwd_noalloc", "gla_fwd_host", "gla_host_release", "gla_bwd",
-            "gla_bwd_workspace_size", "gla_segment_pair_workspace_size", "gla_segment_pair",
+            "gla_bwd_workspace_size", "gla_bwd_num_stages", "gla_bwd_stage", "gla_bwd_stage_name",
+            "gla_segment_pair_workspace_size", "gla_segment_pair",
             "gla_pair_scan", "gla_pair_combine", "gla_selftest_bounded_wait")
 
 
@@ -103,6 +104,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.gla_bwd.argtypes = [ctypes.POINTER(gla_bwd_params), vp]
         lib.gla_bwd_workspace_size.restype = ctypes.c_size_t
         lib.gla_bwd_workspace_size.argtypes = [ctypes.POINTER(gla_bwd_params)]
+        lib.gla_bwd_num_stages.restype = i
+        lib.gla_bwd_num_stages.argtypes = [ctypes.POINTER(gla_bwd_params)]
+        lib.gla_bwd_stage.restype = st
+        lib.gla_bwd_stage.argtypes = [ctypes.POINTER(gla_bwd_params), i, vp]
+        lib.gla_bwd_stage_name.restype = ctypes.c_char_p
+        lib.gla_bwd_stage_name.argtypes = [ctypes.POINTER(gla_bwd_params), i]
         lib.gla_fwd_host.restype = st
         lib.gla_fwd_host.argtypes = [P, ctypes.c_size_t, vp]
         lib.gla_host_release.restype = st
@@ -206,6 +213,21 @@ def gla_bwd(p: gla_bwd_params, stream=None, check=True) -> int:
 
 def gla_bwd_workspace_size(p: gla_bwd_params) -> int:
     return int(load().gla_bwd_workspace_size(ctypes.byref(p)))
+
+
+def gla_bwd_num_stages(p: gla_bwd_params) -> int:
+    return int(load().gla_bwd_num_stages(ctypes.byref(p)))
+
+
+def gla_bwd_stage(p: gla_bwd_params, stage: int, stream=None, check=True) -> int:
+    s = load().gla_bwd_stage(ctypes.byref(p), stage, _stream(stream))
+    if check:
+        _check(s, f"gla_bwd_stage({stage})")
+    return s
+
+
+def gla_bwd_stage_name(p: gla_bwd_params, stage: int) -> str:
+    return load().gla_bwd_stage_name(ctypes.byref(p), stage).decode()
 
 
 def make_bwd_params(q, k, v, log_g, S0, dO, dST, dq, dk, dv, dlog_g, dS0, gate=None,

@@ -1326,74 +1326,117 @@ int device_sm_count() {
     return n;
 }
 
-// The chunk form: prep (Q (.) Lambda, K (.) Gamma, gamma, scores), the state sweep forward
-// (H, and S_T), the sweep of dL/dS backward (D, and dS0), the boundary term, the
-// chunk-parallel gradients, the gate tail.
-cudaError_t launch_chunk_form(const gla_bwd_params& p, const ChunkPlan& cp, uint8_t* w, int* status, cudaStream_t s)
+// The chunk form in stages: the prep (Q (.) Lambda, K (.) Gamma, gamma, scores), the state
+// sweep forward (H, and S_T), the sweep of dL/dS backward (D, and dS0), the boundary term
+// rowsum(dST (.) S_T), the chunk-parallel gradients, the gate tail (the later chunks' totals
+// added to each chunk's in-chunk sums; sums over keys for the scalar gates).
+enum ChunkStage { CS_PREP, CS_SWEEP_FWD, CS_SWEEP_REV, CS_BOUNDARY, CS_GRADS, CS_GATE, CS_N };
+
+const char* chunk_stage_name(int k)
+{
+    switch (k) {
+    case CS_PREP: return "gla_chunk_prep";
+    case CS_SWEEP_FWD: return "gla_bwd_state_sweep";
+    case CS_SWEEP_REV: return "gla_bwd_dstate_sweep";
+    case CS_BOUNDARY: return "gla_bwd_boundary";
+    case CS_GRADS: return "gla_bwd_grads";
+    case CS_GATE: return "gla_bwd_gate_tail";
+    }
+    return "?";
+}
+
+// the stages the chunk form runs for *p, in order
+int chunk_stages(const gla_bwd_params* p, int* out)
+{
+    int n = 0;
+    out[n++] = CS_PREP;
+    out[n++] = CS_SWEEP_FWD;
+    out[n++] = CS_SWEEP_REV;
+    if (p->grad_log_g && p->grad_ST) out[n++] = CS_BOUNDARY;
+    out[n++] = CS_GRADS;
+    if (p->grad_log_g) out[n++] = CS_GATE;
+    return n;
+}
+
+cudaError_t run_chunk_stage(const gla_bwd_params& p, const ChunkPlan& cp, uint8_t* w, int* status, int k,
+                            cudaStream_t s)
 {
     cudaError_t e;
     const int sms = device_sm_count();
     const int BH = p.B * p.H;
     const bool gated = p.gate != GLA_GATE_NONE;
-    gla_fwd_params fp;
-    std::memset(&fp, 0, sizeof(fp));
-    fp.q = p.q; fp.k = p.k; fp.v = p.v; fp.log_g = p.log_g; fp.S0 = p.S0;
-    fp.B = p.B; fp.H = p.H; fp.T = p.T; fp.dk = p.dk; fp.dv = p.dv;
-    fp.dtype = p.dtype; fp.gate = p.gate; fp.path = GLA_PATH_TENSOR;
-    Plan pl;
-    pl.path = GLA_PATH_TENSOR;
-    pl.nchunks = cp.nch; pl.Tpad = cp.Tpad; pl.n_dvt = p.dv / kDvTile; pl.raw_qk = cp.raw; pl.sms = sms;
-    pl.off_qt = cp.off_qt; pl.off_kt = cp.off_kt; pl.off_A = cp.off_A; pl.off_gam = cp.off_gam;
-    if ((e = launch_prep(fp, pl, w, status, s, false)) != cudaSuccess) return e;
     const void* qt = cp.raw ? p.q : static_cast<const void*>(w + cp.off_qt);
     const void* kt = cp.raw ? p.k : static_cast<const void*>(w + cp.off_kt);
     const long long kt_rows = cp.raw ? p.T : cp.Tpad;
     const float* gam = gated ? reinterpret_cast<const float*>(w + cp.off_gam) : nullptr;
     float* ST = cp.off_ST ? reinterpret_cast<float*>(w + cp.off_ST) : nullptr;
     float* bnd = cp.off_bnd ? reinterpret_cast<float*>(w + cp.off_bnd) : nullptr;
-    StateSweep fw;
-    fw.kt = kt; fw.kt_rows = kt_rows; fw.v = p.v; fw.gam = gam; fw.S_in = p.S0; fw.S_out = ST;
-    fw.Hst = w + cp.off_H; fw.reverse = false;
-    fw.BH = BH; fw.T = p.T; fw.dk = p.dk; fw.dv = p.dv; fw.nch = cp.nch;
-    if ((e = launch_state_sweep(fw, status, s)) != cudaSuccess) return e;
-    StateSweep rv = fw;
-    rv.kt = qt; rv.v = p.grad_O; rv.S_in = p.grad_ST; rv.S_out = p.grad_S0; rv.Hst = w + cp.off_D; rv.reverse = true;
-    if ((e = launch_state_sweep(rv, status, s)) != cudaSuccess) return e;
-    if (ST && bnd && (e = launch_bwd_boundary(p.grad_ST, ST, bnd, (long long)BH * p.dk, p.dv, sms, s)) != cudaSuccess)
-        return e;
-    BwdGrads g;
-    g.q = p.q; g.k = p.k; g.v = p.v; g.dO = p.grad_O; g.log_g = p.log_g;
-    g.qt = qt; g.kt = kt; g.kt_rows = kt_rows;
-    g.A = w + cp.off_A; g.gam = gam;
-    g.Hst = w + cp.off_H; g.Dst = w + cp.off_D;
-    g.bnd = bnd;
-    g.gq = p.grad_q; g.gk = p.grad_k; g.gv = p.grad_v;
     const bool per_key = p.gate == GLA_GATE_PER_KEY;
-    g.R = !p.grad_log_g ? nullptr : per_key ? p.grad_log_g : reinterpret_cast<float*>(w + cp.off_dla);
-    g.ctot = p.grad_log_g ? reinterpret_cast<float*>(w + cp.off_ctot) : nullptr;
-    g.BH = BH; g.H = p.H; g.T = p.T; g.dk = p.dk; g.dv = p.dv; g.gate = p.gate; g.sms = sms;
-    if ((e = launch_bwd_grads(g, status, s)) != cudaSuccess) return e;
-    if (!p.grad_log_g) return cudaSuccess;
-    // the gate gradient: each chunk's terms are already summed over its later rows; add the
-    // totals of the later chunks (their reverse cumulative sum, in place, then a shifted add)
-    BwdArgs a;
-    std::memset(&a, 0, sizeof(a));
-    a.B = p.B; a.H = p.H; a.T = cp.nch; a.dk = p.dk; a.dv = p.dv; a.gate = p.gate;
-    gla_bwd_revsum_kernel<<<dim3(BH, (p.dk + 31) / 32), NT, 0, s>>>(a, g.ctot, g.ctot, p.dk);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_bwd_gate_fixup(g.R, g.ctot, BH, p.T, p.dk, sms, s)) != cudaSuccess) return e;
-    if (per_key) return cudaSuccess;
-    a.T = p.T;
-    a.glog = p.grad_log_g;
-    a.dla = g.R;
-    if (p.gate == GLA_GATE_TOKEN_SCALAR) {
-        const size_t rows = (size_t)BH * p.T;
-        const int grid = (int)((rows * 32 + NT - 1) / NT < 4096 ? (rows * 32 + NT - 1) / NT : 4096);
-        gla_bwd_token_gate_kernel<<<grid, NT, 0, s>>>(a);
-    } else {
-        gla_bwd_head_gate_kernel<<<p.H, NT, 0, s>>>(a);
+    float* R = !p.grad_log_g ? nullptr : per_key ? p.grad_log_g : reinterpret_cast<float*>(w + cp.off_dla);
+    float* ctot = p.grad_log_g ? reinterpret_cast<float*>(w + cp.off_ctot) : nullptr;
+    switch (k) {
+    case CS_PREP: {
+        gla_fwd_params fp;
+        std::memset(&fp, 0, sizeof(fp));
+        fp.q = p.q; fp.k = p.k; fp.v = p.v; fp.log_g = p.log_g; fp.S0 = p.S0;
+        fp.B = p.B; fp.H = p.H; fp.T = p.T; fp.dk = p.dk; fp.dv = p.dv;
+        fp.dtype = p.dtype; fp.gate = p.gate; fp.path = GLA_PATH_TENSOR;
+        Plan pl;
+        pl.path = GLA_PATH_TENSOR;
+        pl.nchunks = cp.nch; pl.Tpad = cp.Tpad; pl.n_dvt = p.dv / kDvTile; pl.raw_qk = cp.raw; pl.sms = sms;
+        pl.off_qt = cp.off_qt; pl.off_kt = cp.off_kt; pl.off_A = cp.off_A; pl.off_gam = cp.off_gam;
+        return launch_prep(fp, pl, w, status, s, false);
     }
-    return cudaGetLastError();
+    case CS_SWEEP_FWD:
+    case CS_SWEEP_REV: {
+        StateSweep sw;
+        const bool fwd = k == CS_SWEEP_FWD;
+        sw.kt = fwd ? kt : qt; sw.kt_rows = kt_rows; sw.v = fwd ? p.v : p.grad_O; sw.gam = gam;
+        sw.S_in = fwd ? p.S0 : p.grad_ST;
+        sw.S_out = fwd ? ST : p.grad_S0;
+        sw.Hst = w + (fwd ? cp.off_H : cp.off_D);
+        sw.reverse = !fwd;
+        sw.BH = BH; sw.T = p.T; sw.dk = p.dk; sw.dv = p.dv; sw.nch = cp.nch;
+        return launch_state_sweep(sw, status, s);
+    }
+    case CS_BOUNDARY:
+        return launch_bwd_boundary(p.grad_ST, ST, bnd, (long long)BH * p.dk, p.dv, sms, s);
+    case CS_GRADS: {
+        BwdGrads g;
+        g.q = p.q; g.k = p.k; g.v = p.v; g.dO = p.grad_O; g.log_g = p.log_g;
+        g.qt = qt; g.kt = kt; g.kt_rows = kt_rows;
+        g.A = w + cp.off_A; g.gam = gam;
+        g.Hst = w + cp.off_H; g.Dst = w + cp.off_D;
+        g.bnd = (ST && bnd) ? bnd : nullptr;
+        g.gq = p.grad_q; g.gk = p.grad_k; g.gv = p.grad_v;
+        g.R = R; g.ctot = ctot;
+        g.BH = BH; g.H = p.H; g.T = p.T; g.dk = p.dk; g.dv = p.dv; g.gate = p.gate; g.sms = sms;
+        return launch_bwd_grads(g, status, s);
+    }
+    case CS_GATE: {
+        // each chunk's terms are already summed over its later rows: add the totals of the
+        // later chunks (their reverse cumulative sum, in place, then a shifted add)
+        BwdArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.B = p.B; a.H = p.H; a.T = cp.nch; a.dk = p.dk; a.dv = p.dv; a.gate = p.gate;
+        gla_bwd_revsum_kernel<<<dim3(BH, (p.dk + 31) / 32), NT, 0, s>>>(a, ctot, ctot, p.dk);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_bwd_gate_fixup(R, ctot, BH, p.T, p.dk, sms, s)) != cudaSuccess) return e;
+        if (per_key) return cudaSuccess;
+        a.T = p.T;
+        a.glog = p.grad_log_g;
+        a.dla = R;
+        if (p.gate == GLA_GATE_TOKEN_SCALAR) {
+            const size_t rows = (size_t)BH * p.T;
+            const int grid = (int)((rows * 32 + NT - 1) / NT < 4096 ? (rows * 32 + NT - 1) / NT : 4096);
+            gla_bwd_token_gate_kernel<<<grid, NT, 0, s>>>(a);
+        } else {
+            gla_bwd_head_gate_kernel<<<p.H, NT, 0, s>>>(a);
+        }
+        return cudaGetLastError();
+    }
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <typename Tin>
@@ -1466,8 +1509,12 @@ extern "C" gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream)
         if (!p->workspace || p->workspace_bytes < cp.bytes) return GLA_ERR_WORKSPACE;
         int* status = device_status_ptr();
         if (!status) return GLA_ERR_CUDA;
-        const cudaError_t e = launch_chunk_form(*p, cp, static_cast<uint8_t*>(p->workspace), status, stream);
-        return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+        int st[CS_N];
+        const int n = chunk_stages(p, st);
+        for (int i = 0; i < n; ++i)
+            if (run_chunk_stage(*p, cp, static_cast<uint8_t*>(p->workspace), status, st[i], stream) != cudaSuccess)
+                return GLA_ERR_CUDA;
+        return GLA_OK;
     }
     const BwdPlan pl = bwd_plan(p);
     if (!p->workspace || p->workspace_bytes < pl.bytes) return GLA_ERR_WORKSPACE;
@@ -1492,4 +1539,39 @@ extern "C" gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream)
     const cudaError_t e = p->dtype == GLA_FP32 ? launch_all<float>(a, *p, stream, false)
                                                : launch_all<__nv_bfloat16>(a, *p, stream, use_tc);
     return e == cudaSuccess ? GLA_OK : GLA_ERR_CUDA;
+}
+
+extern "C" int gla_bwd_num_stages(const gla_bwd_params* p)
+{
+    if (bwd_validate(p) != GLA_OK) return -1;
+    if (bwd_kind(p) != BWD_CHUNK) return 1;
+    int st[CS_N];
+    return chunk_stages(p, st);
+}
+
+extern "C" const char* gla_bwd_stage_name(const gla_bwd_params* p, int stage)
+{
+    const int n = gla_bwd_num_stages(p);
+    if (n < 0 || stage < 0 || stage >= n) return "invalid";
+    if (bwd_kind(p) != BWD_CHUNK) return bwd_kind(p) == BWD_SPLIT ? "gla_bwd_split" : "gla_bwd_simt";
+    int st[CS_N];
+    chunk_stages(p, st);
+    return chunk_stage_name(st[stage]);
+}
+
+extern "C" gla_status gla_bwd_stage(const gla_bwd_params* p, int stage, cudaStream_t stream)
+{
+    const int n = gla_bwd_num_stages(p);
+    if (n < 0) return bwd_validate(p);
+    if (stage < 0 || stage >= n) return GLA_ERR_INVALID_ARG;
+    if (bwd_kind(p) != BWD_CHUNK) return gla_bwd(p, stream);
+    const ChunkPlan cp = chunk_plan(p);
+    if (!p->workspace || p->workspace_bytes < cp.bytes) return GLA_ERR_WORKSPACE;
+    int* status = device_status_ptr();
+    if (!status) return GLA_ERR_CUDA;
+    int st[CS_N];
+    chunk_stages(p, st);
+    return run_chunk_stage(*p, cp, static_cast<uint8_t*>(p->workspace), status, st[stage], stream) == cudaSuccess
+               ? GLA_OK
+               : GLA_ERR_CUDA;
 }

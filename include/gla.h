@@ -97,7 +97,10 @@ typedef enum {
  *                    memory; it needs no workspace (gla_fwd_workspace_size
  *                    returns 0), at the cost of speed on this hardware (the
  *                    cross-CTA exchange of every chunk sits on the chain).
- *                    GLA_ERR_UNSUPPORTED for other shapes or gates. */
+ *                    GLA_ERR_UNSUPPORTED for other shapes or gates.
+ *   GLA_PATH_SPLIT   backward only (gla_bwd): the 16-row form with split bf16
+ *                    operands; GLA_ERR_INVALID_ARG for the forward pass.
+ * For the backward, TENSOR names its 64-row chunk form (see gla_bwd). */
 typedef enum {
     GLA_PATH_AUTO = 0,
     GLA_PATH_TENSOR = 1,
@@ -302,25 +305,40 @@ gla_status gla_pair_combine(const float* log_Gamma2, const float* S2, float* log
  * grad_ST = dL/dS_T (NULL: zero). It returns dL/dq, dL/dk, dL/dv, dL/dlog_g
  * (shaped like log_g: per key, per token, or per head summed over batch
  * rows) and dL/dS0 (even when S0 is NULL, i.e. zero). The chunkwise form
- * follows the GLA paper's §3.3 / §4.2: a forward sweep keeps the state after
- * every 16-row chunk, a reverse sweep carries dL/dS through the chunks, and
+ * follows the GLA paper's §3.3 / §4.2: a forward sweep keeps the state
+ * entering every chunk, a reverse sweep carries dL/dS through the chunks, and
  * the gate gradient is the reverse cumulative sum over tokens of
  * q (.) dq - k (.) dk (plus rowsum(grad_ST (.) S_T) at the last token).
  * Every gate mode and both dtypes are supported (q, k, v and grad_O in
- * `dtype`; all gradients fp32; dk <= 256). The bilinear gate takes log_b and
- * returns dL/dlog_b in grad_log_b ([B,H,T,dv], may be NULL), on the CUDA-core
- * path; that gradient is the reverse cumulative sum over tokens of
- * o (.) do - v (.) dv (plus colsum(grad_ST (.) S_T) at the last token), with o
- * recomputed inside. For bf16 inputs with dk in {64, 128, 256} and the other
- * gates, the chunk products run on the tensor cores (mma.sync, operands split
- * into hi + lo bf16 parts, fp32 accumulation); otherwise, or with
- * path = GLA_PATH_SIMT, everything runs in fp32 on CUDA cores. (The backward
- * is the next step after the forward pass; no page gives numbers for it.)
+ * `dtype`; all gradients fp32; dk <= 256). Three forms compute it:
+ *   chunk form (AUTO's choice for bf16 inputs with dk in {128, 256}, dv a
+ *     multiple of 128, q, k, v and grad_O 16-byte aligned, and any gate but
+ *     the bilinear one; also GLA_PATH_TENSOR, which returns
+ *     GLA_ERR_UNSUPPORTED for other inputs): 64-row chunks on the tcgen05
+ *     tensor cores. The chunk pass's state sweeps keep every chunk's state
+ *     and every chunk's dL/dS (bf16), then one chunk-parallel kernel forms
+ *     dq, dk, dv and the gate terms. bf16 operands, fp32 accumulation, like
+ *     the forward pass.
+ *   split form (AUTO's choice for the other bf16 inputs with dk in
+ *     {64, 128, 256} and no bilinear gate; GLA_PATH_SPLIT): 16-row chunks
+ *     whose products run on the tensor cores (mma.sync) with every
+ *     non-input operand split into hi + lo bf16 parts, about 16 mantissa
+ *     bits, fp32 accumulation.
+ *   CUDA-core form (fp32 inputs, other shapes, the bilinear gate, or
+ *     GLA_PATH_SIMT): 16-row chunks in fp32 on CUDA cores.
+ * The bilinear gate takes log_b and returns dL/dlog_b in grad_log_b
+ * ([B,H,T,dv], may be NULL), on the CUDA-core form; that gradient is the
+ * reverse cumulative sum over tokens of o (.) do - v (.) dv (plus
+ * colsum(grad_ST (.) S_T) at the last token), with o recomputed inside.
+ * (The backward is the next step after the forward pass; no page gives
+ * numbers for it.)
  *
  * Ownership and asynchrony are as for gla_fwd_ex: every pointer is a device
  * pointer owned by the caller, work is enqueued on `stream`, and the caller
  * supplies a workspace of gla_bwd_workspace_size(p) bytes (256-byte aligned;
- * it holds the chunk states, BH * ceil(T/16) * dk * dv * 4 bytes, and the
+ * the size depends on the form the pointers and shapes select: the chunk
+ * form keeps two bf16 states per 64-row chunk, BH * ceil(T/64) * dk * dv * 4
+ * bytes in all, the 16-row forms one fp32 state per 16-row chunk and
  * per-tile partial gradients). grad_log_g and grad_S0 may be NULL (not
  * wanted); grad_log_g must be NULL without a gate. Outputs may not overlap
  * inputs or each other. Results are bitwise reproducible.
@@ -343,8 +361,7 @@ typedef struct {
     gla_gate gate;
     void* workspace;
     size_t workspace_bytes;
-    int path;               /* gla_path: AUTO takes the tensor-core products for bf16 with dk in
-                               {64,128,256} (not with the bilinear gate), else the fp32 CUDA-core path */
+    int path;               /* gla_path: AUTO, TENSOR (chunk form), SPLIT or SIMT (see above) */
     const float* log_b;     /* [B,H,T,dv] log(beta_t) for GLA_GATE_BILINEAR, else NULL */
     float* grad_log_b;      /* [B,H,T,dv] dL/dlog_b, or NULL (not wanted; bilinear gate only) */
 } gla_bwd_params;
@@ -353,6 +370,17 @@ gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream);
 
 /* Bytes of workspace gla_bwd needs for *p (0 for invalid parameters). */
 size_t gla_bwd_workspace_size(const gla_bwd_params* p);
+
+/* gla_bwd in its stages, for timing each kernel: gla_bwd(p) ==
+ * gla_bwd_stage(p, 0) ... gla_bwd_stage(p, n-1) on one stream (each stage
+ * reads what the ones before it wrote to the workspace). The chunk form has
+ * up to six (gate prep, state sweep, dL/dS sweep, boundary term, gradients,
+ * gate tail); the 16-row forms one. gla_bwd_num_stages returns n, or -1 for
+ * invalid parameters; gla_bwd_stage_name a static string naming stage i's
+ * kernel ("invalid" out of range). */
+int gla_bwd_num_stages(const gla_bwd_params* p);
+gla_status gla_bwd_stage(const gla_bwd_params* p, int stage, cudaStream_t stream);
+const char* gla_bwd_stage_name(const gla_bwd_params* p, int stage);
 
 /* Synchronises `stream`, then reads and clears the library's device status
  * word for the current device. GLA_ERR_TIMEOUT if a kernel gave up on a

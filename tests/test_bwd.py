@@ -263,6 +263,32 @@ def test_bwd_chunk_form_many_items_per_cta():
 
 
 @pytest.mark.gpu
+def test_bwd_stages_in_sequence_equal_the_call():
+    """gla_bwd_stage(p, 0) ... gla_bwd_stage(p, n-1) gives bitwise the same gradients as gla_bwd."""
+    gbuild.build()
+    w = gi.Workload("t", B=2, H=2, T=300, dk=128, dv=256, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY, s0_std=0.2)
+    x, dO, dST = _inputs(w, 18)
+    ref = _gpu(x, dO, dST)
+    c = lambda t: None if t is None else t.cuda()
+    dev = torch.device("cuda")
+    f32 = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)
+    dq, dk, dv = f32(2, 2, 300, 128), f32(2, 2, 300, 128), f32(2, 2, 300, 256)
+    dg, dS0 = f32(2, 2, 300, 128), f32(2, 2, 128, 256)
+    p = bnd.make_bwd_params(c(x["q"]), c(x["k"]), c(x["v"]), c(x["log_g"]), c(x["S0"]), c(dO), c(dST), dq, dk, dv,
+                            dg, dS0, gate=x["gate"])
+    n = bnd.gla_bwd_workspace_size(p)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), n
+    assert bnd.gla_bwd_num_stages(p) == 6
+    for i in range(6):
+        bnd.gla_bwd_stage(p, i)
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    for a, b in zip(ref, [dq, dk, dv, dg, dS0]):
+        np.testing.assert_array_equal(a, to_np(b))
+
+
+@pytest.mark.gpu
 def test_bwd_empty_sequence():
     gbuild.build(); oracle.build()
     for gate in GATES:
@@ -396,6 +422,25 @@ def test_bwd_workspace_size():
     nch, ndvt, BH = 7, 2, 6
     assert n >= 4 * (BH * nch * 64 * 128 + 2 * ndvt * BH * 100 * 64 + BH * 100 * 64)
     assert bnd.gla_bwd_workspace_size(_bp(dk=40)) == 0
+
+
+def test_bwd_stages():
+    """The staged backward: the chunk form's six stages (four without a gate gradient, five
+    without grad_ST), the 16-row forms' one; out-of-range names."""
+    gbuild.build()
+    far = {n: (i + 1) << 28 for i, n in enumerate(["q", "k", "v", "log_g", "grad_O", "grad_q", "grad_k", "grad_v",
+                                                   "grad_log_g", "grad_ST"])}
+    p = _bp(B=2, H=3, T=100, dk=128, dv=256, **far)
+    names = [bnd.gla_bwd_stage_name(p, i) for i in range(bnd.gla_bwd_num_stages(p))]
+    assert names == ["gla_chunk_prep", "gla_bwd_state_sweep", "gla_bwd_dstate_sweep", "gla_bwd_boundary",
+                     "gla_bwd_grads", "gla_bwd_gate_tail"]
+    assert bnd.gla_bwd_num_stages(_bp(B=2, H=3, T=100, dk=128, dv=256, **dict(far, grad_ST=None))) == 5
+    assert bnd.gla_bwd_num_stages(_bp(B=2, H=3, T=100, dk=128, dv=256, **dict(far, grad_log_g=None))) == 4
+    split = _bp(B=2, H=3, T=100, dk=64, dv=128, **far)
+    assert bnd.gla_bwd_num_stages(split) == 1 and bnd.gla_bwd_stage_name(split, 0) == "gla_bwd_split"
+    assert bnd.gla_bwd_stage_name(split, 1) == "invalid"
+    assert bnd.gla_bwd_num_stages(_bp(dk=40)) == -1
+    assert bnd.gla_bwd_stage(p, 7, stream=0, check=False) == bnd.GLA_ERR_INVALID_ARG
 
 
 def test_bwd_chunk_form_workspace_size():
