@@ -385,7 +385,18 @@ def algorithmic_bwd(w):
     return w.B * w.H * w.T * (10 * w.dk * w.dv + 2 * (C + 1) * (w.dk + w.dv))
 
 
-def bwd_stage_bytes(w, name, glog=True, dst=True, s0=True):
+def bwd_segments(w, sms):
+    """The chunk form's sequence split of its two sweeps (the library's rule)."""
+    nch = -(-w.T // 64)
+    units = w.B * w.H * (w.dv // 128)
+    if units * 2 > sms or nch < 16:
+        return 1
+    n = max(1, min(sms // units, nch // 8))
+    cps = -(-nch // n)
+    return -(-nch // cps)
+
+
+def bwd_stage_bytes(w, name, glog=True, dst=True, s0=True, nseg=1):
     """Compulsory DRAM bytes of one launch of a chunk-form stage: what it must read and write
     once (inputs, the workspace tensors it consumes and produces, its outputs)."""
     from chunkwise_gated_linear_gla_gb300 import inputs as gi
@@ -401,6 +412,10 @@ def bwd_stage_bytes(w, name, glog=True, dst=True, s0=True):
         b = T * dk * 2 + T * dv * 2 + nch * dk * 4 + nch * dv * dk * 2 + (st if s0 else 0) + (st if glog and dst else 0)
     elif name == "gla_bwd_dstate_sweep":
         b = T * dk * 2 + T * dv * 2 + nch * dk * 4 + nch * dv * dk * 2 + (st if dst else 0) + st
+    elif name in ("gla_chunk_state", "gla_chunk_dstate"):
+        b = T * dk * 2 + T * dv * 2 + nch * dk * 4 + nseg * st
+    elif name in ("gla_state_scan", "gla_dstate_scan"):
+        b = 2 * nseg * st + nch * dk * 4 + (st if (s0 if name == "gla_state_scan" else dst) else 0)
     elif name == "gla_bwd_boundary":
         b = 2 * st + dk * 4
     elif name == "gla_bwd_grads":
@@ -504,9 +519,10 @@ def run_backward(args, w):
     dom = max(range(nst), key=lambda i: stage_ms[i])
     if bwd_chunk_form(w):
         glog, dst_ = g is not None, True
+        nseg = bwd_segments(w, torch.cuda.get_device_properties(dev).multi_processor_count)
         per_kernel = []
         for n_, t_ in zip(names, stage_ms):
-            b_ = bwd_stage_bytes(w, n_, glog=glog, dst=dst_, s0=S0 is not None)
+            b_ = bwd_stage_bytes(w, n_, glog=glog, dst=dst_, s0=S0 is not None, nseg=nseg)
             per_kernel.append({"kernel": n_, "ms": t_, "compulsory_bytes": b_,
                                "compulsory_gbs": b_ / (t_ * 1e-3) / 1e9, "dram_bytes_ncu": ncu_traffic(w.name, n_, "bwd")})
         dk_ = per_kernel[dom]
@@ -541,6 +557,7 @@ def run_backward(args, w):
         "config": {"workload": f"{w.name} backward: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
                                f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar', 'bilinear'][w.gate]}",
                    "form": kind, "stages": names, "stage_ms": stage_ms,
+                   "sweep_segments": nseg if bwd_chunk_form(w) else None,
                    "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",
                    "workspace_bytes": nbytes},
         "tflops": tflops, "tflops_frac_bf16_peak": tflops / bf16_burst,

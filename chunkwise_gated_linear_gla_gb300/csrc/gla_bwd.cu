@@ -59,6 +59,7 @@ struct BwdArgs {
     // bilinear gate: log beta, its gradient, and the per-token terms o (.) do - v (.) dv
     // (plus colsum(dST (.) S_T) at the last token) whose reverse cumulative sum it is
     const float* log_b; float* glb; float* dlbe;   // [BH][T][dv] each
+    float* hpart;  // [H][HG_SPLIT] partial sums of the per-head gate gradient
     int B, H, T, dk, dv, gate, nch, ndvt, nplanes;
 };
 
@@ -1085,24 +1086,48 @@ __global__ void __launch_bounds__(NT) gla_bwd_token_gate_kernel(BwdArgs a)
     }
 }
 
-// per head: one CTA per h sums b, t and keys
-__global__ void __launch_bounds__(NT) gla_bwd_head_gate_kernel(BwdArgs a)
+// per head: the sum over b, t and keys in two levels with a fixed partition (bitwise
+// reproducible): CTA (h, j) sums slice j of head h's B * T * dk values, then one thread per
+// head adds the HG_SPLIT partial sums in order
+constexpr int HG_SPLIT = 64;
+__global__ void __launch_bounds__(NT) gla_bwd_head_gate_part_kernel(BwdArgs a, float* part)
 {
-    __shared__ float part[NT];
-    const int h = blockIdx.x;
-    const size_t per = (size_t)a.T * a.dk;
+    __shared__ float red[NT];
+    const int h = blockIdx.x, j = blockIdx.y;
+    const size_t per = (size_t)a.T * a.dk, tot = (size_t)a.B * per;   // per is a multiple of 16
+    const size_t L = ((tot + HG_SPLIT - 1) / HG_SPLIT + 3) / 4 * 4;
+    const size_t e0 = min(tot, (size_t)j * L), e1 = min(tot, e0 + L);
     float s = 0.f;
-    for (int b = 0; b < a.B; ++b) {
-        const float* p = a.dla + ((size_t)b * a.H + h) * per;
-        for (size_t e = threadIdx.x; e < per; e += NT) s += p[e];
+    for (size_t e = e0 + (size_t)threadIdx.x * 4; e < e1; e += (size_t)NT * 4) {
+        const size_t b = e / per, off = e % per;   // a float4 never crosses from one b to the next
+        const float4 v = *reinterpret_cast<const float4*>(a.dla + ((size_t)b * a.H + h) * per + off);
+        s += (v.x + v.y) + (v.z + v.w);
     }
-    part[threadIdx.x] = s;
+    red[threadIdx.x] = s;
     __syncthreads();
     for (int w = NT / 2; w > 0; w >>= 1) {
-        if ((int)threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+        if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
         __syncthreads();
     }
-    if (threadIdx.x == 0) a.glog[h] = part[0];
+    if (threadIdx.x == 0) part[(size_t)h * HG_SPLIT + j] = red[0];
+}
+
+__global__ void gla_bwd_head_gate_sum_kernel(const float* part, float* glog, int H)
+{
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= H) return;
+    float s = 0.f;
+    for (int j = 0; j < HG_SPLIT; ++j) s += part[(size_t)h * HG_SPLIT + j];
+    glog[h] = s;
+}
+
+cudaError_t launch_head_gate(const BwdArgs& a, float* part, cudaStream_t s)
+{
+    gla_bwd_head_gate_part_kernel<<<dim3(a.H, HG_SPLIT), NT, 0, s>>>(a, part);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    gla_bwd_head_gate_sum_kernel<<<(a.H + 127) / 128, 128, 0, s>>>(part, a.glog, a.H);
+    return cudaGetLastError();
 }
 
 size_t states_smem(int dk) { return sizeof(float) * ((size_t)dk * DVT + (size_t)CS * dk + CS * DVT + dk + DVT); }
@@ -1113,7 +1138,8 @@ size_t chunks_smem(int dk) {
 
 struct BwdPlan {
     int nch = 0, ndvt = 0;
-    size_t off_S = 0, off_Pq = 0, off_Pk = 0, off_Ag = 0, off_bnd = 0, off_dla = 0, off_dlbe = 0, bytes = 0;
+    size_t off_S = 0, off_Pq = 0, off_Pk = 0, off_Ag = 0, off_bnd = 0, off_dla = 0, off_dlbe = 0, off_hpart = 0,
+           bytes = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1133,6 +1159,9 @@ BwdPlan bwd_plan(const gla_bwd_params* p)
     pl.off_dla = off; off = up256(off + BH * p->T * p->dk * 4);
     if (p->gate == GLA_GATE_BILINEAR) {
         pl.off_dlbe = off; off = up256(off + BH * p->T * p->dv * 4);
+    }
+    if (p->gate == GLA_GATE_HEAD_SCALAR) {
+        pl.off_hpart = off; off = up256(off + (size_t)p->H * HG_SPLIT * 4);
     }
     pl.bytes = off;
     return pl;
@@ -1163,15 +1192,35 @@ BwdKind bwd_kind(const gla_bwd_params* p) {
     return tc_shape_ok(p) ? BWD_SPLIT : BWD_SIMT;
 }
 
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 148;
+    return n;
+}
+
+// Sequence segments of the chunk form's two sweeps: as for the forward pass, a split pays
+// when the B * H * dv-tile sweeps are well under one wave and the sequence is long.
+int bwd_segments(const gla_bwd_params* p, int nch, int sms)
+{
+    const long long units = (long long)p->B * p->H * (p->dv / kDvTile);
+    if (units * 2 > sms || nch < 16) return 1;
+    long long n = sms / units;
+    if (n > nch / 8) n = nch / 8;
+    return n < 1 ? 1 : (int)n;
+}
+
 // Workspace of the chunk form: the prep's Q (.) Lambda, K (.) Gamma (gated), scores and
 // chunk decays; the two sweeps' chunk states H and D (bf16); S_T and the boundary term
 // (gate gradient with grad_ST); the per-token gate terms (scalar gates; the per-key
 // gradient takes them in place) and their per-chunk totals.
 struct ChunkPlan {
     int nch = 0, Tpad = 0;
+    int nseg = 1, cps = 0;   // the sweeps' sequence split
+    size_t off_segS = 0, off_segin = 0;
     bool raw = false;
     size_t off_qt = 0, off_kt = 0, off_A = 0, off_gam = 0, off_H = 0, off_D = 0, off_ST = 0, off_bnd = 0,
-           off_dla = 0, off_ctot = 0, bytes = 0;
+           off_dla = 0, off_ctot = 0, off_hpart = 0, bytes = 0;
 };
 
 ChunkPlan chunk_plan(const gla_bwd_params* p)
@@ -1190,6 +1239,13 @@ ChunkPlan chunk_plan(const gla_bwd_params* p)
     c.off_gam = off; off = up256(off + BH * c.nch * p->dk * 4);
     c.off_H = off;   off = up256(off + BH * c.nch * p->dv * p->dk * 2);
     c.off_D = off;   off = up256(off + BH * c.nch * p->dv * p->dk * 2);
+    c.nseg = bwd_segments(p, c.nch, device_sm_count());
+    c.cps = (c.nch + c.nseg - 1) / c.nseg;
+    c.nseg = (c.nch + c.cps - 1) / c.cps;
+    if (c.nseg > 1) {   // each segment's zero-start state, then its entering state (both sweeps in turn)
+        c.off_segS = off;  off = up256(off + BH * c.nseg * p->dk * p->dv * 4);
+        c.off_segin = off; off = up256(off + BH * c.nseg * p->dk * p->dv * 4);
+    }
     if (p->grad_log_g) {
         if (p->grad_ST) {
             c.off_ST = off;  off = up256(off + BH * p->dk * p->dv * 4);
@@ -1199,6 +1255,9 @@ ChunkPlan chunk_plan(const gla_bwd_params* p)
             c.off_dla = off; off = up256(off + BH * p->T * p->dk * 4);
         }
         c.off_ctot = off; off = up256(off + BH * c.nch * p->dk * 4);
+        if (p->gate == GLA_GATE_HEAD_SCALAR) {
+            c.off_hpart = off; off = up256(off + (size_t)p->H * HG_SPLIT * 4);
+        }
     }
     c.bytes = off;
     return c;
@@ -1295,7 +1354,7 @@ cudaError_t launch_states_tc(const BwdArgs& a, int BH, cudaStream_t s)
 // The gate gradient from the per-token terms dla: the reverse cumulative sum over tokens
 // (per key: straight to grad_log_g), then the sums over keys (per token) or over batch rows,
 // tokens and keys (per head).
-cudaError_t launch_gate_tail(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s)
+cudaError_t launch_gate_tail(const BwdArgs& a, const gla_bwd_params& p, float* hpart, cudaStream_t s)
 {
     cudaError_t e;
     const int BH = p.B * p.H;
@@ -1313,29 +1372,29 @@ cudaError_t launch_gate_tail(const BwdArgs& a, const gla_bwd_params& p, cudaStre
     }
     if (a.glog && p.gate == GLA_GATE_HEAD_SCALAR) {
         if (n == 0) return cudaMemsetAsync(a.glog, 0, (size_t)p.H * sizeof(float), s);
-        gla_bwd_head_gate_kernel<<<p.H, NT, 0, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_head_gate(a, hpart, s)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
-int device_sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 148;
-    return n;
-}
 
 // The chunk form in stages: the prep (Q (.) Lambda, K (.) Gamma, gamma, scores), the state
 // sweep forward (H, and S_T), the sweep of dL/dS backward (D, and dS0), the boundary term
 // rowsum(dST (.) S_T), the chunk-parallel gradients, the gate tail (the later chunks' totals
 // added to each chunk's in-chunk sums; sums over keys for the scalar gates).
-enum ChunkStage { CS_PREP, CS_SWEEP_FWD, CS_SWEEP_REV, CS_BOUNDARY, CS_GRADS, CS_GATE, CS_N };
+enum ChunkStage {
+    CS_PREP, CS_SEG_FWD, CS_SCAN_FWD, CS_SWEEP_FWD, CS_SEG_REV, CS_SCAN_REV, CS_SWEEP_REV, CS_BOUNDARY, CS_GRADS,
+    CS_GATE, CS_N
+};
 
 const char* chunk_stage_name(int k)
 {
     switch (k) {
     case CS_PREP: return "gla_chunk_prep";
+    case CS_SEG_FWD: return "gla_chunk_state";
+    case CS_SCAN_FWD: return "gla_state_scan";
+    case CS_SEG_REV: return "gla_chunk_dstate";
+    case CS_SCAN_REV: return "gla_dstate_scan";
     case CS_SWEEP_FWD: return "gla_bwd_state_sweep";
     case CS_SWEEP_REV: return "gla_bwd_dstate_sweep";
     case CS_BOUNDARY: return "gla_bwd_boundary";
@@ -1348,9 +1407,12 @@ const char* chunk_stage_name(int k)
 // the stages the chunk form runs for *p, in order
 int chunk_stages(const gla_bwd_params* p, int* out)
 {
+    const bool split = chunk_plan(p).nseg > 1;
     int n = 0;
     out[n++] = CS_PREP;
+    if (split) { out[n++] = CS_SEG_FWD; out[n++] = CS_SCAN_FWD; }
     out[n++] = CS_SWEEP_FWD;
+    if (split) { out[n++] = CS_SEG_REV; out[n++] = CS_SCAN_REV; }
     out[n++] = CS_SWEEP_REV;
     if (p->grad_log_g && p->grad_ST) out[n++] = CS_BOUNDARY;
     out[n++] = CS_GRADS;
@@ -1387,16 +1449,42 @@ cudaError_t run_chunk_stage(const gla_bwd_params& p, const ChunkPlan& cp, uint8_
         pl.off_qt = cp.off_qt; pl.off_kt = cp.off_kt; pl.off_A = cp.off_A; pl.off_gam = cp.off_gam;
         return launch_prep(fp, pl, w, status, s, false);
     }
+    case CS_SEG_FWD:
+    case CS_SEG_REV: {
+        // each segment's state (or dL/dS contribution) from a zero start
+        SegStateJob j;
+        const bool fwd = k == CS_SEG_FWD;
+        j.kt = fwd ? kt : qt; j.kt_rows = kt_rows; j.v = fwd ? p.v : p.grad_O; j.gam = gam;
+        j.S_out = reinterpret_cast<float*>(w + cp.off_segS);
+        j.reverse = !fwd;
+        j.BH = BH; j.T = p.T; j.dk = p.dk; j.dv = p.dv; j.nch = cp.nch; j.cps = cp.cps; j.nseg = cp.nseg;
+        return launch_seg_state_job(j, status, s);
+    }
+    case CS_SCAN_FWD:
+    case CS_SCAN_REV: {
+        // the state entering each segment (from S0), or the dL/dS leaving it (from dST)
+        SegScanJob j;
+        const bool fwd = k == CS_SCAN_FWD;
+        j.S_start = fwd ? p.S0 : p.grad_ST;
+        j.S_end = nullptr;
+        j.gam = gam;
+        j.segS = reinterpret_cast<const float*>(w + cp.off_segS);
+        j.segin = reinterpret_cast<float*>(w + cp.off_segin);
+        j.reverse = !fwd;
+        j.BH = BH; j.dk = p.dk; j.dv = p.dv; j.nch = cp.nch; j.cps = cp.cps; j.nseg = cp.nseg;
+        return launch_seg_scan_job(j, s);
+    }
     case CS_SWEEP_FWD:
     case CS_SWEEP_REV: {
         StateSweep sw;
         const bool fwd = k == CS_SWEEP_FWD;
         sw.kt = fwd ? kt : qt; sw.kt_rows = kt_rows; sw.v = fwd ? p.v : p.grad_O; sw.gam = gam;
-        sw.S_in = fwd ? p.S0 : p.grad_ST;
+        sw.S_in = cp.nseg > 1 ? reinterpret_cast<const float*>(w + cp.off_segin) : (fwd ? p.S0 : p.grad_ST);
         sw.S_out = fwd ? ST : p.grad_S0;
         sw.Hst = w + (fwd ? cp.off_H : cp.off_D);
         sw.reverse = !fwd;
         sw.BH = BH; sw.T = p.T; sw.dk = p.dk; sw.dv = p.dv; sw.nch = cp.nch;
+        sw.nseg = cp.nseg; sw.cps = cp.cps;
         return launch_state_sweep(sw, status, s);
     }
     case CS_BOUNDARY:
@@ -1431,7 +1519,7 @@ cudaError_t run_chunk_stage(const gla_bwd_params& p, const ChunkPlan& cp, uint8_
             const int grid = (int)((rows * 32 + NT - 1) / NT < 4096 ? (rows * 32 + NT - 1) / NT : 4096);
             gla_bwd_token_gate_kernel<<<grid, NT, 0, s>>>(a);
         } else {
-            gla_bwd_head_gate_kernel<<<p.H, NT, 0, s>>>(a);
+            return launch_head_gate(a, reinterpret_cast<float*>(w + cp.off_hpart), s);
         }
         return cudaGetLastError();
     }
@@ -1485,7 +1573,7 @@ cudaError_t launch_all(const BwdArgs& a, const gla_bwd_params& p, cudaStream_t s
         gla_bwd_revsum_kernel<<<dim3(BH, (p.dv + 31) / 32), NT, 0, s>>>(a, a.dlbe, a.glb, p.dv);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    return launch_gate_tail(a, p, s);
+    return launch_gate_tail(a, p, a.hpart, s);
 }
 
 }  // namespace
@@ -1533,6 +1621,7 @@ extern "C" gla_status gla_bwd(const gla_bwd_params* p, cudaStream_t stream)
     a.log_b = p->log_b;
     a.glb = p->grad_log_b;
     a.dlbe = p->gate == GLA_GATE_BILINEAR ? reinterpret_cast<float*>(w + pl.off_dlbe) : nullptr;
+    a.hpart = p->gate == GLA_GATE_HEAD_SCALAR ? reinterpret_cast<float*>(w + pl.off_hpart) : nullptr;
     a.nch = pl.nch; a.ndvt = pl.ndvt;
     const bool use_tc = kind == BWD_SPLIT;
     a.nplanes = pl.ndvt + (use_tc ? 1 : 0);

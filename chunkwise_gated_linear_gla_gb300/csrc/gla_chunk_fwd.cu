@@ -525,8 +525,11 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             const bool ok = mbar_wait(s_done, (nloc - 1) & 1, kTimeoutNs);
             if (group_all_ok(ok, BAR_EPI, NEPI)) {
                 tc_fence_after();
-                // (with per-segment start states, only the last segment's end state is kept)
-                if (a.S_out && (a.mode != kModeSegOut || seg == (int)gridDim.z - 1)) {
+                // (with per-segment start states, only the end state of the segment that ends
+                // the walk is kept: the last one, or the first for the reverse sweep)
+                const bool keep = a.mode == kModeSegState || a.mode == kModeFull ||
+                                  (a.mode == kModeSweepRev ? seg == 0 : seg == (int)gridDim.z - 1);
+                if (a.S_out && keep) {
                     float* so = a.S_out + bh * a.s_out_bh + seg * a.s_out_seg + dv0 + d;
 #pragma unroll 1
                     for (int b = 0; b < NB; ++b) {
@@ -810,13 +813,15 @@ cudaError_t launch_state_sweep(const StateSweep& w, int* status, cudaStream_t s)
     CUtensorMap mk, mv;
     if (!map3(&mk, w.kt, w.dk, (uint64_t)w.kt_rows, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     if (!map3(&mv, w.v, w.dv, w.T, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (w.nseg < 1 || (w.nseg > 1 && (w.cps <= 0 || (long long)w.cps * (w.nseg - 1) >= w.nch)))
+        return cudaErrorInvalidValue;
     FwdArgs a;
     const long long st = (long long)w.dk * w.dv;
-    a.S_in = w.S_in; a.s_in_bh = st; a.s_in_seg = 0;
+    a.S_in = w.S_in; a.s_in_bh = w.nseg > 1 ? st * w.nseg : st; a.s_in_seg = w.nseg > 1 ? st : 0;
     a.S_out = w.S_out; a.s_out_bh = st; a.s_out_seg = 0;
     a.gam = w.gam;
     a.status = status;
-    a.dv = w.dv; a.nchunks = w.nch; a.cps = w.nch;
+    a.dv = w.dv; a.nchunks = w.nch; a.cps = w.nseg > 1 ? w.cps : w.nch;
     a.mode = w.reverse ? kModeSweepRev : kModeSweep;
     a.gated = w.gam != nullptr;
     a.lbc = nullptr;
@@ -825,7 +830,7 @@ cudaError_t launch_state_sweep(const StateSweep& w, int* status, cudaStream_t s)
     a.T = w.T;
     a.H = 1;
     a.Hst = static_cast<__nv_bfloat16*>(w.Hst);
-    const dim3 grid(w.dv / DVT, (unsigned)BH, 1);
+    const dim3 grid(w.dv / DVT, (unsigned)BH, (unsigned)w.nseg);
     // the states leave through the O map's slot: [BH * nch * dv rows][dk] bf16, boxes of 64 keys
     // x 128 rows (128-byte swizzle); no Q, score or O tile is read in a sweep, the K map stands
     // in for those arguments

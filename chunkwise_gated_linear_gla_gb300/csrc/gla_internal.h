@@ -143,8 +143,37 @@ struct StateSweep {
     void* Hst;
     bool reverse;
     int BH, T, dk, dv, nch;
+    // sequence split (nseg > 1): segment s covers chunks [s cps, (s + 1) cps) and starts from
+    // S_in + (bh nseg + s) dk dv; S_out is written by the last segment (the first, reverse)
+    int nseg = 1, cps = 0;
 };
 cudaError_t launch_state_sweep(const StateSweep& w, int* status, cudaStream_t s);
+
+// The sequence split for the backward's sweeps. launch_seg_state_job (gla_state.cu): each
+// segment's state from a zero start, S*_s = sum over its chunks n of (KT_n (.) d_n)^T V_n, d_n
+// the product of the segment's gates after chunk n (before it when `reverse`), to S_out
+// [BH][nseg][dk][dv]. launch_seg_scan_job (gla_scan.cu): segin[s] = the state entering segment
+// s from S_start (the recurrence over segments, from the last when `reverse`), S_end the
+// state after all of them (either may be null).
+struct SegStateJob {
+    const void* kt; long long kt_rows;
+    const void* v;
+    const float* gam;
+    float* S_out;
+    bool reverse;
+    int BH, T, dk, dv, nch, cps, nseg;
+};
+cudaError_t launch_seg_state_job(const SegStateJob& j, int* status, cudaStream_t s);
+struct SegScanJob {
+    const float* S_start;
+    float* S_end;
+    const float* gam;
+    const float* segS;
+    float* segin;
+    bool reverse;
+    int BH, dk, dv, nch, cps, nseg;
+};
+cudaError_t launch_seg_scan_job(const SegScanJob& j, cudaStream_t s);
 
 // The chunk-parallel gradients of the backward (gla_bwd_chunk.cu): dq, dk, dv and the gate
 // terms q (.) dq - k (.) dk per token, from the prep's Kt, Qt ([BH][kt_rows][dk] bf16), A and

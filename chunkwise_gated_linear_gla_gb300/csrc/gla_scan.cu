@@ -30,6 +30,7 @@ struct ScanArgs {
     const float* segS;   // [BH][nseg][dk][dv]
     float* segin;        // [BH][nseg][dk][dv]
     int dk, dv, nchunks, nseg, cps;
+    int rev;             // from the last segment to the first (the backward's dL/dS)
 };
 
 __global__ void __launch_bounds__(NT) gla_state_scan_kernel(ScanArgs a)
@@ -64,17 +65,19 @@ __global__ void __launch_bounds__(NT) gla_state_scan_kernel(ScanArgs a)
     float* ip = a.segin + (size_t)bh * a.nseg * st + e;
     float S = a.S0 ? a.S0[(size_t)bh * st + e] : 0.f;
     float buf[AHEAD];
+    // step i visits segment seg(i): i in the forward order, nseg - 1 - i in the reverse one
+    auto seg = [&](int i) { return a.rev ? a.nseg - 1 - i : i; };
 #pragma unroll
-    for (int i = 0; i < AHEAD; ++i) buf[i] = (i < a.nseg) ? sp[(size_t)i * st] : 0.f;
+    for (int i = 0; i < AHEAD; ++i) buf[i] = (i < a.nseg) ? sp[(size_t)seg(i) * st] : 0.f;
     for (int s = 0; s < a.nseg; s += AHEAD) {
 #pragma unroll
         for (int i = 0; i < AHEAD; ++i) {
             const int ss = s + i;
             if (ss < a.nseg) {
                 const float cur = buf[i];
-                if (ss + AHEAD < a.nseg) buf[i] = sp[(size_t)(ss + AHEAD) * st];
-                ip[(size_t)ss * st] = S;
-                S = fmaf(Gs[r * a.nseg + ss], S, cur);
+                if (ss + AHEAD < a.nseg) buf[i] = sp[(size_t)seg(ss + AHEAD) * st];
+                ip[(size_t)seg(ss) * st] = S;
+                S = fmaf(Gs[r * a.nseg + seg(ss)], S, cur);
             }
         }
     }
@@ -94,11 +97,30 @@ cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, i
     a.segS = reinterpret_cast<const float*>(base + pl.off_segS);
     a.segin = reinterpret_cast<float*>(base + pl.off_segin);
     a.dk = p.dk; a.dv = p.dv; a.nchunks = pl.nchunks; a.nseg = pl.nseg; a.cps = pl.chunks_per_seg;
+    a.rev = 0;
     const size_t st = (size_t)p.dk * p.dv;
     dim3 grid((unsigned)((st + NT - 1) / NT), p.B * p.H);
     // rows one CTA touches: NT elements span at most NT / dv + 2 rows
     const int max_rows = NT / p.dv + 2;
     const size_t smem = (size_t)max_rows * pl.nseg * sizeof(float);
+    gla_state_scan_kernel<<<grid, NT, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_seg_scan_job(const SegScanJob& j, cudaStream_t s)
+{
+    ScanArgs a;
+    a.S0 = j.S_start;
+    a.ST = j.S_end;
+    a.gam = j.gam;
+    a.segS = j.segS;
+    a.segin = j.segin;
+    a.dk = j.dk; a.dv = j.dv; a.nchunks = j.nch; a.nseg = j.nseg; a.cps = j.cps;
+    a.rev = j.reverse ? 1 : 0;
+    const size_t st = (size_t)j.dk * j.dv;
+    dim3 grid((unsigned)((st + NT - 1) / NT), (unsigned)j.BH);
+    const int max_rows = NT / j.dv + 2;
+    const size_t smem = (size_t)max_rows * j.nseg * sizeof(float);
     gla_state_scan_kernel<<<grid, NT, smem, s>>>(a);
     return cudaGetLastError();
 }

@@ -46,6 +46,7 @@ struct StateArgs {
     int* status;
     int dv, nchunks, cps, gated;
     int win;            // > 0: segment s covers the win chunks before chunk s * cps (sliding window)
+    int rev;            // walk from the segment's first chunk (the decay runs over the earlier chunks)
 };
 
 template <int DK>
@@ -131,7 +132,7 @@ gla_chunk_state_kernel(StateArgs a, const __grid_constant__ CUtensorMap tmK, con
             int issued = 0;
             for (int j = 0; j < nloc; ++j) {
                 if (*abort_flag) break;
-                const int st = j % NS, c = c_end - 1 - j;
+                const int st = j % NS, c = a.rev ? c_begin + j : c_end - 1 - j;
                 if (j >= NS && !mbar_wait(&empty[st], ((j / NS) - 1) & 1, kTimeoutNs)) {
                     fail(a.status, abort_flag, ERR_PRODUCER);
                     break;
@@ -143,8 +144,8 @@ gla_chunk_state_kernel(StateArgs a, const __grid_constant__ CUtensorMap tmK, con
                 for (int i = 0; i < DK / 64; ++i) tma_load_3d(sb + L::K_OFF + i * 8192, &tmK, &full[st], i * 64, c * C, bh);
                 tma_load_3d(sb + L::V_OFF, &tmV, &full[st], dv0, c * C, bh);
                 tma_load_3d(sb + L::V_OFF + 8192, &tmV, &full[st], dv0 + 64, c * C, bh);
-                const int cp = c - NS;   // NS chunks ahead in this order
-                if (cp >= c_begin) {
+                const int cp = a.rev ? c + NS : c - NS;   // NS chunks ahead in this order
+                if (a.rev ? cp < c_end : cp >= c_begin) {
                     prefetch_l2_tile_3d(&tmV, dv0, cp * C, bh);
                     prefetch_l2_tile_3d(&tmV, dv0 + 64, cp * C, bh);
                     const int nt = gridDim.x, me = blockIdx.x;
@@ -315,6 +316,7 @@ cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, 
     a.dv = p.dv; a.nchunks = pl.nchunks; a.cps = pl.chunks_per_seg;
     a.gated = p.gate != GLA_GATE_NONE;
     a.win = 0;
+    a.rev = 0;
     dim3 grid(pl.n_dvt, (unsigned)BH, pl.nseg);
     switch (p.dk) {
     case 64: return launch_state_dk<64>(a, grid, mk, mv, s);
@@ -350,8 +352,36 @@ cudaError_t launch_seg_window(const gla_fwd_params& p, const Plan& pl, void* ws,
     a.dv = p.dv; a.nchunks = pl.nchunks; a.cps = pl.chunks_per_seg;
     a.gated = p.gate != GLA_GATE_NONE;
     a.win = pl.window;
+    a.rev = 0;
     dim3 grid(pl.n_dvt, (unsigned)BH, pl.nseg);
     switch (p.dk) {
+    case 64: return launch_state_dk<64>(a, grid, mk, mv, s);
+    case 128: return launch_state_dk<128>(a, grid, mk, mv, s);
+    case 256: return launch_state_dk<256>(a, grid, mk, mv, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_seg_state_job(const SegStateJob& j, int* status, cudaStream_t s)
+{
+    if (j.dv % DVT != 0 || j.nseg < 1) return cudaErrorInvalidValue;
+    const uint64_t BH = (uint64_t)j.BH;
+    CUtensorMap mk, mv;
+    if (!map_tiles(&mk, j.kt, j.dk, (uint64_t)j.kt_rows, BH)) return cudaErrorInvalidValue;
+    if (!map_tiles(&mv, j.v, j.dv, j.T, BH)) return cudaErrorInvalidValue;
+    StateArgs a;
+    const long long st = (long long)j.dk * j.dv;
+    a.gam = j.gam;
+    a.S_out = j.S_out;
+    a.s_out_bh = st * j.nseg;
+    a.s_out_seg = st;
+    a.status = status;
+    a.dv = j.dv; a.nchunks = j.nch; a.cps = j.cps;
+    a.gated = j.gam != nullptr;
+    a.win = 0;
+    a.rev = j.reverse ? 1 : 0;
+    dim3 grid(j.dv / DVT, (unsigned)BH, j.nseg);
+    switch (j.dk) {
     case 64: return launch_state_dk<64>(a, grid, mk, mv, s);
     case 128: return launch_state_dk<128>(a, grid, mk, mv, s);
     case 256: return launch_state_dk<256>(a, grid, mk, mv, s);

@@ -251,6 +251,35 @@ def test_bwd_chunk_form_extreme_gates(dist):
     print(dist, [(n, f"{rf:.1e}", f"{ma:.1e}") for n, rf, ma in rep])
 
 
+def _stage_names(w, dst=True):
+    """The backward's stages for workload w's shapes (host-side planning only)."""
+    x, dO, dST = _inputs(w, 0, dst)
+    c = lambda t: None if t is None else t.cuda()
+    dev = torch.device("cuda")
+    f32 = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)
+    p = bnd.make_bwd_params(c(x["q"]), c(x["k"]), c(x["v"]), c(x["log_g"]), c(x["S0"]), c(dO), c(dST),
+                            f32(w.B, w.H, w.T, w.dk), f32(w.B, w.H, w.T, w.dk), f32(w.B, w.H, w.T, w.dv),
+                            None if x["log_g"] is None else f32(*x["log_g"].shape), f32(w.B, w.H, w.dk, w.dv),
+                            gate=x["gate"])
+    return [bnd.gla_bwd_stage_name(p, i) for i in range(bnd.gla_bwd_num_stages(p))]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("gate", GATES)
+@pytest.mark.parametrize("T,dk,dv", [(1100, 128, 128), (2000, 128, 128), (2100, 256, 256)])
+def test_bwd_chunk_form_sequence_split(gate, T, dk, dv):
+    """Few heads and a long sequence: both sweeps run split into segments (each segment's
+    zero-start state, the scan over segments, forward for the states and backward for
+    dL/dS), with S0 and dST given."""
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=1, H=2, T=T, dk=dk, dv=dv, dtype=torch.bfloat16, gate=gate, s0_std=0.3)
+    names = _stage_names(w)
+    assert "gla_chunk_dstate" in names and "gla_dstate_scan" in names, names
+    rep = []
+    _check(w, seed=T + gate, report=rep)
+    print("split", gate, T, dk, [(n, f"{rf:.1e}", f"{ma:.1e}") for n, rf, ma in rep])
+
+
 @pytest.mark.gpu
 def test_bwd_chunk_form_many_items_per_cta():
     """More (b, h, chunk) items than multiprocessors, so each CTA of the persistent gradient
