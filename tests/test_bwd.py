@@ -281,6 +281,72 @@ def test_bwd_chunk_form_sequence_split(gate, T, dk, dv):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("gate", [gi.GATE_PER_KEY, gi.GATE_HEAD_SCALAR])
+def test_bwd_chunk_form_optional_outputs(gate):
+    """The chunk form without dL/dS0 and without the gate gradient (no boundary term, no
+    gate tail): dq, dk and dv are unchanged, and nothing is written where no output was
+    asked for."""
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=2, H=2, T=150, dk=128, dv=128, dtype=torch.bfloat16, gate=gate, s0_std=0.2)
+    x, dO, dST = _inputs(w, 19)
+    ref = oracle.gla_backward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], dO, dST)
+    c = lambda t: None if t is None else t.cuda()
+    dev = torch.device("cuda")
+    f32 = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)
+    dq, dk, dv = f32(2, 2, 150, 128), f32(2, 2, 150, 128), f32(2, 2, 150, 128)
+    p = bnd.make_bwd_params(c(x["q"]), c(x["k"]), c(x["v"]), c(x["log_g"]), c(x["S0"]), c(dO), c(dST), dq, dk, dv,
+                            None, None, gate=x["gate"])
+    assert [bnd.gla_bwd_stage_name(p, i) for i in range(bnd.gla_bwd_num_stages(p))] == [
+        "gla_chunk_prep", "gla_bwd_state_sweep", "gla_bwd_dstate_sweep", "gla_bwd_grads"]
+    n = bnd.gla_bwd_workspace_size(p)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), n
+    bnd.gla_bwd(p)
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    for name, a, r in zip(["dq", "dk", "dv"], [dq, dk, dv], ref[:3]):
+        rf, ma = errors(to_np(a), r)
+        assert rf <= CH_REL_FRO and ma <= CH_MAX_ABS, (name, rf, ma)
+
+
+@pytest.mark.gpu
+def test_bwd_misaligned_inputs_take_the_split_form():
+    """q two bytes past a 16-byte boundary: AUTO takes the 16-row split form (the chunk form's
+    tensor-memory-access copies need 16-byte bases), GLA_PATH_TENSOR is refused, and the
+    split form's bar holds."""
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=1, H=2, T=130, dk=128, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY, s0_std=0.1)
+    x, dO, dST = _inputs(w, 20)
+    buf = torch.empty(x["q"].numel() + 8, dtype=torch.bfloat16, device="cuda")
+    qs = buf[1:1 + x["q"].numel()].view(x["q"].shape)
+    qs.copy_(x["q"].cuda())
+    assert qs.data_ptr() % 16 == 2
+    c = lambda t: None if t is None else t.cuda()
+    dev = torch.device("cuda")
+    f32 = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)
+    outs = [f32(1, 2, 130, 128), f32(1, 2, 130, 128), f32(1, 2, 130, 128), f32(1, 2, 130, 128), f32(1, 2, 128, 128)]
+    p = bnd.make_bwd_params(qs, c(x["k"]), c(x["v"]), c(x["log_g"]), c(x["S0"]), c(dO), c(dST), *outs,
+                            gate=x["gate"])
+    assert bnd.gla_bwd_num_stages(p) == 1 and bnd.gla_bwd_stage_name(p, 0) == "gla_bwd_split"
+    pt = bnd.make_bwd_params(qs, c(x["k"]), c(x["v"]), c(x["log_g"]), c(x["S0"]), c(dO), c(dST), *outs,
+                             gate=x["gate"], path=TENSOR)
+    assert bnd.gla_bwd(pt, check=False) == bnd.GLA_ERR_UNSUPPORTED
+    n = bnd.gla_bwd_workspace_size(p)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), n
+    bnd.gla_bwd(p)
+    torch.cuda.synchronize()
+    assert gla.gla_device_status() == 0
+    ref = oracle.gla_backward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"], dO, dST)
+    for name, a, r in zip(["dq", "dk", "dv", "dlog_g", "dS0"], outs, ref):
+        rf, ma = errors(to_np(a), r)
+        if name == "dlog_g":
+            assert rf <= TC_GATE_REL_FRO and ma <= TC_GATE_MAX_ABS, (name, rf, ma)
+        else:
+            assert rf <= TC_REL_FRO and ma <= TC_MAX_ABS, (name, rf, ma)
+
+
+@pytest.mark.gpu
 def test_bwd_chunk_form_many_items_per_cta():
     """More (b, h, chunk) items than multiprocessors, so each CTA of the persistent gradient
     kernel takes several chunks, with no S0 and no dST."""
