@@ -71,6 +71,14 @@ constexpr uint32_t TQ = 0;      // dq^T, 64 columns per key half
 constexpr uint32_t TK = 128;    // dk^T
 constexpr uint32_t TV = 256;    // dv^T, two buffers of 64
 constexpr uint32_t TA = 384;    // dA (lanes 0-63)
+constexpr uint32_t TG = 448;    // the drain's Kg columns, 32 per key half (bf16 pairs)
+
+// 8 columns of this warp's 32 lanes from tensor memory (32x32b.x8)
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
 
 struct GradArgs {
     const __nv_bfloat16* q;   // raw q, k for the gate term q (.) dq - k (.) dk
@@ -187,9 +195,10 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
     uint64_t* dq_empty = bar + 20;      // dq^T read out (NKH * 128 arrivals)
     uint64_t* mma_fin = bar + 21;
     uint64_t* kt_free = bar + 22;       // the chunk's last product reading Kt done
-    uint64_t* p3_done = bar + 23;       // the drain done with the Kg and Qg tiles (NKH * 128 arrivals)
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 24);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 25);
+    uint64_t* p3_done = bar + 23;       // the drain done with the Qg tile (NKH * 128 arrivals)
+    uint64_t* kg_read = bar + 24;       // the drain has its Kg columns in registers (NKH * 128 arrivals)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 25);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 26);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int items = a.BH * a.nch;
@@ -205,6 +214,7 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
         mbar_init(da_full, 1); mbar_init(dat_ready, NEPI);
         mbar_init(dqdk_full, 1); mbar_init(dk_empty, NKH * 128); mbar_init(dq_empty, NKH * 128);
         mbar_init(mma_fin, 1); mbar_init(kt_free, 1); mbar_init(p3_done, NKH * 128);
+        mbar_init(kg_read, NKH * 128);
         *abort_flag = 0;
         mbar_fence_init();
         prefetch_tmap(&tmK); prefetch_tmap(&tmQ); prefetch_tmap(&tmA); prefetch_tmap(&tmO);
@@ -259,7 +269,7 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                         // Kt, A and gamma, once the previous chunk's last products are done with
                         // them (the first block's tiles are already on their way)
                         if (i >= 1 && (!mbar_wait(res_empty, (i - 1) & 1, kTimeoutNs) ||
-                                       !mbar_wait(p3_done, (i - 1) & 1, kTimeoutNs))) { ok = false; break; }
+                                       !mbar_wait(kg_read, (i - 1) & 1, kTimeoutNs))) { ok = false; break; }
                         mbar_arrive_expect_tx(res_full, L::KTB + 8192 + (gated ? DK * 4 : 0));
 #pragma unroll
                         for (int j = 0; j < DK / 64; ++j)
@@ -506,7 +516,7 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
             // tiles stay until the drain is done with them)
             if (!group_all_ok(ok, BAR_EPI, NEPI)) break;
             const uint8_t* qcol = sm + L::UNIT_OFF + usq * 32768 + (key >> 6) * 8192 + (key & 7) * 2;
-            const uint8_t* kcol = sm + L::KT_OFF + (key >> 6) * 8192 + (key & 7) * 2;
+            const uint8_t* kcol = sm + L::KT_OFF + (key >> 6) * 8192 + (key & 7) * 2;   // read once, below
             mbar_arrive(dat_ready);
             // phase 3: dq and dk of key `key` (warpgroup e = key half e), rows from the last,
             // with the gate terms summed over the later rows of the chunk
@@ -529,12 +539,28 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                     // gamma (Qg (.) Xq - Kg (.) Xk) (q Lambda = Qt = gamma Qg, k Gamma = Kt =
                     // gamma Kg), summed over the later rows of the chunk
                     const int cc = (key & 63) >> 3;
+                    // this key's Kg column into the spare tensor-memory columns (bf16 pairs, this
+                    // thread's lane), so that the next chunk's Kt can land in the tile while the
+                    // drain runs
+                    {
+                        uint32_t kg2[C / 2];
+#pragma unroll
+                        for (int t = 0; t < C; t += 2) {
+                            const uint32_t lo = *reinterpret_cast<const uint16_t*>(kcol + swz_off(t, cc));
+                            const uint32_t hi = *reinterpret_cast<const uint16_t*>(kcol + swz_off(t + 1, cc));
+                            kg2[t / 2] = lo | (hi << 16);
+                        }
+                        tmem_st32(tmem + lb + TG + 32 * e, kg2);
+                        tmem_wait_st();
+                    }
+                    mbar_arrive(kg_read);
                     float rsum = 0.f;
 #pragma unroll
                     for (int qd = C / 16 - 1; qd >= 0; --qd) {
-                        uint32_t xq[16], xk[16];
+                        uint32_t xq[16], xk[16], kq[8];
                         tmem_ld16(tmem + lb + TQ + e * 64 + 16 * qd, xq);
                         tmem_ld16(tmem + lb + TK + e * 64 + 16 * qd, xk);
+                        tmem_ld8(tmem + lb + TG + 32 * e + 8 * qd, kq);
                         tmem_wait_ld();
                         if (qd == 0) {
                             tc_fence_before();
@@ -550,7 +576,8 @@ gla_bwd_grads_kernel(GradArgs a, const __grid_constant__ CUtensorMap tmK, const 
                                 ok_[(size_t)r * DK] = exp2f(tot - Bc[r]) * Xk;   // Gamma_r Xk
                                 if (oR) {
                                     const float qg = bf16_at(qcol + swz_off(r, cc));
-                                    const float kg = bf16_at(kcol + swz_off(r, cc));
+                                    const uint32_t kp = kq[j >> 1];
+                                    const float kg = __uint_as_float(j & 1 ? kp & 0xffff0000u : kp << 16);
                                     rsum += gk * (qg * Xq - kg * Xk);
                                     if (c * C + r == a.T - 1) rsum += bnd;
                                     oR[(size_t)r * DK] = rsum;
