@@ -346,6 +346,27 @@ def test_bwd_misaligned_inputs_take_the_split_form():
             assert rf <= TC_REL_FRO and ma <= TC_MAX_ABS, (name, rf, ma)
 
 
+FUZZ = [(int(b), int(h), int(t), int(dk), int(dv), int(g), int(seed))
+        for b, h, t, dk, dv, g, seed in zip(
+            np.random.default_rng(7).integers(1, 4, 10), np.random.default_rng(8).integers(1, 4, 10),
+            np.random.default_rng(9).integers(1, 700, 10), np.random.default_rng(10).choice([128, 256], 10),
+            np.random.default_rng(11).choice([128, 256, 384], 10), np.random.default_rng(12).choice(GATES, 10),
+            range(10))]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,H,T,dk,dv,gate,seed", FUZZ, ids=[f"{f[0]}x{f[1]}x{f[2]}-{f[3]}-{f[4]}-g{f[5]}" for f in FUZZ])
+def test_bwd_chunk_form_seeded_shapes(B, H, T, dk, dv, gate, seed):
+    """Seeded shapes across the chunk form's range (one to three batch rows and heads, T up to
+    700 with ragged tails, dk in {128, 256}, dv in {128, 256, 384}, every gate), with S0 and
+    dST present or absent by seed."""
+    gbuild.build(); oracle.build()
+    w = gi.Workload("t", B=B, H=H, T=T, dk=dk, dv=dv, dtype=torch.bfloat16, gate=gate,
+                    s0_std=0.2 if seed % 2 else 0.0)
+    assert _kind(w, AUTO) == "chunk"
+    _check(w, seed=100 + seed, dst=seed % 3 != 0)
+
+
 @pytest.mark.gpu
 def test_bwd_chunk_form_many_items_per_cta():
     """More (b, h, chunk) items than multiprocessors, so each CTA of the persistent gradient
