@@ -15,3 +15,4 @@ from .binding import (  # noqa: F401
     gla_segment_pair_workspace_size, gla_status_string, gla_version, make_params, pair_combine, pair_scan,
     segment_pair,
 )
+from .autograd import gla_attention  # noqa: F401,E402
