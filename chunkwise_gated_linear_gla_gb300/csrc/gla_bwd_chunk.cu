@@ -19,8 +19,10 @@
 // key, and each gradient shares one accumulator between its inter and intra
 // terms.) H and D come from the two state sweeps of the chunk pass (bf16,
 // [BH][nch][dv][dk]). The gate gradient's per-token term q (.) dq - k (.) dk
-// (plus rowsum(dL/dS_T (.) S_T) at the last token) goes to `dla` for the
-// reverse cumulative sum.
+// = gamma (Qg (.) Xq - Kg (.) Xk) (Xq, Xk the two accumulators; plus
+// rowsum(dL/dS_T (.) S_T) at the last token) is summed over the chunk's later
+// rows into R, with each chunk's total in ctot; the gate tail then adds the
+// later chunks' totals.
 //
 // Every product is a tcgen05 MMA with M = 128 and N = 64 (the chunk's rows),
 // the accumulators in tensor memory:
@@ -38,10 +40,16 @@
 // space, exp(Bc_t - Bc_s) with t >= s (the paper's full-precision rule).
 //
 // Warp roles: 0 TMA producer, 1 MMA issuer (and tensor-memory owner), 4-11
-// the epilogue (two warpgroups: dv drains, the dA readout and the Kg / Qg
-// rescale, then dq and dk per key half). Persistent: CTA i takes items
-// i, i + grid, ... Every wait is bounded; on a timeout the CTA records an
-// error code and winds down.
+// the epilogue, two warpgroups, per chunk in three phases:
+//   1. the dv drains (each warpgroup one of the two dv^T buffers);
+//   2. 1 / gamma per key, Kt -> Kg as soon as the last dv product has read Kt,
+//      dA -> shared memory (bf16, masked), Qt -> Qg;
+//   3. the drain, one key per thread (warpgroup e = key half e). It parks its
+//      Kg column in the spare tensor-memory columns and signals the producer,
+//      which then refills Kt, A and gamma for the next chunk, and reads Qg from
+//      the Qt tile, held until the drain is done.
+// Persistent: CTA i takes items i, i + grid, ... Every wait is bounded; on a
+// timeout the CTA records an error code and winds down.
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
