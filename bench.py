@@ -99,12 +99,14 @@ def algorithmic(w):
     return flops, byts
 
 
-def stage_bytes(w, name, nseg=1):
+def stage_bytes(w, name, split=None):
     """Compulsory bytes one launch of a stage moves (each operand once, bf16 tiles).
 
     Qt/Kt (Q (.) Lambda, K (.) Gamma) exist only with a gate; without one the
-    chunk pass reads q and k directly. S0/S_T are counted when present.
+    chunk pass reads q and k directly. S0/S_T are counted when present. `split` is
+    planned_split's (nseg, cps, sub, st_nseg, st_cps) of a sequence split.
     """
+    nseg, _, _, st_nseg, st_cps = split or (1, 0, 1, 0, 0)
     BH, T, dk, dv, C = w.B * w.H, w.T, w.dk, w.dv, w.chunk
     nch = (T + C - 1) // C
     Tp = nch * C
@@ -132,21 +134,26 @@ def stage_bytes(w, name, nseg=1):
             return half + BH * (nch * C * C * 2 + T * dv * 4)
         return half + BH * (T * dv * 4 + T * dv * 2)
     if name == "gla_chunk_fwd":
-        last_state = (s0 + st) if nseg == 1 else BH * nseg * dk * dv * 4
+        # split: each segment reads its start state, the last one writes S_T
+        last_state = (s0 + st) if nseg == 1 else BH * nseg * dk * dv * 4 + st
         # bilinear gate: V (.) D' in place of v, plus log beta and the chunks' column decays
         bil_in = T * dv * 4 + nch * dv * 4 if bil else 0
         return BH * (qk_tiles + nch * C * C * 2 + gam + T * dv * 2 * 2 + bil_in) + last_state
     if name == "gla_value_prep":
         return BH * (T * dv * (2 + 4 + 2) + nch * dv * 4)
+    # the split's state pass covers the chunks before the last segment, in st_nseg pieces
+    covered = st_nseg * st_cps
     if name == "gla_chunk_state":
-        return BH * (qk_tiles // 2 + gam + T * dv * 2) + BH * nseg * dk * dv * 4
+        return BH * covered * (C * dk * 2 + C * dv * 2 + (dk * 4 if gated else 0)) + BH * st_nseg * dk * dv * 4
     if name == "gla_state_scan":
-        return 2 * BH * nseg * dk * dv * 4 + s0 + st + BH * nch * dk * 4 * (1 if gated else 0)
+        return BH * (2 * st_nseg + 1) * dk * dv * 4 + s0 + BH * covered * dk * 4 * (1 if gated else 0)
     return 0
 
 
-def planned_segments(w, force, sms):
-    """Segments per (b,h) the library's planner picks (same rule as csrc/gla_api.cu)."""
+def planned_split(w, force, sms, state_ctas_per_sm=1, min_state_chunks=4):
+    """The sequence split the library's planner picks (same rule as csrc/gla_api.cu):
+    (segments per (b,h), chunks per segment, state-pass pieces per segment, state-pass
+    pieces per (b,h), chunks per piece)."""
     nch = (w.T + w.chunk - 1) // w.chunk
     units = w.B * w.H * (w.dv // 128)
     if force > 0:
@@ -156,7 +163,20 @@ def planned_segments(w, force, sms):
     else:
         n = max(1, min(sms // units, nch // 8))
     cps = (nch + n - 1) // n
-    return (nch + cps - 1) // cps
+    n = (nch + cps - 1) // cps
+    if n == 1:
+        return 1, cps, 1, 0, 0
+    sub = 1
+    for f in range(cps // min_state_chunks, 1, -1):
+        if cps % f == 0 and (n - 1) * f * units <= sms * state_ctas_per_sm:
+            sub = f
+            break
+    return n, cps, sub, (n - 1) * sub, cps // sub
+
+
+def planned_segments(w, force, sms):
+    """Segments per (b,h) the library's planner picks."""
+    return planned_split(w, force, sms)[0]
 
 
 def kernel_source_sha(name):
@@ -831,8 +851,9 @@ def main():
     tflops = flops * world / (step_ms * 1e-3) / 1e12
     dom = max(range(nst), key=lambda i: stage_ms[i])
     dname = names[dom]
-    nseg = planned_segments(w, args.segments, torch.cuda.get_device_properties(dev).multi_processor_count) \
-        if "gla_chunk_state" in names else 1
+    split = planned_split(w, args.segments, torch.cuda.get_device_properties(dev).multi_processor_count) \
+        if "gla_chunk_state" in names else None
+    nseg = split[0] if split else 1
     if dname == "gla_fwd_simt":
         # the CUDA-core pass: fp32 FFMA work against the nominal FFMA rate
         alu = flops / (stage_ms[dom] * 1e-3) / 1e12
@@ -846,8 +867,8 @@ def main():
         # whole step otherwise (each kernel's own compulsory bytes are listed separately)
         span_ms = stage_ms[0] if nst == 1 else step_ms
         ach = byts / (span_ms * 1e-3) / 1e9
-        per_kernel = [{"kernel": n, "ms": t, "compulsory_bytes": stage_bytes(w, n, nseg),
-                       "compulsory_gbs": stage_bytes(w, n, nseg) / (t * 1e-3) / 1e9,
+        per_kernel = [{"kernel": n, "ms": t, "compulsory_bytes": stage_bytes(w, n, split),
+                       "compulsory_gbs": stage_bytes(w, n, split) / (t * 1e-3) / 1e9,
                        "dram_bytes_ncu": ncu_traffic(w.name, n)} for n, t in zip(names, stage_ms)]
         tr = [k["dram_bytes_ncu"] for k in per_kernel]
         traffic = sum(tr) if tr and all(t is not None for t in tr) else None
@@ -866,6 +887,7 @@ def main():
                                f"gate={['none', 'per-head scalar', 'per-key', 'per-token scalar', 'bilinear'][w.gate]}, "
                                f"S0={'given' if w.s0_std > 0 else 'zero'}",
                    "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "segments": nseg,
+                   "state_pieces": split[3] if split else 0,
                    "l2": "flushed between steps (256 MB write then 256 MB read, outside the timed events)",
                    "stages": names, "stage_ms": stage_ms, "other_workloads": others, "fused_path": fused},
         "tflops": tflops, "tflops_frac_bf16_peak": tflops / bf16,

@@ -202,6 +202,23 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     pl.chunks_per_seg = (pl.nchunks + pl.nseg - 1) / pl.nseg;
     pl.nseg = (pl.nchunks + pl.chunks_per_seg - 1) / pl.chunks_per_seg;
     pl.window = pl.nseg > 1 ? p->window_chunks : 0;
+    if (pl.nseg > 1 && pl.window == 0) {
+        // The last segment's own chunk pass ends at S_T, so the state pass only covers the
+        // chunks before it. It cuts them into the most pieces that still fit in one wave,
+        // each a whole fraction of a segment and at least kMinStateChunks long.
+        const int cps = pl.chunks_per_seg, slots = (sms > 0 ? sms : 148) * kStateCtasPerSm;
+        pl.sub = 1;
+        for (int f = cps / kMinStateChunks; f > 1; --f)
+            if (cps % f == 0 && (long long)(pl.nseg - 1) * f * units <= slots) {
+                pl.sub = f;
+                break;
+            }
+        pl.st_nseg = (pl.nseg - 1) * pl.sub;
+        pl.st_cps = cps / pl.sub;
+        pl.segin_n = pl.st_nseg + 1;
+    } else if (pl.nseg > 1) {
+        pl.segin_n = pl.nseg;
+    }
 
     const size_t BH = (size_t)p->B * p->H;
     size_t off = 0;
@@ -212,8 +229,8 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     pl.off_A = off;   off = align_up(off + BH * pl.nchunks * kChunk * kChunk * 2, 256);
     pl.off_gam = off; off = align_up(off + BH * pl.nchunks * p->dk * 4, 256);
     if (pl.nseg > 1) {
-        pl.off_segS = off;  off = align_up(off + BH * pl.nseg * p->dk * p->dv * 4, 256);
-        pl.off_segin = off; off = align_up(off + BH * pl.nseg * p->dk * p->dv * 4, 256);
+        pl.off_segS = off;  off = align_up(off + BH * pl.st_nseg * p->dk * p->dv * 4, 256);
+        pl.off_segin = off; off = align_up(off + BH * pl.segin_n * p->dk * p->dv * 4, 256);
     }
     if (halves) {
         pl.off_opart = off; off = align_up(off + BH * p->T * p->dv * 4, 256);

@@ -752,9 +752,11 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     } else if (mode == kModeSegState) {
         a.S_out = reinterpret_cast<float*>(base + pl.off_segS); a.s_out_bh = st * pl.nseg; a.s_out_seg = st;
     } else {
-        a.S_in = reinterpret_cast<const float*>(base + pl.off_segin); a.s_in_bh = st * pl.nseg; a.s_in_seg = st;
-        // the sliding-window split has no scan to give S_T: the last segment's pass writes it
-        if (pl.window > 0 && p.ST) { a.S_out = p.ST; a.s_out_bh = st; a.s_out_seg = 0; }
+        // segment s starts from the workspace's start state s * sub (sub state-pass pieces per
+        // segment; one per segment with the sliding window); the last segment's pass ends at S_T
+        a.S_in = reinterpret_cast<const float*>(base + pl.off_segin);
+        a.s_in_bh = st * pl.segin_n; a.s_in_seg = st * pl.sub;
+        if (p.ST) { a.S_out = p.ST; a.s_out_bh = st; a.s_out_seg = 0; }
     }
     a.gam = reinterpret_cast<const float*>(base + pl.off_gam);
     a.status = status;

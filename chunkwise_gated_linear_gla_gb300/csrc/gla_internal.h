@@ -15,6 +15,8 @@ constexpr int kSimtChunk = 16;    // chunk length of the CUDA-core path
 constexpr int kDvTile = 128;      // dv columns per CTA on the tensor-core path
 constexpr int kSimtDvTile = 64;   // dv columns per CTA on the CUDA-core path
 constexpr int kMaxDk = 256;       // widest keys of the tensor-core path and of the 16-row CUDA-core form
+constexpr int kStateCtasPerSm = 1;  // resident CTAs per SM of the state pass (gla_chunk_state)
+constexpr int kMinStateChunks = 4;  // shortest piece the planner gives the state pass
 // CUDA-core forward for dk > kMaxDk: 8-row chunks and 32 columns per CTA keep
 // the fp32 state tile (dk x 32) and five [8 x dk] row buffers within the
 // 227 KB of shared memory a CTA may hold, up to dk = kSimtMaxDk.
@@ -57,6 +59,11 @@ struct Plan {
     int nseg = 1;          // sequence segments per (b,h)
     int chunks_per_seg = 0;
     int window = 0;        // sliding-window split: chunks of the window (0: exact split)
+    // exact split: the state pass covers the chunks before the last segment in st_nseg
+    // pieces of st_cps chunks, sub of them per segment (finer than the segments, so that
+    // it fills the SMs), and the workspace keeps segin_n start states per (b,h): one per
+    // piece and the state after the last (the sliding window keeps one per segment)
+    int sub = 1, st_nseg = 0, st_cps = 0, segin_n = 0;
     bool raw_qk = false;   // tensor path reads q,k directly (no gate)
     int sms = 0;           // multiprocessors of the device the plan was made for
     // workspace layout (byte offsets from the workspace base)

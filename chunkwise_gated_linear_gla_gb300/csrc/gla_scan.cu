@@ -28,7 +28,9 @@ struct ScanArgs {
     float* ST;           // [BH][dk][dv] or null
     const float* gam;    // [BH][nchunks][dk] or null (no gate)
     const float* segS;   // [BH][nseg][dk][dv]
-    float* segin;        // [BH][nseg][dk][dv]
+    float* segin;        // segment s of (b,h) at segin + bh in_bh + s dk dv
+    long long in_bh;
+    long long st_bh;     // ST of (b,h) at ST + bh st_bh
     int dk, dv, nchunks, nseg, cps;
     int rev;             // from the last segment to the first (the backward's dL/dS)
 };
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(NT) gla_state_scan_kernel(ScanArgs a)
     if (e >= st) return;
     const int r = (int)(e / a.dv) - k0;
     const float* sp = a.segS + (size_t)bh * a.nseg * st + e;
-    float* ip = a.segin + (size_t)bh * a.nseg * st + e;
+    float* ip = a.segin + (size_t)bh * a.in_bh + e;
     float S = a.S0 ? a.S0[(size_t)bh * st + e] : 0.f;
     float buf[AHEAD];
     // step i visits segment seg(i): i in the forward order, nseg - 1 - i in the reverse one
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(NT) gla_state_scan_kernel(ScanArgs a)
             }
         }
     }
-    if (a.ST) a.ST[(size_t)bh * st + e] = S;
+    if (a.ST) a.ST[(size_t)bh * a.st_bh + e] = S;
 }
 
 }  // namespace
@@ -90,19 +92,24 @@ cudaError_t launch_seg_scan(const gla_fwd_params& p, const Plan& pl, void* ws, i
 {
     (void)status;
     uint8_t* base = static_cast<uint8_t*>(ws);
+    if (pl.st_nseg < 1 || pl.segin_n != pl.st_nseg + 1) return cudaErrorInvalidValue;
+    const size_t st = (size_t)p.dk * p.dv;
     ScanArgs a;
+    // the state pass's pieces from S0; the state after the last piece, where the last
+    // segment starts, is kept as the final start state (its chunk pass writes S_T)
     a.S0 = p.S0;
-    a.ST = p.ST;
     a.gam = p.gate == GLA_GATE_NONE ? nullptr : reinterpret_cast<const float*>(base + pl.off_gam);
     a.segS = reinterpret_cast<const float*>(base + pl.off_segS);
     a.segin = reinterpret_cast<float*>(base + pl.off_segin);
-    a.dk = p.dk; a.dv = p.dv; a.nchunks = pl.nchunks; a.nseg = pl.nseg; a.cps = pl.chunks_per_seg;
+    a.in_bh = (long long)pl.segin_n * st;
+    a.ST = a.segin + (size_t)pl.st_nseg * st;
+    a.st_bh = a.in_bh;
+    a.dk = p.dk; a.dv = p.dv; a.nchunks = pl.nchunks; a.nseg = pl.st_nseg; a.cps = pl.st_cps;
     a.rev = 0;
-    const size_t st = (size_t)p.dk * p.dv;
     dim3 grid((unsigned)((st + NT - 1) / NT), p.B * p.H);
     // rows one CTA touches: NT elements span at most NT / dv + 2 rows
     const int max_rows = NT / p.dv + 2;
-    const size_t smem = (size_t)max_rows * pl.nseg * sizeof(float);
+    const size_t smem = (size_t)max_rows * a.nseg * sizeof(float);
     gla_state_scan_kernel<<<grid, NT, smem, s>>>(a);
     return cudaGetLastError();
 }
@@ -115,6 +122,8 @@ cudaError_t launch_seg_scan_job(const SegScanJob& j, cudaStream_t s)
     a.gam = j.gam;
     a.segS = j.segS;
     a.segin = j.segin;
+    a.in_bh = (long long)j.nseg * j.dk * j.dv;
+    a.st_bh = (long long)j.dk * j.dv;
     a.dk = j.dk; a.dv = j.dv; a.nchunks = j.nch; a.nseg = j.nseg; a.cps = j.cps;
     a.rev = j.reverse ? 1 : 0;
     const size_t st = (size_t)j.dk * j.dv;

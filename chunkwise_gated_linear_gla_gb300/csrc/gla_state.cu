@@ -309,15 +309,18 @@ cudaError_t launch_seg_state(const gla_fwd_params& p, const Plan& pl, void* ws, 
     StateArgs a;
     const long long st = (long long)p.dk * p.dv;
     a.gam = reinterpret_cast<const float*>(base + pl.off_gam);
+    // one segment: the whole sequence to S_out; the split: its st_nseg pieces to the workspace
+    const int nz = S_out ? 1 : pl.st_nseg;
+    if (nz < 1) return cudaErrorInvalidValue;
     a.S_out = S_out ? S_out : reinterpret_cast<float*>(base + pl.off_segS);
-    a.s_out_bh = st * pl.nseg;
+    a.s_out_bh = st * nz;
     a.s_out_seg = st;
     a.status = status;
-    a.dv = p.dv; a.nchunks = pl.nchunks; a.cps = pl.chunks_per_seg;
+    a.dv = p.dv; a.nchunks = pl.nchunks; a.cps = S_out ? pl.chunks_per_seg : pl.st_cps;
     a.gated = p.gate != GLA_GATE_NONE;
     a.win = 0;
     a.rev = 0;
-    dim3 grid(pl.n_dvt, (unsigned)BH, pl.nseg);
+    dim3 grid(pl.n_dvt, (unsigned)BH, nz);
     switch (p.dk) {
     case 64: return launch_state_dk<64>(a, grid, mk, mv, s);
     case 128: return launch_state_dk<128>(a, grid, mk, mv, s);
@@ -334,9 +337,9 @@ cudaError_t launch_seg_window(const gla_fwd_params& p, const Plan& pl, void* ws,
     const size_t st = (size_t)p.dk * p.dv;
     float* segin = reinterpret_cast<float*>(base + pl.off_segin);
     // segment 0 starts from S0 (or zero): [BH] blocks of st floats, nseg * st apart
-    cudaError_t e = p.S0 ? cudaMemcpy2DAsync(segin, pl.nseg * st * 4, p.S0, st * 4, st * 4, BH,
+    cudaError_t e = p.S0 ? cudaMemcpy2DAsync(segin, pl.segin_n * st * 4, p.S0, st * 4, st * 4, BH,
                                              cudaMemcpyDeviceToDevice, s)
-                         : cudaMemset2DAsync(segin, pl.nseg * st * 4, 0, st * 4, BH, s);
+                         : cudaMemset2DAsync(segin, pl.segin_n * st * 4, 0, st * 4, BH, s);
     if (e != cudaSuccess) return e;
     const void* kb = pl.raw_qk ? p.k : base + pl.off_kt;
     const uint64_t krows = pl.raw_qk ? (uint64_t)p.T : (uint64_t)pl.Tpad;
@@ -346,7 +349,7 @@ cudaError_t launch_seg_window(const gla_fwd_params& p, const Plan& pl, void* ws,
     StateArgs a;
     a.gam = reinterpret_cast<const float*>(base + pl.off_gam);
     a.S_out = segin;   // segment s's window state goes to its start state; segment 0 has no window
-    a.s_out_bh = (long long)st * pl.nseg;
+    a.s_out_bh = (long long)st * pl.segin_n;
     a.s_out_seg = (long long)st;
     a.status = status;
     a.dv = p.dv; a.nchunks = pl.nchunks; a.cps = pl.chunks_per_seg;

@@ -179,11 +179,13 @@ def test_plan_on_host():
     assert names == ["gla_chunk_prep", "gla_chunk_state", "gla_state_scan", "gla_chunk_fwd"]
     ws_exact = bnd.gla_fwd_workspace_size(p)
     # the sliding-window split (opt-in) replaces the state pass and the scan with one window
-    # pass; the same workspace
+    # pass, which writes the 4 segments' start states directly; the exact split also keeps
+    # the 3 pieces' states of its state pass (one piece per segment here: 3 x 128 pieces
+    # would not fit in one wave) and one more start state
     p.window_chunks = 4
     names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
     assert names == ["gla_chunk_prep", "gla_chunk_state_window", "gla_chunk_fwd"]
-    assert bnd.gla_fwd_workspace_size(p) == ws_exact
+    assert bnd.gla_fwd_workspace_size(p) == ws_exact - 3 * 32 * 256 * 512 * 4
     # without a split the window changes nothing
     p.force_segments = 1
     names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
@@ -224,8 +226,9 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
 
 
 def test_bench_segment_rule_matches_library_plan():
-    """bench.py mirrors the library's segment rule to count bytes; the workspace the
-    library plans (which holds two fp32 states per segment) must agree with it."""
+    """bench.py mirrors the library's split rule to count bytes; the workspace the library
+    plans (one fp32 state per state-pass piece, and one start state per piece plus the
+    last segment's) must agree with it."""
     import sys
     sys.path.insert(0, ROOT)
     import bench
@@ -235,11 +238,13 @@ def test_bench_segment_rule_matches_library_plan():
         p = _params(B=w.B, H=w.H, T=w.T, dk=w.dk, dv=w.dv, gate=w.gate,
                     log_g=None if w.gate == 0 else 0x40000000, q=0x100000000, k=0x200000000,
                     v=0x300000000, O=0x400000000)
-        nseg = bench.planned_segments(w, 0, 148)   # the library plans for 148 SMs without a device
+        # the library plans for 148 SMs without a device
+        nseg, cps, sub, st_nseg, st_cps = bench.planned_split(w, 0, 148)
+        assert st_nseg == (nseg - 1) * sub and st_cps * sub == (cps if nseg > 1 else 0), name
         BH = w.B * w.H
         nch = (w.T + 63) // 64
         base = (0 if w.gate == 0 else 2 * BH * nch * 64 * w.dk * 2) + BH * nch * 64 * 64 * 2 + BH * nch * w.dk * 4
-        seg = 2 * BH * nseg * w.dk * w.dv * 4 if nseg > 1 else 0
+        seg = BH * (2 * st_nseg + 1) * w.dk * w.dv * 4 if nseg > 1 else 0
         assert bnd.gla_fwd_workspace_size(p) == got_staged(p), name
         got = bnd.gla_fwd_workspace_size(p)
         assert abs(got - (base + seg)) < 4096, (name, got, base + seg, nseg)

@@ -177,6 +177,20 @@ def test_forced_segments_other_gates(gate):
     _check_full(w, seed=4, force_segments=5)
 
 
+@pytest.mark.parametrize("nseg,s0", [(2, 0.02), (3, 0.0), (3, 0.02)])
+def test_state_pass_pieces(nseg, s0):
+    """The split's state pass in pieces finer than the segments, over the chunks before the
+    last segment only; the last segment's chunk pass writes S_T. 41 chunks (ragged last
+    one), two dv tiles: 2 segments of 21 chunks take 3 pieces of 7 each, 3 segments of 14
+    take 2 pieces of 7 each per segment (the last segment 13 chunks)."""
+    import bench
+    w = gi.Workload("t", B=1, H=2, T=64 * 40 + 17, dk=128, dv=256, dtype=torch.bfloat16,
+                    gate=gi.GATE_PER_KEY, s0_std=s0)
+    split = bench.planned_split(w, nseg, 148)
+    assert split == ((2, 21, 3, 3, 7) if nseg == 2 else (3, 14, 2, 4, 7))
+    _check_full(w, seed=11 + nseg, force_segments=nseg)
+
+
 def test_steep_gate_stays_finite_and_exact():
     """log alpha ~ -U(0,4) per entry: a chunk-level reference would overflow; the
     sub-chunk references keep every factor bounded."""
