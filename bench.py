@@ -120,11 +120,14 @@ def stage_bytes(w, name, split=None):
     if name == "gla_chunk_fused":
         # the whole pass in one kernel: q, k, v, the log gate read once, O written once, S0 / S_T
         return algorithmic(w)[1]
+    sc = scores_in_chunk_pass(w)
     if name == "gla_chunk_prep":
         # per-head decay with dk <= 128: chunks whose decay stays within e^-60 (every chunk of the
-        # workloads' lambda_h) leave Q (.) Lambda to the chunk pass, so only K (.) Gamma is written
-        qk_out = 0 if not gated else Tp * dk * 2 * (1 if (w.gate == 1 and dk <= 128) else 2)
-        return BH * (T * dk * 2 * 2 + gate_in + qk_out + nch * C * C * 2 + gam)
+        # workloads' lambda_h) leave Q (.) Lambda and their scores to the chunk pass, so the prep
+        # reads only k and writes only K (.) Gamma
+        if sc:
+            return BH * (T * dk * 2 + Tp * dk * 2 + gam)
+        return BH * (T * dk * 2 * 2 + gate_in + (Tp * dk * 2 * 2 if gated else 0) + nch * C * C * 2 + gam)
     if dk == 512 and name in ("gla_chunk_fwd", "gla_chunk_fwd_keys_hi"):
         # two chunk passes over key halves: each reads its half of Q (.) Lambda, K (.) Gamma, gamma,
         # S0 and writes its half of S_T; the first reads the scores and writes O as an fp32
@@ -138,7 +141,8 @@ def stage_bytes(w, name, split=None):
         last_state = (s0 + st) if nseg == 1 else BH * nseg * dk * dv * 4 + st
         # bilinear gate: V (.) D' in place of v, plus log beta and the chunks' column decays
         bil_in = T * dv * 4 + nch * dv * 4 if bil else 0
-        return BH * (qk_tiles + nch * C * C * 2 + gam + T * dv * 2 * 2 + bil_in) + last_state
+        scores = 0 if sc else nch * C * C * 2   # formed in the pass (dk <= 128, no gate or per-head decay)
+        return BH * (qk_tiles + scores + gam + T * dv * 2 * 2 + bil_in) + last_state
     if name == "gla_value_prep":
         return BH * (T * dv * (2 + 4 + 2) + nch * dv * 4)
     # the split's state pass covers the chunks before the last segment, in st_nseg pieces
@@ -148,6 +152,13 @@ def stage_bytes(w, name, split=None):
     if name == "gla_state_scan":
         return BH * (2 * st_nseg + 1) * dk * dv * 4 + s0 + BH * covered * dk * 4 * (1 if gated else 0)
     return 0
+
+
+def scores_in_chunk_pass(w):
+    """Whether the chunk pass forms the intra-chunk scores itself (same rule as csrc/gla_api.cu):
+    dk <= 128 with no gate or a per-head decay (whose chunks all keep the query factor out at
+    the workloads' decays)."""
+    return w.dk <= 128 and w.gate in (0, 1) and "bfloat16" in str(w.dtype)
 
 
 def planned_split(w, force, sms, state_ctas_per_sm=1, min_state_chunks=4):

@@ -193,6 +193,9 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     pl.Tpad = pl.nchunks * kChunk;
     pl.n_dvt = p->dv / kDvTile;
     pl.raw_qk = (p->gate == GLA_GATE_NONE);
+    // the intra-chunk scores formed in the chunk pass: dk <= 128 (its tensor memory has room
+    // for the score accumulator), no gate, or a per-head gate with the query factor left to it
+    pl.sc = p->dk <= 128 && (p->gate == GLA_GATE_NONE || q_factor_offload(*p));
     pl.sms = sms;
     const int units = p->B * p->H * pl.n_dvt;
     const bool bil = p->gate == GLA_GATE_BILINEAR;
@@ -226,8 +229,13 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
         pl.off_qt = off; off = align_up(off + BH * pl.Tpad * p->dk * 2, 256);
         pl.off_kt = off; off = align_up(off + BH * pl.Tpad * p->dk * 2, 256);
     }
-    pl.off_A = off;   off = align_up(off + BH * pl.nchunks * kChunk * kChunk * 2, 256);
-    pl.off_gam = off; off = align_up(off + BH * pl.nchunks * p->dk * 4, 256);
+    const bool prep = !(pl.sc && p->gate == GLA_GATE_NONE);   // no gate, scores in the pass: nothing to prepare
+    if (prep) {
+        pl.off_A = off;   off = align_up(off + BH * pl.nchunks * kChunk * kChunk * 2, 256);
+    }
+    if (p->gate != GLA_GATE_NONE) {
+        pl.off_gam = off; off = align_up(off + BH * pl.nchunks * p->dk * 4, 256);
+    }
     if (pl.nseg > 1) {
         pl.off_segS = off;  off = align_up(off + BH * pl.st_nseg * p->dk * p->dv * 4, 256);
         pl.off_segin = off; off = align_up(off + BH * pl.segin_n * p->dk * p->dv * 4, 256);
@@ -242,7 +250,7 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
     }
     pl.ws_bytes = off;
     int n = 0;
-    pl.stages[n++] = STAGE_PREP;
+    if (prep) pl.stages[n++] = STAGE_PREP;
     if (bil) pl.stages[n++] = STAGE_VALUE_PREP;
     if (pl.nseg > 1 && pl.window > 0) {
         pl.stages[n++] = STAGE_SEG_WINDOW;
@@ -506,7 +514,9 @@ gla_status gla_segment_pair(const gla_fwd_params* p, float* log_Gamma, float* S_
     if (q.T == 0) {
         e = cudaMemsetAsync(S_star, 0, ns, stream);
     } else if (pp.tensor) {
-        e = launch_prep(q, pp.pl, ws, c->status, stream);
+        // (no gate with the scores formed in the chunk pass: nothing to prepare, the state
+        // pass reads k itself)
+        if (pp.pl.nstages > 0 && pp.pl.stages[0] == STAGE_PREP) e = launch_prep(q, pp.pl, ws, c->status, stream);
         if (e == cudaSuccess) e = launch_seg_state(q, pp.pl, ws, c->status, stream, S_star);
     } else {
         q.O = ws + pp.off_o;

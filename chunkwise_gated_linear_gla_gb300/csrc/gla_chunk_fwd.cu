@@ -55,19 +55,20 @@ constexpr int PF_AHEAD = 2;                       // L2 prefetches run this many
 constexpr int NT = 512;
 constexpr int NEPI = 256;                         // state epilogue threads (warps 4-11)
 constexpr int NDR = 128;                          // output drain threads (warps 12-15)
-constexpr int BAR_EPI = 1, BAR_DR = 2;            // named barriers (0 is __syncthreads)
+constexpr int BAR_EPI = 1, BAR_DR = 2, BAR_SC = 3;   // named barriers (0 is __syncthreads)
 constexpr uint64_t kTimeoutNs = 2000000000ull;    // 2 s per wait
 // Registers per thread of each warpgroup after setmaxnreg (the launch gives 128 each):
 // producer/MMA, state epilogue (two warpgroups), drain.
 // The split that compiles without spills differs between instantiations.
-template <int DK, bool BIL>
+template <int DK, bool BIL, bool SC = false>
 struct Regs {
     static constexpr bool wide = DK == 256 && !BIL;
-    static constexpr int ctl = wide ? 64 : 80, epi = wide ? 176 : 160, drain = wide ? 96 : 112;
+    // SC: warps 2 and 3 of the first warpgroup also read the scores out
+    static constexpr int ctl = wide ? 64 : SC ? 96 : 80, epi = wide ? 176 : 160, drain = wide || SC ? 96 : 112;
     static_assert(128 * (ctl + 2 * epi + drain) <= NT * 128, "register split");
 };
 
-enum { ERR_PRODUCER = 0x101, ERR_MMA = 0x102, ERR_EPI = 0x103, ERR_DRAIN = 0x104 };
+enum { ERR_PRODUCER = 0x101, ERR_MMA = 0x102, ERR_EPI = 0x103, ERR_DRAIN = 0x104, ERR_READOUT = 0x105 };
 
 struct FwdArgs {
     const float* S_in;  long long s_in_bh, s_in_seg;
@@ -90,28 +91,35 @@ struct FwdArgs {
 };
 static_assert(sizeof(FwdArgs) <= 128, "FwdArgs stays within 128 bytes");
 
-template <int DK, bool BIL>
+// SC: the pass forms the intra-chunk scores itself (see the kernel's header); the stage then
+// holds the K tile before the Q tile, so that the score product's 128-row A operand can start
+// 64 rows before the Q tile and place the chunk's rows in tensor-memory lanes 64-127.
+template <int DK, bool BIL, bool SC = false>
 struct Lay {
     static constexpr int QB = DK * C * 2;
     static constexpr int KB = DK * C * 2;
     static constexpr int VB = DVT * C * 2;
     static constexpr int AB = C * C * 2;
     static constexpr int GB = DK * 4;
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = QB;
+    static constexpr int Q_OFF = SC ? KB : 0;
+    static constexpr int K_OFF = SC ? 0 : QB;
     static constexpr int V_OFF = QB + KB;
     static constexpr int A_OFF = V_OFF + VB;
     static constexpr int STAGE = (A_OFF + AB + 1023) / 1024 * 1024;
+    // operand stages: SC with dk <= 128 holds three (a stage is released only after the score
+    // readout the intra MMA waits for, so its turnaround is longer), else two
+    static constexpr int NST = (SC && DK <= 128) ? 3 : NSTAGE;
     // the gate ring: slot = the chunk's key decays gamma (and, bilinear gate, its column
     // decays' logs B'_C), NG chunks deep, so the decay of the state never waits for a stage
     static constexpr int GVB = BIL ? DVT * 4 : 0;
     static constexpr int GSL = GB + GVB;
-    static constexpr int GR_OFF = NSTAGE * STAGE;
+    static constexpr int GR_OFF = NST * STAGE;
     static constexpr int OB = C * DVT * 2;
     static constexpr int O_OFF = GR_OFF + NG * GSL;
     static constexpr int BAR_OFF = O_OFF + 2 * OB;
-    static constexpr int SMEM = BAR_OFF + 256 + 1024;
-    static constexpr int TCOLS_USED = DK + DK / 2 + 2 * 64;
+    static constexpr int BARB = SC ? 512 : 256;   // SC: the stage barriers after the first 32 slots
+    static constexpr int SMEM = BAR_OFF + BARB + 1024;
+    static constexpr int TCOLS_USED = DK + DK / 2 + 2 * 64 + (SC ? 64 : 0);   // + the score accumulator
     static constexpr int TCOLS = TCOLS_USED <= 256 ? 256 : 512;
     static_assert(TCOLS_USED <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -143,13 +151,14 @@ __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.
 // 2 = keys [DK, 2 DK), no intra-chunk term, the partial added before the bf16 store.
 // Each half carries its own rows of the state: the gate scales rows, so the two
 // halves' recurrences are independent and only their outputs add.
-template <int DK, bool BIL, bool SCAL, int KH>
+template <int DK, bool BIL, bool SCAL, int KH, bool SC>
 __global__ void __launch_bounds__(NT, 1)
 gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmQr)
 {
-    using L = Lay<DK, BIL>;
+    static_assert(!SC || (!BIL && KH == 0 && DK <= 128), "on-chip scores: no bilinear gate, dk <= 128");
+    using L = Lay<DK, BIL, SC>;
     constexpr int HC = DK / 2;   // state columns per epilogue thread
     constexpr int DKT = KH ? 2 * DK : DK;    // keys of the head
     constexpr int KOFF = KH == 2 ? DK : 0;   // this CTA's first key
@@ -159,8 +168,10 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
-    uint64_t* full = bar + 0;      // [2] stage's K and V tiles landed (TMA transaction count)
-    uint64_t* empty = bar + 2;     // [2] stage consumed (MMA commit)
+    constexpr int NST = L::NST;
+    // [NST] stage's K and V tiles landed (TMA transaction count) / stage consumed (MMA commit)
+    uint64_t* full = SC ? bar + 32 : bar + 0;
+    uint64_t* empty = SC ? bar + 32 + NST : bar + 2;
     uint64_t* s_ready = bar + 4;   // state decayed in TMEM (256 arrivals)
     uint64_t* s_done = bar + 5;    // state MMA of the chunk complete
     uint64_t* sb_free = bar + 6;   // inter MMA complete: bf16 state copy reusable
@@ -172,8 +183,10 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     uint64_t* mma_fin = bar + 14;  // every MMA of the CTA complete (the issuer's last commit)
     uint64_t* gfull = bar + 15;    // [NG] gate ring slot filled (transaction count)
     uint64_t* gempty = bar + 15 + NG;   // [NG] gate ring slot read (256 arrivals)
-    uint64_t* full_qa = bar + 15 + 2 * NG;   // [2] stage's Q and score tiles landed
+    uint64_t* full_qa = SC ? bar + 32 + 2 * NST : bar + 15 + 2 * NG;   // [NST] stage's Q and score tiles landed
     volatile int* issued_ctr = reinterpret_cast<volatile int*>(bar + 17 + 2 * NG);   // chunks whose loads are out
+    uint64_t* p_full = bar + 18 + 2 * NG;    // SC: score product complete
+    uint64_t* p_ready = bar + 32 + 3 * NST;  // SC: [NST] masked bf16 scores written to the stage (64 arrivals)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.y, seg = blockIdx.z;
@@ -184,7 +197,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     const bool want_out = a.mode == kModeFull || a.mode == kModeSegOut;
     // the state sweeps keep the state entering every chunk; the reverse one walks the chunks
     // from the last (the backward's recurrence for dL/dS)
-    const bool sweep = !BIL && !SCAL && KH == 0 && (a.mode == kModeSweep || a.mode == kModeSweepRev);
+    const bool sweep = !BIL && !SCAL && !SC && KH == 0 && (a.mode == kModeSweep || a.mode == kModeSweepRev);
     const bool rev = sweep && a.mode == kModeSweepRev;
     auto chunk_of = [&](int j) { return rev ? c_end - 1 - j : c_begin + j; };
     const bool gated = a.gated != 0;
@@ -192,16 +205,25 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     // made the same decision on the same float, rows x log lambda)
     const float lam_h = SCAL ? a.lamh[bh % a.H] : 0.f;
     auto q_fac = [&](int ch) -> bool { return SCAL && q_factored((float)min(C, a.T - ch * C) * lam_h); };
+    // SC: whether chunk ch's scores are formed here (no gate: every chunk; per-head gate: the
+    // chunks that take raw q) instead of read from the prep's score tiles
+    auto sc_chunk = [&](int ch) -> bool { return SC && (!SCAL || q_fac(ch)); };
 
     if (threadIdx.x == 0) {
-        mbar_init(&full[0], 1); mbar_init(&full[1], 1);
-        mbar_init(&full_qa[0], 1); mbar_init(&full_qa[1], 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&full_qa[i], 1);
+            mbar_init(&empty[i], 1);
+        }
         *issued_ctr = 0;
-        mbar_init(&empty[0], 1); mbar_init(&empty[1], 1);
         mbar_init(s_ready, NEPI); mbar_init(s_done, 1); mbar_init(sb_free, 1); mbar_init(sb_ready, NEPI);
         mbar_init(&o_full[0], 1); mbar_init(&o_full[1], 1);
         mbar_init(&o_empty[0], NDR); mbar_init(&o_empty[1], NDR);
         mbar_init(mma_fin, 1);
+        if (SC) {
+            mbar_init(p_full, 1);
+            for (int i = 0; i < NST; ++i) mbar_init(&p_ready[i], 64);
+        }
         for (int i = 0; i < NG; ++i) {
             mbar_init(&gfull[i], 1);
             mbar_init(&gempty[i], NEPI);
@@ -221,9 +243,10 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const uint32_t tS = tmem, tSb = tmem + DK, tO0 = tmem + DK + DK / 2;
+    const uint32_t tP = tO0 + 128;   // SC: the score accumulator, 64 columns (lanes 64-127)
 
     const int wg = warp >> 2;
-    if (wg == 0) regs_dec<Regs<DK, BIL>::ctl>();   // warps 2 and 3 have no role
+    if (wg == 0) regs_dec<Regs<DK, BIL, SC>::ctl>();   // warp 2 prefetches; SC: warps 2 and 3 read the scores out
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
@@ -246,8 +269,8 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 for (; gissued < G_AHEAD && gissued < nloc; ++gissued) load_g(gissued);
             for (int n = 0; n < nloc; ++n) {
                 if (*abort_flag) break;
-                const int st = n & 1, c = chunk_of(n);
-                if (n >= 2 && !mbar_wait(&empty[st], ((n >> 1) - 1) & 1, kTimeoutNs)) {
+                const int st = n % NST, c = chunk_of(n);
+                if (n >= NST && !mbar_wait(&empty[st], ((n / NST) - 1) & 1, kTimeoutNs)) {
                     fail(a.status, abort_flag, ERR_PRODUCER);
                     break;
                 }
@@ -261,12 +284,13 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 tma_load_3d(sb + L::V_OFF, &tmV, &full[st], dv0, c * C, bh);
                 tma_load_3d(sb + L::V_OFF + 8192, &tmV, &full[st], dv0 + 64, c * C, bh);
                 if (want_out) {
-                    mbar_arrive_expect_tx(&full_qa[st], L::QB + (KH == 2 ? 0 : L::AB));
+                    const bool ldA = KH != 2 && !sc_chunk(c);
+                    mbar_arrive_expect_tx(&full_qa[st], L::QB + (ldA ? L::AB : 0));
                     const CUtensorMap* mq = q_fac(c) ? &tmQr : &tmQ;
 #pragma unroll
                     for (int i = 0; i < DK / 64; ++i)
                         tma_load_3d(sb + L::Q_OFF + i * 8192, mq, &full_qa[st], KOFF + i * 64, c * C, bh);
-                    if (KH != 2) tma_load_2d(sb + L::A_OFF, &tmA, &full_qa[st], 0, (bh * a.nchunks + c) * C);
+                    if (ldA) tma_load_2d(sb + L::A_OFF, &tmA, &full_qa[st], 0, (bh * a.nchunks + c) * C);
                 }
                 *issued_ctr = n + 1;   // paces the L2 prefetches of warp 2
                 issued = n + 1;
@@ -279,49 +303,139 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 }
             }
             // no copy may land after the CTA exits: wait for the last fills
-            for (int n = max(0, issued - 2); n < issued; ++n) {
-                mbar_wait(&full[n & 1], (n >> 1) & 1, kTimeoutNs);
-                if (want_out) mbar_wait(&full_qa[n & 1], (n >> 1) & 1, kTimeoutNs);
+            for (int n = max(0, issued - NST); n < issued; ++n) {
+                mbar_wait(&full[n % NST], (n / NST) & 1, kTimeoutNs);
+                if (want_out) mbar_wait(&full_qa[n % NST], (n / NST) & 1, kTimeoutNs);
             }
             for (int j = max(0, gissued - NG); j < gissued; ++j) mbar_wait(&gfull[j % NG], (j / NG) & 1, kTimeoutNs);
         }
-    } else if (warp == 2) {
-        // ---------------------------------------------------------- L2 prefetcher
-        // Once the producer has issued chunk m's loads, pull chunk m + PF_AHEAD's tiles into
-        // L2, so that the stage loads, issued only when a stage frees up, find them there.
-        // The tiles all dv-tile CTAs of this head share are split among them. Prefetches are
-        // hints: if the producer stops (an abort) this thread just stops too.
-        if (lane == 0) {
-            const uint64_t t_start = globaltimer();
-            for (int m = 0; m + PF_AHEAD < nloc; ++m) {
-                bool go = true;
-                while (*issued_ctr <= m) {
-                    if (*abort_flag || globaltimer() - t_start > kTimeoutNs) {
-                        go = false;
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-                if (!go) break;
-                const int cp = chunk_of(m + PF_AHEAD);
-                prefetch_l2_tile_3d(&tmV, dv0, cp * C, bh);
-                prefetch_l2_tile_3d(&tmV, dv0 + 64, cp * C, bh);
-                const int nt = gridDim.x, me = blockIdx.x;
-                int item = 0;
+    } else if (warp == 2 || (SC && warp == 3)) {
+        // ---------------------------------------------------------- L2 prefetcher (and SC readout)
+        // Once the producer has issued chunk m's loads, pull chunk m + PFA's tiles into L2, so
+        // that the stage loads, issued only when a stage frees up, find them there. The tiles
+        // all dv-tile CTAs of this head share are split among them. Prefetches are hints: if
+        // the producer stops (an abort) this thread just stops too.
+        constexpr int PFA = SC ? PF_AHEAD + 1 : PF_AHEAD;   // SC: issued after the chunk's readout
+        const uint64_t t_start = globaltimer();
+        // bounded wait until the producer has issued chunk m's loads
+        auto wait_issued = [&](int m) -> bool {
+            while (*issued_ctr <= m) {
+                if (*abort_flag || globaltimer() - t_start > kTimeoutNs) return false;
+                __nanosleep(64);
+            }
+            return true;
+        };
+        auto prefetch = [&](int m) -> bool {
+            if (!wait_issued(m)) return false;
+            const int cp = chunk_of(m + PFA);
+            prefetch_l2_tile_3d(&tmV, dv0, cp * C, bh);
+            prefetch_l2_tile_3d(&tmV, dv0 + 64, cp * C, bh);
+            const int nt = gridDim.x, me = blockIdx.x;
+            int item = 0;
+#pragma unroll
+            for (int i = 0; i < DK / 64; ++i, ++item)
+                if (item % nt == me) prefetch_l2_tile_3d(&tmK, KOFF + i * 64, cp * C, bh);
+            if (want_out) {
+                const CUtensorMap* mq = q_fac(cp) ? &tmQr : &tmQ;
 #pragma unroll
                 for (int i = 0; i < DK / 64; ++i, ++item)
-                    if (item % nt == me) prefetch_l2_tile_3d(&tmK, KOFF + i * 64, cp * C, bh);
-                if (want_out) {
-                    const CUtensorMap* mq = q_fac(cp) ? &tmQr : &tmQ;
-#pragma unroll
-                    for (int i = 0; i < DK / 64; ++i, ++item)
-                        if (item % nt == me) prefetch_l2_tile_3d(mq, KOFF + i * 64, cp * C, bh);
-                    if (KH != 2 && item % nt == me) prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
-                    ++item;
-                }
-                if (gated && item % nt == me && m + PF_AHEAD + G_AHEAD < nloc)
-                    prefetch_l2(a.gam + ((size_t)bh * a.nchunks + chunk_of(m + PF_AHEAD + G_AHEAD)) * DKT + KOFF, L::GB);
+                    if (item % nt == me) prefetch_l2_tile_3d(mq, KOFF + i * 64, cp * C, bh);
+                if (KH != 2 && !sc_chunk(cp) && item % nt == me)
+                    prefetch_l2_tile_2d(&tmA, 0, (bh * a.nchunks + cp) * C);
+                ++item;
             }
+            if (gated && item % nt == me && m + PFA + G_AHEAD < nloc)
+                prefetch_l2(a.gam + ((size_t)bh * a.nchunks + chunk_of(m + PFA + G_AHEAD)) * DKT + KOFF, L::GB);
+            return true;
+        };
+        if (!SC || !want_out) {
+            if (warp == 2 && lane == 0)
+                for (int m = 0; m + PFA < nloc; ++m)
+                    if (!prefetch(m)) break;
+        } else {
+            // SC: warps 2 and 3 form the chunk's scores. Lane 0 of warp 2 issues the product
+            // P = Q K^T (its own MMAs and commit, beside the issuer's) as soon as the stage's Q and
+            // K have landed: both operands K-major, A = 128 rows from 64 rows before the Q tile
+            // (the K tile's last 64-column slab, or the Q tile's previous one), so that the
+            // chunk's rows r = 0..63 land in TMEM lanes 64-127, the lane quarters of warps 2 and 3.
+            // Those turn it into the masked bf16 tile the intra MMA reads, in the stage's score
+            // slot (which the producer leaves empty for these chunks): row r, 128-byte swizzle, as
+            // the prep's tiles. Per-head gate: times lambda^-nr, which with K (.) Gamma gives the
+            // factored scores (q_r . k_s) lambda^-(s+1). The product reads the stage, which the
+            // issuer releases only after the intra MMA, which waits for this readout, which waits
+            // for the product: so it is done before the stage is refilled.
+            const int r = (warp - 2) * 32 + lane;
+            const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t id_score = idesc_bf16(128, 64, false, false);
+            const uint32_t sbase = smem_u32(sm);
+            const uint64_t dQm0 = sdesc(sbase + L::Q_OFF - 8192, 16, 1024, kSwizzle128);
+            const uint64_t dKk0 = sdesc(sbase + L::K_OFF, 16, 1024, kSwizzle128);
+            bool alive = true, pf = true;
+            for (int m = 0, j = 0; m < nloc && alive; ++m) {
+                const int c = chunk_of(m), st = m % NST;
+                if (sc_chunk(c)) {
+                    bool ok = true;
+                    if (warp == 2) {
+                        if (lane == 0) {
+                            // chunk m's loads issued first: its stage's barriers are then in chunk
+                            // m's phase (chunks skipped above did not wait on them, and chunk m + NST
+                            // cannot be loaded before this readout is done)
+                            ok = wait_issued(m) && mbar_wait(&full[st], (m / NST) & 1, kTimeoutNs) &&
+                                 mbar_wait(&full_qa[st], (m / NST) & 1, kTimeoutNs) && !*abort_flag;
+                            if (ok) {
+                                tc_fence_after();
+                                const uint64_t so = (uint64_t)((st * L::STAGE) >> 4);
+#pragma unroll
+                                for (int kk = 0; kk < DK / 16; ++kk) {
+                                    const uint64_t ko = so + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
+                                    mma_ss(tP, dQm0 + ko, dKk0 + ko, id_score, kk > 0);
+                                }
+                                mma_commit(p_full);
+                            }
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                    }
+                    ok = __all_sync(0xffffffffu, ok && mbar_wait(p_full, j & 1, kTimeoutNs) && !*abort_flag);
+                    ++j;
+                    if (ok) {
+                        tc_fence_after();
+                        const float fac = SCAL ? __expf(-(float)min(C, a.T - c * C) * lam_h) : 1.f;
+                        uint8_t* row = sm + st * L::STAGE + L::A_OFF + r * 128;
+                        // 16 bf16 pairs of key rows 32 h .. 32 h + 31 of row r, masked to s <= r
+                        auto half = [&](int h, const uint32_t* v) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int col = 32 * h + 2 * i;   // key row s of the chunk
+                                float x0 = __uint_as_float(v[2 * i]), x1 = __uint_as_float(v[2 * i + 1]);
+                                if (SCAL) { x0 *= fac; x1 *= fac; }
+                                pk[i] = pack_bf16(col <= r ? x0 : 0.f, col + 1 <= r ? x1 : 0.f);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                *reinterpret_cast<uint4*>(row + (((4 * h + i) ^ (r & 7)) << 4)) =
+                                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        };
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t v[32];
+                            tmem_ld32(tP + lb + 32 * h, v);
+                            tmem_wait_ld();
+                            half(h, v);
+                        }
+                        fence_proxy_async_smem();
+                        tc_fence_before();
+                        mbar_arrive(&p_ready[st]);
+                    }
+                    // both warps' loads of the accumulator are done before the next product
+                    alive = group_all_ok(ok, BAR_SC, 64);
+                    tc_fence_after();
+                    if (!alive) break;
+                }
+                if (warp == 2 && lane == 0 && pf && m + PFA < nloc) pf = prefetch(m);
+                __syncwarp();
+            }
+            if (!alive && lane == 0) fail(a.status, abort_flag, ERR_READOUT);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -337,10 +451,14 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
             const uint64_t dK0 = sdesc(s0 + L::K_OFF, 8192, 1024, kSwizzle128);
             const uint64_t dQ0 = sdesc(s0 + L::Q_OFF, 16, 1024, kSwizzle128);
             const uint64_t dA0 = sdesc(s0 + L::A_OFF, 16, 1024, kSwizzle128);
+            // bit st: the parity of the chunks in stage st whose scores warps 2 and 3 formed so far
+            // (p_ready[st]'s phase: a stage's next readout needs the stage refilled, so it cannot
+            // run two phases ahead)
+            uint32_t jpar = 0;
             for (int n = 0; n < nloc; ++n) {
                 if (*abort_flag) break;
-                const int st = n & 1;
-                bool ok = mbar_wait(&full[st], (n >> 1) & 1, kTimeoutNs);
+                const int st = n % NST;
+                bool ok = mbar_wait(&full[st], (n / NST) & 1, kTimeoutNs);
                 ok = ok && mbar_wait(s_ready, n & 1, kTimeoutNs);
                 if (!ok) {
                     fail(a.status, abort_flag, ERR_MMA);
@@ -357,7 +475,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                 if (want_out) {
                     ok = mbar_wait(sb_ready, n & 1, kTimeoutNs);
                     if (ok && n >= 2) ok = mbar_wait(&o_empty[n & 1], ((n >> 1) - 1) & 1, kTimeoutNs);
-                    if (ok) ok = mbar_wait(&full_qa[st], (n >> 1) & 1, kTimeoutNs);
+                    if (ok) ok = mbar_wait(&full_qa[st], (n / NST) & 1, kTimeoutNs);
                     if (!ok) {
                         fail(a.status, abort_flag, ERR_MMA);
                         break;
@@ -371,6 +489,16 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
                     mma_commit(sb_free);
                     // intra: O^T += V^T (P (.) M)^T (the second key half leaves it to the first)
                     if (KH != 2) {
+                        if (sc_chunk(chunk_of(n))) {
+                            // warps 2 and 3's masked scores in the stage's score slot
+                            const bool okp = mbar_wait(&p_ready[st], (jpar >> st) & 1, kTimeoutNs);
+                            jpar ^= 1u << st;
+                            if (!okp) {
+                                fail(a.status, abort_flag, ERR_MMA);
+                                break;
+                            }
+                            tc_fence_after();
+                        }
 #pragma unroll
                         for (int kk = 0; kk < C / 16; ++kk)
                             mma_ss(tO, dV + kk * (2048 >> 4), dA + kk * (32 >> 4), id_intra, 1);
@@ -388,15 +516,17 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         // ---------------------------------------------------------- state epilogue (2 groups of 4 warps)
         // Group g owns state columns [g*DK/2, (g+1)*DK/2); the warp's TMEM lane quarter is
         // (warp % 4) and its thread's dv column d.
-        regs_inc<Regs<DK, BIL>::epi>();
+        regs_inc<Regs<DK, BIL, SC>::epi>();
         const int grp = wg - 1;
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const int d = (warp & 3) * 32 + lane;   // dv column within the tile
         const int cb = grp * HC;                 // first state column of this group
         const int gt = threadIdx.x - 128 - grp * 128;   // thread index within the group
         // S0 is the caller's and no earlier grid of the pass writes it; the segment scan's
-        // start states (sequence split) come from the grid ahead
-        if (a.mode != kModeFull) grid_dependency_wait();
+        // start states (sequence split) come from the grid ahead. Without a gate and with the
+        // scores formed here (SC, not SCAL) no prep runs first: the grid ahead may then be the
+        // caller's previous pass, whose S_T can be this S0, so wait for it too.
+        if (a.mode != kModeFull || (SC && !SCAL)) grid_dependency_wait();
         {
             // S_in of this thread's column and HC keys: every load in flight at once, then to TMEM
             const float* sin = a.S_in ? a.S_in + bh * a.s_in_bh + seg * a.s_in_seg + dv0 + d : nullptr;
@@ -550,7 +680,7 @@ gla_chunk_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         // ---------------------------------------------------------- output drain (4 warps)
         // Thread (warp % 4, lane) owns dv column d of the tile in all 64 rows of each chunk:
         // O^T TMEM -> registers -> bf16 smem tile -> TMA store, 32 rows at a time.
-        regs_dec<Regs<DK, BIL>::drain>();
+        regs_dec<Regs<DK, BIL, SC>::drain>();
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const int d = (warp & 3) * 32 + lane;
         const int dt = threadIdx.x - 384;   // thread index within the drain warps
@@ -680,16 +810,16 @@ bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, str, box, swz);
 }
 
-template <int DK, bool BIL, bool SCAL, int KH = 0>
+template <int DK, bool BIL, bool SCAL, int KH = 0, bool SC = false>
 cudaError_t launch_dk(const FwdArgs& a, dim3 grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                       const CUtensorMap& A, const CUtensorMap& o, const CUtensorMap& qr, cudaStream_t s) {
-    using L = Lay<DK, BIL>;
-    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK, BIL, SCAL, KH>,
+    using L = Lay<DK, BIL, SC>;
+    cudaError_t e = cudaFuncSetAttribute(gla_chunk_fwd_kernel<DK, BIL, SCAL, KH, SC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
     // the setmaxnreg split redistributes the 128 registers per thread the launch provides
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, gla_chunk_fwd_kernel<DK, BIL, SCAL, KH>);
+    e = cudaFuncGetAttributes(&fa, gla_chunk_fwd_kernel<DK, BIL, SCAL, KH, SC>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
     // Programmatic stream serialization lets the CTAs start (barriers, tensor memory, S0)
@@ -707,7 +837,7 @@ cudaError_t launch_dk(const FwdArgs& a, dim3 grid, const CUtensorMap& q, const C
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (!BIL && KH != 2) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gla_chunk_fwd_kernel<DK, BIL, SCAL, KH>, a, q, k, v, A, o, qr);
+    return cudaLaunchKernelEx(&cfg, gla_chunk_fwd_kernel<DK, BIL, SCAL, KH, SC>, a, q, k, v, A, o, qr);
 }
 
 }  // namespace
@@ -734,7 +864,12 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
     const void* vb = bil ? base + pl.off_vh : p.v;   // bilinear gate: V (.) D' from gla_value_prep
     if (!map3(&mv, vb, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     if (!map3(&mo, p.O, p.dv, p.T, BH, CU_TENSOR_MAP_SWIZZLE_NONE, 32)) return cudaErrorInvalidValue;
-    {
+    // the scores: pl.sc without a gate forms every chunk's in the pass (no score tiles; the
+    // q map stands in, never read); with the per-head gate, the steep chunks' come from the prep
+    const bool sc = pl.sc && mode != kModeSegState;
+    if (sc && p.gate == GLA_GATE_NONE) {
+        ma = mq;
+    } else {
         uint64_t dims[2] = {64, BH * (uint64_t)pl.nchunks * 64};
         uint64_t str[1] = {128};
         uint32_t box[2] = {64, 64};
@@ -789,6 +924,16 @@ cudaError_t launch_chunk_fwd(const gla_fwd_params& p, const Plan& pl, void* ws, 
         case 64: return launch_dk<64, true, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
         case 128: return launch_dk<128, true, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
         case 256: return launch_dk<256, true, false>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+        }
+        return cudaErrorInvalidValue;
+    }
+    if (sc) {
+        if (!qfac && p.gate != GLA_GATE_NONE) return cudaErrorInvalidValue;
+        switch (p.dk) {
+        case 64: return qfac ? launch_dk<64, false, true, 0, true>(a, grid, mq, mk, mv, ma, mo, mqr, s)
+                             : launch_dk<64, false, false, 0, true>(a, grid, mq, mk, mv, ma, mo, mqr, s);
+        case 128: return qfac ? launch_dk<128, false, true, 0, true>(a, grid, mq, mk, mv, ma, mo, mqr, s)
+                              : launch_dk<128, false, false, 0, true>(a, grid, mq, mk, mv, ma, mo, mqr, s);
         }
         return cudaErrorInvalidValue;
     }

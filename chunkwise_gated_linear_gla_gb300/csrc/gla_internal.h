@@ -65,6 +65,9 @@ struct Plan {
     // piece and the state after the last (the sliding window keeps one per segment)
     int sub = 1, st_nseg = 0, st_cps = 0, segin_n = 0;
     bool raw_qk = false;   // tensor path reads q,k directly (no gate)
+    // the chunk pass forms the intra-chunk scores itself (dk <= 128, no gate or a per-head
+    // gate's chunks with the query factor left to it); no gate then needs no prep at all
+    bool sc = false;
     int sms = 0;           // multiprocessors of the device the plan was made for
     // workspace layout (byte offsets from the workspace base)
     size_t off_qt = 0, off_kt = 0, off_A = 0, off_gam = 0, off_segS = 0, off_segin = 0;

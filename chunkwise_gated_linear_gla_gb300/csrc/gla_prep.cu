@@ -77,6 +77,7 @@ struct PrepArgs {
     int* status;
     int BH, H, T, nchunks, Tpad, gate;
     int qfac;   // per-head scalar gate: chunks that pass q_factored leave Lambda to the chunk pass
+    int sc;     // with qfac: those chunks' scores are formed by the chunk pass too (only K (.) Gamma here)
     // read first by the next stages (see prefetch_next_stage): S0, and v by heads
     const uint8_t* pf_s0;   size_t pf_s0_bytes;
     const uint8_t* pf_v;    size_t pf_v_stride;   uint32_t pf_v_bytes;
@@ -637,14 +638,20 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     constexpr bool gated = GATE != GLA_GATE_NONE;
     constexpr bool tok = GATE == GLA_GATE_TOKEN_SCALAR;
     // the q/k tiles of an item (every box full-size: rows at or past T arrive as zeros)
+    // per-head gate: whether an item's chunk leaves Lambda, and with a.sc its scores, to the chunk pass
+    auto factored = [&](int item) -> bool {
+        const int c = item % a.nchunks, h = (item / a.nchunks) % a.H;
+        return GATE == GLA_GATE_HEAD_SCALAR && a.qfac && q_factored(min(C, a.T - c * C) * a.log_g[h]);
+    };
     auto load = [&](int item, int b) {
         const int c = item % a.nchunks, bh = item / a.nchunks;
         __nv_bfloat16* Qb = tiles + b * 2 * TILE;
+        const bool kq = !(a.sc && factored(item));   // only K (.) Gamma: no q tile
         bulk_wait_read0();   // an earlier item's A store has read its stage (a q tile)
-        mbar_arrive_expect_tx(&cbar[b], 2 * TILE * 2);
+        mbar_arrive_expect_tx(&cbar[b], (kq ? 2 : 1) * TILE * 2);
 #pragma unroll
         for (int i = 0; i < DK / 64; ++i) {
-            tma_load_3d(Qb + i * C * 64, &tmq, &cbar[b], i * 64, c * C, bh);
+            if (kq) tma_load_3d(Qb + i * C * 64, &tmq, &cbar[b], i * 64, c * C, bh);
             tma_load_3d(Qb + TILE + i * C * 64, &tmk, &cbar[b], i * 64, c * C, bh);
         }
     };
@@ -682,7 +689,7 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
         if (nx2 < total) {
             const int c2 = nx2 % a.nchunks, bh2 = nx2 / a.nchunks, nr2 = min(C, a.T - c2 * C);
             const size_t row = (size_t)bh2 * a.T + (size_t)c2 * C;
-            prefetch_l2(a.q + row * DK, (uint32_t)nr2 * DK * 2);
+            if (!(a.sc && factored(nx2))) prefetch_l2(a.q + row * DK, (uint32_t)nr2 * DK * 2);
             prefetch_l2(a.k + row * DK, (uint32_t)nr2 * DK * 2);
             if (tok) prefetch_row_l2(a.log_g + row, nr2);
         }
@@ -707,8 +714,12 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     // The tiles come from TMA and are not written here, so the product can start as soon
     // as they land; Q (.) Lambda (warps 2-3, meanwhile) and K (.) Gamma (warps 0-1, after
     // the readout) are per-row scalings of the same tiles.
+    // per-head gate: a chunk whose decay stays within exp(-kQGuard) leaves Lambda to the chunk pass,
+    // and with a.sc its scores too (block-uniform)
+    const bool fq = GATE == GLA_GATE_HEAD_SCALAR && a.qfac && q_factored(nr * lam);
+    const bool only_k = a.sc && fq;
     bool ok = mbar_wait(&cbar[b], parity, kTimeoutNs);
-    if (warp == 0) {
+    if (warp == 0 && !only_k) {
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             tc_fence_after();
@@ -723,8 +734,6 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     }
     if (tok)
         for (int col = tid; col < DK; col += NTU) a.gam[((size_t)bh * a.nchunks + c) * DK + col] = __expf(Lc[C - 1]);
-    // per-head gate: a chunk whose decay stays within exp(-kQGuard) leaves Lambda to the chunk pass
-    const bool fq = GATE == GLA_GATE_HEAD_SCALAR && a.qfac && q_factored(nr * lam);
     // Q (pass 0) or K (pass 1), rows [r0, r1), by nth threads
     auto scale_rows = [&](int pass, int r0, int r1, int t, int nth) {
         const __nv_bfloat16* T = pass == 0 ? Qs : Ks;
@@ -745,7 +754,9 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
     // the readout stages A in the q tile once the other warps are done reading it
     // (named barrier 2); the K rows are split in proportion to the threads
     constexpr int KSPLIT = C * (NTU - 64) / NTU;
-    if (warp < 2) {
+    if (only_k) {
+        scale_rows(1, 0, C, tid, NTU);
+    } else if (warp < 2) {
         ok = score_readout<tok>(tmem, mbar, mphase, nr, lam, Qs, &tmA, (bh * a.nchunks + c) * C, 2, NTU, Lc, fq);
         if (gated) scale_rows(1, KSPLIT, C, tid, 64);
     } else {
@@ -753,7 +764,7 @@ gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tm
         named_bar_arrive(2, NTU);
         if (gated) scale_rows(1, 0, KSPLIT, tid - 64, NTU - 64);
     }
-    mphase ^= 1u;
+    if (!only_k) mphase ^= 1u;
     if (__syncthreads_or(!ok)) {   // also: the tiles and the accumulator are reused by the next item
         if (tid == 0) atomicExch(a.status, ERR_PREP);
         break;
@@ -841,6 +852,7 @@ cudaError_t launch_prep(const gla_fwd_params& p, const Plan& pl, void* ws, int* 
     a.status = status;
     a.BH = p.B * p.H; a.H = p.H; a.T = p.T; a.nchunks = pl.nchunks; a.Tpad = pl.Tpad; a.gate = p.gate;
     a.qfac = allow_qfac && q_factor_offload(p);
+    a.sc = a.qfac && pl.sc;
     a.pf_s0 = static_cast<const uint8_t*>(static_cast<const void*>(p.S0));
     a.pf_s0_bytes = p.S0 ? (size_t)a.BH * p.dk * p.dv * 4 : 0;
     a.pf_v = static_cast<const uint8_t*>(p.v);

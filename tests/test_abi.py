@@ -243,11 +243,37 @@ def test_bench_segment_rule_matches_library_plan():
         assert st_nseg == (nseg - 1) * sub and st_cps * sub == (cps if nseg > 1 else 0), name
         BH = w.B * w.H
         nch = (w.T + 63) // 64
-        base = (0 if w.gate == 0 else 2 * BH * nch * 64 * w.dk * 2) + BH * nch * 64 * 64 * 2 + BH * nch * w.dk * 4
+        # Q (.) Lambda and K (.) Gamma and the chunk decays with a gate; the score tiles unless
+        # the chunk pass forms every chunk's scores itself (no gate, dk <= 128)
+        sc_all = bench.scores_in_chunk_pass(w) and w.gate == 0
+        base = (0 if w.gate == 0 else 2 * BH * nch * 64 * w.dk * 2 + BH * nch * w.dk * 4) + \
+            (0 if sc_all else BH * nch * 64 * 64 * 2)
         seg = BH * (2 * st_nseg + 1) * w.dk * w.dv * 4 if nseg > 1 else 0
         assert bnd.gla_fwd_workspace_size(p) == got_staged(p), name
         got = bnd.gla_fwd_workspace_size(p)
         assert abs(got - (base + seg)) < 4096, (name, got, base + seg, nseg)
+
+
+def test_plan_scores_in_chunk_pass():
+    """dk <= 128 without a gate: the chunk pass forms the intra-chunk scores itself, so there is
+    no prep stage and, without a split, no workspace; the per-head decay keeps its prep (for
+    K (.) Gamma, and the steep chunks' scores); dk = 256 or a per-key gate keep the score tiles."""
+    kw = dict(B=8, H=16, T=2048, dk=128, dv=128, q=0x1000000, k=0x9000000, v=0x11000000,
+              O=0x31000000, gate=bnd.GLA_GATE_NONE, log_g=None)
+    p = _params(**kw)
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_fwd"] and bnd.gla_fwd_workspace_size(p) == 0
+    p.force_segments = 2   # only the split's states
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_state", "gla_state_scan", "gla_chunk_fwd"]
+    assert bnd.gla_fwd_workspace_size(p) == 128 * (1 + 1 + 1) * 128 * 128 * 4
+    p = _params(**dict(kw, dk=256))
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_prep", "gla_chunk_fwd"]
+    assert bnd.gla_fwd_workspace_size(p) == 128 * 32 * 64 * 64 * 2
+    p = _params(**dict(kw, gate=bnd.GLA_GATE_HEAD_SCALAR, log_g=0x21000000))
+    names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+    assert names == ["gla_chunk_prep", "gla_chunk_fwd"]
 
 
 def got_staged(p):

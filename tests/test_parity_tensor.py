@@ -89,9 +89,9 @@ def test_prep_stage_outputs():
 
 def test_prep_stage_factored_scalar_gate():
     """Stage 0 under a per-head scalar gate: a chunk whose decay (rows x log lambda) stays
-    above -60 leaves the query factor lambda^(r+1) to the chunk pass, so its scores are
-    (q_r . k_s) lambda^-(s+1) and no Q (.) Lambda rows are written; a steeper head keeps
-    the scores (q_r . k_s) lambda^(r-s) and its Q (.) Lambda rows."""
+    above -60 leaves the query factor lambda^(r+1) and its scores to the chunk pass, so only
+    its K (.) Gamma rows are written (no Q (.) Lambda rows, no score tile); a steeper head
+    keeps the scores (q_r . k_s) lambda^(r-s) and its Q (.) Lambda rows."""
     w = gi.Workload("t", B=1, H=2, T=100, dk=64, dv=128, dtype=torch.bfloat16, gate=gi.GATE_HEAD_SCALAR)
     x = gi.make_inputs(w, seed=2)
     x["log_g"] = torch.tensor([-0.04, -2.0], dtype=torch.float32)   # 64 x 2.0 > 60: head 1 is not factored
@@ -106,6 +106,7 @@ def test_prep_stage_factored_scalar_gate():
     BH, Tpad, dk, nch = 2, 128, 64, 2
     off = BH * Tpad * dk * 2
     qt = ws[:off].view(torch.bfloat16).view(BH, Tpad, dk).float().cpu().numpy()
+    kt = ws[off:2 * off].view(torch.bfloat16).view(BH, Tpad, dk).float().cpu().numpy()
     A = ws[2 * off: 2 * off + BH * nch * 64 * 64 * 2].view(torch.bfloat16).view(BH, nch, 64, 64).float().cpu().numpy()
     q = x["q"].double().numpy().reshape(BH, 100, dk)
     k = x["k"].double().numpy().reshape(BH, 100, dk)
@@ -117,9 +118,12 @@ def test_prep_stage_factored_scalar_gate():
             r = np.arange(n_)
             factored = n_ * lam[bh] >= -60.0
             S = q[bh, t0:t1] @ k[bh, t0:t1].T
+            np.testing.assert_allclose(kt[bh, t0:t1], k[bh, t0:t1] * np.exp((n_ - 1 - r) * lam[bh])[:, None],
+                                       rtol=1e-2, atol=1e-3)
             if factored:
-                P = np.tril(S * np.exp(-(r[None, :] + 1) * lam[bh]))
-                assert np.all(qt[bh, t0:t1] == 0)
+                # the chunk pass forms these scores from raw q and K (.) Gamma
+                assert np.all(qt[bh, t0:t1] == 0) and np.all(A[bh, ch] == 0)
+                continue
             else:
                 P = np.tril(S * np.exp((r[:, None] - r[None, :]) * lam[bh] * (r[:, None] >= r[None, :])))
                 np.testing.assert_allclose(qt[bh, t0:t1], q[bh, t0:t1] * np.exp((r + 1) * lam[bh])[:, None],
