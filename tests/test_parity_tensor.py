@@ -261,6 +261,28 @@ def test_in_place_state_carry_with_split():
     assert_close(to_np(S), STref, torch.bfloat16, "ST")
 
 
+@pytest.mark.parametrize("gate", [gi.GATE_NONE, gi.GATE_HEAD_SCALAR])
+def test_state_carried_in_place_across_calls(gate):
+    """A long sequence fed as consecutive calls, each call's S_T written over the next call's
+    S0 in one buffer, with no synchronisation in between: the scores formed in the chunk pass
+    (dk <= 128), where no gate means no prep kernel ahead of the pass, so the pass itself must
+    wait for the previous call's S_T before it reads S0. Equal to one call over the sequence."""
+    w = gi.Workload("t", B=2, H=4, T=3 * 256, dk=128, dv=256, dtype=torch.bfloat16, gate=gate, s0_std=0.2)
+    x = gi.make_inputs(w, seed=21 + gate)
+    c = _dev(x)
+    S = c["S0"].clone()
+    parts = [tuple(c[n][:, :, 256 * i:256 * (i + 1)].contiguous() for n in ("q", "k", "v")) for i in range(3)]
+    Os = [torch.empty(2, 4, 256, 256, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    for (q, k, v), Oi in zip(parts, Os):   # the calls' kernels back to back on the stream
+        gla.forward(q, k, v, c["log_g"], S, O=Oi, ST=S, gate=x["gate"], path=gla.GLA_PATH_TENSOR)
+    torch.cuda.synchronize()
+    O = torch.cat(Os, dim=2)
+    assert gla.gla_device_status() == 0
+    Oref, STref = oracle.gla_forward(x["q"], x["k"], x["v"], x["log_g"], x["gate"], x["S0"])
+    assert_close(to_np(O), Oref, torch.bfloat16, "O")
+    assert_close(to_np(S), STref, torch.bfloat16, "ST")
+
+
 def test_gla_fwd_public_signature():
     """gla_fwd(q,k,v,log_g,S0,O,ST,B,H,T,dk,dv,chunk,stream): per-key gate, stream-ordered workspace."""
     w = gi.Workload("t", B=2, H=2, T=130, dk=128, dv=128, dtype=torch.bfloat16, gate=gi.GATE_PER_KEY, s0_std=0.02)
