@@ -88,7 +88,11 @@ typedef enum {
  *   GLA_PATH_TENSOR  the tensor-core path, as AUTO plans it (a gate-prep kernel
  *                    writing Q (.) Lambda, K (.) Gamma, the chunk decays and the
  *                    masked intra-chunk scores to the workspace, then the
- *                    chunk-serial pass; a sequence split when B*H is small)
+ *                    chunk-serial pass; a sequence split when B*H is small).
+ *                    With dk <= 128 and no gate or a per-head decay the chunk
+ *                    pass forms the intra-chunk scores itself: no gate then
+ *                    runs no prep kernel and, without a split, needs no
+ *                    workspace (gla_fwd_workspace_size returns 0)
  *   GLA_PATH_STAGED  the same, under its explicit name
  *   GLA_PATH_FUSED   per-key gate, bf16, dk = 256, dv in {256, 512}, one pass
  *                    over the sequence: one kernel in which a thread-block
