@@ -35,6 +35,15 @@
 // and the drain scales O[r][j] by exp(B'_r[j] - B'_C[j]), formed from log beta
 // (a prefix sum for the first 32 rows, a suffix sum for the last 32). A head
 // that gla_value_prep flagged out of range is left to the CUDA-core pass.
+//
+// The SC instantiations (dk <= 128, no gate or a per-head decay) form the
+// intra-chunk scores themselves instead of reading the prep's tiles: warp 2's
+// lane 0 issues P = Q K^T into spare tensor-memory columns as soon as a
+// stage's Q and K have landed (rows in lanes 64-127, see the readout), warps 2
+// and 3 mask it, scale it by lambda^-nr for the decay (with K (.) Gamma that is
+// (q_r . k_s) lambda^-(s+1), the scores of the query-factored form), and write
+// it as the bf16 score tile into the stage, and the intra MMA waits for it.
+// Without a gate nothing is prepared at all: the pass reads q, k, v directly.
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
