@@ -276,6 +276,42 @@ def test_plan_scores_in_chunk_pass():
     assert names == ["gla_chunk_prep", "gla_chunk_fwd"]
 
 
+def test_split_rule_over_random_shapes():
+    """The library's sequence-split plan (segments, state-pass pieces) and its score placement
+    against bench.py's mirror of the rule, over seeded random shapes, gates and forced segment
+    counts, through the workspace size: the per-gate tiles, plus one fp32 state per piece and
+    one start state per piece and after the last."""
+    import random
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunkwise_gated_linear_gla_gb300 import inputs as gi
+    rnd = random.Random(5)
+    gates = [(bnd.GLA_GATE_NONE, 0), (bnd.GLA_GATE_HEAD_SCALAR, 1), (bnd.GLA_GATE_PER_KEY, 2),
+             (bnd.GLA_GATE_TOKEN_SCALAR, 3)]
+    for _ in range(300):
+        gate, g = rnd.choice(gates)
+        B, H = rnd.choice([1, 2, 3]), rnd.choice([1, 2, 4, 8])
+        dk, dv = rnd.choice([64, 128, 256]), 128 * rnd.choice([1, 2, 4])
+        T = rnd.randint(1, 64 * 300)
+        force = rnd.choice([0, 0, 1, 2, 3, 5, 9, 17])
+        ng = {0: None, 1: 0x2000000000, 2: 0x2000000000, 3: 0x2000000000}[g]
+        p = _params(B=B, H=H, T=T, dk=dk, dv=dv, gate=gate, log_g=ng, q=0x100000000, k=0x400000000,
+                    v=0x800000000, O=0xC00000000, force_segments=force)
+        w = gi.Workload("t", B=B, H=H, T=T, dk=dk, dv=dv, dtype=gi.WORKLOADS["gla_1p3b"].dtype, gate=g)
+        nseg, cps, sub, st_nseg, st_cps = bench.planned_split(w, force, 148)
+        BH, nch = B * H, (T + 63) // 64
+        sc_all = bench.scores_in_chunk_pass(w) and g == 0
+        base = (0 if g == 0 else 2 * BH * nch * 64 * dk * 2 + BH * nch * dk * 4) + \
+            (0 if sc_all else BH * nch * 64 * 64 * 2)
+        seg = BH * (2 * st_nseg + 1) * dk * dv * 4 if nseg > 1 else 0
+        got = bnd.gla_fwd_workspace_size(p)
+        assert abs(got - (base + seg)) < 4 * 256, (B, H, T, dk, dv, g, force, got, base + seg, nseg, sub)
+        names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+        assert ("gla_chunk_prep" in names) == (not sc_all), names
+        assert ("gla_chunk_state" in names) == (nseg > 1), (names, nseg)
+
+
 def got_staged(p):
     q = bnd.gla_fwd_params.from_buffer_copy(p)
     q.path = bnd.GLA_PATH_STAGED
