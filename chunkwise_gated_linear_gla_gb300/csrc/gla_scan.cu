@@ -8,7 +8,14 @@
 // the state correction of the FlashQLA talk ("core technical principles":
 // a wrongly started segment is fixed by one matrix per rank), which for a
 // diagonal gate collapses from a dk x dk matrix to the vector Gamma_s. With
-// S_in(0) = S0 this also yields S_T = S_in(nseg).
+// S_in(0) = S0 this also yields S_in(nseg), the state after the last one.
+//
+// In the forward pass the "segments" here are the state pass's pieces: they
+// cover the chunks before the chunk pass's last segment, sub pieces per
+// segment, and the chunk pass's segment j starts from S_in(j sub); the state
+// after the last piece is where its last segment starts (that segment's own
+// pass then ends at S_T). The backward runs the same recurrence over its
+// sweeps' segments, forward or from the last one.
 //
 // One CTA covers 256 consecutive state elements of one (b,h) (they share a
 // key row k when dv >= 256, else two rows); one thread per element. The

@@ -12,7 +12,9 @@
 // sfx is a running product, so each chunk's K tile is scaled once in shared
 // memory (every factor <= 1) and the tensor cores only accumulate; no state
 // is rescaled in tensor memory between chunks. The gla_state_scan kernel then
-// chains the segments with the segment decays.
+// chains the segments with the segment decays. (In the forward pass the
+// "segments" are the split's state-pass pieces: the chunks before the chunk
+// pass's last segment, cut finer than its segments so that they fill the GPU.)
 //
 // Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2-9 scale the K
 // tiles and finally read the state out (two groups of four warps, one TMEM
