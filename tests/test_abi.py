@@ -274,6 +274,15 @@ def test_plan_scores_in_chunk_pass():
     p = _params(**dict(kw, gate=bnd.GLA_GATE_HEAD_SCALAR, log_g=0x21000000))
     names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
     assert names == ["gla_chunk_prep", "gla_chunk_fwd"]
+    # dk = 64 without a gate: the chunk pass alone as well; the per-token and per-key gates
+    # (whose scores need the prep's per-row or per-key factors) keep the prep at dk <= 128
+    p = _params(**dict(kw, dk=64))
+    assert [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))] == ["gla_chunk_fwd"]
+    assert bnd.gla_fwd_workspace_size(p) == 0
+    for g in (bnd.GLA_GATE_TOKEN_SCALAR, bnd.GLA_GATE_PER_KEY):
+        p = _params(**dict(kw, gate=g, log_g=0x21000000))
+        names = [bnd.gla_fwd_stage_name(p, i) for i in range(bnd.gla_fwd_num_stages(p))]
+        assert names == ["gla_chunk_prep", "gla_chunk_fwd"], (g, names)
 
 
 def test_split_rule_over_random_shapes():
