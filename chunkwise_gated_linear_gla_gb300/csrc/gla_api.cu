@@ -210,9 +210,10 @@ gla_status make_plan(const gla_fwd_params* p, Plan& pl, int sms)
         // chunks before it. It cuts them into the most pieces that still fit in one wave,
         // each a whole fraction of a segment and at least kMinStateChunks long.
         const int cps = pl.chunks_per_seg, slots = (sms > 0 ? sms : 148) * kStateCtasPerSm;
+        const long long fit = slots / ((long long)(pl.nseg - 1) * units);   // pieces per segment in one wave
         pl.sub = 1;
-        for (int f = cps / kMinStateChunks; f > 1; --f)
-            if (cps % f == 0 && (long long)(pl.nseg - 1) * f * units <= slots) {
+        for (int f = (int)(fit < cps / kMinStateChunks ? fit : cps / kMinStateChunks); f > 1; --f)
+            if (cps % f == 0) {
                 pl.sub = f;
                 break;
             }
