@@ -588,8 +588,12 @@ gla_chunk_prep_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const
 // memory allows); with the per-head decay, eight warps share the Q and K scaling.
 template <int DK>
 constexpr int prep_uniform_bufs() { return 1; }
-template <int DK, int NTU>
-constexpr int prep_uniform_ctas_per_sm() { return DK > 256 ? 1 : DK > 128 ? 3 : (NTU == 128 ? 6 : 4); }
+// (the per-token gate at dk = 256 runs two: three left it 80 registers and a 72-byte spill, and
+// two measured 2% faster on the 1.3B-shaped layer)
+template <int DK, int NTU, int GATE>
+constexpr int prep_uniform_ctas_per_sm() {
+    return DK > 256 ? 1 : DK > 128 ? (GATE == GLA_GATE_TOKEN_SCALAR ? 2 : 3) : (NTU == 128 ? 6 : 4);
+}
 template <int DK>
 constexpr int prep_uniform_smem() { return prep_uniform_bufs<DK>() * 2 * C * DK * 2 + 64 + C * 4 + 1024; }
 
@@ -601,7 +605,7 @@ __device__ __forceinline__ void prefetch_row_l2(const float* p, int n) {
 }
 
 template <int DK, int NTU, int GATE>
-__global__ void __launch_bounds__(NTU, prep_uniform_ctas_per_sm<DK, NTU>())
+__global__ void __launch_bounds__(NTU, prep_uniform_ctas_per_sm<DK, NTU, GATE>())
 gla_chunk_prep_uniform_kernel(PrepArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                               const __grid_constant__ CUtensorMap tmA)
 {
@@ -800,7 +804,7 @@ cudaError_t launch_prep_uniform_nt(const PrepArgs& a, const CUtensorMap& mq, con
 {
     const int smem = prep_uniform_smem<DK>();
     const int total = a.BH * a.nchunks;
-    const int resident = prep_uniform_ctas_per_sm<DK, NTU>() * sms;
+    const int resident = prep_uniform_ctas_per_sm<DK, NTU, GATE>() * sms;
     const dim3 grid(total < resident ? total : resident);
     cudaError_t e = cudaFuncSetAttribute(gla_chunk_prep_uniform_kernel<DK, NTU, GATE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
